@@ -1,0 +1,130 @@
+"""Float64 CPU oracle for the gated delta-rule recurrence and its stable rank.
+
+TEST INFRASTRUCTURE ONLY.  The oracle is the plain definition of what the GPU
+path computes, written for a reader to check by eye.  Only the tests, the
+package smoke check and the benchmark's CPU-baseline leg may import it; the
+product library never does, and the two share no code.
+
+Functions
+---------
+recurrence(q, k, v, alpha, beta, S0=None, mode="gdn", threads=None)
+    Token-by-token recurrence in float64 (C, ``gdn_oracle.c``).  Follows
+    "On State Reduction in Linear Attention" notes, Sec. 2.1, Eqs. (1)-(2)
+    (error-correction form of the delta rule, read o_t = S_t q_t, scalar decay
+    of Gated DeltaNet) and "Linear Attention Architectures" notes, Sec. 2.4,
+    Eqs. 15-17 (decay the old state first, then form the error).
+stable_rank(S)
+    ||S||_F^2, sigma_1 and er(S) = ||S||_F^2 / ||S||_2^2, the stable rank of
+    "On State Reduction in Linear Attention" notes, Sec. 2.2, Eq. (5); sigma_1
+    comes from LAPACK's SVD (numpy), a library routine independent of the GPU
+    power iteration.  For S = 0 the ratio is undefined (the notes define it
+    for nonzero states); this oracle returns (0, 0, 0) there.
+
+Parity pins: every function here is checked by ``tests/test_oracle_pins.py``
+against closed forms, worked examples and invariants fixed by the pages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MODES = {"gdn": 0, "linear": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gdn_oracle.c`` into ``liboracle.so`` with gcc (plain -O2,
+    no architecture-specific flags, so it builds the same on x86 and Arm)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.gdn_oracle_recurrence.argtypes = [dp] * 8 + [ctypes.c_int] * 7
+            lib.gdn_oracle_recurrence.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _as_f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def recurrence(q, k, v, alpha, beta, S0=None, mode="gdn", threads=None, want_o=True):
+    """Run the recurrence over every (batch, head) sequence.
+
+    q, k: [B, T, H, K]; v: [B, T, H, V]; alpha, beta: [B, T, H];
+    S0: [B, H, V, K] or None (zero state).  Inputs are upcast to float64 from
+    whatever exact values the caller passes (bf16- or fp32-rounded).
+    Returns (o [B, T, H, V] or None, S_T [B, H, V, K]) in float64.
+    """
+    k = _as_f64(k)
+    B, T, H, K = k.shape
+    v = _as_f64(v)
+    V = v.shape[-1]
+    q = _as_f64(q) if q is not None else None
+    alpha = _as_f64(alpha)
+    beta = _as_f64(beta)
+    assert v.shape == (B, T, H, V)
+    assert alpha.shape == (B, T, H) and beta.shape == (B, T, H)
+    if q is not None:
+        assert q.shape == (B, T, H, K)
+    S0a = None
+    if S0 is not None:
+        S0a = _as_f64(S0)
+        assert S0a.shape == (B, H, V, K)
+    o = np.empty((B, T, H, V), dtype=np.float64) if (want_o and q is not None) else None
+    ST = np.empty((B, H, V, K), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = _load().gdn_oracle_recurrence(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0a), _ptr(o), _ptr(ST),
+        B, T, H, K, V, MODES[mode], int(threads),
+    )
+    if rc != 0:
+        raise RuntimeError(f"oracle recurrence failed with code {rc}")
+    return o, ST
+
+
+def stable_rank(S):
+    """Return (fro2, sigma1, er) per matrix for S of shape [..., V, K].
+
+    fro2 = sum of squared entries; sigma1 = largest singular value (LAPACK);
+    er = fro2 / sigma1^2, and 0 where S is exactly zero.
+    """
+    S = _as_f64(S)
+    lead = S.shape[:-2]
+    M = S.reshape((-1,) + S.shape[-2:])
+    fro2 = np.einsum("nij,nij->n", M, M)
+    sig = np.linalg.svd(M, compute_uv=False)
+    sigma1 = sig[:, 0] if sig.shape[1] else np.zeros(M.shape[0])
+    er = np.zeros_like(fro2)
+    nz = sigma1 > 0
+    er[nz] = fro2[nz] / sigma1[nz] ** 2
+    return fro2.reshape(lead), sigma1.reshape(lead), er.reshape(lead)
