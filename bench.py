@@ -1,0 +1,503 @@
+"""Benchmark of the gated delta-rule path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: Gated DeltaNet layer prefill, B=8, T=4096, H=16,
+d_k = d_v = 128, bf16 q/k/v, fp32 state, chunk 64, S0 = 0.  A timed step is
+one gdn_prefill call over the whole batch; `value` is tokens/s (B*T per
+step, summed over ranks).  The same JSON line carries the rest of the
+metric, measured in the same run: the channel-pruned d_k' = 64 prefill and
+its speed-up, the decode state GB/s (B = 64 and B = 1, d_k 128 and 64; as
+specified and L2-cold) and the stable-rank epilogue time.
+
+Inputs live in HBM before the timed region; the prefill working set
+(q, k, v, o: 537 MB) is larger than L2, so no flush is needed between steps.
+Multi-GPU (torchrun): every rank runs the same independent batch on its own
+GPU (sequences shard with no exchange step); barrier + max over ranks.
+
+--impl reference times the float64 CPU oracle (the reference arm of this
+repository) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = {"workload": "gated-deltanet-prefill", "B": 8, "T": 4096, "H": 16, "d_k": 128,
+            "d_v": 128, "chunk": 64, "state": "fp32", "qkv": "bf16", "S0": "zero"}
+METRIC = "prefill tokens/s and decode state GB/s (% of HBM/TC roofline) at d_k 128 vs 64"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- accounting
+def prefill_bytes(B, T, H, K, V, qkv_bytes=2, with_S0=False):
+    """Algorithmic HBM bytes of one prefill launch: q, k, v read, o written,
+    alpha/beta read, final state written (and S0 read if given)."""
+    per_token_head = 2 * K * qkv_bytes + V * qkv_bytes + V * qkv_bytes + 8
+    state = 4 * V * K * (2 if with_S0 else 1)
+    return B * T * H * per_token_head + B * H * state
+
+
+def prefill_flops(B, T, H, K, V, C=64):
+    """Chunked-form FLOPs per launch: 2 * (3CK + 2CV + 3KV + C^2/6) per token-head
+    (KK^T, W, QK^T; U~, P U; W S^T, Q S^T, state update; triangular solve)."""
+    macs = 3 * C * K + 2 * C * V + 3 * K * V + C * C / 6.0
+    return 2.0 * macs * B * T * H
+
+
+def decode_state_bytes(B, H, K, V):
+    return 2 * 4 * V * K * B * H
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                clk, mx, util = float(parts[0]), float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            smax = mx
+            if util > 0:
+                sm.append(clk)
+            for n, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                    "samples": len(self.lines)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples_under_load": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+def to_dev_bf16(x, torch):
+    from gated_delta_rule_49_gb300 import inputs
+    bits = inputs.bf16_bits(np.ascontiguousarray(x, np.float32)).view(np.int16)
+    return torch.from_numpy(bits).view(torch.bfloat16).cuda()
+
+
+def problem_to_dev(p, torch):
+    return dict(q=to_dev_bf16(p.q, torch), k=to_dev_bf16(p.k, torch), v=to_dev_bf16(p.v, torch),
+                alpha=torch.from_numpy(np.ascontiguousarray(p.alpha)).cuda(),
+                beta=torch.from_numpy(np.ascontiguousarray(p.beta)).cuda())
+
+
+def time_calls(fn, steps, warmup, torch, barrier=None):
+    """Warm up, then time exactly `steps` calls with CUDA events on the current
+    stream; returns (total_ms, per-call ms list)."""
+    for _ in range(warmup):
+        fn()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i in range(steps):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return evs[0].elapsed_time(evs[-1]), per
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, barrier, max_over_ranks):
+    import torch
+    from gated_delta_rule_49_gb300 import binding, inputs
+
+    binding.load()
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sampler = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+                           if "CUDA_VISIBLE_DEVICES" in os.environ else torch.cuda.current_device())
+    sampler.start()
+    launches = 0
+
+    # ---- headline: prefill, d_k = 128 ----
+    W = WORKLOAD
+    B, T, H, K, V = W["B"], W["T"], W["H"], W["d_k"], W["d_v"]
+    p = inputs.make_prefill(B=B, T=T, H=H, K=K, V=V)
+    d = problem_to_dev(p, torch)
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
+    ST = torch.empty((B, H, V, K), dtype=torch.float32, device="cuda")
+
+    def step():
+        binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T, H,
+                            K, V, binding.GDN_BF16)
+
+    total_ms, per = time_calls(step, args.steps, args.warmup, torch, barrier)
+    launches += args.steps
+    total_ms = max_over_ranks(total_ms)
+    ms_per_step = total_ms / args.steps
+    tokens = B * T * world * args.steps
+    value = tokens / (total_ms / 1e3)
+    kern_ms = statistics.mean(per)
+    byts = prefill_bytes(B, T, H, K, V)
+    flops = prefill_flops(B, T, H, K, V)
+    achieved_gbs = byts / (kern_ms / 1e3) / 1e9
+    achieved_tf = flops / (kern_ms / 1e3) / 1e12
+    status = binding.gdn_get_last_device_status()
+
+    extra = {}
+    if not args.quick:
+        # ---- pruned d_k' = 64, same draws ----
+        del d
+        pp = inputs.make_prefill(B=B, T=T, H=H, K=K, V=V, pruned_K=64)
+        dp = problem_to_dev(pp, torch)
+        STp = torch.empty((B, H, V, 64), dtype=torch.float32, device="cuda")
+
+        def step64():
+            binding.gdn_prefill(dp["q"], dp["k"], dp["v"], dp["alpha"], dp["beta"], None, o, STp,
+                                B, T, H, 64, V, binding.GDN_BF16)
+
+        t64, per64 = time_calls(step64, args.steps, args.warmup, torch, barrier)
+        t64 = max_over_ranks(t64)
+        k64 = statistics.mean(per64)
+        extra["pruned_dk64"] = {
+            "tokens_per_s": B * T * world * args.steps / (t64 / 1e3),
+            "ms_per_step": t64 / args.steps,
+            "speedup_vs_dk128": (total_ms / args.steps) / (t64 / args.steps),
+            "achieved_gbs": prefill_bytes(B, T, H, 64, V) / (k64 / 1e3) / 1e9,
+            "achieved_tflops": prefill_flops(B, T, H, 64, V) / (k64 / 1e3) / 1e12,
+        }
+        extra["pruned_dk64"]["hbm_frac"] = extra["pruned_dk64"]["achieved_gbs"] / peaks["hbm_gbs"]
+        del dp, pp
+
+        # ---- stable-rank epilogue on the final states of the headline run ----
+        f2 = torch.empty(B * H, device="cuda")
+        s1 = torch.empty_like(f2)
+        er = torch.empty_like(f2)
+
+        def rank_call():
+            binding.gdn_state_rank(ST, B * H, V, K, f2, s1, er, 500, 1e-7)
+
+        tr, perr = time_calls(rank_call, 5, 2, torch, barrier)
+        extra["state_rank"] = {"ms_per_call": tr / 5, "states": B * H,
+                               "median_er": float(er.median().item())}
+
+        # ---- decode: B = 64 and 1, d_k 128 and 64 ----
+        extra["decode"] = bench_decode(args, torch, binding, inputs, peaks, props, barrier,
+                                       max_over_ranks)
+
+    clocks = sampler.stop()
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world)
+
+    roof_bound = "hbm" if byts / peaks["hbm_gbs"] >= flops / 1e3 / peaks["bf16_tflops"] else "tensor"
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded generator; per-head decay centres, L2-normalised q/k)",
+        "config": dict(W, l2="inputs larger than L2 (537 MB per step)",
+                       parallelism=f"independent batch per GPU x{world}"),
+        "roofline": {
+            "bound": roof_bound,
+            "achieved": achieved_gbs if roof_bound == "hbm" else achieved_tf,
+            "peak": peaks["hbm_gbs"] if roof_bound == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if roof_bound == "hbm" else "TFLOP/s",
+            "frac": (achieved_gbs / peaks["hbm_gbs"]) if roof_bound == "hbm"
+            else achieved_tf / peaks["bf16_tflops"],
+            "traffic": None,
+            "kernel": "gdn_prefill",
+            "algorithmic_bytes": byts,
+            "algorithmic_flops": flops,
+            "tensor_frac": achieved_tf / peaks["bf16_tflops"],
+            "peak_source": peaks["source"],
+        },
+        "gpu_launches": launches,
+        "device_status": status,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu": props.name,
+        "sm_count": props.multi_processor_count,
+    }
+    line.update(extra)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p, seqs=args.cpu_seqs)
+    return line
+
+
+def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_ranks):
+    """Decode state GB/s.  Steps are replayed from a CUDA graph of `nsteps`
+    launches; 'as specified' updates one state in place (it may sit in L2);
+    'l2_cold' rotates over enough state buffers (>= 4x L2) per step."""
+    res = {}
+    l2 = props.L2_cache_size if hasattr(props, "L2_cache_size") else 126 * 2**20
+    H, V = 16, 128
+    nsteps = 64
+    for B in (64, 1):
+        for K in (128, 64):
+            p = inputs.make_decode(B=B, H=H, K=128, V=V, steps=nsteps,
+                                   pruned_K=None if K == 128 else 64)
+            q = to_dev_bf16(np.ascontiguousarray(p.q.transpose(1, 0, 2, 3)), torch)
+            k = to_dev_bf16(np.ascontiguousarray(p.k.transpose(1, 0, 2, 3)), torch)
+            v = to_dev_bf16(np.ascontiguousarray(p.v.transpose(1, 0, 2, 3)), torch)
+            al = torch.from_numpy(np.ascontiguousarray(p.alpha.transpose(1, 0, 2))).cuda()
+            be = torch.from_numpy(np.ascontiguousarray(p.beta.transpose(1, 0, 2))).cuda()
+            o = torch.empty((nsteps, B, H, V), dtype=torch.bfloat16, device="cuda")
+            sbytes = 4 * B * H * V * K
+            nbuf_cold = max(1, -(-4 * l2 // sbytes))
+            S0 = torch.from_numpy(p.S0).cuda()
+            out = {}
+            for mode, nbuf in (("as_specified", 1), ("l2_cold", nbuf_cold)):
+                states = [S0.clone() for _ in range(nbuf)]
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    for t in range(3):  # warm-up outside capture
+                        binding.gdn_decode_step(q[t], k[t], v[t], al[t], be[t], states[t % nbuf],
+                                                o[t], B, H, K, V, binding.GDN_BF16)
+                torch.cuda.current_stream().wait_stream(s)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g):
+                    for t in range(nsteps):
+                        binding.gdn_decode_step(q[t], k[t], v[t], al[t], be[t], states[t % nbuf],
+                                                o[t], B, H, K, V, binding.GDN_BF16)
+                reps = max(3, args.decode_reps)
+                tot, per = time_calls(g.replay, reps, 3, torch, barrier)
+                tot = max_over_ranks(tot)
+                step_us = tot / reps / nsteps * 1e3
+                gbs = decode_state_bytes(B, H, K, V) / (step_us / 1e6) / 1e9
+                out[mode] = {"us_per_step": step_us, "state_gbs": gbs,
+                             "hbm_frac": gbs / peaks["hbm_gbs"], "state_buffers": nbuf,
+                             "tokens_per_s": B / (step_us / 1e6)}
+                del g, states
+            res[f"B{B}_dk{K}"] = out
+    for B in (64, 1):
+        a, b = res[f"B{B}_dk128"], res[f"B{B}_dk64"]
+        res[f"B{B}_speedup_dk64"] = {m: a[m]["us_per_step"] / b[m]["us_per_step"] for m in a}
+    res["note"] = ("state GB/s = 8 V K B H / step time; steps replayed from a CUDA graph of "
+                   f"{nsteps} launches; hbm_frac uses the measured copy bandwidth")
+    return res
+
+
+def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world):
+    """Same prefill through the C ABI with pinned HOST buffers: H2D of the
+    step's inputs, the call, D2H of o and S_T, all inside the timed region."""
+    B, T, H, K = p.k.shape
+    V = p.v.shape[-1]
+    from gated_delta_rule_49_gb300 import inputs
+    hq = torch.from_numpy(inputs.bf16_bits(p.q).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(inputs.bf16_bits(p.k).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(inputs.bf16_bits(p.v).view(np.int16)).view(torch.bfloat16).pin_memory()
+    ha = torch.from_numpy(np.ascontiguousarray(p.alpha)).pin_memory()
+    hb = torch.from_numpy(np.ascontiguousarray(p.beta)).pin_memory()
+    ho = torch.empty((B, T, H, V), dtype=torch.bfloat16).pin_memory()
+    hS = torch.empty((B, H, V, K), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(x, device="cuda") for x in (hq, hk, hv))
+    da, db = torch.empty_like(ha, device="cuda"), torch.empty_like(hb, device="cuda")
+    do = torch.empty_like(ho, device="cuda")
+    dS = torch.empty_like(hS, device="cuda")
+
+    def step():
+        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (da, ha), (db, hb)):
+            dst.copy_(src, non_blocking=True)
+        binding.gdn_prefill(dq, dk, dv, da, db, None, do, dS, B, T, H, K, V, binding.GDN_BF16)
+        ho.copy_(do, non_blocking=True)
+        hS.copy_(dS, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    tot, _ = time_calls(step, steps, 2, torch, barrier)
+    tot = max_over_ranks(tot)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ha, hb))
+    d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
+    return {"value": B * T * world * steps / (tot / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_sample(p, seqs):
+    """Pick `seqs` (b, h) sequences of the workload (full length)."""
+    B, T, H, K = p.k.shape
+    pick = [(i % B, (i * 5) % H) for i in range(seqs)]
+    from gated_delta_rule_49_gb300 import inputs
+    subs = [inputs.take_sequences(p, [b], [h]) for b, h in pick]
+    cat = lambda xs: np.concatenate(xs, axis=0)  # noqa: E731
+    return inputs.Problem(p.name, p.dtype, cat([s.q for s in subs]), cat([s.k for s in subs]),
+                          cat([s.v for s in subs]), cat([s.alpha for s in subs]),
+                          cat([s.beta for s in subs]), None, {})
+
+
+def cpu_baseline(p, seqs=None, reps=1):
+    import oracle
+    cores = os.cpu_count() or 1
+    seqs = seqs or 2 * cores
+    sub = oracle_sample(p, seqs)
+    B, T, H, K = p.k.shape
+    threads = min(cores, seqs)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.recurrence(sub.q, sub.k, sub.v, sub.alpha, sub.beta, threads=threads)
+    dt = (time.perf_counter() - t0) / reps
+    token_heads = seqs * T
+    return {"value": token_heads / H / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{seqs} of {B * H} (b, h) sequences x {T} tokens, float64 C oracle; "
+                      f"tokens/s = sequences*T/H / wall time ({dt:.2f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    headline workload (whole sequences) on the host cores."""
+    if rank != 0:
+        return None
+    from gated_delta_rule_49_gb300 import inputs
+    import oracle
+    oracle.build()
+    W = WORKLOAD
+    p = inputs.make_prefill(B=W["B"], T=W["T"], H=W["H"], K=W["d_k"], V=W["d_v"])
+    cores = os.cpu_count() or 1
+    seqs = min(cores, 16)
+    sub = oracle_sample(p, seqs)
+    T, H = W["T"], W["H"]
+    for _ in range(args.warmup):
+        oracle.recurrence(sub.q[:, :256], sub.k[:, :256], sub.v[:, :256], sub.alpha[:, :256],
+                          sub.beta[:, :256], threads=seqs)
+    t0 = time.perf_counter()
+    Tc = args.ref_tokens
+    for _ in range(args.steps):
+        oracle.recurrence(sub.q[:, :Tc], sub.k[:, :Tc], sub.v[:, :Tc], sub.alpha[:, :Tc],
+                          sub.beta[:, :Tc], threads=seqs)
+    dt = time.perf_counter() - t0
+    value = seqs * Tc * args.steps / H / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": dict(WORKLOAD),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": seqs, "kind": "oracle",
+                         "sample": f"{seqs} (b, h) sequences x first {Tc} tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline prefill only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seqs", type=int, default=None)
+    ap.add_argument("--decode-reps", type=int, default=20)
+    ap.add_argument("--ref-tokens", type=int, default=4096)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line))
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    barrier = None
+    max_over_ranks = lambda x: x  # noqa: E731
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = dist.barrier
+
+        def max_over_ranks(x):
+            t = torch.tensor([x], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+
+    line = run_ours(args, rank, world, barrier, max_over_ranks)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+"""Thin ctypes binding over libgdn.so (``include/gdn.h``).
+
+Argument marshalling only: every step of the recurrence runs in the
+library's CUDA kernels.  Functions with the C names take torch CUDA tensors
+(or raw integer device pointers) for every buffer, pass ``data_ptr()`` and the
+current torch stream, and raise ``GDNError`` on a negative status.  There is
+no CPU fallback: if the library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgdn.so")
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = -1
+GDN_ERR_UNSUPPORTED = -2
+GDN_ERR_ALIGNMENT = -3
+GDN_ERR_CUDA = -4
+GDN_ERR_TIMEOUT = -5
+GDN_ERR_WORKSPACE = -6
+GDN_ERR_DEVICE_BOUNDS = -7
+GDN_WARN_ZERO_STATE = 1
+
+GDN_BF16 = 0
+GDN_FP32 = 1
+
+EXPORTS = (
+    "gdn_prefill",
+    "gdn_prefill_workspace_size",
+    "gdn_decode_step",
+    "gdn_state_rank",
+    "gdn_get_last_device_status",
+    "gdn_status_string",
+    "gdn_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgdn.so (built by ``gated_delta_rule_49_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libgdn.so is not built ({path} missing): run "
+                "`python -m gated_delta_rule_49_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.gdn_prefill.argtypes = [vp] * 8 + [i] * 6 + [vp, sz, vp]
+        lib.gdn_prefill.restype = i
+        lib.gdn_prefill_workspace_size.argtypes = [i] * 6
+        lib.gdn_prefill_workspace_size.restype = sz
+        lib.gdn_decode_step.argtypes = [vp] * 7 + [i] * 5 + [vp]
+        lib.gdn_decode_step.restype = i
+        lib.gdn_state_rank.argtypes = [vp, i, i, i, vp, vp, vp, i, f, vp]
+        lib.gdn_state_rank.restype = i
+        lib.gdn_get_last_device_status.argtypes = [vp]
+        lib.gdn_get_last_device_status.restype = i
+        lib.gdn_status_string.argtypes = [i]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_version.argtypes = []
+        lib.gdn_version.restype = i
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().gdn_status_string(int(status)).decode()
+    except RuntimeError:
+        return "libgdn.so not loaded"
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_FP32
+    raise GDNError(GDN_ERR_INVALID_ARG, f"dtype {t.dtype}")
+
+
+def _check(status: int, where: str) -> int:
+    if status < 0:
+        raise GDNError(status, where)
+    return status
+
+
+def gdn_prefill(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, workspace=None,
+                workspace_bytes=0, stream=None) -> int:
+    st = load().gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                            _ptr(o), _ptr(S_T), B, T, H, K, V, dtype, _ptr(workspace),
+                            workspace_bytes, _stream(stream))
+    return _check(st, "gdn_prefill")
+
+
+def gdn_prefill_workspace_size(B, T, H, K, V, dtype) -> int:
+    return int(load().gdn_prefill_workspace_size(B, T, H, K, V, dtype))
+
+
+def gdn_decode_step(q, k, v, alpha, beta, S, o, B, H, K, V, dtype, stream=None) -> int:
+    st = load().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S),
+                                _ptr(o), B, H, K, V, dtype, _stream(stream))
+    return _check(st, "gdn_decode_step")
+
+
+def gdn_state_rank(S, BH, V, K, fro2, sigma1, stable_rank, max_iter=500, tol=1e-7,
+                   stream=None) -> int:
+    st = load().gdn_state_rank(_ptr(S), BH, V, K, _ptr(fro2), _ptr(sigma1), _ptr(stable_rank),
+                               max_iter, tol, _stream(stream))
+    return _check(st, "gdn_state_rank")
+
+
+def gdn_get_last_device_status(stream=None) -> int:
+    return int(load().gdn_get_last_device_status(_stream(stream)))
+
+
+def gdn_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def gdn_version() -> int:
+    return int(load().gdn_version())
+
+
+# ---- tensor-level conveniences (allocate outputs with torch, then call) ----
+
+def prefill(q, k, v, alpha, beta, S0=None, want_o=True, want_state=True, out_state=None,
+            stream=None):
+    """q, k [B,T,H,K]; v [B,T,H,V] (bf16 or fp32 CUDA tensors); alpha, beta
+    [B,T,H] fp32; S0 [B,H,V,K] fp32 or None.  Returns (o, S_T)."""
+    import torch
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    dt = _dtype_code(k)
+    o = torch.empty((B, T, H, V), dtype=k.dtype, device=k.device) if want_o else None
+    ST = None
+    if want_state:
+        ST = out_state if out_state is not None else torch.empty(
+            (B, H, V, K), dtype=torch.float32, device=k.device)
+    ws_bytes = gdn_prefill_workspace_size(B, T, H, K, V, dt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=k.device) if ws_bytes else None
+    gdn_prefill(q, k, v, alpha, beta, S0, o, ST, B, T, H, K, V, dt, ws, ws_bytes, stream)
+    return o, ST
+
+
+def decode_step(q, k, v, alpha, beta, S, o=None, stream=None):
+    """One token: q, k [B,H,K]; v [B,H,V]; alpha, beta [B,H]; S [B,H,V,K]
+    updated in place.  Returns o [B,H,V]."""
+    import torch
+    B, H, K = k.shape
+    V = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, H, V), dtype=k.dtype, device=k.device)
+    gdn_decode_step(q, k, v, alpha, beta, S, o, B, H, K, V, _dtype_code(k), stream)
+    return o
+
+
+def state_rank(S, max_iter=500, tol=1e-7, stream=None):
+    """S [..., V, K] fp32.  Returns (fro2, sigma1, stable_rank) shaped [...]."""
+    import torch
+    lead = S.shape[:-2]
+    V, K = S.shape[-2:]
+    BH = 1
+    for d in lead:
+        BH *= d
+    outs = [torch.empty(lead, dtype=torch.float32, device=S.device) for _ in range(3)]
+    gdn_state_rank(S, BH, V, K, *outs, max_iter=max_iter, tol=tol, stream=stream)
+    return tuple(outs)

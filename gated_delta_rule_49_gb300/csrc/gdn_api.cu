@@ -1,0 +1,164 @@
+// C ABI of libgdn.so: host-side validation and dispatch (declared in gdn.h).
+#include <cstring>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// Per-device status word.  Kernels OR kStatus* bits into it; the host reads
+// and clears it in gdn_get_last_device_status.
+static __device__ int g_device_status;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+}  // namespace
+
+int *device_status_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace gdn
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_kv(int K, int V) {
+    return (K == 32 && V == 32) || (K == 64 && V == 128) || (K == 128 && V == 128);
+}
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    if (e == cudaErrorInvalidValue) return GDN_ERR_INVALID_ARG;
+    return GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported (K, V) variant or device";
+        case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case GDN_ERR_CUDA: return "CUDA runtime or launch error";
+        case GDN_ERR_TIMEOUT: return "device wait timed out";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_DEVICE_BOUNDS: return "device-side index check failed";
+        case GDN_WARN_ZERO_STATE: return "warning: all-zero state (stable rank undefined, 0 returned)";
+        default: return "unknown status";
+    }
+}
+
+size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype) {
+    (void)B; (void)T; (void)H; (void)K; (void)V; (void)dtype;
+    return 0;
+}
+
+int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
+                const float *beta, const float *S0, void *o, float *S_T, int B, int T, int H,
+                int K, int V, gdn_dtype dtype, void *workspace, size_t workspace_bytes,
+                void *stream) {
+    if (B < 0 || T < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if (!o && !S_T) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, alpha, beta, S0, o, S_T};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    const size_t need = gdn_prefill_workspace_size(B, T, H, K, V, dtype);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
+    if ((long long)B * H == 0) return GDN_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (!S_T) return GDN_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * V * K;
+        cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
+                                        : cudaMemcpyAsync(S_T, S0, bytes, cudaMemcpyDeviceToDevice, st))
+                           : cudaMemsetAsync(S_T, 0, bytes, st);
+        return from_cuda(e);
+    }
+    return from_cuda(gdn::launch_prefill_simt(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
+                                              dtype, st));
+}
+
+int gdn_decode_step(const void *q, const void *k, const void *v, const float *alpha,
+                    const float *beta, float *S, void *o, int B, int H, int K, int V,
+                    gdn_dtype dtype, void *stream) {
+    if (B < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0) return GDN_OK;
+    if (!q || !k || !v || !alpha || !beta || !S || !o) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, alpha, beta, S, o};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
+    return from_cuda(gdn::launch_decode(q, k, v, alpha, beta, S, o, B, H, K, V, dtype,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
+                   float *stable_rank, int max_iter, float tol, void *stream) {
+    if (BH < 0 || V < 1 || K < 1 || V > 128 || K > 128) return GDN_ERR_INVALID_ARG;
+    if (max_iter < 1 || !(tol >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (BH == 0) return GDN_OK;
+    if (!S || !fro2 || !sigma1 || !stable_rank) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {S, fro2, sigma1, stable_rank};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
+    return from_cuda(gdn::launch_state_rank(S, BH, V, K, fro2, sigma1, stable_rank, max_iter,
+                                            tol, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_get_last_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, gdn::g_device_status, sizeof(int)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const int zero = 0;
+    if (word != 0 && cudaMemcpyToSymbol(gdn::g_device_status, &zero, sizeof(int)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (word & gdn::kStatusTimeout) return GDN_ERR_TIMEOUT;
+    if (word & gdn::kStatusBounds) return GDN_ERR_DEVICE_BOUNDS;
+    if (word & gdn::kStatusZeroState) return GDN_WARN_ZERO_STATE;
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Internal declarations shared by the translation units of libgdn.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Bits of the per-device status word (see gdn_get_last_device_status).
+enum : int { kStatusTimeout = 1, kStatusBounds = 2, kStatusZeroState = 4 };
+
+// Chunk length of the chunkwise prefill.
+constexpr int kChunk = 64;
+
+// Address of the current device's status word (nullptr if the symbol lookup
+// failed).  Kernels OR their bits into it.
+int *device_status_ptr();
+
+// Streaming multiprocessor count of the current device (cached).
+int sm_count();
+
+// --- launchers (return the launch error, never synchronise) ---------------
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *alpha,
+                          const float *beta, float *S, void *o, int B, int H, int K, int V,
+                          gdn_dtype dt, cudaStream_t stream);
+
+cudaError_t launch_state_rank(const float *S, int BH, int V, int K, float *fro2,
+                              float *sigma1, float *er, int max_iter, float tol,
+                              cudaStream_t stream);
+
+cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v,
+                                const float *alpha, const float *beta, const float *S0,
+                                void *o, float *ST, int B, int T, int H, int K, int V,
+                                gdn_dtype dt, cudaStream_t stream);
+
+// Loads of the run dtype as float.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+}  // namespace gdn

@@ -1,0 +1,144 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: the gated delta-rule recurrence on one GPU.
+ *
+ * The recurrence (per batch element b and head h, state S in R^{V x K}):
+ *
+ *     S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t
+ *
+ * equivalently: decay the old state first, form the error of its prediction
+ * u_t = beta_t (v_t - alpha_t S_{t-1} k_t), write u_t k_t^T, then read with
+ * the query.  Sources: "On State Reduction in Linear Attention" reading notes,
+ * Sec. 2.1, Eqs. (1)-(2) (DeltaNet update in error-correction form, the read
+ * o_t = S_t q_t, Gated DeltaNet's scalar decay) and "Linear Attention
+ * Architectures" reading notes, Sec. 2.4, Eqs. 15-17 (decay before the error).
+ * A channel-pruned state keeps d_k' of the key/query channels ("On State
+ * Reduction" notes, Sec. 2.6): callers pass the gathered, re-normalised
+ * q/k with K = d_k'.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller, dense and
+ *    row-major, each 16-byte aligned (else GDN_ERR_ALIGNMENT).  The library
+ *    never allocates device memory in these calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise, except
+ *    gdn_get_last_device_status.
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing.  A failed launch returns GDN_ERR_CUDA.  No entry point
+ *    calls exit(), traps or asserts on the device.
+ *  - Supported (K, V) pairs: (32, 32), (64, 128), (128, 128); others return
+ *    GDN_ERR_UNSUPPORTED.  K is d_k (or a pruned d_k'), V is d_v.
+ *  - State tensors, alpha and beta are always float32; q, k, v and o are
+ *    bf16 (GDN_BF16) or float32 (GDN_FP32).  Arithmetic is float32 with the
+ *    state carried in float32; in GDN_BF16 mode the chunked prefill's tensor
+ *    core products take bf16 operands with float32 accumulation.
+ *  - alpha is expected in (0, 1] and beta in [0, 2); values are not checked.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad dtype, ... */
+    GDN_ERR_UNSUPPORTED = -2,   /* (K, V) not a compiled variant, or no sm_103 device */
+    GDN_ERR_ALIGNMENT = -3,     /* a pointer is not 16-byte aligned */
+    GDN_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+    GDN_ERR_TIMEOUT = -5,       /* device status: a bounded wait in a kernel gave up */
+    GDN_ERR_WORKSPACE = -6,     /* workspace missing or smaller than required */
+    GDN_ERR_DEVICE_BOUNDS = -7, /* device status: a kernel's own index check failed */
+    GDN_WARN_ZERO_STATE = 1     /* device status: gdn_state_rank saw an all-zero state */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
+
+/*
+ * gdn_prefill -- run the recurrence over T tokens of every (b, h) sequence.
+ *
+ *   q, k   [B, T, H, K] (dtype)      v  [B, T, H, V] (dtype)
+ *   alpha, beta [B, T, H] float32    S0 [B, H, V, K] float32, or NULL = zero
+ *   o      [B, T, H, V] (dtype), or NULL to skip the outputs
+ *   S_T    [B, H, V, K] float32, or NULL to skip the final state; S_T may be
+ *          the same pointer as S0 (in-place continuation)
+ *
+ * Chunkwise-parallel form with 64-token chunks: within a chunk the
+ * pseudo-values u_t solve a unit lower-triangular system (the UT/WY
+ * transform), the chunk-local products run as matrix products, and the
+ * state is carried from chunk to chunk in float32.  Any T >= 0 is accepted
+ * (a ragged last chunk is masked; T = 0 copies S0, or zero, into S_T).
+ * B = 0 or H = 0 is a no-op.
+ *
+ * workspace: device scratch of at least gdn_prefill_workspace_size() bytes
+ * (may be NULL when that size is 0); 256-byte aligned.
+ */
+GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
+                const float *beta, const float *S0, void *o, float *S_T, int B, int T, int H,
+                int K, int V, gdn_dtype dtype, void *workspace, size_t workspace_bytes,
+                void *stream);
+
+/* Bytes of device workspace gdn_prefill needs for this problem (0 if none). */
+GDN_API size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype);
+
+/*
+ * gdn_decode_step -- one token of the recurrence for every (b, h), with the
+ * state updated in place:
+ *
+ *   q, k [B, H, K] (dtype)   v [B, H, V] (dtype)   alpha, beta [B, H] float32
+ *   S    [B, H, V, K] float32, read once and written once
+ *   o    [B, H, V] (dtype)
+ *
+ * Each value channel (row of S) is an independent system ("On State
+ * Reduction" notes, Sec. 2.5), so a row is decayed, dotted with k and q,
+ * corrected and written back in one pass.
+ */
+GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const float *alpha,
+                    const float *beta, float *S, void *o, int B, int H, int K, int V,
+                    gdn_dtype dtype, void *stream);
+
+/*
+ * gdn_state_rank -- stable rank of BH states ("On State Reduction" notes,
+ * Sec. 2.2, Eq. (5)): er(S) = ||S||_F^2 / ||S||_2^2.
+ *
+ *   S [BH, V, K] float32 (1 <= V, K <= 128)
+ *   fro2, sigma1, stable_rank [BH] float32 outputs: ||S||_F^2, sigma_1, er
+ *
+ * sigma_1^2 is the largest eigenvalue of S^T S by power iteration from the
+ * fixed start x_j = 1 + j/K, stopping when the Rayleigh quotient changes by
+ * at most tol (relative) or after max_iter iterations (max_iter >= 1,
+ * tol >= 0).  An all-zero state yields 0 in all three outputs and sets the
+ * GDN_WARN_ZERO_STATE device status.
+ */
+GDN_API int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
+                   float *stable_rank, int max_iter, float tol, void *stream);
+
+/*
+ * gdn_get_last_device_status -- synchronise `stream`, then read and clear the
+ * current device's status word.  Returns GDN_OK, GDN_ERR_TIMEOUT,
+ * GDN_ERR_DEVICE_BOUNDS, GDN_WARN_ZERO_STATE (only when no error is set) or
+ * GDN_ERR_CUDA if the synchronisation itself failed.
+ */
+GDN_API int gdn_get_last_device_status(void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+GDN_API const char *gdn_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+GDN_API int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

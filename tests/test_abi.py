@@ -1,0 +1,115 @@
+"""The C ABI library loads, exports what include/gdn.h declares, and rejects
+bad arguments on the host before any launch (no GPU needed: every call here
+fails validation, so nothing touches a device)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from gated_delta_rule_49_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing but the C ABI is exported
+    assert {s for s in exported if not s.startswith("gdn_")} <= {"_init", "_fini"}
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1):
+        s = binding.status_string(code)
+        assert s and s != "unknown status"
+    assert binding.status_string(12345) == "unknown status"
+    assert binding.gdn_version() >= 100
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation
+
+
+def _prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, beta=FAKE, S0=None, o=FAKE, ST=FAKE, B=1, T=4,
+             H=1, K=128, V=128, dt=0, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.gdn_prefill(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["S0"], a["o"],
+                           a["ST"], a["B"], a["T"], a["H"], a["K"], a["V"], a["dt"], a["ws"],
+                           a["wsb"], a["stream"])
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert _prefill(lib, K=96) == binding.GDN_ERR_UNSUPPORTED
+    assert _prefill(lib, K=128, V=64) == binding.GDN_ERR_UNSUPPORTED
+    assert _prefill(lib, K=32, V=128) == binding.GDN_ERR_UNSUPPORTED
+    assert _prefill(lib, B=-1) == binding.GDN_ERR_INVALID_ARG
+    assert _prefill(lib, T=-3) == binding.GDN_ERR_INVALID_ARG
+    assert _prefill(lib, dt=7) == binding.GDN_ERR_INVALID_ARG
+    assert _prefill(lib, q=None) == binding.GDN_ERR_INVALID_ARG
+    assert _prefill(lib, alpha=None) == binding.GDN_ERR_INVALID_ARG
+    assert _prefill(lib, o=None, ST=None) == binding.GDN_ERR_INVALID_ARG
+    assert _prefill(lib, k=FAKE + 8) == binding.GDN_ERR_ALIGNMENT
+    assert _prefill(lib, S0=FAKE + 4) == binding.GDN_ERR_ALIGNMENT
+    assert _prefill(lib, ST=FAKE + 2) == binding.GDN_ERR_ALIGNMENT
+    # empty batch or head count: nothing to do, nothing launched
+    assert _prefill(lib, B=0) == binding.GDN_OK
+    assert _prefill(lib, H=0) == binding.GDN_OK
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, beta=FAKE, S=FAKE, o=FAKE, B=1, H=1, K=128,
+                 V=128, dt=0)
+        a.update(kw)
+        return lib.gdn_decode_step(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["S"],
+                                   a["o"], a["B"], a["H"], a["K"], a["V"], a["dt"], None)
+    assert call(K=16) == binding.GDN_ERR_UNSUPPORTED
+    assert call(S=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(o=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(H=-1) == binding.GDN_ERR_INVALID_ARG
+    assert call(dt=2) == binding.GDN_ERR_INVALID_ARG
+    assert call(v=FAKE + 2) == binding.GDN_ERR_ALIGNMENT
+    assert call(B=0) == binding.GDN_OK
+
+
+def test_state_rank_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(S=FAKE, BH=1, V=128, K=128, f=FAKE, s=FAKE, e=FAKE, it=10, tol=1e-6)
+        a.update(kw)
+        return lib.gdn_state_rank(a["S"], a["BH"], a["V"], a["K"], a["f"], a["s"], a["e"],
+                                  a["it"], ctypes.c_float(a["tol"]), None)
+    assert call(V=129) == binding.GDN_ERR_INVALID_ARG
+    assert call(K=0) == binding.GDN_ERR_INVALID_ARG
+    assert call(it=0) == binding.GDN_ERR_INVALID_ARG
+    assert call(tol=-1.0) == binding.GDN_ERR_INVALID_ARG
+    assert call(tol=float("nan")) == binding.GDN_ERR_INVALID_ARG
+    assert call(e=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(S=FAKE + 4) == binding.GDN_ERR_ALIGNMENT
+    assert call(BH=0) == binding.GDN_OK
+
+
+def test_workspace_query(lib):
+    for K, V in ((32, 32), (64, 128), (128, 128)):
+        assert binding.gdn_prefill_workspace_size(8, 4096, 16, K, V, 0) >= 0
