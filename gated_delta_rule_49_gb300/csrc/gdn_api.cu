@@ -114,6 +114,11 @@ int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
                            : cudaMemsetAsync(S_T, 0, bytes, st);
         return from_cuda(e);
     }
+    // bf16 at V = 128 runs on the tensor cores; float32 mode and the small
+    // (32, 32) variant run the CUDA-core chunked kernel.
+    if (dtype == GDN_BF16 && V == 128 && (K == 128 || K == 64))
+        return from_cuda(gdn::launch_prefill_tc(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
+                                                st));
     return from_cuda(gdn::launch_prefill_simt(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
                                               dtype, st));
 }

@@ -38,6 +38,11 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v,
                                 void *o, float *ST, int B, int T, int H, int K, int V,
                                 gdn_dtype dt, cudaStream_t stream);
 
+// Tensor-core (tcgen05) chunked prefill: bf16 q/k/v, V = 128, K in {64, 128}.
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,
+                              const float *beta, const float *S0, void *o, float *ST, int B,
+                              int T, int H, int K, int V, cudaStream_t stream);
+
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
