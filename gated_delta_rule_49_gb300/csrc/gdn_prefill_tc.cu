@@ -1,32 +1,40 @@
 // Chunkwise prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
 // bf16 q/k/v, float32 state carried on chip from chunk to chunk.
 //
-// One CTA (8 warps) owns one (b, h) sequence and walks its 64-token chunks.
-// With G_t the in-chunk cumulative log-decay, gamma_t = exp(G_t),
+// One CTA owns one (b, h) sequence and walks its 64-token chunks.  With G_t
+// the in-chunk cumulative log-decay, gamma_t = exp(G_t) and
 // Gamma_ts = exp(G_t - G_s) (a difference, never a ratio of gammas):
 //
 //   A_ts = beta_t Gamma_ts (k_t . k_s) (s < t)     P_ts = Gamma_ts (q_t . k_s) (s <= t)
 //   T    = (I + A)^{-1},  T' = T diag(beta gamma),  T'' = T diag(beta)
 //   W^T  = K^T T'^T,      U~^T = V^T T''^T
 //   U^T  = U~^T - S W^T          pseudo-values u_t = beta_t (v_t - alpha_t S_{t-1} k_t)
-//   O^T  = diag-scaled S Q^T (by gamma_t) + U^T P^T
+//   O^T  = S (diag(gamma) Q)^T + U^T P^T
 //   S   <- gamma_C S + U^T diag(exp(G_C - G_s)) K
 //
 // -- the token recurrence unrolled over a chunk (the pseudo-value rewriting
 // of the delta rule, "On State Reduction in Linear Attention" notes, Sec. 2.3).
-// Everything is written transposed so that every product has M = 128 rows
-// (value channels or stacked tiles), the natural TMEM layout (row = lane).
+// Every product is written transposed so that its M dimension is 128 (value
+// rows, or two stacked 64-row tiles): the accumulator row is the TMEM lane.
 //
-// Data movement: TMA loads 64-token x 64-channel bf16 boxes of q, k, v with
-// the 128-byte swizzle into a two-stage ring; the same K tile serves as a
-// K-major operand (contraction over channels) and as an MN-major operand
-// (contraction over tokens).  Intermediate operands (P, T', T'', -W^T, U^T,
-// U^T diag(decay), the bf16 copy of S) are written by threads in the same
-// swizzled layout.  The float32 state lives in registers: thread (lane c,
-// half h) holds row c, columns [h K/2, (h+1) K/2).
+// Warp roles (12 warps):
+//   key group   (warps 0-3): gates, A/P from [K;Q] K^T, the triangular
+//               inverse T (blocked, CUDA cores), the W^T / U~^T products and the
+//               -W^T operand; it also folds gamma into the Q tile in place.
+//               Thread 0 issues the TMA loads of V and these MMAs.  This group
+//               runs up to one chunk ahead of the state group.
+//   state group (warps 4-11): U epilogue, state update, output.  Thread 128
+//               issues the state-dependent MMAs and the q/k TMA loads.
+// The float32 state lives in state-group registers: thread (lane c, half h)
+// holds row c, columns [h K/2, (h+1) K/2); a bf16 copy in shared memory is the
+// MMA operand.  Groups hand off through mbarriers; every wait is bounded.
 //
-// A ragged last chunk: TMA fills tokens past T with zeros; beta = 0 and
-// log alpha = 0 there, which leaves every valid row unchanged.
+// Data movement: TMA loads 64-token x 64-channel bf16 boxes of q, k (two-stage
+// ring) and v (single buffer) with the 128-byte swizzle; the same K tile is a
+// K-major operand (contraction over channels) and an MN-major operand
+// (contraction over tokens).  A ragged last chunk: TMA fills tokens past T
+// with zeros; beta = 0 and log alpha = 0 there, which leaves valid rows
+// unchanged.
 #include "gdn_internal.cuh"
 #include "gdn_sm100.cuh"
 
@@ -37,27 +45,34 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 256;
+constexpr int kKeyThreads = 128;
+constexpr int kStateThreads = 256;
+constexpr int kTcThreads = kKeyThreads + kStateThreads;
+constexpr int kBarKey = 1, kBarState = 2;  // named barrier ids
 constexpr long long kSpinLimit = 2000000000LL;  // ~1 s of SM clocks per wait
 
 template <int K>
 struct TcLayout {
-    // one TMA stage: 64 x 64 bf16 boxes, 8 KB each
+    // q/k stage (two stages): 64 x 64 bf16 boxes, 8 KB each; K and Q of one
+    // 64-channel block are adjacent so [K;Q] is one 128-row operand
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
-    static constexpr uint32_t VC0 = K == 128 ? 32768 : 16384, VC1 = VC0 + 8192;
-    static constexpr uint32_t STAGE = VC1 + 8192;
-    static constexpr uint32_t TP = 2 * STAGE, TPP = TP + 8192, PT = TPP + 8192;
-    static constexpr uint32_t NW = PT + 8192;                // K rows x 128 B (MN-major)
-    static constexpr uint32_t SB = NW + K * 128;             // K/64 blocks of 128 rows
+    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
+    static constexpr uint32_t VB = 2 * STAGE;           // V: two 64-channel boxes
+    static constexpr uint32_t TP = VB + 16384, TPP = TP + 8192;
+    static constexpr uint32_t PT = TPP + 8192;          // two buffers of 8 KB
+    static constexpr uint32_t NW = PT + 16384;          // K rows x 128 B (MN-major)
+    static constexpr uint32_t SB = NW + K * 128;        // K/64 blocks of 128 rows
     static constexpr uint32_t UT = SB + (K / 64) * 16384;
     static constexpr uint32_t UD = UT + 16384;
-    static constexpr uint32_t AF = UD + 16384;               // float [64][65]
-    static constexpr uint32_t GATE = AF + 64 * 65 * 4;       // G, gamma, beta, decay
-    static constexpr uint32_t END = GATE + 4 * 64 * 4;
-    static constexpr uint32_t TX_BYTES = (K == 128 ? 6u : 4u) * 8192u;
-    static constexpr size_t SMEM = END + 1024;               // + alignment slack
+    static constexpr uint32_t AF = UD + 16384;          // float [64][68]
+    static constexpr uint32_t KGATE = AF + 64 * 68 * 4; // key group: G2, gamma, beta
+    static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;  // state group: 3 x (decay[64], gamma_C)
+    static constexpr uint32_t END = SGATE + 3 * 68 * 4;
+    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
+    static constexpr uint32_t V_BYTES = 2u * 8192u;
+    static constexpr size_t SMEM = END + 1024;          // + alignment slack
     // TMEM columns
-    static constexpr uint32_t D1 = 0, WT = 64, UA = 128, OA = 192, OB = 256, DS = 320;
+    static constexpr uint32_t D1 = 0, WT = 64, UA = 128, O = 256, DS = 384;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -65,7 +80,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-// Store 32 floats of one tile row as 4 swizzled 16-byte chunks starting at chunk c0.
+// Store 32 floats (times `scale`) of one tile row as 4 swizzled 16-byte chunks
+// starting at chunk c0.
 __device__ __forceinline__ void store_row32(uint8_t *tile, uint32_t row, uint32_t c0,
                                             const float (&v)[32], float scale = 1.f) {
 #pragma unroll
@@ -79,6 +95,95 @@ __device__ __forceinline__ void store_row32(uint8_t *tile, uint32_t row, uint32_
     }
 }
 
+// Inclusive prefix sum of log2(alpha) over a 64-token chunk held two per lane
+// (tokens lane and lane + 32).  Past `nvalid` alpha counts as 1.
+__device__ __forceinline__ void chunk_log2_prefix(float a0, float a1, int lane, int nvalid,
+                                                  float &g0, float &g1) {
+    g0 = lane < nvalid ? log2f(a0) : 0.f;
+    g1 = lane + 32 < nvalid ? log2f(a1) : 0.f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
+        const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
+        if (lane >= off) { g0 += u0; g1 += u1; }
+    }
+    g1 += __shfl_sync(0xffffffffu, g0, 31);
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A held in AF (row stride 68),
+// in place, by the 128 key-group threads: the two 32 x 32 diagonal blocks by
+// forward substitution (one column per thread), then
+// T21 = -T22 (A21 T11).  Upper-triangle entries of AF must be zero on entry.
+__device__ __forceinline__ void unit_lower_inverse(float *AF, int tid) {
+    constexpr int LD = 68;
+    {
+        float x[32];
+        const int blk = tid >> 5, s = tid & 31;
+        if (tid < 64) {
+            const float *Ab = AF + (32 * blk) * LD + 32 * blk;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = (t == s) ? 1.f : 0.f;
+#pragma unroll
+            for (int t = 1; t < 32; ++t) {
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                for (int r = 0; r < t; r += 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(Ab + t * LD + r);
+                    a0 = fmaf(a.x, x[r], a0);
+                    if (r + 1 < t) a1 = fmaf(a.y, x[r + 1], a1);
+                    if (r + 2 < t) a2 = fmaf(a.z, x[r + 2], a2);
+                    if (r + 3 < t) a3 = fmaf(a.w, x[r + 3], a3);
+                }
+                x[t] -= (a0 + a1) + (a2 + a3);
+            }
+        }
+        named_sync(kBarKey, kKeyThreads);  // every read of A11 / A22 done
+        if (tid < 64) {
+            float *Tb = AF + (32 * blk) * LD + 32 * blk;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) Tb[t * LD + s] = x[t];
+        }
+        named_sync(kBarKey, kKeyThreads);
+    }
+    const int i = tid >> 2, j0 = (tid & 3) * 8;
+    float y[8];
+    // X = A21 T11  (T11 lower: terms m < j vanish)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[c] = 0.f;
+#pragma unroll 4
+    for (int m = 0; m < 32; ++m) {
+        const float a = AF[(32 + i) * LD + m];
+        const float4 t0 = *reinterpret_cast<const float4 *>(AF + m * LD + j0);
+        const float4 t1 = *reinterpret_cast<const float4 *>(AF + m * LD + j0 + 4);
+        y[0] = fmaf(a, t0.x, y[0]); y[1] = fmaf(a, t0.y, y[1]);
+        y[2] = fmaf(a, t0.z, y[2]); y[3] = fmaf(a, t0.w, y[3]);
+        y[4] = fmaf(a, t1.x, y[4]); y[5] = fmaf(a, t1.y, y[5]);
+        y[6] = fmaf(a, t1.z, y[6]); y[7] = fmaf(a, t1.w, y[7]);
+    }
+    named_sync(kBarKey, kKeyThreads);  // every read of A21 done
+    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0) = make_float4(y[0], y[1], y[2], y[3]);
+    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
+    named_sync(kBarKey, kKeyThreads);
+    // T21 = -T22 X  (T22 lower with unit diagonal)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[c] = 0.f;
+#pragma unroll 4
+    for (int m = 0; m < 32; ++m) {
+        const float a = AF[(32 + i) * LD + 32 + m];
+        const float4 t0 = *reinterpret_cast<const float4 *>(AF + (32 + m) * LD + j0);
+        const float4 t1 = *reinterpret_cast<const float4 *>(AF + (32 + m) * LD + j0 + 4);
+        y[0] = fmaf(a, t0.x, y[0]); y[1] = fmaf(a, t0.y, y[1]);
+        y[2] = fmaf(a, t0.z, y[2]); y[3] = fmaf(a, t0.w, y[3]);
+        y[4] = fmaf(a, t1.x, y[4]); y[5] = fmaf(a, t1.y, y[5]);
+        y[6] = fmaf(a, t1.z, y[6]); y[7] = fmaf(a, t1.w, y[7]);
+    }
+    named_sync(kBarKey, kKeyThreads);  // every read of X done
+    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0 + 4) =
+        make_float4(-y[4], -y[5], -y[6], -y[7]);
+    named_sync(kBarKey, kKeyThreads);
+}
+
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -89,25 +194,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       int *status) {
     using L = TcLayout<K>;
     constexpr int V = 128;
-    constexpr int KH = K / 2;  // state columns per thread
+    constexpr int KH = K / 2;  // state columns per state-group thread
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[2];
-    __shared__ uint64_t bar_mma;
+    __shared__ uint64_t kq_full[2], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready, nw_free;
+    __shared__ uint64_t ua_free[2], pt_free[2];
     __shared__ uint32_t tmem_base_sh;
-
-    float *AF = reinterpret_cast<float *>(sm + L::AF);
-    float *Gs = reinterpret_cast<float *>(sm + L::GATE);
-    float *gam = Gs + 64;
-    float *bet = Gs + 128;
-    float *dcy = Gs + 192;
+    __shared__ int abort_flag;
+    volatile int *abort_v = &abort_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
-    const int row = quad * 32 + lane;  // TMEM lane owned by this thread
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int b = blockIdx.x / H, h = blockIdx.x % H;
     const size_t seq = (size_t)blockIdx.x;
     const int nchunks = (T + 63) / 64;
@@ -121,297 +219,408 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_init(&bar_full[0], 1);
-        mbar_init(&bar_full[1], 1);
-        mbar_init(&bar_mma, 1);
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &v_full, &bar_p1, &bar_w, &bar_u, &bar_s,
+                            &nw_ready, &nw_free, &ua_free[0], &ua_free[1], &pt_free[0],
+                            &pt_free[1]};
+        for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
+        abort_flag = 0;
     }
-
-    // initial state: fp32 in registers, bf16 copy in the SB tile
-    float S[KH];
-    {
-        const int c = row;
-        const int j0 = half * KH;
-#pragma unroll
-        for (int j = 0; j < KH; j += 4) {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (S0) x = *reinterpret_cast<const float4 *>(S0 + (seq * V + c) * K + j0 + j);
-            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-        }
-#pragma unroll
-        for (int p = 0; p < KH / 32; ++p) {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
-            const int j = j0 + 32 * p;
-            store_row32(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
-        }
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base_sh;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-    auto issue_loads = [&](int n) {
+    auto load_kq = [&](int n) {
         const int st = n & 1;
         uint8_t *stg = sm + st * L::STAGE;
-        const int t0 = n * 64;
-        mbar_arrive_expect_tx(&bar_full[st], L::TX_BYTES);
-        tma_load_4d(stg + L::KC0, &tm_k, &bar_full[st], 0, h, t0, b);
-        tma_load_4d(stg + L::QC0, &tm_q, &bar_full[st], 0, h, t0, b);
+        mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
+        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, n * 64, b);
+        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, n * 64, b);
         if (K == 128) {
-            tma_load_4d(stg + L::KC1, &tm_k, &bar_full[st], 64, h, t0, b);
-            tma_load_4d(stg + L::QC1, &tm_q, &bar_full[st], 64, h, t0, b);
+            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, n * 64, b);
+            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, n * 64, b);
         }
-        tma_load_4d(stg + L::VC0, &tm_v, &bar_full[st], 0, h, t0, b);
-        tma_load_4d(stg + L::VC1, &tm_v, &bar_full[st], 64, h, t0, b);
     };
-    if (tid == 0) {
-        issue_loads(0);
-        if (nchunks > 1) issue_loads(1);
-    }
-
-    constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);   // K-major x K-major
-    constexpr uint32_t I_AMN = idesc_bf16(128, 64, true, false);   // MN-major A
-    constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);   // MN-major B, N = 64
-    constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);     // MN-major B, N = K
-
-    uint32_t mma_phase = 0;
-    bool failed = false;
-
-    auto wait_mma = [&]() -> bool {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma, mma_phase & 1, kSpinLimit));
-        ++mma_phase;
-        tc_fence_after();
+    auto load_v = [&](int n) {
+        mbar_arrive_expect_tx(&v_full, L::V_BYTES);
+        tma_load_4d(sm + L::VB, &tm_v, &v_full, 0, h, n * 64, b);
+        tma_load_4d(sm + L::VB + 8192, &tm_v, &v_full, 64, h, n * 64, b);
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
+        if (!ok) *abort_v = 1;
         return ok;
     };
 
-    for (int n = 0; n < nchunks; ++n) {
-        const int st = n & 1;
-        const uint32_t stg = base + st * L::STAGE;
-        const int c0 = n * 64;
-        const int nvalid = min(64, T - c0);
+    constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);  // K-major x K-major
+    constexpr uint32_t I_AMN = idesc_bf16(128, 64, true, false);  // MN-major A
+    constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);  // MN-major B, N = 64
+    constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);    // MN-major B, N = K
 
-        // ---- (1) chunk operands landed: KK^T, QK^T and S Q^T ----
-        bool ok = true;
+    bool failed = false;
+
+    if (tid < kKeyThreads) {
+        // ================================================================ key group
+        float *AF = reinterpret_cast<float *>(sm + L::AF);
+        float *G2 = reinterpret_cast<float *>(sm + L::KGATE);
+        float *gam = G2 + 64;
+        float *bet = G2 + 128;
+        const int r = tid;  // TMEM lane
+        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs
+        auto prefetch_gates = [&](int n) {
+            if (warp == 0 && n < nchunks) {
+                const int nv = min(64, T - n * 64);
+                const size_t i0 = ((size_t)b * T + n * 64 + lane) * H + h;
+                const size_t i1 = i0 + (size_t)32 * H;
+                pa0 = lane < nv ? alpha[i0] : 1.f;
+                pb0 = lane < nv ? beta[i0] : 0.f;
+                pa1 = lane + 32 < nv ? alpha[i1] : 1.f;
+                pb1 = lane + 32 < nv ? beta[i1] : 0.f;
+            }
+        };
+        prefetch_gates(0);
         if (tid == 0) {
-            ok = mbar_wait(&bar_full[st], (n >> 1) & 1, kSpinLimit);
-            tc_fence_after();
+            load_kq(0);
+            if (nchunks > 1) load_kq(1);
+            load_v(0);
+        }
+        for (int n = 0; n < nchunks; ++n) {
+            const int st = n & 1;
+            const uint32_t stg = base + st * L::STAGE;
+            const int nvalid = min(64, T - n * 64);
+            bool ok = true;
+            // ---- [K;Q] K^T ----
+            if (tid == 0) {
+                ok = wait(&kq_full[st], (n >> 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < K / 16; ++ks) {
+                        const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                        const uint32_t kblk = stg + (kb ? L::KC1 : L::KC0) + ko;
+                        mma_bf16(tb + L::D1, sdesc(kblk, 16, 1024), sdesc(kblk, 16, 1024), I_MM,
+                                 ks > 0);
+                    }
+                    mma_commit(&bar_p1);
+                }
+            }
+            // ---- gates of chunk n (warp 0), then prefetch chunk n + 1 ----
+            if (warp == 0) {
+                float g0, g1;
+                chunk_log2_prefix(pa0, pa1, lane, nvalid, g0, g1);
+                G2[lane] = g0;
+                G2[lane + 32] = g1;
+                gam[lane] = exp2f(g0);
+                gam[lane + 32] = exp2f(g1);
+                bet[lane] = pb0;
+                bet[lane + 32] = pb1;
+                prefetch_gates(n + 1);
+            }
+            if (n >= 2 && r >= 64) ok = ok && wait(&pt_free[st], ((n - 2) >> 1) & 1);
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+
+            // ---- A (fp32, solve input) and P (bf16 operand) ----
+            ok = __all_sync(0xffffffffu, wait(&bar_p1, n & 1));
             if (ok) {
+                tc_fence_after();
+                float v0[32], v1[32];
+                tmem_ld32(tb + lane_off + L::D1, v0);
+                tmem_ld32(tb + lane_off + L::D1 + 32, v1);
+                tmem_ld_wait();
+                const int t = r & 63;
+                const float gt = G2[t];
+                if (r < 64) {
+                    const float bt = bet[t];
 #pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks) {
-                    const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                    const uint32_t kblk = stg + (kb ? L::KC1 : L::KC0) + ko;
-                    const uint32_t qblk = stg + (kb ? L::QC1 : L::QC0) + ko;
-                    mma_bf16(tb + L::D1, sdesc(kblk, 16, 1024), sdesc(kblk, 16, 1024), I_MM,
-                             ks > 0);
-                    mma_bf16(tb + L::OA, sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                             sdesc(qblk, 16, 1024), I_MM, ks > 0);
+                    for (int s = 0; s < 64; s += 4) {
+                        float a[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int ss = s + e;
+                            const float kk = ss < 32 ? v0[ss & 31] : v1[ss & 31];
+                            a[e] = ss < t ? bt * exp2f(gt - G2[ss]) * kk : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(AF + t * 68 + s) = make_float4(a[0], a[1], a[2], a[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v0[i] = i <= t ? exp2f(gt - G2[i]) * v0[i] : 0.f;
+                        v1[i] = i + 32 <= t ? exp2f(gt - G2[i + 32]) * v1[i] : 0.f;
+                    }
+                    uint8_t *pt = sm + L::PT + st * 8192;
+                    store_row32(pt, t, 0, v0);
+                    store_row32(pt, t, 4, v1);
                 }
-                mma_commit(&bar_mma);
             }
-        }
-        // gates of this chunk (warp 0): prefix sum of log alpha over 64 tokens
-        if (warp == 0) {
-            const int t0 = lane, t1 = lane + 32;
-            const size_t i0 = ((size_t)b * T + c0 + t0) * H + h;
-            const size_t i1 = ((size_t)b * T + c0 + t1) * H + h;
-            float g0 = t0 < nvalid ? logf(alpha[i0]) : 0.f;
-            float g1 = t1 < nvalid ? logf(alpha[i1]) : 0.f;
-            bet[t0] = t0 < nvalid ? beta[i0] : 0.f;
-            bet[t1] = t1 < nvalid ? beta[i1] : 0.f;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+
+            // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
+            unit_lower_inverse(AF, tid);
+            {
+                const int t = tid >> 1, hf = tid & 1;
+                float tp[32], tpp[32];
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float a0 = __shfl_up_sync(0xffffffffu, g0, off);
-                const float a1 = __shfl_up_sync(0xffffffffu, g1, off);
-                if (lane >= off) { g0 += a0; g1 += a1; }
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(AF + t * 68 + 32 * hf + c);
+                    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = 32 * hf + c + e;
+                        tpp[c + e] = xs[e] * bet[s];
+                        tp[c + e] = tpp[c + e] * gam[s];
+                    }
+                }
+                store_row32(sm + L::TP, t, 4 * hf, tp);
+                store_row32(sm + L::TPP, t, 4 * hf, tpp);
             }
-            g1 += __shfl_sync(0xffffffffu, g0, 31);
+            fence_proxy_async_smem();
+            named_sync(kBarKey, kKeyThreads);
+
+            // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
+            if (tid == 0) {
+                ok = true;
+                if (n >= 2) ok = wait(&ua_free[st], ((n - 2) >> 1) & 1);
+                ok = ok && wait(&v_full, n & 1);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t lbo_k = K == 128 ? 16384u : (L::VB - st * L::STAGE);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, lbo_k, 1024),
+                                 sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
+                        mma_bf16(tb + L::UA + 64 * st, sdesc(base + L::VB + ks * 2048, 8192, 1024),
+                                 sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
+                    }
+                    mma_commit(&bar_w);
+                }
+            }
+            __syncwarp();
+            ok = __all_sync(0xffffffffu, wait(&bar_w, n & 1));
+            if (ok && tid == 0 && n + 1 < nchunks) load_v(n + 1);  // V consumed
+            if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                if (r < K) {
+                    float v0[32], v1[32];
+                    tmem_ld32(tb + lane_off + L::WT, v0);
+                    tmem_ld32(tb + lane_off + L::WT + 32, v1);
+                    tmem_ld_wait();
+                    store_row32(sm + L::NW, r, 0, v0, -1.f);
+                    store_row32(sm + L::NW, r, 4, v1, -1.f);
+                }
+                // Q <- diag(gamma) Q in place (the q tile is read again only by S Q^T)
+                uint8_t *stq = sm + st * L::STAGE;
+#pragma unroll
+                for (int e = tid; e < (K / 64) * 512; e += kKeyThreads) {
+                    const int blk = e >> 9, ee = e & 511;
+                    uint4 *p = reinterpret_cast<uint4 *>(stq + (blk ? L::QC1 : L::QC0) + ee * 16);
+                    const float g = gam[ee >> 3];
+                    uint4 w = *p;
+                    uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 f = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162 *>(&wv[c]));
+                        wv[c] = pack_bf16(f.x * g, f.y * g);
+                    }
+                    *p = w;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+            if (tid == 0) mbar_arrive(&nw_ready);
+        }
+    } else {
+        // ================================================================ state group
+        const int sid = tid - kKeyThreads;  // 0..255
+        const int sw = sid >> 5;            // state warp 0..7
+        const int c = (warp & 3) * 32 + lane;  // state row = TMEM lane
+        const int hf = sw >> 2;             // column half
+        float *sg = reinterpret_cast<float *>(sm + L::SGATE);  // 3 slots of 68 floats
+        // gates of chunk m for the state group (warp 4 only): decay[64], gamma_C
+        auto state_gates = [&](int m) {
+            if (m >= nchunks) return;
+            const int nv = min(64, T - m * 64);
+            const size_t i0 = ((size_t)b * T + m * 64 + lane) * H + h;
+            const float a0 = lane < nv ? alpha[i0] : 1.f;
+            const float a1 = lane + 32 < nv ? alpha[i0 + (size_t)32 * H] : 1.f;
+            float g0, g1;
+            chunk_log2_prefix(a0, a1, lane, nv, g0, g1);
             const float gC = __shfl_sync(0xffffffffu, g1, 31);
-            Gs[t0] = g0; Gs[t1] = g1;
-            gam[t0] = expf(g0); gam[t1] = expf(g1);
-            dcy[t0] = expf(gC - g0); dcy[t1] = expf(gC - g1);
+            float *slot = sg + (m % 3) * 68;
+            slot[lane] = exp2f(gC - g0);
+            slot[lane + 32] = exp2f(gC - g1);
+            if (lane == 0) slot[64] = exp2f(gC);
+        };
+        if (sw == 0) {
+            state_gates(0);
+            state_gates(1);
+            state_gates(2);
         }
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-
-        // ---- (2) A (fp32, for the solve) and P (bf16 operand) ----
-        ok = wait_mma();
-        if (ok) {
-            float v[32];
-            tmem_ld32(tb + lane_off + L::D1 + half * 32, v);
-            tmem_ld_wait();
-            const int t = row & 63;
-            const float Gt = Gs[t];
-            if (quad < 2) {
-                const float bt = bet[t];
+        // initial state: fp32 registers + bf16 operand copy
+        float S[KH];
+        {
+            const int j0 = hf * KH;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int s = half * 32 + i;
-                    AF[t * 65 + s] = s < t ? bt * expf(Gt - Gs[s]) * v[i] : 0.f;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int s = half * 32 + i;
-                    v[i] = s <= t ? expf(Gt - Gs[s]) * v[i] : 0.f;
-                }
-                store_row32(sm + L::PT, t, half * 4, v);
+            for (int j = 0; j < KH; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (S0) x = *reinterpret_cast<const float4 *>(S0 + (seq * V + c) * K + j0 + j);
+                S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
             }
-        }
-        fence_proxy_async_smem();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-
-        // ---- (3) T = (I + A)^{-1}, one column per thread; T' and T'' tiles ----
-        if (tid < 64) {
-            const int s = tid;
-            float x[64];
-#pragma unroll
-            for (int t = 0; t < 64; ++t) x[t] = (t == s) ? 1.f : 0.f;
-#pragma unroll
-            for (int t = 1; t < 64; ++t) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-                for (int r = 0; r < t; ++r) {
-                    const float a = AF[t * 65 + r];
-                    if ((r & 3) == 0) a0 = fmaf(a, x[r], a0);
-                    else if ((r & 3) == 1) a1 = fmaf(a, x[r], a1);
-                    else if ((r & 3) == 2) a2 = fmaf(a, x[r], a2);
-                    else a3 = fmaf(a, x[r], a3);
-                }
-                x[t] -= (a0 + a1) + (a2 + a3);
-            }
-            const float bs = bet[s], bgs = bet[s] * gam[s];
-            const uint32_t off = (s & 7) * 2;
-#pragma unroll
-            for (int t = 0; t < 64; ++t) {
-                const uint32_t at = swz128(t, s >> 3) + off;
-                *reinterpret_cast<__nv_bfloat16 *>(sm + L::TP + at) = __float2bfloat16_rn(x[t] * bgs);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + L::TPP + at) = __float2bfloat16_rn(x[t] * bs);
-            }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- (4) W^T = K^T T'^T and U~^T = V^T T''^T ----
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, 16384, 1024),
-                         sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
-                mma_bf16(tb + L::UA, sdesc(stg + L::VC0 + ks * 2048, 8192, 1024),
-                         sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        ok = wait_mma();
-        if (ok && row < K) {
-            float v[32];
-            tmem_ld32(tb + lane_off + L::WT + half * 32, v);
-            tmem_ld_wait();
-            store_row32(sm + L::NW, row, half * 4, v, -1.f);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-
-        // ---- (5) U^T = U~^T - S W^T ----
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                mma_bf16(tb + L::UA, sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN, 1);
-            }
-            mma_commit(&bar_mma);
-        }
-        ok = wait_mma();
-        if (ok) {
-            float v[32];
-            tmem_ld32(tb + lane_off + L::UA + half * 32, v);
-            tmem_ld_wait();
-            store_row32(sm + L::UT, row, half * 4, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= dcy[half * 32 + i];
-            store_row32(sm + L::UD, row, half * 4, v);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-
-        // ---- (6) O_b^T = U^T P^T and dS = U^T diag(decay) K ----
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tb + L::OB, sdesc(base + L::UT + ks * 32, 16, 1024),
-                         sdesc(base + L::PT + ks * 32, 16, 1024), I_MM, ks > 0);
-                mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
-                         sdesc(stg + L::KC0 + ks * 2048, 16384, 1024), I_DS, ks > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        ok = wait_mma();
-        if (ok) {
-            // state: S <- gamma_C S + dS, then its bf16 copy for the next chunk
-            const float gC = gam[63];
-            const int j0 = half * KH;
 #pragma unroll
             for (int p = 0; p < KH / 32; ++p) {
                 float v[32];
-                tmem_ld32(tb + lane_off + L::DS + j0 + 32 * p, v);
-                tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    S[32 * p + i] = fmaf(gC, S[32 * p + i], v[i]);
-                    v[i] = S[32 * p + i];
-                }
+                for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
                 const int j = j0 + 32 * p;
-                store_row32(sm + L::SB + (j / 64) * 16384, row, (j % 64) / 8, v);
-            }
-            // output: o[t][c] = gamma_t (S Q^T)[c][t] + (U^T P^T)[c][t]
-            float oa[32], ob[32];
-            tmem_ld32(tb + lane_off + L::OA + half * 32, oa);
-            tmem_ld32(tb + lane_off + L::OB + half * 32, ob);
-            tmem_ld_wait();
-            __nv_bfloat16 *orow = o + (((size_t)b * T + c0) * H + h) * V + row;
-            const size_t tstride = (size_t)H * V;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = half * 32 + i;
-                if (o != nullptr && t < nvalid)
-                    orow[t * tstride] = __float2bfloat16_rn(fmaf(gam[t], oa[i], ob[i]));
+                store_row32(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        // this stage's tiles are consumed: prefetch chunk n + 2 into it
-        if (tid == 0 && n + 2 < nchunks) issue_loads(n + 2);
+        named_sync(kBarState, kStateThreads);
+
+        // U^T += S (-W^T) and O^T = S (gamma Q)^T for chunk m
+        auto issue_su = [&](int m) -> bool {
+            if (!wait(&nw_ready, m & 1)) return false;
+            tc_fence_after();
+            const int st = m & 1;
+            const uint32_t stg = base + st * L::STAGE;
+#pragma unroll
+            for (int ks = 0; ks < K / 16; ++ks) {
+                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                const uint64_t sdA = sdesc(base + L::SB + kb * 16384 + ko, 16, 1024);
+                mma_bf16(tb + L::UA + 64 * st, sdA, sdesc(base + L::NW + ks * 2048, 8192, 1024),
+                         I_BMN, 1);
+                mma_bf16(tb + L::O + 64 * st, sdA,
+                         sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM, ks > 0);
+            }
+            mma_commit(&bar_u);
+            mma_commit(&nw_free);
+            return true;
+        };
+        if (sw == 0) {
+            bool ok0 = true;
+            if (lane == 0) ok0 = issue_su(0);
+            ok0 = __shfl_sync(0xffffffffu, ok0, 0);
+            failed = !ok0;
+        }
+        if (named_sync_or(kBarState, kStateThreads, failed)) failed = true;
+
+        for (int n = 0; n < nchunks && !failed; ++n) {
+            const int st = n & 1;
+            const uint32_t stg = base + st * L::STAGE;
+            const int nvalid = min(64, T - n * 64);
+            const float *slot = sg + (n % 3) * 68;
+            // ---- U epilogue: U^T -> UT, U^T diag(decay) -> UD ----
+            bool ok = __all_sync(0xffffffffu, wait(&bar_u, n & 1));
+            if (ok) {
+                tc_fence_after();
+                float v[32];
+                tmem_ld32(tb + lane_off + L::UA + 64 * st + 32 * hf, v);
+                tmem_ld_wait();
+                store_row32(sm + L::UT, c, 4 * hf, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= slot[32 * hf + i];
+                store_row32(sm + L::UD, c, 4 * hf, v);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            if (sid == 0) {
+                mbar_arrive(&ua_free[st]);
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    mma_bf16(tb + L::O + 64 * st, sdesc(base + L::UT + ks * 32, 16, 1024),
+                             sdesc(base + L::PT + st * 8192 + ks * 32, 16, 1024), I_MM, 1);
+                    mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
+                             sdesc(stg + L::KC0 + ks * 2048, 16384, 1024), I_DS, ks > 0);
+                }
+                mma_commit(&bar_s);
+                mma_commit(&pt_free[st]);
+            }
+            // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
+            ok = __all_sync(0xffffffffu, wait(&bar_s, n & 1));
+            if (ok) {
+                tc_fence_after();
+                if (sid == 0 && n + 2 < nchunks) load_kq(n + 2);  // stage consumed
+                const float gC = slot[64];
+                const int j0 = hf * KH;
+#pragma unroll
+                for (int p = 0; p < KH / 32; ++p) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::DS + j0 + 32 * p, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        S[32 * p + i] = fmaf(gC, S[32 * p + i], v[i]);
+                        v[i] = S[32 * p + i];
+                    }
+                    const int j = j0 + 32 * p;
+                    store_row32(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            // ---- next chunk's S-dependent products (warp 4), then this chunk's output ----
+            if (sw == 0) {
+                bool ok1 = true;
+                if (lane == 0 && n + 1 < nchunks) ok1 = issue_su(n + 1);
+                ok1 = __shfl_sync(0xffffffffu, ok1, 0);
+                if (!ok1) failed = true;
+                state_gates(n + 3);  // slot (n + 3) % 3 == n % 3: this chunk's gates are done
+            }
+            {
+                float v[32];
+                tmem_ld32(tb + lane_off + L::O + 64 * st + 32 * hf, v);
+                tmem_ld_wait();
+                if (o != nullptr) {
+                    __nv_bfloat16 *orow = o + (((size_t)b * T + n * 64) * H + h) * V + c;
+                    const size_t tstride = (size_t)H * V;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * hf + i;
+                        if (t < nvalid) orow[t * tstride] = __float2bfloat16_rn(v[i]);
+                    }
+                }
+                tc_fence_before();
+            }
+            if (named_sync_or(kBarState, kStateThreads, failed)) { failed = true; break; }
+        }
+        if (!failed && ST != nullptr) {
+            const int j0 = hf * KH;
+#pragma unroll
+            for (int j = 0; j < KH; j += 4)
+                *reinterpret_cast<float4 *>(ST + (seq * V + c) * K + j0 + j) =
+                    make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
     }
 
-    if (failed) {
-        if (tid == 0 && status) atomicOr(status, kStatusTimeout);
-        // let in-flight loads land before the CTA's shared memory is released
-        if (tid == 0) {
-            for (int s = 0; s < 2; ++s) {
-                // a stage with an outstanding load has had more arrivals issued than waited;
-                // bounded waits on both parities cover it
-                mbar_wait(&bar_full[s], 0, kSpinLimit / 8);
-                mbar_wait(&bar_full[s], 1, kSpinLimit / 8);
-            }
-        }
-    } else if (ST != nullptr) {
-        const int j0 = half * KH;
-#pragma unroll
-        for (int j = 0; j < KH; j += 4)
-            *reinterpret_cast<float4 *>(ST + (seq * V + row) * K + j0 + j) =
-                make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-    }
+    if (failed) *abort_v = 1;
     tc_fence_before();
     __syncthreads();
+    if (*abort_v) {
+        if (tid == 0) {
+            if (status) atomicOr(status, kStatusTimeout);
+            // let in-flight loads land before the CTA's shared memory is released
+            for (int s = 0; s < 2; ++s) {
+                mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
+            }
+            mbar_wait(&v_full, 0, kSpinLimit / 16);
+            mbar_wait(&v_full, 1, kSpinLimit / 16);
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tb, 512);
