@@ -9,27 +9,32 @@
 //   T    = (I + A)^{-1},  T' = T diag(beta gamma),  T'' = T diag(beta)
 //   W^T  = K^T T'^T,      U~^T = V^T T''^T
 //   U^T  = U~^T - S W^T          pseudo-values u_t = beta_t (v_t - alpha_t S_{t-1} k_t)
-//   O^T  = S (diag(gamma) Q)^T + U^T P^T
+//   O    = (diag(gamma) Q) S^T + P U
 //   S   <- gamma_C S + U^T diag(exp(G_C - G_s)) K
 //
 // -- the token recurrence unrolled over a chunk (the pseudo-value rewriting
 // of the delta rule, "On State Reduction in Linear Attention" notes, Sec. 2.3).
-// Every product is written transposed so that its M dimension is 128 (value
-// rows, or two stacked 64-row tiles): the accumulator row is the TMEM lane.
+// Every product has M = 128 so that the accumulator row is the TMEM lane: the
+// key-side and state products are written transposed (rows = value or key
+// channels), and O is computed token-major from two stacked 64-row operands
+// ([K; gamma Q] and [any 64 rows; P]) whose upper half is discarded, so each
+// output row is one token's contiguous 256 bytes.
 //
-// Warp roles (12 warps):
-//   key group   (warps 0-3): gates, A/P from [K;Q] K^T, the triangular
-//               inverse T (blocked, CUDA cores), the W^T / U~^T products and the
-//               -W^T operand; it also folds gamma into the Q tile in place.
-//               Thread 0 issues the TMA loads of V and these MMAs.  This group
-//               runs up to one chunk ahead of the state group.
-//   state group (warps 4-11): U epilogue, state update, output.  Thread 128
-//               issues the state-dependent MMAs and the q/k TMA loads.
+// Warp roles (16 warps, two warpgroups each):
+//   key group   (warps 0-7): gates, A/P from [K;Q] K^T, the triangular
+//               inverse T (16 x 16 blocks on CUDA cores), the W^T / U~^T
+//               products and the -W^T operand; it also folds gamma into the Q
+//               tile in place.  Thread 0 issues the V loads and these MMAs.
+//               The key group depends on no state, so it runs up to one chunk
+//               ahead of the state group.
+//   state group (warps 8-15): U epilogue, state update, output.  Thread 256
+//               issues the state-dependent MMAs and the q/k loads.
 // The float32 state lives in state-group registers: thread (lane c, half h)
 // holds row c, columns [h K/2, (h+1) K/2); a bf16 copy in shared memory is the
-// MMA operand.  Groups hand off through mbarriers; every wait is bounded.
+// MMA operand.  Register budgets are moved between the groups with
+// setmaxnreg.  Groups hand off through mbarriers; every wait is bounded.
 //
-// Data movement: TMA loads 64-token x 64-channel bf16 boxes of q, k (two-stage
+// Data movement: TMA loads 64-token x 64-channel bf16 boxes of q, k (three-stage
 // ring) and v (single buffer) with the 128-byte swizzle; the same K tile is a
 // K-major operand (contraction over channels) and an MN-major operand
 // (contraction over tokens).  A ragged last chunk: TMA fills tokens past T
@@ -45,32 +50,42 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kKeyThreads = 128;
+constexpr int kKeyThreads = 256;
 constexpr int kStateThreads = 256;
 constexpr int kTcThreads = kKeyThreads + kStateThreads;
-constexpr int kBarKey = 1, kBarState = 2;  // named barrier ids
+constexpr int kBarKey = 1, kBarState = 2;       // named barrier ids
 constexpr long long kSpinLimit = 2000000000LL;  // ~1 s of SM clocks per wait
+constexpr int kLD = 68;                         // row stride of the fp32 64 x 64 matrix
 
 template <int K>
 struct TcLayout {
-    // q/k stage (two stages): 64 x 64 bf16 boxes, 8 KB each; K and Q of one
+    // q/k stages (three): 64 x 64 bf16 boxes, 8 KB each; K and Q of one
     // 64-channel block are adjacent so [K;Q] is one 128-row operand
+    static constexpr int NSTAGE = 3;
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
-    static constexpr uint32_t VB = 2 * STAGE;           // V: two 64-channel boxes
+    static constexpr uint32_t VB = NSTAGE * STAGE;      // V: two 64-channel boxes
     static constexpr uint32_t TP = VB + 16384, TPP = TP + 8192;
+    static constexpr uint32_t NW = TP;                  // -W^T (K rows) reuses T', T''
     static constexpr uint32_t PT = TPP + 8192;          // two buffers of 8 KB
-    static constexpr uint32_t NW = PT + 16384;          // K rows x 128 B (MN-major)
-    static constexpr uint32_t SB = NW + K * 128;        // K/64 blocks of 128 rows
-    static constexpr uint32_t UT = SB + (K / 64) * 16384;
-    static constexpr uint32_t UD = UT + 16384;
+    static constexpr uint32_t SB = PT + 16384;          // K/64 blocks of 128 rows
+    // U^T (128 rows, split in two 64-row halves): at K = 128 it reuses the
+    // gamma-scaled Q tiles of the chunk's own stage, which are spent by then
+    static constexpr uint32_t UTS = SB + (K / 64) * 16384;
+    static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);
     static constexpr uint32_t AF = UD + 16384;          // float [64][68]
-    static constexpr uint32_t KGATE = AF + 64 * 68 * 4; // key group: G2, gamma, beta
-    static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;  // state group: 3 x (decay[64], gamma_C)
+    static constexpr uint32_t XS = AF + 64 * kLD * 4;   // float [3][16][16] block scratch
+    static constexpr uint32_t KGATE = XS + 3 * 256 * 4; // key group: G2, gamma, beta
+    static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;  // state: 3 x (decay[64], gamma_C)
     static constexpr uint32_t END = SGATE + 3 * 68 * 4;
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr uint32_t V_BYTES = 2u * 8192u;
     static constexpr size_t SMEM = END + 1024;          // + alignment slack
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static __device__ __forceinline__ uint32_t ut_half(int st, int hh) {
+        if (K == 128) return st * STAGE + (hh ? QC1 : QC0);
+        return UTS + hh * 8192;
+    }
     // TMEM columns
     static constexpr uint32_t D1 = 0, WT = 64, UA = 128, O = 256, DS = 384;
 };
@@ -80,12 +95,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-// Store 32 floats (times `scale`) of one tile row as 4 swizzled 16-byte chunks
-// starting at chunk c0.
-__device__ __forceinline__ void store_row32(uint8_t *tile, uint32_t row, uint32_t c0,
-                                            const float (&v)[32], float scale = 1.f) {
+// Store 8*NCH floats (times `scale`) of one tile row as NCH swizzled 16-byte
+// chunks starting at chunk c0.
+template <int NCH, int N>
+__device__ __forceinline__ void store_row(uint8_t *tile, uint32_t row, uint32_t c0,
+                                          const float (&v)[N], float scale = 1.f) {
+    static_assert(N == 8 * NCH, "row piece");
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < NCH; ++k) {
         uint4 w;
         w.x = pack_bf16(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
         w.y = pack_bf16(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
@@ -110,78 +127,106 @@ __device__ __forceinline__ void chunk_log2_prefix(float a0, float a1, int lane, 
     g1 += __shfl_sync(0xffffffffu, g0, 31);
 }
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A held in AF (row stride 68),
-// in place, by the 128 key-group threads: the two 32 x 32 diagonal blocks by
-// forward substitution (one column per thread), then
-// T21 = -T22 (A21 T11).  Upper-triangle entries of AF must be zero on entry.
-__device__ __forceinline__ void unit_lower_inverse(float *AF, int tid) {
-    constexpr int LD = 68;
+// Blocks of the fp32 64 x 64 matrix in AF (16 x 16 blocks, row stride kLD):
+//   A_ij (i > j) at block position (i, j); after the inverse, T_ii at (i, i)
+//   and T_ij (i > j) at the mirrored position (j, i).
+__device__ __forceinline__ float *blk(float *AF, int i, int j) {
+    return AF + 16 * i * kLD + 16 * j;
+}
+
+// Y = sum_k L_k R_k for 16 x 16 blocks (row stride kLD, or 16 when ld == 16),
+// 4 outputs per thread: row `row`, columns [c0, c0 + 4).
+__device__ __forceinline__ float4 blk_mac(const float *L0, const float *R0, int ldr,
+                                          const float *L1, const float *R1,
+                                          const float *L2, const float *R2, int nterm, int row,
+                                          int c0) {
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *Ls[3] = {L0, L1, L2};
+    const float *Rs[3] = {R0, R1, R2};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        if (k >= nterm) break;
+        const int ldrk = (k == 0) ? ldr : kLD;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float a = Ls[k][row * kLD + m];
+            const float4 r = *reinterpret_cast<const float4 *>(Rs[k] + m * ldrk + c0);
+            y.x = fmaf(a, r.x, y.x);
+            y.y = fmaf(a, r.y, y.y);
+            y.z = fmaf(a, r.z, y.z);
+            y.w = fmaf(a, r.w, y.w);
+        }
+    }
+    return y;
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A in AF (zeros on and above
+// the diagonal), by the 256 key-group threads: the four 16 x 16 diagonal
+// blocks by forward substitution (one column per thread), then the
+// off-diagonal blocks level by level, T_ij = -T_ii (sum_{j<=m<i} A_im T_mj),
+// each level a pair of 16 x 16 block products.  XS: scratch for 3 blocks.
+__device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid) {
     {
-        float x[32];
-        const int blk = tid >> 5, s = tid & 31;
+        float x[16];
+        const int bb = tid >> 4, s = tid & 15;
         if (tid < 64) {
-            const float *Ab = AF + (32 * blk) * LD + 32 * blk;
+            const float *Ab = blk(AF, bb, bb);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) x[t] = (t == s) ? 1.f : 0.f;
+            for (int t = 0; t < 16; ++t) x[t] = (t == s) ? 1.f : 0.f;
 #pragma unroll
-            for (int t = 1; t < 32; ++t) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            for (int t = 1; t < 16; ++t) {
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                 for (int r = 0; r < t; r += 4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(Ab + t * LD + r);
+                    const float4 a = *reinterpret_cast<const float4 *>(Ab + t * kLD + r);
                     a0 = fmaf(a.x, x[r], a0);
                     if (r + 1 < t) a1 = fmaf(a.y, x[r + 1], a1);
-                    if (r + 2 < t) a2 = fmaf(a.z, x[r + 2], a2);
-                    if (r + 3 < t) a3 = fmaf(a.w, x[r + 3], a3);
+                    if (r + 2 < t) a0 = fmaf(a.z, x[r + 2], a0);
+                    if (r + 3 < t) a1 = fmaf(a.w, x[r + 3], a1);
                 }
-                x[t] -= (a0 + a1) + (a2 + a3);
+                x[t] -= a0 + a1;
             }
         }
-        named_sync(kBarKey, kKeyThreads);  // every read of A11 / A22 done
+        named_sync(kBarKey, kKeyThreads);  // every read of the diagonal A blocks done
         if (tid < 64) {
-            float *Tb = AF + (32 * blk) * LD + 32 * blk;
+            float *Tb = blk(AF, bb, bb);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) Tb[t * LD + s] = x[t];
+            for (int t = 0; t < 16; ++t) Tb[t * kLD + s] = x[t];
         }
         named_sync(kBarKey, kKeyThreads);
     }
-    const int i = tid >> 2, j0 = (tid & 3) * 8;
-    float y[8];
-    // X = A21 T11  (T11 lower: terms m < j vanish)
+    const int job = tid >> 6;          // which block of this level
+    const int e = tid & 63;
+    const int row = e >> 2, c0 = (e & 3) * 4;
+    // level d: blocks (j + d, j), j = 0 .. 3 - d
 #pragma unroll
-    for (int c = 0; c < 8; ++c) y[c] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < 32; ++m) {
-        const float a = AF[(32 + i) * LD + m];
-        const float4 t0 = *reinterpret_cast<const float4 *>(AF + m * LD + j0);
-        const float4 t1 = *reinterpret_cast<const float4 *>(AF + m * LD + j0 + 4);
-        y[0] = fmaf(a, t0.x, y[0]); y[1] = fmaf(a, t0.y, y[1]);
-        y[2] = fmaf(a, t0.z, y[2]); y[3] = fmaf(a, t0.w, y[3]);
-        y[4] = fmaf(a, t1.x, y[4]); y[5] = fmaf(a, t1.y, y[5]);
-        y[6] = fmaf(a, t1.z, y[6]); y[7] = fmaf(a, t1.w, y[7]);
+    for (int d = 1; d <= 3; ++d) {
+        const int j = job, i = job + d;
+        const bool active = job <= 3 - d;
+        if (active) {
+            // X = sum_{m=j}^{i-1} A_im T_mj   (T_jj on the diagonal, T_mj, m > j, mirrored)
+            float4 y;
+            if (d == 1)
+                y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, nullptr, nullptr, nullptr, nullptr,
+                            1, row, c0);
+            else if (d == 2)
+                y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
+                            blk(AF, j, j + 1), nullptr, nullptr, 2, row, c0);
+            else
+                y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
+                            blk(AF, j, j + 1), blk(AF, i, j + 2), blk(AF, j, j + 2), 3, row, c0);
+            *reinterpret_cast<float4 *>(XS + job * 256 + row * 16 + c0) = y;
+        }
+        named_sync(kBarKey, kKeyThreads);
+        if (active) {
+            // T_ij = -T_ii X, stored mirrored at block (j, i)
+            const float4 y = blk_mac(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr,
+                                     nullptr, nullptr, 1, row, c0);
+            *reinterpret_cast<float4 *>(blk(AF, j, i) + row * kLD + c0) =
+                make_float4(-y.x, -y.y, -y.z, -y.w);
+        }
+        named_sync(kBarKey, kKeyThreads);
     }
-    named_sync(kBarKey, kKeyThreads);  // every read of A21 done
-    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0) = make_float4(y[0], y[1], y[2], y[3]);
-    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
-    named_sync(kBarKey, kKeyThreads);
-    // T21 = -T22 X  (T22 lower with unit diagonal)
-#pragma unroll
-    for (int c = 0; c < 8; ++c) y[c] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < 32; ++m) {
-        const float a = AF[(32 + i) * LD + 32 + m];
-        const float4 t0 = *reinterpret_cast<const float4 *>(AF + (32 + m) * LD + j0);
-        const float4 t1 = *reinterpret_cast<const float4 *>(AF + (32 + m) * LD + j0 + 4);
-        y[0] = fmaf(a, t0.x, y[0]); y[1] = fmaf(a, t0.y, y[1]);
-        y[2] = fmaf(a, t0.z, y[2]); y[3] = fmaf(a, t0.w, y[3]);
-        y[4] = fmaf(a, t1.x, y[4]); y[5] = fmaf(a, t1.y, y[5]);
-        y[6] = fmaf(a, t1.z, y[6]); y[7] = fmaf(a, t1.w, y[7]);
-    }
-    named_sync(kBarKey, kKeyThreads);  // every read of X done
-    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
-    *reinterpret_cast<float4 *>(AF + (32 + i) * LD + j0 + 4) =
-        make_float4(-y[4], -y[5], -y[6], -y[7]);
-    named_sync(kBarKey, kKeyThreads);
 }
 
 template <int K>
@@ -198,7 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    __shared__ uint64_t kq_full[2], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready, nw_free;
+    __shared__ uint64_t kq_full[3], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready, nw_free;
     __shared__ uint64_t ua_free[2], pt_free[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
@@ -219,7 +264,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &v_full, &bar_p1, &bar_w, &bar_u, &bar_s,
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full, &bar_p1, &bar_w, &bar_u, &bar_s,
                             &nw_ready, &nw_free, &ua_free[0], &ua_free[1], &pt_free[0],
                             &pt_free[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
@@ -231,9 +276,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tb = tmem_base_sh;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int quad_row = (warp & 3) * 32 + lane;  // TMEM lane of this thread
+    const int colhalf = (warp >> 2) & 1;          // which 32-column half this warp reads
 
     auto load_kq = [&](int n) {
-        const int st = n & 1;
+        const int st = n % L::NSTAGE;
         uint8_t *stg = sm + st * L::STAGE;
         mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
         tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, n * 64, b);
@@ -258,19 +305,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t I_AMN = idesc_bf16(128, 64, true, false);  // MN-major A
     constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);  // MN-major B, N = 64
     constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);    // MN-major B, N = K
+    constexpr uint32_t I_MM128 = idesc_bf16(128, 128, false, false);  // K-major, N = 128
 
     bool failed = false;
 
     if (tid < kKeyThreads) {
         // ================================================================ key group
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
         float *AF = reinterpret_cast<float *>(sm + L::AF);
+        float *XS = reinterpret_cast<float *>(sm + L::XS);
         float *G2 = reinterpret_cast<float *>(sm + L::KGATE);
         float *gam = G2 + 64;
         float *bet = G2 + 128;
-        const int r = tid;  // TMEM lane
-        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs
+        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
         auto prefetch_gates = [&](int n) {
-            if (warp == 0 && n < nchunks) {
+            if (warp == 1 && n < nchunks) {
                 const int nv = min(64, T - n * 64);
                 const size_t i0 = ((size_t)b * T + n * 64 + lane) * H + h;
                 const size_t i1 = i0 + (size_t)32 * H;
@@ -282,18 +331,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         prefetch_gates(0);
         if (tid == 0) {
-            load_kq(0);
-            if (nchunks > 1) load_kq(1);
+            for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
             load_v(0);
         }
         for (int n = 0; n < nchunks; ++n) {
-            const int st = n & 1;
+            const int st = n % L::NSTAGE;  // q/k stage
+            const int p2 = n & 1;          // P and U~ buffers
             const uint32_t stg = base + st * L::STAGE;
             const int nvalid = min(64, T - n * 64);
             bool ok = true;
             // ---- [K;Q] K^T ----
             if (tid == 0) {
-                ok = wait(&kq_full[st], (n >> 1) & 1);
+                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
                 if (ok) {
                     tc_fence_after();
 #pragma unroll
@@ -305,9 +354,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     mma_commit(&bar_p1);
                 }
+                if (ok && n >= 2) ok = wait(&pt_free[p2], ((n - 2) >> 1) & 1);
+                // T' / T'' share their buffer with the previous chunk's -W^T
+                if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
+                if (ok) ok = wait(&bar_p1, n & 1);
             }
-            // ---- gates of chunk n (warp 0), then prefetch chunk n + 1 ----
-            if (warp == 0) {
+            // ---- gates of chunk n (warp 1), then prefetch chunk n + 1 ----
+            if (warp == 1) {
                 float g0, g1;
                 chunk_log2_prefix(pa0, pa1, lane, nvalid, g0, g1);
                 G2[lane] = g0;
@@ -318,41 +371,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bet[lane + 32] = pb1;
                 prefetch_gates(n + 1);
             }
-            if (n >= 2 && r >= 64) ok = ok && wait(&pt_free[st], ((n - 2) >> 1) & 1);
+            // one thread waited for [K;Q] K^T (and for the P buffer); the barrier
+            // hands both, and the gates, to the whole group
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
 
-            // ---- A (fp32, solve input) and P (bf16 operand) ----
-            ok = __all_sync(0xffffffffu, wait(&bar_p1, n & 1));
-            if (ok) {
+            // ---- A (fp32, solve input) and P (bf16 operand): row quad_row, 32 columns ----
+            {
                 tc_fence_after();
-                float v0[32], v1[32];
-                tmem_ld32(tb + lane_off + L::D1, v0);
-                tmem_ld32(tb + lane_off + L::D1 + 32, v1);
+                float v[32];
+                tmem_ld32(tb + lane_off + L::D1 + 32 * colhalf, v);
                 tmem_ld_wait();
-                const int t = r & 63;
+                const int t = quad_row & 63;
                 const float gt = G2[t];
-                if (r < 64) {
+                const int s0 = 32 * colhalf;
+                float gs[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
+                    gs[i] = g.x; gs[i + 1] = g.y; gs[i + 2] = g.z; gs[i + 3] = g.w;
+                }
+                if (quad_row < 64) {
                     const float bt = bet[t];
 #pragma unroll
-                    for (int s = 0; s < 64; s += 4) {
+                    for (int i = 0; i < 32; i += 4) {
                         float a[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int ss = s + e;
-                            const float kk = ss < 32 ? v0[ss & 31] : v1[ss & 31];
-                            a[e] = ss < t ? bt * exp2f(gt - G2[ss]) * kk : 0.f;
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const int s = s0 + i + e2;
+                            a[e2] = s < t ? bt * exp2f(gt - gs[i + e2]) * v[i + e2] : 0.f;
                         }
-                        *reinterpret_cast<float4 *>(AF + t * 68 + s) = make_float4(a[0], a[1], a[2], a[3]);
+                        *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) =
+                            make_float4(a[0], a[1], a[2], a[3]);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v0[i] = i <= t ? exp2f(gt - G2[i]) * v0[i] : 0.f;
-                        v1[i] = i + 32 <= t ? exp2f(gt - G2[i + 32]) * v1[i] : 0.f;
-                    }
-                    uint8_t *pt = sm + L::PT + st * 8192;
-                    store_row32(pt, t, 0, v0);
-                    store_row32(pt, t, 4, v1);
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = s0 + i <= t ? exp2f(gt - gs[i]) * v[i] : 0.f;
+                    store_row<4>(sm + L::PT + p2 * 8192, t, 4 * colhalf, v);
                 }
             }
             fence_proxy_async_smem();
@@ -360,23 +415,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
 
             // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
-            unit_lower_inverse(AF, tid);
+            unit_lower_inverse(AF, XS, tid);
             {
-                const int t = tid >> 1, hf = tid & 1;
-                float tp[32], tpp[32];
+                const int t = tid >> 2, cb = tid & 3;  // row t, columns [16 cb, 16 cb + 16)
+                const int bt = t >> 4;
+                float x[16];
+                if (cb > bt) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(AF + t * 68 + 32 * hf + c);
-                    const float xs[4] = {x.x, x.y, x.z, x.w};
+                    for (int c = 0; c < 16; ++c) x[c] = 0.f;
+                } else {
+                    const float *src = (cb == bt) ? AF + t * kLD + 16 * cb
+                                                  : blk(AF, cb, bt) + (t & 15) * kLD;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 32 * hf + c + e;
-                        tpp[c + e] = xs[e] * bet[s];
-                        tp[c + e] = tpp[c + e] * gam[s];
+                    for (int c = 0; c < 16; c += 4) {
+                        const float4 y = *reinterpret_cast<const float4 *>(src + c);
+                        x[c] = y.x; x[c + 1] = y.y; x[c + 2] = y.z; x[c + 3] = y.w;
                     }
                 }
-                store_row32(sm + L::TP, t, 4 * hf, tp);
-                store_row32(sm + L::TPP, t, 4 * hf, tpp);
+                float tp[16], tpp[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int s = 16 * cb + c;
+                    tpp[c] = x[c] * bet[s];
+                    tp[c] = tpp[c] * gam[s];
+                }
+                store_row<2>(sm + L::TP, t, 2 * cb, tp);
+                store_row<2>(sm + L::TPP, t, 2 * cb, tpp);
             }
             fence_proxy_async_smem();
             named_sync(kBarKey, kKeyThreads);
@@ -384,42 +448,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
             if (tid == 0) {
                 ok = true;
-                if (n >= 2) ok = wait(&ua_free[st], ((n - 2) >> 1) & 1);
+                if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
                 ok = ok && wait(&v_full, n & 1);
                 if (ok) {
                     tc_fence_after();
-                    const uint32_t lbo_k = K == 128 ? 16384u : (L::VB - st * L::STAGE);
+                    const uint32_t lbo_k = K == 128 ? 16384u : (uint32_t)(L::VB - st * L::STAGE);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, lbo_k, 1024),
                                  sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
-                        mma_bf16(tb + L::UA + 64 * st, sdesc(base + L::VB + ks * 2048, 8192, 1024),
+                        mma_bf16(tb + L::UA + 64 * p2, sdesc(base + L::VB + ks * 2048, 8192, 1024),
                                  sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
                     }
                     mma_commit(&bar_w);
+                    ok = wait(&bar_w, n & 1);
                 }
+                if (ok && n + 1 < nchunks) load_v(n + 1);  // V consumed
             }
-            __syncwarp();
-            ok = __all_sync(0xffffffffu, wait(&bar_w, n & 1));
-            if (ok && tid == 0 && n + 1 < nchunks) load_v(n + 1);  // V consumed
-            if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+            {
                 tc_fence_after();
-                if (r < K) {
-                    float v0[32], v1[32];
-                    tmem_ld32(tb + lane_off + L::WT, v0);
-                    tmem_ld32(tb + lane_off + L::WT + 32, v1);
+                if (quad_row < K) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
                     tmem_ld_wait();
-                    store_row32(sm + L::NW, r, 0, v0, -1.f);
-                    store_row32(sm + L::NW, r, 4, v1, -1.f);
+                    store_row<4>(sm + L::NW, quad_row, 4 * colhalf, v, -1.f);
                 }
                 // Q <- diag(gamma) Q in place (the q tile is read again only by S Q^T)
                 uint8_t *stq = sm + st * L::STAGE;
 #pragma unroll
                 for (int e = tid; e < (K / 64) * 512; e += kKeyThreads) {
-                    const int blk = e >> 9, ee = e & 511;
-                    uint4 *p = reinterpret_cast<uint4 *>(stq + (blk ? L::QC1 : L::QC0) + ee * 16);
+                    const int blk_i = e >> 9, ee = e & 511;
+                    uint4 *p = reinterpret_cast<uint4 *>(stq + (blk_i ? L::QC1 : L::QC0) + ee * 16);
                     const float g = gam[ee >> 3];
                     uint4 w = *p;
                     uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
@@ -439,20 +499,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ================================================================ state group
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
         const int sid = tid - kKeyThreads;  // 0..255
         const int sw = sid >> 5;            // state warp 0..7
-        const int c = (warp & 3) * 32 + lane;  // state row = TMEM lane
+        const int c = quad_row;             // state row = TMEM lane
         const int hf = sw >> 2;             // column half
         float *sg = reinterpret_cast<float *>(sm + L::SGATE);  // 3 slots of 68 floats
-        // gates of chunk m for the state group (warp 4 only): decay[64], gamma_C
-        auto state_gates = [&](int m) {
+        // state-group gates (warp 8 only): decay[64] and gamma_C of chunk m into
+        // slot m % 3, from alpha values loaded one call earlier
+        float sa0 = 1.f, sa1 = 1.f;
+        auto sg_load = [&](int m) {
+            if (m < nchunks) {
+                const int nv = min(64, T - m * 64);
+                const size_t i0 = ((size_t)b * T + m * 64 + lane) * H + h;
+                sa0 = lane < nv ? alpha[i0] : 1.f;
+                sa1 = lane + 32 < nv ? alpha[i0 + (size_t)32 * H] : 1.f;
+            }
+        };
+        auto sg_compute = [&](int m) {
             if (m >= nchunks) return;
             const int nv = min(64, T - m * 64);
-            const size_t i0 = ((size_t)b * T + m * 64 + lane) * H + h;
-            const float a0 = lane < nv ? alpha[i0] : 1.f;
-            const float a1 = lane + 32 < nv ? alpha[i0 + (size_t)32 * H] : 1.f;
             float g0, g1;
-            chunk_log2_prefix(a0, a1, lane, nv, g0, g1);
+            chunk_log2_prefix(sa0, sa1, lane, nv, g0, g1);
             const float gC = __shfl_sync(0xffffffffu, g1, 31);
             float *slot = sg + (m % 3) * 68;
             slot[lane] = exp2f(gC - g0);
@@ -460,9 +528,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) slot[64] = exp2f(gC);
         };
         if (sw == 0) {
-            state_gates(0);
-            state_gates(1);
-            state_gates(2);
+            for (int m = 0; m < 3; ++m) {
+                sg_load(m);
+                sg_compute(m);
+            }
+            sg_load(3);
         }
         // initial state: fp32 registers + bf16 operand copy
         float S[KH];
@@ -480,78 +550,97 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
                 const int j = j0 + 32 * p;
-                store_row32(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+                store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         named_sync(kBarState, kStateThreads);
 
-        // U^T += S (-W^T) and O^T = S (gamma Q)^T for chunk m
-        auto issue_su = [&](int m) -> bool {
+        // U^T += S (-W^T) for chunk m (after the key group handed over -W^T)
+        auto issue_u = [&](int m) -> bool {
             if (!wait(&nw_ready, m & 1)) return false;
             tc_fence_after();
-            const int st = m & 1;
-            const uint32_t stg = base + st * L::STAGE;
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks) {
                 const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                const uint64_t sdA = sdesc(base + L::SB + kb * 16384 + ko, 16, 1024);
-                mma_bf16(tb + L::UA + 64 * st, sdA, sdesc(base + L::NW + ks * 2048, 8192, 1024),
-                         I_BMN, 1);
-                mma_bf16(tb + L::O + 64 * st, sdA,
-                         sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM, ks > 0);
+                mma_bf16(tb + L::UA + 64 * (m & 1),
+                         sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
+                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN, 1);
             }
-            mma_commit(&bar_u);
             mma_commit(&nw_free);
             return true;
         };
+        // O = [K; gamma Q] S^T for chunk m (token-major; TMEM lanes 64..127 hold
+        // gamma Q S^T), then bar_u tracks both products of the chunk
+        auto issue_o = [&](int m) {
+            tc_fence_after();
+            const uint32_t stg = base + (m % L::NSTAGE) * L::STAGE;
+#pragma unroll
+            for (int ks = 0; ks < K / 16; ++ks) {
+                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                mma_bf16(tb + L::O, sdesc(stg + (kb ? L::KC1 : L::KC0) + ko, 16, 1024),
+                         sdesc(base + L::SB + kb * 16384 + ko, 16, 1024), I_MM128, ks > 0);
+            }
+            mma_commit(&bar_u);
+        };
         if (sw == 0) {
             bool ok0 = true;
-            if (lane == 0) ok0 = issue_su(0);
+            if (lane == 0) {
+                ok0 = issue_u(0);
+                if (ok0) issue_o(0);
+            }
             ok0 = __shfl_sync(0xffffffffu, ok0, 0);
             failed = !ok0;
         }
-        if (named_sync_or(kBarState, kStateThreads, failed)) failed = true;
 
-        for (int n = 0; n < nchunks && !failed; ++n) {
-            const int st = n & 1;
+        for (int n = 0; n < nchunks; ++n) {
+            const int st = n % L::NSTAGE;
+            const int p2 = n & 1;
             const uint32_t stg = base + st * L::STAGE;
             const int nvalid = min(64, T - n * 64);
             const float *slot = sg + (n % 3) * 68;
-            // ---- U epilogue: U^T -> UT, U^T diag(decay) -> UD ----
-            bool ok = __all_sync(0xffffffffu, wait(&bar_u, n & 1));
-            if (ok) {
+            // ---- U epilogue: U^T -> UT halves, U^T diag(decay) -> UD ----
+            bool ok = !failed;
+            if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            {
                 tc_fence_after();
                 float v[32];
-                tmem_ld32(tb + lane_off + L::UA + 64 * st + 32 * hf, v);
+                tmem_ld32(tb + lane_off + L::UA + 64 * p2 + 32 * hf, v);
                 tmem_ld_wait();
-                store_row32(sm + L::UT, c, 4 * hf, v);
+                store_row<4>(sm + L::ut_half(st, c >> 6), c & 63, 4 * hf, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= slot[32 * hf + i];
-                store_row32(sm + L::UD, c, 4 * hf, v);
+                store_row<4>(sm + L::UD, c, 4 * hf, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            named_sync(kBarState, kStateThreads);
+            // ---- O += [any; P] U (token-major) and dS = U^T diag(decay) K ----
             if (sid == 0) {
-                mbar_arrive(&ua_free[st]);
+                mbar_arrive(&ua_free[p2]);
                 tc_fence_after();
+                const uint32_t pa = base + L::PT + p2 * 8192 - 8192;  // rows 64..127 = P
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    mma_bf16(tb + L::O + 64 * st, sdesc(base + L::UT + ks * 32, 16, 1024),
-                             sdesc(base + L::PT + st * 8192 + ks * 32, 16, 1024), I_MM, 1);
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tb + L::O + 64 * hh, sdesc(pa + ks * 32, 16, 1024),
+                                 sdesc(base + L::ut_half(st, hh) + ks * 32, 16, 1024), I_MM, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
                              sdesc(stg + L::KC0 + ks * 2048, 16384, 1024), I_DS, ks > 0);
-                }
                 mma_commit(&bar_s);
-                mma_commit(&pt_free[st]);
+                mma_commit(&pt_free[p2]);
+                ok = wait(&bar_s, n & 1);
+                if (ok && n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);  // stage consumed
             }
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
-            ok = __all_sync(0xffffffffu, wait(&bar_s, n & 1));
-            if (ok) {
+            {
                 tc_fence_after();
-                if (sid == 0 && n + 2 < nchunks) load_kq(n + 2);  // stage consumed
                 const float gC = slot[64];
                 const int j0 = hf * KH;
 #pragma unroll
@@ -565,36 +654,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         v[i] = S[32 * p + i];
                     }
                     const int j = j0 + 32 * p;
-                    store_row32(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+                    store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
-            // ---- next chunk's S-dependent products (warp 4), then this chunk's output ----
+            named_sync(kBarState, kStateThreads);
+            // ---- next chunk's U product (warp 8) while this chunk's output is stored ----
             if (sw == 0) {
                 bool ok1 = true;
-                if (lane == 0 && n + 1 < nchunks) ok1 = issue_su(n + 1);
+                if (lane == 0 && n + 1 < nchunks) ok1 = issue_u(n + 1);
                 ok1 = __shfl_sync(0xffffffffu, ok1, 0);
                 if (!ok1) failed = true;
-                state_gates(n + 3);  // slot (n + 3) % 3 == n % 3: this chunk's gates are done
+                // slot (n + 3) % 3 == n % 3: every reader of this chunk's gates has
+                // passed the barrier above
+                sg_compute(n + 3);
+                sg_load(n + 4);
             }
-            {
-                float v[32];
-                tmem_ld32(tb + lane_off + L::O + 64 * st + 32 * hf, v);
+            if ((warp & 3) >= 2) {
+                // token t = TMEM lane - 64; channels [64 hf, 64 hf + 64): two 128 B rows
+                const int t = c - 64;
+                float v0[32], v1[32];
+                tmem_ld32(tb + lane_off + L::O + 64 * hf, v0);
+                tmem_ld32(tb + lane_off + L::O + 64 * hf + 32, v1);
                 tmem_ld_wait();
-                if (o != nullptr) {
-                    __nv_bfloat16 *orow = o + (((size_t)b * T + n * 64) * H + h) * V + c;
-                    const size_t tstride = (size_t)H * V;
+                if (o != nullptr && t < nvalid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        o + (((size_t)b * T + n * 64 + t) * H + h) * V + 64 * hf);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * hf + i;
-                        if (t < nvalid) orow[t * tstride] = __float2bfloat16_rn(v[i]);
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(pack_bf16(v0[8 * k], v0[8 * k + 1]),
+                                            pack_bf16(v0[8 * k + 2], v0[8 * k + 3]),
+                                            pack_bf16(v0[8 * k + 4], v0[8 * k + 5]),
+                                            pack_bf16(v0[8 * k + 6], v0[8 * k + 7]));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[4 + k] = make_uint4(pack_bf16(v1[8 * k], v1[8 * k + 1]),
+                                                pack_bf16(v1[8 * k + 2], v1[8 * k + 3]),
+                                                pack_bf16(v1[8 * k + 4], v1[8 * k + 5]),
+                                                pack_bf16(v1[8 * k + 6], v1[8 * k + 7]));
                 }
-                tc_fence_before();
             }
+            tc_fence_before();
             if (named_sync_or(kBarState, kStateThreads, failed)) { failed = true; break; }
+            // O is free again: the next chunk's S Q^T
+            if (sid == 0 && n + 1 < nchunks) issue_o(n + 1);
         }
         if (!failed && ST != nullptr) {
             const int j0 = hf * KH;
@@ -612,7 +716,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tid == 0) {
             if (status) atomicOr(status, kStatusTimeout);
             // let in-flight loads land before the CTA's shared memory is released
-            for (int s = 0; s < 2; ++s) {
+            for (int s = 0; s < 3; ++s) {
                 mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
             }
