@@ -297,9 +297,11 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
 
 
 def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_ranks):
-    """Decode state GB/s.  Steps are replayed from a CUDA graph of `nsteps`
-    launches; 'as specified' updates one state in place (it may sit in L2);
-    'l2_cold' rotates over enough state buffers (>= 4x L2) per step."""
+    """Decode state GB/s.  Steps are replayed from a CUDA graph; 'as specified'
+    runs 64 steps on one state updated in place (it may sit in L2); 'l2_cold'
+    rotates every step to the next of n state buffers with n * state >= 4x L2,
+    and its graph holds max(64, n) steps so that every buffer is touched once
+    per replay (the per-step inputs cycle over 64 drawn steps)."""
     res = {}
     l2 = props.L2_cache_size if hasattr(props, "L2_cache_size") else 126 * 2**20
     H, V = 16, 128
@@ -319,6 +321,7 @@ def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_r
             S0 = torch.from_numpy(p.S0).cuda()
             out = {}
             for mode, nbuf in (("as_specified", 1), ("l2_cold", nbuf_cold)):
+                gsteps = max(nsteps, nbuf)
                 states = [S0.clone() for _ in range(nbuf)]
                 g = torch.cuda.CUDAGraph()
                 s = torch.cuda.Stream()
@@ -330,24 +333,26 @@ def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_r
                 torch.cuda.current_stream().wait_stream(s)
                 torch.cuda.synchronize()
                 with torch.cuda.graph(g):
-                    for t in range(nsteps):
-                        binding.gdn_decode_step(q[t], k[t], v[t], al[t], be[t], states[t % nbuf],
-                                                o[t], B, H, K, V, binding.GDN_BF16)
+                    for t in range(gsteps):
+                        i = t % nsteps
+                        binding.gdn_decode_step(q[i], k[i], v[i], al[i], be[i], states[t % nbuf],
+                                                o[i], B, H, K, V, binding.GDN_BF16)
                 reps = max(3, args.decode_reps)
                 tot, per = time_calls(g.replay, reps, 3, torch, barrier)
                 tot = max_over_ranks(tot)
-                step_us = tot / reps / nsteps * 1e3
+                step_us = tot / reps / gsteps * 1e3
                 gbs = decode_state_bytes(B, H, K, V) / (step_us / 1e6) / 1e9
                 out[mode] = {"us_per_step": step_us, "state_gbs": gbs,
                              "hbm_frac": gbs / peaks["hbm_gbs"], "state_buffers": nbuf,
+                             "graph_steps": gsteps,
                              "tokens_per_s": B / (step_us / 1e6)}
                 del g, states
             res[f"B{B}_dk{K}"] = out
     for B in (64, 1):
         a, b = res[f"B{B}_dk128"], res[f"B{B}_dk64"]
         res[f"B{B}_speedup_dk64"] = {m: a[m]["us_per_step"] / b[m]["us_per_step"] for m in a}
-    res["note"] = ("state GB/s = 8 V K B H / step time; steps replayed from a CUDA graph of "
-                   f"{nsteps} launches; hbm_frac uses the measured copy bandwidth")
+    res["note"] = ("state GB/s = 8 V K B H / step time; steps replayed from a CUDA graph; "
+                   "hbm_frac uses the measured copy bandwidth")
     return res
 
 
@@ -387,9 +392,13 @@ def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world):
 
 # ----------------------------------------------------------------- oracle arm
 def oracle_sample(p, seqs):
-    """Pick `seqs` (b, h) sequences of the workload (full length)."""
+    """`seqs` distinct (b, h) sequences of the workload, evenly spread, full length."""
     B, T, H, K = p.k.shape
-    pick = [(i % B, (i * 5) % H) for i in range(seqs)]
+    seqs = min(seqs, B * H)
+    if seqs == B * H:
+        return p
+    step = (B * H) // seqs
+    pick = [((j * step) // H, (j * step) % H) for j in range(seqs)]
     from gated_delta_rule_49_gb300 import inputs
     subs = [inputs.take_sequences(p, [b], [h]) for b, h in pick]
     cat = lambda xs: np.concatenate(xs, axis=0)  # noqa: E731
@@ -401,9 +410,9 @@ def oracle_sample(p, seqs):
 def cpu_baseline(p, seqs=None, reps=1):
     import oracle
     cores = os.cpu_count() or 1
-    seqs = seqs or 2 * cores
-    sub = oracle_sample(p, seqs)
     B, T, H, K = p.k.shape
+    seqs = seqs or B * H  # the whole workload: ~1 s on 16 cores
+    sub = oracle_sample(p, seqs)
     threads = min(cores, seqs)
     t0 = time.perf_counter()
     for _ in range(reps):

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     gdn_get_last_device_status,
     gdn_prefill,
     gdn_prefill_workspace_size,
+    gdn_selftest_wait_timeout,
     gdn_state_rank,
     gdn_status_string,
     gdn_version,

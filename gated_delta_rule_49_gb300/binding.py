@@ -36,6 +36,7 @@ EXPORTS = (
     "gdn_get_last_device_status",
     "gdn_status_string",
     "gdn_version",
+    "gdn_selftest_wait_timeout",
 )
 
 _lock = threading.Lock()
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = i
+        lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
+        lib.gdn_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
 
@@ -148,6 +151,11 @@ def gdn_get_last_device_status(stream=None) -> int:
 
 def gdn_status_string(status: int) -> str:
     return status_string(status)
+
+
+def gdn_selftest_wait_timeout(limit_cycles, stream=None) -> int:
+    st = load().gdn_selftest_wait_timeout(int(limit_cycles), _stream(stream))
+    return _check(st, "gdn_selftest_wait_timeout")
 
 
 def gdn_version() -> int:

@@ -131,6 +131,17 @@ GDN_API int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, fl
  */
 GDN_API int gdn_get_last_device_status(void *stream);
 
+/*
+ * gdn_selftest_wait_timeout -- exercise the bounded wait that every mbarrier
+ * wait of the tensor-core prefill goes through.  One thread of one CTA waits
+ * on a shared-memory barrier that nothing ever completes, gives up after
+ * limit_cycles SM clock cycles (1 <= limit_cycles <= 2^31), sets the timeout
+ * bit of the device status word and returns; the context stays usable.
+ * Asynchronous on `stream`; read the outcome with gdn_get_last_device_status
+ * (GDN_ERR_TIMEOUT).  Meant for tests of the failure-detection path.
+ */
+GDN_API int gdn_selftest_wait_timeout(long long limit_cycles, void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 GDN_API const char *gdn_status_string(int status);
 

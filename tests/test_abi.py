@@ -113,3 +113,8 @@ def test_state_rank_rejects_bad_arguments(lib):
 def test_workspace_query(lib):
     for K, V in ((32, 32), (64, 128), (128, 128)):
         assert binding.gdn_prefill_workspace_size(8, 4096, 16, K, V, 0) >= 0
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.gdn_selftest_wait_timeout(0, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_selftest_wait_timeout(1 << 40, None) == binding.GDN_ERR_INVALID_ARG
