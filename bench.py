@@ -67,6 +67,24 @@ def prefill_flops(B, T, H, K, V, C=64):
     return 2.0 * macs * B * T * H
 
 
+def measured_traffic(profile, source):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source has changed since the counters were taken (the summary
+    records the first 16 hex digits of the source's sha256)."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        src = open(os.path.join(ROOT, "gated_delta_rule_49_gb300", "csrc", source), "rb").read()
+    except OSError:
+        return None
+    sha = re.search(r"sha256 \(first 16 hex\): `([0-9a-f]{16})`", text)
+    byts = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+    if not sha or not byts or hashlib.sha256(src).hexdigest()[:16] != sha.group(1):
+        return None
+    return int(byts.group(1))
+
+
 def decode_state_bytes(B, H, K, V):
     return 2 * 4 * V * K * B * H
 
@@ -276,7 +294,8 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
             "unit": "GB/s" if roof_bound == "hbm" else "TFLOP/s",
             "frac": (achieved_gbs / peaks["hbm_gbs"]) if roof_bound == "hbm"
             else achieved_tf / peaks["bf16_tflops"],
-            "traffic": None,
+            "traffic": measured_traffic("prefill_tc_d128_prefill-workload.md",
+                                        "gdn_prefill_tc.cu"),
             "kernel": "gdn_prefill",
             "algorithmic_bytes": byts,
             "algorithmic_flops": flops,
