@@ -37,12 +37,12 @@ int *device_status_ptr() {
 
 int sm_count() {
     const int dev = current_device();
-    if (dev < 0) return 1;
+    if (dev < 0) return 0;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_sm_count[dev]) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-            n = 1;
+            return 0;
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
@@ -86,8 +86,10 @@ const char *gdn_status_string(int status) {
 }
 
 size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype) {
-    (void)B; (void)T; (void)H; (void)K; (void)V; (void)dtype;
-    return 0;
+    if (B <= 0 || T <= 0 || H <= 0 || V != 128 || (K != 128 && K != 64) || dtype != GDN_BF16)
+        return 0;
+    if ((long long)B * H > 0x7fffffffLL) return 0;
+    return gdn::segment_shape(B * H, T, K, gdn::sm_count()).workspace_bytes;
 }
 
 int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
@@ -118,7 +120,7 @@ int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
     // (32, 32) variant run the CUDA-core chunked kernel.
     if (dtype == GDN_BF16 && V == 128 && (K == 128 || K == 64))
         return from_cuda(gdn::launch_prefill_tc(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
-                                                st));
+                                                workspace, workspace_bytes, st));
     return from_cuda(gdn::launch_prefill_simt(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
                                               dtype, st));
 }

@@ -39,9 +39,20 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v,
                                 gdn_dtype dt, cudaStream_t stream);
 
 // Tensor-core (tcgen05) chunked prefill: bf16 q/k/v, V = 128, K in {64, 128}.
+// Long sequences on few heads run segment-parallel and need `workspace`.
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *ST, int B,
-                              int T, int H, int K, int V, cudaStream_t stream);
+                              int T, int H, int K, int V, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+// How the tensor-core prefill splits B*H sequences of T tokens into segments
+// on a device with `nsm` SMs (nseg == 1: one CTA per whole sequence).
+struct SegShape {
+    int nseg;
+    int seg_len;
+    size_t workspace_bytes;
+};
+SegShape segment_shape(int BH, int T, int K, int nsm);
 
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }

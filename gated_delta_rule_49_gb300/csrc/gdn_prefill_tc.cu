@@ -229,6 +229,25 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
     }
 }
 
+// Which token range, initial state and final-state slot a CTA works on.
+//   kWhole:  CTA = one (b, h) sequence, tokens [0, T), S0 / S_T as given.
+//   kFirst:  long sequences cut into `nseg` segments of `seg_len` tokens; per
+//            sequence 2 nseg - 1 CTAs: segment 0 from S0 with outputs (its end
+//            state into slot E), and for each later segment p the end state
+//            from a zero start (slot H) and the transition matrix (slot M: the
+//            same recurrence run on the rows of the identity with v = 0).
+//   kSecond: segments p >= 1 again from their start states (slot S, filled by
+//            the combine kernel) with outputs; the last one writes S_T.
+// The end state of a segment is affine in its start state (the update is
+// S -> alpha S (I - beta k k^T) + beta v k^T), so S_end = S_start M + H.
+enum SegMode : int { kWhole = 0, kFirst = 1, kSecond = 2 };
+struct SegPlan {
+    int mode;
+    int nseg;
+    int seg_len;  // multiple of 64
+    float *ws;    // [3][B*H][nseg][V][K]: H/E slots, M slots, start-state slots
+};
+
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -236,7 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ alpha,
                       const float *__restrict__ beta, const float *__restrict__ S0,
                       __nv_bfloat16 *__restrict__ o, float *__restrict__ ST, int T, int H,
-                      int *status) {
+                      int BH, SegPlan plan, int *status) {
     using L = TcLayout<K>;
     constexpr int V = 128;
     constexpr int KH = K / 2;  // state columns per state-group thread
@@ -251,9 +270,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x / H, h = blockIdx.x % H;
-    const size_t seq = (size_t)blockIdx.x;
-    const int nchunks = (T + 63) / 64;
+    // ---- this CTA's task ----
+    size_t seq = blockIdx.x;
+    int t0 = 0, t1 = T;
+    const float *s0p = S0;   // initial state (nullptr: zero)
+    bool s0_identity = false;
+    float *stp = ST ? ST + seq * V * K : nullptr;  // final state destination
+    bool zero_v = false;
+    if (plan.mode != kWhole) {
+        const size_t VK = (size_t)V * K;
+        auto slot = [&](int kind, size_t sq, int p) {
+            return plan.ws + ((kind * (size_t)BH + sq) * plan.nseg + p) * VK;
+        };
+        int p;
+        if (plan.mode == kFirst) {
+            seq = blockIdx.x / (2 * plan.nseg - 1);
+            const int i = blockIdx.x % (2 * plan.nseg - 1);
+            p = (i + 1) / 2;
+            if (i == 0) {
+                stp = slot(0, seq, 0);  // end of segment 0 (E)
+            } else if (i & 1) {
+                s0p = nullptr;          // zero start: H
+                stp = slot(0, seq, p);
+                o = nullptr;
+            } else {
+                s0p = nullptr;          // identity start, v = 0: M
+                s0_identity = true;
+                zero_v = true;
+                stp = slot(1, seq, p);
+                o = nullptr;
+            }
+        } else {
+            seq = blockIdx.x / (plan.nseg - 1);
+            p = 1 + blockIdx.x % (plan.nseg - 1);
+            s0p = slot(2, seq, p);
+            stp = (p == plan.nseg - 1 && ST) ? ST + seq * V * K : nullptr;
+        }
+        t0 = p * plan.seg_len;
+        t1 = min(T, t0 + plan.seg_len);
+        if (s0p == S0 && S0) s0p = S0 + seq * V * K;  // segment 0 of kFirst
+    } else if (S0) {
+        s0p = S0 + seq * V * K;
+    }
+    const int b = (int)(seq / H), h = (int)(seq % H);
+    const int nchunks = (t1 - t0 + 63) / 64;
     const uint32_t base = smem_u32(sm);
 
     if (warp == 0) {
@@ -283,17 +343,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int st = n % L::NSTAGE;
         uint8_t *stg = sm + st * L::STAGE;
         mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
-        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, n * 64, b);
-        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, n * 64, b);
+        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
+        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
         if (K == 128) {
-            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, n * 64, b);
-            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, n * 64, b);
+            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
+            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
         }
     };
     auto load_v = [&](int n) {
         mbar_arrive_expect_tx(&v_full, L::V_BYTES);
-        tma_load_4d(sm + L::VB, &tm_v, &v_full, 0, h, n * 64, b);
-        tma_load_4d(sm + L::VB + 8192, &tm_v, &v_full, 64, h, n * 64, b);
+        tma_load_4d(sm + L::VB, &tm_v, &v_full, 0, h, t0 + n * 64, b);
+        tma_load_4d(sm + L::VB + 8192, &tm_v, &v_full, 64, h, t0 + n * 64, b);
     };
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
@@ -320,8 +380,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
         auto prefetch_gates = [&](int n) {
             if (warp == 1 && n < nchunks) {
-                const int nv = min(64, T - n * 64);
-                const size_t i0 = ((size_t)b * T + n * 64 + lane) * H + h;
+                const int nv = min(64, t1 - t0 - n * 64);
+                const size_t i0 = ((size_t)b * T + t0 + n * 64 + lane) * H + h;
                 const size_t i1 = i0 + (size_t)32 * H;
                 pa0 = lane < nv ? alpha[i0] : 1.f;
                 pb0 = lane < nv ? beta[i0] : 0.f;
@@ -332,13 +392,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_gates(0);
         if (tid == 0) {
             for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
-            load_v(0);
+            if (!zero_v) load_v(0);
         }
         for (int n = 0; n < nchunks; ++n) {
             const int st = n % L::NSTAGE;  // q/k stage
             const int p2 = n & 1;          // P and U~ buffers
             const uint32_t stg = base + st * L::STAGE;
-            const int nvalid = min(64, T - n * 64);
+            const int nvalid = min(64, t1 - t0 - n * 64);
             bool ok = true;
             // ---- [K;Q] K^T ----
             if (tid == 0) {
@@ -449,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (tid == 0) {
                 ok = true;
                 if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
-                ok = ok && wait(&v_full, n & 1);
+                if (!zero_v) ok = ok && wait(&v_full, n & 1);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t lbo_k = K == 128 ? 16384u : (uint32_t)(L::VB - st * L::STAGE);
@@ -457,13 +517,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int ks = 0; ks < 4; ++ks) {
                         mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, lbo_k, 1024),
                                  sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
-                        mma_bf16(tb + L::UA + 64 * p2, sdesc(base + L::VB + ks * 2048, 8192, 1024),
-                                 sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
+                        if (!zero_v)
+                            mma_bf16(tb + L::UA + 64 * p2,
+                                     sdesc(base + L::VB + ks * 2048, 8192, 1024),
+                                     sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
                     }
                     mma_commit(&bar_w);
                     ok = wait(&bar_w, n & 1);
                 }
-                if (ok && n + 1 < nchunks) load_v(n + 1);  // V consumed
+                if (ok && !zero_v && n + 1 < nchunks) load_v(n + 1);  // V consumed
             }
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
             {
@@ -510,15 +572,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float sa0 = 1.f, sa1 = 1.f;
         auto sg_load = [&](int m) {
             if (m < nchunks) {
-                const int nv = min(64, T - m * 64);
-                const size_t i0 = ((size_t)b * T + m * 64 + lane) * H + h;
+                const int nv = min(64, t1 - t0 - m * 64);
+                const size_t i0 = ((size_t)b * T + t0 + m * 64 + lane) * H + h;
                 sa0 = lane < nv ? alpha[i0] : 1.f;
                 sa1 = lane + 32 < nv ? alpha[i0 + (size_t)32 * H] : 1.f;
             }
         };
         auto sg_compute = [&](int m) {
             if (m >= nchunks) return;
-            const int nv = min(64, T - m * 64);
+            const int nv = min(64, t1 - t0 - m * 64);
             float g0, g1;
             chunk_log2_prefix(sa0, sa1, lane, nv, g0, g1);
             const float gC = __shfl_sync(0xffffffffu, g1, 31);
@@ -541,7 +603,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int j = 0; j < KH; j += 4) {
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (S0) x = *reinterpret_cast<const float4 *>(S0 + (seq * V + c) * K + j0 + j);
+                if (s0p) x = *reinterpret_cast<const float4 *>(s0p + (size_t)c * K + j0 + j);
+                if (s0_identity) {
+                    x.x = (c == j0 + j) ? 1.f : 0.f;
+                    x.y = (c == j0 + j + 1) ? 1.f : 0.f;
+                    x.z = (c == j0 + j + 2) ? 1.f : 0.f;
+                    x.w = (c == j0 + j + 3) ? 1.f : 0.f;
+                }
                 S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
             }
 #pragma unroll
@@ -564,9 +632,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks) {
                 const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                // with v = 0 there is no U~ product: this one starts the accumulator
                 mma_bf16(tb + L::UA + 64 * (m & 1),
                          sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN, 1);
+                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN,
+                         zero_v ? (uint32_t)(ks > 0) : 1u);
             }
             mma_commit(&nw_free);
             return true;
@@ -598,7 +668,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int st = n % L::NSTAGE;
             const int p2 = n & 1;
             const uint32_t stg = base + st * L::STAGE;
-            const int nvalid = min(64, T - n * 64);
+            const int nvalid = min(64, t1 - t0 - n * 64);
             const float *slot = sg + (n % 3) * 68;
             // ---- U epilogue: U^T -> UT halves, U^T diag(decay) -> UD ----
             bool ok = !failed;
@@ -680,7 +750,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_ld_wait();
                 if (o != nullptr && t < nvalid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(
-                        o + (((size_t)b * T + n * 64 + t) * H + h) * V + 64 * hf);
+                        o + (((size_t)b * T + t0 + n * 64 + t) * H + h) * V + 64 * hf);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         dst[k] = make_uint4(pack_bf16(v0[8 * k], v0[8 * k + 1]),
@@ -700,11 +770,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // O is free again: the next chunk's S Q^T
             if (sid == 0 && n + 1 < nchunks) issue_o(n + 1);
         }
-        if (!failed && ST != nullptr) {
+        if (!failed && stp != nullptr) {
             const int j0 = hf * KH;
 #pragma unroll
             for (int j = 0; j < KH; j += 4)
-                *reinterpret_cast<float4 *>(ST + (seq * V + c) * K + j0 + j) =
+                *reinterpret_cast<float4 *>(stp + (size_t)c * K + j0 + j) =
                     make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
     }
@@ -761,10 +831,53 @@ bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int C)
            CUDA_SUCCESS;
 }
 
+// Start states of the later segments: S_1 = E (end of segment 0) and
+// S_{p+1} = S_p M_p + H_p, in float32.  Rows of the state are independent, so
+// a CTA owns 16 rows of one sequence: thread (i, j) = (tid / 16, tid % 16)
+// holds row i, columns j, j + 16, ...
+template <int K>
+__global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH, int nseg) {
+    constexpr int V = 128;
+    constexpr int NJ = K / 16;
+    __shared__ float srow[16][K + 4];
+    const size_t VK = (size_t)V * K;
+    const size_t seq = blockIdx.x;
+    const int r0 = blockIdx.y * 16;
+    const int i = threadIdx.x >> 4, jl = threadIdx.x & 15;
+    auto slot = [&](int kind, int p) { return ws + ((kind * (size_t)BH + seq) * nseg + p) * VK; };
+    const size_t rowoff = (size_t)(r0 + i) * K + jl;
+    float sv[NJ];
+    const float *E = slot(0, 0);
+#pragma unroll
+    for (int q = 0; q < NJ; ++q) sv[q] = E[rowoff + 16 * q];
+    for (int p = 1; p < nseg; ++p) {
+        float *Sp = slot(2, p);
+#pragma unroll
+        for (int q = 0; q < NJ; ++q) Sp[rowoff + 16 * q] = sv[q];
+        if (p == nseg - 1) break;
+        __syncthreads();  // every read of the previous rows done
+#pragma unroll
+        for (int q = 0; q < NJ; ++q) srow[i][jl + 16 * q] = sv[q];
+        __syncthreads();
+        const float *M = slot(1, p);
+        const float *Hp = slot(0, p);
+        float acc[NJ];
+#pragma unroll
+        for (int q = 0; q < NJ; ++q) acc[q] = Hp[rowoff + 16 * q];
+        for (int m = 0; m < K; ++m) {
+            const float x = srow[i][m];
+#pragma unroll
+            for (int q = 0; q < NJ; ++q) acc[q] = fmaf(x, M[(size_t)m * K + jl + 16 * q], acc[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < NJ; ++q) sv[q] = acc[q];
+    }
+}
+
 template <int K>
 cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *S0, void *o, float *ST, int B, int T,
-                        int H, cudaStream_t stream) {
+                        int H, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
     if (!make_token_map(&mq, q, B, T, H, K) || !make_token_map(&mk, k, B, T, H, K) ||
         !make_token_map(&mv, v, B, T, H, 128))
@@ -780,22 +893,76 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const long long grid = (long long)B * H;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, static_cast<__nv_bfloat16 *>(o), ST, T, H,
-        device_status_ptr());
+    const long long BH = (long long)B * H;
+    const SegShape sh = segment_shape(B * H, T, K, sm_count());
+    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(o);
+    int *status = device_status_ptr();
+    if (sh.nseg == 1) {
+        if (BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        kern<<<(unsigned)BH, kTcThreads, TcLayout<K>::SMEM, stream>>>(
+            mq, mk, mv, alpha, beta, S0, ob, ST, T, H, (int)BH, SegPlan{kWhole, 1, T, nullptr},
+            status);
+        return cudaGetLastError();
+    }
+    if (!workspace || workspace_bytes < sh.workspace_bytes) return cudaErrorInvalidValue;
+    float *ws = static_cast<float *>(workspace);
+    const long long g1 = BH * (2 * sh.nseg - 1), g2 = BH * (sh.nseg - 1);
+    if (g1 > 0x7fffffffLL || BH > 65535) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)g1, kTcThreads, TcLayout<K>::SMEM, stream>>>(
+        mq, mk, mv, alpha, beta, S0, ob, ST, T, H, (int)BH,
+        SegPlan{kFirst, sh.nseg, sh.seg_len, ws}, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    segment_combine_kernel<K><<<dim3((unsigned)BH, 128 / 16), 256, 0, stream>>>(ws, (int)BH,
+                                                                                sh.nseg);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)g2, kTcThreads, TcLayout<K>::SMEM, stream>>>(
+        mq, mk, mv, alpha, beta, S0, ob, ST, T, H, (int)BH,
+        SegPlan{kSecond, sh.nseg, sh.seg_len, ws}, status);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// Number of segments for B*H sequences of T tokens on `nsm` SMs: a cost model
+// in chunk-times.  One CTA per sequence costs ceil(BH / nsm) waves of the
+// whole length; with P segments the first pass runs BH (2P - 1) CTAs and the
+// second BH (P - 1), each over T / P tokens, plus the combine (~0.6 chunk-time
+// per segment) and a ~2 chunk-time start-up per wave.
+SegShape segment_shape(int BH, int T, int K, int nsm) {
+    SegShape sh{1, T, 0};
+    const int nchunks = (T + 63) / 64;
+    if (nsm < 2 || BH < 1 || BH * 2 > nsm || nchunks < 16) return sh;
+    auto waves = [&](long long ctas) { return (double)((ctas + nsm - 1) / nsm); };
+    double best = (nchunks + 2) * waves(BH);
+    int bestP = 1;
+    for (int P = 2; P <= 64 && nchunks / P >= 4; ++P) {
+        const int segc = (nchunks + P - 1) / P;
+        const double cost = (segc + 2) * (waves((long long)BH * (2 * P - 1)) +
+                                          waves((long long)BH * (P - 1))) + 0.6 * P;
+        if (cost < best) { best = cost; bestP = P; }
+    }
+    if (bestP == 1) return sh;
+    const int segc = (nchunks + bestP - 1) / bestP;
+    sh.seg_len = segc * 64;
+    sh.nseg = (T + sh.seg_len - 1) / sh.seg_len;
+    if (sh.nseg < 2) return SegShape{1, T, 0};
+    sh.workspace_bytes = 3ull * BH * sh.nseg * 128ull * K * sizeof(float);
+    return sh;
+}
+
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *ST, int B,
-                              int T, int H, int K, int V, cudaStream_t stream) {
+                              int T, int H, int K, int V, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
     if (V != 128) return cudaErrorInvalidValue;
-    if (K == 128) return launch_tc_t<128>(q, k, v, alpha, beta, S0, o, ST, B, T, H, stream);
-    if (K == 64) return launch_tc_t<64>(q, k, v, alpha, beta, S0, o, ST, B, T, H, stream);
+    if (K == 128)
+        return launch_tc_t<128>(q, k, v, alpha, beta, S0, o, ST, B, T, H, workspace,
+                                workspace_bytes, stream);
+    if (K == 64)
+        return launch_tc_t<64>(q, k, v, alpha, beta, S0, o, ST, B, T, H, workspace,
+                               workspace_bytes, stream);
     return cudaErrorInvalidValue;
 }
 
