@@ -262,6 +262,10 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         extra["state_rank"] = {"ms_per_call": tr / 5, "states": B * H,
                                "median_er": float(er.median().item())}
 
+        # ---- long-context prefill: B=1, T=65536, H=16 (segment-parallel) ----
+        extra["long_context"] = bench_long(args, torch, binding, inputs, peaks, barrier,
+                                           max_over_ranks, world)
+
         # ---- decode: B = 64 and 1, d_k 128 and 64 ----
         extra["decode"] = bench_decode(args, torch, binding, inputs, peaks, props, barrier,
                                        max_over_ranks)
@@ -377,6 +381,40 @@ def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_r
     res["note"] = ("state GB/s = 8 V K B H / step time; steps replayed from a CUDA graph; "
                    "hbm_frac uses the measured copy bandwidth")
     return res
+
+
+def bench_long(args, torch, binding, inputs, peaks, barrier, max_over_ranks, world):
+    """Long-context prefill (B=1, T=65536, H=16, d_k=d_v=128, alpha in
+    [0.9995, 0.9999], keys in a narrow cone) and the stable rank of its final
+    states.  Few heads and a long sequence: the prefill runs segment-parallel
+    with the workspace reported by gdn_prefill_workspace_size."""
+    p = inputs.make_long()
+    B, T, H, K = p.k.shape
+    V = p.v.shape[-1]
+    d = problem_to_dev(p, torch)
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
+    ST = torch.empty((B, H, V, K), dtype=torch.float32, device="cuda")
+    wsb = binding.gdn_prefill_workspace_size(B, T, H, K, V, binding.GDN_BF16)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+
+    def step():
+        binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T, H,
+                            K, V, binding.GDN_BF16, ws if wsb else None, wsb)
+
+    steps = max(3, min(args.steps, 10))
+    tot, per = time_calls(step, steps, 3, torch, barrier)
+    tot = max_over_ranks(tot)
+    ms = tot / steps
+    f2 = torch.empty(B * H, device="cuda")
+    s1 = torch.empty_like(f2)
+    er = torch.empty_like(f2)
+    binding.gdn_state_rank(ST, B * H, V, K, f2, s1, er, 2000, 0.0)
+    return {"workload": "B=1 T=65536 H=16 d_k=d_v=128 bf16, alpha U[0.9995,0.9999], cone keys",
+            "ms_per_step": ms, "tokens_per_s": B * T * world / (ms / 1e3),
+            "achieved_gbs": prefill_bytes(B, T, H, K, V) / (ms / 1e3) / 1e9,
+            "hbm_frac": prefill_bytes(B, T, H, K, V) / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "workspace_bytes": wsb,
+            "stable_rank_per_head": [round(float(x), 3) for x in er.cpu()]}
 
 
 def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world):
