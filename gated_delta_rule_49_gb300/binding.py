@@ -37,6 +37,8 @@ EXPORTS = (
     "gdn_status_string",
     "gdn_version",
     "gdn_selftest_wait_timeout",
+    "gdn_prefill_noalloc",
+    "gdn_prefill_noalloc_max_workspace",
 )
 
 _lock = threading.Lock()
@@ -77,6 +79,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_version.restype = i
         lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
         lib.gdn_selftest_wait_timeout.restype = i
+        lib.gdn_prefill_noalloc.argtypes = [vp] * 8 + [i] * 6 + [vp]
+        lib.gdn_prefill_noalloc.restype = i
+        lib.gdn_prefill_noalloc_max_workspace.argtypes = []
+        lib.gdn_prefill_noalloc_max_workspace.restype = sz
         _lib = lib
         return lib
 
@@ -126,6 +132,19 @@ def gdn_prefill(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, workspac
                             _ptr(o), _ptr(S_T), B, T, H, K, V, dtype, _ptr(workspace),
                             workspace_bytes, _stream(stream))
     return _check(st, "gdn_prefill")
+
+
+def gdn_prefill_noalloc(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype,
+                        stream=None) -> int:
+    """gdn_prefill without a workspace argument: its scratch is a fixed array
+    inside the library (for callers that cannot allocate device memory)."""
+    st = load().gdn_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                                    _ptr(o), _ptr(S_T), B, T, H, K, V, dtype, _stream(stream))
+    return _check(st, "gdn_prefill_noalloc")
+
+
+def gdn_prefill_noalloc_max_workspace() -> int:
+    return int(load().gdn_prefill_noalloc_max_workspace())
 
 
 def gdn_prefill_workspace_size(B, T, H, K, V, dtype) -> int:

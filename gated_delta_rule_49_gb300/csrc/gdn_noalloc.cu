@@ -1,0 +1,54 @@
+// gdn_prefill_noalloc: gdn_prefill for callers that cannot allocate device
+// memory.  The scratch that the segment-parallel prefill needs lives in one
+// file-scope device array of fixed size instead of a caller-supplied buffer.
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+namespace {
+
+// Scratch for gdn_prefill_noalloc.  Every GPU that loads the library holds
+// these 32 MiB until the process exits.  In host code `g_noalloc_scratch` is
+// only a host-side stand-in for the symbol, never a device address: the
+// address is looked up per device with cudaGetSymbolAddress below.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDev];
+
+// Device address of the scratch array on the current device (looked up once
+// per device, with that device current), or nullptr on failure.
+void *scratch_address() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t gdn_prefill_noalloc_max_workspace(void) { return kNoAllocScratchBytes; }
+
+extern "C" int gdn_prefill_noalloc(const void *q, const void *k, const void *v,
+                                   const float *alpha, const float *beta, const float *S0,
+                                   void *o, float *S_T, int B, int T, int H, int K, int V,
+                                   gdn_dtype dtype, void *stream) {
+    const size_t need = gdn_prefill_workspace_size(B, T, H, K, V, dtype);
+    if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
+    void *ws = nullptr;
+    if (need > 0) {
+        ws = scratch_address();
+        if (!ws) return GDN_ERR_CUDA;
+    }
+    // Every slot of the scratch that the prefill reads is written earlier in
+    // the same call, so nothing has to be cleared between calls.
+    return gdn_prefill(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, ws,
+                       need > 0 ? kNoAllocScratchBytes : 0, stream);
+}

@@ -92,6 +92,37 @@ GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const float
 GDN_API size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype);
 
 /*
+ * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate device
+ * memory: for example a component that only receives device pointers from the
+ * framework that owns the GPU's memory, or a server that reserves all of its
+ * memory at start-up and must not call cudaMalloc afterwards (an allocation can
+ * synchronise the device and its size is not known in advance).  The pages
+ * have no counterpart; this is a deployment convenience of this library.
+ *
+ * Same arguments, results and errors as gdn_prefill, without the workspace:
+ * the scratch that the segment-parallel path needs (see
+ * gdn_prefill_workspace_size) comes from one 32 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  A problem that needs more scratch than that returns
+ * GDN_ERR_WORKSPACE before anything is launched.  The call allocates nothing.
+ *
+ *  - The first call on a device that needs scratch looks up the array's
+ *    device address (cudaGetSymbolAddress) with that device current; make
+ *    that first call before any stream capture.
+ *  - All calls on a device share the one array, and it keeps the contents of
+ *    the last call.  Nothing needs clearing (each call writes every scratch
+ *    value it reads), but calls that may overlap on the GPU -- on different
+ *    streams, or from several host threads -- race on the scratch: order them
+ *    on one stream or serialise them.
+ */
+GDN_API int gdn_prefill_noalloc(const void *q, const void *k, const void *v, const float *alpha,
+                                const float *beta, const float *S0, void *o, float *S_T, int B,
+                                int T, int H, int K, int V, gdn_dtype dtype, void *stream);
+
+/* Scratch bytes available to gdn_prefill_noalloc (the size of its array). */
+GDN_API size_t gdn_prefill_noalloc_max_workspace(void);
+
+/*
  * gdn_decode_step -- one token of the recurrence for every (b, h), with the
  * state updated in place:
  *
