@@ -494,7 +494,8 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     W = WORKLOAD
-    p = inputs.make_prefill(B=W["B"], T=W["T"], H=W["H"], K=W["d_k"], V=W["d_v"])
+    Bw = args.ref_batch or W["B"]
+    p = inputs.make_prefill(B=Bw, T=W["T"], H=W["H"], K=W["d_k"], V=W["d_v"])
     cores = os.cpu_count() or 1
     seqs = min(cores, 16)
     sub = oracle_sample(p, seqs)
@@ -513,7 +514,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": dict(WORKLOAD),
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": dict(WORKLOAD, B=Bw),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": seqs, "kind": "oracle",
                          "sample": f"{seqs} (b, h) sequences x first {Tc} tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -522,6 +523,28 @@ def run_reference(args, rank, world):
 
 
 # ----------------------------------------------------------------- main
+def rank_sync(world, backend, device):
+    """(barrier, max_over_ranks) for `world` ranks.  The path shards whole
+    sequences across GPUs with no exchange step, so the only collectives are
+    the timing barrier and the max over ranks of the elapsed time."""
+    if world <= 1:
+        return None, (lambda x: x)
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        if backend == "nccl":
+            dist.init_process_group(backend, device_id=device)
+        else:
+            dist.init_process_group(backend)
+
+    def max_over_ranks(x):
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return dist.barrier, max_over_ranks
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,6 +556,9 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=None)
     ap.add_argument("--decode-reps", type=int, default=20)
     ap.add_argument("--ref-tokens", type=int, default=4096)
+    ap.add_argument("--ref-batch", type=int, default=None,
+                    help="batch of the workload the reference arm samples (default: the "
+                         "headline batch); the sample is whole sequences either way")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -549,17 +575,7 @@ def main():
 
     import torch
     torch.cuda.set_device(local)
-    barrier = None
-    max_over_ranks = lambda x: x  # noqa: E731
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        barrier = dist.barrier
-
-        def max_over_ranks(x):
-            t = torch.tensor([x], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
+    barrier, max_over_ranks = rank_sync(world, "nccl", torch.device("cuda", local))
 
     line = run_ours(args, rank, world, barrier, max_over_ranks)
     if rank == 0:
