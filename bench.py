@@ -228,7 +228,6 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
     extra = {}
     if not args.quick:
         # ---- pruned d_k' = 64, same draws ----
-        del d
         pp = inputs.make_prefill(B=B, T=T, H=H, K=K, V=V, pruned_K=64)
         dp = problem_to_dev(pp, torch)
         STp = torch.empty((B, H, V, 64), dtype=torch.float32, device="cuda")
@@ -248,7 +247,12 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
             "achieved_tflops": prefill_flops(B, T, H, 64, V) / (k64 / 1e3) / 1e12,
         }
         extra["pruned_dk64"]["hbm_frac"] = extra["pruned_dk64"]["achieved_gbs"] / peaks["hbm_gbs"]
-        del dp, pp
+
+        # ---- pruning prologue from the full-width q/k of the headline run ----
+        idx = torch.from_numpy(pp.meta["kept_channels"].astype(np.int32)).cuda()
+        extra["prologue"] = bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier,
+                                           max_over_ranks, world)
+        del d, dp, pp
 
         # ---- stable-rank epilogue on the final states of the headline run ----
         f2 = torch.empty(B * H, device="cuda")
@@ -325,62 +329,134 @@ def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_r
     rotates every step to the next of n state buffers with n * state >= 4x L2,
     and its graph holds max(64, n) steps so that every buffer is touched once
     per replay (the per-step inputs cycle over 64 drawn steps).  At B = 1 a
-    step is latency-bound and only the as-specified run is reported."""
+    step is latency-bound and only the as-specified run is reported.  At
+    B = 64 the pruned step is also timed from full-width q/k: gathered and
+    renormalised inside the step ('gathered'), and as two prologue launches
+    followed by the plain step ('unfused')."""
     res = {}
     l2 = props.L2_cache_size if hasattr(props, "L2_cache_size") else 126 * 2**20
     H, V = 16, 128
     nsteps = 64
+    launches = 0
+
+    def steps_first(x, bf16=True):
+        x = np.ascontiguousarray(np.moveaxis(x, 1, 0))
+        return to_dev_bf16(x, torch) if bf16 else torch.from_numpy(x).cuda()
+
+    def graph_time(call, S0, nbuf, B, K, per_step_launches):
+        nonlocal launches
+        gsteps = max(nsteps, nbuf)
+        states = [S0.clone() for _ in range(nbuf)]
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for t in range(3):  # warm-up outside capture
+                call(t, states[t % nbuf])
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for t in range(gsteps):
+                call(t % nsteps, states[t % nbuf])
+        reps = max(3, args.decode_reps)
+        tot, _ = time_calls(g.replay, reps, 3, torch, barrier)
+        launches += reps * gsteps * per_step_launches
+        tot = max_over_ranks(tot)
+        step_us = tot / reps / gsteps * 1e3
+        gbs = decode_state_bytes(B, H, K, V) / (step_us / 1e6) / 1e9
+        del g, states
+        return {"us_per_step": step_us, "state_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+                "state_buffers": nbuf, "graph_steps": gsteps,
+                "tokens_per_s": B / (step_us / 1e6)}
+
     for B in (64, 1):
         for K in (128, 64):
             p = inputs.make_decode(B=B, H=H, K=128, V=V, steps=nsteps,
                                    pruned_K=None if K == 128 else 64)
-            q = to_dev_bf16(np.ascontiguousarray(p.q.transpose(1, 0, 2, 3)), torch)
-            k = to_dev_bf16(np.ascontiguousarray(p.k.transpose(1, 0, 2, 3)), torch)
-            v = to_dev_bf16(np.ascontiguousarray(p.v.transpose(1, 0, 2, 3)), torch)
-            al = torch.from_numpy(np.ascontiguousarray(p.alpha.transpose(1, 0, 2))).cuda()
-            be = torch.from_numpy(np.ascontiguousarray(p.beta.transpose(1, 0, 2))).cuda()
+            q, k, v = steps_first(p.q), steps_first(p.k), steps_first(p.v)
+            al, be = steps_first(p.alpha, False), steps_first(p.beta, False)
             o = torch.empty((nsteps, B, H, V), dtype=torch.bfloat16, device="cuda")
             sbytes = 4 * B * H * V * K
             nbuf_cold = max(1, -(-4 * l2 // sbytes))
             S0 = torch.from_numpy(p.S0).cuda()
-            out = {}
             modes = [("as_specified", 1)]
             if B > 1:  # a B = 1 step (1 MB of state) is latency-bound; no L2-cold run
                 modes.append(("l2_cold", nbuf_cold))
-            for mode, nbuf in modes:
-                gsteps = max(nsteps, nbuf)
-                states = [S0.clone() for _ in range(nbuf)]
-                g = torch.cuda.CUDAGraph()
-                s = torch.cuda.Stream()
-                s.wait_stream(torch.cuda.current_stream())
-                with torch.cuda.stream(s):
-                    for t in range(3):  # warm-up outside capture
-                        binding.gdn_decode_step(q[t], k[t], v[t], al[t], be[t], states[t % nbuf],
-                                                o[t], B, H, K, V, binding.GDN_BF16)
-                torch.cuda.current_stream().wait_stream(s)
-                torch.cuda.synchronize()
-                with torch.cuda.graph(g):
-                    for t in range(gsteps):
-                        i = t % nsteps
-                        binding.gdn_decode_step(q[i], k[i], v[i], al[i], be[i], states[t % nbuf],
-                                                o[i], B, H, K, V, binding.GDN_BF16)
-                reps = max(3, args.decode_reps)
-                tot, per = time_calls(g.replay, reps, 3, torch, barrier)
-                tot = max_over_ranks(tot)
-                step_us = tot / reps / gsteps * 1e3
-                gbs = decode_state_bytes(B, H, K, V) / (step_us / 1e6) / 1e9
-                out[mode] = {"us_per_step": step_us, "state_gbs": gbs,
-                             "hbm_frac": gbs / peaks["hbm_gbs"], "state_buffers": nbuf,
-                             "graph_steps": gsteps,
-                             "tokens_per_s": B / (step_us / 1e6)}
-                del g, states
-            res[f"B{B}_dk{K}"] = out
+
+            def plain(i, S):
+                binding.gdn_decode_step(q[i], k[i], v[i], al[i], be[i], S, o[i], B, H, K, V,
+                                        binding.GDN_BF16)
+
+            res[f"B{B}_dk{K}"] = {m: graph_time(plain, S0, n, B, K, 1) for m, n in modes}
+            if B == 64 and K == 64:
+                pf = inputs.make_decode(B=B, H=H, K=128, V=V, steps=nsteps)
+                qf, kf = steps_first(pf.q), steps_first(pf.k)
+                idx = torch.from_numpy(p.meta["kept_channels"].astype(np.int32)).cuda()
+                qg = torch.empty((B, H, K), dtype=torch.bfloat16, device="cuda")
+                kg = torch.empty_like(qg)
+
+                def fused(i, S):
+                    binding.gdn_decode_step_gathered(qf[i], kf[i], idx, 128, v[i], al[i], be[i],
+                                                     S, o[i], B, H, K, V, binding.GDN_BF16)
+
+                def unfused(i, S):
+                    binding.gdn_gather_normalize(qf[i], idx, qg, B, H, 128, K, binding.GDN_BF16)
+                    binding.gdn_gather_normalize(kf[i], idx, kg, B, H, 128, K, binding.GDN_BF16)
+                    binding.gdn_decode_step(qg, kg, v[i], al[i], be[i], S, o[i], B, H, K, V,
+                                            binding.GDN_BF16)
+
+                res[f"B{B}_dk{K}_gathered"] = {m: graph_time(fused, S0, n, B, K, 1)
+                                               for m, n in modes}
+                res[f"B{B}_dk{K}_unfused"] = {m: graph_time(unfused, S0, n, B, K, 3)
+                                              for m, n in modes}
+                del pf, qf, kf
     for B in (64, 1):
         a, b = res[f"B{B}_dk128"], res[f"B{B}_dk64"]
         res[f"B{B}_speedup_dk64"] = {m: a[m]["us_per_step"] / b[m]["us_per_step"] for m in a}
+    a, g = res["B64_dk128"], res["B64_dk64_gathered"]
+    res["B64_speedup_dk64_gathered"] = {m: a[m]["us_per_step"] / g[m]["us_per_step"] for m in a}
     res["note"] = ("state GB/s = 8 V K B H / step time; steps replayed from a CUDA graph; "
-                   "hbm_frac uses the measured copy bandwidth")
+                   "hbm_frac uses the measured copy bandwidth; 'gathered' and 'unfused' take "
+                   "full-width (d_k = 128) q/k and keep 64 channels per head")
+    res["launches"] = launches
     return res
+
+
+def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over_ranks, world):
+    """The pruning prologue on the prefill workload's full-width bf16 q and k
+    (d_k = 128 -> 64 kept channels per head): the prologue alone (two
+    launches), and prologue + d_k' = 64 prefill as one pruned pipeline.
+    Prologue bytes per row: the full-width row read (a random half of the
+    channels touches every 32-byte sector) plus the kept row written."""
+    B, T, H, Kin = d["q"].shape
+    Kout = idx.shape[-1]
+    V = o.shape[-1]
+    rows = B * T * H
+    qg = torch.empty((B, T, H, Kout), dtype=torch.bfloat16, device="cuda")
+    kg = torch.empty_like(qg)
+    ST = torch.empty((B, H, V, Kout), dtype=torch.float32, device="cuda")
+
+    def pro():
+        binding.gdn_gather_normalize(d["q"], idx, qg, B * T, H, Kin, Kout, binding.GDN_BF16)
+        binding.gdn_gather_normalize(d["k"], idx, kg, B * T, H, Kin, Kout, binding.GDN_BF16)
+
+    def pipeline():
+        pro()
+        binding.gdn_prefill(qg, kg, dp["v"], dp["alpha"], dp["beta"], None, o, ST, B, T, H,
+                            Kout, V, binding.GDN_BF16)
+
+    tp, _ = time_calls(pro, args.steps, args.warmup, torch, barrier)
+    tp = max_over_ranks(tp)
+    tl, _ = time_calls(pipeline, args.steps, args.warmup, torch, barrier)
+    tl = max_over_ranks(tl)
+    byts = 2 * rows * (2 * Kin + 2 * Kout)
+    gbs = byts / (tp / args.steps / 1e3) / 1e9
+    return {"workload": f"B={B} T={T} H={H} bf16 q and k, d_k {Kin} -> {Kout}",
+            "prologue_us": tp / args.steps * 1e3, "prologue_gbs": gbs,
+            "prologue_hbm_frac": gbs / peaks["hbm_gbs"],
+            "pipeline_ms_per_step": tl / args.steps,
+            "pipeline_tokens_per_s": B * T * world * args.steps / (tl / 1e3),
+            "launches": args.steps * 5}
 
 
 def bench_long(args, torch, binding, inputs, peaks, barrier, max_over_ranks, world):

@@ -12,6 +12,9 @@ from .binding import (  # noqa: F401
     GDNError,
     decode_step,
     gdn_decode_step,
+    gdn_decode_step_gathered,
+    gdn_gather_normalize,
+    gather_normalize,
     gdn_get_last_device_status,
     gdn_prefill,
     gdn_prefill_workspace_size,

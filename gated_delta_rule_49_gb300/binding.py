@@ -39,6 +39,8 @@ EXPORTS = (
     "gdn_selftest_wait_timeout",
     "gdn_prefill_noalloc",
     "gdn_prefill_noalloc_max_workspace",
+    "gdn_gather_normalize",
+    "gdn_decode_step_gathered",
 )
 
 _lock = threading.Lock()
@@ -81,6 +83,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_selftest_wait_timeout.restype = i
         lib.gdn_prefill_noalloc.argtypes = [vp] * 8 + [i] * 6 + [vp]
         lib.gdn_prefill_noalloc.restype = i
+        lib.gdn_gather_normalize.argtypes = [vp, vp, vp, ctypes.c_longlong, i, i, i, i, vp]
+        lib.gdn_gather_normalize.restype = i
+        lib.gdn_decode_step_gathered.argtypes = [vp, vp, vp, i] + [vp] * 5 + [i] * 5 + [vp]
+        lib.gdn_decode_step_gathered.restype = i
         lib.gdn_prefill_noalloc_max_workspace.argtypes = []
         lib.gdn_prefill_noalloc_max_workspace.restype = sz
         _lib = lib
@@ -162,6 +168,32 @@ def gdn_state_rank(S, BH, V, K, fro2, sigma1, stable_rank, max_iter=500, tol=1e-
     st = load().gdn_state_rank(_ptr(S), BH, V, K, _ptr(fro2), _ptr(sigma1), _ptr(stable_rank),
                                max_iter, tol, _stream(stream))
     return _check(st, "gdn_state_rank")
+
+
+def gdn_gather_normalize(x, idx, y, N, H, K_in, K_out, dtype, stream=None) -> int:
+    st = load().gdn_gather_normalize(_ptr(x), _ptr(idx), _ptr(y), N, H, K_in, K_out, dtype,
+                                     _stream(stream))
+    return _check(st, "gdn_gather_normalize")
+
+
+def gdn_decode_step_gathered(q_full, k_full, idx, K_in, v, alpha, beta, S, o, B, H, K, V, dtype,
+                             stream=None) -> int:
+    st = load().gdn_decode_step_gathered(_ptr(q_full), _ptr(k_full), _ptr(idx), K_in, _ptr(v),
+                                         _ptr(alpha), _ptr(beta), _ptr(S), _ptr(o), B, H, K, V,
+                                         dtype, _stream(stream))
+    return _check(st, "gdn_decode_step_gathered")
+
+
+def gather_normalize(x, idx, stream=None):
+    """x [..., H, K_in] (bf16/fp32 CUDA); idx [H, K_out] int32 CUDA.  Returns
+    the pruned, renormalised [..., H, K_out]."""
+    import torch
+    H, K_in = x.shape[-2:]
+    K_out = idx.shape[-1]
+    N = x.numel() // (H * K_in)
+    y = torch.empty(x.shape[:-1] + (K_out,), dtype=x.dtype, device=x.device)
+    gdn_gather_normalize(x, idx, y, N, H, K_in, K_out, _dtype_code(x), stream)
+    return y
 
 
 def gdn_get_last_device_status(stream=None) -> int:

@@ -140,6 +140,38 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const float *al
                                         static_cast<cudaStream_t>(stream)));
 }
 
+int gdn_gather_normalize(const void *x, const int *idx, void *y, long long N, int H, int K_in,
+                         int K_out, gdn_dtype dtype, void *stream) {
+    if (N < 0 || H < 1 || (K_out != 32 && K_out != 64) || K_in < K_out || K_in > 1024)
+        return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (N == 0) return GDN_OK;
+    if (!x || !idx || !y) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, idx, y};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
+    if (N > (1LL << 40) / H) return GDN_ERR_INVALID_ARG;
+    return from_cuda(gdn::launch_gather_normalize(x, idx, y, N * H, H, K_in, K_out, dtype, 1e-12f,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_decode_step_gathered(const void *q_full, const void *k_full, const int *idx, int K_in,
+                             const void *v, const float *alpha, const float *beta, float *S,
+                             void *o, int B, int H, int K, int V, gdn_dtype dtype, void *stream) {
+    if (B < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if (K_in < K || K_in > 1024) return GDN_ERR_INVALID_ARG;
+    if ((long long)B * H == 0) return GDN_OK;
+    if (!q_full || !k_full || !idx || !v || !alpha || !beta || !S || !o) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q_full, k_full, idx, v, alpha, beta, S, o};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
+    return from_cuda(gdn::launch_decode_gathered(q_full, k_full, idx, K_in, v, alpha, beta, S, o,
+                                                 B, H, K, V, dtype, 1e-12f,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
                    float *stable_rank, int max_iter, float tol, void *stream) {
     if (BH < 0 || V < 1 || K < 1 || V > 128 || K > 128) return GDN_ERR_INVALID_ARG;

@@ -12,6 +12,11 @@
 //
 // Layout: S [B, H, V, K] float32 (K contiguous, 16-byte aligned rows);
 // q, k [B, H, K]; v, o [B, H, V]; alpha, beta [B, H].
+//
+// The gathering variant reads full-width q, k [B, H, K_in] and keeps channels
+// idx[h, 0..K) of each head, renormalised over the kept coordinates (the
+// pruning prologue of "On State Reduction" notes, Sec. 2.6, fused into the
+// step: no separate pass over q and k).
 // The kernel is HBM-bound: 8 V K bytes of state traffic per head.  Each lane
 // issues all of its row loads before any arithmetic so that every warp keeps
 // kRowsPerLane 16-byte loads in flight.
@@ -44,12 +49,35 @@ __device__ __forceinline__ float group_sum(float x) {
 // K: key width (row length); LPR = K / 4 lanes per row; RPW = 32 / LPR rows
 // per warp per pass.  A CTA covers rows_per_cta = 4 warps * RPW * kRowsPerLane
 // consecutive rows of one head.
-template <int K, typename Tin>
+template <int LPR, typename Tin>
+__device__ __forceinline__ float4 gather4_normalized(const Tin *row, const int *ih, int cl,
+                                                     int Kin, float eps, bool &bad) {
+    const int4 i4 = __ldg(reinterpret_cast<const int4 *>(ih) + cl);
+    const int ci[4] = {i4.x, i4.y, i4.z, i4.w};
+    float g[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int c = ci[e];
+        if ((unsigned)c < (unsigned)Kin) {
+            g[e] = to_f32(row[c]);
+        } else {
+            g[e] = 0.f;
+            bad = true;
+        }
+    }
+    float ss = g[0] * g[0] + g[1] * g[1] + g[2] * g[2] + g[3] * g[3];
+    ss = group_sum<LPR>(ss);
+    const float inv = 1.f / fmaxf(sqrtf(ss), eps);
+    return make_float4(g[0] * inv, g[1] * inv, g[2] * inv, g[3] * inv);
+}
+
+template <int K, typename Tin, bool GATHER>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                        const Tin *__restrict__ v, const float *__restrict__ alpha,
                        const float *__restrict__ beta, float *__restrict__ S,
-                       Tin *__restrict__ o, int V, int blocks_per_head) {
+                       Tin *__restrict__ o, int V, int blocks_per_head, const int *idx, int Kin,
+                       int H, float eps, int *status) {
     constexpr int LPR = K / 4;
     constexpr int RPW = 32 / LPR;
     constexpr int kRowsPerWarp = RPW * kRowsPerLane;
@@ -62,9 +90,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int sub = lane / LPR;  // row within the warp's pass
     const int cl = lane % LPR;   // float4 column index
 
-    const float4 kf = load4(k + (size_t)bh * K + 4 * cl);
-    const float4 qf = load4(q + (size_t)bh * K + 4 * cl);
-    const float kq = group_sum<LPR>(kf.x * qf.x + kf.y * qf.y + kf.z * qf.z + kf.w * qf.w);
+    float4 kf, qf;
+    if constexpr (!GATHER) {
+        kf = load4(k + (size_t)bh * K + 4 * cl);
+        qf = load4(q + (size_t)bh * K + 4 * cl);
+    }
     const float a = alpha[bh];
     const float be = beta[bh];
 
@@ -84,6 +114,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
             vi[r] = 0.f;
         }
     }
+    if constexpr (GATHER) {
+        // The state loads above are already in flight: the index -> channel
+        // load chain and the norm reductions overlap them.
+        bool bad = false;
+        const int *ih = idx + (bh % H) * K;
+        kf = gather4_normalized<LPR>(k + (size_t)bh * Kin, ih, cl, Kin, eps, bad);
+        qf = gather4_normalized<LPR>(q + (size_t)bh * Kin, ih, cl, Kin, eps, bad);
+        if (bad && status && blk == 0) atomicOr(status, kStatusBounds);
+    }
+    const float kq = group_sum<LPR>(kf.x * qf.x + kf.y * qf.y + kf.z * qf.z + kf.w * qf.w);
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r) {
         const int row = row0 + r * RPW;
@@ -108,17 +148,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 }
 
-template <int K, typename Tin>
+template <int K, typename Tin, bool GATHER = false>
 cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const float *alpha,
                             const float *beta, float *S, void *o, int BH, int V,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const int *idx = nullptr, int Kin = K, int H = 1,
+                            float eps = 0.f) {
     constexpr int kRowsPerCta = (kDecodeThreads / 32) * (32 / (K / 4)) * kRowsPerLane;
     const int blocks_per_head = (V + kRowsPerCta - 1) / kRowsPerCta;
     const long long grid = (long long)BH * blocks_per_head;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    decode_step_kernel<K, Tin><<<(unsigned)grid, kDecodeThreads, 0, stream>>>(
+    decode_step_kernel<K, Tin, GATHER><<<(unsigned)grid, kDecodeThreads, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
-        alpha, beta, S, static_cast<Tin *>(o), V, blocks_per_head);
+        alpha, beta, S, static_cast<Tin *>(o), V, blocks_per_head, idx, Kin, H, eps,
+        GATHER ? device_status_ptr() : nullptr);
     return cudaGetLastError();
 }
 
@@ -142,6 +184,28 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
             return cudaErrorInvalidValue;
     }
 #undef GDN_DECODE_CASE
+}
+
+cudaError_t launch_decode_gathered(const void *q, const void *k, const int *idx, int Kin,
+                                   const void *v, const float *alpha, const float *beta,
+                                   float *S, void *o, int B, int H, int K, int V, gdn_dtype dt,
+                                   float eps, cudaStream_t stream) {
+    const int BH = B * H;
+#define GDN_DECODE_G(KK)                                                                       \
+    case KK:                                                                                   \
+        return dt == GDN_BF16                                                                  \
+                   ? launch_decode_t<KK, __nv_bfloat16, true>(q, k, v, alpha, beta, S, o, BH, V, \
+                                                              stream, idx, Kin, H, eps)        \
+                   : launch_decode_t<KK, float, true>(q, k, v, alpha, beta, S, o, BH, V,       \
+                                                      stream, idx, Kin, H, eps);
+    switch (K) {
+        GDN_DECODE_G(32)
+        GDN_DECODE_G(64)
+        GDN_DECODE_G(128)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef GDN_DECODE_G
 }
 
 }  // namespace gdn

@@ -54,6 +54,18 @@ struct SegShape {
 };
 SegShape segment_shape(int BH, int T, int K, int nsm);
 
+// Pruning prologue: gather K_out of K_in channels per head and L2-normalise.
+cudaError_t launch_gather_normalize(const void *x, const int *idx, void *y, long long rows,
+                                    int H, int Kin, int Kout, gdn_dtype dt, float eps,
+                                    cudaStream_t stream);
+
+// Decode step reading full-width q/k and gathering + renormalising the kept
+// channels in the kernel (idx [H, K], K_in the full width).
+cudaError_t launch_decode_gathered(const void *q, const void *k, const int *idx, int Kin,
+                                   const void *v, const float *alpha, const float *beta,
+                                   float *S, void *o, int B, int H, int K, int V, gdn_dtype dt,
+                                   float eps, cudaStream_t stream);
+
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -139,6 +139,40 @@ GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const f
                     gdn_dtype dtype, void *stream);
 
 /*
+ * gdn_gather_normalize -- the pruning prologue: keep d_k' of the d_k
+ * key/query channels of every head and recompute the L2 normalisation on
+ * the kept coordinates ("On State Reduction" notes, Sec. 2.6 and Alg. 1):
+ *
+ *     y[n, h, :] = x[n, h, idx[h, :]] / max(|x[n, h, idx[h, :]]|, 1e-12)
+ *
+ *   x   [N, H, K_in] (dtype), N = B * T rows per head (any scale: a full-width
+ *       normalisation before this call changes nothing)
+ *   idx [H, K_out] int32 channel indices in [0, K_in) (any order)
+ *   y   [N, H, K_out] (dtype), K_out in {32, 64}, K_out <= K_in <= 1024
+ *
+ * An index outside [0, K_in) is not read; it contributes 0 and sets the
+ * GDN_ERR_DEVICE_BOUNDS device status.  Use it to feed gdn_prefill the pruned
+ * q and k from full-width projections.
+ */
+GDN_API int gdn_gather_normalize(const void *x, const int *idx, void *y, long long N, int H,
+                                 int K_in, int K_out, gdn_dtype dtype, void *stream);
+
+/*
+ * gdn_decode_step_gathered -- gdn_decode_step on a channel-pruned state that
+ * reads full-width q and k and applies the pruning prologue inside the step
+ * (same formula as gdn_gather_normalize, no separate pass):
+ *
+ *   q_full, k_full [B, H, K_in] (dtype); idx [H, K] int32; K <= K_in <= 1024
+ *   v [B, H, V]; alpha, beta [B, H]; S [B, H, V, K] updated in place; o [B, H, V]
+ *
+ * (K, V) as for gdn_decode_step.  Bad indices as for gdn_gather_normalize.
+ */
+GDN_API int gdn_decode_step_gathered(const void *q_full, const void *k_full, const int *idx,
+                                     int K_in, const void *v, const float *alpha,
+                                     const float *beta, float *S, void *o, int B, int H, int K,
+                                     int V, gdn_dtype dtype, void *stream);
+
+/*
  * gdn_state_rank -- stable rank of BH states ("On State Reduction" notes,
  * Sec. 2.2, Eq. (5)): er(S) = ||S||_F^2 / ||S||_2^2.
  *

@@ -20,6 +20,12 @@ stable_rank(S)
     power iteration.  For S = 0 the ratio is undefined (the notes define it
     for nonzero states); this oracle returns (0, 0, 0) there.
 
+gather_normalize(x, idx, eps=1e-12)
+    Channel selection with the normalisation recomputed on the kept
+    coordinates ("On State Reduction in Linear Attention" notes, Sec. 2.6 and
+    Alg. 1): y[..., h, :] = P_I x / max(|P_I x|, eps) with P_I the rows
+    idx[h] of the identity.
+
 Parity pins: every function here is checked by ``tests/test_oracle_pins.py``
 against closed forms, worked examples and invariants fixed by the pages.
 """
@@ -128,3 +134,16 @@ def stable_rank(S):
     nz = sigma1 > 0
     er[nz] = fro2[nz] / sigma1[nz] ** 2
     return fro2.reshape(lead), sigma1.reshape(lead), er.reshape(lead)
+
+
+def gather_normalize(x, idx, eps=1e-12):
+    """x: [..., H, K_in]; idx: [H, K_out] integer channel indices.  Returns
+    float64 [..., H, K_out]: the kept channels of each head, divided by their
+    Euclidean norm (or by eps when that norm is smaller)."""
+    x = _as_f64(x)
+    idx = np.asarray(idx)
+    H = x.shape[-2]
+    assert idx.ndim == 2 and idx.shape[0] == H
+    y = np.take_along_axis(x, np.broadcast_to(idx, x.shape[:-2] + idx.shape), axis=-1)
+    n = np.sqrt(np.einsum("...k,...k->...", y, y))
+    return y / np.maximum(n, eps)[..., None]

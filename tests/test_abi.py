@@ -118,3 +118,24 @@ def test_workspace_query(lib):
 def test_selftest_rejects_bad_limit(lib):
     assert lib.gdn_selftest_wait_timeout(0, None) == binding.GDN_ERR_INVALID_ARG
     assert lib.gdn_selftest_wait_timeout(1 << 40, None) == binding.GDN_ERR_INVALID_ARG
+
+
+def test_prologue_rejects_bad_arguments(lib):
+    F = FAKE
+    assert lib.gdn_gather_normalize(F, F, F, 10, 2, 128, 48, 0, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_gather_normalize(F, F, F, 10, 2, 32, 64, 0, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_gather_normalize(F, None, F, 10, 2, 128, 64, 0, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_gather_normalize(F + 4, F, F, 10, 2, 128, 64, 0, None) == binding.GDN_ERR_ALIGNMENT
+    assert lib.gdn_gather_normalize(F, F, F, 0, 2, 128, 64, 0, None) == binding.GDN_OK
+
+    def dec(**kw):
+        a = dict(q=F, k=F, idx=F, kin=128, v=F, al=F, be=F, S=F, o=F, B=1, H=1, K=64, V=128, dt=0)
+        a.update(kw)
+        return lib.gdn_decode_step_gathered(a["q"], a["k"], a["idx"], a["kin"], a["v"], a["al"],
+                                            a["be"], a["S"], a["o"], a["B"], a["H"], a["K"],
+                                            a["V"], a["dt"], None)
+    assert dec(kin=32) == binding.GDN_ERR_INVALID_ARG
+    assert dec(K=48) == binding.GDN_ERR_UNSUPPORTED
+    assert dec(idx=None) == binding.GDN_ERR_INVALID_ARG
+    assert dec(idx=F + 4) == binding.GDN_ERR_ALIGNMENT
+    assert dec(B=0) == binding.GDN_OK

@@ -270,3 +270,36 @@ def test_continuation_equals_one_pass():
     ob, Sb = oracle.recurrence(q[:, 5:], k[:, 5:], v[:, 5:], alpha[:, 5:], beta[:, 5:], S0=Sa)
     np.testing.assert_allclose(np.concatenate([oa, ob], axis=1), o, atol=1e-13, rtol=0)
     np.testing.assert_allclose(Sb, ST, atol=1e-13, rtol=0)
+
+
+# Channel selection with renormalisation ("On State Reduction" notes, Sec. 2.6,
+# Alg. 1): checked against the selection matrix P_I = [e_i1 .. e_id']^T of the
+# notes (a matrix product, not an index gather), unit norm, and direction.
+def test_gather_normalize_matches_selection_matrix():
+    rng = np.random.default_rng(21)
+    H, K, Kp = 3, 16, 6
+    x = rng.standard_normal((5, 4, H, K)) * rng.uniform(0.1, 10.0, size=(5, 4, H, 1))
+    idx = np.stack([rng.permutation(K)[:Kp] for _ in range(H)])  # unsorted on purpose
+    y = oracle.gather_normalize(x, idx)
+    for h in range(H):
+        P = np.zeros((Kp, K))
+        P[np.arange(Kp), idx[h]] = 1.0
+        z = x[..., h, :] @ P.T
+        z = z / np.linalg.norm(z, axis=-1, keepdims=True)
+        np.testing.assert_allclose(y[..., h, :], z, atol=1e-15, rtol=0)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), 1.0, atol=1e-14)
+
+
+def test_gather_normalize_keeps_direction_and_handles_zero():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((7, 2, 8))
+    idx = np.array([[0, 3, 5, 7], [1, 2, 4, 6]])
+    y = oracle.gather_normalize(x, idx)
+    g = np.take_along_axis(x, np.broadcast_to(idx, (7, 2, 4)), axis=-1)
+    cos = (y * g).sum(-1) / np.linalg.norm(g, axis=-1)
+    np.testing.assert_allclose(cos, 1.0, atol=1e-14)
+    # normalisation is scale invariant: a full-width L2 norm first changes nothing
+    xn = x / np.linalg.norm(x, axis=-1, keepdims=True)
+    np.testing.assert_allclose(oracle.gather_normalize(xn, idx), y, atol=1e-14)
+    z = np.zeros((1, 2, 8))
+    assert np.all(oracle.gather_normalize(z, idx) == 0.0)
