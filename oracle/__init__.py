@@ -20,6 +20,11 @@ stable_rank(S)
     power iteration.  For S = 0 the ratio is undefined (the notes define it
     for nonzero states); this oracle returns (0, 0, 0) there.
 
+recurrence_gated(q, k, v, alpha, beta=None, b=None, w=None, S0=None, gate="kda")
+    The channel-gated rules of "Linear Attention Architectures" notes,
+    Sec. 2.5 (KDA: per-key-channel decay on the right of the state, scalar
+    beta) and Sec. 2.6 (GDN2: key-side erase gate b, value-side write gate
+    w), token by token in float64 (C, ``gdn_oracle_gated.c``).
 gather_normalize(x, idx, eps=1e-12)
     Channel selection with the normalisation recomputed on the kept
     coordinates ("On State Reduction in Linear Attention" notes, Sec. 2.6 and
@@ -40,6 +45,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "gdn_oracle_gated.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -48,12 +54,14 @@ MODES = {"gdn": 0, "linear": 1}
 
 
 def build(force: bool = False) -> str:
-    """Compile ``gdn_oracle.c`` into ``liboracle.so`` with gcc (plain -O2,
-    no architecture-specific flags, so it builds the same on x86 and Arm)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    """Compile the oracle's C sources into ``liboracle.so`` with gcc (plain
+    -O2, no architecture-specific flags, so it builds the same on x86 and Arm)."""
+    stale = not os.path.exists(_LIB) or any(
+        os.path.getmtime(_LIB) < os.path.getmtime(src) for src in _SRCS)
+    if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+            ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, *_SRCS, "-lm"]
         )
         os.replace(tmp, _LIB)
     return _LIB
@@ -68,6 +76,8 @@ def _load():
             dp = ctypes.POINTER(ctypes.c_double)
             lib.gdn_oracle_recurrence.argtypes = [dp] * 8 + [ctypes.c_int] * 7
             lib.gdn_oracle_recurrence.restype = ctypes.c_int
+            lib.gdn_oracle_gated.argtypes = [dp] * 10 + [ctypes.c_int] * 7
+            lib.gdn_oracle_gated.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -115,6 +125,45 @@ def recurrence(q, k, v, alpha, beta, S0=None, mode="gdn", threads=None, want_o=T
     )
     if rc != 0:
         raise RuntimeError(f"oracle recurrence failed with code {rc}")
+    return o, ST
+
+
+GATES = {"kda": 1, "gdn2": 2}
+
+
+def recurrence_gated(q, k, v, alpha, beta=None, b=None, w=None, S0=None, gate="kda",
+                     threads=None, want_o=True):
+    """KDA (gate="kda": alpha [B,T,H,K], beta [B,T,H]) or GDN2 (gate="gdn2":
+    alpha [B,T,H,K], b [B,T,H,K], w [B,T,H,V]).  Returns (o, S_T) in float64
+    with the shapes of ``recurrence``."""
+    k = _as_f64(k)
+    B, T, H, K = k.shape
+    v = _as_f64(v)
+    V = v.shape[-1]
+    q = _as_f64(q) if q is not None else None
+    alpha = _as_f64(alpha)
+    assert v.shape == (B, T, H, V) and alpha.shape == (B, T, H, K)
+    betaa = ba = wa = None
+    if gate == "kda":
+        betaa = _as_f64(beta)
+        assert betaa.shape == (B, T, H)
+    else:
+        ba, wa = _as_f64(b), _as_f64(w)
+        assert ba.shape == (B, T, H, K) and wa.shape == (B, T, H, V)
+    S0a = None
+    if S0 is not None:
+        S0a = _as_f64(S0)
+        assert S0a.shape == (B, H, V, K)
+    o = np.empty((B, T, H, V), dtype=np.float64) if (want_o and q is not None) else None
+    ST = np.empty((B, H, V, K), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = _load().gdn_oracle_gated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(betaa), _ptr(ba), _ptr(wa), _ptr(S0a),
+        _ptr(o), _ptr(ST), B, T, H, K, V, GATES[gate], int(threads),
+    )
+    if rc != 0:
+        raise RuntimeError(f"gated oracle failed with code {rc}")
     return o, ST
 
 
