@@ -270,6 +270,10 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         extra["long_context"] = bench_long(args, torch, binding, inputs, peaks, barrier,
                                            max_over_ranks, world)
 
+        # ---- channel-gated rules (KDA, GDN2) on the prefill shapes ----
+        extra["gated"] = bench_gated(args, torch, binding, inputs, peaks, barrier,
+                                     max_over_ranks, world)
+
         # ---- decode: B = 64 and 1, d_k 128 and 64 ----
         extra["decode"] = bench_decode(args, torch, binding, inputs, peaks, props, barrier,
                                        max_over_ranks)
@@ -410,6 +414,26 @@ def bench_decode(args, torch, binding, inputs, peaks, props, barrier, max_over_r
                 res[f"B{B}_dk{K}_unfused"] = {m: graph_time(unfused, S0, n, B, K, 3)
                                               for m, n in modes}
                 del pf, qf, kf
+            if B == 64 and K == 128:
+                for gate in ("kda", "gdn2"):
+                    pg = inputs.make_channel_gated(B=B, T=nsteps, H=H, K=K, V=V, gate=gate)
+                    gq, gk, gv = steps_first(pg.q), steps_first(pg.k), steps_first(pg.v)
+                    ga = steps_first(pg.alpha, False)
+                    gb = None if pg.beta is None else steps_first(pg.beta, False)
+                    gbb = None if pg.b is None else steps_first(pg.b, False)
+                    gw = None if pg.w is None else steps_first(pg.w, False)
+                    code = binding.GATES[gate]
+
+                    def gated(i, S, gq=gq, gk=gk, gv=gv, ga=ga, gb=gb, gbb=gbb, gw=gw,
+                              code=code):
+                        binding.gdn_decode_step_gated(
+                            gq[i], gk[i], gv[i], ga[i], None if gb is None else gb[i],
+                            None if gbb is None else gbb[i], None if gw is None else gw[i], S,
+                            o[i], B, H, K, V, code, binding.GDN_BF16)
+
+                    res[f"B{B}_dk{K}_{gate}"] = {m: graph_time(gated, S0, n, B, K, 1)
+                                                 for m, n in modes}
+                    del pg, gq, gk, gv, ga, gb, gbb, gw
     for B in (64, 1):
         a, b = res[f"B{B}_dk128"], res[f"B{B}_dk64"]
         res[f"B{B}_speedup_dk64"] = {m: a[m]["us_per_step"] / b[m]["us_per_step"] for m in a}
@@ -457,6 +481,48 @@ def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over
             "pipeline_ms_per_step": tl / args.steps,
             "pipeline_tokens_per_s": B * T * world * args.steps / (tl / 1e3),
             "launches": args.steps * 5}
+
+
+def gated_bytes(B, T, H, K, V, gate):
+    """Algorithmic HBM bytes of a gated prefill: bf16 q, k, v, o; float32
+    per-channel alpha; beta (KDA) or b and w (GDN2); S_T."""
+    per = 2 * 2 * K + 2 * 2 * V + 4 * K + (4 if gate == "kda" else 4 * K + 4 * V)
+    return B * T * H * per + 4 * B * H * V * K
+
+
+def bench_gated(args, torch, binding, inputs, peaks, barrier, max_over_ranks, world):
+    """KDA and GDN2 prefill (token-by-token kernel) on the prefill workload's
+    shapes: B=8, T=4096, H=16, d_k=d_v=128, bf16."""
+    out = {}
+    for gate in ("kda", "gdn2"):
+        p = inputs.make_channel_gated(gate=gate)
+        B, T, H, K = p.k.shape
+        V = p.v.shape[-1]
+        dq, dk, dv = to_dev_bf16(p.q, torch), to_dev_bf16(p.k, torch), to_dev_bf16(p.v, torch)
+        f32 = lambda x: None if x is None else torch.from_numpy(x).cuda()  # noqa: E731
+        al, be, bg, wg = f32(p.alpha), f32(p.beta), f32(p.b), f32(p.w)
+        del p
+        o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
+        ST = torch.empty((B, H, V, K), dtype=torch.float32, device="cuda")
+        code = binding.GATES[gate]
+
+        def step():
+            binding.gdn_prefill_gated(dq, dk, dv, al, be, bg, wg, None, o, ST, B, T, H, K, V,
+                                      code, binding.GDN_BF16)
+
+        steps = max(3, min(args.steps, 10))
+        tot, _ = time_calls(step, steps, 3, torch, barrier)
+        tot = max_over_ranks(tot)
+        ms = tot / steps
+        gbs = gated_bytes(B, T, H, K, V, gate) / (ms / 1e3) / 1e9
+        out[gate] = {"ms_per_step": ms, "tokens_per_s": B * T * world / (ms / 1e3),
+                     "achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+                     "launches": steps}
+        del dq, dk, dv, al, be, bg, wg, o, ST
+    out["workload"] = "B=8 T=4096 H=16 d_k=d_v=128 bf16, per-channel decay"
+    out["note"] = ("token-by-token CUDA-core kernel: bound by instruction issue, not HBM; "
+                   "bytes = q, k, v, o, gates, S_T")
+    return out
 
 
 def bench_long(args, torch, binding, inputs, peaks, barrier, max_over_ranks, world):

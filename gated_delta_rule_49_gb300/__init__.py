@@ -17,6 +17,9 @@ from .binding import (  # noqa: F401
     gather_normalize,
     gdn_get_last_device_status,
     gdn_prefill,
+    gdn_prefill_gated,
+    gdn_decode_step_gated,
+    prefill_gated,
     gdn_prefill_workspace_size,
     gdn_selftest_wait_timeout,
     gdn_state_rank,

@@ -28,6 +28,11 @@ GDN_WARN_ZERO_STATE = 1
 GDN_BF16 = 0
 GDN_FP32 = 1
 
+GDN_GATE_SCALAR = 0
+GDN_GATE_KDA = 1
+GDN_GATE_GDN2 = 2
+GATES = {"gdn": GDN_GATE_SCALAR, "kda": GDN_GATE_KDA, "gdn2": GDN_GATE_GDN2}
+
 EXPORTS = (
     "gdn_prefill",
     "gdn_prefill_workspace_size",
@@ -41,6 +46,8 @@ EXPORTS = (
     "gdn_prefill_noalloc_max_workspace",
     "gdn_gather_normalize",
     "gdn_decode_step_gathered",
+    "gdn_prefill_gated",
+    "gdn_decode_step_gated",
 )
 
 _lock = threading.Lock()
@@ -87,6 +94,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_gather_normalize.restype = i
         lib.gdn_decode_step_gathered.argtypes = [vp, vp, vp, i] + [vp] * 5 + [i] * 5 + [vp]
         lib.gdn_decode_step_gathered.restype = i
+        lib.gdn_prefill_gated.argtypes = [vp] * 10 + [i] * 7 + [vp]
+        lib.gdn_prefill_gated.restype = i
+        lib.gdn_decode_step_gated.argtypes = [vp] * 9 + [i] * 6 + [vp]
+        lib.gdn_decode_step_gated.restype = i
         lib.gdn_prefill_noalloc_max_workspace.argtypes = []
         lib.gdn_prefill_noalloc_max_workspace.restype = sz
         _lib = lib
@@ -182,6 +193,37 @@ def gdn_decode_step_gathered(q_full, k_full, idx, K_in, v, alpha, beta, S, o, B,
                                          _ptr(alpha), _ptr(beta), _ptr(S), _ptr(o), B, H, K, V,
                                          dtype, _stream(stream))
     return _check(st, "gdn_decode_step_gathered")
+
+
+def gdn_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, H, K, V, gate, dtype,
+                      stream=None) -> int:
+    st = load().gdn_prefill_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(b),
+                                  _ptr(w), _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, K, V, gate,
+                                  dtype, _stream(stream))
+    return _check(st, "gdn_prefill_gated")
+
+
+def gdn_decode_step_gated(q, k, v, alpha, beta, b, w, S, o, B, H, K, V, gate, dtype,
+                          stream=None) -> int:
+    st = load().gdn_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                      _ptr(b), _ptr(w), _ptr(S), _ptr(o), B, H, K, V, gate, dtype,
+                                      _stream(stream))
+    return _check(st, "gdn_decode_step_gated")
+
+
+def prefill_gated(q, k, v, alpha, beta=None, b=None, w=None, S0=None, gate="kda",
+                  want_o=True, want_state=True, stream=None):
+    """gdn_prefill_gated on torch CUDA tensors: q, k [B,T,H,K]; v [B,T,H,V];
+    alpha [B,T,H] (gate "gdn") or [B,T,H,K]; beta [B,T,H] ("gdn", "kda");
+    b [B,T,H,K], w [B,T,H,V] ("gdn2").  Returns (o, S_T)."""
+    import torch
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = torch.empty((B, T, H, V), dtype=v.dtype, device=v.device) if want_o else None
+    ST = torch.empty((B, H, V, K), dtype=torch.float32, device=v.device) if want_state else None
+    gdn_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, ST, B, T, H, K, V, GATES[gate],
+                      _dtype_code(v), stream)
+    return o, ST
 
 
 def gather_normalize(x, idx, stream=None):

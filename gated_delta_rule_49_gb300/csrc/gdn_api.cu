@@ -92,6 +92,27 @@ size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype d
     return gdn::segment_shape(B * H, T, K, gdn::sm_count()).workspace_bytes;
 }
 
+namespace {
+// T = 0: the final state is the start state (or zero).
+int empty_prefill(const float *S0, float *S_T, int B, int H, int K, int V, cudaStream_t st) {
+    if (!S_T) return GDN_OK;
+    const size_t bytes = sizeof(float) * (size_t)B * H * V * K;
+    cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
+                                    : cudaMemcpyAsync(S_T, S0, bytes, cudaMemcpyDeviceToDevice, st))
+                       : cudaMemsetAsync(S_T, 0, bytes, st);
+    return from_cuda(e);
+}
+
+// Which gate arrays a gate needs (non-NULL) and forbids (NULL).
+bool gates_match(gdn_gate gate, const float *beta, const float *b, const float *w) {
+    if (gate == GDN_GATE_GDN2) return !beta && b && w;
+    return beta && !b && !w;
+}
+bool valid_gate(int gate) {
+    return gate == GDN_GATE_SCALAR || gate == GDN_GATE_KDA || gate == GDN_GATE_GDN2;
+}
+}  // namespace
+
 int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
                 const float *beta, const float *S0, void *o, float *S_T, int B, int T, int H,
                 int K, int V, gdn_dtype dtype, void *workspace, size_t workspace_bytes,
@@ -108,14 +129,7 @@ int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
     if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
     if ((long long)B * H == 0) return GDN_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (T == 0) {
-        if (!S_T) return GDN_OK;
-        const size_t bytes = sizeof(float) * (size_t)B * H * V * K;
-        cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
-                                        : cudaMemcpyAsync(S_T, S0, bytes, cudaMemcpyDeviceToDevice, st))
-                           : cudaMemsetAsync(S_T, 0, bytes, st);
-        return from_cuda(e);
-    }
+    if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
     // bf16 at V = 128 runs on the tensor cores; float32 mode and the small
     // (32, 32) variant run the CUDA-core chunked kernel.
     if (dtype == GDN_BF16 && V == 128 && (K == 128 || K == 64))
@@ -170,6 +184,46 @@ int gdn_decode_step_gathered(const void *q_full, const void *k_full, const int *
     return from_cuda(gdn::launch_decode_gathered(q_full, k_full, idx, K_in, v, alpha, beta, S, o,
                                                  B, H, K, V, dtype, 1e-12f,
                                                  static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_prefill_gated(const void *q, const void *k, const void *v, const float *alpha,
+                      const float *beta, const float *b, const float *w, const float *S0,
+                      void *o, float *S_T, int B, int T, int H, int K, int V, gdn_gate gate,
+                      gdn_dtype dtype, void *stream) {
+    if (B < 0 || T < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!valid_gate(gate)) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if (!o && !S_T) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !gates_match(gate, beta, b, w)))
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, alpha, beta, b, w, S0, o, S_T};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    if ((long long)B * H == 0) return GDN_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
+    return from_cuda(gdn::launch_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, H,
+                                               K, V, gate, dtype, st));
+}
+
+int gdn_decode_step_gated(const void *q, const void *k, const void *v, const float *alpha,
+                          const float *beta, const float *b, const float *w, float *S, void *o,
+                          int B, int H, int K, int V, gdn_gate gate, gdn_dtype dtype,
+                          void *stream) {
+    if (B < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!valid_gate(gate)) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0) return GDN_OK;
+    if (!q || !k || !v || !alpha || !S || !o || !gates_match(gate, beta, b, w))
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, alpha, beta, b, w, S, o};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    if ((long long)B * H > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    return from_cuda(gdn::launch_decode_gated(q, k, v, alpha, beta, b, w, S, o, B, H, K, V, gate,
+                                              dtype, static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,

@@ -1,0 +1,448 @@
+// Channel-gated delta rules ("Linear Attention Architectures" notes,
+// Secs. 2.4-2.6), token by token on the CUDA cores:
+//
+//   SCALAR (GDN):  S <- a S;              u = beta (v - S k)
+//   KDA:           S <- S diag(alpha);    u = beta (v - S k)
+//   GDN2:          S <- S diag(alpha);    u = w (.) v - S (b (.) k)
+//   then           S <- S + u k^T,        o = S q
+//
+// Each value row of S is an independent system (the gates act on the key
+// channels or per value row), so the state is split by rows across CTAs and
+// lanes and nothing is exchanged between rows.
+//
+// Prefill: a CTA owns R rows of one (b, h) sequence; a row is spread over
+// K/8 lanes holding 8 channels each in registers.  The per-token operands
+// (k, q, the channel gates, and the CTA's slice of v / w) are staged 16
+// tokens at a time into a two-stage shared-memory ring by cp.async, so the
+// loads of block n+1 are in flight while block n is processed.  Per token and
+// row: decay, one dot product (the erase read) reduced across the row's
+// lanes, the rank-one write, then o = S q (a second reduction, off the
+// recurrence's critical path); outputs are collected per block in shared
+// memory and written with 16-byte stores.  Bound: CUDA-core issue (about 25
+// warp instructions per row-token); see the measurement notes.
+//
+// Decode: the layout of the plain decode step (K/4 lanes per row, four rows
+// per lane, all state loads issued first); HBM-bound on the state.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+enum GateMode : int { kScalar = GDN_GATE_SCALAR, kKda = GDN_GATE_KDA, kGdn2 = GDN_GATE_GDN2 };
+
+constexpr int kTB = 16;  // tokens per staged block
+constexpr int kE = 8;    // state channels per lane (prefill)
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all_but_one() {
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+}
+
+// Eight consecutive values (shared or global memory, 16-byte aligned) as float.
+__device__ __forceinline__ void ld8(const float *p, float *x) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float *x) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+template <int L>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int off = L / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Shared-memory layout of one stage (byte offsets, all multiples of 16).
+template <int K, int R, typename Tin, int GATE>
+struct GatedStage {
+    static constexpr int KA = GATE == kScalar ? 4 : K;  // floats of alpha per token
+    static constexpr int KQ = 0;                                           // [kTB][2][K] Tin
+    static constexpr int AL = KQ + kTB * 2 * K * (int)sizeof(Tin);          // [kTB][KA] f32
+    static constexpr int BG = AL + kTB * KA * 4;                            // [kTB][K] f32
+    static constexpr int BE = BG + (GATE == kGdn2 ? kTB * K * 4 : 0);       // [kTB] f32
+    static constexpr int VV = BE + kTB * 4;                                 // [kTB][R] Tin
+    static constexpr int WW = VV + kTB * R * (int)sizeof(Tin);              // [kTB][R] f32
+    static constexpr int BYTES = WW + (GATE == kGdn2 ? kTB * R * 4 : 0);
+    static constexpr int OB = 2 * BYTES;                                    // [kTB][R] Tin
+    static constexpr int SMEM = OB + kTB * R * (int)sizeof(Tin);
+    static_assert(AL % 16 == 0 && BG % 16 == 0 && VV % 16 == 0 && WW % 16 == 0 &&
+                      BYTES % 16 == 0,
+                  "16-byte aligned regions");
+};
+
+// Issue the cp.async copies of tokens [t0, t0 + n) of sequence (b, h) for
+// rows [r0, r0 + R) into one stage.
+template <int K, int R, typename Tin, int GATE>
+__device__ __forceinline__ void stage_block(unsigned char *st, const Tin *q, const Tin *k,
+                                            const Tin *v, const float *alpha,
+                                            const float *beta, const float *bg,
+                                            const float *wg, size_t th0, int H, int V, int r0,
+                                            int n) {
+    using L = GatedStage<K, R, Tin, GATE>;
+    constexpr int EPC = 16 / (int)sizeof(Tin);  // elements per 16-byte chunk
+    constexpr int nK = K / EPC;                 // chunks of one k (or q) row
+    constexpr int nA = GATE == kScalar ? 0 : K / 4;
+    constexpr int nB = GATE == kGdn2 ? K / 4 : 0;
+    constexpr int nV = R / EPC;
+    constexpr int nW = GATE == kGdn2 ? R / 4 : 0;
+    constexpr int nTok = 2 * nK + nA + nB + nV + nW;
+    for (int j = threadIdx.x; j < n * nTok; j += blockDim.x) {
+        const int tau = j / nTok;
+        int c = j - tau * nTok;
+        const size_t th = th0 + (size_t)tau * H;  // token-head index of token t0 + tau
+        if (c < 2 * nK) {
+            const int which = c / nK;  // 0: k, 1: q
+            c -= which * nK;
+            const Tin *src = (which ? q : k) + th * K + c * EPC;
+            cp_async16(st + L::KQ + ((tau * 2 + which) * K + c * EPC) * (int)sizeof(Tin), src);
+            continue;
+        }
+        c -= 2 * nK;
+        if (c < nA) {
+            cp_async16(st + L::AL + (tau * K + c * 4) * 4, alpha + th * K + c * 4);
+            continue;
+        }
+        c -= nA;
+        if (c < nB) {
+            cp_async16(st + L::BG + (tau * K + c * 4) * 4, bg + th * K + c * 4);
+            continue;
+        }
+        c -= nB;
+        if (c < nV) {
+            cp_async16(st + L::VV + (tau * R + c * EPC) * (int)sizeof(Tin),
+                       v + th * V + r0 + c * EPC);
+            continue;
+        }
+        c -= nV;
+        cp_async16(st + L::WW + (tau * R + c * 4) * 4, wg + th * V + r0 + c * 4);
+    }
+    for (int tau = threadIdx.x; tau < n; tau += blockDim.x) {
+        const size_t th = th0 + (size_t)tau * H;
+        if (GATE == kScalar) cp_async4(st + L::AL + tau * L::KA * 4, alpha + th);
+        if (GATE != kGdn2) cp_async4(st + L::BE + tau * 4, beta + th);
+    }
+}
+
+// grid: B*H*(V/R) CTAs of (R / RPI) warps; CTA x -> sequence x / (V/R), slab x % (V/R).
+template <int K, int R, typename Tin, int GATE>
+__global__ void __launch_bounds__(256)
+    prefill_gated_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                         const Tin *__restrict__ v, const float *__restrict__ alpha,
+                         const float *__restrict__ beta, const float *__restrict__ bg,
+                         const float *__restrict__ wg, const float *__restrict__ S0,
+                         Tin *__restrict__ o, float *__restrict__ ST, int T, int H, int V) {
+    using L = GatedStage<K, R, Tin, GATE>;
+    constexpr int LPR = K / kE;  // lanes per row
+    constexpr int RPI = 32 / LPR;
+    constexpr int EPC = 16 / (int)sizeof(Tin);
+    extern __shared__ __align__(16) unsigned char smem[];
+
+    const int slabs = V / R;
+    const int seq = blockIdx.x / slabs;
+    const int r0 = (blockIdx.x % slabs) * R;
+    const int b = seq / H, h = seq % H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane / LPR, cl = lane % LPR;
+    const int row = warp * RPI + g;  // within the slab
+    const size_t srow = ((size_t)seq * V + r0 + row) * K + cl * kE;
+
+    float s[kE];
+    if (S0) {
+        ld8(S0 + srow, s);
+    } else {
+#pragma unroll
+        for (int e = 0; e < kE; ++e) s[e] = 0.f;
+    }
+
+    const int nblk = (T + kTB - 1) / kTB;
+    auto th_of = [&](int t) { return ((size_t)b * T + t) * H + h; };
+    if (nblk > 0)
+        stage_block<K, R, Tin, GATE>(smem, q, k, v, alpha, beta, bg, wg, th_of(0), H, V, r0,
+                                     min(kTB, T));
+    cp_async_commit();
+    Tin *ob = reinterpret_cast<Tin *>(smem + L::OB);
+    for (int n = 0; n < nblk; ++n) {
+        const int t0 = n * kTB;
+        if (n + 1 < nblk)
+            stage_block<K, R, Tin, GATE>(smem + ((n + 1) & 1) * L::BYTES, q, k, v, alpha, beta,
+                                         bg, wg, th_of(t0 + kTB), H, V, r0,
+                                         min(kTB, T - t0 - kTB));
+        cp_async_commit();
+        cp_async_wait_all_but_one();
+        __syncthreads();
+        const unsigned char *st = smem + (n & 1) * L::BYTES;
+        const Tin *kq = reinterpret_cast<const Tin *>(st + L::KQ);
+        const float *al = reinterpret_cast<const float *>(st + L::AL);
+        const float *bgs = reinterpret_cast<const float *>(st + L::BG);
+        const float *bes = reinterpret_cast<const float *>(st + L::BE);
+        const Tin *vv = reinterpret_cast<const Tin *>(st + L::VV);
+        const float *ww = reinterpret_cast<const float *>(st + L::WW);
+        const int nt = min(kTB, T - t0);
+        for (int tau = 0; tau < nt; ++tau) {
+            float kk[kE], qq[kE], ee[kE];
+            ld8(kq + (tau * 2) * K + cl * kE, kk);
+            ld8(kq + (tau * 2 + 1) * K + cl * kE, qq);
+            if constexpr (GATE == kScalar) {
+                const float a = al[tau * L::KA];
+#pragma unroll
+                for (int e = 0; e < kE; ++e) s[e] *= a;
+            } else {
+                float aa[kE];
+                ld8(al + tau * K + cl * kE, aa);
+#pragma unroll
+                for (int e = 0; e < kE; ++e) s[e] *= aa[e];
+            }
+            if constexpr (GATE == kGdn2) {
+                ld8(bgs + tau * K + cl * kE, ee);
+#pragma unroll
+                for (int e = 0; e < kE; ++e) ee[e] *= kk[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < kE; ++e) ee[e] = kk[e];
+            }
+            float p = 0.f;
+#pragma unroll
+            for (int e = 0; e < kE; ++e) p = fmaf(s[e], ee[e], p);
+            p = group_sum<LPR>(p);
+            const float vi = to_f32(vv[tau * R + row]);
+            float u;
+            if constexpr (GATE == kGdn2)
+                u = ww[tau * R + row] * vi - p;
+            else
+                u = bes[tau] * (vi - p);
+            float r = 0.f;
+#pragma unroll
+            for (int e = 0; e < kE; ++e) {
+                s[e] = fmaf(u, kk[e], s[e]);
+                r = fmaf(s[e], qq[e], r);
+            }
+            r = group_sum<LPR>(r);
+            if (cl == 0) ob[tau * R + row] = from_f32<Tin>(r);
+        }
+        __syncthreads();  // outputs complete; stage n & 1 free for block n + 2
+        if (o) {
+            constexpr int nO = R / EPC;
+            for (int j = threadIdx.x; j < nt * nO; j += blockDim.x) {
+                const int tau = j / nO, c = j % nO;
+                *reinterpret_cast<uint4 *>(o + th_of(t0 + tau) * V + r0 + c * EPC) =
+                    *reinterpret_cast<const uint4 *>(ob + tau * R + c * EPC);
+            }
+        }
+    }
+    if (ST) {
+        float4 *dst = reinterpret_cast<float4 *>(ST + srow);
+        dst[0] = make_float4(s[0], s[1], s[2], s[3]);
+        dst[1] = make_float4(s[4], s[5], s[6], s[7]);
+    }
+}
+
+template <int K, int R, typename Tin, int GATE>
+cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *alpha,
+                      const float *beta, const float *bg, const float *wg, const float *S0,
+                      void *o, float *ST, int B, int T, int H, int V, cudaStream_t stream) {
+    using L = GatedStage<K, R, Tin, GATE>;
+    constexpr int RPI = 32 / (K / kE);
+    constexpr int threads = (R / RPI) * 32;
+    static_assert(threads <= 256, "at most 8 warps");
+    auto kern = prefill_gated_kernel<K, R, Tin, GATE>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (L::SMEM > 48 * 1024 && !attr_set[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const long long grid = (long long)B * H * (V / R);
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, threads, L::SMEM, stream>>>(
+        static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
+        alpha, beta, bg, wg, S0, static_cast<Tin *>(o), ST, T, H, V);
+    return cudaGetLastError();
+}
+
+template <typename Tin, int GATE>
+cudaError_t pg_dispatch(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *beta, const float *bg, const float *wg, const float *S0,
+                        void *o, float *ST, int B, int T, int H, int K, int V,
+                        cudaStream_t stream) {
+    if (K == 128 && V == 128)
+        return launch_pg<128, 16, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, V,
+                                             stream);
+    if (K == 64 && V == 128)
+        return launch_pg<64, 32, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, V,
+                                            stream);
+    if (K == 32 && V == 32)
+        return launch_pg<32, 32, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, V,
+                                            stream);
+    return cudaErrorInvalidValue;
+}
+
+// ---- decode -----------------------------------------------------------------
+
+constexpr int kDecThreads = 128;
+constexpr int kDecRowsPerLane = 4;
+
+__device__ __forceinline__ float4 ld4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+    const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+
+template <int K, typename Tin, int GATE>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_gated_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                        const Tin *__restrict__ v, const float *__restrict__ alpha,
+                        const float *__restrict__ beta, const float *__restrict__ bg,
+                        const float *__restrict__ wg, float *__restrict__ S,
+                        Tin *__restrict__ o, int V, int blocks_per_head) {
+    constexpr int LPR = K / 4;
+    constexpr int RPW = 32 / LPR;
+    constexpr int kRowsPerWarp = RPW * kDecRowsPerLane;
+    constexpr int kRowsPerCta = (kDecThreads / 32) * kRowsPerWarp;
+    const int bh = blockIdx.x / blocks_per_head;
+    const int blk = blockIdx.x % blocks_per_head;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LPR, cl = lane % LPR;
+    const int row0 = blk * kRowsPerCta + warp * kRowsPerWarp + sub;
+    float *Sh = S + (size_t)bh * V * K;
+
+    float4 s[kDecRowsPerLane];
+    float vi[kDecRowsPerLane], wi[kDecRowsPerLane];
+#pragma unroll
+    for (int r = 0; r < kDecRowsPerLane; ++r) {
+        const int row = row0 + r * RPW;
+        const bool ok = row < V;
+        s[r] = ok ? ld4(Sh + (size_t)row * K + 4 * cl) : make_float4(0.f, 0.f, 0.f, 0.f);
+        vi[r] = ok ? to_f32(v[(size_t)bh * V + row]) : 0.f;
+        wi[r] = (GATE == kGdn2 && ok) ? wg[(size_t)bh * V + row] : 0.f;
+    }
+    const float4 kf = ld4(k + (size_t)bh * K + 4 * cl);
+    const float4 qf = ld4(q + (size_t)bh * K + 4 * cl);
+    float4 af;
+    if constexpr (GATE == kScalar) {
+        const float a = alpha[bh];
+        af = make_float4(a, a, a, a);
+    } else {
+        af = ld4(alpha + (size_t)bh * K + 4 * cl);
+    }
+    float4 ef = kf;
+    if constexpr (GATE == kGdn2) {
+        const float4 bb = ld4(bg + (size_t)bh * K + 4 * cl);
+        ef = make_float4(bb.x * kf.x, bb.y * kf.y, bb.z * kf.z, bb.w * kf.w);
+    }
+    const float be = GATE == kGdn2 ? 0.f : beta[bh];
+    const float kq = group_sum<LPR>(dot4(kf, qf));
+#pragma unroll
+    for (int r = 0; r < kDecRowsPerLane; ++r) {
+        const int row = row0 + r * RPW;
+        float4 x = s[r];
+        x.x *= af.x; x.y *= af.y; x.z *= af.z; x.w *= af.w;
+        float p = dot4(x, ef);
+        float rq = dot4(x, qf);
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) {
+            p += __shfl_xor_sync(0xffffffffu, p, off);
+            rq += __shfl_xor_sync(0xffffffffu, rq, off);
+        }
+        const float u = GATE == kGdn2 ? wi[r] * vi[r] - p : be * (vi[r] - p);
+        x.x = fmaf(u, kf.x, x.x);
+        x.y = fmaf(u, kf.y, x.y);
+        x.z = fmaf(u, kf.z, x.z);
+        x.w = fmaf(u, kf.w, x.w);
+        if (row < V) {
+            *reinterpret_cast<float4 *>(Sh + (size_t)row * K + 4 * cl) = x;
+            if (cl == 0) o[(size_t)bh * V + row] = from_f32<Tin>(fmaf(u, kq, rq));
+        }
+    }
+}
+
+template <int K, typename Tin, int GATE>
+cudaError_t launch_dg(const void *q, const void *k, const void *v, const float *alpha,
+                      const float *beta, const float *bg, const float *wg, float *S, void *o,
+                      int BH, int V, cudaStream_t stream) {
+    constexpr int kRowsPerCta = (kDecThreads / 32) * (32 / (K / 4)) * kDecRowsPerLane;
+    const int bph = (V + kRowsPerCta - 1) / kRowsPerCta;
+    const long long grid = (long long)BH * bph;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    decode_gated_kernel<K, Tin, GATE><<<(unsigned)grid, kDecThreads, 0, stream>>>(
+        static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
+        alpha, beta, bg, wg, S, static_cast<Tin *>(o), V, bph);
+    return cudaGetLastError();
+}
+
+template <typename Tin, int GATE>
+cudaError_t dg_dispatch(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *beta, const float *bg, const float *wg, float *S, void *o,
+                        int BH, int K, int V, cudaStream_t stream) {
+    if (K == 128) return launch_dg<128, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S, o, BH, V, stream);
+    if (K == 64) return launch_dg<64, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S, o, BH, V, stream);
+    if (K == 32) return launch_dg<32, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S, o, BH, V, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_gated(const void *q, const void *k, const void *v,
+                                 const float *alpha, const float *beta, const float *bg,
+                                 const float *wg, const float *S0, void *o, float *ST, int B,
+                                 int T, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
+                                 cudaStream_t stream) {
+#define GDN_PG(TIN, G) \
+    pg_dispatch<TIN, G>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, K, V, stream)
+    const bool bf = dt == GDN_BF16;
+    switch (gate) {
+        case GDN_GATE_SCALAR: return bf ? GDN_PG(__nv_bfloat16, kScalar) : GDN_PG(float, kScalar);
+        case GDN_GATE_KDA: return bf ? GDN_PG(__nv_bfloat16, kKda) : GDN_PG(float, kKda);
+        case GDN_GATE_GDN2: return bf ? GDN_PG(__nv_bfloat16, kGdn2) : GDN_PG(float, kGdn2);
+    }
+#undef GDN_PG
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, const float *alpha,
+                                const float *beta, const float *bg, const float *wg, float *S,
+                                void *o, int B, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
+                                cudaStream_t stream) {
+    const int BH = B * H;
+#define GDN_DG(TIN, G) dg_dispatch<TIN, G>(q, k, v, alpha, beta, bg, wg, S, o, BH, K, V, stream)
+    const bool bf = dt == GDN_BF16;
+    switch (gate) {
+        case GDN_GATE_SCALAR: return bf ? GDN_DG(__nv_bfloat16, kScalar) : GDN_DG(float, kScalar);
+        case GDN_GATE_KDA: return bf ? GDN_DG(__nv_bfloat16, kKda) : GDN_DG(float, kKda);
+        case GDN_GATE_GDN2: return bf ? GDN_DG(__nv_bfloat16, kGdn2) : GDN_DG(float, kGdn2);
+    }
+#undef GDN_DG
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

@@ -66,6 +66,17 @@ cudaError_t launch_decode_gathered(const void *q, const void *k, const int *idx,
                                    float *S, void *o, int B, int H, int K, int V, gdn_dtype dt,
                                    float eps, cudaStream_t stream);
 
+// Channel-gated rules (GDN / KDA / GDN2), token by token on the CUDA cores.
+cudaError_t launch_prefill_gated(const void *q, const void *k, const void *v,
+                                 const float *alpha, const float *beta, const float *bg,
+                                 const float *wg, const float *S0, void *o, float *ST, int B,
+                                 int T, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
+                                 cudaStream_t stream);
+cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, const float *alpha,
+                                const float *beta, const float *bg, const float *wg, float *S,
+                                void *o, int B, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
+                                cudaStream_t stream);
+
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

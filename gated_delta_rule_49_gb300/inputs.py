@@ -18,9 +18,12 @@ input-dependent decay):
               steps from a low-stable-rank initial state
   long        B=1,  H=16, T=65536, K=V=128, bf16, alpha in [0.9995, 0.9999],
               keys in a narrow cone (|mean k| ~ 0.9 per head)
+  gated       the prefill shapes under the channel-gated rules (KDA, GDN2):
+              per-key-channel decay, and for GDN2 per-channel erase / write
+              gates
 
 Random streams: numpy PCG64.  The tiny workload uses seed ``seed`` directly;
-the others use child ``i`` of ``SeedSequence(seed).spawn(5)`` (prefill and
+the others use child ``i`` of ``SeedSequence(seed)`` (prefill and
 pruned share child 1, so the pruned run sees the same Gaussian draws).  Draw
 order inside a stream: q, k, v, beta logits, alpha logits, pruning subsets,
 initial state.
@@ -31,7 +34,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-WORKLOADS = ("tiny", "prefill", "pruned", "decode", "long")
+WORKLOADS = ("tiny", "prefill", "pruned", "decode", "long", "gated")
 
 
 def round_to_bf16(x) -> np.ndarray:
@@ -77,7 +80,8 @@ def _sigmoid(x):
 def _stream(seed: int, index: int) -> np.random.Generator:
     if index == 0:
         return np.random.default_rng(seed)
-    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(5)[index]))
+    children = np.random.SeedSequence(seed).spawn(max(5, index + 1))
+    return np.random.Generator(np.random.PCG64(children[index]))
 
 
 @dataclass
@@ -212,6 +216,64 @@ def make_long(seed=0, B=1, T=65536, H=16, K=128, V=128, dtype="bf16") -> Problem
     return Problem("long", dtype, _round(q, dtype), _round(k, dtype), _round(v, dtype),
                    alpha.astype(np.float32), beta.astype(np.float32), None,
                    {"seed": seed, "cone_offset": CONE_OFFSET})
+
+
+@dataclass
+class GatedProblem:
+    """Inputs of the channel-gated rules: q/k [B,T,H,K], v [B,T,H,V], alpha
+    [B,T,H,K]; beta [B,T,H] for KDA, b [B,T,H,K] and w [B,T,H,V] for GDN2
+    (the unused ones are None); S0 [B,H,V,K] or None."""
+
+    gate: str
+    dtype: str
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    alpha: np.ndarray
+    beta: np.ndarray | None
+    b: np.ndarray | None
+    w: np.ndarray | None
+    S0: np.ndarray | None
+    meta: dict = field(default_factory=dict)
+
+
+def make_channel_gated(seed=0, B=8, T=4096, H=16, K=128, V=128, dtype="bf16", gate="kda",
+                       with_S0=False) -> GatedProblem:
+    """q, k, v and beta drawn as the prefill workload; the decay per key
+    channel, log alpha[t, h, c] = -softplus(x), x ~ N(m_{h,c}, 0.5^2) around
+    a per-(head, channel) centre m_{h,c} ~ N(-4, 1.5^2) (the per-head centres
+    of the prefill workload, one per channel); for GDN2 the erase gate
+    b = sigmoid(N(0,1)) per key channel and the write gate w = sigmoid(N(0,1))
+    per value channel, per token."""
+    rng = _stream(seed, 5)
+    zq, zk, v, beta, _ = _gated_draws(rng, B, T, H, K, V)
+    m = rng.normal(-4.0, 1.5, size=(H, K))
+    x = rng.normal(m[None, None], 0.5, size=(B, T, H, K))
+    alpha = np.exp(-_softplus(x)).astype(np.float32)
+    bg = wg = None
+    if gate == "gdn2":
+        bg = _sigmoid(rng.standard_normal((B, T, H, K))).astype(np.float32)
+        wg = _sigmoid(rng.standard_normal((B, T, H, V))).astype(np.float32)
+        beta = None
+    elif gate != "kda":
+        raise ValueError(gate)
+    S0 = (0.1 * rng.standard_normal((B, H, V, K))).astype(np.float32) if with_S0 else None
+    return GatedProblem(gate, dtype, _round(_unit_rows(zq), dtype), _round(_unit_rows(zk), dtype),
+                        _round(v, dtype), alpha,
+                        None if beta is None else beta.astype(np.float32), bg, wg, S0,
+                        {"seed": seed})
+
+
+def take_gated_sequences(p: GatedProblem, b_idx, h_idx) -> GatedProblem:
+    """Sub-problem of sequences (b, h), b in b_idx, h in h_idx."""
+    sl = np.ix_(np.asarray(b_idx), np.arange(p.k.shape[1]), np.asarray(h_idx))
+
+    def g(x):
+        return None if x is None else np.ascontiguousarray(x[sl])
+
+    S0 = None if p.S0 is None else np.ascontiguousarray(p.S0[np.ix_(b_idx, h_idx)])
+    return GatedProblem(p.gate, p.dtype, g(p.q), g(p.k), g(p.v), g(p.alpha), g(p.beta), g(p.b),
+                        g(p.w), S0, dict(p.meta))
 
 
 def take_sequences(p: Problem, b_idx, h_idx) -> Problem:

@@ -173,6 +173,55 @@ GDN_API int gdn_decode_step_gathered(const void *q_full, const void *k_full, con
                                      int V, gdn_dtype dtype, void *stream);
 
 /*
+ * Gates of the channel-gated delta rules ("Linear Attention Architectures"
+ * reading notes, Secs. 2.4-2.6).  Per token and head, S in R^{V x K}:
+ *
+ *   GDN_GATE_SCALAR  Gated DeltaNet: S <- a S; u = beta (v - S k)
+ *                    alpha, beta [.., H]
+ *   GDN_GATE_KDA     Kimi Delta Attention: the decay acts per key channel, on
+ *                    the right of the state: S <- S diag(alpha); u = beta (v - S k)
+ *                    alpha [.., H, K], beta [.., H]
+ *   GDN_GATE_GDN2    Gated DeltaNet-2: separate erase (key side) and write
+ *                    (value side) gates: S <- S diag(alpha); u = w (.) v - S (b (.) k)
+ *                    alpha, b [.., H, K], w [.., H, V]
+ *
+ * then, for all three, S <- S + u k^T and o = S q (the write keeps the
+ * original key on its right).  alpha = a 1 turns KDA into GDN; b = w = beta 1
+ * turns GDN2 into KDA.
+ */
+typedef enum { GDN_GATE_SCALAR = 0, GDN_GATE_KDA = 1, GDN_GATE_GDN2 = 2 } gdn_gate;
+
+/*
+ * gdn_prefill_gated -- the recurrence over T tokens under any of the gates
+ * above, token by token on the CUDA cores (value rows split across CTAs).
+ *
+ *   q, k [B, T, H, K], v [B, T, H, V] (dtype);  o [B, T, H, V] (dtype)
+ *   alpha [B, T, H] (SCALAR) or [B, T, H, K] (KDA, GDN2), float32
+ *   beta [B, T, H] float32 (SCALAR, KDA; must be NULL for GDN2)
+ *   b [B, T, H, K], w [B, T, H, V] float32 (GDN2; must be NULL otherwise)
+ *   S0 [B, H, V, K] float32 or NULL (zero state);  S_T [B, H, V, K] float32
+ *
+ * (K, V) as for gdn_prefill; any T >= 0 (T = 0 copies S0, or zeros, into
+ * S_T).  o or S_T may be NULL (not both); S_T may alias S0.  Needs no
+ * workspace.  Host validation as for gdn_prefill.
+ */
+GDN_API int gdn_prefill_gated(const void *q, const void *k, const void *v, const float *alpha,
+                              const float *beta, const float *b, const float *w,
+                              const float *S0, void *o, float *S_T, int B, int T, int H, int K,
+                              int V, gdn_gate gate, gdn_dtype dtype, void *stream);
+
+/*
+ * gdn_decode_step_gated -- one token of gdn_prefill_gated on a state updated
+ * in place:  q, k [B, H, K]; v, o [B, H, V]; alpha [B, H] or [B, H, K];
+ * beta [B, H]; b [B, H, K]; w [B, H, V]; S [B, H, V, K].  Which gates must be
+ * given (and which must be NULL) as for gdn_prefill_gated.
+ */
+GDN_API int gdn_decode_step_gated(const void *q, const void *k, const void *v,
+                                  const float *alpha, const float *beta, const float *b,
+                                  const float *w, float *S, void *o, int B, int H, int K, int V,
+                                  gdn_gate gate, gdn_dtype dtype, void *stream);
+
+/*
  * gdn_state_rank -- stable rank of BH states ("On State Reduction" notes,
  * Sec. 2.2, Eq. (5)): er(S) = ||S||_F^2 / ||S||_2^2.
  *

@@ -139,3 +139,40 @@ def test_prologue_rejects_bad_arguments(lib):
     assert dec(idx=None) == binding.GDN_ERR_INVALID_ARG
     assert dec(idx=F + 4) == binding.GDN_ERR_ALIGNMENT
     assert dec(B=0) == binding.GDN_OK
+
+
+def test_gated_rejects_bad_arguments(lib):
+    F = FAKE
+
+    def pre(**kw):
+        a = dict(q=F, k=F, v=F, al=F, be=F, b=None, w=None, S0=None, o=F, ST=F, B=1, T=4, H=1,
+                 K=128, V=128, gate=binding.GDN_GATE_KDA, dt=0)
+        a.update(kw)
+        return lib.gdn_prefill_gated(a["q"], a["k"], a["v"], a["al"], a["be"], a["b"], a["w"],
+                                     a["S0"], a["o"], a["ST"], a["B"], a["T"], a["H"], a["K"],
+                                     a["V"], a["gate"], a["dt"], None)
+    assert pre(gate=3) == binding.GDN_ERR_INVALID_ARG
+    assert pre(K=96) == binding.GDN_ERR_UNSUPPORTED
+    assert pre(be=None) == binding.GDN_ERR_INVALID_ARG            # KDA needs beta
+    assert pre(b=F, w=F) == binding.GDN_ERR_INVALID_ARG           # ... and no b / w
+    assert pre(gate=binding.GDN_GATE_GDN2) == binding.GDN_ERR_INVALID_ARG  # GDN2: b, w, no beta
+    assert pre(gate=binding.GDN_GATE_GDN2, be=None, b=F) == binding.GDN_ERR_INVALID_ARG
+    assert pre(o=None, ST=None) == binding.GDN_ERR_INVALID_ARG
+    assert pre(al=F + 4) == binding.GDN_ERR_ALIGNMENT
+    assert pre(gate=binding.GDN_GATE_GDN2, be=None, b=F, w=F + 8) == binding.GDN_ERR_ALIGNMENT
+    assert pre(B=0) == binding.GDN_OK
+
+    def dec(**kw):
+        a = dict(q=F, k=F, v=F, al=F, be=None, b=F, w=F, S=F, o=F, B=1, H=1, K=64, V=128,
+                 gate=binding.GDN_GATE_GDN2, dt=0)
+        a.update(kw)
+        return lib.gdn_decode_step_gated(a["q"], a["k"], a["v"], a["al"], a["be"], a["b"],
+                                         a["w"], a["S"], a["o"], a["B"], a["H"], a["K"], a["V"],
+                                         a["gate"], a["dt"], None)
+    assert dec(be=F) == binding.GDN_ERR_INVALID_ARG
+    assert dec(w=None) == binding.GDN_ERR_INVALID_ARG
+    assert dec(S=None) == binding.GDN_ERR_INVALID_ARG
+    assert dec(K=16) == binding.GDN_ERR_UNSUPPORTED
+    assert dec(dt=5) == binding.GDN_ERR_INVALID_ARG
+    assert dec(b=F + 4) == binding.GDN_ERR_ALIGNMENT
+    assert dec(B=0) == binding.GDN_OK
