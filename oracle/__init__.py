@@ -25,6 +25,14 @@ recurrence_gated(q, k, v, alpha, beta=None, b=None, w=None, S0=None, gate="kda")
     Sec. 2.5 (KDA: per-key-channel decay on the right of the state, scalar
     beta) and Sec. 2.6 (GDN2: key-side erase gate b, value-side write gate
     w), token by token in float64 (C, ``gdn_oracle_gated.c``).
+truncate_state(S, r)
+    Rank-r truncation of "How much of a Gated DeltaNet state is used" blog,
+    Sec. 3: project each state onto its top-r left singular directions,
+    S_r = U_r U_r^T S (LAPACK SVD); r >= min(V, K) leaves S unchanged.
+recurrence_truncated(q, k, v, alpha, beta, S0=None, seg_len=256, r=...)
+    The same blog section's experiment: run the recurrence in segments of
+    seg_len tokens and truncate the carried state to rank r at every segment
+    boundary inside the sequence (the final state is not truncated).
 gather_normalize(x, idx, eps=1e-12)
     Channel selection with the normalisation recomputed on the kept
     coordinates ("On State Reduction in Linear Attention" notes, Sec. 2.6 and
@@ -183,6 +191,40 @@ def stable_rank(S):
     nz = sigma1 > 0
     er[nz] = fro2[nz] / sigma1[nz] ** 2
     return fro2.reshape(lead), sigma1.reshape(lead), er.reshape(lead)
+
+
+def truncate_state(S, r):
+    """S [..., V, K] -> float64 U_r U_r^T S, U_r the left singular vectors of
+    the r largest singular values of each state."""
+    S = _as_f64(S)
+    V, K = S.shape[-2:]
+    if r >= min(V, K):
+        return S.copy()
+    U, _, _ = np.linalg.svd(S, full_matrices=False)
+    Ur = U[..., :, :r]
+    return Ur @ (np.swapaxes(Ur, -1, -2) @ S)
+
+
+def recurrence_truncated(q, k, v, alpha, beta, S0=None, seg_len=256, r=None, threads=None):
+    """Segments [0, L), [L, 2L), ...: run ``recurrence`` on each from the
+    carried state, then replace that state by ``truncate_state(S, r)`` if the
+    segment does not end the sequence.  Returns (o, S_T) in float64."""
+    k = _as_f64(k)
+    B, T, H, K = k.shape
+    V = np.asarray(v).shape[-1]
+    o = np.empty((B, T, H, V), dtype=np.float64)
+    S = None if S0 is None else _as_f64(S0)
+    if T == 0:
+        return o, (np.zeros((B, H, V, K)) if S is None else S.copy())
+    for t0 in range(0, T, seg_len):
+        t1 = min(T, t0 + seg_len)
+        sl = slice(t0, t1)
+        o[:, sl], S = recurrence(np.asarray(q)[:, sl], k[:, sl], np.asarray(v)[:, sl],
+                                 np.asarray(alpha)[:, sl], np.asarray(beta)[:, sl], S0=S,
+                                 threads=threads)
+        if t1 < T:
+            S = truncate_state(S, r)
+    return o, S
 
 
 def gather_normalize(x, idx, eps=1e-12):
