@@ -252,7 +252,8 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         idx = torch.from_numpy(pp.meta["kept_channels"].astype(np.int32)).cuda()
         extra["prologue"] = bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier,
                                            max_over_ranks, world)
-        del d, dp, pp
+        d_head = d
+        del dp, pp
 
         # ---- stable-rank epilogue on the final states of the headline run ----
         f2 = torch.empty(B * H, device="cuda")
@@ -265,6 +266,10 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         tr, perr = time_calls(rank_call, 5, 2, torch, barrier)
         extra["state_rank"] = {"ms_per_call": tr / 5, "states": B * H,
                                "median_er": float(er.median().item())}
+
+        # ---- rank-r truncation: the headline's final states, and the segmented prefill ----
+        extra["truncation"] = bench_truncation(args, torch, binding, d_head, ST, barrier,
+                                               max_over_ranks, world)
 
         # ---- long-context prefill: B=1, T=65536, H=16 (segment-parallel) ----
         extra["long_context"] = bench_long(args, torch, binding, inputs, peaks, barrier,
@@ -481,6 +486,41 @@ def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over
             "pipeline_ms_per_step": tl / args.steps,
             "pipeline_tokens_per_s": B * T * world * args.steps / (tl / 1e3),
             "launches": args.steps * 5}
+
+
+def bench_truncation(args, torch, binding, d, ST, barrier, max_over_ranks, world):
+    """Rank-r truncation ("How much of a Gated DeltaNet state is used" blog,
+    Sec. 3): one gdn_state_truncate call on the 128 final states of the
+    headline run (r = 32; the kernel also returns every singular value), and
+    the headline prefill run in 256-token segments with the carried state cut
+    to rank 32 at each of the 15 boundaries."""
+    B, T, H, K = d["k"].shape
+    V = d["v"].shape[-1]
+    S = ST.clone()
+    sig = torch.empty((B * H, min(V, K)), device="cuda")
+
+    def trunc():
+        S.copy_(ST)
+        binding.gdn_state_truncate(S, B * H, V, K, 32, sig, 30)
+
+    steps = max(3, min(args.steps, 10))
+    tt, _ = time_calls(trunc, steps, 2, torch, barrier)
+    status = binding.gdn_get_last_device_status()
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
+    S_T = torch.empty_like(ST)
+
+    def seg():
+        binding.gdn_prefill_truncated(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o,
+                                      S_T, B, T, H, K, V, binding.GDN_BF16, 256, 32, 30)
+
+    ts, _ = time_calls(seg, steps, 2, torch, barrier)
+    ts = max_over_ranks(ts)
+    return {"state_truncate_ms": max_over_ranks(tt) / steps, "states": B * H, "r": 32,
+            "includes": "a 8 MB state copy per call (the truncation works in place)",
+            "device_status": status,
+            "segmented_prefill": {"seg_len": 256, "r": 32, "ms_per_step": ts / steps,
+                                  "tokens_per_s": B * T * world / (ts / steps / 1e3)},
+            "sigma1_median": float(sig[:, 0].median().item())}
 
 
 def gated_bytes(B, T, H, K, V, gate):

@@ -20,6 +20,10 @@ from .binding import (  # noqa: F401
     gdn_prefill_gated,
     gdn_decode_step_gated,
     prefill_gated,
+    prefill_truncated,
+    state_truncate,
+    gdn_state_truncate,
+    gdn_prefill_truncated,
     gdn_prefill_workspace_size,
     gdn_selftest_wait_timeout,
     gdn_state_rank,

@@ -24,6 +24,7 @@ GDN_ERR_TIMEOUT = -5
 GDN_ERR_WORKSPACE = -6
 GDN_ERR_DEVICE_BOUNDS = -7
 GDN_WARN_ZERO_STATE = 1
+GDN_WARN_NOT_CONVERGED = 2
 
 GDN_BF16 = 0
 GDN_FP32 = 1
@@ -48,6 +49,8 @@ EXPORTS = (
     "gdn_decode_step_gathered",
     "gdn_prefill_gated",
     "gdn_decode_step_gated",
+    "gdn_state_truncate",
+    "gdn_prefill_truncated",
 )
 
 _lock = threading.Lock()
@@ -98,6 +101,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_gated.restype = i
         lib.gdn_decode_step_gated.argtypes = [vp] * 9 + [i] * 6 + [vp]
         lib.gdn_decode_step_gated.restype = i
+        lib.gdn_state_truncate.argtypes = [vp, i, i, i, i, vp, i, vp]
+        lib.gdn_state_truncate.restype = i
+        lib.gdn_prefill_truncated.argtypes = [vp] * 8 + [i] * 9 + [vp, sz, vp]
+        lib.gdn_prefill_truncated.restype = i
         lib.gdn_prefill_noalloc_max_workspace.argtypes = []
         lib.gdn_prefill_noalloc_max_workspace.restype = sz
         _lib = lib
@@ -223,6 +230,50 @@ def prefill_gated(q, k, v, alpha, beta=None, b=None, w=None, S0=None, gate="kda"
     ST = torch.empty((B, H, V, K), dtype=torch.float32, device=v.device) if want_state else None
     gdn_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, ST, B, T, H, K, V, GATES[gate],
                       _dtype_code(v), stream)
+    return o, ST
+
+
+def gdn_state_truncate(S, BH, V, K, r, sigma=None, max_sweeps=30, stream=None) -> int:
+    st = load().gdn_state_truncate(_ptr(S), BH, V, K, r, _ptr(sigma), max_sweeps,
+                                   _stream(stream))
+    return _check(st, "gdn_state_truncate")
+
+
+def gdn_prefill_truncated(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, seg_len, r,
+                          max_sweeps=30, workspace=None, workspace_bytes=0, stream=None) -> int:
+    st = load().gdn_prefill_truncated(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                      _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, K, V, dtype,
+                                      seg_len, r, max_sweeps, _ptr(workspace), workspace_bytes,
+                                      _stream(stream))
+    return _check(st, "gdn_prefill_truncated")
+
+
+def state_truncate(S, r, want_sigma=False, max_sweeps=30, stream=None):
+    """In-place rank-r truncation of S [..., V, K] (float32 CUDA); returns the
+    singular values [..., min(V, K)] if asked."""
+    import torch
+    V, K = S.shape[-2:]
+    BH = S.numel() // (V * K)
+    sigma = (torch.empty(S.shape[:-2] + (min(V, K),), dtype=torch.float32, device=S.device)
+             if want_sigma else None)
+    gdn_state_truncate(S, BH, V, K, r, sigma, max_sweeps, stream)
+    return sigma
+
+
+def prefill_truncated(q, k, v, alpha, beta, S0=None, seg_len=256, r=32, max_sweeps=30,
+                      stream=None):
+    """gdn_prefill_truncated on torch CUDA tensors.  Returns (o, S_T)."""
+    import torch
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = torch.empty((B, T, H, V), dtype=v.dtype, device=v.device)
+    ST = torch.empty((B, H, V, K), dtype=torch.float32, device=v.device)
+    dt = _dtype_code(v)
+    L = min(seg_len, T) if T > 0 else 0
+    need = max([gdn_prefill_workspace_size(B, n, H, K, V, dt) for n in (L, T % seg_len) if n] + [0])
+    ws = torch.empty(need, dtype=torch.uint8, device=v.device) if need else None
+    gdn_prefill_truncated(q, k, v, alpha, beta, S0, o, ST, B, T, H, K, V, dt, seg_len, r,
+                          max_sweeps, ws, need, stream)
     return o, ST
 
 

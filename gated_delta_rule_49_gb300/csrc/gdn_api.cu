@@ -81,6 +81,7 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_WORKSPACE: return "workspace missing or too small";
         case GDN_ERR_DEVICE_BOUNDS: return "device-side index check failed";
         case GDN_WARN_ZERO_STATE: return "warning: all-zero state (stable rank undefined, 0 returned)";
+        case GDN_WARN_NOT_CONVERGED: return "warning: Jacobi sweeps stopped at max_sweeps before convergence";
         default: return "unknown status";
     }
 }
@@ -133,9 +134,9 @@ int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
     // bf16 at V = 128 runs on the tensor cores; float32 mode and the small
     // (32, 32) variant run the CUDA-core chunked kernel.
     if (dtype == GDN_BF16 && V == 128 && (K == 128 || K == 64))
-        return from_cuda(gdn::launch_prefill_tc(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
+        return from_cuda(gdn::launch_prefill_tc(q, k, v, alpha, beta, S0, o, S_T, B, T, T, H, K, V,
                                                 workspace, workspace_bytes, st));
-    return from_cuda(gdn::launch_prefill_simt(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
+    return from_cuda(gdn::launch_prefill_simt(q, k, v, alpha, beta, S0, o, S_T, B, T, T, H, K, V,
                                               dtype, st));
 }
 
@@ -226,6 +227,68 @@ int gdn_decode_step_gated(const void *q, const void *k, const void *v, const flo
                                               dtype, static_cast<cudaStream_t>(stream)));
 }
 
+int gdn_state_truncate(float *S, int BH, int V, int K, int r, float *sigma, int max_sweeps,
+                       void *stream) {
+    if (BH < 0 || r < 1 || max_sweeps < 1 || max_sweeps > 1000) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if (BH == 0) return GDN_OK;
+    if (!S) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(S) || (sigma && !aligned16(sigma))) return GDN_ERR_ALIGNMENT;
+    if (r >= (K < V ? K : V) && !sigma) return GDN_OK;  // nothing to cut, nothing asked
+    return from_cuda(gdn::launch_state_truncate(S, BH, V, K, r, sigma, max_sweeps,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_prefill_truncated(const void *q, const void *k, const void *v, const float *alpha,
+                          const float *beta, const float *S0, void *o, float *S_T, int B, int T,
+                          int H, int K, int V, gdn_dtype dtype, int seg_len, int r,
+                          int max_sweeps, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    if (B < 0 || T < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if (seg_len < 1 || r < 1 || max_sweeps < 1 || max_sweeps > 1000) return GDN_ERR_INVALID_ARG;
+    if (!S_T) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, alpha, beta, S0, o, S_T};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    // windows are seg_len tokens long, the last one possibly shorter
+    const int L = seg_len < T ? seg_len : T, tail = T % seg_len;
+    size_t need = gdn_prefill_workspace_size(B, L, H, K, V, dtype);
+    if (tail > 0) {
+        const size_t need_tail = gdn_prefill_workspace_size(B, tail, H, K, V, dtype);
+        if (need_tail > need) need = need_tail;
+    }
+    if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
+    if ((long long)B * H == 0) return GDN_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
+    const size_t esz = dtype == GDN_BF16 ? 2 : 4;
+    const bool tc = dtype == GDN_BF16 && V == 128 && (K == 128 || K == 64);
+    const float *start = S0;
+    for (int t0 = 0; t0 < T; t0 += seg_len) {
+        const int n = T - t0 < seg_len ? T - t0 : seg_len;
+        const size_t tok = (size_t)t0 * H;  // token-head offset of the window
+        const char *qw = static_cast<const char *>(q) + tok * K * esz;
+        const char *kw = static_cast<const char *>(k) + tok * K * esz;
+        const char *vw = static_cast<const char *>(v) + tok * V * esz;
+        char *ow = o ? static_cast<char *>(o) + tok * V * esz : nullptr;
+        cudaError_t e = tc ? gdn::launch_prefill_tc(qw, kw, vw, alpha + tok, beta + tok, start, ow,
+                                                    S_T, B, n, T, H, K, V, workspace,
+                                                    workspace_bytes, st)
+                           : gdn::launch_prefill_simt(qw, kw, vw, alpha + tok, beta + tok, start,
+                                                      ow, S_T, B, n, T, H, K, V, dtype, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        start = S_T;
+        if (t0 + n < T && r < (K < V ? K : V)) {
+            e = gdn::launch_state_truncate(S_T, B * H, V, K, r, nullptr, max_sweeps, st);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+    }
+    return GDN_OK;
+}
+
 int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
                    float *stable_rank, int max_iter, float tol, void *stream) {
     if (BH < 0 || V < 1 || K < 1 || V > 128 || K > 128) return GDN_ERR_INVALID_ARG;
@@ -250,6 +313,7 @@ int gdn_get_last_device_status(void *stream) {
         return GDN_ERR_CUDA;
     if (word & gdn::kStatusTimeout) return GDN_ERR_TIMEOUT;
     if (word & gdn::kStatusBounds) return GDN_ERR_DEVICE_BOUNDS;
+    if (word & gdn::kStatusNotConverged) return GDN_WARN_NOT_CONVERGED;
     if (word & gdn::kStatusZeroState) return GDN_WARN_ZERO_STATE;
     return GDN_OK;
 }

@@ -12,7 +12,7 @@
 namespace gdn {
 
 // Bits of the per-device status word (see gdn_get_last_device_status).
-enum : int { kStatusTimeout = 1, kStatusBounds = 2, kStatusZeroState = 4 };
+enum : int { kStatusTimeout = 1, kStatusBounds = 2, kStatusZeroState = 4, kStatusNotConverged = 8 };
 
 // Chunk length of the chunkwise prefill.
 constexpr int kChunk = 64;
@@ -35,15 +35,19 @@ cudaError_t launch_state_rank(const float *S, int BH, int V, int K, float *fro2,
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v,
                                 const float *alpha, const float *beta, const float *S0,
-                                void *o, float *ST, int B, int T, int H, int K, int V,
+                                void *o, float *ST, int B, int T, int Ts, int H, int K, int V,
                                 gdn_dtype dt, cudaStream_t stream);
 
 // Tensor-core (tcgen05) chunked prefill: bf16 q/k/v, V = 128, K in {64, 128}.
 // Long sequences on few heads run segment-parallel and need `workspace`.
+//
+// Both chunked prefills process tokens [0, T) of token tensors laid out as
+// [B, Ts, H, *] (Ts >= T tokens per batch entry; alpha/beta [B, Ts, H]):
+// Ts = T for a whole tensor, Ts > T for a window of a longer one.
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *ST, int B,
-                              int T, int H, int K, int V, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream);
+                              int T, int Ts, int H, int K, int V, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 // How the tensor-core prefill splits B*H sequences of T tokens into segments
 // on a device with `nsm` SMs (nseg == 1: one CTA per whole sequence).
@@ -76,6 +80,10 @@ cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, con
                                 const float *beta, const float *bg, const float *wg, float *S,
                                 void *o, int B, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
                                 cudaStream_t stream);
+
+// Rank-r truncation (and singular values) of BH states [V, K] by one-sided Jacobi.
+cudaError_t launch_state_truncate(float *S, int BH, int V, int K, int r, float *sigma,
+                                  int max_sweeps, cudaStream_t stream);
 
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1)
     prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                         const Tin *__restrict__ v, const float *__restrict__ alpha,
                         const float *__restrict__ beta, const float *__restrict__ S0,
-                        Tin *__restrict__ o, float *__restrict__ ST, int T, int H, int V) {
+                        Tin *__restrict__ o, float *__restrict__ ST, int T, int Ts, int H,
+                        int V) {
     using L = SimtSmem<K, VS>;
     extern __shared__ float sm[];
     float *Ks = sm + L::kKs;
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1)
             const int t = e / K, j = e % K;
             float kv = 0.f, qv = 0.f;
             if (t < n) {
-                const size_t off = (((size_t)b * T + c0 + t) * H + h) * K + j;
+                const size_t off = (((size_t)b * Ts + c0 + t) * H + h) * K + j;
                 kv = to_f32(k[off]);
                 qv = to_f32(q[off]);
             }
@@ -96,14 +97,14 @@ __global__ void __launch_bounds__(kSimtThreads, 1)
         for (int e = tid; e < C * VS; e += kSimtThreads) {
             const int t = e / VS, i = e % VS;
             float vv = 0.f;
-            if (t < n) vv = to_f32(v[(((size_t)b * T + c0 + t) * H + h) * V + i0 + i]);
+            if (t < n) vv = to_f32(v[(((size_t)b * Ts + c0 + t) * H + h) * V + i0 + i]);
             Vsm[t * L::LV + i] = vv;
         }
         if (tid < 32) {
             // in-chunk inclusive prefix sum of log alpha over 64 tokens
             const int t0 = tid, t1 = tid + 32;
-            const size_t g0i = ((size_t)b * T + c0 + t0) * H + h;
-            const size_t g1i = ((size_t)b * T + c0 + t1) * H + h;
+            const size_t g0i = ((size_t)b * Ts + c0 + t0) * H + h;
+            const size_t g1i = ((size_t)b * Ts + c0 + t1) * H + h;
             float g0 = t0 < n ? logf(alpha[g0i]) : 0.f;
             float g1 = t1 < n ? logf(alpha[g1i]) : 0.f;
             bet[t0] = t0 < n ? beta[g0i] : 0.f;
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1)
                     for (int c = 0; c < NI; ++c) oq[c] = fmaf(p, Um[s * L::LV + ib + c], oq[c]);
                 }
                 if (t < n) {
-                    Tin *orow = o + (((size_t)b * T + c0 + t) * H + h) * V + i0 + ib;
+                    Tin *orow = o + (((size_t)b * Ts + c0 + t) * H + h) * V + i0 + ib;
 #pragma unroll
                     for (int c = 0; c < NI; ++c) orow[c] = from_f32<Tin>(oq[c]);
                 }
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1)
 template <int K, int VS, typename Tin>
 cudaError_t launch_simt_t(const void *q, const void *k, const void *v, const float *alpha,
                           const float *beta, const float *S0, void *o, float *ST, int B,
-                          int T, int H, int V, cudaStream_t stream) {
+                          int T, int Ts, int H, int V, cudaStream_t stream) {
     static_assert(kSimtThreads % C == 0 && VS % (kSimtThreads / C) == 0, "tiling");
     static_assert(K <= kSimtThreads && kSimtThreads % K == 0 && VS % (kSimtThreads / K) == 0,
                   "tiling");
@@ -269,7 +270,7 @@ cudaError_t launch_simt_t(const void *q, const void *k, const void *v, const flo
     dim3 grid(V / VS, H, B);
     kern<<<grid, kSimtThreads, smem, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
-        alpha, beta, S0, static_cast<Tin *>(o), ST, T, H, V);
+        alpha, beta, S0, static_cast<Tin *>(o), ST, T, Ts, H, V);
     return cudaGetLastError();
 }
 
@@ -277,24 +278,24 @@ cudaError_t launch_simt_t(const void *q, const void *k, const void *v, const flo
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v,
                                 const float *alpha, const float *beta, const float *S0,
-                                void *o, float *ST, int B, int T, int H, int K, int V,
+                                void *o, float *ST, int B, int T, int Ts, int H, int K, int V,
                                 gdn_dtype dt, cudaStream_t stream) {
     const bool bf = dt == GDN_BF16;
     if (K == 32 && V == 32)
         return bf ? launch_simt_t<32, 32, __nv_bfloat16>(q, k, v, alpha, beta, S0, o, ST, B, T,
-                                                        H, V, stream)
-                  : launch_simt_t<32, 32, float>(q, k, v, alpha, beta, S0, o, ST, B, T, H, V,
-                                                stream);
+                                                        Ts, H, V, stream)
+                  : launch_simt_t<32, 32, float>(q, k, v, alpha, beta, S0, o, ST, B, T, Ts, H,
+                                                V, stream);
     if (K == 64 && V == 128)
         return bf ? launch_simt_t<64, 32, __nv_bfloat16>(q, k, v, alpha, beta, S0, o, ST, B, T,
-                                                        H, V, stream)
-                  : launch_simt_t<64, 32, float>(q, k, v, alpha, beta, S0, o, ST, B, T, H, V,
-                                                stream);
+                                                        Ts, H, V, stream)
+                  : launch_simt_t<64, 32, float>(q, k, v, alpha, beta, S0, o, ST, B, T, Ts, H,
+                                                V, stream);
     if (K == 128 && V == 128)
         return bf ? launch_simt_t<128, 32, __nv_bfloat16>(q, k, v, alpha, beta, S0, o, ST, B,
-                                                         T, H, V, stream)
-                  : launch_simt_t<128, 32, float>(q, k, v, alpha, beta, S0, o, ST, B, T, H, V,
-                                                 stream);
+                                                         T, Ts, H, V, stream)
+                  : launch_simt_t<128, 32, float>(q, k, v, alpha, beta, S0, o, ST, B, T, Ts, H,
+                                                 V, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ alpha,
                       const float *__restrict__ beta, const float *__restrict__ S0,
-                      __nv_bfloat16 *__restrict__ o, float *__restrict__ ST, int T, int H,
+                      __nv_bfloat16 *__restrict__ o, float *__restrict__ ST, int T, int Ts, int H,
                       int BH, SegPlan plan, int *status) {
     using L = TcLayout<K>;
     constexpr int V = 128;
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto prefetch_gates = [&](int n) {
             if (warp == 1 && n < nchunks) {
                 const int nv = min(64, t1 - t0 - n * 64);
-                const size_t i0 = ((size_t)b * T + t0 + n * 64 + lane) * H + h;
+                const size_t i0 = ((size_t)b * Ts + t0 + n * 64 + lane) * H + h;
                 const size_t i1 = i0 + (size_t)32 * H;
                 pa0 = lane < nv ? alpha[i0] : 1.f;
                 pb0 = lane < nv ? beta[i0] : 0.f;
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto sg_load = [&](int m) {
             if (m < nchunks) {
                 const int nv = min(64, t1 - t0 - m * 64);
-                const size_t i0 = ((size_t)b * T + t0 + m * 64 + lane) * H + h;
+                const size_t i0 = ((size_t)b * Ts + t0 + m * 64 + lane) * H + h;
                 sa0 = lane < nv ? alpha[i0] : 1.f;
                 sa1 = lane + 32 < nv ? alpha[i0 + (size_t)32 * H] : 1.f;
             }
@@ -750,7 +750,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_ld_wait();
                 if (o != nullptr && t < nvalid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(
-                        o + (((size_t)b * T + t0 + n * 64 + t) * H + h) * V + 64 * hf);
+                        o + (((size_t)b * Ts + t0 + n * 64 + t) * H + h) * V + 64 * hf);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         dst[k] = make_uint4(pack_bf16(v0[8 * k], v0[8 * k + 1]),
@@ -816,13 +816,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// [B, T, H, C] bf16 tensor viewed as 4-D (C, H, T, B) with 64 x 1 x 64 x 1 boxes.
-bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int C) {
+// [B, Ts, H, C] bf16 tensor whose first T tokens per batch entry are used,
+// viewed as 4-D (C, H, T, B) with 64 x 1 x 64 x 1 boxes.
+bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int Ts, int H, int C) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)C * 2 * H,
-                             (cuuint64_t)C * 2 * H * T};
+                             (cuuint64_t)C * 2 * H * Ts};
     cuuint32_t box[4] = {64, 1, 64, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
@@ -877,10 +878,11 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
 template <int K>
 cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *S0, void *o, float *ST, int B, int T,
-                        int H, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+                        int Ts, int H, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
-    if (!make_token_map(&mq, q, B, T, H, K) || !make_token_map(&mk, k, B, T, H, K) ||
-        !make_token_map(&mv, v, B, T, H, 128))
+    if (!make_token_map(&mq, q, B, T, Ts, H, K) || !make_token_map(&mk, k, B, T, Ts, H, K) ||
+        !make_token_map(&mv, v, B, T, Ts, H, 128))
         return cudaErrorInvalidValue;
     auto kern = prefill_tc_kernel<K>;
     static bool attr_set[64] = {};
@@ -900,7 +902,7 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
     if (sh.nseg == 1) {
         if (BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         kern<<<(unsigned)BH, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-            mq, mk, mv, alpha, beta, S0, ob, ST, T, H, (int)BH, SegPlan{kWhole, 1, T, nullptr},
+            mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH, SegPlan{kWhole, 1, T, nullptr},
             status);
         return cudaGetLastError();
     }
@@ -909,7 +911,7 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
     const long long g1 = BH * (2 * sh.nseg - 1), g2 = BH * (sh.nseg - 1);
     if (g1 > 0x7fffffffLL || BH > 65535) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)g1, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, ob, ST, T, H, (int)BH,
+        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
         SegPlan{kFirst, sh.nseg, sh.seg_len, ws}, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -918,7 +920,7 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)g2, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, ob, ST, T, H, (int)BH,
+        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
         SegPlan{kSecond, sh.nseg, sh.seg_len, ws}, status);
     return cudaGetLastError();
 }
@@ -954,14 +956,14 @@ SegShape segment_shape(int BH, int T, int K, int nsm) {
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *ST, int B,
-                              int T, int H, int K, int V, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream) {
+                              int T, int Ts, int H, int K, int V, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
     if (V != 128) return cudaErrorInvalidValue;
     if (K == 128)
-        return launch_tc_t<128>(q, k, v, alpha, beta, S0, o, ST, B, T, H, workspace,
+        return launch_tc_t<128>(q, k, v, alpha, beta, S0, o, ST, B, T, Ts, H, workspace,
                                 workspace_bytes, stream);
     if (K == 64)
-        return launch_tc_t<64>(q, k, v, alpha, beta, S0, o, ST, B, T, H, workspace,
+        return launch_tc_t<64>(q, k, v, alpha, beta, S0, o, ST, B, T, Ts, H, workspace,
                                workspace_bytes, stream);
     return cudaErrorInvalidValue;
 }

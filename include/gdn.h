@@ -59,7 +59,8 @@ typedef enum {
     GDN_ERR_TIMEOUT = -5,       /* device status: a bounded wait in a kernel gave up */
     GDN_ERR_WORKSPACE = -6,     /* workspace missing or smaller than required */
     GDN_ERR_DEVICE_BOUNDS = -7, /* device status: a kernel's own index check failed */
-    GDN_WARN_ZERO_STATE = 1     /* device status: gdn_state_rank saw an all-zero state */
+    GDN_WARN_ZERO_STATE = 1,    /* device status: gdn_state_rank saw an all-zero state */
+    GDN_WARN_NOT_CONVERGED = 2  /* device status: gdn_state_truncate hit max_sweeps */
 } gdn_status;
 
 typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
@@ -238,9 +239,50 @@ GDN_API int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, fl
                    float *stable_rank, int max_iter, float tol, void *stream);
 
 /*
+ * gdn_state_truncate -- rank-r truncation of BH states, in place ("How much
+ * of a Gated DeltaNet state is used" blog, Sec. 3): each state is projected
+ * onto its top-r left singular directions,
+ *
+ *     S <- U_r U_r^T S      (the best rank-r approximation of S),
+ *
+ * and, if `sigma` is given, its singular values are written in descending
+ * order.
+ *
+ *   S     [BH, V, K] float32, (K, V) one of the supported variants
+ *   r     >= 1; r >= min(V, K) leaves S unchanged
+ *   sigma [BH, min(V, K)] float32 or NULL
+ *   max_sweeps  1..1000 one-sided Jacobi sweeps (about 6-10 reach float32
+ *         orthogonality); stopping there sets GDN_WARN_NOT_CONVERGED
+ *
+ * Where sigma_r == sigma_{r+1} the kept subspace is not unique; the result is
+ * then one of the equally good truncations.
+ */
+GDN_API int gdn_state_truncate(float *S, int BH, int V, int K, int r, float *sigma,
+                               int max_sweeps, void *stream);
+
+/*
+ * gdn_prefill_truncated -- the same blog section's experiment: the prefill
+ * run in segments of seg_len tokens, the carried state truncated to rank r
+ * (gdn_state_truncate) at every segment boundary inside the sequence.  The
+ * final state S_T is not truncated, nor is S0.
+ *
+ * Arguments as for gdn_prefill, with S_T required (it carries the state
+ * between segments; it may alias S0) and a workspace as
+ * gdn_prefill_workspace_size reports for B, min(seg_len, T) and for the
+ * last, shorter segment (0 for the usual shapes).  seg_len >= 1, r >= 1,
+ * max_sweeps as for gdn_state_truncate.
+ */
+GDN_API int gdn_prefill_truncated(const void *q, const void *k, const void *v,
+                                  const float *alpha, const float *beta, const float *S0,
+                                  void *o, float *S_T, int B, int T, int H, int K, int V,
+                                  gdn_dtype dtype, int seg_len, int r, int max_sweeps,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * gdn_get_last_device_status -- synchronise `stream`, then read and clear the
  * current device's status word.  Returns GDN_OK, GDN_ERR_TIMEOUT,
- * GDN_ERR_DEVICE_BOUNDS, GDN_WARN_ZERO_STATE (only when no error is set) or
+ * GDN_ERR_DEVICE_BOUNDS, GDN_WARN_NOT_CONVERGED or GDN_WARN_ZERO_STATE (warnings
+ * only when no error is set) or
  * GDN_ERR_CUDA if the synchronisation itself failed.
  */
 GDN_API int gdn_get_last_device_status(void *stream);

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2):
         s = binding.status_string(code)
         assert s and s != "unknown status"
     assert binding.status_string(12345) == "unknown status"
@@ -176,3 +176,32 @@ def test_gated_rejects_bad_arguments(lib):
     assert dec(dt=5) == binding.GDN_ERR_INVALID_ARG
     assert dec(b=F + 4) == binding.GDN_ERR_ALIGNMENT
     assert dec(B=0) == binding.GDN_OK
+
+
+def test_truncation_rejects_bad_arguments(lib):
+    F = FAKE
+    assert lib.gdn_state_truncate(F, 2, 128, 128, 0, None, 30, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_state_truncate(F, 2, 128, 128, 4, None, 0, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_state_truncate(F, 2, 128, 96, 4, None, 30, None) == binding.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_state_truncate(F + 4, 2, 128, 128, 4, None, 30, None) == binding.GDN_ERR_ALIGNMENT
+    assert lib.gdn_state_truncate(F, 2, 128, 128, 4, F + 8, 30, None) == binding.GDN_ERR_ALIGNMENT
+    # nothing to cut and no singular values asked: returns before any launch
+    assert lib.gdn_state_truncate(F, 2, 128, 128, 128, None, 30, None) == binding.GDN_OK
+    assert lib.gdn_state_truncate(F, 0, 128, 128, 4, None, 30, None) == binding.GDN_OK
+
+    def pre(**kw):
+        a = dict(q=F, k=F, v=F, al=F, be=F, S0=None, o=F, ST=F, B=1, T=300, H=1, K=128, V=128,
+                 dt=0, seg=256, r=8, sw=30)
+        a.update(kw)
+        return lib.gdn_prefill_truncated(a["q"], a["k"], a["v"], a["al"], a["be"], a["S0"],
+                                         a["o"], a["ST"], a["B"], a["T"], a["H"], a["K"],
+                                         a["V"], a["dt"], a["seg"], a["r"], a["sw"], None, 0,
+                                         None)
+    assert pre(ST=None) == binding.GDN_ERR_INVALID_ARG
+    assert pre(seg=0) == binding.GDN_ERR_INVALID_ARG
+    assert pre(r=0) == binding.GDN_ERR_INVALID_ARG
+    assert pre(sw=1001) == binding.GDN_ERR_INVALID_ARG
+    assert pre(K=32) == binding.GDN_ERR_UNSUPPORTED
+    assert pre(be=None) == binding.GDN_ERR_INVALID_ARG
+    assert pre(o=F + 2) == binding.GDN_ERR_ALIGNMENT
+    assert pre(H=0) == binding.GDN_OK
