@@ -33,6 +33,15 @@ recurrence_truncated(q, k, v, alpha, beta, S0=None, seg_len=256, r=...)
     The same blog section's experiment: run the recurrence in segments of
     seg_len tokens and truncate the carried state to rank r at every segment
     boundary inside the sequence (the final state is not truncated).
+channel_gram(k, q)
+    G_h = K_h^T K_h + Q_h^T Q_h = M_h^T M_h for M_h = [K_cal; Q_cal] of head h
+    ("On State Reduction in Linear Attention" notes, Sec. 2.8), float64.
+drrqr(M, k, f=2.0, max_swaps=...)
+    The same section's DRRQR channel selector: column-pivoted QR (LAPACK
+    geqp3) for the initial permutation, then strong-RRQR swaps while the
+    largest rho_ij = sqrt(U_ij^2 + (gamma_j / omega_i)^2) exceeds f, with
+    U = A_k^{-1} B_k, omega_i = 1 / |row i of A_k^{-1}|, gamma_j = |column j of
+    C_k|; returns the first k channels of the final permutation.
 gather_normalize(x, idx, eps=1e-12)
     Channel selection with the normalisation recomputed on the kept
     coordinates ("On State Reduction in Linear Attention" notes, Sec. 2.6 and
@@ -225,6 +234,49 @@ def recurrence_truncated(q, k, v, alpha, beta, S0=None, seg_len=256, r=None, thr
         if t1 < T:
             S = truncate_state(S, r)
     return o, S
+
+
+def channel_gram(k, q):
+    """k, q [..., H, K] (any leading token axes) -> [H, K, K] float64."""
+    k = _as_f64(k)
+    q = _as_f64(q)
+    H, K = k.shape[-2:]
+    kf = k.reshape(-1, H, K)
+    qf = q.reshape(-1, H, K)
+    return np.einsum("nhi,nhj->hij", kf, kf) + np.einsum("nhi,nhj->hij", qf, qf)
+
+
+def rrqr_factors(R, k):
+    """From the upper-triangular R of M P (columns in the current order):
+    A_k, B_k, C_k and the rho matrix of the strong-RRQR test."""
+    A = R[:k, :k]
+    Bk = R[:k, k:]
+    C = R[k:, k:]
+    Ainv = np.linalg.inv(A)
+    U = Ainv @ Bk
+    omega = 1.0 / np.linalg.norm(Ainv, axis=1)   # 1 / |row i of A_k^{-1}|
+    gamma = np.linalg.norm(C, axis=0)             # |column j of C_k|
+    rho = np.sqrt(U ** 2 + (gamma[None, :] / omega[:, None]) ** 2)
+    return A, Bk, C, rho
+
+
+def drrqr(M, k, f=2.0, max_swaps=1000):
+    """M [rows, n] float64 -> (perm, rho_max, swaps): perm[:k] are the kept
+    channels in selection order."""
+    import scipy.linalg
+    M = _as_f64(M)
+    n = M.shape[1]
+    _, _, perm = scipy.linalg.qr(M, mode="economic", pivoting=True)
+    perm = np.array(perm)
+    swaps = 0
+    while True:
+        R = scipy.linalg.qr(M[:, perm], mode="r")[0][:n, :n]
+        _, _, _, rho = rrqr_factors(R, k)
+        i, j = np.unravel_index(np.argmax(rho), rho.shape)
+        if rho[i, j] <= f or swaps >= max_swaps:
+            return perm, float(rho.max()), swaps
+        perm[i], perm[k + j] = perm[k + j], perm[i]
+        swaps += 1
 
 
 def gather_normalize(x, idx, eps=1e-12):
