@@ -271,6 +271,10 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         extra["truncation"] = bench_truncation(args, torch, binding, d_head, ST, barrier,
                                                max_over_ranks, world)
 
+        # ---- DRRQR channel selection (calibration Gram + selection) ----
+        extra["drrqr"] = bench_drrqr(args, torch, binding, inputs, peaks, barrier,
+                                     max_over_ranks)
+
         # ---- long-context prefill: B=1, T=65536, H=16 (segment-parallel) ----
         extra["long_context"] = bench_long(args, torch, binding, inputs, peaks, barrier,
                                            max_over_ranks, world)
@@ -521,6 +525,41 @@ def bench_truncation(args, torch, binding, d, ST, barrier, max_over_ranks, world
             "segmented_prefill": {"seg_len": 256, "r": 32, "ms_per_step": ts / steps,
                                   "tokens_per_s": B * T * world / (ts / steps / 1e3)},
             "sigma1_median": float(sig[:, 0].median().item())}
+
+
+def bench_drrqr(args, torch, binding, inputs, peaks, barrier, max_over_ranks):
+    """DRRQR channel selection on calibration activations of the prefill
+    workload's size (B=8, T=4096, H=16, d_k=128, bf16): the Gram on the
+    tensor cores (HBM-bound: every calibration byte read once) and the
+    per-head selection of 64 channels with f = 2."""
+    k, q = inputs.make_calibration()
+    B, T, H, K = k.shape
+    dk, dq = to_dev_bf16(k, torch), to_dev_bf16(q, torch)
+    del k, q
+    G = torch.empty((H, K, K), device="cuda")
+    need = binding.gdn_channel_gram_workspace_size(B, T, H, K)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def gram():
+        binding.gdn_channel_gram(dk, dq, B, T, H, K, binding.GDN_BF16, G, ws, need)
+
+    steps = max(3, min(args.steps, 10))
+    tg, per = time_calls(gram, steps, 3, torch, barrier)
+    tg = max_over_ranks(tg)
+    byts = 2 * B * T * H * K * 2
+    gbs = byts / (statistics.mean(per) / 1e3) / 1e9
+    idx = torch.empty((H, 64), dtype=torch.int32, device="cuda")
+    rho = torch.empty(H, device="cuda")
+    sw = torch.empty(H, dtype=torch.int32, device="cuda")
+
+    def select():
+        binding.gdn_drrqr_select(G, H, K, 64, 2.0, 1000, idx, rho, sw)
+
+    ts, _ = time_calls(select, 3, 1, torch, barrier)
+    return {"workload": "calibration k, q: B=8 T=4096 H=16 d_k=128 bf16 -> 64 channels, f=2",
+            "gram_ms": tg / steps, "gram_gbs": gbs, "gram_hbm_frac": gbs / peaks["hbm_gbs"],
+            "select_ms": max_over_ranks(ts) / 3, "swaps_per_head": sw.cpu().tolist(),
+            "rho_max": float(rho.max().item())}
 
 
 def gated_bytes(B, T, H, K, V, gate):

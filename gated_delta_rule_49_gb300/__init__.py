@@ -21,6 +21,8 @@ from .binding import (  # noqa: F401
     gdn_decode_step_gated,
     prefill_gated,
     prefill_truncated,
+    channel_gram,
+    drrqr_select,
     state_truncate,
     gdn_state_truncate,
     gdn_prefill_truncated,

@@ -25,6 +25,7 @@ GDN_ERR_WORKSPACE = -6
 GDN_ERR_DEVICE_BOUNDS = -7
 GDN_WARN_ZERO_STATE = 1
 GDN_WARN_NOT_CONVERGED = 2
+GDN_WARN_RANK_DEFICIENT = 3
 
 GDN_BF16 = 0
 GDN_FP32 = 1
@@ -51,6 +52,9 @@ EXPORTS = (
     "gdn_decode_step_gated",
     "gdn_state_truncate",
     "gdn_prefill_truncated",
+    "gdn_channel_gram_workspace_size",
+    "gdn_channel_gram",
+    "gdn_drrqr_select",
 )
 
 _lock = threading.Lock()
@@ -105,6 +109,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_state_truncate.restype = i
         lib.gdn_prefill_truncated.argtypes = [vp] * 8 + [i] * 9 + [vp, sz, vp]
         lib.gdn_prefill_truncated.restype = i
+        lib.gdn_channel_gram_workspace_size.argtypes = [i] * 4
+        lib.gdn_channel_gram_workspace_size.restype = sz
+        lib.gdn_channel_gram.argtypes = [vp, vp] + [i] * 5 + [vp, vp, sz, vp]
+        lib.gdn_channel_gram.restype = i
+        lib.gdn_drrqr_select.argtypes = [vp, i, i, i, f, i, vp, vp, vp, vp]
+        lib.gdn_drrqr_select.restype = i
         lib.gdn_prefill_noalloc_max_workspace.argtypes = []
         lib.gdn_prefill_noalloc_max_workspace.restype = sz
         _lib = lib
@@ -275,6 +285,47 @@ def prefill_truncated(q, k, v, alpha, beta, S0=None, seg_len=256, r=32, max_swee
     gdn_prefill_truncated(q, k, v, alpha, beta, S0, o, ST, B, T, H, K, V, dt, seg_len, r,
                           max_sweeps, ws, need, stream)
     return o, ST
+
+
+def gdn_channel_gram_workspace_size(B, T, H, K) -> int:
+    return int(load().gdn_channel_gram_workspace_size(B, T, H, K))
+
+
+def gdn_channel_gram(k, q, B, T, H, K, dtype, G, workspace, workspace_bytes,
+                     stream=None) -> int:
+    st = load().gdn_channel_gram(_ptr(k), _ptr(q), B, T, H, K, dtype, _ptr(G), _ptr(workspace),
+                                 workspace_bytes, _stream(stream))
+    return _check(st, "gdn_channel_gram")
+
+
+def gdn_drrqr_select(G, H, n, k, f, max_swaps, idx, rho_max=None, swaps=None,
+                     stream=None) -> int:
+    st = load().gdn_drrqr_select(_ptr(G), H, n, k, ctypes.c_float(f), max_swaps, _ptr(idx),
+                                 _ptr(rho_max), _ptr(swaps), _stream(stream))
+    return _check(st, "gdn_drrqr_select")
+
+
+def channel_gram(k, q, stream=None):
+    """k, q [B, T, H, 128] bf16 CUDA -> G [H, 128, 128] float32."""
+    import torch
+    B, T, H, K = k.shape
+    G = torch.empty((H, K, K), dtype=torch.float32, device=k.device)
+    need = gdn_channel_gram_workspace_size(B, T, H, K)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=k.device)
+    gdn_channel_gram(k, q, B, T, H, K, _dtype_code(k), G, ws, need, stream)
+    return G
+
+
+def drrqr_select(G, k, f=2.0, max_swaps=1000, stream=None):
+    """G [H, n, n] float32 CUDA -> (idx [H, k] int32 in selection order,
+    rho_max [H], swaps [H])."""
+    import torch
+    H, n, _ = G.shape
+    idx = torch.empty((H, k), dtype=torch.int32, device=G.device)
+    rho = torch.empty(H, dtype=torch.float32, device=G.device)
+    sw = torch.empty(H, dtype=torch.int32, device=G.device)
+    gdn_drrqr_select(G, H, n, k, f, max_swaps, idx, rho, sw, stream)
+    return idx, rho, sw
 
 
 def gather_normalize(x, idx, stream=None):

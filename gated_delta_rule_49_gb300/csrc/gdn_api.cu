@@ -82,6 +82,7 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_DEVICE_BOUNDS: return "device-side index check failed";
         case GDN_WARN_ZERO_STATE: return "warning: all-zero state (stable rank undefined, 0 returned)";
         case GDN_WARN_NOT_CONVERGED: return "warning: Jacobi sweeps stopped at max_sweeps before convergence";
+        case GDN_WARN_RANK_DEFICIENT: return "warning: calibration matrix has rank < k (greedy choice kept, no swaps)";
         default: return "unknown status";
     }
 }
@@ -289,6 +290,45 @@ int gdn_prefill_truncated(const void *q, const void *k, const void *v, const flo
     return GDN_OK;
 }
 
+size_t gdn_channel_gram_workspace_size(int B, int T, int H, int K) {
+    if (B <= 0 || T <= 0 || H <= 0 || K != 128) return 0;
+    return (size_t)H * gdn::gram_splits(B, T, H) * 128 * 128 * sizeof(float);
+}
+
+int gdn_channel_gram(const void *k, const void *q, int B, int T, int H, int K, gdn_dtype dtype,
+                     float *G, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || T < 0 || H < 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (K != 128 || dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (H == 0) return GDN_OK;
+    if (!G) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((long long)B * T == 0)
+        return from_cuda(cudaMemsetAsync(G, 0, sizeof(float) * (size_t)H * K * K, st));
+    if (!k || !q) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {k, q, G, workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    if ((long long)B * ((T + 63) / 64) > 0x7fffffffLL || H > 65535) return GDN_ERR_INVALID_ARG;
+    const size_t need = gdn_channel_gram_workspace_size(B, T, H, K);
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    return from_cuda(gdn::launch_channel_gram(k, q, B, T, H, G, workspace, st));
+}
+
+int gdn_drrqr_select(const float *G, int H, int n, int k, float f, int max_swaps, int *idx,
+                     float *rho_max, int *swaps, void *stream) {
+    if (H < 0 || n < 2 || n > 128 || k < 1 || k >= n) return GDN_ERR_INVALID_ARG;
+    if (!(f >= 1.f) || !(f < 3.0e38f) || max_swaps < 0 || max_swaps > 100000)
+        return GDN_ERR_INVALID_ARG;
+    if (H == 0) return GDN_OK;
+    if (!G || !idx) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {G, idx, rho_max, swaps};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    return from_cuda(gdn::launch_drrqr_select(G, H, n, k, f, max_swaps, idx, rho_max, swaps,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
                    float *stable_rank, int max_iter, float tol, void *stream) {
     if (BH < 0 || V < 1 || K < 1 || V > 128 || K > 128) return GDN_ERR_INVALID_ARG;
@@ -314,6 +354,7 @@ int gdn_get_last_device_status(void *stream) {
     if (word & gdn::kStatusTimeout) return GDN_ERR_TIMEOUT;
     if (word & gdn::kStatusBounds) return GDN_ERR_DEVICE_BOUNDS;
     if (word & gdn::kStatusNotConverged) return GDN_WARN_NOT_CONVERGED;
+    if (word & gdn::kStatusRankDeficient) return GDN_WARN_RANK_DEFICIENT;
     if (word & gdn::kStatusZeroState) return GDN_WARN_ZERO_STATE;
     return GDN_OK;
 }

@@ -12,7 +12,13 @@
 namespace gdn {
 
 // Bits of the per-device status word (see gdn_get_last_device_status).
-enum : int { kStatusTimeout = 1, kStatusBounds = 2, kStatusZeroState = 4, kStatusNotConverged = 8 };
+enum : int {
+    kStatusTimeout = 1,
+    kStatusBounds = 2,
+    kStatusZeroState = 4,
+    kStatusNotConverged = 8,
+    kStatusRankDeficient = 16
+};
 
 // Chunk length of the chunkwise prefill.
 constexpr int kChunk = 64;
@@ -84,6 +90,15 @@ cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, con
 // Rank-r truncation (and singular values) of BH states [V, K] by one-sided Jacobi.
 cudaError_t launch_state_truncate(float *S, int BH, int V, int K, int r, float *sigma,
                                   int max_sweeps, cudaStream_t stream);
+
+// DRRQR channel selection: calibration Gram on the tensor cores (K = 128,
+// bf16; workspace H * gram_splits * 64 KiB) and the per-head selection.
+int gram_splits(int B, int T, int H);
+cudaError_t launch_channel_gram(const void *k, const void *q, int B, int T, int H, float *G,
+                                void *workspace, cudaStream_t stream);
+size_t drrqr_select_smem(int n, int k);
+cudaError_t launch_drrqr_select(const float *G, int H, int n, int k, float f, int max_swaps,
+                                int *idx, float *rho, int *swaps, cudaStream_t stream);
 
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }

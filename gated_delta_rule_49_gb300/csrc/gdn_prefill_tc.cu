@@ -801,6 +801,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static bool tried = false;
@@ -831,6 +833,8 @@ bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int Ts, int H
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
+
+namespace {
 
 // Start states of the later segments: S_1 = E (end of segment 0) and
 // S_{p+1} = S_p M_p + H_p, in float32.  Rows of the state are independent, so

@@ -197,4 +197,11 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 }  // namespace sm100
+
+// Host: tensor map of a [B, Ts, H, C] bf16 tensor viewed as 4-D (C, H, T, B)
+// (first T tokens of each batch entry) with 64 x 1 x 64 x 1 boxes and the
+// 128-byte swizzle.  Returns false if the driver entry point is missing or
+// the encoder rejects the arguments.
+bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int Ts, int H, int C);
+
 }  // namespace gdn

@@ -21,6 +21,9 @@ input-dependent decay):
   gated       the prefill shapes under the channel-gated rules (KDA, GDN2):
               per-key-channel decay, and for GDN2 per-channel erase / write
               gates
+  calibration key/query activations for channel selection: per-head
+              channel scales and a shared low-rank channel mixing, then
+              per-token L2 normalisation
 
 Random streams: numpy PCG64.  The tiny workload uses seed ``seed`` directly;
 the others use child ``i`` of ``SeedSequence(seed)`` (prefill and
@@ -34,7 +37,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-WORKLOADS = ("tiny", "prefill", "pruned", "decode", "long", "gated")
+WORKLOADS = ("tiny", "prefill", "pruned", "decode", "long", "gated", "calibration")
 
 
 def round_to_bf16(x) -> np.ndarray:
@@ -262,6 +265,29 @@ def make_channel_gated(seed=0, B=8, T=4096, H=16, K=128, V=128, dtype="bf16", ga
                         _round(v, dtype), alpha,
                         None if beta is None else beta.astype(np.float32), bg, wg, S0,
                         {"seed": seed})
+
+
+def make_calibration(seed=0, B=8, T=4096, H=16, K=128, rank=16, dtype="bf16"):
+    """Calibration activations (k, q) [B, T, H, K] for channel selection.
+    Per head: channel scales s_c ~ LogNormal(0, 0.5^2) and a mixing
+    L ~ N(0, 1/rank) of shape [K, rank] shared by keys and queries; a token is
+    x = s (.) (g + 1.5 L w), g ~ N(0, I_K), w ~ N(0, I_rank), then L2-normalised,
+    so that channels differ in energy and are correlated (the structure a
+    channel selector has to see; i.i.d. channels would make every subset
+    equivalent)."""
+    rng = _stream(seed, 6)
+    s = rng.lognormal(0.0, 0.5, size=(H, K))
+    L = rng.standard_normal((H, K, rank)) / np.sqrt(rank)
+
+    def draw():
+        g = rng.standard_normal((B, T, H, K))
+        w = rng.standard_normal((B, T, H, rank))
+        x = s[None, None] * (g + 1.5 * np.einsum("hkr,bthr->bthk", L, w))
+        return _round(_unit_rows(x), dtype)
+
+    k = draw()
+    q = draw()
+    return k, q
 
 
 def take_gated_sequences(p: GatedProblem, b_idx, h_idx) -> GatedProblem:

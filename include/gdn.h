@@ -60,7 +60,8 @@ typedef enum {
     GDN_ERR_WORKSPACE = -6,     /* workspace missing or smaller than required */
     GDN_ERR_DEVICE_BOUNDS = -7, /* device status: a kernel's own index check failed */
     GDN_WARN_ZERO_STATE = 1,    /* device status: gdn_state_rank saw an all-zero state */
-    GDN_WARN_NOT_CONVERGED = 2  /* device status: gdn_state_truncate hit max_sweeps */
+    GDN_WARN_NOT_CONVERGED = 2, /* device status: gdn_state_truncate hit max_sweeps */
+    GDN_WARN_RANK_DEFICIENT = 3 /* device status: gdn_drrqr_select saw rank(M) < k */
 } gdn_status;
 
 typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
@@ -279,9 +280,52 @@ GDN_API int gdn_prefill_truncated(const void *q, const void *k, const void *v,
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * DRRQR channel selection ("On State Reduction in Linear Attention" notes,
+ * Sec. 2.8): pick d_k' = k of the d_k = n key/query channels of every head so
+ * that the kept columns of the calibration matrix M_h = [K_cal; Q_cal]
+ * (tokens as rows) form a well-conditioned basis.
+ *
+ * gdn_channel_gram -- G_h = K_h^T K_h + Q_h^T Q_h = M_h^T M_h (the QR's R
+ *   satisfies R^T R = G), summed over the calibration tokens on the tensor
+ *   cores:  k, q [B, T, H, 128] bf16 (the activations as the layer feeds them
+ *   to the recurrence);  G [H, 128, 128] float32 output.  Needs a workspace of
+ *   gdn_channel_gram_workspace_size(B, T, H, K) bytes.  Only K = 128 and bf16
+ *   (GDN_ERR_UNSUPPORTED otherwise).  B * T = 0 gives G = 0.
+ */
+GDN_API size_t gdn_channel_gram_workspace_size(int B, int T, int H, int K);
+GDN_API int gdn_channel_gram(const void *k, const void *q, int B, int T, int H, int K,
+                             gdn_dtype dtype, float *G, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_drrqr_select -- per head, column-pivoted QR of M (through the pivoted
+ *   Cholesky factorisation of G) for the initial permutation, then
+ *   strong-RRQR swaps of a kept and a candidate channel while
+ *   max rho_ij = sqrt(U_ij^2 + (gamma_j / omega_i)^2) > f, with U = A_k^{-1} B_k,
+ *   omega_i = 1 / |row i of A_k^{-1}|, gamma_j = |column j of C_k|.
+ *
+ *   G [H, n, n] float32 (from gdn_channel_gram, or any symmetric PSD matrix)
+ *   2 <= n <= 128, 1 <= k < n;  f >= 1;  0 <= max_swaps
+ *   idx [H, k] int32 output: the kept channels in selection order
+ *   rho_max [H] float32 (final max rho) and swaps [H] int32, each optional
+ *
+ * At the end every rho_ij <= f (unless max_swaps stopped it), which gives the
+ * notes' bounds with c_f = sqrt(1 + f^2 k (n - k)).  If rank(M) < k (a pivot of
+ * G below 1e-6 of its largest diagonal entry, i.e. sigma_k below about 1e-3
+ * sigma_1) the greedy choice is returned without swaps and
+ * GDN_WARN_RANK_DEFICIENT is set.
+ * Computed in float32: near-ties (equal pivots or rho values) may be broken
+ * differently from a float64 computation; any such result satisfies the same
+ * stopping test to float32 accuracy.
+ */
+GDN_API int gdn_drrqr_select(const float *G, int H, int n, int k, float f, int max_swaps,
+                             int *idx, float *rho_max, int *swaps, void *stream);
+
+/*
  * gdn_get_last_device_status -- synchronise `stream`, then read and clear the
  * current device's status word.  Returns GDN_OK, GDN_ERR_TIMEOUT,
- * GDN_ERR_DEVICE_BOUNDS, GDN_WARN_NOT_CONVERGED or GDN_WARN_ZERO_STATE (warnings
+ * GDN_ERR_DEVICE_BOUNDS, GDN_WARN_NOT_CONVERGED, GDN_WARN_RANK_DEFICIENT or
+ * GDN_WARN_ZERO_STATE (warnings
  * only when no error is set) or
  * GDN_ERR_CUDA if the synchronisation itself failed.
  */

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 1, 2, 3):
         s = binding.status_string(code)
         assert s and s != "unknown status"
     assert binding.status_string(12345) == "unknown status"
@@ -205,3 +205,36 @@ def test_truncation_rejects_bad_arguments(lib):
     assert pre(be=None) == binding.GDN_ERR_INVALID_ARG
     assert pre(o=F + 2) == binding.GDN_ERR_ALIGNMENT
     assert pre(H=0) == binding.GDN_OK
+
+
+def test_drrqr_rejects_bad_arguments(lib):
+    F = FAKE
+    ws = binding.gdn_channel_gram_workspace_size(8, 4096, 16, 128)
+    assert ws > 0 and binding.gdn_channel_gram_workspace_size(8, 4096, 16, 64) == 0
+    g = lambda **kw: lib.gdn_channel_gram(kw.get("k", F), kw.get("q", F), kw.get("B", 8),  # noqa: E731
+                                          kw.get("T", 4096), kw.get("H", 16), kw.get("K", 128),
+                                          kw.get("dt", 0), kw.get("G", F), kw.get("ws", F),
+                                          kw.get("wsb", ws), None)
+    assert g(K=64) == binding.GDN_ERR_UNSUPPORTED
+    assert g(dt=1) == binding.GDN_ERR_UNSUPPORTED
+    assert g(dt=4) == binding.GDN_ERR_INVALID_ARG
+    assert g(G=None) == binding.GDN_ERR_INVALID_ARG
+    assert g(k=F + 2) == binding.GDN_ERR_ALIGNMENT
+    assert g(wsb=ws - 1) == binding.GDN_ERR_WORKSPACE
+    assert g(ws=None) == binding.GDN_ERR_WORKSPACE
+    assert g(H=0) == binding.GDN_OK
+
+    def sel(**kw):
+        a = dict(G=F, H=16, n=128, k=64, f=2.0, sw=100, idx=F)
+        a.update(kw)
+        return lib.gdn_drrqr_select(a["G"], a["H"], a["n"], a["k"], ctypes.c_float(a["f"]),
+                                    a["sw"], a["idx"], None, None, None)
+    assert sel(k=128) == binding.GDN_ERR_INVALID_ARG
+    assert sel(k=0) == binding.GDN_ERR_INVALID_ARG
+    assert sel(n=129) == binding.GDN_ERR_INVALID_ARG
+    assert sel(f=0.5) == binding.GDN_ERR_INVALID_ARG
+    assert sel(f=float("nan")) == binding.GDN_ERR_INVALID_ARG
+    assert sel(sw=-1) == binding.GDN_ERR_INVALID_ARG
+    assert sel(idx=None) == binding.GDN_ERR_INVALID_ARG
+    assert sel(G=F + 4) == binding.GDN_ERR_ALIGNMENT
+    assert sel(H=0) == binding.GDN_OK
