@@ -226,7 +226,13 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
     status = binding.gdn_get_last_device_status()
 
     extra = {}
-    if not args.quick:
+    SECTIONS = ("pruned", "prologue", "state_rank", "truncation", "drrqr", "long_context",
+                "gated", "decode")
+
+    def want(name):
+        return not args.quick and (args.only is None or args.only == name)
+
+    if want("pruned") or want("prologue"):
         # ---- pruned d_k' = 64, same draws ----
         pp = inputs.make_prefill(B=B, T=T, H=H, K=K, V=V, pruned_K=64)
         dp = problem_to_dev(pp, torch)
@@ -236,26 +242,29 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
             binding.gdn_prefill(dp["q"], dp["k"], dp["v"], dp["alpha"], dp["beta"], None, o, STp,
                                 B, T, H, 64, V, binding.GDN_BF16)
 
-        t64, per64 = time_calls(step64, args.steps, args.warmup, torch, barrier)
-        t64 = max_over_ranks(t64)
-        k64 = statistics.mean(per64)
-        extra["pruned_dk64"] = {
-            "tokens_per_s": B * T * world * args.steps / (t64 / 1e3),
-            "ms_per_step": t64 / args.steps,
-            "speedup_vs_dk128": (total_ms / args.steps) / (t64 / args.steps),
-            "achieved_gbs": prefill_bytes(B, T, H, 64, V) / (k64 / 1e3) / 1e9,
-            "achieved_tflops": prefill_flops(B, T, H, 64, V) / (k64 / 1e3) / 1e12,
-        }
-        extra["pruned_dk64"]["hbm_frac"] = extra["pruned_dk64"]["achieved_gbs"] / peaks["hbm_gbs"]
+        if want("pruned"):
+            t64, per64 = time_calls(step64, args.steps, args.warmup, torch, barrier)
+            t64 = max_over_ranks(t64)
+            k64 = statistics.mean(per64)
+            extra["pruned_dk64"] = {
+                "tokens_per_s": B * T * world * args.steps / (t64 / 1e3),
+                "ms_per_step": t64 / args.steps,
+                "speedup_vs_dk128": (total_ms / args.steps) / (t64 / args.steps),
+                "achieved_gbs": prefill_bytes(B, T, H, 64, V) / (k64 / 1e3) / 1e9,
+                "achieved_tflops": prefill_flops(B, T, H, 64, V) / (k64 / 1e3) / 1e12,
+            }
+            extra["pruned_dk64"]["hbm_frac"] = (extra["pruned_dk64"]["achieved_gbs"] /
+                                                peaks["hbm_gbs"])
 
         # ---- pruning prologue from the full-width q/k of the headline run ----
-        idx = torch.from_numpy(pp.meta["kept_channels"].astype(np.int32)).cuda()
-        extra["prologue"] = bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier,
-                                           max_over_ranks, world)
-        d_head = d
+        if want("prologue"):
+            idx = torch.from_numpy(pp.meta["kept_channels"].astype(np.int32)).cuda()
+            extra["prologue"] = bench_prologue(args, torch, binding, d, idx, dp, o, peaks,
+                                               barrier, max_over_ranks, world)
         del dp, pp
 
-        # ---- stable-rank epilogue on the final states of the headline run ----
+    # ---- stable-rank epilogue on the final states of the headline run ----
+    if want("state_rank"):
         f2 = torch.empty(B * H, device="cuda")
         s1 = torch.empty_like(f2)
         er = torch.empty_like(f2)
@@ -267,25 +276,31 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         extra["state_rank"] = {"ms_per_call": tr / 5, "states": B * H,
                                "median_er": float(er.median().item())}
 
-        # ---- rank-r truncation: the headline's final states, and the segmented prefill ----
-        extra["truncation"] = bench_truncation(args, torch, binding, d_head, ST, barrier,
+    # ---- rank-r truncation: the headline's final states, and the segmented prefill ----
+    if want("truncation"):
+        extra["truncation"] = bench_truncation(args, torch, binding, d, ST, barrier,
                                                max_over_ranks, world)
 
-        # ---- DRRQR channel selection (calibration Gram + selection) ----
+    # ---- DRRQR channel selection (calibration Gram + selection) ----
+    if want("drrqr"):
         extra["drrqr"] = bench_drrqr(args, torch, binding, inputs, peaks, barrier,
                                      max_over_ranks)
 
-        # ---- long-context prefill: B=1, T=65536, H=16 (segment-parallel) ----
+    # ---- long-context prefill: B=1, T=65536, H=16 (segment-parallel) ----
+    if want("long_context"):
         extra["long_context"] = bench_long(args, torch, binding, inputs, peaks, barrier,
                                            max_over_ranks, world)
 
-        # ---- channel-gated rules (KDA, GDN2) on the prefill shapes ----
+    # ---- channel-gated rules (KDA, GDN2) on the prefill shapes ----
+    if want("gated"):
         extra["gated"] = bench_gated(args, torch, binding, inputs, peaks, barrier,
                                      max_over_ranks, world)
 
-        # ---- decode: B = 64 and 1, d_k 128 and 64 ----
+    # ---- decode: B = 64 and 1, d_k 128 and 64 ----
+    if want("decode"):
         extra["decode"] = bench_decode(args, torch, binding, inputs, peaks, props, barrier,
                                        max_over_ranks)
+    assert args.only is None or args.only in SECTIONS
 
     clocks = sampler.stop()
 
@@ -773,6 +788,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline prefill only")
+    ap.add_argument("--only", default=None,
+                    choices=["pruned", "prologue", "state_rank", "truncation", "drrqr",
+                             "long_context", "gated", "decode"],
+                    help="headline prefill plus this one section (e.g. for a profiler run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=None)
     ap.add_argument("--decode-reps", type=int, default=20)

@@ -11,15 +11,17 @@
 // lanes and nothing is exchanged between rows.
 //
 // Prefill: a CTA owns R rows of one (b, h) sequence; a row is spread over
-// K/8 lanes holding 8 channels each in registers.  The per-token operands
-// (k, q, the channel gates, and the CTA's slice of v / w) are staged 16
-// tokens at a time into a two-stage shared-memory ring by cp.async, so the
-// loads of block n+1 are in flight while block n is processed.  Per token and
-// row: decay, one dot product (the erase read) reduced across the row's
-// lanes, the rank-one write, then o = S q (a second reduction, off the
-// recurrence's critical path); outputs are collected per block in shared
-// memory and written with 16-byte stores.  Bound: CUDA-core issue (about 25
-// warp instructions per row-token); see the measurement notes.
+// K/8 lanes holding 8 channels each in registers, and every lane holds
+// four rows, so that the per-token operands it reads from shared memory
+// (k, q, the channel decay, the erase direction) serve all of them.  The
+// per-token operands and the CTA's slice of v / w are staged 8 tokens at a
+// time into a two-stage shared-memory ring by cp.async (block n+1 in flight
+// while block n is processed); bf16 k / q are converted to float32 once per
+// CTA.  Per token and row: decay, the erase read p = s~ . e and r = s~ . q
+// (reduced together over the row's lanes), the rank-one write, and
+// o = r + u (k . q); the state arithmetic runs on packed float2 FMA.  Outputs are collected per block in
+// shared memory and written with 16-byte stores.  Bound: shared-memory
+// wavefronts and instruction issue together.
 //
 // Decode: the layout of the plain decode step (K/4 lanes per row, four rows
 // per lane, all state loads issued first); HBM-bound on the state.
@@ -30,8 +32,7 @@ namespace {
 
 enum GateMode : int { kScalar = GDN_GATE_SCALAR, kKda = GDN_GATE_KDA, kGdn2 = GDN_GATE_GDN2 };
 
-constexpr int kTB = 16;  // tokens per staged block
-constexpr int kE = 8;    // state channels per lane (prefill)
+constexpr int kTB = 8;   // tokens per staged block
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -48,22 +49,24 @@ __device__ __forceinline__ void cp_async_wait_all_but_one() {
     asm volatile("cp.async.wait_group 1;\n" ::: "memory");
 }
 
-// Eight consecutive values (shared or global memory, 16-byte aligned) as float.
-__device__ __forceinline__ void ld8(const float *p, float *x) {
-    const float4 a = *reinterpret_cast<const float4 *>(p);
-    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float *x) {
-    const uint4 r = *reinterpret_cast<const uint4 *>(p);
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
+// The CPL channels a lane holds: CPL/4 float4 pieces at channel offsets
+// 4 cl + 4 LPR j, so the LPR lanes of a row read 16 LPR contiguous floats per
+// piece (conflict-free shared-memory reads).  As float2 pairs: x[CPL / 2].
+template <int LPR, int CPL>
+__device__ __forceinline__ void ldc(const float *row, int cl, float2 (&x)[CPL / 2]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
+    for (int j = 0; j < CPL / 4; ++j) {
+        const float4 v = *reinterpret_cast<const float4 *>(row + 4 * cl + 4 * LPR * j);
+        x[2 * j] = make_float2(v.x, v.y);
+        x[2 * j + 1] = make_float2(v.z, v.w);
     }
+}
+template <int LPR, int CPL>
+__device__ __forceinline__ void stc(float *row, int cl, const float2 (&x)[CPL / 2]) {
+#pragma unroll
+    for (int j = 0; j < CPL / 4; ++j)
+        *reinterpret_cast<float4 *>(row + 4 * cl + 4 * LPR * j) =
+            make_float4(x[2 * j].x, x[2 * j].y, x[2 * j + 1].x, x[2 * j + 1].y);
 }
 
 template <int L>
@@ -73,21 +76,24 @@ __device__ __forceinline__ float group_sum(float x) {
     return x;
 }
 
-// Shared-memory layout of one stage (byte offsets, all multiples of 16).
+// Shared-memory layout (byte offsets, all multiples of 16): two stages of raw
+// per-token operands, the current block's k/q as float32, and the outputs.
 template <int K, int R, typename Tin, int GATE>
 struct GatedStage {
+    static constexpr bool kBf = sizeof(Tin) == 2;
     static constexpr int KA = GATE == kScalar ? 4 : K;  // floats of alpha per token
     static constexpr int KQ = 0;                                           // [kTB][2][K] Tin
     static constexpr int AL = KQ + kTB * 2 * K * (int)sizeof(Tin);          // [kTB][KA] f32
     static constexpr int BG = AL + kTB * KA * 4;                            // [kTB][K] f32
     static constexpr int BE = BG + (GATE == kGdn2 ? kTB * K * 4 : 0);       // [kTB] f32
-    static constexpr int VV = BE + kTB * 4;                                 // [kTB][R] Tin
+    static constexpr int VV = BE + (kTB * 4 + 15) / 16 * 16;                // [kTB][R] Tin
     static constexpr int WW = VV + kTB * R * (int)sizeof(Tin);              // [kTB][R] f32
     static constexpr int BYTES = WW + (GATE == kGdn2 ? kTB * R * 4 : 0);
-    static constexpr int OB = 2 * BYTES;                                    // [kTB][R] Tin
+    static constexpr int KQF = 2 * BYTES;                                   // [kTB][2][K] f32
+    static constexpr int OB = KQF + (kBf ? kTB * 2 * K * 4 : 0);            // [kTB][R] Tin
     static constexpr int SMEM = OB + kTB * R * (int)sizeof(Tin);
     static_assert(AL % 16 == 0 && BG % 16 == 0 && VV % 16 == 0 && WW % 16 == 0 &&
-                      BYTES % 16 == 0,
+                      BYTES % 16 == 0 && KQF % 16 == 0 && OB % 16 == 0,
                   "16-byte aligned regions");
 };
 
@@ -144,17 +150,25 @@ __device__ __forceinline__ void stage_block(unsigned char *st, const Tin *q, con
     }
 }
 
-// grid: B*H*(V/R) CTAs of (R / RPI) warps; CTA x -> sequence x / (V/R), slab x % (V/R).
-template <int K, int R, typename Tin, int GATE>
-__global__ void __launch_bounds__(256)
+// grid: B*H*(V/R) CTAs; CTA x -> sequence x / (V/R), slab x % (V/R).  A row's
+// K channels sit on K / CPL lanes (CPL each); a warp holds RPI * RPL rows:
+// lane group g holds rows w RPI RPL + rr RPI + g, rr < RPL, so the per-token
+// operands a lane loads (k, q, the channel decay, the erase direction) serve
+// RPL rows.  Per token and row the two dot products p = s~ . e and
+// r = s~ . q of the decayed state are reduced together, then
+// u = (write) - p, s = s~ + u k and o = r + u (k . q), k . q being shared by
+// all rows.
+template <int K, int R, int CPL, int RPL, typename Tin, int GATE>
+__global__ void __launch_bounds__(128)
     prefill_gated_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                          const Tin *__restrict__ v, const float *__restrict__ alpha,
                          const float *__restrict__ beta, const float *__restrict__ bg,
                          const float *__restrict__ wg, const float *__restrict__ S0,
                          Tin *__restrict__ o, float *__restrict__ ST, int T, int H, int V) {
     using L = GatedStage<K, R, Tin, GATE>;
-    constexpr int LPR = K / kE;  // lanes per row
+    constexpr int LPR = K / CPL;  // lanes per row
     constexpr int RPI = 32 / LPR;
+    constexpr int NP = CPL / 2;   // float2 pairs per lane
     constexpr int EPC = 16 / (int)sizeof(Tin);
     extern __shared__ __align__(16) unsigned char smem[];
 
@@ -164,15 +178,19 @@ __global__ void __launch_bounds__(256)
     const int b = seq / H, h = seq % H;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane / LPR, cl = lane % LPR;
-    const int row = warp * RPI + g;  // within the slab
-    const size_t srow = ((size_t)seq * V + r0 + row) * K + cl * kE;
-
-    float s[kE];
-    if (S0) {
-        ld8(S0 + srow, s);
-    } else {
+    int row[RPL];
 #pragma unroll
-        for (int e = 0; e < kE; ++e) s[e] = 0.f;
+    for (int rr = 0; rr < RPL; ++rr) row[rr] = (warp * RPL + rr) * RPI + g;  // within the slab
+
+    float2 s[RPL][NP];
+#pragma unroll
+    for (int rr = 0; rr < RPL; ++rr) {
+        if (S0) {
+            ldc<LPR, CPL>(S0 + ((size_t)seq * V + r0 + row[rr]) * K, cl, s[rr]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < NP; ++e) s[rr][e] = make_float2(0.f, 0.f);
+        }
     }
 
     const int nblk = (T + kTB - 1) / kTB;
@@ -192,55 +210,83 @@ __global__ void __launch_bounds__(256)
         cp_async_wait_all_but_one();
         __syncthreads();
         const unsigned char *st = smem + (n & 1) * L::BYTES;
-        const Tin *kq = reinterpret_cast<const Tin *>(st + L::KQ);
+        const int nt = min(kTB, T - t0);
+        const float *kqf;
+        if constexpr (L::kBf) {  // this block's k and q as float32, once per CTA
+            const __nv_bfloat162 *src = reinterpret_cast<const __nv_bfloat162 *>(st + L::KQ);
+            float2 *dst = reinterpret_cast<float2 *>(smem + L::KQF);
+            for (int e = threadIdx.x; e < nt * K; e += blockDim.x)
+                dst[e] = __bfloat1622float2(src[e]);
+            __syncthreads();
+            kqf = reinterpret_cast<const float *>(smem + L::KQF);
+        } else {
+            kqf = reinterpret_cast<const float *>(st + L::KQ);
+        }
         const float *al = reinterpret_cast<const float *>(st + L::AL);
         const float *bgs = reinterpret_cast<const float *>(st + L::BG);
         const float *bes = reinterpret_cast<const float *>(st + L::BE);
         const Tin *vv = reinterpret_cast<const Tin *>(st + L::VV);
         const float *ww = reinterpret_cast<const float *>(st + L::WW);
-        const int nt = min(kTB, T - t0);
         for (int tau = 0; tau < nt; ++tau) {
-            float kk[kE], qq[kE], ee[kE];
-            ld8(kq + (tau * 2) * K + cl * kE, kk);
-            ld8(kq + (tau * 2 + 1) * K + cl * kE, qq);
+            float2 kk[NP], qq[NP], ee[NP], aa[NP];
+            ldc<LPR, CPL>(kqf + (tau * 2) * K, cl, kk);
+            ldc<LPR, CPL>(kqf + (tau * 2 + 1) * K, cl, qq);
             if constexpr (GATE == kScalar) {
                 const float a = al[tau * L::KA];
 #pragma unroll
-                for (int e = 0; e < kE; ++e) s[e] *= a;
+                for (int e = 0; e < NP; ++e) aa[e] = make_float2(a, a);
             } else {
-                float aa[kE];
-                ld8(al + tau * K + cl * kE, aa);
-#pragma unroll
-                for (int e = 0; e < kE; ++e) s[e] *= aa[e];
+                ldc<LPR, CPL>(al + tau * K, cl, aa);
             }
             if constexpr (GATE == kGdn2) {
-                ld8(bgs + tau * K + cl * kE, ee);
+                ldc<LPR, CPL>(bgs + tau * K, cl, ee);
 #pragma unroll
-                for (int e = 0; e < kE; ++e) ee[e] *= kk[e];
+                for (int e = 0; e < NP; ++e) ee[e] = __fmul2_rn(ee[e], kk[e]);
             } else {
 #pragma unroll
-                for (int e = 0; e < kE; ++e) ee[e] = kk[e];
+                for (int e = 0; e < NP; ++e) ee[e] = kk[e];
             }
-            float p = 0.f;
+            float2 kq2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < kE; ++e) p = fmaf(s[e], ee[e], p);
-            p = group_sum<LPR>(p);
-            const float vi = to_f32(vv[tau * R + row]);
-            float u;
-            if constexpr (GATE == kGdn2)
-                u = ww[tau * R + row] * vi - p;
-            else
-                u = bes[tau] * (vi - p);
-            float r = 0.f;
+            for (int e = 0; e < NP; ++e) kq2 = __ffma2_rn(kk[e], qq[e], kq2);
+            float kq = kq2.x + kq2.y;
+            float p[RPL], r[RPL];
 #pragma unroll
-            for (int e = 0; e < kE; ++e) {
-                s[e] = fmaf(u, kk[e], s[e]);
-                r = fmaf(s[e], qq[e], r);
+            for (int rr = 0; rr < RPL; ++rr) {
+                float2 p2 = make_float2(0.f, 0.f), r2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < NP; ++e) {
+                    s[rr][e] = __fmul2_rn(s[rr][e], aa[e]);
+                    p2 = __ffma2_rn(s[rr][e], ee[e], p2);
+                    r2 = __ffma2_rn(s[rr][e], qq[e], r2);
+                }
+                p[rr] = p2.x + p2.y;
+                r[rr] = r2.x + r2.y;
             }
-            r = group_sum<LPR>(r);
-            if (cl == 0) ob[tau * R + row] = from_f32<Tin>(r);
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) {
+                kq += __shfl_xor_sync(0xffffffffu, kq, off);
+#pragma unroll
+                for (int rr = 0; rr < RPL; ++rr) {
+                    p[rr] += __shfl_xor_sync(0xffffffffu, p[rr], off);
+                    r[rr] += __shfl_xor_sync(0xffffffffu, r[rr], off);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < RPL; ++rr) {
+                const float vi = to_f32(vv[tau * R + row[rr]]);
+                float u;
+                if constexpr (GATE == kGdn2)
+                    u = ww[tau * R + row[rr]] * vi - p[rr];
+                else
+                    u = bes[tau] * (vi - p[rr]);
+                const float2 u2 = make_float2(u, u);
+#pragma unroll
+                for (int e = 0; e < NP; ++e) s[rr][e] = __ffma2_rn(u2, kk[e], s[rr][e]);
+                if (cl == 0) ob[tau * R + row[rr]] = from_f32<Tin>(fmaf(u, kq, r[rr]));
+            }
         }
-        __syncthreads();  // outputs complete; stage n & 1 free for block n + 2
+        __syncthreads();  // outputs complete; stage n & 1 (and the float32 k/q) free
         if (o) {
             constexpr int nO = R / EPC;
             for (int j = threadIdx.x; j < nt * nO; j += blockDim.x) {
@@ -250,22 +296,22 @@ __global__ void __launch_bounds__(256)
             }
         }
     }
-    if (ST) {
-        float4 *dst = reinterpret_cast<float4 *>(ST + srow);
-        dst[0] = make_float4(s[0], s[1], s[2], s[3]);
-        dst[1] = make_float4(s[4], s[5], s[6], s[7]);
-    }
+    if (ST)
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr)
+            stc<LPR, CPL>(ST + ((size_t)seq * V + r0 + row[rr]) * K, cl, s[rr]);
 }
 
-template <int K, int R, typename Tin, int GATE>
+template <int K, int R, int CPL, int RPL, typename Tin, int GATE>
 cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *alpha,
                       const float *beta, const float *bg, const float *wg, const float *S0,
                       void *o, float *ST, int B, int T, int H, int V, cudaStream_t stream) {
     using L = GatedStage<K, R, Tin, GATE>;
-    constexpr int RPI = 32 / (K / kE);
-    constexpr int threads = (R / RPI) * 32;
-    static_assert(threads <= 256, "at most 8 warps");
-    auto kern = prefill_gated_kernel<K, R, Tin, GATE>;
+    constexpr int RPI = 32 / (K / CPL);
+    constexpr int threads = R / (RPI * RPL) * 32;
+    static_assert(threads >= 32 && threads <= 128 && R % (RPI * RPL) == 0, "tiling");
+    static_assert(CPL % 4 == 0 && K % CPL == 0 && 32 % (K / CPL) == 0, "channels per lane");
+    auto kern = prefill_gated_kernel<K, R, CPL, RPL, Tin, GATE>;
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -283,20 +329,24 @@ cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *
     return cudaGetLastError();
 }
 
+// (K, V) -> rows per CTA R, channels per lane CPL, rows per lane RPL:
+// (128, 128): 16 lanes x 8 channels per row, 4 rows per lane, 4 warps of 8
+// rows; (64, 128): 8 lanes x 8 channels, 4 rows per lane, 2 warps of 16 rows;
+// (32, 32): 4 lanes x 8 channels, 4 rows per lane, 1 warp of 32 rows.
 template <typename Tin, int GATE>
 cudaError_t pg_dispatch(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *bg, const float *wg, const float *S0,
                         void *o, float *ST, int B, int T, int H, int K, int V,
                         cudaStream_t stream) {
     if (K == 128 && V == 128)
-        return launch_pg<128, 16, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, V,
-                                             stream);
+        return launch_pg<128, 32, 16, 4, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T,
+                                                    H, V, stream);
     if (K == 64 && V == 128)
-        return launch_pg<64, 32, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, V,
-                                            stream);
+        return launch_pg<64, 32, 8, 4, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T,
+                                                  H, V, stream);
     if (K == 32 && V == 32)
-        return launch_pg<32, 32, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, V,
-                                            stream);
+        return launch_pg<32, 32, 8, 4, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T,
+                                                  H, V, stream);
     return cudaErrorInvalidValue;
 }
 
