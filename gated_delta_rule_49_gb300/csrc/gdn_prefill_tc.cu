@@ -523,20 +523,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                      sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
                     }
                     mma_commit(&bar_w);
-                    ok = wait(&bar_w, n & 1);
                 }
-                if (ok && !zero_v && n + 1 < nchunks) load_v(n + 1);  // V consumed
             }
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
             {
-                tc_fence_after();
-                if (quad_row < K) {
-                    float v[32];
-                    tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
-                    tmem_ld_wait();
-                    store_row<4>(sm + L::NW, quad_row, 4 * colhalf, v, -1.f);
-                }
-                // Q <- diag(gamma) Q in place (the q tile is read again only by S Q^T)
+                // Q <- diag(gamma) Q in place while the W / U~ products run (they
+                // read the K tile and T', T''; this chunk's [K;Q] K^T has finished;
+                // the q tile is read again only by S Q^T)
                 uint8_t *stq = sm + st * L::STAGE;
 #pragma unroll
                 for (int e = tid; e < (K / 64) * 512; e += kKeyThreads) {
@@ -552,6 +544,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         wv[c] = pack_bf16(f.x * g, f.y * g);
                     }
                     *p = w;
+                }
+            }
+            if (tid == 0) {
+                if (ok) ok = wait(&bar_w, n & 1);
+                if (ok && !zero_v && n + 1 < nchunks) load_v(n + 1);  // V consumed
+            }
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+            {
+                tc_fence_after();
+                if (quad_row < K) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
+                    tmem_ld_wait();
+                    store_row<4>(sm + L::NW, quad_row, 4 * colhalf, v, -1.f);
                 }
             }
             fence_proxy_async_smem();
