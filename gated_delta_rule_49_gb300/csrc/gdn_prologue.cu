@@ -6,23 +6,28 @@
 //
 // Memory-bound.  A random half of a row's channels touches every 32-byte
 // sector of it, so the row is read whole: the staged kernel moves a warp's
-// tile of consecutive rows (one contiguous block of up to 4 KB) with 16-byte
-// coalesced loads, all issued before any is used, parks it in the warp's own
-// shared-memory slot and gathers the kept channels from there; each output
+// tile of consecutive rows (one contiguous block of up to 4 KB) with one TMA
+// bulk copy into the warp's two-slot ring (the next tile in flight while one
+// is gathered; 64 KB per CTA keeps three CTAs per SM) and gathers the kept
+// channels from shared memory; each output
 // row is written by K_out/8 lanes with one 16-byte (bf16) or 32-byte (fp32)
 // store per lane.  Rows whose byte width is not a multiple of 16 take the
 // row-wise kernel (a warp per row, channel loads straight from global memory).
 // An index outside [0, K_in) is not read in either: it contributes 0 and sets
 // the device status's bounds bit.
 #include "gdn_internal.cuh"
+#include "gdn_sm100.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kRowsPerWarp = 4;
-constexpr int kTileBytes = 4096;                  // per warp
-constexpr int kChunksPerLane = kTileBytes / 16 / 32;
+constexpr int kTileBytes = 4096;                  // per warp and slot
+constexpr int kBulkStages = 2;                    // slots per warp
 constexpr int kStagedWarps = 8;
+constexpr long long kBulkSpin = 2000000000LL;     // ~1 s of SM clocks per wait
+constexpr size_t kStagedSmem =
+    (size_t)kStagedWarps * kBulkStages * kTileBytes + kStagedWarps * kBulkStages * 8;
 
 template <typename T, int LPR>
 __device__ __forceinline__ float group_sum(float x) {
@@ -46,8 +51,20 @@ __device__ __forceinline__ void store8(float *dst, const float *g, float inv) {
     reinterpret_cast<float4 *>(dst)[1] = make_float4(g[4] * inv, g[5] * inv, g[6] * inv, g[7] * inv);
 }
 
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            sm100::smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(sm100::smem_u32(bar))
+        : "memory");
+}
+
 // rows_per_tile = floor(4096 / row bytes) >= 1 consecutive rows per warp tile;
-// row bytes (K_in * sizeof(T)) is a multiple of 16 and at most 4096.
+// row bytes (K_in * sizeof(T)) is a multiple of 16 and at most 4096, so a
+// tile is one contiguous, 16-byte aligned block: lane 0 of each warp fetches
+// it with one bulk copy into the warp's ring of kBulkStages slots, completing
+// on the slot's mbarrier (every wait bounded).
 template <typename T, int KOUT>
 __global__ void __launch_bounds__(kStagedWarps * 32)
     gather_normalize_staged(const T *__restrict__ x, const int *__restrict__ idx,
@@ -56,35 +73,45 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
     constexpr int OPL = 8;            // outputs per lane
     constexpr int LPR = KOUT / OPL;   // lanes per output row
     constexpr int RPP = 32 / LPR;     // rows per gather pass
-    __shared__ __align__(16) uint4 tile[kStagedWarps][kTileBytes / 16];
+    extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    uint4 *mine = tile[warp];
-    const T *ts = reinterpret_cast<const T *>(mine);
-    const int row_chunks = Kin * (int)sizeof(T) / 16;
+    uint8_t *mine = smem + (size_t)warp * kBulkStages * kTileBytes;
+    uint64_t *mb = reinterpret_cast<uint64_t *>(smem + kStagedWarps * kBulkStages * kTileBytes) +
+                   warp * kBulkStages;
+    if (lane == 0) {
+        for (int s = 0; s < kBulkStages; ++s) sm100::mbar_init(&mb[s], 1);
+        sm100::fence_mbar_init();
+    }
+    __syncwarp();
+    const long long row_bytes = (long long)Kin * (long long)sizeof(T);
     const int sub = lane / LPR, cl = lane % LPR;
     const long long ntiles = (rows + rows_per_tile - 1) / rows_per_tile;
     const long long gw = (long long)blockIdx.x * kStagedWarps + warp;
     const long long nw = (long long)gridDim.x * kStagedWarps;
-    bool bad = false;
-    for (long long t = gw; t < ntiles; t += nw) {
-        const long long r0 = t * rows_per_tile;
+    const long long my_n = gw < ntiles ? (ntiles - gw + nw - 1) / nw : 0;  // this warp's tiles
+    auto issue = [&](long long i) {  // lane 0: tile gw + i nw into slot i mod kBulkStages
+        const long long r0 = (gw + i * nw) * rows_per_tile;
+        const long long nrows = min((long long)rows_per_tile, rows - r0);
+        const uint32_t bytes = (uint32_t)(nrows * row_bytes);
+        uint64_t *bar = &mb[i % kBulkStages];
+        sm100::fence_proxy_async_smem();  // earlier generic reads of the slot come first
+        sm100::mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(mine + (i % kBulkStages) * kTileBytes, x + r0 * Kin, bytes, bar);
+    };
+    if (lane == 0)
+        for (long long i = 0; i < my_n && i < kBulkStages; ++i) issue(i);
+    bool bad = false, ok = true;
+    long long i = 0;
+    for (; i < my_n; ++i) {
+        const int slot = (int)(i % kBulkStages);
+        if (!sm100::mbar_wait(&mb[slot], (uint32_t)((i / kBulkStages) & 1), kBulkSpin)) {
+            ok = false;
+            break;
+        }
+        const T *ts = reinterpret_cast<const T *>(mine + slot * kTileBytes);
+        const long long r0 = (gw + i * nw) * rows_per_tile;
         const int nrows = (int)min((long long)rows_per_tile, rows - r0);
-        const int nchunks = nrows * row_chunks;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + r0 * Kin);
-        uint4 buf[kChunksPerLane];
-#pragma unroll
-        for (int i = 0; i < kChunksPerLane; ++i) {
-            const int c = lane + 32 * i;
-            if (c < nchunks) buf[i] = __ldg(src + c);
-        }
-        __syncwarp();  // every lane is done reading the previous tile
-#pragma unroll
-        for (int i = 0; i < kChunksPerLane; ++i) {
-            const int c = lane + 32 * i;
-            if (c < nchunks) mine[c] = buf[i];
-        }
-        __syncwarp();
         const int npass = (nrows + RPP - 1) / RPP;
         for (int p = 0; p < npass; ++p) {
             const int rr = p * RPP + sub;
@@ -114,6 +141,14 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
             const float inv = 1.f / fmaxf(sqrtf(ss), eps);
             if (valid) store8(y + (r0 + rr) * KOUT + cl * OPL, g, inv);
         }
+        __syncwarp();  // every lane is done with this slot
+        if (lane == 0 && i + kBulkStages < my_n) issue(i + kBulkStages);
+    }
+    if (!ok) {
+        if (lane == 0 && status) atomicOr(status, kStatusTimeout);
+        // copies still in flight must land before the CTA's shared memory goes away
+        for (long long j = i; j < my_n && j < i + kBulkStages; ++j)
+            sm100::mbar_wait(&mb[j % kBulkStages], (uint32_t)((j / kBulkStages) & 1), kBulkSpin);
     }
     if (bad && status) atomicOr(status, kStatusBounds);
 }
@@ -176,9 +211,20 @@ cudaError_t launch_gn_t(const void *x, const int *idx, void *y, long long rows, 
         const int rpt = kTileBytes / row_bytes;
         const long long tiles = (rows + rpt - 1) / rpt;
         long long blocks = (tiles + kStagedWarps - 1) / kStagedWarps;
-        if (blocks > sms * 3) blocks = sms * 3;  // 76 registers x 256 threads: 3 CTAs per SM
+        if (blocks > sms * 3) blocks = sms * 3;  // 64 KB of slots: three CTAs per SM
         if (blocks < 1) blocks = 1;
-        gather_normalize_staged<T, KOUT><<<(unsigned)blocks, kStagedWarps * 32, 0, stream>>>(
+        auto kern = gather_normalize_staged<T, KOUT>;
+        static bool attr_set[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            return cudaErrorInvalidDevice;
+        if (!attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStagedSmem);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+        kern<<<(unsigned)blocks, kStagedWarps * 32, kStagedSmem, stream>>>(
             static_cast<const T *>(x), idx, static_cast<T *>(y), rows, H, Kin, rpt, eps,
             device_status_ptr());
         return cudaGetLastError();
