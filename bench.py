@@ -653,9 +653,11 @@ def bench_long(args, torch, binding, inputs, peaks, barrier, max_over_ranks, wor
             "stable_rank_per_head": [round(float(x), 3) for x in er.cpu()]}
 
 
-def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world):
-    """Same prefill through the C ABI with pinned HOST buffers: H2D of the
-    step's inputs, the call, D2H of o and S_T, all inside the timed region."""
+def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world, window=512):
+    """The same prefill through the C ABI on pinned HOST buffers
+    (gdn_prefill_host): every step copies its inputs host->device and o and
+    S_T device->host, pipelined with the recurrence over 512-token windows;
+    all of it inside the timed region."""
     B, T, H, K = p.k.shape
     V = p.v.shape[-1]
     from gated_delta_rule_49_gb300 import inputs
@@ -666,17 +668,12 @@ def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world):
     hb = torch.from_numpy(np.ascontiguousarray(p.beta)).pin_memory()
     ho = torch.empty((B, T, H, V), dtype=torch.bfloat16).pin_memory()
     hS = torch.empty((B, H, V, K), dtype=torch.float32).pin_memory()
-    dq, dk, dv = (torch.empty_like(x, device="cuda") for x in (hq, hk, hv))
-    da, db = torch.empty_like(ha, device="cuda"), torch.empty_like(hb, device="cuda")
-    do = torch.empty_like(ho, device="cuda")
-    dS = torch.empty_like(hS, device="cuda")
+    need = binding.gdn_prefill_host_workspace_size(B, T, H, K, V, binding.GDN_BF16, window)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
 
     def step():
-        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (da, ha), (db, hb)):
-            dst.copy_(src, non_blocking=True)
-        binding.gdn_prefill(dq, dk, dv, da, db, None, do, dS, B, T, H, K, V, binding.GDN_BF16)
-        ho.copy_(do, non_blocking=True)
-        hS.copy_(dS, non_blocking=True)
+        binding.gdn_prefill_host(hq, hk, hv, ha, hb, None, ho, hS, B, T, H, K, V,
+                                 binding.GDN_BF16, window, ws, need)
 
     steps = max(3, min(args.steps, 10))
     tot, _ = time_calls(step, steps, 2, torch, barrier)
@@ -684,7 +681,9 @@ def bench_e2e(p, torch, binding, args, barrier, max_over_ranks, world):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ha, hb))
     d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
     return {"value": B * T * world * steps / (tot / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "api": f"gdn_prefill_host, pinned host buffers, {window}-token windows",
+            "copy_gbs": (h2d + d2h) / (tot / steps / 1e3) / 1e9}
 
 
 # ----------------------------------------------------------------- oracle arm

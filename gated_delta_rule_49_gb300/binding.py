@@ -55,6 +55,8 @@ EXPORTS = (
     "gdn_channel_gram_workspace_size",
     "gdn_channel_gram",
     "gdn_drrqr_select",
+    "gdn_prefill_host_workspace_size",
+    "gdn_prefill_host",
 )
 
 _lock = threading.Lock()
@@ -115,6 +117,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_channel_gram.restype = i
         lib.gdn_drrqr_select.argtypes = [vp, i, i, i, f, i, vp, vp, vp, vp]
         lib.gdn_drrqr_select.restype = i
+        lib.gdn_prefill_host_workspace_size.argtypes = [i] * 7
+        lib.gdn_prefill_host_workspace_size.restype = sz
+        lib.gdn_prefill_host.argtypes = [vp] * 8 + [i] * 7 + [vp, sz, vp]
+        lib.gdn_prefill_host.restype = i
         lib.gdn_prefill_noalloc_max_workspace.argtypes = []
         lib.gdn_prefill_noalloc_max_workspace.restype = sz
         _lib = lib
@@ -326,6 +332,20 @@ def drrqr_select(G, k, f=2.0, max_swaps=1000, stream=None):
     sw = torch.empty(H, dtype=torch.int32, device=G.device)
     gdn_drrqr_select(G, H, n, k, f, max_swaps, idx, rho, sw, stream)
     return idx, rho, sw
+
+
+def gdn_prefill_host_workspace_size(B, T, H, K, V, dtype, window) -> int:
+    return int(load().gdn_prefill_host_workspace_size(B, T, H, K, V, dtype, window))
+
+
+def gdn_prefill_host(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, window, workspace,
+                     workspace_bytes, stream=None) -> int:
+    """Host-buffer prefill: q .. S_T are (pinned) CPU tensors or host addresses;
+    workspace is device memory."""
+    st = load().gdn_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                                 _ptr(o), _ptr(S_T), B, T, H, K, V, dtype, window,
+                                 _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(st, "gdn_prefill_host")
 
 
 def gather_normalize(x, idx, stream=None):

@@ -329,6 +329,32 @@ int gdn_drrqr_select(const float *G, int H, int n, int k, float f, int max_swaps
                                               static_cast<cudaStream_t>(stream)));
 }
 
+size_t gdn_prefill_host_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype,
+                                       int window) {
+    if (B <= 0 || T < 0 || H <= 0 || window < 1 || !supported_kv(K, V)) return 0;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return 0;
+    if ((long long)B * H > 0x7fffffffLL) return 0;
+    return gdn::host_layout(B, T, H, K, V, dtype, window).total;
+}
+
+int gdn_prefill_host(const void *q, const void *k, const void *v, const float *alpha,
+                     const float *beta, const float *S0, void *o, float *S_T, int B, int T, int H,
+                     int K, int V, gdn_dtype dtype, int window, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    if (B < 0 || T < 0 || H < 0 || K <= 0 || V <= 0 || window < 1) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!supported_kv(K, V)) return GDN_ERR_UNSUPPORTED;
+    if (!o && !S_T) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+    if ((long long)B * H == 0) return GDN_OK;
+    const size_t need = gdn_prefill_host_workspace_size(B, T, H, K, V, dtype, window);
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GDN_ERR_ALIGNMENT;
+    return from_cuda(gdn::launch_prefill_host(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
+                                              dtype, window, workspace,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
                    float *stable_rank, int max_iter, float tol, void *stream) {
     if (BH < 0 || V < 1 || K < 1 || V > 128 || K > 128) return GDN_ERR_INVALID_ARG;

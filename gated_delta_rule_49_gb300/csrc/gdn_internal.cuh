@@ -100,6 +100,18 @@ size_t drrqr_select_smem(int n, int k);
 cudaError_t launch_drrqr_select(const float *G, int H, int n, int k, float f, int max_swaps,
                                 int *idx, float *rho, int *swaps, cudaStream_t stream);
 
+// Prefill on host buffers, pipelined over windows of `window` tokens: byte
+// offsets of one window slot's device buffers (two slots), the float32 state
+// and the segment scratch inside the caller's device workspace.
+struct HostLayout {
+    size_t q, k, v, a, b, o, slot, state, seg, seg_bytes, total;
+};
+HostLayout host_layout(int B, int T, int H, int K, int V, gdn_dtype dt, int window);
+cudaError_t launch_prefill_host(const void *q, const void *k, const void *v, const float *alpha,
+                                const float *beta, const float *S0, void *o, float *ST, int B,
+                                int T, int H, int K, int V, gdn_dtype dt, int window,
+                                void *workspace, cudaStream_t stream);
+
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -175,6 +175,33 @@ GDN_API int gdn_decode_step_gathered(const void *q_full, const void *k_full, con
                                      int V, gdn_dtype dtype, void *stream);
 
 /*
+ * gdn_prefill_host -- gdn_prefill on HOST-resident buffers (pinned host
+ * memory for the copies to overlap; pageable memory works, serialised).
+ * The sequence axis is cut into windows of `window` tokens; the host->device
+ * copy of window w + 1, the prefill of window w (on `stream`, from the
+ * float32 state left by window w - 1) and the device->host copy of window
+ * w - 1's outputs run concurrently, on two internal copy streams and `stream`.
+ *
+ *   q, k, v, alpha, beta, S0, o, S_T: host pointers, same shapes and dtypes as
+ *     gdn_prefill (S0 may be NULL; o or S_T may be NULL, not both)
+ *   window: tokens per pipeline stage (>= 1; a multiple of 64 gives results
+ *     identical to gdn_prefill on device copies of the same inputs)
+ *   workspace: DEVICE memory of gdn_prefill_host_workspace_size(...) bytes,
+ *     16-byte aligned (two window slots, the state and the prefill's scratch)
+ *
+ * Asynchronous with respect to the host like every call here: the host
+ * buffers must stay valid, and the outputs are complete, once `stream` has
+ * reached the point after this call (cudaStreamSynchronize(stream)).
+ * Concurrent calls on one device are serialised while they enqueue.
+ */
+GDN_API size_t gdn_prefill_host_workspace_size(int B, int T, int H, int K, int V,
+                                               gdn_dtype dtype, int window);
+GDN_API int gdn_prefill_host(const void *q, const void *k, const void *v, const float *alpha,
+                             const float *beta, const float *S0, void *o, float *S_T, int B,
+                             int T, int H, int K, int V, gdn_dtype dtype, int window,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Gates of the channel-gated delta rules ("Linear Attention Architectures"
  * reading notes, Secs. 2.4-2.6).  Per token and head, S in R^{V x K}:
  *

@@ -238,3 +238,24 @@ def test_drrqr_rejects_bad_arguments(lib):
     assert sel(idx=None) == binding.GDN_ERR_INVALID_ARG
     assert sel(G=F + 4) == binding.GDN_ERR_ALIGNMENT
     assert sel(H=0) == binding.GDN_OK
+
+
+def test_host_prefill_rejects_bad_arguments(lib):
+    F = FAKE
+    need = binding.gdn_prefill_host_workspace_size(8, 4096, 16, 128, 128, 0, 512)
+    assert need > 0 and binding.gdn_prefill_host_workspace_size(8, 4096, 16, 96, 128, 0, 512) == 0
+
+    def call(**kw):
+        a = dict(q=F, k=F, v=F, al=F, be=F, S0=None, o=F, ST=F, B=8, T=4096, H=16, K=128, V=128,
+                 dt=0, w=512, ws=F, wsb=need)
+        a.update(kw)
+        return lib.gdn_prefill_host(a["q"], a["k"], a["v"], a["al"], a["be"], a["S0"], a["o"],
+                                    a["ST"], a["B"], a["T"], a["H"], a["K"], a["V"], a["dt"],
+                                    a["w"], a["ws"], a["wsb"], None)
+    assert call(w=0) == binding.GDN_ERR_INVALID_ARG
+    assert call(K=96) == binding.GDN_ERR_UNSUPPORTED
+    assert call(o=None, ST=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(be=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(wsb=need - 1) == binding.GDN_ERR_WORKSPACE
+    assert call(ws=F + 8) == binding.GDN_ERR_ALIGNMENT
+    assert call(B=0) == binding.GDN_OK
