@@ -227,7 +227,7 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
 
     extra = {}
     SECTIONS = ("pruned", "prologue", "state_rank", "truncation", "drrqr", "long_context",
-                "gated", "decode")
+                "gated", "fp32", "decode")
 
     def want(name):
         return not args.quick and (args.only is None or args.only == name)
@@ -295,6 +295,11 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
     if want("gated"):
         extra["gated"] = bench_gated(args, torch, binding, inputs, peaks, barrier,
                                      max_over_ranks, world)
+
+    # ---- all-fp32 mode on the prefill shapes ----
+    if want("fp32"):
+        extra["fp32"] = bench_fp32(args, torch, binding, inputs, peaks, barrier, max_over_ranks,
+                                   world)
 
     # ---- decode: B = 64 and 1, d_k 128 and 64 ----
     if want("decode"):
@@ -577,6 +582,33 @@ def bench_drrqr(args, torch, binding, inputs, peaks, barrier, max_over_ranks):
             "rho_max": float(rho.max().item())}
 
 
+def bench_fp32(args, torch, binding, inputs, peaks, barrier, max_over_ranks, world):
+    """All-fp32 mode: gdn_prefill with float32 q, k, v, o on the prefill
+    workload's shapes, and the tiny 32 x 32 workload (B=1, H=1, T=256)."""
+    out = {}
+    for name, p in (("prefill_shapes", inputs.make_prefill(dtype="fp32")),
+                    ("tiny_32x32", inputs.make_tiny())):
+        B, T, H, K = p.k.shape
+        V = p.v.shape[-1]
+        f = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda()  # noqa: E731
+        q, k, v, al, be = f(p.q), f(p.k), f(p.v), f(p.alpha), f(p.beta)
+        o = torch.empty((B, T, H, V), device="cuda")
+        ST = torch.empty((B, H, V, K), device="cuda")
+
+        def step():
+            binding.gdn_prefill(q, k, v, al, be, None, o, ST, B, T, H, K, V, binding.GDN_FP32)
+
+        steps = max(3, min(args.steps, 10))
+        tot, _ = time_calls(step, steps, 2, torch, barrier)
+        ms = max_over_ranks(tot) / steps
+        byts = B * T * H * (4 * 2 * K + 4 * 2 * V + 8) + 4 * B * H * V * K
+        out[name] = {"shape": f"B={B} T={T} H={H} d_k={K} d_v={V}", "ms_per_step": ms,
+                     "tokens_per_s": B * T * world / (ms / 1e3),
+                     "achieved_gbs": byts / (ms / 1e3) / 1e9}
+    out["note"] = "token-by-token CUDA-core kernel (scalar gate); float32 q/k/v/o"
+    return out
+
+
 def gated_bytes(B, T, H, K, V, gate):
     """Algorithmic HBM bytes of a gated prefill: bf16 q, k, v, o; float32
     per-channel alpha; beta (KDA) or b and w (GDN2); S_T."""
@@ -789,7 +821,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline prefill only")
     ap.add_argument("--only", default=None,
                     choices=["pruned", "prologue", "state_rank", "truncation", "drrqr",
-                             "long_context", "gated", "decode"],
+                             "long_context", "gated", "fp32", "decode"],
                     help="headline prefill plus this one section (e.g. for a profiler run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=None)

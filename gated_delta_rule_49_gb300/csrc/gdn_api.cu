@@ -133,12 +133,12 @@ int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
     // bf16 at V = 128 runs on the tensor cores; float32 mode and the small
-    // (32, 32) variant run the CUDA-core chunked kernel.
+    // (32, 32) variant run the token-by-token CUDA-core kernel (scalar gate).
     if (dtype == GDN_BF16 && V == 128 && (K == 128 || K == 64))
         return from_cuda(gdn::launch_prefill_tc(q, k, v, alpha, beta, S0, o, S_T, B, T, T, H, K, V,
                                                 workspace, workspace_bytes, st));
-    return from_cuda(gdn::launch_prefill_simt(q, k, v, alpha, beta, S0, o, S_T, B, T, T, H, K, V,
-                                              dtype, st));
+    return from_cuda(gdn::launch_prefill_gated(q, k, v, alpha, beta, nullptr, nullptr, S0, o, S_T,
+                                               B, T, T, H, K, V, GDN_GATE_SCALAR, dtype, st));
 }
 
 int gdn_decode_step(const void *q, const void *k, const void *v, const float *alpha,
@@ -205,8 +205,8 @@ int gdn_prefill_gated(const void *q, const void *k, const void *v, const float *
     if ((long long)B * H == 0) return GDN_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
-    return from_cuda(gdn::launch_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, H,
-                                               K, V, gate, dtype, st));
+    return from_cuda(gdn::launch_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, T,
+                                               H, K, V, gate, dtype, st));
 }
 
 int gdn_decode_step_gated(const void *q, const void *k, const void *v, const float *alpha,
@@ -278,8 +278,9 @@ int gdn_prefill_truncated(const void *q, const void *k, const void *v, const flo
         cudaError_t e = tc ? gdn::launch_prefill_tc(qw, kw, vw, alpha + tok, beta + tok, start, ow,
                                                     S_T, B, n, T, H, K, V, workspace,
                                                     workspace_bytes, st)
-                           : gdn::launch_prefill_simt(qw, kw, vw, alpha + tok, beta + tok, start,
-                                                      ow, S_T, B, n, T, H, K, V, dtype, st);
+                           : gdn::launch_prefill_gated(qw, kw, vw, alpha + tok, beta + tok,
+                                                       nullptr, nullptr, start, ow, S_T, B, n, T,
+                                                       H, K, V, GDN_GATE_SCALAR, dtype, st);
         if (e != cudaSuccess) return from_cuda(e);
         start = S_T;
         if (t0 + n < T && r < (K < V ? K : V)) {

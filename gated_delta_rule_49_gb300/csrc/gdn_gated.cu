@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(128)
                          const Tin *__restrict__ v, const float *__restrict__ alpha,
                          const float *__restrict__ beta, const float *__restrict__ bg,
                          const float *__restrict__ wg, const float *__restrict__ S0,
-                         Tin *__restrict__ o, float *__restrict__ ST, int T, int H, int V) {
+                         Tin *__restrict__ o, float *__restrict__ ST, int T, int Ts, int H,
+                         int V) {
     using L = GatedStage<K, R, Tin, GATE>;
     constexpr int LPR = K / CPL;  // lanes per row
     constexpr int RPI = 32 / LPR;
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(128)
     }
 
     const int nblk = (T + kTB - 1) / kTB;
-    auto th_of = [&](int t) { return ((size_t)b * T + t) * H + h; };
+    auto th_of = [&](int t) { return ((size_t)b * Ts + t) * H + h; };
     if (nblk > 0)
         stage_block<K, R, Tin, GATE>(smem, q, k, v, alpha, beta, bg, wg, th_of(0), H, V, r0,
                                      min(kTB, T));
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(128)
 template <int K, int R, int CPL, int RPL, typename Tin, int GATE>
 cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *alpha,
                       const float *beta, const float *bg, const float *wg, const float *S0,
-                      void *o, float *ST, int B, int T, int H, int V, cudaStream_t stream) {
+                      void *o, float *ST, int B, int T, int Ts, int H, int V,
+                      cudaStream_t stream) {
     using L = GatedStage<K, R, Tin, GATE>;
     constexpr int RPI = 32 / (K / CPL);
     constexpr int threads = R / (RPI * RPL) * 32;
@@ -325,7 +327,7 @@ cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, threads, L::SMEM, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
-        alpha, beta, bg, wg, S0, static_cast<Tin *>(o), ST, T, H, V);
+        alpha, beta, bg, wg, S0, static_cast<Tin *>(o), ST, T, Ts, H, V);
     return cudaGetLastError();
 }
 
@@ -336,17 +338,17 @@ cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *
 template <typename Tin, int GATE>
 cudaError_t pg_dispatch(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *bg, const float *wg, const float *S0,
-                        void *o, float *ST, int B, int T, int H, int K, int V,
+                        void *o, float *ST, int B, int T, int Ts, int H, int K, int V,
                         cudaStream_t stream) {
     if (K == 128 && V == 128)
         return launch_pg<128, 32, 16, 4, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T,
-                                                    H, V, stream);
+                                                    Ts, H, V, stream);
     if (K == 64 && V == 128)
         return launch_pg<64, 32, 8, 4, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T,
-                                                  H, V, stream);
+                                                  Ts, H, V, stream);
     if (K == 32 && V == 32)
         return launch_pg<32, 32, 8, 4, Tin, GATE>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T,
-                                                  H, V, stream);
+                                                  Ts, H, V, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -465,10 +467,10 @@ cudaError_t dg_dispatch(const void *q, const void *k, const void *v, const float
 cudaError_t launch_prefill_gated(const void *q, const void *k, const void *v,
                                  const float *alpha, const float *beta, const float *bg,
                                  const float *wg, const float *S0, void *o, float *ST, int B,
-                                 int T, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
+                                 int T, int Ts, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
                                  cudaStream_t stream) {
 #define GDN_PG(TIN, G) \
-    pg_dispatch<TIN, G>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, H, K, V, stream)
+    pg_dispatch<TIN, G>(q, k, v, alpha, beta, bg, wg, S0, o, ST, B, T, Ts, H, K, V, stream)
     const bool bf = dt == GDN_BF16;
     switch (gate) {
         case GDN_GATE_SCALAR: return bf ? GDN_PG(__nv_bfloat16, kScalar) : GDN_PG(float, kScalar);

@@ -152,10 +152,11 @@ cudaError_t launch_prefill_host(const void *q, const void *k, const void *v, con
                                   n, window, H, K, V, L.seg_bytes ? ws + L.seg : nullptr,
                                   L.seg_bytes, stream);
         else
-            e = launch_prefill_simt(base + L.q, base + L.k, base + L.v,
-                                    reinterpret_cast<const float *>(base + L.a),
-                                    reinterpret_cast<const float *>(base + L.b), start, ow, Sdev,
-                                    B, n, window, H, K, V, dt, stream);
+            e = launch_prefill_gated(base + L.q, base + L.k, base + L.v,
+                                     reinterpret_cast<const float *>(base + L.a),
+                                     reinterpret_cast<const float *>(base + L.b), nullptr, nullptr,
+                                     start, ow, Sdev, B, n, window, H, K, V, GDN_GATE_SCALAR, dt,
+                                     stream);
         if (e != cudaSuccess) return e;
         GDN_TRY(cudaEventRecord(P->in_free[slot], stream));
         // ---- outputs of window w ----

@@ -39,17 +39,13 @@ cudaError_t launch_state_rank(const float *S, int BH, int V, int K, float *fro2,
                               float *sigma1, float *er, int max_iter, float tol,
                               cudaStream_t stream);
 
-cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v,
-                                const float *alpha, const float *beta, const float *S0,
-                                void *o, float *ST, int B, int T, int Ts, int H, int K, int V,
-                                gdn_dtype dt, cudaStream_t stream);
 
 // Tensor-core (tcgen05) chunked prefill: bf16 q/k/v, V = 128, K in {64, 128}.
 // Long sequences on few heads run segment-parallel and need `workspace`.
 //
-// Both chunked prefills process tokens [0, T) of token tensors laid out as
-// [B, Ts, H, *] (Ts >= T tokens per batch entry; alpha/beta [B, Ts, H]):
-// Ts = T for a whole tensor, Ts > T for a window of a longer one.
+// Processes tokens [0, T) of token tensors laid out as [B, Ts, H, *]
+// (Ts >= T tokens per batch entry; alpha/beta [B, Ts, H]): Ts = T for a whole
+// tensor, Ts > T for a window of a longer one.
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,
                               const float *beta, const float *S0, void *o, float *ST, int B,
                               int T, int Ts, int H, int K, int V, void *workspace,
@@ -76,11 +72,13 @@ cudaError_t launch_decode_gathered(const void *q, const void *k, const int *idx,
                                    float *S, void *o, int B, int H, int K, int V, gdn_dtype dt,
                                    float eps, cudaStream_t stream);
 
-// Channel-gated rules (GDN / KDA / GDN2), token by token on the CUDA cores.
+// Channel-gated rules (GDN / KDA / GDN2), token by token on the CUDA cores;
+// also the prefill for float32 inputs and the (32, 32) variant (scalar gate).
+// Tokens [0, T) of [B, Ts, H, *] tensors, as for the chunked prefill.
 cudaError_t launch_prefill_gated(const void *q, const void *k, const void *v,
                                  const float *alpha, const float *beta, const float *bg,
                                  const float *wg, const float *S0, void *o, float *ST, int B,
-                                 int T, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
+                                 int T, int Ts, int H, int K, int V, gdn_gate gate, gdn_dtype dt,
                                  cudaStream_t stream);
 cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, const float *alpha,
                                 const float *beta, const float *bg, const float *wg, float *S,

@@ -31,8 +31,9 @@
  *    GDN_ERR_UNSUPPORTED.  K is d_k (or a pruned d_k'), V is d_v.
  *  - State tensors, alpha and beta are always float32; q, k, v and o are
  *    bf16 (GDN_BF16) or float32 (GDN_FP32).  Arithmetic is float32 with the
- *    state carried in float32; in GDN_BF16 mode the chunked prefill's tensor
- *    core products take bf16 operands with float32 accumulation.
+ *    state carried in float32; in GDN_BF16 mode at V = 128 the prefill runs
+ *    the chunk form on the tensor cores (bf16 operands, float32 accumulation),
+ *    otherwise it runs token by token on the CUDA cores.
  *  - alpha is expected in (0, 1] and beta in [0, 2); values are not checked.
  */
 #ifndef GDN_H
