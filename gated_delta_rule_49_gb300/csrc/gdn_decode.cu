@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int sub = lane / LPR;  // row within the warp's pass
     const int cl = lane % LPR;   // float4 column index
 
+    // plain steps are launched with programmatic dependent launch: wait for
+    // the previous step's state writes before the first global read
+    if constexpr (!GATHER) pdl_wait();
     float4 kf, qf;
     if constexpr (!GATHER) {
         kf = load4(k + (size_t)bh * K + 4 * cl);
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             vi[r] = 0.f;
         }
     }
+    if constexpr (!GATHER) pdl_trigger();  // the next step may be scheduled early
     if constexpr (GATHER) {
         // The state loads above are already in flight: the index -> channel
         // load chain and the norm reductions overlap them.
@@ -157,10 +161,21 @@ cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const f
     const int blocks_per_head = (V + kRowsPerCta - 1) / kRowsPerCta;
     const long long grid = (long long)BH * blocks_per_head;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if constexpr (!GATHER) {
+        // consecutive plain steps overlap their launch with the previous step's
+        // tail (measured: 23.3 -> 21.3 us per step at B = 64, d_k = 128, L2-cold).
+        // The gathering step (and the gated step) measured slower with it, and
+        // slower even with the wait / trigger instructions present but a plain
+        // launch, so they have neither.
+        return launch_pdl(decode_step_kernel<K, Tin, GATHER>, (unsigned)grid, kDecodeThreads, 0,
+                          stream, static_cast<const Tin *>(q), static_cast<const Tin *>(k),
+                          static_cast<const Tin *>(v), alpha, beta, S, static_cast<Tin *>(o), V,
+                          blocks_per_head, idx, Kin, H, eps, nullptr);
+    }
     decode_step_kernel<K, Tin, GATHER><<<(unsigned)grid, kDecodeThreads, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
         alpha, beta, S, static_cast<Tin *>(o), V, blocks_per_head, idx, Kin, H, eps,
-        GATHER ? device_status_ptr() : nullptr);
+        device_status_ptr());
     return cudaGetLastError();
 }
 

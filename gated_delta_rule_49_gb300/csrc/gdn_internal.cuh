@@ -110,6 +110,31 @@ cudaError_t launch_prefill_host(const void *q, const void *k, const void *v, con
                                 int T, int H, int K, int V, gdn_dtype dt, int window,
                                 void *workspace, cudaStream_t stream);
 
+// Programmatic dependent launch: a kernel launched this way may be scheduled
+// while the previous kernel on the stream finishes; it must execute
+// pdl_wait() before its first global-memory access (which then sees all of
+// the previous kernel's writes) and may call pdl_trigger() to let its own
+// successor be scheduled early.  (Used by the plain decode step.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Loads of the run dtype as float.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
