@@ -10,18 +10,21 @@
 // channels or per value row), so the state is split by rows across CTAs and
 // lanes and nothing is exchanged between rows.
 //
-// Prefill: a CTA owns R rows of one (b, h) sequence; a row is spread over
-// K/8 lanes holding 8 channels each in registers, and every lane holds
-// four rows, so that the per-token operands it reads from shared memory
-// (k, q, the channel decay, the erase direction) serve all of them.  The
-// per-token operands and the CTA's slice of v / w are staged 8 tokens at a
-// time into a two-stage shared-memory ring by cp.async (block n+1 in flight
-// while block n is processed); bf16 k / q are converted to float32 once per
-// CTA.  Per token and row: decay, the erase read p = s~ . e and r = s~ . q
-// (reduced together over the row's lanes), the rank-one write, and
-// o = r + u (k . q); the state arithmetic runs on packed float2 FMA.  Outputs are collected per block in
-// shared memory and written with 16-byte stores.  Bound: shared-memory
-// wavefronts and instruction issue together.
+// Prefill: a CTA owns R = 32 rows of one (b, h) sequence; a row is spread
+// over K / CPL lanes holding CPL channels each in registers (CPL = 16 at
+// d_k = 128, 8 otherwise), and every lane holds four rows, so that the
+// per-token operands it reads from shared memory (k, q, the channel decay,
+// the erase direction) serve all of them.  The per-token operands and the
+// CTA's slice of v / w are staged 8 tokens at a time into a two-stage
+// shared-memory ring by cp.async (block n+1 in flight while block n is
+// processed); bf16 k / q are converted to float32 once per CTA.  Per token
+// and row: decay, the erase read p = s~ . e and r = s~ . q (reduced together
+// over the row's lanes), the rank-one write, and o = r + u (k . q); the state
+// arithmetic runs on packed float2 FMA.  Outputs are collected per block in
+// shared memory and written with 16-byte stores.  Bound: the latency of the
+// token-serial chain per warp (few warps per SM at these row counts).
+// This kernel is also the prefill for float32 inputs and for the (32, 32)
+// variant (scalar gate).
 //
 // Decode: the layout of the plain decode step (K/4 lanes per row, four rows
 // per lane, all state loads issued first); HBM-bound on the state.
