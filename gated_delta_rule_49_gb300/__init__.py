@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     gdn_state_truncate,
     gdn_prefill_truncated,
     gdn_prefill_workspace_size,
+    gdn_prefill_two_pass_workspace_size,
     gdn_selftest_wait_timeout,
     gdn_state_rank,
     gdn_status_string,

@@ -38,6 +38,7 @@ GATES = {"gdn": GDN_GATE_SCALAR, "kda": GDN_GATE_KDA, "gdn2": GDN_GATE_GDN2}
 EXPORTS = (
     "gdn_prefill",
     "gdn_prefill_workspace_size",
+    "gdn_prefill_two_pass_workspace_size",
     "gdn_decode_step",
     "gdn_state_rank",
     "gdn_get_last_device_status",
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill.restype = i
         lib.gdn_prefill_workspace_size.argtypes = [i] * 6
         lib.gdn_prefill_workspace_size.restype = sz
+        lib.gdn_prefill_two_pass_workspace_size.argtypes = [i] * 6
+        lib.gdn_prefill_two_pass_workspace_size.restype = sz
         lib.gdn_decode_step.argtypes = [vp] * 7 + [i] * 5 + [vp]
         lib.gdn_decode_step.restype = i
         lib.gdn_state_rank.argtypes = [vp, i, i, i, vp, vp, vp, i, f, vp]
@@ -189,6 +192,10 @@ def gdn_prefill_noalloc_max_workspace() -> int:
 
 def gdn_prefill_workspace_size(B, T, H, K, V, dtype) -> int:
     return int(load().gdn_prefill_workspace_size(B, T, H, K, V, dtype))
+
+
+def gdn_prefill_two_pass_workspace_size(B, T, H, K, V, dtype) -> int:
+    return int(load().gdn_prefill_two_pass_workspace_size(B, T, H, K, V, dtype))
 
 
 def gdn_decode_step(q, k, v, alpha, beta, S, o, B, H, K, V, dtype, stream=None) -> int:
@@ -380,9 +387,11 @@ def gdn_version() -> int:
 # ---- tensor-level conveniences (allocate outputs with torch, then call) ----
 
 def prefill(q, k, v, alpha, beta, S0=None, want_o=True, want_state=True, out_state=None,
-            stream=None):
+            stream=None, two_pass=True):
     """q, k [B,T,H,K]; v [B,T,H,V] (bf16 or fp32 CUDA tensors); alpha, beta
-    [B,T,H] fp32; S0 [B,H,V,K] fp32 or None.  Returns (o, S_T)."""
+    [B,T,H] fp32; S0 [B,H,V,K] fp32 or None.  Returns (o, S_T).  two_pass:
+    allocate the workspace of the two-pass form where the problem has one
+    (identical results; False runs the one-pass form)."""
     import torch
     B, T, H, K = k.shape
     V = v.shape[-1]
@@ -393,6 +402,8 @@ def prefill(q, k, v, alpha, beta, S0=None, want_o=True, want_state=True, out_sta
         ST = out_state if out_state is not None else torch.empty(
             (B, H, V, K), dtype=torch.float32, device=k.device)
     ws_bytes = gdn_prefill_workspace_size(B, T, H, K, V, dt)
+    if two_pass:
+        ws_bytes = max(ws_bytes, gdn_prefill_two_pass_workspace_size(B, T, H, K, V, dt))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=k.device) if ws_bytes else None
     gdn_prefill(q, k, v, alpha, beta, S0, o, ST, B, T, H, K, V, dt, ws, ws_bytes, stream)
     return o, ST

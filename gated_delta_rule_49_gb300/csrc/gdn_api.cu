@@ -94,6 +94,14 @@ size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype d
     return gdn::segment_shape(B * H, T, K, gdn::sm_count()).workspace_bytes;
 }
 
+size_t gdn_prefill_two_pass_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || V != 128 || (K != 128 && K != 64) || dtype != GDN_BF16)
+        return 0;
+    if ((long long)B * H > 0x7fffffffLL) return 0;
+    const gdn::SegShape sh = gdn::segment_shape(B * H, T, K, gdn::sm_count());
+    return gdn::prefill_prep_offset(sh) + gdn::prefill_prep_bytes((long long)B * H, T);
+}
+
 namespace {
 // T = 0: the final state is the start state (or zero).
 int empty_prefill(const float *S0, float *S_T, int B, int H, int K, int V, cudaStream_t st) {

@@ -60,6 +60,13 @@ struct SegShape {
 };
 SegShape segment_shape(int BH, int T, int K, int nsm);
 
+// Two-pass form of the tensor-core prefill: a key-side pass writes T', T'' and
+// P of every chunk (prefill_prep_bytes) at byte offset prefill_prep_offset of
+// the workspace, after the segment slots; launch_prefill_tc takes this form
+// whenever workspace_bytes >= offset + bytes.
+size_t prefill_prep_offset(const SegShape &sh);
+size_t prefill_prep_bytes(long long BH, int T);
+
 // Pruning prologue: gather K_out of K_in channels per head and L2-normalise.
 cudaError_t launch_gather_normalize(const void *x, const int *idx, void *y, long long rows,
                                     int H, int Kin, int Kout, gdn_dtype dt, float eps,

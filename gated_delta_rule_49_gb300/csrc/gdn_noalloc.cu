@@ -42,13 +42,15 @@ extern "C" int gdn_prefill_noalloc(const void *q, const void *k, const void *v,
                                    gdn_dtype dtype, void *stream) {
     const size_t need = gdn_prefill_workspace_size(B, T, H, K, V, dtype);
     if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
+    const size_t two_pass = gdn_prefill_two_pass_workspace_size(B, T, H, K, V, dtype);
+    const bool use = need > 0 || (two_pass > 0 && two_pass <= kNoAllocScratchBytes);
     void *ws = nullptr;
-    if (need > 0) {
+    if (use) {
         ws = scratch_address();
         if (!ws) return GDN_ERR_CUDA;
     }
-    // Every slot of the scratch that the prefill reads is written earlier in
+    // Every byte of the scratch that the prefill reads is written earlier in
     // the same call, so nothing has to be cleared between calls.
     return gdn_prefill(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, ws,
-                       need > 0 ? kNoAllocScratchBytes : 0, stream);
+                       use ? kNoAllocScratchBytes : 0, stream);
 }

@@ -45,6 +45,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 namespace gdn {
 namespace {
 
@@ -57,34 +59,57 @@ constexpr int kBarKey = 1, kBarState = 2;       // named barrier ids
 constexpr long long kSpinLimit = 2000000000LL;  // ~1 s of SM clocks per wait
 constexpr int kLD = 68;                         // row stride of the fp32 64 x 64 matrix
 
-template <int K>
+// Bytes of one chunk's key-side operands in the two-pass form: T', T'' and P,
+// each a 64 x 64 bf16 tile stored as its 128-byte-swizzled shared-memory image.
+constexpr uint32_t kPrepChunkBytes = 3 * 8192;
+
+// PREP = false: the fused kernel (key group computes A, P and the inverse).
+// PREP = true:  the state-side kernel of the two-pass form, which loads each
+//               chunk's T', T'', P from the key-side pass instead.
+template <int K, bool PREP>
 struct TcLayout {
     // q/k stages (three): 64 x 64 bf16 boxes, 8 KB each; K and Q of one
     // 64-channel block are adjacent so [K;Q] is one 128-row operand
     static constexpr int NSTAGE = 3;
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
-    static constexpr uint32_t VB = NSTAGE * STAGE;      // V: two 64-channel boxes
-    static constexpr uint32_t TP = VB + 16384, TPP = TP + 8192;
-    static constexpr uint32_t NW = TP;                  // -W^T (K rows) reuses T', T''
-    static constexpr uint32_t PT = TPP + 8192;          // two buffers of 8 KB
-    static constexpr uint32_t SB = PT + 16384;          // K/64 blocks of 128 rows
+    // V: two 64-channel boxes per buffer; the two-pass form double-buffers it
+    // (its key group has no solve to hide the load behind)
+    static constexpr int NV = PREP ? 2 : 1;
+    static constexpr uint32_t VB = NSTAGE * STAGE;
+    // fused: T', T'' (-W^T reuses them) and two P buffers of 8 KB;
+    // PREP: a two-stage ring of [T' | T'' | P], -W^T reusing the stage's T', T''
+    static constexpr uint32_t TP = VB + NV * 16384, TPP = TP + 8192;
+    static constexpr uint32_t PT = TPP + 8192;
+    static constexpr uint32_t PR = VB + NV * 16384;
+    static constexpr uint32_t SB = PREP ? PR + 2 * kPrepChunkBytes : PT + 16384;  // K/64 blocks
     // U^T (128 rows, split in two 64-row halves): at K = 128 it reuses the
     // gamma-scaled Q tiles of the chunk's own stage, which are spent by then
     static constexpr uint32_t UTS = SB + (K / 64) * 16384;
     static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);
-    static constexpr uint32_t AF = UD + 16384;          // float [64][68]
-    static constexpr uint32_t XS = AF + 64 * kLD * 4;   // float [3][16][16] block scratch
-    static constexpr uint32_t KGATE = XS + 3 * 256 * 4; // key group: G2, gamma, beta
+    static constexpr uint32_t AF = UD + 16384;          // float [64][68] (fused only)
+    static constexpr uint32_t XS = AF + (PREP ? 0u : 64u * kLD * 4u);  // [3][16][16] (fused)
+    static constexpr uint32_t KGATE = XS + (PREP ? 0u : 3u * 256u * 4u);  // G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;  // state: 3 x (decay[64], gamma_C)
     static constexpr uint32_t END = SGATE + 3 * 68 * 4;
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr uint32_t V_BYTES = 2u * 8192u;
-    static constexpr size_t SMEM = END + 1024;          // + alignment slack
-    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr size_t SMEM = END;
+    // 227 KB per CTA, of which the kernel's static variables take 1 KB (the
+    // 1024-byte alignment of the dynamic region pads them)
+    static_assert(SMEM + 1024 <= 232448, "shared memory budget");
     static __device__ __forceinline__ uint32_t ut_half(int st, int hh) {
         if (K == 128) return st * STAGE + (hh ? QC1 : QC0);
         return UTS + hh * 8192;
+    }
+    // T' / T'' of chunk n, -W^T of chunk n, and the [any 64 rows; P] operand
+    static __device__ __forceinline__ uint32_t tp(int n) {
+        return PREP ? PR + (n & 1) * kPrepChunkBytes : TP;
+    }
+    static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
+    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }
+    static __device__ __forceinline__ uint32_t pa(int n) {
+        return PREP ? tp(n) + 8192 : PT + (n & 1) * 8192 - 8192;
     }
     // TMEM columns
     static constexpr uint32_t D1 = 0, WT = 64, UA = 128, O = 256, DS = 384;
@@ -229,6 +254,110 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
     }
 }
 
+// ---- the key-side steps of one chunk, shared by the fused kernel and the
+// ---- separate key-side pass so that both compute bit-identical operands
+
+// Gates of one chunk by one warp from alpha / beta held two per lane (tokens
+// lane and lane + 32): G2 = in-chunk prefix of log2 alpha, gamma = 2^G2, beta.
+__device__ __forceinline__ void chunk_gates(float pa0, float pa1, float pb0, float pb1, int lane,
+                                            int nvalid, float *G2, float *gam, float *bet) {
+    float g0, g1;
+    chunk_log2_prefix(pa0, pa1, lane, nvalid, g0, g1);
+    G2[lane] = g0;
+    G2[lane + 32] = g1;
+    gam[lane] = exp2f(g0);
+    gam[lane + 32] = exp2f(g1);
+    bet[lane] = pb0;
+    bet[lane + 32] = pb1;
+}
+
+// [K;Q] K^T of one chunk into 64 TMEM columns at d1 (issued by one thread).
+// The stage holds the 64-channel K and Q boxes adjacently (K at kc, Q at
+// kc + 8 KB), so [K;Q] is one 128-row K-major operand.
+template <int K>
+__device__ __forceinline__ void issue_kq_kt(uint32_t d1, uint32_t stg, uint32_t kc0,
+                                            uint32_t kc1) {
+    constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+        const uint32_t kblk = stg + (kb ? kc1 : kc0) + ko;
+        mma_bf16(d1, sdesc(kblk, 16, 1024), sdesc(kblk, 16, 1024), I_MM, ks > 0);
+    }
+}
+
+// A (float32, rows 0..63 of AF) and P (bf16 operand tile) from [K;Q] K^T in
+// TMEM; the thread holds TMEM lane quad_row, columns [32 colhalf, +32):
+//   A_ts = beta_t 2^(G_t - G_s) (k_t . k_s) for s < t, else 0
+//   P_ts = 2^(G_t - G_s) (q_t . k_s)       for s <= t, else 0
+// Ptile may be shared or global memory (the tile's swizzled image).
+__device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colhalf,
+                                         const float *G2, const float *bet, float *AF,
+                                         uint8_t *Ptile) {
+    float v[32];
+    tmem_ld32(taddr, v);
+    tmem_ld_wait();
+    const int t = quad_row & 63;
+    const float gt = G2[t];
+    const int s0 = 32 * colhalf;
+    if (quad_row < 64) {
+        const float bt = bet[t];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
+            const float gs[4] = {g.x, g.y, g.z, g.w};
+            float a[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const int s = s0 + i + e2;
+                a[e2] = s < t ? bt * exp2f(gt - gs[e2]) * v[i + e2] : 0.f;
+            }
+            *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) = make_float4(a[0], a[1], a[2], a[3]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
+            const float gs[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2)
+                v[i + e2] = s0 + i + e2 <= t ? exp2f(gt - gs[e2]) * v[i + e2] : 0.f;
+        }
+        store_row<4>(Ptile, t, 4 * colhalf, v);
+    }
+}
+
+// T' = T diag(beta gamma) and T'' = T diag(beta) as bf16 operand tiles from
+// the inverse in AF (T_ii in place, T_ij mirrored at block (j, i)); thread tid
+// of 256 writes row tid / 4, columns [16 (tid % 4), +16).  The tiles may be
+// shared or global memory.
+__device__ __forceinline__ void chunk_tprime(float *AF, const float *bet, const float *gam,
+                                             uint8_t *TPtile, uint8_t *TPPtile, int tid) {
+    const int t = tid >> 2, cb = tid & 3;
+    const int bt = t >> 4;
+    float x[16];
+    if (cb > bt) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) x[c] = 0.f;
+    } else {
+        const float *src = (cb == bt) ? AF + t * kLD + 16 * cb : blk(AF, cb, bt) + (t & 15) * kLD;
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+            const float4 y = *reinterpret_cast<const float4 *>(src + c);
+            x[c] = y.x; x[c + 1] = y.y; x[c + 2] = y.z; x[c + 3] = y.w;
+        }
+    }
+    float tp[16], tpp[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const int s = 16 * cb + c;
+        tpp[c] = x[c] * bet[s];
+        tp[c] = tpp[c] * gam[s];
+    }
+    store_row<2>(TPtile, t, 2 * cb, tp);
+    store_row<2>(TPPtile, t, 2 * cb, tpp);
+}
+
 // Which token range, initial state and final-state slot a CTA works on.
 //   kWhole:  CTA = one (b, h) sequence, tokens [0, T), S0 / S_T as given.
 //   kFirst:  long sequences cut into `nseg` segments of `seg_len` tokens; per
@@ -248,22 +377,30 @@ struct SegPlan {
     float *ws;    // [3][B*H][nseg][V][K]: H/E slots, M slots, start-state slots
 };
 
-template <int K>
+// PREP: `prep` holds T', T'', P of every chunk ([B*H][ceil(T/64)] blocks of
+// kPrepChunkBytes, written by prefill_prep_kernel) and the key group only
+// forms W^T, U~^T and -W^T from them.
+template <int K, bool PREP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ alpha,
                       const float *__restrict__ beta, const float *__restrict__ S0,
                       __nv_bfloat16 *__restrict__ o, float *__restrict__ ST, int T, int Ts, int H,
-                      int BH, SegPlan plan, int *status) {
-    using L = TcLayout<K>;
+                      int BH, SegPlan plan, const uint8_t *__restrict__ prep, int *status) {
+    using L = TcLayout<K, PREP>;
     constexpr int V = 128;
     constexpr int KH = K / 2;  // state columns per state-group thread
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
-    __shared__ uint64_t kq_full[3], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready, nw_free;
-    __shared__ uint64_t ua_free[2], pt_free[2];
+    // the swizzle atoms and operand descriptors need a 1024-byte aligned
+    // base; the declaration provides it and the kernel checks it
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0 && status) atomicOr(status, kStatusBounds);
+        return;
+    }
+    uint8_t *sm = smem_raw;
+    __shared__ uint64_t kq_full[3], v_full[2], bar_p1, bar_w, bar_u, bar_s, nw_ready[2], nw_free;
+    __shared__ uint64_t ua_free[2], pt_free[2], prep_full[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -324,9 +461,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full, &bar_p1, &bar_w, &bar_u, &bar_s,
-                            &nw_ready, &nw_free, &ua_free[0], &ua_free[1], &pt_free[0],
-                            &pt_free[1]};
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0], &v_full[1], &bar_p1,
+                            &bar_w, &bar_u, &bar_s,
+                            &nw_ready[0], &nw_ready[1], &nw_free, &ua_free[0], &ua_free[1],
+                            &pt_free[0], &pt_free[1], &prep_full[0], &prep_full[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -351,9 +489,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     };
     auto load_v = [&](int n) {
-        mbar_arrive_expect_tx(&v_full, L::V_BYTES);
-        tma_load_4d(sm + L::VB, &tm_v, &v_full, 0, h, t0 + n * 64, b);
-        tma_load_4d(sm + L::VB + 8192, &tm_v, &v_full, 64, h, t0 + n * 64, b);
+        uint64_t *bar = &v_full[n % L::NV];
+        uint8_t *dst = sm + L::VB + (n % L::NV) * 16384;
+        mbar_arrive_expect_tx(bar, L::V_BYTES);
+        tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
+        tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
+    };
+    // T', T'', P of chunk n (of this CTA's token range) into ring stage n % 2
+    const uint8_t *prep_seq =
+        PREP ? prep + (seq * (size_t)((T + 63) / 64) + t0 / 64) * kPrepChunkBytes : nullptr;
+    auto load_prep = [&](int n) {
+        if constexpr (PREP) {
+            mbar_arrive_expect_tx(&prep_full[n & 1], kPrepChunkBytes);
+            bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes, kPrepChunkBytes,
+                      &prep_full[n & 1]);
+        }
     };
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
@@ -392,7 +542,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_gates(0);
         if (tid == 0) {
             for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
-            if (!zero_v) load_v(0);
+            if (!zero_v)
+                for (int m = 0; m < L::NV && m < nchunks; ++m) load_v(m);
+            for (int m = 0; m < 2 && m < nchunks; ++m) load_prep(m);
         }
         for (int n = 0; n < nchunks; ++n) {
             const int st = n % L::NSTAGE;  // q/k stage
@@ -400,127 +552,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t stg = base + st * L::STAGE;
             const int nvalid = min(64, t1 - t0 - n * 64);
             bool ok = true;
-            // ---- [K;Q] K^T ----
-            if (tid == 0) {
-                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
-                if (ok) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < K / 16; ++ks) {
-                        const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                        const uint32_t kblk = stg + (kb ? L::KC1 : L::KC0) + ko;
-                        mma_bf16(tb + L::D1, sdesc(kblk, 16, 1024), sdesc(kblk, 16, 1024), I_MM,
-                                 ks > 0);
+            if constexpr (!PREP) {
+                // ---- [K;Q] K^T ----
+                if (tid == 0) {
+                    ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_kq_kt<K>(tb + L::D1, stg, L::KC0, L::KC1);
+                        mma_commit(&bar_p1);
                     }
-                    mma_commit(&bar_p1);
+                    if (ok && n >= 2) ok = wait(&pt_free[p2], ((n - 2) >> 1) & 1);
+                    // T' / T'' share their buffer with the previous chunk's -W^T
+                    if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
+                    if (ok) ok = wait(&bar_p1, n & 1);
                 }
-                if (ok && n >= 2) ok = wait(&pt_free[p2], ((n - 2) >> 1) & 1);
-                // T' / T'' share their buffer with the previous chunk's -W^T
-                if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
-                if (ok) ok = wait(&bar_p1, n & 1);
+            } else {
+                // ---- this chunk's q/k tiles and its T', T'', P ----
+                if (tid == 0) {
+                    // warm L2 for the loads two and three chunks ahead (the
+                    // operands are copied in only once a ring slot frees)
+                    if (n + 2 < nchunks)
+                        bulk_prefetch_l2(prep_seq + (size_t)(n + 2) * kPrepChunkBytes,
+                                         kPrepChunkBytes);
+                    if (!zero_v && n + 3 < nchunks) {
+                        tma_prefetch_l2_4d(&tm_v, 0, h, t0 + (n + 3) * 64, b);
+                        tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + 3) * 64, b);
+                    }
+                    ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+                    if (ok) ok = wait(&prep_full[p2], (n >> 1) & 1);
+                }
             }
             // ---- gates of chunk n (warp 1), then prefetch chunk n + 1 ----
             if (warp == 1) {
-                float g0, g1;
-                chunk_log2_prefix(pa0, pa1, lane, nvalid, g0, g1);
-                G2[lane] = g0;
-                G2[lane + 32] = g1;
-                gam[lane] = exp2f(g0);
-                gam[lane + 32] = exp2f(g1);
-                bet[lane] = pb0;
-                bet[lane + 32] = pb1;
+                chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
                 prefetch_gates(n + 1);
             }
-            // one thread waited for [K;Q] K^T (and for the P buffer); the barrier
-            // hands both, and the gates, to the whole group
+            // one thread waited (for [K;Q] K^T and the P buffer, or for the
+            // loaded operands); the barrier hands them, and the gates, to the group
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
 
-            // ---- A (fp32, solve input) and P (bf16 operand): row quad_row, 32 columns ----
-            {
+            if constexpr (!PREP) {
+                // ---- A (fp32, solve input) and P (bf16 operand) ----
                 tc_fence_after();
-                float v[32];
-                tmem_ld32(tb + lane_off + L::D1 + 32 * colhalf, v);
-                tmem_ld_wait();
-                const int t = quad_row & 63;
-                const float gt = G2[t];
-                const int s0 = 32 * colhalf;
-                float gs[32];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
-                    gs[i] = g.x; gs[i + 1] = g.y; gs[i + 2] = g.z; gs[i + 3] = g.w;
-                }
-                if (quad_row < 64) {
-                    const float bt = bet[t];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        float a[4];
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const int s = s0 + i + e2;
-                            a[e2] = s < t ? bt * exp2f(gt - gs[i + e2]) * v[i + e2] : 0.f;
-                        }
-                        *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) =
-                            make_float4(a[0], a[1], a[2], a[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = s0 + i <= t ? exp2f(gt - gs[i]) * v[i] : 0.f;
-                    store_row<4>(sm + L::PT + p2 * 8192, t, 4 * colhalf, v);
-                }
+                chunk_ap(tb + lane_off + L::D1 + 32 * colhalf, quad_row, colhalf, G2, bet, AF,
+                         sm + L::PT + p2 * 8192);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+                // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
+                unit_lower_inverse(AF, XS, tid);
+                chunk_tprime(AF, bet, gam, sm + L::TP, sm + L::TPP, tid);
+                fence_proxy_async_smem();
+                named_sync(kBarKey, kKeyThreads);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-
-            // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
-            unit_lower_inverse(AF, XS, tid);
-            {
-                const int t = tid >> 2, cb = tid & 3;  // row t, columns [16 cb, 16 cb + 16)
-                const int bt = t >> 4;
-                float x[16];
-                if (cb > bt) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] = 0.f;
-                } else {
-                    const float *src = (cb == bt) ? AF + t * kLD + 16 * cb
-                                                  : blk(AF, cb, bt) + (t & 15) * kLD;
-#pragma unroll
-                    for (int c = 0; c < 16; c += 4) {
-                        const float4 y = *reinterpret_cast<const float4 *>(src + c);
-                        x[c] = y.x; x[c + 1] = y.y; x[c + 2] = y.z; x[c + 3] = y.w;
-                    }
-                }
-                float tp[16], tpp[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int s = 16 * cb + c;
-                    tpp[c] = x[c] * bet[s];
-                    tp[c] = tpp[c] * gam[s];
-                }
-                store_row<2>(sm + L::TP, t, 2 * cb, tp);
-                store_row<2>(sm + L::TPP, t, 2 * cb, tpp);
-            }
-            fence_proxy_async_smem();
-            named_sync(kBarKey, kKeyThreads);
 
             // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
             if (tid == 0) {
                 ok = true;
                 if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
-                if (!zero_v) ok = ok && wait(&v_full, n & 1);
+                if (!zero_v) ok = ok && wait(&v_full[n % L::NV], (n / L::NV) & 1);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t lbo_k = K == 128 ? 16384u : (uint32_t)(L::VB - st * L::STAGE);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, lbo_k, 1024),
-                                 sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
+                                 sdesc(base + L::tp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
                         if (!zero_v)
                             mma_bf16(tb + L::UA + 64 * p2,
-                                     sdesc(base + L::VB + ks * 2048, 8192, 1024),
-                                     sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
+                                     sdesc(base + L::VB + (n % L::NV) * 16384 + ks * 2048, 8192,
+                                           1024),
+                                     sdesc(base + L::tpp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
                     }
                     mma_commit(&bar_w);
                 }
@@ -548,22 +650,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (tid == 0) {
                 if (ok) ok = wait(&bar_w, n & 1);
-                if (ok && !zero_v && n + 1 < nchunks) load_v(n + 1);  // V consumed
+                if (ok && !zero_v && n + L::NV < nchunks) load_v(n + L::NV);  // buffer consumed
             }
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
             {
+                // -W^T over T', T'' (consumed by the products above)
                 tc_fence_after();
                 if (quad_row < K) {
                     float v[32];
                     tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
                     tmem_ld_wait();
-                    store_row<4>(sm + L::NW, quad_row, 4 * colhalf, v, -1.f);
+                    store_row<4>(sm + L::nw(n), quad_row, 4 * colhalf, v, -1.f);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-            if (tid == 0) mbar_arrive(&nw_ready);
+            // one barrier per chunk parity: in the two-pass form the key group
+            // may finish chunk n + 1 before the state group has waited for
+            // chunk n (nothing else holds it back), and two completed phases of
+            // one barrier would be indistinguishable from none; chunk n + 2
+            // needs operands loaded only after the state group passed chunk n
+            if (tid == 0) mbar_arrive(&nw_ready[n & 1]);
         }
     } else {
         // ================================================================ state group
@@ -633,7 +741,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // U^T += S (-W^T) for chunk m (after the key group handed over -W^T)
         auto issue_u = [&](int m) -> bool {
-            if (!wait(&nw_ready, m & 1)) return false;
+            if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks) {
@@ -641,10 +749,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // with v = 0 there is no U~ product: this one starts the accumulator
                 mma_bf16(tb + L::UA + 64 * (m & 1),
                          sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN,
+                         sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
                          zero_v ? (uint32_t)(ks > 0) : 1u);
             }
-            mma_commit(&nw_free);
+            if constexpr (!PREP) mma_commit(&nw_free);
             return true;
         };
         // O = [K; gamma Q] S^T for chunk m (token-major; TMEM lanes 64..127 hold
@@ -697,7 +805,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (sid == 0) {
                 mbar_arrive(&ua_free[p2]);
                 tc_fence_after();
-                const uint32_t pa = base + L::PT + p2 * 8192 - 8192;  // rows 64..127 = P
+                const uint32_t pa = base + L::pa(n);  // rows 64..127 = P
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
@@ -709,9 +817,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
                              sdesc(stg + L::KC0 + ks * 2048, 16384, 1024), I_DS, ks > 0);
                 mma_commit(&bar_s);
-                mma_commit(&pt_free[p2]);
+                if constexpr (!PREP) mma_commit(&pt_free[p2]);
                 ok = wait(&bar_s, n & 1);
                 if (ok && n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);  // stage consumed
+                // every product that reads ring stage n % 2 (-W^T, P) is done
+                if (ok && n + 2 < nchunks) load_prep(n + 2);
             }
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
@@ -796,14 +906,181 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
             }
-            mbar_wait(&v_full, 0, kSpinLimit / 16);
-            mbar_wait(&v_full, 1, kSpinLimit / 16);
+            for (int s = 0; s < L::NV; ++s) {
+                mbar_wait(&v_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&v_full[s], 1, kSpinLimit / 16);
+            }
+            if (PREP)
+                for (int s = 0; s < 2; ++s) {
+                    mbar_wait(&prep_full[s], 0, kSpinLimit / 16);
+                    mbar_wait(&prep_full[s], 1, kSpinLimit / 16);
+                }
         }
         __syncthreads();
     }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tb, 512);
+    }
+}
+
+// ---------------------------------------------------------------- key-side pass
+// The two-pass form's first kernel.  Everything of a chunk that depends only
+// on its keys, queries and gates -- A, P, the inverse T and T', T'' -- has no
+// dependence on the state, so it runs for all B * H * ceil(T/64) chunks at
+// once instead of in each sequence's serial chunk loop.  Persistent CTAs of
+// 256 threads (three per SM) stride over the chunks; each chunk's [K;Q] K^T
+// is one tcgen05 product into 64 TMEM columns, the next chunk's q/k boxes load
+// (TMA) while the current one is solved, and T', T'', P go to global memory as
+// their swizzled shared-memory images, which the state-side kernel copies in
+// with one bulk copy per chunk.  Same arithmetic as the fused kernel's key
+// group (the shared helpers above), so both forms give identical results.
+template <int K>
+struct PrepLayout {
+    static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
+    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;  // one q/k stage
+    static constexpr uint32_t AF = STAGE;                        // float [64][68]
+    static constexpr uint32_t XS = AF + 64 * kLD * 4;            // float [3][16][16]
+    static constexpr uint32_t GATE = XS + 3 * 256 * 4;           // G2, gamma, beta
+    static constexpr uint32_t END = GATE + 3 * 64 * 4;
+    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
+    static constexpr size_t SMEM = END;
+};
+constexpr int kPrepCtasPerSm = 3;
+// three CTAs of dynamic + 1 KB static + 1 KB reserved shared memory per SM
+static_assert(kPrepCtasPerSm * (PrepLayout<128>::SMEM + 2048) <= 233472, "prep residency");
+
+template <int K>
+__global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
+    prefill_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ alpha,
+                        const float *__restrict__ beta, uint8_t *__restrict__ prep, int T, int Ts,
+                        int H, long long nchunk_all, int *status) {
+    using L = PrepLayout<K>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the swizzle atoms and operand descriptors need a 1024-byte aligned
+    // base; the declaration provides it and the kernel checks it
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0 && status) atomicOr(status, kStatusBounds);
+        return;
+    }
+    uint8_t *sm = smem_raw;
+    __shared__ uint64_t kq_full, bar_p1;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+    volatile int *abort_v = &abort_flag;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int nch = (T + 63) / 64;  // chunks per sequence
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_sh, 64);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        mbar_init(&kq_full, 1);
+        mbar_init(&bar_p1, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base_sh;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int quad_row = (warp & 3) * 32 + lane;
+    const int colhalf = (warp >> 2) & 1;
+    float *AF = reinterpret_cast<float *>(sm + L::AF);
+    float *XS = reinterpret_cast<float *>(sm + L::XS);
+    float *G2 = reinterpret_cast<float *>(sm + L::GATE);
+    float *gam = G2 + 64;
+    float *bet = G2 + 128;
+
+    auto load_kq = [&](long long j) {
+        const long long seq = j / nch;
+        const int n = (int)(j - seq * nch);
+        const int b = (int)(seq / H), h = (int)(seq % H);
+        mbar_arrive_expect_tx(&kq_full, L::KQ_BYTES);
+        tma_load_4d(sm + L::KC0, &tm_k, &kq_full, 0, h, n * 64, b);
+        tma_load_4d(sm + L::QC0, &tm_q, &kq_full, 0, h, n * 64, b);
+        if (K == 128) {
+            tma_load_4d(sm + L::KC1, &tm_k, &kq_full, 64, h, n * 64, b);
+            tma_load_4d(sm + L::QC1, &tm_q, &kq_full, 64, h, n * 64, b);
+        }
+    };
+    float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
+    auto prefetch_gates = [&](long long j) {
+        if (warp == 1 && j < nchunk_all) {
+            const long long seq = j / nch;
+            const int n = (int)(j - seq * nch);
+            const int b = (int)(seq / H), h = (int)(seq % H);
+            const int nv = min(64, T - n * 64);
+            const size_t i0 = ((size_t)b * Ts + n * 64 + lane) * H + h;
+            const size_t i1 = i0 + (size_t)32 * H;
+            pa0 = lane < nv ? alpha[i0] : 1.f;
+            pb0 = lane < nv ? beta[i0] : 0.f;
+            pa1 = lane + 32 < nv ? alpha[i1] : 1.f;
+            pb1 = lane + 32 < nv ? beta[i1] : 0.f;
+        }
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
+        if (!ok) *abort_v = 1;
+        return ok;
+    };
+
+    const long long G = gridDim.x;
+    long long j = blockIdx.x;
+    if (tid == 0 && j < nchunk_all) load_kq(j);
+    prefetch_gates(j);
+    bool failed = false;
+    for (int it = 0; j < nchunk_all; j += G, ++it) {
+        const int n = (int)(j % nch);
+        const int nvalid = min(64, T - n * 64);
+        bool ok = true;
+        if (tid == 0) {
+            ok = wait(&kq_full, it & 1);
+            if (ok) {
+                tc_fence_after();
+                issue_kq_kt<K>(tb, smem_u32(sm), L::KC0, L::KC1);
+                mma_commit(&bar_p1);
+                ok = wait(&bar_p1, it & 1);
+                // the product has read the stage: the next chunk's boxes may land
+                if (ok && j + G < nchunk_all) load_kq(j + G);
+            }
+        }
+        if (warp == 1) {
+            chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
+            prefetch_gates(j + G);
+        }
+        if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T' | T'' | P]
+        tc_fence_after();
+        chunk_ap(tb + lane_off + 32 * colhalf, quad_row, colhalf, G2, bet, AF, out + 16384);
+        tc_fence_before();
+        named_sync(kBarKey, kKeyThreads);
+        unit_lower_inverse(AF, XS, tid);
+        chunk_tprime(AF, bet, gam, out, out + 8192, tid);
+        named_sync(kBarKey, kKeyThreads);  // AF and the gates are rewritten next
+    }
+
+    if (failed) *abort_v = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_v) {
+        if (tid == 0) {
+            if (status) atomicOr(status, kStatusTimeout);
+            // let an in-flight load land before the CTA's shared memory is released
+            mbar_wait(&kq_full, 0, kSpinLimit / 16);
+            mbar_wait(&kq_full, 1, kSpinLimit / 16);
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 64);
     }
 }
 
@@ -886,6 +1163,71 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
 }
 
 template <int K>
+cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const float *alpha,
+                        const float *beta, uint8_t *prep, long long BH, int T, int Ts, int H,
+                        cudaStream_t stream) {
+    auto kern = prefill_prep_kernel<K>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)PrepLayout<K>::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    // persistent CTAs, kPrepCtasPerSm per SM (the loop is correct for any residency)
+    const long long total = BH * ((T + 63) / 64);
+    const long long grid = std::min<long long>(total, (long long)kPrepCtasPerSm * sm_count());
+    kern<<<(unsigned)grid, kKeyThreads, PrepLayout<K>::SMEM, stream>>>(
+        mq, mk, alpha, beta, prep, T, Ts, H, total, device_status_ptr());
+    return cudaGetLastError();
+}
+
+template <int K, bool PREP>
+cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                   const float *alpha, const float *beta, const float *S0, void *o, float *ST,
+                   long long BH, int T, int Ts, int H, const SegShape &sh, float *ws,
+                   const uint8_t *prep, cudaStream_t stream) {
+    using L = TcLayout<K, PREP>;
+    auto kern = prefill_tc_kernel<K, PREP>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)L::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(o);
+    int *status = device_status_ptr();
+    if (sh.nseg == 1) {
+        kern<<<(unsigned)BH, kTcThreads, L::SMEM, stream>>>(
+            mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH, SegPlan{kWhole, 1, T, nullptr},
+            prep, status);
+        return cudaGetLastError();
+    }
+    const long long g1 = BH * (2 * sh.nseg - 1), g2 = BH * (sh.nseg - 1);
+    kern<<<(unsigned)g1, kTcThreads, L::SMEM, stream>>>(
+        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
+        SegPlan{kFirst, sh.nseg, sh.seg_len, ws}, prep, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    segment_combine_kernel<K><<<dim3((unsigned)BH, 128 / 16), 256, 0, stream>>>(ws, (int)BH,
+                                                                                sh.nseg);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)g2, kTcThreads, L::SMEM, stream>>>(
+        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
+        SegPlan{kSecond, sh.nseg, sh.seg_len, ws}, prep, status);
+    return cudaGetLastError();
+}
+
+template <int K>
 cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float *alpha,
                         const float *beta, const float *S0, void *o, float *ST, int B, int T,
                         int Ts, int H, void *workspace, size_t workspace_bytes,
@@ -894,45 +1236,27 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
     if (!make_token_map(&mq, q, B, T, Ts, H, K) || !make_token_map(&mk, k, B, T, Ts, H, K) ||
         !make_token_map(&mv, v, B, T, Ts, H, 128))
         return cudaErrorInvalidValue;
-    auto kern = prefill_tc_kernel<K>;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)TcLayout<K>::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     const long long BH = (long long)B * H;
     const SegShape sh = segment_shape(B * H, T, K, sm_count());
-    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(o);
-    int *status = device_status_ptr();
-    if (sh.nseg == 1) {
-        if (BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        kern<<<(unsigned)BH, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-            mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH, SegPlan{kWhole, 1, T, nullptr},
-            status);
-        return cudaGetLastError();
+    if (sh.nseg == 1 && BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (sh.nseg > 1) {
+        if (!workspace || workspace_bytes < sh.workspace_bytes) return cudaErrorInvalidValue;
+        if (BH * (2 * sh.nseg - 1) > 0x7fffffffLL || BH > 65535)
+            return cudaErrorInvalidConfiguration;
     }
-    if (!workspace || workspace_bytes < sh.workspace_bytes) return cudaErrorInvalidValue;
     float *ws = static_cast<float *>(workspace);
-    const long long g1 = BH * (2 * sh.nseg - 1), g2 = BH * (sh.nseg - 1);
-    if (g1 > 0x7fffffffLL || BH > 65535) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)g1, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
-        SegPlan{kFirst, sh.nseg, sh.seg_len, ws}, status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    segment_combine_kernel<K><<<dim3((unsigned)BH, 128 / 16), 256, 0, stream>>>(ws, (int)BH,
-                                                                                sh.nseg);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)g2, kTcThreads, TcLayout<K>::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
-        SegPlan{kSecond, sh.nseg, sh.seg_len, ws}, status);
-    return cudaGetLastError();
+    // Two-pass form when the workspace also holds every chunk's key-side operands.
+    const size_t prep_off = prefill_prep_offset(sh);
+    const size_t need = prep_off + prefill_prep_bytes(BH, T);
+    if (workspace && workspace_bytes >= need) {
+        uint8_t *prep = static_cast<uint8_t *>(workspace) + prep_off;
+        const cudaError_t e = launch_prep<K>(mq, mk, alpha, beta, prep, BH, T, Ts, H, stream);
+        if (e != cudaSuccess) return e;
+        return run_tc<K, true>(mq, mk, mv, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, prep,
+                               stream);
+    }
+    return run_tc<K, false>(mq, mk, mv, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, nullptr,
+                            stream);
 }
 
 }  // namespace
@@ -962,6 +1286,13 @@ SegShape segment_shape(int BH, int T, int K, int nsm) {
     if (sh.nseg < 2) return SegShape{1, T, 0};
     sh.workspace_bytes = 3ull * BH * sh.nseg * 128ull * K * sizeof(float);
     return sh;
+}
+
+size_t prefill_prep_offset(const SegShape &sh) {
+    return sh.nseg > 1 ? (sh.workspace_bytes + 255) & ~size_t(255) : 0;
+}
+size_t prefill_prep_bytes(long long BH, int T) {
+    return (size_t)BH * (size_t)((T + 63) / 64) * kPrepChunkBytes;
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,

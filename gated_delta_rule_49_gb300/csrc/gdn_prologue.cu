@@ -51,15 +51,6 @@ __device__ __forceinline__ void store8(float *dst, const float *g, float inv) {
     reinterpret_cast<float4 *>(dst)[1] = make_float4(g[4] * inv, g[5] * inv, g[6] * inv, g[7] * inv);
 }
 
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            sm100::smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(sm100::smem_u32(bar))
-        : "memory");
-}
-
 // rows_per_tile = floor(4096 / row bytes) >= 1 consecutive rows per warp tile;
 // row bytes (K_in * sizeof(T)) is a multiple of 16 and at most 4096, so a
 // tile is one contiguous, 16-byte aligned block: lane 0 of each warp fetches
@@ -97,7 +88,7 @@ __global__ void __launch_bounds__(kStagedWarps * 32)
         uint64_t *bar = &mb[i % kBulkStages];
         sm100::fence_proxy_async_smem();  // earlier generic reads of the slot come first
         sm100::mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(mine + (i % kBulkStages) * kTileBytes, x + r0 * Kin, bytes, bar);
+        sm100::bulk_load(mine + (i % kBulkStages) * kTileBytes, x + r0 * Kin, bytes, bar);
     };
     if (lane == 0)
         for (long long i = 0; i < my_n && i < kBulkStages; ++i) issue(i);

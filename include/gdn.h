@@ -84,7 +84,12 @@ typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
  * B = 0 or H = 0 is a no-op.
  *
  * workspace: device scratch of at least gdn_prefill_workspace_size() bytes
- * (may be NULL when that size is 0); 256-byte aligned.
+ * (may be NULL when that size is 0); 256-byte aligned.  With at least
+ * gdn_prefill_two_pass_workspace_size() bytes the bf16 tensor-core path runs
+ * in two passes: first the state-independent part of every chunk (A, P, the
+ * triangular inverse) for all chunks of all sequences at once, then the
+ * state recurrence, which only loads those operands.  The results are
+ * bit-identical to the one-pass form; only the speed differs.
  */
 GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
                 const float *beta, const float *S0, void *o, float *S_T, int B, int T, int H,
@@ -93,6 +98,14 @@ GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const float
 
 /* Bytes of device workspace gdn_prefill needs for this problem (0 if none). */
 GDN_API size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn_dtype dtype);
+
+/* Bytes of device workspace with which gdn_prefill takes the two-pass form:
+ * the segment scratch of gdn_prefill_workspace_size (rounded up to 256 bytes)
+ * plus 24 KiB per 64-token chunk per (b, h) for the key-side operands.
+ * 0 when the problem has no two-pass form (float32, or V != 128, or
+ * K not in {64, 128}). */
+GDN_API size_t gdn_prefill_two_pass_workspace_size(int B, int T, int H, int K, int V,
+                                                   gdn_dtype dtype);
 
 /*
  * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate device
@@ -107,7 +120,9 @@ GDN_API size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn
  * gdn_prefill_workspace_size) comes from one 32 MiB array compiled into the
  * library, which every GPU that loads the library holds until the process
  * exits.  A problem that needs more scratch than that returns
- * GDN_ERR_WORKSPACE before anything is launched.  The call allocates nothing.
+ * GDN_ERR_WORKSPACE before anything is launched.  Problems whose two-pass
+ * workspace fits in the array take the two-pass form.  The call allocates
+ * nothing.
  *
  *  - The first call on a device that needs scratch looks up the array's
  *    device address (cudaGetSymbolAddress) with that device current; make
