@@ -63,33 +63,25 @@ constexpr int kLD = 68;                         // row stride of the fp32 64 x 6
 // each a 64 x 64 bf16 tile stored as its 128-byte-swizzled shared-memory image.
 constexpr uint32_t kPrepChunkBytes = 3 * 8192;
 
-// PREP = false: the fused kernel (key group computes A, P and the inverse).
-// PREP = true:  the state-side kernel of the two-pass form, which loads each
-//               chunk's T', T'', P from the key-side pass instead.
-template <int K, bool PREP>
+template <int K>
 struct TcLayout {
     // q/k stages (three): 64 x 64 bf16 boxes, 8 KB each; K and Q of one
     // 64-channel block are adjacent so [K;Q] is one 128-row operand
     static constexpr int NSTAGE = 3;
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
-    // V: two 64-channel boxes per buffer; the two-pass form double-buffers it
-    // (its key group has no solve to hide the load behind)
-    static constexpr int NV = PREP ? 2 : 1;
-    static constexpr uint32_t VB = NSTAGE * STAGE;
-    // fused: T', T'' (-W^T reuses them) and two P buffers of 8 KB;
-    // PREP: a two-stage ring of [T' | T'' | P], -W^T reusing the stage's T', T''
-    static constexpr uint32_t TP = VB + NV * 16384, TPP = TP + 8192;
-    static constexpr uint32_t PT = TPP + 8192;
-    static constexpr uint32_t PR = VB + NV * 16384;
-    static constexpr uint32_t SB = PREP ? PR + 2 * kPrepChunkBytes : PT + 16384;  // K/64 blocks
+    static constexpr uint32_t VB = NSTAGE * STAGE;      // V: two 64-channel boxes
+    static constexpr uint32_t TP = VB + 16384, TPP = TP + 8192;
+    static constexpr uint32_t NW = TP;                  // -W^T (K rows) reuses T', T''
+    static constexpr uint32_t PT = TPP + 8192;          // two buffers of 8 KB
+    static constexpr uint32_t SB = PT + 16384;          // K/64 blocks of 128 rows
     // U^T (128 rows, split in two 64-row halves): at K = 128 it reuses the
     // gamma-scaled Q tiles of the chunk's own stage, which are spent by then
     static constexpr uint32_t UTS = SB + (K / 64) * 16384;
     static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);
-    static constexpr uint32_t AF = UD + 16384;          // float [64][68] (fused only)
-    static constexpr uint32_t XS = AF + (PREP ? 0u : 64u * kLD * 4u);  // [3][16][16] (fused)
-    static constexpr uint32_t KGATE = XS + (PREP ? 0u : 3u * 256u * 4u);  // G2, gamma, beta
+    static constexpr uint32_t AF = UD + 16384;          // float [64][68]
+    static constexpr uint32_t XS = AF + 64 * kLD * 4;   // float [3][16][16] block scratch
+    static constexpr uint32_t KGATE = XS + 3 * 256 * 4; // key group: G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;  // state: 3 x (decay[64], gamma_C)
     static constexpr uint32_t END = SGATE + 3 * 68 * 4;
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
@@ -101,15 +93,6 @@ struct TcLayout {
     static __device__ __forceinline__ uint32_t ut_half(int st, int hh) {
         if (K == 128) return st * STAGE + (hh ? QC1 : QC0);
         return UTS + hh * 8192;
-    }
-    // T' / T'' of chunk n, -W^T of chunk n, and the [any 64 rows; P] operand
-    static __device__ __forceinline__ uint32_t tp(int n) {
-        return PREP ? PR + (n & 1) * kPrepChunkBytes : TP;
-    }
-    static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
-    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }
-    static __device__ __forceinline__ uint32_t pa(int n) {
-        return PREP ? tp(n) + 8192 : PT + (n & 1) * 8192 - 8192;
     }
     // TMEM columns
     static constexpr uint32_t D1 = 0, WT = 64, UA = 128, O = 256, DS = 384;
@@ -377,18 +360,65 @@ struct SegPlan {
     float *ws;    // [3][B*H][nseg][V][K]: H/E slots, M slots, start-state slots
 };
 
-// PREP: `prep` holds T', T'', P of every chunk ([B*H][ceil(T/64)] blocks of
-// kPrepChunkBytes, written by prefill_prep_kernel) and the key group only
-// forms W^T, U~^T and -W^T from them.
-template <int K, bool PREP>
+struct SegTask {
+    size_t seq;        // (b, h) sequence
+    int t0, t1;        // token range
+    const float *s0p;  // start state (nullptr: zero)
+    bool s0_identity;  // start from the identity (transition-matrix run)
+    float *stp;        // end-state destination (nullptr: none)
+    bool zero_v;       // v = 0 (transition-matrix run)
+    bool outputs;      // this run writes o
+};
+__device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int T,
+                                                const float *S0, float *ST, int BH) {
+    constexpr int V = 128;
+    const size_t VK = (size_t)V * K;
+    SegTask tk{blockIdx.x, 0, T, nullptr, false, nullptr, false, true};
+    if (plan.mode == kWhole) {
+        if (S0) tk.s0p = S0 + tk.seq * VK;
+        if (ST) tk.stp = ST + tk.seq * VK;
+        return tk;
+    }
+    auto slot = [&](int kind, size_t sq, int p) {
+        return plan.ws + ((kind * (size_t)BH + sq) * plan.nseg + p) * VK;
+    };
+    int p;
+    if (plan.mode == kFirst) {
+        tk.seq = blockIdx.x / (2 * plan.nseg - 1);
+        const int i = blockIdx.x % (2 * plan.nseg - 1);
+        p = (i + 1) / 2;
+        if (i == 0) {
+            if (S0) tk.s0p = S0 + tk.seq * VK;
+            tk.stp = slot(0, tk.seq, 0);  // end of segment 0 (E)
+        } else if (i & 1) {
+            tk.stp = slot(0, tk.seq, p);  // zero start: H
+            tk.outputs = false;
+        } else {
+            tk.s0_identity = true;        // identity start, v = 0: M
+            tk.zero_v = true;
+            tk.stp = slot(1, tk.seq, p);
+            tk.outputs = false;
+        }
+    } else {
+        tk.seq = blockIdx.x / (plan.nseg - 1);
+        p = 1 + blockIdx.x % (plan.nseg - 1);
+        tk.s0p = slot(2, tk.seq, p);
+        tk.stp = (p == plan.nseg - 1 && ST) ? ST + tk.seq * VK : nullptr;
+    }
+    tk.t0 = p * plan.seg_len;
+    tk.t1 = min(T, tk.t0 + plan.seg_len);
+    return tk;
+}
+
+template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ alpha,
                       const float *__restrict__ beta, const float *__restrict__ S0,
                       __nv_bfloat16 *__restrict__ o, float *__restrict__ ST, int T, int Ts, int H,
-                      int BH, SegPlan plan, const uint8_t *__restrict__ prep, int *status) {
-    using L = TcLayout<K, PREP>;
+                      int BH, SegPlan plan, int *status) {
+    using L = TcLayout<K>;
     constexpr int V = 128;
     constexpr int KH = K / 2;  // state columns per state-group thread
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -399,8 +429,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full[3], v_full[2], bar_p1, bar_w, bar_u, bar_s, nw_ready[2], nw_free;
-    __shared__ uint64_t ua_free[2], pt_free[2], prep_full[2];
+    __shared__ uint64_t kq_full[3], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready[2], nw_free;
+    __shared__ uint64_t ua_free[2], pt_free[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -408,47 +438,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     // ---- this CTA's task ----
-    size_t seq = blockIdx.x;
-    int t0 = 0, t1 = T;
-    const float *s0p = S0;   // initial state (nullptr: zero)
-    bool s0_identity = false;
-    float *stp = ST ? ST + seq * V * K : nullptr;  // final state destination
-    bool zero_v = false;
-    if (plan.mode != kWhole) {
-        const size_t VK = (size_t)V * K;
-        auto slot = [&](int kind, size_t sq, int p) {
-            return plan.ws + ((kind * (size_t)BH + sq) * plan.nseg + p) * VK;
-        };
-        int p;
-        if (plan.mode == kFirst) {
-            seq = blockIdx.x / (2 * plan.nseg - 1);
-            const int i = blockIdx.x % (2 * plan.nseg - 1);
-            p = (i + 1) / 2;
-            if (i == 0) {
-                stp = slot(0, seq, 0);  // end of segment 0 (E)
-            } else if (i & 1) {
-                s0p = nullptr;          // zero start: H
-                stp = slot(0, seq, p);
-                o = nullptr;
-            } else {
-                s0p = nullptr;          // identity start, v = 0: M
-                s0_identity = true;
-                zero_v = true;
-                stp = slot(1, seq, p);
-                o = nullptr;
-            }
-        } else {
-            seq = blockIdx.x / (plan.nseg - 1);
-            p = 1 + blockIdx.x % (plan.nseg - 1);
-            s0p = slot(2, seq, p);
-            stp = (p == plan.nseg - 1 && ST) ? ST + seq * V * K : nullptr;
-        }
-        t0 = p * plan.seg_len;
-        t1 = min(T, t0 + plan.seg_len);
-        if (s0p == S0 && S0) s0p = S0 + seq * V * K;  // segment 0 of kFirst
-    } else if (S0) {
-        s0p = S0 + seq * V * K;
-    }
+    const SegTask tk = segment_task(plan, K, T, S0, ST, BH);
+    const size_t seq = tk.seq;
+    const int t0 = tk.t0, t1 = tk.t1;
+    const float *s0p = tk.s0p;
+    const bool s0_identity = tk.s0_identity, zero_v = tk.zero_v;
+    float *stp = tk.stp;
+    if (!tk.outputs) o = nullptr;
     const int b = (int)(seq / H), h = (int)(seq % H);
     const int nchunks = (t1 - t0 + 63) / 64;
     const uint32_t base = smem_u32(sm);
@@ -461,10 +457,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0], &v_full[1], &bar_p1,
-                            &bar_w, &bar_u, &bar_s,
-                            &nw_ready[0], &nw_ready[1], &nw_free, &ua_free[0], &ua_free[1],
-                            &pt_free[0], &pt_free[1], &prep_full[0], &prep_full[1]};
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full, &bar_p1, &bar_w,
+                            &bar_u, &bar_s, &nw_ready[0], &nw_ready[1], &nw_free,
+                            &ua_free[0], &ua_free[1], &pt_free[0], &pt_free[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -489,21 +484,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     };
     auto load_v = [&](int n) {
-        uint64_t *bar = &v_full[n % L::NV];
-        uint8_t *dst = sm + L::VB + (n % L::NV) * 16384;
-        mbar_arrive_expect_tx(bar, L::V_BYTES);
-        tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
-        tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
-    };
-    // T', T'', P of chunk n (of this CTA's token range) into ring stage n % 2
-    const uint8_t *prep_seq =
-        PREP ? prep + (seq * (size_t)((T + 63) / 64) + t0 / 64) * kPrepChunkBytes : nullptr;
-    auto load_prep = [&](int n) {
-        if constexpr (PREP) {
-            mbar_arrive_expect_tx(&prep_full[n & 1], kPrepChunkBytes);
-            bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes, kPrepChunkBytes,
-                      &prep_full[n & 1]);
-        }
+        mbar_arrive_expect_tx(&v_full, L::V_BYTES);
+        tma_load_4d(sm + L::VB, &tm_v, &v_full, 0, h, t0 + n * 64, b);
+        tma_load_4d(sm + L::VB + 8192, &tm_v, &v_full, 64, h, t0 + n * 64, b);
     };
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
@@ -542,9 +525,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_gates(0);
         if (tid == 0) {
             for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
-            if (!zero_v)
-                for (int m = 0; m < L::NV && m < nchunks; ++m) load_v(m);
-            for (int m = 0; m < 2 && m < nchunks; ++m) load_prep(m);
+            if (!zero_v) load_v(0);
         }
         for (int n = 0; n < nchunks; ++n) {
             const int st = n % L::NSTAGE;  // q/k stage
@@ -552,77 +533,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t stg = base + st * L::STAGE;
             const int nvalid = min(64, t1 - t0 - n * 64);
             bool ok = true;
-            if constexpr (!PREP) {
-                // ---- [K;Q] K^T ----
-                if (tid == 0) {
-                    ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_kq_kt<K>(tb + L::D1, stg, L::KC0, L::KC1);
-                        mma_commit(&bar_p1);
-                    }
-                    if (ok && n >= 2) ok = wait(&pt_free[p2], ((n - 2) >> 1) & 1);
-                    // T' / T'' share their buffer with the previous chunk's -W^T
-                    if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
-                    if (ok) ok = wait(&bar_p1, n & 1);
+            // ---- [K;Q] K^T ----
+            if (tid == 0) {
+                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    issue_kq_kt<K>(tb + L::D1, stg, L::KC0, L::KC1);
+                    mma_commit(&bar_p1);
                 }
-            } else {
-                // ---- this chunk's q/k tiles and its T', T'', P ----
-                if (tid == 0) {
-                    // warm L2 for the loads two and three chunks ahead (the
-                    // operands are copied in only once a ring slot frees)
-                    if (n + 2 < nchunks)
-                        bulk_prefetch_l2(prep_seq + (size_t)(n + 2) * kPrepChunkBytes,
-                                         kPrepChunkBytes);
-                    if (!zero_v && n + 3 < nchunks) {
-                        tma_prefetch_l2_4d(&tm_v, 0, h, t0 + (n + 3) * 64, b);
-                        tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + 3) * 64, b);
-                    }
-                    ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
-                    if (ok) ok = wait(&prep_full[p2], (n >> 1) & 1);
-                }
+                if (ok && n >= 2) ok = wait(&pt_free[p2], ((n - 2) >> 1) & 1);
+                // T' / T'' share their buffer with the previous chunk's -W^T
+                if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
+                if (ok) ok = wait(&bar_p1, n & 1);
             }
             // ---- gates of chunk n (warp 1), then prefetch chunk n + 1 ----
             if (warp == 1) {
                 chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
                 prefetch_gates(n + 1);
             }
-            // one thread waited (for [K;Q] K^T and the P buffer, or for the
-            // loaded operands); the barrier hands them, and the gates, to the group
+            // one thread waited for [K;Q] K^T (and for the P buffer); the barrier
+            // hands both, and the gates, to the whole group
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
 
-            if constexpr (!PREP) {
-                // ---- A (fp32, solve input) and P (bf16 operand) ----
-                tc_fence_after();
-                chunk_ap(tb + lane_off + L::D1 + 32 * colhalf, quad_row, colhalf, G2, bet, AF,
-                         sm + L::PT + p2 * 8192);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-                // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
-                unit_lower_inverse(AF, XS, tid);
-                chunk_tprime(AF, bet, gam, sm + L::TP, sm + L::TPP, tid);
-                fence_proxy_async_smem();
-                named_sync(kBarKey, kKeyThreads);
-            }
+            // ---- A (fp32, solve input) and P (bf16 operand) ----
+            tc_fence_after();
+            chunk_ap(tb + lane_off + L::D1 + 32 * colhalf, quad_row, colhalf, G2, bet, AF,
+                     sm + L::PT + p2 * 8192);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+            // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
+            unit_lower_inverse(AF, XS, tid);
+            chunk_tprime(AF, bet, gam, sm + L::TP, sm + L::TPP, tid);
+            fence_proxy_async_smem();
+            named_sync(kBarKey, kKeyThreads);
 
             // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
             if (tid == 0) {
                 ok = true;
                 if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
-                if (!zero_v) ok = ok && wait(&v_full[n % L::NV], (n / L::NV) & 1);
+                if (!zero_v) ok = ok && wait(&v_full, n & 1);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t lbo_k = K == 128 ? 16384u : (uint32_t)(L::VB - st * L::STAGE);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, lbo_k, 1024),
-                                 sdesc(base + L::tp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
+                                 sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
                         if (!zero_v)
                             mma_bf16(tb + L::UA + 64 * p2,
-                                     sdesc(base + L::VB + (n % L::NV) * 16384 + ks * 2048, 8192,
-                                           1024),
-                                     sdesc(base + L::tpp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
+                                     sdesc(base + L::VB + ks * 2048, 8192, 1024),
+                                     sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
                     }
                     mma_commit(&bar_w);
                 }
@@ -650,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (tid == 0) {
                 if (ok) ok = wait(&bar_w, n & 1);
-                if (ok && !zero_v && n + L::NV < nchunks) load_v(n + L::NV);  // buffer consumed
+                if (ok && !zero_v && n + 1 < nchunks) load_v(n + 1);  // V consumed
             }
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
             {
@@ -660,7 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float v[32];
                     tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
                     tmem_ld_wait();
-                    store_row<4>(sm + L::nw(n), quad_row, 4 * colhalf, v, -1.f);
+                    store_row<4>(sm + L::NW, quad_row, 4 * colhalf, v, -1.f);
                 }
             }
             fence_proxy_async_smem();
@@ -749,10 +710,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // with v = 0 there is no U~ product: this one starts the accumulator
                 mma_bf16(tb + L::UA + 64 * (m & 1),
                          sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
+                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN,
                          zero_v ? (uint32_t)(ks > 0) : 1u);
             }
-            if constexpr (!PREP) mma_commit(&nw_free);
+            mma_commit(&nw_free);
             return true;
         };
         // O = [K; gamma Q] S^T for chunk m (token-major; TMEM lanes 64..127 hold
@@ -805,7 +766,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (sid == 0) {
                 mbar_arrive(&ua_free[p2]);
                 tc_fence_after();
-                const uint32_t pa = base + L::pa(n);  // rows 64..127 = P
+                const uint32_t pa = base + L::PT + p2 * 8192 - 8192;  // rows 64..127 = P
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
@@ -817,11 +778,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
                              sdesc(stg + L::KC0 + ks * 2048, 16384, 1024), I_DS, ks > 0);
                 mma_commit(&bar_s);
-                if constexpr (!PREP) mma_commit(&pt_free[p2]);
+                mma_commit(&pt_free[p2]);
                 ok = wait(&bar_s, n & 1);
                 if (ok && n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);  // stage consumed
-                // every product that reads ring stage n % 2 (-W^T, P) is done
-                if (ok && n + 2 < nchunks) load_prep(n + 2);
             }
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
@@ -906,15 +865,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
             }
-            for (int s = 0; s < L::NV; ++s) {
-                mbar_wait(&v_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&v_full[s], 1, kSpinLimit / 16);
-            }
-            if (PREP)
-                for (int s = 0; s < 2; ++s) {
-                    mbar_wait(&prep_full[s], 0, kSpinLimit / 16);
-                    mbar_wait(&prep_full[s], 1, kSpinLimit / 16);
-                }
+            mbar_wait(&v_full, 0, kSpinLimit / 16);
+            mbar_wait(&v_full, 1, kSpinLimit / 16);
         }
         __syncthreads();
     }
@@ -1084,6 +1036,520 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
     }
 }
 
+// ---------------------------------------------------------------- state-side pass
+// The two-pass form's second kernel: one CTA per (b, h) sequence (or segment)
+// walks its chunks like the fused kernel, but loads T', T'', P (one bulk copy
+// per chunk) instead of solving for them.  Its key group forms W^T and U~^T,
+// writes -W^T, scales Q by gamma and hands the state group the chunk's decay
+// factors; it depends on no state and runs ahead.  The state group keeps only
+// the state dependency chain serial:
+//
+//   U^T(n) = U~^T(n) + S(n-1) (-W^T(n))      (warp 8 issues)
+//   O^T(n) = S(n-1) (gamma Q(n))^T           (warp 9 issues, alongside)
+//   epilogue: U^T -> bf16, U^T diag(decay) -> bf16
+//   dS(n)  = U^T diag(decay) K(n)            (warp 8)
+//   O^T(n) += U^T P(n)^T                     (warp 9, alongside)
+//   S(n)   = gamma_C S(n-1) + dS(n)
+//
+// while warps 12-15 stage each chunk's output in the chunk's spent q/k stage
+// and store it with TMA (a ragged tail is clipped by the tensor map; the same
+// thread then loads the next q/k boxes into that stage), and warp 10 loads the
+// next T', T'', P.  O is computed transposed (value channels on the TMEM
+// lanes, 64 token columns), so two O accumulators fit in TMEM.  The q/k stage
+// holds the K blocks before the Q blocks; at K = 128 the bf16 U^T is written
+// over the chunk's gamma Q blocks once O^T's first product has read them.
+// Every state quantity is the fused kernel's arithmetic on the same operands,
+// so S_T is bit-identical to it (o agrees to the accumulation order of the
+// transposed product).
+template <int K>
+struct StLayout {
+    static constexpr int NSTAGE = 3;
+    static constexpr uint32_t KC0 = 0, KC1 = 8192;               // K blocks (KC1: K = 128)
+    static constexpr uint32_t QC0 = K == 128 ? 16384 : 8192, QC1 = QC0 + 8192;
+    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
+    static constexpr uint32_t VB = NSTAGE * STAGE;               // V: two buffers of 16 KB
+    static constexpr uint32_t PR = VB + 2 * 16384;               // ring of [T' | T'' | P]
+    static constexpr uint32_t SB = PR + 2 * kPrepChunkBytes;     // bf16 state, K/64 x 16 KB
+    static constexpr uint32_t UTS = SB + (K / 64) * 16384;       // U^T (K = 64 only)
+    static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);  // U^T diag(decay)
+    static constexpr uint32_t KGATE = UD + 16384;                // G2, gamma, beta
+    static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;        // 3 x (decay[64], gamma_C)
+    static constexpr uint32_t END = SGATE + 3 * 68 * 4;
+    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
+    static constexpr uint32_t V_BYTES = 2u * 8192u;
+    static constexpr size_t SMEM = END;
+    static_assert(SMEM + 1024 <= 232448, "shared memory budget");
+    static __device__ __forceinline__ uint32_t ut(int st) {
+        return K == 128 ? st * STAGE + QC0 : UTS;
+    }
+    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * kPrepChunkBytes; }
+    static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
+    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // -W^T over T', T''
+    static __device__ __forceinline__ uint32_t ptile(int n) { return tp(n) + 16384; }
+    // output staging of a chunk in stage st (16 KB, spent by then): two 64 x 64 tiles
+    static __device__ __forceinline__ uint32_t ost(int st) {
+        return st * STAGE + (K == 128 ? QC0 : 0u);
+    }
+    // TMEM columns: O^T of even / odd chunks, W^T, U~^T / U^T of even / odd chunks, dS
+    static constexpr uint32_t O0 = 0, WT = 64, UA = 128, O1 = 256, DS = 384;
+    static __device__ __forceinline__ uint32_t ocol(int n) { return (n & 1) ? O1 : O0; }
+};
+
+constexpr int kBarOut = 3;  // named barrier of the four output warps
+
+template <int K>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_state_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ alpha,
+                         const float *__restrict__ beta, const float *__restrict__ S0,
+                         bool want_o, float *__restrict__ ST, int T, int Ts, int H, int BH,
+                         SegPlan plan, const uint8_t *__restrict__ prep, int *status) {
+    using L = StLayout<K>;
+    constexpr int KH = K / 2;  // state columns per state-group thread
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0 && status) atomicOr(status, kStatusBounds);
+        return;
+    }
+    uint8_t *sm = smem_raw;
+    __shared__ uint64_t kq_full[3], v_full[2], prep_full[2], bar_w, bar_u, bar_o1, bar_s, bar_o2,
+        nw_ready[2], ua_free[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+    volatile int *abort_v = &abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const SegTask tk = segment_task(plan, K, T, S0, ST, BH);
+    const size_t seq = tk.seq;
+    const int t0 = tk.t0, t1 = tk.t1;
+    const bool zero_v = tk.zero_v;
+    const bool outs = want_o && tk.outputs;
+    const int b = (int)(seq / H), h = (int)(seq % H);
+    const int nchunks = (t1 - t0 + 63) / 64;
+    const uint32_t base = smem_u32(sm);
+    // T', T'', P of chunk n of this CTA's token range
+    const uint8_t *prep_seq = prep + (seq * (size_t)((T + 63) / 64) + t0 / 64) * kPrepChunkBytes;
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        if (outs) tma_prefetch_desc(&tm_o);
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0], &v_full[1],
+                            &prep_full[0], &prep_full[1], &bar_w, &bar_u, &bar_o1, &bar_s,
+                            &bar_o2, &nw_ready[0], &nw_ready[1], &ua_free[0], &ua_free[1]};
+        for (uint64_t *bb : bars) mbar_init(bb, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base_sh;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int quad_row = (warp & 3) * 32 + lane;  // TMEM lane of this thread
+    const int colhalf = (warp >> 2) & 1;          // which 32-column half this warp reads
+    // decay[64] and gamma_C of chunk n in slot n % 3 (written by the key group)
+    float *sg = reinterpret_cast<float *>(sm + L::SGATE);
+
+    auto load_kq = [&](int n) {
+        const int st = n % L::NSTAGE;
+        uint8_t *stg = sm + st * L::STAGE;
+        mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
+        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
+        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
+        if (K == 128) {
+            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
+            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
+        }
+    };
+    auto load_v = [&](int n) {
+        uint64_t *bar = &v_full[n & 1];
+        uint8_t *dst = sm + L::VB + (n & 1) * 16384;
+        mbar_arrive_expect_tx(bar, L::V_BYTES);
+        tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
+        tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
+    };
+    auto load_prep = [&](int n) {
+        mbar_arrive_expect_tx(&prep_full[n & 1], kPrepChunkBytes);
+        bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes, kPrepChunkBytes,
+                  &prep_full[n & 1]);
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
+        if (!ok) *abort_v = 1;
+        return ok;
+    };
+
+    constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);  // K-major x K-major, N = 64
+    constexpr uint32_t I_AMN = idesc_bf16(128, 64, true, false);  // MN-major A
+    constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);  // MN-major B, N = 64
+    constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);    // MN-major B, N = K
+
+    bool failed = false;
+
+    if (tid < kKeyThreads) {
+        // ================================================================ key group
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+        float *G2 = reinterpret_cast<float *>(sm + L::KGATE);
+        float *gam = G2 + 64;
+        float *bet = G2 + 128;
+        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
+        auto prefetch_gates = [&](int n) {
+            if (warp == 1 && n < nchunks) {
+                const int nv = min(64, t1 - t0 - n * 64);
+                const size_t i0 = ((size_t)b * Ts + t0 + n * 64 + lane) * H + h;
+                const size_t i1 = i0 + (size_t)32 * H;
+                pa0 = lane < nv ? alpha[i0] : 1.f;
+                pb0 = lane < nv ? beta[i0] : 0.f;
+                pa1 = lane + 32 < nv ? alpha[i1] : 1.f;
+                pb1 = lane + 32 < nv ? beta[i1] : 0.f;
+            }
+        };
+        prefetch_gates(0);
+        if (tid == 0) {
+            for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
+            if (!zero_v)
+                for (int m = 0; m < 2 && m < nchunks; ++m) load_v(m);
+            for (int m = 0; m < 2 && m < nchunks; ++m) load_prep(m);
+        }
+        for (int n = 0; n < nchunks; ++n) {
+            const int st = n % L::NSTAGE;  // q/k stage
+            const int p2 = n & 1;          // V buffer, operand ring stage, U~ accumulator
+            const uint32_t stg = base + st * L::STAGE;
+            const int nvalid = min(64, t1 - t0 - n * 64);
+            bool ok = true;
+            if (tid == 0) {
+                // warm L2 for loads two and three chunks ahead (they are
+                // copied in only when a ring slot frees)
+                if (n + 2 < nchunks)
+                    bulk_prefetch_l2(prep_seq + (size_t)(n + 2) * kPrepChunkBytes,
+                                     kPrepChunkBytes);
+                if (!zero_v && n + 3 < nchunks) {
+                    tma_prefetch_l2_4d(&tm_v, 0, h, t0 + (n + 3) * 64, b);
+                    tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + 3) * 64, b);
+                }
+                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+                if (ok) ok = wait(&prep_full[p2], (n >> 1) & 1);
+            }
+            if (warp == 1) {
+                chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
+                __syncwarp();
+                // the state group's decay to the chunk end and gamma_C; slot
+                // n % 3 was last read by the state group's chunk n - 3, which
+                // finished before this chunk's q/k boxes could load
+                float *slot = sg + (n % 3) * 68;
+                const float gC = G2[63];
+                slot[lane] = exp2f(gC - G2[lane]);
+                slot[lane + 32] = exp2f(gC - G2[lane + 32]);
+                if (lane == 0) slot[64] = exp2f(gC);
+                prefetch_gates(n + 1);
+            }
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+
+            // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
+            if (tid == 0) {
+                if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
+                if (!zero_v) ok = ok && wait(&v_full[p2], (n >> 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, 8192, 1024),
+                                 sdesc(base + L::tp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
+                        if (!zero_v)
+                            mma_bf16(tb + L::UA + 64 * p2,
+                                     sdesc(base + L::VB + p2 * 16384 + ks * 2048, 8192, 1024),
+                                     sdesc(base + L::tpp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
+                    }
+                    mma_commit(&bar_w);
+                }
+            }
+            uint8_t *stq = sm + st * L::STAGE;
+            // Q <- diag(gamma) Q in place while the products run (they read the
+            // K blocks, V and T', T''; Q is next read by O^T)
+#pragma unroll
+            for (int e = tid; e < (K / 64) * 512; e += kKeyThreads) {
+                const int blk_i = e >> 9, ee = e & 511;
+                uint4 *p = reinterpret_cast<uint4 *>(stq + (blk_i ? L::QC1 : L::QC0) + ee * 16);
+                const float g = gam[ee >> 3];
+                uint4 w = *p;
+                uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float2 f =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[c]));
+                    wv[c] = pack_bf16(f.x * g, f.y * g);
+                }
+                *p = w;
+            }
+            if (tid == 0) {
+                if (ok) ok = wait(&bar_w, n & 1);
+                if (ok && !zero_v && n + 2 < nchunks) load_v(n + 2);  // buffer consumed
+            }
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+            {
+                // -W^T over T', T'' (consumed by the products above)
+                tc_fence_after();
+                if (quad_row < K) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
+                    tmem_ld_wait();
+                    store_row<4>(sm + L::nw(n), quad_row, 4 * colhalf, v, -1.f);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+            // one barrier per chunk parity: the key group may finish chunk n + 1
+            // before the state group has waited for chunk n; chunk n + 2 needs
+            // operands that are loaded only after the state group passed chunk n
+            if (tid == 0) mbar_arrive(&nw_ready[p2]);
+        }
+    } else {
+        // ================================================================ state group
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
+        const int sid = tid - kKeyThreads;  // 0..255
+        const int sw = sid >> 5;            // state warp 0..7
+        const int c = quad_row;             // state row = TMEM lane = value channel
+        const int hf = sw >> 2;             // column half
+        // initial state: fp32 registers + bf16 operand copy
+        float S[KH];
+        {
+            const int j0 = hf * KH;
+#pragma unroll
+            for (int j = 0; j < KH; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tk.s0p) x = *reinterpret_cast<const float4 *>(tk.s0p + (size_t)c * K + j0 + j);
+                if (tk.s0_identity) {
+                    x.x = (c == j0 + j) ? 1.f : 0.f;
+                    x.y = (c == j0 + j + 1) ? 1.f : 0.f;
+                    x.z = (c == j0 + j + 2) ? 1.f : 0.f;
+                    x.w = (c == j0 + j + 3) ? 1.f : 0.f;
+                }
+                S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+            }
+#pragma unroll
+            for (int p = 0; p < KH / 32; ++p) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
+                const int j = j0 + 32 * p;
+                store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(kBarState, kStateThreads);
+
+        // U^T += S (-W^T) of chunk m (warp 8, once the key group handed over -W^T)
+        auto issue_u = [&](int m) -> bool {
+            if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < K / 16; ++ks) {
+                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                // with v = 0 there is no U~ product: this one starts the accumulator
+                mma_bf16(tb + L::UA + 64 * (m & 1),
+                         sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
+                         sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
+                         zero_v ? (uint32_t)(ks > 0) : 1u);
+            }
+            mma_commit(&bar_u);
+            return true;
+        };
+        // O^T = S (gamma Q)^T of chunk m (warp 9, also after gamma Q is ready)
+        auto issue_o1 = [&](int m) -> bool {
+            if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
+            tc_fence_after();
+            const uint32_t stg = base + (m % L::NSTAGE) * L::STAGE;
+#pragma unroll
+            for (int ks = 0; ks < K / 16; ++ks) {
+                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                mma_bf16(tb + L::ocol(m), sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
+                         sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM, ks > 0);
+            }
+            mma_commit(&bar_o1);
+            return true;
+        };
+        // chunk m's O^T -> staging tile in its spent q/k stage -> TMA store, by
+        // warps 12-15 (TMEM lane quarter w % 4, all 64 columns).  One thread
+        // waits for the products (the last readers of the stage); false on a
+        // timeout (the same for all 128 threads).
+        auto store_out = [&](int m) -> bool {
+            bool okw = true;
+            if (sid == 128) okw = wait(&bar_o2, m & 1);
+            if (named_sync_or(kBarOut, 128, !okw)) return false;
+            tc_fence_after();
+            const bool odd = lane & 1;
+            uint8_t *tile = sm + L::ost(m % L::NSTAGE) + (c >> 6) * 8192;
+            const uint32_t cb = (uint32_t)(c & 63) >> 3, cw = (uint32_t)(c & 6) * 2;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float v[32];
+                tmem_ld32(tb + lane_off + L::ocol(m) + 32 * half, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    // pairs of lanes swap one value: each writes two channels of one token
+                    const float got = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[i + 1], 1);
+                    const uint32_t t = 32 * half + i + (odd ? 1 : 0);
+                    const float lo = odd ? got : v[i], hi = odd ? v[i + 1] : got;
+                    *reinterpret_cast<uint32_t *>(tile + swz128(t, cb) + cw) = pack_bf16(lo, hi);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarOut, 128);
+            if (sid == 128) {
+                uint8_t *ost = sm + L::ost(m % L::NSTAGE);
+                tma_store_4d(&tm_o, ost, 0, h, t0 + m * 64, b);
+                tma_store_4d(&tm_o, ost + 8192, 64, h, t0 + m * 64, b);
+                bulk_commit_group();
+                // the stage is free once the store has read it: the q/k boxes
+                // three chunks ahead go there
+                bulk_wait_read_all();
+                if (m + L::NSTAGE < nchunks) load_kq(m + L::NSTAGE);
+            }
+            return true;
+        };
+        if (sw <= 1) {
+            bool ok0 = true;
+            if (lane == 0) ok0 = sw == 0 ? issue_u(0) : (outs ? issue_o1(0) : true);
+            ok0 = __shfl_sync(0xffffffffu, ok0, 0);
+            failed = !ok0;
+        }
+
+        for (int n = 0; n < nchunks; ++n) {
+            const int st = n % L::NSTAGE;
+            const int p2 = n & 1;
+            const uint32_t stg = base + st * L::STAGE;
+            // ---- U epilogue: U^T -> bf16 (over gamma Q once O^T has read it) and
+            // ---- U^T diag(decay) -> UD ----
+            const float *slot = sg + (n % 3) * 68;
+            bool ok = !failed;
+            if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
+            if (sid == 0 && ok && outs) ok = wait(&bar_o1, n & 1);
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            {
+                tc_fence_after();
+                float v[32];
+                tmem_ld32(tb + lane_off + L::UA + 64 * p2 + 32 * hf, v);
+                tmem_ld_wait();
+                store_row<4>(sm + L::ut(st) + (c >> 6) * 8192, c & 63, 4 * hf, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= slot[32 * hf + i];
+                store_row<4>(sm + L::UD, c, 4 * hf, v);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarState, kStateThreads);
+            // ---- dS = U^T diag(decay) K (warp 8) and O^T += U^T P^T (warp 9) ----
+            if (sid == 0) {
+                mbar_arrive(&ua_free[p2]);
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
+                             sdesc(stg + L::KC0 + ks * 2048, 8192, 1024), I_DS, ks > 0);
+                mma_commit(&bar_s);
+                ok = wait(&bar_s, n & 1);
+            } else if (sid == 32 && outs) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + L::ocol(n), sdesc(base + L::ut(st) + ks * 32, 16, 1024),
+                             sdesc(base + L::ptile(n) + ks * 32, 16, 1024), I_MM, 1);
+                mma_commit(&bar_o2);
+            }
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
+            {
+                tc_fence_after();
+                const float gC = slot[64];
+                const int j0 = hf * KH;
+#pragma unroll
+                for (int p = 0; p < KH / 32; ++p) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::DS + j0 + 32 * p, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        S[32 * p + i] = fmaf(gC, S[32 * p + i], v[i]);
+                        v[i] = S[32 * p + i];
+                    }
+                    const int j = j0 + 32 * p;
+                    store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarState, kStateThreads);
+            // ---- next chunk's products (warps 8, 9), loads (warp 10), this
+            // ---- chunk's output (warps 12-15) ----
+            bool ok1 = true;
+            if (sw == 0) {
+                if (lane == 0 && n + 1 < nchunks) ok1 = issue_u(n + 1);
+            } else if (sw == 1) {
+                if (lane == 0 && outs && n + 1 < nchunks) ok1 = issue_o1(n + 1);
+            } else if (sw == 2) {
+                // ring stage n % 2 is free once O^T += U^T P^T (the last reader of
+                // P) has completed; without outputs stage n % 3 is free as well
+                // (with outputs it stages them and is reloaded after the store)
+                if (lane == 0) {
+                    if (outs) ok1 = wait(&bar_o2, n & 1);
+                    if (ok1 && !outs && n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);
+                    if (ok1 && n + 2 < nchunks) load_prep(n + 2);
+                }
+            } else if (sw >= 4 && outs) {
+                ok1 = store_out(n);
+            }
+            if (sw <= 2) ok1 = __shfl_sync(0xffffffffu, ok1, 0);
+            if (!ok1) failed = true;
+        }
+        if (sid == 128 && outs) bulk_wait_all();  // outputs written before the CTA ends
+        if (!failed && tk.stp != nullptr) {
+            const int j0 = hf * KH;
+#pragma unroll
+            for (int j = 0; j < KH; j += 4)
+                *reinterpret_cast<float4 *>(tk.stp + (size_t)c * K + j0 + j) =
+                    make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+    }
+
+    if (failed) *abort_v = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_v) {
+        if (tid == 0) {
+            if (status) atomicOr(status, kStatusTimeout);
+            // let in-flight loads land before the CTA's shared memory is released
+            for (int s = 0; s < 3; ++s) {
+                mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
+            }
+            for (int s = 0; s < 2; ++s) {
+                mbar_wait(&v_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&v_full[s], 1, kSpinLimit / 16);
+                mbar_wait(&prep_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&prep_full[s], 1, kSpinLimit / 16);
+            }
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1187,44 +1653,48 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
     return cudaGetLastError();
 }
 
-template <int K, bool PREP>
+// Whole-sequence launch, or the segment-parallel sequence (first pass,
+// combine, second pass) of the one-pass kernel (prep == nullptr) or of the
+// state-side kernel of the two-pass form.
+template <int K>
 cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                   const float *alpha, const float *beta, const float *S0, void *o, float *ST,
-                   long long BH, int T, int Ts, int H, const SegShape &sh, float *ws,
-                   const uint8_t *prep, cudaStream_t stream) {
-    using L = TcLayout<K, PREP>;
-    auto kern = prefill_tc_kernel<K, PREP>;
-    static bool attr_set[64] = {};
+                   const CUtensorMap &mo, const float *alpha, const float *beta, const float *S0,
+                   void *o, float *ST, long long BH, int T, int Ts, int H, const SegShape &sh,
+                   float *ws, const uint8_t *prep, cudaStream_t stream) {
+    static bool attr_set[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)L::SMEM);
+    const int two = prep != nullptr;
+    const size_t smem = two ? StLayout<K>::SMEM : TcLayout<K>::SMEM;
+    if (!attr_set[two][dev]) {
+        const cudaError_t e =
+            two ? cudaFuncSetAttribute(prefill_state_kernel<K>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                : cudaFuncSetAttribute(prefill_tc_kernel<K>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[two][dev] = true;
     }
     __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(o);
     int *status = device_status_ptr();
-    if (sh.nseg == 1) {
-        kern<<<(unsigned)BH, kTcThreads, L::SMEM, stream>>>(
-            mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH, SegPlan{kWhole, 1, T, nullptr},
-            prep, status);
+    auto launch = [&](long long grid, SegPlan plan) {
+        if (two)
+            prefill_state_kernel<K><<<(unsigned)grid, kTcThreads, smem, stream>>>(
+                mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan, prep,
+                status);
+        else
+            prefill_tc_kernel<K><<<(unsigned)grid, kTcThreads, smem, stream>>>(
+                mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH, plan, status);
         return cudaGetLastError();
-    }
-    const long long g1 = BH * (2 * sh.nseg - 1), g2 = BH * (sh.nseg - 1);
-    kern<<<(unsigned)g1, kTcThreads, L::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
-        SegPlan{kFirst, sh.nseg, sh.seg_len, ws}, prep, status);
-    cudaError_t e = cudaGetLastError();
+    };
+    if (sh.nseg == 1) return launch(BH, SegPlan{kWhole, 1, T, nullptr});
+    cudaError_t e = launch(BH * (2 * sh.nseg - 1), SegPlan{kFirst, sh.nseg, sh.seg_len, ws});
     if (e != cudaSuccess) return e;
     segment_combine_kernel<K><<<dim3((unsigned)BH, 128 / 16), 256, 0, stream>>>(ws, (int)BH,
                                                                                 sh.nseg);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)g2, kTcThreads, L::SMEM, stream>>>(
-        mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH,
-        SegPlan{kSecond, sh.nseg, sh.seg_len, ws}, prep, status);
-    return cudaGetLastError();
+    return launch(BH * (sh.nseg - 1), SegPlan{kSecond, sh.nseg, sh.seg_len, ws});
 }
 
 template <int K>
@@ -1232,10 +1702,16 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
                         const float *beta, const float *S0, void *o, float *ST, int B, int T,
                         int Ts, int H, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_token_map(&mq, q, B, T, Ts, H, K) || !make_token_map(&mk, k, B, T, Ts, H, K) ||
         !make_token_map(&mv, v, B, T, Ts, H, 128))
         return cudaErrorInvalidValue;
+    // outputs of the two-pass form go out by TMA store (unused without outputs)
+    if (o) {
+        if (!make_token_map(&mo, o, B, T, Ts, H, 128)) return cudaErrorInvalidValue;
+    } else {
+        mo = mv;
+    }
     const long long BH = (long long)B * H;
     const SegShape sh = segment_shape(B * H, T, K, sm_count());
     if (sh.nseg == 1 && BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1252,11 +1728,11 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
         uint8_t *prep = static_cast<uint8_t *>(workspace) + prep_off;
         const cudaError_t e = launch_prep<K>(mq, mk, alpha, beta, prep, BH, T, Ts, H, stream);
         if (e != cudaSuccess) return e;
-        return run_tc<K, true>(mq, mk, mv, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, prep,
-                               stream);
+        return run_tc<K>(mq, mk, mv, mo, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, prep,
+                         stream);
     }
-    return run_tc<K, false>(mq, mk, mv, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, nullptr,
-                            stream);
+    return run_tc<K>(mq, mk, mv, mo, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, nullptr,
+                     stream);
 }
 
 }  // namespace
