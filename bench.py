@@ -207,13 +207,16 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
     d = problem_to_dev(p, torch)
     o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
     ST = torch.empty((B, H, V, K), dtype=torch.float32, device="cuda")
+    # two-pass form: the workspace holds every chunk's key-side operands
+    wsb = binding.gdn_prefill_two_pass_workspace_size(B, T, H, K, V, binding.GDN_BF16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
 
     def step():
         binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T, H,
-                            K, V, binding.GDN_BF16)
+                            K, V, binding.GDN_BF16, ws, wsb)
 
     total_ms, per = time_calls(step, args.steps, args.warmup, torch, barrier)
-    launches += args.steps
+    launches += 2 * args.steps  # key-side pass + state pass
     total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
     tokens = B * T * world * args.steps
@@ -226,6 +229,19 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
     status = binding.gdn_get_last_device_status()
 
     extra = {}
+    # the one-pass form (no workspace) on the same inputs, for comparison
+    if not args.quick:
+        def step1():
+            binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T,
+                                H, K, V, binding.GDN_BF16)
+
+        t1, _ = time_calls(step1, args.steps, args.warmup, torch, barrier)
+        t1 = max_over_ranks(t1)
+        extra["one_pass"] = {"ms_per_step": t1 / args.steps,
+                             "tokens_per_s": B * T * world * args.steps / (t1 / 1e3),
+                             "two_pass_speedup": t1 / total_ms, "launches": args.steps,
+                             "note": "gdn_prefill without the two-pass workspace (one fused "
+                                     "kernel); identical results"}
     SECTIONS = ("pruned", "prologue", "state_rank", "truncation", "drrqr", "long_context",
                 "gated", "fp32", "decode")
 
@@ -237,10 +253,11 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         pp = inputs.make_prefill(B=B, T=T, H=H, K=K, V=V, pruned_K=64)
         dp = problem_to_dev(pp, torch)
         STp = torch.empty((B, H, V, 64), dtype=torch.float32, device="cuda")
+        wsb64 = binding.gdn_prefill_two_pass_workspace_size(B, T, H, 64, V, binding.GDN_BF16)
 
         def step64():
             binding.gdn_prefill(dp["q"], dp["k"], dp["v"], dp["alpha"], dp["beta"], None, o, STp,
-                                B, T, H, 64, V, binding.GDN_BF16)
+                                B, T, H, 64, V, binding.GDN_BF16, ws, wsb64)
 
         if want("pruned"):
             t64, per64 = time_calls(step64, args.steps, args.warmup, torch, barrier)
@@ -335,9 +352,9 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
             "unit": "GB/s" if roof_bound == "hbm" else "TFLOP/s",
             "frac": (achieved_gbs / peaks["hbm_gbs"]) if roof_bound == "hbm"
             else achieved_tf / peaks["bf16_tflops"],
-            "traffic": measured_traffic("prefill_tc_d128_prefill-workload.md",
+            "traffic": measured_traffic("prefill_two_pass_d128_prefill-workload.md",
                                         "gdn_prefill_tc.cu"),
-            "kernel": "gdn_prefill",
+            "kernel": "gdn_prefill (two-pass: prefill_prep_kernel + prefill_state_kernel)",
             "algorithmic_bytes": byts,
             "algorithmic_flops": flops,
             "tensor_frac": achieved_tf / peaks["bf16_tflops"],
@@ -493,10 +510,13 @@ def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over
         binding.gdn_gather_normalize(d["q"], idx, qg, B * T, H, Kin, Kout, binding.GDN_BF16)
         binding.gdn_gather_normalize(d["k"], idx, kg, B * T, H, Kin, Kout, binding.GDN_BF16)
 
+    wsb = binding.gdn_prefill_two_pass_workspace_size(B, T, H, Kout, V, binding.GDN_BF16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+
     def pipeline():
         pro()
         binding.gdn_prefill(qg, kg, dp["v"], dp["alpha"], dp["beta"], None, o, ST, B, T, H,
-                            Kout, V, binding.GDN_BF16)
+                            Kout, V, binding.GDN_BF16, ws, wsb)
 
     tp, _ = time_calls(pro, args.steps, args.warmup, torch, barrier)
     tp = max_over_ranks(tp)
@@ -509,7 +529,7 @@ def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over
             "prologue_hbm_frac": gbs / peaks["hbm_gbs"],
             "pipeline_ms_per_step": tl / args.steps,
             "pipeline_tokens_per_s": B * T * world * args.steps / (tl / 1e3),
-            "launches": args.steps * 5}
+            "launches": args.steps * 6}
 
 
 def bench_truncation(args, torch, binding, d, ST, barrier, max_over_ranks, world):
@@ -654,22 +674,29 @@ def bench_gated(args, torch, binding, inputs, peaks, barrier, max_over_ranks, wo
 def bench_long(args, torch, binding, inputs, peaks, barrier, max_over_ranks, world):
     """Long-context prefill (B=1, T=65536, H=16, d_k=d_v=128, alpha in
     [0.9995, 0.9999], keys in a narrow cone) and the stable rank of its final
-    states.  Few heads and a long sequence: the prefill runs segment-parallel
-    with the workspace reported by gdn_prefill_workspace_size."""
+    states.  Few heads and a long sequence: the prefill runs segment-parallel,
+    in the two-pass form (workspace of gdn_prefill_two_pass_workspace_size)."""
     p = inputs.make_long()
     B, T, H, K = p.k.shape
     V = p.v.shape[-1]
     d = problem_to_dev(p, torch)
     o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
     ST = torch.empty((B, H, V, K), dtype=torch.float32, device="cuda")
-    wsb = binding.gdn_prefill_workspace_size(B, T, H, K, V, binding.GDN_BF16)
+    wsb = binding.gdn_prefill_two_pass_workspace_size(B, T, H, K, V, binding.GDN_BF16)
+    wsb1 = binding.gdn_prefill_workspace_size(B, T, H, K, V, binding.GDN_BF16)
     ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
 
     def step():
         binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T, H,
-                            K, V, binding.GDN_BF16, ws if wsb else None, wsb)
+                            K, V, binding.GDN_BF16, ws, wsb)
+
+    def step1():  # one-pass form: the segment scratch only
+        binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T, H,
+                            K, V, binding.GDN_BF16, ws, wsb1)
 
     steps = max(3, min(args.steps, 10))
+    tot1, _ = time_calls(step1, steps, 3, torch, barrier)
+    tot1 = max_over_ranks(tot1)
     tot, per = time_calls(step, steps, 3, torch, barrier)
     tot = max_over_ranks(tot)
     ms = tot / steps
@@ -682,6 +709,7 @@ def bench_long(args, torch, binding, inputs, peaks, barrier, max_over_ranks, wor
             "achieved_gbs": prefill_bytes(B, T, H, K, V) / (ms / 1e3) / 1e9,
             "hbm_frac": prefill_bytes(B, T, H, K, V) / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
             "workspace_bytes": wsb,
+            "one_pass_ms_per_step": tot1 / steps,
             "stable_rank_per_head": [round(float(x), 3) for x in er.cpu()]}
 
 

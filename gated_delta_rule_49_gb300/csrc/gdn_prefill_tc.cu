@@ -1068,8 +1068,9 @@ struct StLayout {
     static constexpr uint32_t QC0 = K == 128 ? 16384 : 8192, QC1 = QC0 + 8192;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
     static constexpr uint32_t VB = NSTAGE * STAGE;               // V: two buffers of 16 KB
-    static constexpr uint32_t PR = VB + 2 * 16384;               // ring of [T' | T'' | P]
-    static constexpr uint32_t SB = PR + 2 * kPrepChunkBytes;     // bf16 state, K/64 x 16 KB
+    static constexpr uint32_t PR = VB + 2 * 16384;               // ring of [T' | T'']
+    static constexpr uint32_t PP = PR + 2 * 16384;               // ring of P
+    static constexpr uint32_t SB = PP + 2 * 8192;                // bf16 state, K/64 x 16 KB
     static constexpr uint32_t UTS = SB + (K / 64) * 16384;       // U^T (K = 64 only)
     static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);  // U^T diag(decay)
     static constexpr uint32_t KGATE = UD + 16384;                // G2, gamma, beta
@@ -1082,10 +1083,10 @@ struct StLayout {
     static __device__ __forceinline__ uint32_t ut(int st) {
         return K == 128 ? st * STAGE + QC0 : UTS;
     }
-    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * kPrepChunkBytes; }
+    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * 16384; }
     static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
     static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // -W^T over T', T''
-    static __device__ __forceinline__ uint32_t ptile(int n) { return tp(n) + 16384; }
+    static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
     // output staging of a chunk in stage st (16 KB, spent by then): two 64 x 64 tiles
     static __device__ __forceinline__ uint32_t ost(int st) {
         return st * STAGE + (K == 128 ? QC0 : 0u);
@@ -1095,7 +1096,7 @@ struct StLayout {
     static __device__ __forceinline__ uint32_t ocol(int n) { return (n & 1) ? O1 : O0; }
 };
 
-constexpr int kBarOut = 3;  // named barrier of the four output warps
+constexpr int kBarOut = 3, kBarOut2 = 4;  // the output warps (11-15)
 
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -1114,8 +1115,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full[3], v_full[2], prep_full[2], bar_w, bar_u, bar_o1, bar_s, bar_o2,
-        nw_ready[2], ua_free[2];
+    __shared__ uint64_t kq_full[3], v_full[2], tt_full[2], p_full[2], bar_w, bar_u, bar_o1, bar_s,
+        bar_o2, nw_ready[2], ua_free[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -1142,9 +1143,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         if (outs) tma_prefetch_desc(&tm_o);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0], &v_full[1],
-                            &prep_full[0], &prep_full[1], &bar_w, &bar_u, &bar_o1, &bar_s,
-                            &bar_o2, &nw_ready[0], &nw_ready[1], &ua_free[0], &ua_free[1]};
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0],  &v_full[1],
+                            &tt_full[0], &tt_full[1], &p_full[0],  &p_full[1],  &bar_w,
+                            &bar_u,      &bar_o1,     &bar_s,      &bar_o2,     &nw_ready[0],
+                            &nw_ready[1], &ua_free[0], &ua_free[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -1177,10 +1179,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
         tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
     };
-    auto load_prep = [&](int n) {
-        mbar_arrive_expect_tx(&prep_full[n & 1], kPrepChunkBytes);
-        bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes, kPrepChunkBytes,
-                  &prep_full[n & 1]);
+    // T', T'' of chunk n into ring stage n % 2 (key group), P into its own ring
+    // (state group's O^T); one chunk's block in global memory is [T' | T'' | P]
+    auto load_tt = [&](int n) {
+        mbar_arrive_expect_tx(&tt_full[n & 1], 16384);
+        bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes, 16384, &tt_full[n & 1]);
+    };
+    auto load_p = [&](int n) {
+        mbar_arrive_expect_tx(&p_full[n & 1], 8192);
+        bulk_load(sm + L::ptile(n), prep_seq + (size_t)n * kPrepChunkBytes + 16384, 8192,
+                  &p_full[n & 1]);
     };
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
@@ -1218,7 +1226,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
             if (!zero_v)
                 for (int m = 0; m < 2 && m < nchunks; ++m) load_v(m);
-            for (int m = 0; m < 2 && m < nchunks; ++m) load_prep(m);
+            for (int m = 0; m < 2 && m < nchunks; ++m) {
+                load_tt(m);
+                if (outs) load_p(m);
+            }
         }
         for (int n = 0; n < nchunks; ++n) {
             const int st = n % L::NSTAGE;  // q/k stage
@@ -1237,7 +1248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + 3) * 64, b);
                 }
                 ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
-                if (ok) ok = wait(&prep_full[p2], (n >> 1) & 1);
+                if (ok) ok = wait(&tt_full[p2], (n >> 1) & 1);
             }
             if (warp == 1) {
                 chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
@@ -1250,7 +1261,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 slot[lane] = exp2f(gC - G2[lane]);
                 slot[lane + 32] = exp2f(gC - G2[lane + 32]);
                 if (lane == 0) slot[64] = exp2f(gC);
-                prefetch_gates(n + 1);
             }
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
 
@@ -1290,10 +1300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 *p = w;
             }
-            if (tid == 0) {
-                if (ok) ok = wait(&bar_w, n & 1);
-                if (ok && !zero_v && n + 2 < nchunks) load_v(n + 2);  // buffer consumed
-            }
+            if (tid == 0 && ok) ok = wait(&bar_w, n & 1);
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
             {
                 // -W^T over T', T'' (consumed by the products above)
@@ -1311,7 +1318,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // one barrier per chunk parity: the key group may finish chunk n + 1
             // before the state group has waited for chunk n; chunk n + 2 needs
             // operands that are loaded only after the state group passed chunk n
-            if (tid == 0) mbar_arrive(&nw_ready[p2]);
+            if (tid == 0) {
+                mbar_arrive(&nw_ready[p2]);
+                // U~^T has read this V buffer (bar_w above)
+                if (!zero_v && n + 2 < nchunks) load_v(n + 2);
+            }
+            prefetch_gates(n + 1);
         }
     } else {
         // ================================================================ state group
@@ -1379,46 +1391,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_commit(&bar_o1);
             return true;
         };
-        // chunk m's O^T -> staging tile in its spent q/k stage -> TMA store, by
-        // warps 12-15 (TMEM lane quarter w % 4, all 64 columns).  One thread
-        // waits for the products (the last readers of the stage); false on a
-        // timeout (the same for all 128 threads).
+        // chunk m's O^T -> staging tile in its spent q/k stage, by warps 12-15
+        // (TMEM lane quarter w % 4, all 64 columns), then a TMA store by warp
+        // 11 (which reloads the stage with the q/k boxes of chunk m + 3 once
+        // the store has read it, at the top of the next chunk: reload_stage).
+        // Called by warps 11-15; one thread waits for the products (the last
+        // readers of the stage) and all 160 take the same branch on a timeout
+        // (false).
         auto store_out = [&](int m) -> bool {
             bool okw = true;
             if (sid == 128) okw = wait(&bar_o2, m & 1);
-            if (named_sync_or(kBarOut, 128, !okw)) return false;
-            tc_fence_after();
-            const bool odd = lane & 1;
-            uint8_t *tile = sm + L::ost(m % L::NSTAGE) + (c >> 6) * 8192;
-            const uint32_t cb = (uint32_t)(c & 63) >> 3, cw = (uint32_t)(c & 6) * 2;
+            if (named_sync_or(kBarOut, 160, !okw)) return false;
+            if (sw >= 4) {
+                tc_fence_after();
+                const bool odd = lane & 1;
+                uint8_t *tile = sm + L::ost(m % L::NSTAGE) + (c >> 6) * 8192;
+                const uint32_t cb = (uint32_t)(c & 63) >> 3, cw = (uint32_t)(c & 6) * 2;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float v[32];
-                tmem_ld32(tb + lane_off + L::ocol(m) + 32 * half, v);
-                tmem_ld_wait();
+                for (int half = 0; half < 2; ++half) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::ocol(m) + 32 * half, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    // pairs of lanes swap one value: each writes two channels of one token
-                    const float got = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[i + 1], 1);
-                    const uint32_t t = 32 * half + i + (odd ? 1 : 0);
-                    const float lo = odd ? got : v[i], hi = odd ? v[i + 1] : got;
-                    *reinterpret_cast<uint32_t *>(tile + swz128(t, cb) + cw) = pack_bf16(lo, hi);
+                    for (int i = 0; i < 32; i += 2) {
+                        // pairs of lanes swap one value: each writes two channels of one token
+                        const float got = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[i + 1], 1);
+                        const uint32_t t = 32 * half + i + (odd ? 1 : 0);
+                        const float lo = odd ? got : v[i], hi = odd ? v[i + 1] : got;
+                        *reinterpret_cast<uint32_t *>(tile + swz128(t, cb) + cw) =
+                            pack_bf16(lo, hi);
+                    }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(kBarOut, 128);
-            if (sid == 128) {
+            named_sync(kBarOut2, 160);  // the tile is written
+            if (sw == 3 && lane == 0) {
                 uint8_t *ost = sm + L::ost(m % L::NSTAGE);
                 tma_store_4d(&tm_o, ost, 0, h, t0 + m * 64, b);
                 tma_store_4d(&tm_o, ost + 8192, 64, h, t0 + m * 64, b);
                 bulk_commit_group();
-                // the stage is free once the store has read it: the q/k boxes
-                // three chunks ahead go there
-                bulk_wait_read_all();
-                if (m + L::NSTAGE < nchunks) load_kq(m + L::NSTAGE);
             }
             return true;
+        };
+        // warp 11, lane 0: the store of chunk m has read stage m % 3 -> q/k of m + 3
+        auto reload_stage = [&](int m) {
+            if (m >= 0 && m + L::NSTAGE < nchunks) {
+                bulk_wait_read_all();
+                load_kq(m + L::NSTAGE);
+            }
         };
         if (sw <= 1) {
             bool ok0 = true;
@@ -1437,6 +1458,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = !failed;
             if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
             if (sid == 0 && ok && outs) ok = wait(&bar_o1, n & 1);
+            if (sid == 32 && ok && n + 2 < nchunks) {
+                // U^T has read -W^T: ring stage n % 2 takes chunk n + 2's T', T''
+                ok = wait(&bar_u, n & 1);
+                if (ok) load_tt(n + 2);
+            }
+            if (sid == 96 && outs) reload_stage(n - 1);
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             {
                 tc_fence_after();
@@ -1462,6 +1489,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mma_commit(&bar_s);
                 ok = wait(&bar_s, n & 1);
             } else if (sid == 32 && outs) {
+                ok = wait(&p_full[p2], (n >> 1) & 1);
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -1500,21 +1528,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else if (sw == 1) {
                 if (lane == 0 && outs && n + 1 < nchunks) ok1 = issue_o1(n + 1);
             } else if (sw == 2) {
-                // ring stage n % 2 is free once O^T += U^T P^T (the last reader of
-                // P) has completed; without outputs stage n % 3 is free as well
-                // (with outputs it stages them and is reloaded after the store)
+                // P ring stage n % 2 is free once O^T += U^T P^T has completed;
+                // without outputs q/k stage n % 3 is free as well (with outputs
+                // it stages them and is reloaded after the store)
                 if (lane == 0) {
-                    if (outs) ok1 = wait(&bar_o2, n & 1);
-                    if (ok1 && !outs && n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);
-                    if (ok1 && n + 2 < nchunks) load_prep(n + 2);
+                    if (outs) {
+                        ok1 = wait(&bar_o2, n & 1);
+                        if (ok1 && n + 2 < nchunks) load_p(n + 2);
+                    } else if (n + L::NSTAGE < nchunks) {
+                        load_kq(n + L::NSTAGE);
+                    }
                 }
-            } else if (sw >= 4 && outs) {
+            } else if (sw >= 3 && outs) {
                 ok1 = store_out(n);
             }
             if (sw <= 2) ok1 = __shfl_sync(0xffffffffu, ok1, 0);
             if (!ok1) failed = true;
         }
-        if (sid == 128 && outs) bulk_wait_all();  // outputs written before the CTA ends
+        if (sw == 3 && lane == 0 && outs) bulk_wait_all();  // outputs written before the CTA ends
         if (!failed && tk.stp != nullptr) {
             const int j0 = hf * KH;
 #pragma unroll
@@ -1538,8 +1569,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int s = 0; s < 2; ++s) {
                 mbar_wait(&v_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&v_full[s], 1, kSpinLimit / 16);
-                mbar_wait(&prep_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&prep_full[s], 1, kSpinLimit / 16);
+                mbar_wait(&tt_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&tt_full[s], 1, kSpinLimit / 16);
+                mbar_wait(&p_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&p_full[s], 1, kSpinLimit / 16);
             }
         }
         __syncthreads();
