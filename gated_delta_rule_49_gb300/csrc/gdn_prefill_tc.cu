@@ -269,6 +269,15 @@ __device__ __forceinline__ void issue_kq_kt(uint32_t d1, uint32_t stg, uint32_t 
     }
 }
 
+// 2^x for x <= 0 (a decay between two tokens of a chunk) with the hardware
+// approximation (relative error about 2^-22; results below 2^-126 flush to
+// zero, far under the bf16 operands these factors scale).
+__device__ __forceinline__ float decay_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // A (float32, rows 0..63 of AF) and P (bf16 operand tile) from [K;Q] K^T in
 // TMEM; the thread holds TMEM lane quad_row, columns [32 colhalf, +32):
 //   A_ts = beta_t 2^(G_t - G_s) (k_t . k_s) for s < t, else 0
@@ -293,7 +302,7 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
                 const int s = s0 + i + e2;
-                a[e2] = s < t ? bt * exp2f(gt - gs[e2]) * v[i + e2] : 0.f;
+                a[e2] = s < t ? bt * decay_exp2(gt - gs[e2]) * v[i + e2] : 0.f;
             }
             *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) = make_float4(a[0], a[1], a[2], a[3]);
         }
@@ -304,7 +313,7 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
             const float gs[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2)
-                v[i + e2] = s0 + i + e2 <= t ? exp2f(gt - gs[e2]) * v[i + e2] : 0.f;
+                v[i + e2] = s0 + i + e2 <= t ? decay_exp2(gt - gs[e2]) * v[i + e2] : 0.f;
         }
         store_row<4>(Ptile, t, 4 * colhalf, v);
     }
@@ -312,11 +321,13 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
 
 // T' = T diag(beta gamma) and T'' = T diag(beta) as bf16 operand tiles from
 // the inverse in AF (T_ii in place, T_ij mirrored at block (j, i)); thread tid
-// of 256 writes row tid / 4, columns [16 (tid % 4), +16).  The tiles may be
-// shared or global memory.
+// of 256 writes row tid % 64, columns [16 (tid / 64), +16), so a warp reads
+// 32 consecutive rows of AF (conflict-free with the row stride of 68 floats)
+// and one broadcast slice of beta and gamma.  The tiles may be shared or
+// global memory.
 __device__ __forceinline__ void chunk_tprime(float *AF, const float *bet, const float *gam,
                                              uint8_t *TPtile, uint8_t *TPPtile, int tid) {
-    const int t = tid >> 2, cb = tid & 3;
+    const int t = tid & 63, cb = tid >> 6;
     const int bt = t >> 4;
     float x[16];
     if (cb > bt) {
@@ -332,10 +343,15 @@ __device__ __forceinline__ void chunk_tprime(float *AF, const float *bet, const 
     }
     float tp[16], tpp[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const int s = 16 * cb + c;
-        tpp[c] = x[c] * bet[s];
-        tp[c] = tpp[c] * gam[s];
+    for (int c = 0; c < 16; c += 4) {
+        const float4 b4 = *reinterpret_cast<const float4 *>(bet + 16 * cb + c);
+        const float4 g4 = *reinterpret_cast<const float4 *>(gam + 16 * cb + c);
+        const float bs[4] = {b4.x, b4.y, b4.z, b4.w}, gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            tpp[c + e] = x[c + e] * bs[e];
+            tp[c + e] = tpp[c + e] * gs[e];
+        }
     }
     store_row<2>(TPtile, t, 2 * cb, tp);
     store_row<2>(TPPtile, t, 2 * cb, tpp);
@@ -977,10 +993,19 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
             pb1 = lane + 32 < nv ? beta[i1] : 0.f;
         }
     };
+    // bounded wait that sleeps between polls: other CTAs on the SM are busy
+    // with shared memory, which a tight poll would take cycles from
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-        const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
-        if (!ok) *abort_v = 1;
-        return ok;
+        if (mbar_try_wait(bar, parity)) return true;
+        const long long c0 = clock64();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*abort_v || clock64() - c0 > kSpinLimit) {
+                *abort_v = 1;
+                return false;
+            }
+            __nanosleep(64);
+        }
+        return true;
     };
 
     const long long G = gridDim.x;
