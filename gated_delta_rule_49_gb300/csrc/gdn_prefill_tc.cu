@@ -1063,11 +1063,11 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
 
 // ---------------------------------------------------------------- state-side pass
 // The two-pass form's second kernel: one CTA per (b, h) sequence (or segment)
-// walks its chunks like the fused kernel, but loads T', T'', P (one bulk copy
-// per chunk) instead of solving for them.  Its key group forms W^T and U~^T,
-// writes -W^T, scales Q by gamma and hands the state group the chunk's decay
-// factors; it depends on no state and runs ahead.  The state group keeps only
-// the state dependency chain serial:
+// walks its chunks like the fused kernel, but loads T', T'', P instead of
+// solving for them.  Its key group forms W^T and U~^T, writes -W^T, scales Q
+// by gamma and hands the state group the chunk's decay factors; it depends on
+// no state and runs ahead.  The state group keeps only the state dependency
+// chain serial:
 //
 //   U^T(n) = U~^T(n) + S(n-1) (-W^T(n))      (warp 8 issues)
 //   O^T(n) = S(n-1) (gamma Q(n))^T           (warp 9 issues, alongside)
@@ -1076,16 +1076,18 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
 //   O^T(n) += U^T P(n)^T                     (warp 9, alongside)
 //   S(n)   = gamma_C S(n-1) + dS(n)
 //
-// while warps 12-15 stage each chunk's output in the chunk's spent q/k stage
-// and store it with TMA (a ragged tail is clipped by the tensor map; the same
-// thread then loads the next q/k boxes into that stage), and warp 10 loads the
-// next T', T'', P.  O is computed transposed (value channels on the TMEM
-// lanes, 64 token columns), so two O accumulators fit in TMEM.  The q/k stage
-// holds the K blocks before the Q blocks; at K = 128 the bf16 U^T is written
-// over the chunk's gamma Q blocks once O^T's first product has read them.
-// Every state quantity is the fused kernel's arithmetic on the same operands,
-// so S_T is bit-identical to it (o agrees to the accumulation order of the
-// transposed product).
+// O is computed transposed (value channels on the TMEM lanes, 64 token
+// columns), so two O accumulators fit in TMEM and a chunk's output never holds
+// up the next chunk's products.  The q/k stage holds the K blocks before the Q
+// blocks; at K = 128 the bf16 U^T is written over the chunk's gamma Q blocks
+// once O^T's first product has read them (a 128-row operand).  Warps 12-15
+// stage each chunk's output in its spent q/k stage and warp 11 stores it with
+// TMA (a ragged tail is clipped by the tensor map), then reloads the stage.
+// T', T'' and P have separate two-stage rings: T', T'' of chunk n + 2 load as
+// soon as U(n) has read -W^T (warp 9), P of chunk n + 2 once O^T(n) is
+// complete (warp 10).  Every state quantity is the fused kernel's arithmetic
+// on the same operands, so S_T is bit-identical to it (o agrees to the
+// accumulation order of the transposed product).
 template <int K>
 struct StLayout {
     static constexpr int NSTAGE = 3;
