@@ -274,10 +274,11 @@ GDN_API int gdn_decode_step_gated(const void *q, const void *k, const void *v,
  *   fro2, sigma1, stable_rank [BH] float32 outputs: ||S||_F^2, sigma_1, er
  *
  * sigma_1^2 is the largest eigenvalue of S^T S by power iteration from the
- * fixed start x_j = 1 + j/K, stopping when the Rayleigh quotient changes by
- * at most tol (relative) or after max_iter iterations (max_iter >= 1,
- * tol >= 0).  An all-zero state yields 0 in all three outputs and sets the
- * GDN_WARN_ZERO_STATE device status.
+ * fixed start x_j = 1 + j/K: the Rayleigh quotient is checked every 4
+ * products of S^T S with the iterate, and the iteration stops when it changes
+ * by at most tol (relative) between checks or after max_iter products
+ * (max_iter >= 1, tol >= 0).  An all-zero state yields 0 in all three outputs
+ * and sets the GDN_WARN_ZERO_STATE device status.
  */
 GDN_API int gdn_state_rank(const float *S, int BH, int V, int K, float *fro2, float *sigma1,
                    float *stable_rank, int max_iter, float tol, void *stream);
