@@ -1,6 +1,15 @@
 // Chunkwise prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
 // bf16 q/k/v, float32 state carried on chip from chunk to chunk.
 //
+// Two forms of the same arithmetic live here: the one-pass kernel described
+// in this header (prefill_tc_kernel), and a two-pass form that the launcher
+// takes when the workspace holds every chunk's key-side operands -- a
+// key-side pass over all chunks of all sequences at once
+// (prefill_prep_kernel), then the state recurrence loading those operands
+// (prefill_state_kernel); both are described at their definitions below.
+// The key-side steps are shared device functions, so the two forms give the
+// same final states.
+//
 // One CTA owns one (b, h) sequence and walks its 64-token chunks.  With G_t
 // the in-chunk cumulative log-decay, gamma_t = exp(G_t) and
 // Gamma_ts = exp(G_t - G_s) (a difference, never a ratio of gammas):

@@ -124,3 +124,28 @@ def test_two_pass_outputs_or_state_alone(want_o, want_S):
         assert rel_err(to_np(o), o_ref) <= TOL["bf16"]
     if want_S:
         assert rel_err(to_np(ST), S_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("B,T,H", [(2, 300, 3), (1, 4133, 2)])
+def test_two_pass_in_place_continuation(B, T, H):
+    # S_T may alias S0: each CTA reads its start state before writing the end
+    # state (whole sequences), or the start states are read by the first
+    # segment pass and the end state written by the last (segment-parallel)
+    import torch
+    K, V = 128, 128
+    p = inputs.make_prefill(B=B, T=T, H=H, K=K, seed=11, with_S0=True)
+    d = problem_to_dev(p)
+    need = binding.gdn_prefill_workspace_size(B, T, H, K, V, binding.GDN_BF16)
+    two = binding.gdn_prefill_two_pass_workspace_size(B, T, H, K, V, binding.GDN_BF16)
+    res = []
+    for wsb in (need, two):
+        S = d["S0"].clone()
+        o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+        binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S, o, S, B, T, H, K,
+                            V, binding.GDN_BF16, ws if wsb else None, wsb)
+        assert binding.gdn_get_last_device_status() == binding.GDN_OK
+        res.append(S.cpu().numpy())
+    assert np.array_equal(res[0].view(np.int32), res[1].view(np.int32))
+    _, S_ref = oracle.recurrence(p.q, p.k, p.v, p.alpha, p.beta, S0=p.S0)
+    assert rel_err(res[1], S_ref) <= TOL["bf16"]
