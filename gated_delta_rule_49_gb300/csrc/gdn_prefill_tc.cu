@@ -151,8 +151,8 @@ __device__ __forceinline__ float *blk(float *AF, int i, int j) {
     return AF + 16 * i * kLD + 16 * j;
 }
 
-// Y = sum_k L_k R_k for 16 x 16 blocks (row stride kLD, or 16 when ld == 16),
-// 4 outputs per thread: row `row`, columns [c0, c0 + 4).
+// Y = sum_k L_k R_k for 16 x 16 blocks (row stride kLD, or ldr for R_0), 4
+// outputs per thread: row `row`, columns [c0, c0 + 4) (two warps per block).
 __device__ __forceinline__ float4 blk_mac(const float *L0, const float *R0, int ldr,
                                           const float *L1, const float *R1,
                                           const float *L2, const float *R2, int nterm, int row,
@@ -177,11 +177,54 @@ __device__ __forceinline__ float4 blk_mac(const float *L0, const float *R0, int 
     return y;
 }
 
+// The same products for two rows (r0, r0 + 8) and four columns [c0, c0 + 4)
+// per thread: one warp per block.  Operands are read as float4 (four L columns of a row, four R rows at
+// a time); each output accumulates term by term, m ascending.
+__device__ __forceinline__ void blk_mac2(const float *L0, const float *R0, int ldr,
+                                         const float *L1, const float *R1, const float *L2,
+                                         const float *R2, int nterm, int r0, int c0, float4 &y0,
+                                         float4 &y1) {
+    y0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    y1 = y0;
+    const float *Ls[3] = {L0, L1, L2};
+    const float *Rs[3] = {R0, R1, R2};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        if (k >= nterm) break;
+        const int ldrk = (k == 0) ? ldr : kLD;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(Ls[k] + r0 * kLD + m);
+            const float4 a1 = *reinterpret_cast<const float4 *>(Ls[k] + (r0 + 8) * kLD + m);
+            const float la0[4] = {a0.x, a0.y, a0.z, a0.w}, la1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 r = *reinterpret_cast<const float4 *>(Rs[k] + (m + e) * ldrk + c0);
+                y0.x = fmaf(la0[e], r.x, y0.x);
+                y0.y = fmaf(la0[e], r.y, y0.y);
+                y0.z = fmaf(la0[e], r.z, y0.z);
+                y0.w = fmaf(la0[e], r.w, y0.w);
+                y1.x = fmaf(la1[e], r.x, y1.x);
+                y1.y = fmaf(la1[e], r.y, y1.y);
+                y1.z = fmaf(la1[e], r.z, y1.z);
+                y1.w = fmaf(la1[e], r.w, y1.w);
+            }
+        }
+    }
+}
+
 // T = (I + A)^{-1} for the strictly lower 64 x 64 A in AF (zeros on and above
 // the diagonal), by the 256 key-group threads: the four 16 x 16 diagonal
 // blocks by forward substitution (one column per thread), then the
 // off-diagonal blocks level by level, T_ij = -T_ii (sum_{j<=m<i} A_im T_mj),
-// each level a pair of 16 x 16 block products.  XS: scratch for 3 blocks.
+// each level a pair of 16 x 16 block products (one warp per block).  XS:
+// scratch for 3 blocks.
+// kNarrow selects the level mapping: two warps per block with one row of four
+// outputs per thread (shorter latency: the one-pass kernel, whose chunk loop
+// waits for it), or one warp per block with two rows of four (a third of the
+// shared-memory traffic: the key-side pass, bound by it).  Every output sums
+// the same terms in the same order either way, so the results are identical.
+template <bool kNarrow>
 __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid) {
     {
         float x[16];
@@ -212,9 +255,47 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
         }
         named_sync(kBarKey, kKeyThreads);
     }
-    const int job = tid >> 6;          // which block of this level
-    const int e = tid & 63;
-    const int row = e >> 2, c0 = (e & 3) * 4;
+    if constexpr (!kNarrow) {
+        const int job = tid >> 6;  // which block of this level
+        const int e = tid & 63;
+        const int row = e >> 2, c0 = (e & 3) * 4;
+        // level d: blocks (j + d, j), j = 0 .. 3 - d
+#pragma unroll
+        for (int d = 1; d <= 3; ++d) {
+            const int j = job, i = job + d;
+            const bool active = job <= 3 - d;
+            if (active) {
+                // X = sum_{m=j}^{i-1} A_im T_mj  (T_jj on the diagonal, T_mj, m > j, mirrored)
+                float4 y;
+                if (d == 1)
+                    y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, nullptr, nullptr, nullptr,
+                                nullptr, 1, row, c0);
+                else if (d == 2)
+                    y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
+                                blk(AF, j, j + 1), nullptr, nullptr, 2, row, c0);
+                else
+                    y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
+                                blk(AF, j, j + 1), blk(AF, i, j + 2), blk(AF, j, j + 2), 3, row,
+                                c0);
+                *reinterpret_cast<float4 *>(XS + job * 256 + row * 16 + c0) = y;
+            }
+            named_sync(kBarKey, kKeyThreads);
+            if (active) {
+                // T_ij = -T_ii X, stored mirrored at block (j, i)
+                const float4 y = blk_mac(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr,
+                                         nullptr, nullptr, 1, row, c0);
+                *reinterpret_cast<float4 *>(blk(AF, j, i) + row * kLD + c0) =
+                    make_float4(-y.x, -y.y, -y.z, -y.w);
+            }
+            named_sync(kBarKey, kKeyThreads);
+        }
+        return;
+    }
+    // one warp per block of a level; lane: rows r0 and r0 + 8 (eight distinct
+    // rows per load: conflict-free with the row stride of 68 floats), columns
+    // [c0, c0 + 4)
+    const int job = tid >> 5;
+    const int r0 = (tid & 31) >> 2, c0 = (tid & 3) * 4;
     // level d: blocks (j + d, j), j = 0 .. 3 - d
 #pragma unroll
     for (int d = 1; d <= 3; ++d) {
@@ -222,25 +303,29 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
         const bool active = job <= 3 - d;
         if (active) {
             // X = sum_{m=j}^{i-1} A_im T_mj   (T_jj on the diagonal, T_mj, m > j, mirrored)
-            float4 y;
+            float4 y0, y1;
             if (d == 1)
-                y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, nullptr, nullptr, nullptr, nullptr,
-                            1, row, c0);
+                blk_mac2(blk(AF, i, j), blk(AF, j, j), kLD, nullptr, nullptr, nullptr, nullptr, 1,
+                         r0, c0, y0, y1);
             else if (d == 2)
-                y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
-                            blk(AF, j, j + 1), nullptr, nullptr, 2, row, c0);
+                blk_mac2(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1), blk(AF, j, j + 1),
+                         nullptr, nullptr, 2, r0, c0, y0, y1);
             else
-                y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
-                            blk(AF, j, j + 1), blk(AF, i, j + 2), blk(AF, j, j + 2), 3, row, c0);
-            *reinterpret_cast<float4 *>(XS + job * 256 + row * 16 + c0) = y;
+                blk_mac2(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1), blk(AF, j, j + 1),
+                         blk(AF, i, j + 2), blk(AF, j, j + 2), 3, r0, c0, y0, y1);
+            *reinterpret_cast<float4 *>(XS + job * 256 + r0 * 16 + c0) = y0;
+            *reinterpret_cast<float4 *>(XS + job * 256 + (r0 + 8) * 16 + c0) = y1;
         }
         named_sync(kBarKey, kKeyThreads);
         if (active) {
             // T_ij = -T_ii X, stored mirrored at block (j, i)
-            const float4 y = blk_mac(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr,
-                                     nullptr, nullptr, 1, row, c0);
-            *reinterpret_cast<float4 *>(blk(AF, j, i) + row * kLD + c0) =
-                make_float4(-y.x, -y.y, -y.z, -y.w);
+            float4 y0, y1;
+            blk_mac2(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr, nullptr, nullptr, 1, r0,
+                     c0, y0, y1);
+            *reinterpret_cast<float4 *>(blk(AF, j, i) + r0 * kLD + c0) =
+                make_float4(-y0.x, -y0.y, -y0.z, -y0.w);
+            *reinterpret_cast<float4 *>(blk(AF, j, i) + (r0 + 8) * kLD + c0) =
+                make_float4(-y1.x, -y1.y, -y1.z, -y1.w);
         }
         named_sync(kBarKey, kKeyThreads);
     }
@@ -588,7 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before();
             if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
             // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
-            unit_lower_inverse(AF, XS, tid);
+            unit_lower_inverse<false>(AF, XS, tid);
             chunk_tprime(AF, bet, gam, sm + L::TP, sm + L::TPP, tid);
             fence_proxy_async_smem();
             named_sync(kBarKey, kKeyThreads);
@@ -1047,7 +1132,7 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
         chunk_ap(tb + lane_off + 32 * colhalf, quad_row, colhalf, G2, bet, AF, out + 16384);
         tc_fence_before();
         named_sync(kBarKey, kKeyThreads);
-        unit_lower_inverse(AF, XS, tid);
+        unit_lower_inverse<true>(AF, XS, tid);
         chunk_tprime(AF, bet, gam, out, out + 8192, tid);
         named_sync(kBarKey, kKeyThreads);  // AF and the gates are rewritten next
     }
