@@ -4,11 +4,17 @@
 
 Headline workload: Gated DeltaNet layer prefill, B=8, T=4096, H=16,
 d_k = d_v = 128, bf16 q/k/v, fp32 state, chunk 64, S0 = 0.  A timed step is
-one gdn_prefill call over the whole batch; `value` is tokens/s (B*T per
-step, summed over ranks).  The same JSON line carries the rest of the
-metric, measured in the same run: the channel-pruned d_k' = 64 prefill and
-its speed-up, the decode state GB/s (B = 64 and B = 1, d_k 128 and 64; as
-specified and L2-cold) and the stable-rank epilogue time.
+one gdn_prefill call over the whole batch, given the two-pass workspace (a
+key-side kernel over every chunk, then the state kernel: two launches per
+step); `value` is tokens/s (B*T per step, summed over ranks) and `one_pass`
+times the same call without the workspace (one fused kernel, identical
+results).  The same JSON line carries the rest of the metric, measured in the
+same run: the channel-pruned d_k' = 64 prefill and its speed-up, the decode
+state GB/s (B = 64 and B = 1, d_k 128 and 64; as specified and L2-cold) and
+the stable-rank epilogue time, plus one entry per further path (prologue,
+truncation, DRRQR, long context, KDA/GDN2, fp32).  The roofline counts the
+algorithmic bytes of the call against the time of both kernels; its traffic
+is the two kernels' DRAM bytes from the committed ncu summary.
 
 Inputs live in HBM before the timed region; the prefill working set
 (q, k, v, o: 537 MB) is larger than L2, so no flush is needed between steps.
