@@ -111,6 +111,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&p);
 }
+// 32 floats as 16 bf16 pairs, the even index in the low half (a TMEM row of
+// a bf16 A operand)
+__device__ __forceinline__ void pack_row(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+}
 
 // Store 8*NCH floats (times `scale`) of one tile row as NCH swizzled 16-byte
 // chunks starting at chunk c0.
@@ -1163,58 +1169,66 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
 // no state and runs ahead.  The state group keeps only the state dependency
 // chain serial:
 //
-//   U^T(n) = U~^T(n) + S(n-1) (-W^T(n))      (warp 8 issues)
-//   O^T(n) = S(n-1) (gamma Q(n))^T           (warp 9 issues, alongside)
+//   U^T(n) = U~^T(n) + S(n-1) (-W^T(n))      \  warp 8, issued back to back
+//   O^T(n) = S(n-1) (gamma Q(n))^T           /  at the end of chunk n - 1
 //   epilogue: U^T -> bf16, U^T diag(decay) -> bf16
-//   dS(n)  = U^T diag(decay) K(n)            (warp 8)
-//   O^T(n) += U^T P(n)^T                     (warp 9, alongside)
+//   dS(n)  = U^T diag(decay) K(n)            \  warp 8, issued back to back
+//   O^T(n) += U^T P(n)^T                     /
 //   S(n)   = gamma_C S(n-1) + dS(n)
 //
-// O is computed transposed (value channels on the TMEM lanes, 64 token
-// columns), so two O accumulators fit in TMEM and a chunk's output never holds
-// up the next chunk's products.  The q/k stage holds the K blocks before the Q
-// blocks; at K = 128 the bf16 U^T is written over the chunk's gamma Q blocks
-// once O^T's first product has read them (a 128-row operand).  Warps 12-15
-// stage each chunk's output in its spent q/k stage and warp 11 stores it with
-// TMA (a ragged tail is clipped by the tensor map), then reloads the stage.
-// T', T'' and P have separate two-stage rings: T', T'' of chunk n + 2 load as
-// soon as U(n) has read -W^T (warp 9), P of chunk n + 2 once O^T(n) is
-// complete (warp 10).  Every state quantity is the fused kernel's arithmetic
-// on the same operands, so S_T is bit-identical to it (o agrees to the
-// accumulation order of the transposed product).
+// The chain's A operands live in TMEM: the bf16 copy of the state, and the
+// bf16 U^T and U^T diag(decay) written into the spent halves of the U
+// accumulator, so the chain's products read only their B operands from
+// shared memory and the epilogues write no shared memory.  One thread issues
+// every state-side product in chain order; the tensor pipe runs them in issue
+// order and each commit covers all earlier products of the thread, which is
+// what frees the operands (O^T's first product has read S(n-1) once dS(n) is
+// complete, and the U slot is free once O^T(n) is).  O is computed transposed
+// (value channels on the TMEM lanes, 64 token columns), so two O accumulators
+// fit in TMEM and a chunk's output never holds up the next chunk's products.
+// Warps 12-15 stage each chunk's output in a dedicated tile and warp 11 stores
+// it with TMA (a ragged tail is clipped by the tensor map).  Rings: q/k (three
+// stages, chunk n + 3 loaded once dS(n) is complete), V (three), T', T'' and P
+// (two each: T', T'' of chunk n + 2 as soon as U(n) has read -W^T, P of chunk
+// n + 2 once O^T(n) is complete).  Every state quantity is the fused kernel's
+// arithmetic on the same operands, so S_T is bit-identical to it (o agrees to
+// the accumulation order of the transposed product).
+
 template <int K>
 struct StLayout {
-    static constexpr int NSTAGE = 3;
+    static constexpr int NSTAGE = 3;                             // q/k ring
+    static constexpr int NV = 3;                                 // V ring
     static constexpr uint32_t KC0 = 0, KC1 = 8192;               // K blocks (KC1: K = 128)
     static constexpr uint32_t QC0 = K == 128 ? 16384 : 8192, QC1 = QC0 + 8192;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
-    static constexpr uint32_t VB = NSTAGE * STAGE;               // V: two buffers of 16 KB
-    static constexpr uint32_t PR = VB + 2 * 16384;               // ring of [T' | T'']
+    static constexpr uint32_t VB = NSTAGE * STAGE;               // V ring, 16 KB per chunk
+    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [T' | T'']
     static constexpr uint32_t PP = PR + 2 * 16384;               // ring of P
-    static constexpr uint32_t SB = PP + 2 * 8192;                // bf16 state, K/64 x 16 KB
-    static constexpr uint32_t UTS = SB + (K / 64) * 16384;       // U^T (K = 64 only)
-    static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);  // U^T diag(decay)
-    static constexpr uint32_t KGATE = UD + 16384;                // G2, gamma, beta
+    static constexpr uint32_t OST = PP + 2 * 8192;               // output staging, 2 x 64 x 64
+    static constexpr uint32_t KGATE = OST + 16384;               // G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;        // 3 x (decay[64], gamma_C)
     static constexpr uint32_t END = SGATE + 3 * 68 * 4;
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr uint32_t V_BYTES = 2u * 8192u;
     static constexpr size_t SMEM = END;
     static_assert(SMEM + 1024 <= 232448, "shared memory budget");
-    static __device__ __forceinline__ uint32_t ut(int st) {
-        return K == 128 ? st * STAGE + QC0 : UTS;
-    }
     static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * 16384; }
     static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
     static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // -W^T over T', T''
     static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
-    // output staging of a chunk in stage st (16 KB, spent by then): two 64 x 64 tiles
-    static __device__ __forceinline__ uint32_t ost(int st) {
-        return st * STAGE + (K == 128 ? QC0 : 0u);
-    }
-    // TMEM columns: O^T of even / odd chunks, W^T, U~^T / U^T of even / odd chunks, dS
-    static constexpr uint32_t O0 = 0, WT = 64, UA = 128, O1 = 256, DS = 384;
+    static __device__ __forceinline__ uint32_t vbuf(int n) { return VB + (n % NV) * 16384; }
+    // TMEM columns: O^T of even / odd chunks, W^T, U~^T / U^T of even / odd
+    // chunks, the bf16 state (two K elements per column), dS
+    static constexpr uint32_t O0 = 0, WT = 64, UA = 128, O1 = 256, SBT = 320, DS = 384;
     static __device__ __forceinline__ uint32_t ocol(int n) { return (n & 1) ? O1 : O0; }
+    static __device__ __forceinline__ uint32_t ua(int n) { return UA + 64 * (n & 1); }
+    // After chunk n's epilogue, token half h of its U slot (32 columns) holds
+    // bf16 U^T in its first 16 columns and bf16 U^T diag(decay) in the next
+    // 16: the TMEM A operand of K step ks (16 tokens) of O^T += U^T P^T / dS.
+    static __device__ __forceinline__ uint32_t ut_col(int n, int ks) {
+        return ua(n) + 32 * (ks >> 1) + 8 * (ks & 1);
+    }
+    static __device__ __forceinline__ uint32_t ud_col(int n, int ks) { return ut_col(n, ks) + 16; }
 };
 
 constexpr int kBarOut = 3, kBarOut2 = 4;  // the output warps (11-15)
@@ -1236,8 +1250,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full[3], v_full[2], tt_full[2], p_full[2], bar_w, bar_u, bar_o1, bar_s,
-        bar_o2, nw_ready[2], ua_free[2];
+    __shared__ uint64_t kq_full[3], v_full[3], tt_full[2], p_full[2], bar_w, bar_u, bar_s, bar_o2,
+        nw_ready[2], ua_free[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -1264,9 +1278,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         if (outs) tma_prefetch_desc(&tm_o);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0],  &v_full[1],
-                            &tt_full[0], &tt_full[1], &p_full[0],  &p_full[1],  &bar_w,
-                            &bar_u,      &bar_o1,     &bar_s,      &bar_o2,     &nw_ready[0],
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1],  &kq_full[2], &v_full[0],  &v_full[1],
+                            &v_full[2],  &tt_full[0],  &tt_full[1], &p_full[0],  &p_full[1],
+                            &bar_w,      &bar_u,       &bar_s,      &bar_o2,     &nw_ready[0],
                             &nw_ready[1], &ua_free[0], &ua_free[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
@@ -1294,8 +1308,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     };
     auto load_v = [&](int n) {
-        uint64_t *bar = &v_full[n & 1];
-        uint8_t *dst = sm + L::VB + (n & 1) * 16384;
+        uint64_t *bar = &v_full[n % L::NV];
+        uint8_t *dst = sm + L::vbuf(n);
         mbar_arrive_expect_tx(bar, L::V_BYTES);
         tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
         tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
@@ -1346,7 +1360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tid == 0) {
             for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
             if (!zero_v)
-                for (int m = 0; m < 2 && m < nchunks; ++m) load_v(m);
+                for (int m = 0; m < L::NV && m < nchunks; ++m) load_v(m);
             for (int m = 0; m < 2 && m < nchunks; ++m) {
                 load_tt(m);
                 if (outs) load_p(m);
@@ -1354,19 +1368,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int n = 0; n < nchunks; ++n) {
             const int st = n % L::NSTAGE;  // q/k stage
-            const int p2 = n & 1;          // V buffer, operand ring stage, U~ accumulator
+            const int p2 = n & 1;          // operand ring stage, U~ accumulator
             const uint32_t stg = base + st * L::STAGE;
             const int nvalid = min(64, t1 - t0 - n * 64);
             bool ok = true;
             if (tid == 0) {
-                // warm L2 for loads two and three chunks ahead (they are
-                // copied in only when a ring slot frees)
+                // warm L2 for the key-side block of chunk n + 2 and the V boxes
+                // of chunk n + 4 (copied in only when a ring slot frees)
                 if (n + 2 < nchunks)
                     bulk_prefetch_l2(prep_seq + (size_t)(n + 2) * kPrepChunkBytes,
                                      kPrepChunkBytes);
-                if (!zero_v && n + 3 < nchunks) {
-                    tma_prefetch_l2_4d(&tm_v, 0, h, t0 + (n + 3) * 64, b);
-                    tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + 3) * 64, b);
+                if (!zero_v && n + L::NV + 1 < nchunks) {
+                    tma_prefetch_l2_4d(&tm_v, 0, h, t0 + (n + L::NV + 1) * 64, b);
+                    tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + L::NV + 1) * 64, b);
                 }
                 ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
                 if (ok) ok = wait(&tt_full[p2], (n >> 1) & 1);
@@ -1375,8 +1389,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
                 __syncwarp();
                 // the state group's decay to the chunk end and gamma_C; slot
-                // n % 3 was last read by the state group's chunk n - 3, which
-                // finished before this chunk's q/k boxes could load
+                // n % 3 was last read in the state group's epilogue of chunk
+                // n - 3, before the barrier after which this chunk's q/k boxes
+                // are loaded
                 float *slot = sg + (n % 3) * 68;
                 const float gC = G2[63];
                 slot[lane] = exp2f(gC - G2[lane]);
@@ -1388,7 +1403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
             if (tid == 0) {
                 if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
-                if (!zero_v) ok = ok && wait(&v_full[p2], (n >> 1) & 1);
+                if (!zero_v) ok = ok && wait(&v_full[n % L::NV], (n / L::NV) & 1);
                 if (ok) {
                     tc_fence_after();
 #pragma unroll
@@ -1397,7 +1412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                  sdesc(base + L::tp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
                         if (!zero_v)
                             mma_bf16(tb + L::UA + 64 * p2,
-                                     sdesc(base + L::VB + p2 * 16384 + ks * 2048, 8192, 1024),
+                                     sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
                                      sdesc(base + L::tpp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
                     }
                     mma_commit(&bar_w);
@@ -1441,8 +1456,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // operands that are loaded only after the state group passed chunk n
             if (tid == 0) {
                 mbar_arrive(&nw_ready[p2]);
-                // U~^T has read this V buffer (bar_w above)
-                if (!zero_v && n + 2 < nchunks) load_v(n + 2);
+                // U~^T has read this V slot (bar_w above)
+                if (!zero_v && n + L::NV < nchunks) load_v(n + L::NV);
             }
             prefetch_gates(n + 1);
         }
@@ -1453,7 +1468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int sw = sid >> 5;            // state warp 0..7
         const int c = quad_row;             // state row = TMEM lane = value channel
         const int hf = sw >> 2;             // column half
-        // initial state: fp32 registers + bf16 operand copy
+        // initial state: fp32 registers + bf16 operand copy in TMEM
         float S[KH];
         {
             const int j0 = hf * KH;
@@ -1474,59 +1489,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
-                const int j = j0 + 32 * p;
-                store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+                uint32_t w[16];
+                pack_row(v, w);
+                tmem_st16(tb + lane_off + L::SBT + (j0 + 32 * p) / 2, w);
             }
+            tmem_st_wait();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         named_sync(kBarState, kStateThreads);
 
-        // U^T += S (-W^T) of chunk m (warp 8, once the key group handed over -W^T)
+        // U^T += S (-W^T) of chunk m, then O^T = S (gamma Q)^T (warp 8, once
+        // the key group handed over -W^T and gamma Q)
         auto issue_u = [&](int m) -> bool {
             if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+            for (int ks = 0; ks < K / 16; ++ks)
                 // with v = 0 there is no U~ product: this one starts the accumulator
-                mma_bf16(tb + L::UA + 64 * (m & 1),
-                         sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
-                         zero_v ? (uint32_t)(ks > 0) : 1u);
-            }
+                mma_bf16_ta(tb + L::ua(m), tb + L::SBT + 8 * ks,
+                            sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
+                            zero_v ? (uint32_t)(ks > 0) : 1u);
             mma_commit(&bar_u);
-            return true;
-        };
-        // O^T = S (gamma Q)^T of chunk m (warp 9, also after gamma Q is ready)
-        auto issue_o1 = [&](int m) -> bool {
-            if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
-            tc_fence_after();
-            const uint32_t stg = base + (m % L::NSTAGE) * L::STAGE;
+            if (outs) {
+                const uint32_t stg = base + (m % L::NSTAGE) * L::STAGE;
 #pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                mma_bf16(tb + L::ocol(m), sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM, ks > 0);
+                for (int ks = 0; ks < K / 16; ++ks) {
+                    const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                    mma_bf16_ta(tb + L::ocol(m), tb + L::SBT + 8 * ks,
+                                sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM, ks > 0);
+                }
             }
-            mma_commit(&bar_o1);
             return true;
         };
-        // chunk m's O^T -> staging tile in its spent q/k stage, by warps 12-15
-        // (TMEM lane quarter w % 4, all 64 columns), then a TMA store by warp
-        // 11 (which reloads the stage with the q/k boxes of chunk m + 3 once
-        // the store has read it, at the top of the next chunk: reload_stage).
-        // Called by warps 11-15; one thread waits for the products (the last
-        // readers of the stage) and all 160 take the same branch on a timeout
-        // (false).
+        // chunk m's O^T -> the staging tile, by warps 12-15 (TMEM lane quarter
+        // w % 4, all 64 columns), then a TMA store by warp 11.  Called by warps
+        // 11-15; one thread waits for the products, warp 11 for the previous
+        // store to have read the tile, and all 160 take the same branch on a
+        // timeout (false).
         auto store_out = [&](int m) -> bool {
             bool okw = true;
             if (sid == 128) okw = wait(&bar_o2, m & 1);
+            if (sw == 3 && lane == 0) bulk_wait_read_all();
             if (named_sync_or(kBarOut, 160, !okw)) return false;
             if (sw >= 4) {
                 tc_fence_after();
                 const bool odd = lane & 1;
-                uint8_t *tile = sm + L::ost(m % L::NSTAGE) + (c >> 6) * 8192;
+                uint8_t *tile = sm + L::OST + (c >> 6) * 8192;
                 const uint32_t cb = (uint32_t)(c & 63) >> 3, cw = (uint32_t)(c & 6) * 2;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -1548,23 +1556,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             named_sync(kBarOut2, 160);  // the tile is written
             if (sw == 3 && lane == 0) {
-                uint8_t *ost = sm + L::ost(m % L::NSTAGE);
-                tma_store_4d(&tm_o, ost, 0, h, t0 + m * 64, b);
-                tma_store_4d(&tm_o, ost + 8192, 64, h, t0 + m * 64, b);
+                tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
+                tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
                 bulk_commit_group();
             }
             return true;
         };
-        // warp 11, lane 0: the store of chunk m has read stage m % 3 -> q/k of m + 3
-        auto reload_stage = [&](int m) {
-            if (m >= 0 && m + L::NSTAGE < nchunks) {
-                bulk_wait_read_all();
-                load_kq(m + L::NSTAGE);
-            }
-        };
-        if (sw <= 1) {
+        if (sw == 0) {
             bool ok0 = true;
-            if (lane == 0) ok0 = sw == 0 ? issue_u(0) : (outs ? issue_o1(0) : true);
+            if (lane == 0) ok0 = issue_u(0);
             ok0 = __shfl_sync(0xffffffffu, ok0, 0);
             failed = !ok0;
         }
@@ -1573,56 +1573,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int st = n % L::NSTAGE;
             const int p2 = n & 1;
             const uint32_t stg = base + st * L::STAGE;
-            // ---- U epilogue: U^T -> bf16 (over gamma Q once O^T has read it) and
-            // ---- U^T diag(decay) -> UD ----
+            // ---- U epilogue: bf16 U^T and U^T diag(decay) into the U slot ----
             const float *slot = sg + (n % 3) * 68;
+            float gC;  // read with the decays: the slot is rewritten for chunk n + 3
             bool ok = !failed;
             if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
-            if (sid == 0 && ok && outs) ok = wait(&bar_o1, n & 1);
             if (sid == 32 && ok && n + 2 < nchunks) {
                 // U^T has read -W^T: ring stage n % 2 takes chunk n + 2's T', T''
                 ok = wait(&bar_u, n & 1);
                 if (ok) load_tt(n + 2);
             }
-            if (sid == 96 && outs) reload_stage(n - 1);
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             {
                 tc_fence_after();
+                // each thread rewrites only the 32 columns it has read
+                gC = slot[64];
                 float v[32];
-                tmem_ld32(tb + lane_off + L::UA + 64 * p2 + 32 * hf, v);
+                tmem_ld32(tb + lane_off + L::ua(n) + 32 * hf, v);
                 tmem_ld_wait();
-                store_row<4>(sm + L::ut(st) + (c >> 6) * 8192, c & 63, 4 * hf, v);
+                uint32_t w[16];
+                if (outs) {
+                    pack_row(v, w);
+                    tmem_st16(tb + lane_off + L::ua(n) + 32 * hf, w);
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= slot[32 * hf + i];
-                store_row<4>(sm + L::UD, c, 4 * hf, v);
+                pack_row(v, w);
+                tmem_st16(tb + lane_off + L::ua(n) + 32 * hf + 16, w);
+                tmem_st_wait();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             named_sync(kBarState, kStateThreads);
-            // ---- dS = U^T diag(decay) K (warp 8) and O^T += U^T P^T (warp 9) ----
+            // ---- dS = U^T diag(decay) K, then O^T += U^T P^T (warp 8) ----
             if (sid == 0) {
-                mbar_arrive(&ua_free[p2]);
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
-                             sdesc(stg + L::KC0 + ks * 2048, 8192, 1024), I_DS, ks > 0);
+                    mma_bf16_ta(tb + L::DS, tb + L::ud_col(n, ks),
+                                sdesc(stg + L::KC0 + ks * 2048, 8192, 1024), I_DS, ks > 0);
                 mma_commit(&bar_s);
-                ok = wait(&bar_s, n & 1);
-            } else if (sid == 32 && outs) {
-                ok = wait(&p_full[p2], (n >> 1) & 1);
-                tc_fence_after();
+                if (outs) {
+                    ok = wait(&p_full[p2], (n >> 1) & 1);
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + L::ocol(n), sdesc(base + L::ut(st) + ks * 32, 16, 1024),
-                             sdesc(base + L::ptile(n) + ks * 32, 16, 1024), I_MM, 1);
-                mma_commit(&bar_o2);
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ta(tb + L::ocol(n), tb + L::ut_col(n, ks),
+                                        sdesc(base + L::ptile(n) + ks * 32, 16, 1024), I_MM, 1);
+                        mma_commit(&bar_o2);
+                    }
+                }
+                ok = ok && wait(&bar_s, n & 1);
+                if (ok) {
+                    // dS(n) and, before it, O^T's first product have read q/k
+                    // stage n % 3 (the key group is done with it): chunk n + 3
+                    if (n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);
+                    if (!outs) mbar_arrive(&ua_free[p2]);  // dS has read the U slot
+                }
             }
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
             {
                 tc_fence_after();
-                const float gC = slot[64];
                 const int j0 = hf * KH;
 #pragma unroll
                 for (int p = 0; p < KH / 32; ++p) {
@@ -1634,31 +1646,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         S[32 * p + i] = fmaf(gC, S[32 * p + i], v[i]);
                         v[i] = S[32 * p + i];
                     }
-                    const int j = j0 + 32 * p;
-                    store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
+                    uint32_t w[16];
+                    pack_row(v, w);
+                    tmem_st16(tb + lane_off + L::SBT + (j0 + 32 * p) / 2, w);
                 }
+                tmem_st_wait();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             named_sync(kBarState, kStateThreads);
-            // ---- next chunk's products (warps 8, 9), loads (warp 10), this
-            // ---- chunk's output (warps 12-15) ----
+            // ---- next chunk's products (warp 8), loads (warp 10), this
+            // ---- chunk's output (warps 11-15) ----
             bool ok1 = true;
             if (sw == 0) {
                 if (lane == 0 && n + 1 < nchunks) ok1 = issue_u(n + 1);
-            } else if (sw == 1) {
-                if (lane == 0 && outs && n + 1 < nchunks) ok1 = issue_o1(n + 1);
             } else if (sw == 2) {
-                // P ring stage n % 2 is free once O^T += U^T P^T has completed;
-                // without outputs q/k stage n % 3 is free as well (with outputs
-                // it stages them and is reloaded after the store)
-                if (lane == 0) {
-                    if (outs) {
-                        ok1 = wait(&bar_o2, n & 1);
-                        if (ok1 && n + 2 < nchunks) load_p(n + 2);
-                    } else if (n + L::NSTAGE < nchunks) {
-                        load_kq(n + L::NSTAGE);
-                    }
+                // O^T += U^T P^T has completed (after dS, issued before it):
+                // the U slot and P ring stage n % 2 are free
+                if (lane == 0 && outs) {
+                    ok1 = wait(&bar_o2, n & 1);
+                    if (ok1) mbar_arrive(&ua_free[p2]);
+                    if (ok1 && n + 2 < nchunks) load_p(n + 2);
                 }
             } else if (sw >= 3 && outs) {
                 ok1 = store_out(n);
@@ -1687,9 +1694,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
             }
-            for (int s = 0; s < 2; ++s) {
+            for (int s = 0; s < L::NV; ++s) {
                 mbar_wait(&v_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&v_full[s], 1, kSpinLimit / 16);
+            }
+            for (int s = 0; s < 2; ++s) {
                 mbar_wait(&tt_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&tt_full[s], 1, kSpinLimit / 16);
                 mbar_wait(&p_full[s], 0, kSpinLimit / 16);

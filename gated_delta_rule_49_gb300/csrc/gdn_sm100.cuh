@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for the sm_100-family features used by the tensor-core
 // prefill: mbarriers, TMA tile loads, TMEM allocation, tcgen05.mma with
-// shared-memory operand descriptors, tcgen05.commit and tcgen05.ld.
+// shared-memory (or, for A, TMEM) operands, tcgen05.commit, tcgen05.ld/st.
 //
 // Shared-memory operand tiles all use the 128-byte swizzle: a tile is a stack
 // of 128-byte rows grouped in 1024-byte atoms of 8 rows; inside an atom the
@@ -203,6 +203,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 lanes x 16 consecutive 32-bit columns from registers: thread i of the
+// warp writes lane (quadrant base + i), columns [col, col + 16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+// The warp's TMEM stores are complete (before a fence and a barrier hand the
+// columns to an MMA).
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- MMA
 // Shared-memory matrix descriptor (sm_100 format): start address, leading and
@@ -233,6 +249,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]: A is M = 128 lanes x 16 bf16 K elements in
+// 8 consecutive columns, two per 32-bit column with the lower K index in the
+// low half (the K-major form; idesc's A-transpose bit must be clear).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive once on `bar` when all previously issued MMAs of this thread finish.
