@@ -220,7 +220,8 @@ __device__ __forceinline__ void blk_mac2(const float *L0, const float *R0, int l
 }
 
 // T = (I + A)^{-1} for the strictly lower 64 x 64 A in AF (zeros on and above
-// the diagonal), by the 256 key-group threads: the four 16 x 16 diagonal
+// the diagonal), by NT threads (the fused kernel's 256 key-group threads, or
+// the key-side pass's 128, which take the narrow mapping): the four 16 x 16 diagonal
 // blocks by forward substitution (one column per thread), then the
 // off-diagonal blocks level by level, T_ij = -T_ii (sum_{j<=m<i} A_im T_mj),
 // each level a pair of 16 x 16 block products (one warp per block).  XS:
@@ -230,8 +231,9 @@ __device__ __forceinline__ void blk_mac2(const float *L0, const float *R0, int l
 // waits for it), or one warp per block with two rows of four (a third of the
 // shared-memory traffic: the key-side pass, bound by it).  Every output sums
 // the same terms in the same order either way, so the results are identical.
-template <bool kNarrow>
+template <bool kNarrow, int NT = kKeyThreads>
 __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid) {
+    static_assert(kNarrow ? (NT >= 128 && NT % 32 == 0) : NT == 256, "inverse thread mapping");
     {
         float x[16];
         const int bb = tid >> 4, s = tid & 15;
@@ -253,13 +255,13 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
                 x[t] -= a0 + a1;
             }
         }
-        named_sync(kBarKey, kKeyThreads);  // every read of the diagonal A blocks done
+        named_sync(kBarKey, NT);  // every read of the diagonal A blocks done
         if (tid < 64) {
             float *Tb = blk(AF, bb, bb);
 #pragma unroll
             for (int t = 0; t < 16; ++t) Tb[t * kLD + s] = x[t];
         }
-        named_sync(kBarKey, kKeyThreads);
+        named_sync(kBarKey, NT);
     }
     if constexpr (!kNarrow) {
         const int job = tid >> 6;  // which block of this level
@@ -285,7 +287,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
                                 c0);
                 *reinterpret_cast<float4 *>(XS + job * 256 + row * 16 + c0) = y;
             }
-            named_sync(kBarKey, kKeyThreads);
+            named_sync(kBarKey, NT);
             if (active) {
                 // T_ij = -T_ii X, stored mirrored at block (j, i)
                 const float4 y = blk_mac(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr,
@@ -293,7 +295,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
                 *reinterpret_cast<float4 *>(blk(AF, j, i) + row * kLD + c0) =
                     make_float4(-y.x, -y.y, -y.z, -y.w);
             }
-            named_sync(kBarKey, kKeyThreads);
+            named_sync(kBarKey, NT);
         }
         return;
     }
@@ -322,7 +324,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
             *reinterpret_cast<float4 *>(XS + job * 256 + r0 * 16 + c0) = y0;
             *reinterpret_cast<float4 *>(XS + job * 256 + (r0 + 8) * 16 + c0) = y1;
         }
-        named_sync(kBarKey, kKeyThreads);
+        named_sync(kBarKey, NT);
         if (active) {
             // T_ij = -T_ii X, stored mirrored at block (j, i)
             float4 y0, y1;
@@ -333,7 +335,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
             *reinterpret_cast<float4 *>(blk(AF, j, i) + (r0 + 8) * kLD + c0) =
                 make_float4(-y1.x, -y1.y, -y1.z, -y1.w);
         }
-        named_sync(kBarKey, kKeyThreads);
+        named_sync(kBarKey, NT);
     }
 }
 
@@ -420,8 +422,8 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
 }
 
 // T' = T diag(beta gamma) and T'' = T diag(beta) as bf16 operand tiles from
-// the inverse in AF (T_ii in place, T_ij mirrored at block (j, i)); thread tid
-// of 256 writes row tid % 64, columns [16 (tid / 64), +16), so a warp reads
+// the inverse in AF (T_ii in place, T_ij mirrored at block (j, i)); index tid
+// in [0, 256) writes row tid % 64, columns [16 (tid / 64), +16), so a warp reads
 // 32 consecutive rows of AF (conflict-free with the row stride of 68 floats)
 // and one broadcast slice of beta and gamma.  The tiles may be shared or
 // global memory.
@@ -997,7 +999,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // on its keys, queries and gates -- A, P, the inverse T and T', T'' -- has no
 // dependence on the state, so it runs for all B * H * ceil(T/64) chunks at
 // once instead of in each sequence's serial chunk loop.  Persistent CTAs of
-// 256 threads (three per SM) stride over the chunks; each chunk's [K;Q] K^T
+// 128 threads (four per SM: the inverse keeps only some warps of a CTA busy
+// between its barriers, so more, smaller CTAs fill the SM better) stride over
+// the chunks; each chunk's [K;Q] K^T
 // is one tcgen05 product into 64 TMEM columns, the next chunk's q/k boxes load
 // (TMA) while the current one is solved, and T', T'', P go to global memory as
 // their swizzled shared-memory images, which the state-side kernel copies in
@@ -1014,12 +1018,13 @@ struct PrepLayout {
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr size_t SMEM = END;
 };
-constexpr int kPrepCtasPerSm = 3;
-// three CTAs of dynamic + 1 KB static + 1 KB reserved shared memory per SM
+constexpr int kPrepThreads = 128;
+constexpr int kPrepCtasPerSm = 4;
+// four CTAs of dynamic + 1 KB static + 1 KB reserved shared memory per SM
 static_assert(kPrepCtasPerSm * (PrepLayout<128>::SMEM + 2048) <= 233472, "prep residency");
 
 template <int K>
-__global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     prefill_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ alpha,
                         const float *__restrict__ beta, uint8_t *__restrict__ prep, int T, int Ts,
@@ -1059,7 +1064,6 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
     const uint32_t tb = tmem_base_sh;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int quad_row = (warp & 3) * 32 + lane;
-    const int colhalf = (warp >> 2) & 1;
     float *AF = reinterpret_cast<float *>(sm + L::AF);
     float *XS = reinterpret_cast<float *>(sm + L::XS);
     float *G2 = reinterpret_cast<float *>(sm + L::GATE);
@@ -1132,15 +1136,17 @@ __global__ void __launch_bounds__(kKeyThreads, kPrepCtasPerSm)
             chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
             prefetch_gates(j + G);
         }
-        if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
+        if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
         uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T' | T'' | P]
         tc_fence_after();
-        chunk_ap(tb + lane_off + 32 * colhalf, quad_row, colhalf, G2, bet, AF, out + 16384);
+        for (int ch = 0; ch < 2; ++ch)  // both 32-column halves per thread
+            chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, out + 16384);
         tc_fence_before();
-        named_sync(kBarKey, kKeyThreads);
-        unit_lower_inverse<true>(AF, XS, tid);
-        chunk_tprime(AF, bet, gam, out, out + 8192, tid);
-        named_sync(kBarKey, kKeyThreads);  // AF and the gates are rewritten next
+        named_sync(kBarKey, kPrepThreads);
+        unit_lower_inverse<true, kPrepThreads>(AF, XS, tid);
+        chunk_tprime(AF, bet, gam, out, out + 8192, tid);  // column blocks 0, 1
+        chunk_tprime(AF, bet, gam, out, out + 8192, tid + kPrepThreads);  // 2, 3
+        named_sync(kBarKey, kPrepThreads);  // AF and the gates are rewritten next
     }
 
     if (failed) *abort_v = 1;
@@ -1811,7 +1817,7 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
     // persistent CTAs, kPrepCtasPerSm per SM (the loop is correct for any residency)
     const long long total = BH * ((T + 63) / 64);
     const long long grid = std::min<long long>(total, (long long)kPrepCtasPerSm * sm_count());
-    kern<<<(unsigned)grid, kKeyThreads, PrepLayout<K>::SMEM, stream>>>(
+    kern<<<(unsigned)grid, kPrepThreads, PrepLayout<K>::SMEM, stream>>>(
         mq, mk, alpha, beta, prep, T, Ts, H, total, device_status_ptr());
     return cudaGetLastError();
 }
