@@ -52,3 +52,147 @@ def chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64):
                 o[b, c0:c0 + n, h] = O[:n]
             ST[b, h] = S
     return o, ST
+
+
+def bf16_round(x):
+    """Round float64 values to the nearest bfloat16 (ties to even), returned
+    as float64: the rounding the kernels apply to their MMA operands."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _chunk_operands(k, q, v, alpha, beta, b, h, c0, C):
+    """Zero-padded chunk tiles and its scalar-gate quantities."""
+    T = k.shape[1]
+    n = min(C, T - c0)
+    K, V = k.shape[-1], v.shape[-1]
+    Kc = np.zeros((C, K)); Qc = np.zeros((C, K)); Vc = np.zeros((C, V))
+    g = np.zeros(C); be = np.zeros(C)
+    Kc[:n] = k[b, c0:c0 + n, h]; Qc[:n] = q[b, c0:c0 + n, h]; Vc[:n] = v[b, c0:c0 + n, h]
+    g[:n] = np.log(alpha[b, c0:c0 + n, h]); be[:n] = beta[b, c0:c0 + n, h]
+    G = np.cumsum(g)
+    gam = np.exp(G)
+    Gam = np.exp(G[:, None] - G[None, :])
+    A = be[:, None] * Gam * (Kc @ Kc.T) * np.tril(np.ones((C, C)), -1)
+    Tm = np.linalg.inv(np.eye(C) + A)
+    return dict(n=n, K=Kc, Q=Qc, V=Vc, beta=be, gam=gam, gC=gam[-1],
+                dec=np.exp(G[-1] - G), P=np.tril(Gam * (Qc @ Kc.T)),
+                Tp=Tm * (be * gam)[None, :], Tpp=Tm * be[None, :])
+
+
+def chunk_state_chain(q, k, v, alpha, beta, S0=None, C=64, lookahead=False, rnd=None):
+    """The state pass of the two-pass prefill, one sequence per (b, h), on the
+    key-side operands T' = T diag(beta gamma), T'' = T diag(beta) and P.
+
+    lookahead=False is the chain the kernel runs today (all quantities
+    transposed as in the kernel: value channels on the rows):
+
+      U^T(n) = U~^T(n) + S(n-1) NW(n),   NW = -W^T = -K^T T'^T,  U~^T = V^T T''^T
+      O^T(n) = S(n-1) (gamma Q)^T + U^T(n) P^T
+      S(n)   = gamma_n S(n-1) + U^T(n) diag(dec) K(n)
+
+    lookahead=True forms U(n+1) without waiting for S(n): since
+    S(n) NW(n+1) = S(n-1) [gamma_n NW(n+1)] + U^T(n) M(n) with
+    M(n) = diag(dec_n) K(n) NW(n+1),
+
+      U^T(n+1) = U~^T(n+1) + S(n-1) [gamma_n NW(n+1)] + U^T(n) M(n),
+
+    the same U exactly (S(n) is still formed for O and the final state).
+    rnd (e.g. bf16_round) is applied where the kernel rounds an MMA operand:
+    T', T'', P, NW (and gamma_n NW, M), the state copy, U^T, U^T diag(dec)
+    and gamma Q; products then accumulate in float32 and the state stays
+    float32, as on the GPU.  Returns (o, S_T) like chunk_recurrence.
+    """
+    r = rnd if rnd is not None else (lambda x: x)
+    acc = np.float32 if rnd is not None else np.float64
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    ST = np.zeros((B, H, V, K))
+    mm = lambda a, b_: (np.asarray(a, acc) @ np.asarray(b_, acc)).astype(np.float64)
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((V, K)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
+            S = S.astype(acc).astype(np.float64)
+            ops = [_chunk_operands(k, q, v, alpha, beta, b, h, c0, C) for c0 in range(0, T, C)]
+            nw = [r(-mm(c["K"].T, r(c["Tp"]).T)) for c in ops]     # -W^T(n), K x C
+            ut = [mm(c["V"].T, r(c["Tpp"]).T) for c in ops]          # U~^T(n), V x C
+            U_next = None
+            for n, c in enumerate(ops):
+                if not lookahead or n == 0:
+                    Un = ut[n] + mm(r(S), nw[n])
+                else:
+                    Un = U_next
+                Ub = r(Un)
+                Ud = r(Un * c["dec"][None, :])
+                if lookahead and n + 1 < len(ops):
+                    M = r(c["dec"][:, None] * mm(c["K"], nw[n + 1]))  # rows scaled after
+                    U_next = ut[n + 1] + mm(r(S), r(c["gC"] * nw[n + 1])) + mm(Ub, M)
+                Ot = mm(r(S), r(c["gam"][:, None] * c["Q"]).T) + mm(Ub, r(c["P"]).T)
+                S = (acc(c["gC"]) * S.astype(acc) + mm(Ud, c["K"]).astype(acc)).astype(np.float64)
+                o[b, n * C:n * C + c["n"], h] = Ot.T[:c["n"]]
+            ST[b, h] = S
+    return o, ST
+
+
+def kda_chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64, sub=16):
+    """Chunkwise form of KDA (per-key-channel decay alpha_t in R^K on the right
+    of the state, scalar beta), with the per-channel exponents inside the
+    intra-chunk products referred to the midpoint of each `sub`-token row
+    block.  With G_t in R^K the in-chunk cumulative log-decay:
+
+      A'_ts = beta_t sum_j k_tj k_sj e^(G_tj - G_sj)   (s < t)
+      P'_ts = sum_j q_tj k_sj e^(G_tj - G_sj)         (s <= t)
+      T = (I + A')^{-1},  W = T diag(beta) (K (.) e^G),  U~ = T diag(beta) V
+      U = U~ - W S^T,     O = (Q (.) e^G) S^T + P' U
+      S <- S diag(e^(G_C)) + U^T (K (.) e^(G_C - G))
+
+    For row block I with reference token m (its midpoint), e^(G_t - G_s) =
+    e^(G_t - G_m) e^(G_m - G_s): rows of block I use the left factor, columns
+    s <= the block's last token the right one, so each block row of A' and P'
+    is one product of two scaled operands, and every factor is at most
+    e^(sub/2 max |log alpha|) (at most 1 for s before the block).  Returns
+    (o, S_T, max_factor), max_factor the largest exponential formed.
+    """
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    ST = np.zeros((B, H, V, K))
+    fmax = 0.0
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((V, K)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
+            for c0 in range(0, T, C):
+                n = min(C, T - c0)
+                Kc = np.zeros((C, K)); Qc = np.zeros((C, K)); Vc = np.zeros((C, V))
+                lg = np.zeros((C, K)); be = np.zeros(C)
+                Kc[:n] = k[b, c0:c0 + n, h]; Qc[:n] = q[b, c0:c0 + n, h]
+                Vc[:n] = v[b, c0:c0 + n, h]
+                lg[:n] = np.log(alpha[b, c0:c0 + n, h]); be[:n] = beta[b, c0:c0 + n, h]
+                G = np.cumsum(lg, axis=0)                      # C x K
+                A = np.zeros((C, C)); P = np.zeros((C, C))
+                for i0 in range(0, C, sub):
+                    m = i0 + sub // 2 - 1                      # the block's reference token
+                    last = i0 + sub                            # columns s < last
+                    lf = np.exp(G[i0:last] - G[m])             # rows t of block I
+                    rf = np.exp(G[m] - G[:last])               # columns s <= last token
+                    fmax = max(fmax, lf.max(), rf.max())
+                    kt = Kc[i0:last] * lf
+                    qt = Qc[i0:last] * lf
+                    ks = Kc[:last] * rf
+                    A[i0:last, :last] = kt @ ks.T
+                    P[i0:last, :last] = qt @ ks.T
+                tt = np.arange(C)
+                A = be[:, None] * A * (tt[None, :] < tt[:, None])
+                P = P * (tt[None, :] <= tt[:, None])
+                Tm = np.linalg.inv(np.eye(C) + A)
+                W = Tm @ (be[:, None] * (Kc * np.exp(G)))
+                Ut = Tm @ (be[:, None] * Vc)
+                U = Ut - W @ S.T
+                O = (Qc * np.exp(G)) @ S.T + P @ U
+                S = S * np.exp(G[-1])[None, :] + U.T @ (Kc * np.exp(G[-1] - G))
+                o[b, c0:c0 + n, h] = O[:n]
+            ST[b, h] = S
+    return o, ST, fmax

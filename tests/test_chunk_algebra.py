@@ -20,3 +20,97 @@ def test_chunk_form_equals_recurrence(T, C):
     oc, STc = chunk_recurrence(q, k, v, alpha, beta, S0=S0, C=C)
     np.testing.assert_allclose(oc, o, atol=1e-11, rtol=0)
     np.testing.assert_allclose(STc, ST, atol=1e-11, rtol=0)
+
+
+def _gdn_problem(rng, B, T, H, K, V):
+    q = rng.standard_normal((B, T, H, K)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((B, T, H, K)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, V))
+    alpha = rng.uniform(0.2, 1.0, size=(B, T, H))
+    beta = rng.uniform(0.0, 1.9, size=(B, T, H))
+    S0 = rng.standard_normal((B, H, V, K))
+    return q, k, v, alpha, beta, S0
+
+
+@pytest.mark.parametrize("T", [1, 64, 130, 257])
+@pytest.mark.parametrize("lookahead", [False, True])
+def test_state_chain_forms_equal_recurrence(T, lookahead):
+    """The state pass's chain on T', T'', P -- as run today, and in the
+    look-ahead form U(n+1) = U~ + S(n-1) [gamma_n NW(n+1)] + U(n)^T M(n) --
+    equals the token recurrence to rounding."""
+    from chunk_ref import chunk_state_chain
+    rng = np.random.default_rng(3 * T + int(lookahead))
+    q, k, v, alpha, beta, S0 = _gdn_problem(rng, 1, T, 2, 8, 6)
+    o, ST = oracle.recurrence(q, k, v, alpha, beta, S0=S0)
+    oc, STc = chunk_state_chain(q, k, v, alpha, beta, S0=S0, lookahead=lookahead)
+    np.testing.assert_allclose(oc, o, atol=1e-11, rtol=0)
+    np.testing.assert_allclose(STc, ST, atol=1e-11, rtol=0)
+
+
+def test_lookahead_rounding_stays_in_the_state_bound():
+    """With the kernel's bf16 operand roundings and float32 accumulation
+    emulated, on long-horizon gates and keys in a narrow cone (the case with
+    the thinnest margin), the look-ahead chain's final-state error stays
+    below the 1e-2 bound and within 1.5x of today's chain (it adds one
+    separately rounded term: ~3.4e-3 -> ~4.3e-3 here)."""
+    from chunk_ref import bf16_round, chunk_state_chain
+    rng = np.random.default_rng(7)
+    B, T, H, K, V = 1, 2048, 2, 128, 128
+    mu = rng.standard_normal((H, K))
+    mu *= 8.18 / np.linalg.norm(mu, axis=-1, keepdims=True)
+    k = mu[None, None] + 0.35 * rng.standard_normal((B, T, H, K))
+    k = bf16_round(k / np.linalg.norm(k, axis=-1, keepdims=True))
+    q = rng.standard_normal((B, T, H, K))
+    q = bf16_round(q / np.linalg.norm(q, axis=-1, keepdims=True))
+    v = bf16_round(rng.standard_normal((B, T, H, V)))
+    alpha = rng.uniform(0.9995, 0.9999, size=(B, T, H)).astype(np.float32).astype(np.float64)
+    beta = (1 / (1 + np.exp(-rng.standard_normal((B, T, H))))).astype(np.float32)
+    beta = beta.astype(np.float64)
+    _, ST = oracle.recurrence(q, k, v, alpha, beta)
+    err = {}
+    for la in (False, True):
+        _, STc = chunk_state_chain(q, k, v, alpha, beta, lookahead=la, rnd=bf16_round)
+        err[la] = max(np.linalg.norm(STc[0, h] - ST[0, h]) / np.linalg.norm(ST[0, h])
+                      for h in range(H))
+    assert err[False] < 1e-2 and err[True] < 1e-2, err
+    assert err[True] < 1.5 * err[False], err
+
+
+def test_bf16_round_is_round_to_nearest_even():
+    from chunk_ref import bf16_round
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties go to the even mantissa (1)
+    assert bf16_round(np.array([1 + 2.0 ** -8]))[0] == 1.0
+    assert bf16_round(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
+    assert bf16_round(np.array([1 + 2.0 ** -8 + 2.0 ** -20]))[0] == 1 + 2.0 ** -7
+    assert bf16_round(np.array([-3.0]))[0] == -3.0
+
+
+@pytest.mark.parametrize("T,sub,lo", [(64, 16, 0.5), (130, 16, 0.5), (100, 8, 0.05),
+                                      (200, 16, 0.01)])
+def test_kda_chunk_form_equals_gated_oracle(T, sub, lo):
+    """The chunkwise KDA form with the per-channel exponents of A' and P'
+    referred to each row block's midpoint equals the token-by-token KDA
+    oracle, and every exponential it forms stays below e^(sub/2 max|log a|)
+    -- while the plain split e^(G_t) e^(-G_s) would need e^(-G) beyond the
+    float32 range on fast-decaying channels (the last case)."""
+    from chunk_ref import kda_chunk_recurrence
+    rng = np.random.default_rng(T + sub)
+    B, H, K, V = 1, 2, 8, 6
+    q = rng.standard_normal((B, T, H, K)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((B, T, H, K)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, V))
+    hi = 0.2 if lo < 0.05 else 1.0
+    alpha = rng.uniform(lo, hi, size=(B, T, H, K))
+    beta = rng.uniform(0.0, 1.9, size=(B, T, H))
+    S0 = rng.standard_normal((B, H, V, K))
+    o, ST = oracle.recurrence_gated(q, k, v, alpha, beta, S0=S0, gate="kda")
+    oc, STc, fmax = kda_chunk_recurrence(q, k, v, alpha, beta, S0=S0, sub=sub)
+    scale = max(1.0, np.abs(o).max())
+    np.testing.assert_allclose(oc, o, atol=1e-10 * scale, rtol=0)
+    np.testing.assert_allclose(STc, ST, atol=1e-10 * max(1.0, np.abs(ST).max()), rtol=0)
+    bound = np.exp(sub / 2 * np.abs(np.log(alpha)).max())
+    assert fmax <= bound * (1 + 1e-12)
+    assert fmax < np.finfo(np.float32).max
+    if lo < 0.05:
+        G = np.cumsum(np.log(alpha[0, :64, 0]), axis=0)
+        assert -G.min() > np.log(np.finfo(np.float32).max)
