@@ -349,8 +349,7 @@ def run_ours(args, rank, world, barrier, max_over_ranks):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded generator; per-head decay centres, L2-normalised q/k)",
-        "config": dict(W, l2="inputs larger than L2 (537 MB per step)",
-                       parallelism=f"independent batch per GPU x{world}"),
+        "config": headline_config(W, world),
         "roofline": {
             "bound": roof_bound,
             "achieved": achieved_gbs if roof_bound == "hbm" else achieved_tf,
@@ -786,6 +785,12 @@ def cpu_baseline(p, seqs=None, reps=1):
                       f"tokens/s = sequences*T/H / wall time ({dt:.2f} s)"}
 
 
+def headline_config(W, world):
+    """The `config` object both arms print for the headline workload."""
+    return dict(W, l2="inputs larger than L2 (537 MB per step)",
+                parallelism=f"independent batch per GPU x{world}")
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: each step is a bounded sample of the
     headline workload (whole sequences) on the host cores."""
@@ -815,7 +820,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": dict(WORKLOAD, B=Bw),
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": headline_config(dict(WORKLOAD, B=Bw), world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": seqs, "kind": "oracle",
                          "sample": f"{seqs} (b, h) sequences x first {Tc} tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
