@@ -137,7 +137,7 @@ def chunk_state_chain(q, k, v, alpha, beta, S0=None, C=64, lookahead=False, rnd=
     return o, ST
 
 
-def kda_chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64, sub=16):
+def kda_chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64, sub=16, rnd=None):
     """Chunkwise form of KDA (per-key-channel decay alpha_t in R^K on the right
     of the state, scalar beta), with the per-channel exponents inside the
     intra-chunk products referred to the midpoint of each `sub`-token row
@@ -155,7 +155,14 @@ def kda_chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64, sub=16):
     is one product of two scaled operands, and every factor is at most
     e^(sub/2 max |log alpha|) (at most 1 for s before the block).  Returns
     (o, S_T, max_factor), max_factor the largest exponential formed.
+    rnd (e.g. bf16_round) rounds every tensor-core operand as a kernel would
+    (the scaled block operands, T diag(beta), the scaled keys and queries,
+    the state copy, U, P'); products then accumulate in float32, the inverse
+    and the state stay float32.
     """
+    r = rnd if rnd is not None else (lambda x: x)
+    acc = np.float32 if rnd is not None else np.float64
+    mm = lambda a, b_: (np.asarray(a, acc) @ np.asarray(b_, acc)).astype(np.float64)
     B, T, H, K = k.shape
     V = v.shape[-1]
     o = np.zeros((B, T, H, V))
@@ -179,20 +186,23 @@ def kda_chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64, sub=16):
                     lf = np.exp(G[i0:last] - G[m])             # rows t of block I
                     rf = np.exp(G[m] - G[:last])               # columns s <= last token
                     fmax = max(fmax, lf.max(), rf.max())
-                    kt = Kc[i0:last] * lf
-                    qt = Qc[i0:last] * lf
-                    ks = Kc[:last] * rf
-                    A[i0:last, :last] = kt @ ks.T
-                    P[i0:last, :last] = qt @ ks.T
+                    kt = r(Kc[i0:last] * lf)
+                    qt = r(Qc[i0:last] * lf)
+                    ks = r(Kc[:last] * rf)
+                    A[i0:last, :last] = mm(kt, ks.T)
+                    P[i0:last, :last] = mm(qt, ks.T)
                 tt = np.arange(C)
                 A = be[:, None] * A * (tt[None, :] < tt[:, None])
                 P = P * (tt[None, :] <= tt[:, None])
-                Tm = np.linalg.inv(np.eye(C) + A)
-                W = Tm @ (be[:, None] * (Kc * np.exp(G)))
-                Ut = Tm @ (be[:, None] * Vc)
-                U = Ut - W @ S.T
-                O = (Qc * np.exp(G)) @ S.T + P @ U
-                S = S * np.exp(G[-1])[None, :] + U.T @ (Kc * np.exp(G[-1] - G))
+                Tm = np.linalg.inv((np.eye(C) + A).astype(acc)).astype(np.float64)
+                Tb = r(Tm * be[None, :])                        # T diag(beta)
+                W = r(mm(Tb, r(Kc * np.exp(G))))
+                Ut = mm(Tb, Vc)
+                U = Ut - mm(W, r(S).T)
+                Ub = r(U)
+                O = mm(r(Qc * np.exp(G)), r(S).T) + mm(r(P), Ub)
+                S = (S * np.exp(G[-1])[None, :]).astype(acc).astype(np.float64) + \
+                    mm(Ub.T, r(Kc * np.exp(G[-1] - G)))
                 o[b, c0:c0 + n, h] = O[:n]
             ST[b, h] = S
     return o, ST, fmax

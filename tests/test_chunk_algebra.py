@@ -114,3 +114,20 @@ def test_kda_chunk_form_equals_gated_oracle(T, sub, lo):
     if lo < 0.05:
         G = np.cumsum(np.log(alpha[0, :64, 0]), axis=0)
         assert -G.min() > np.log(np.finfo(np.float32).max)
+
+
+def test_kda_chunk_form_bf16_within_tolerance():
+    """On the KDA workload's gates (per-channel decays, |log alpha| up to ~3)
+    and with bf16 operands emulated, the chunkwise KDA form stays within the
+    bf16 tolerance of the GPU tests against the float64 oracle (~4e-3 here),
+    which is what a tensor-core KDA prefill on these operands would reach."""
+    from chunk_ref import bf16_round, kda_chunk_recurrence
+    from gated_delta_rule_49_gb300 import inputs
+    from gpu_util import TOL, rel_err
+    p = inputs.make_channel_gated(seed=3, B=1, T=1024, H=2, K=128, V=128, gate="kda")
+    q, k, v = (np.asarray(x, np.float64) for x in (p.q, p.k, p.v))
+    alpha, beta = np.asarray(p.alpha, np.float64), np.asarray(p.beta, np.float64)
+    o, ST = oracle.recurrence_gated(q, k, v, alpha, beta, gate="kda")
+    oc, STc, fmax = kda_chunk_recurrence(q, k, v, alpha, beta, rnd=bf16_round)
+    assert rel_err(oc, o) <= TOL["bf16"] / 2 and rel_err(STc, ST) <= TOL["bf16"] / 2
+    assert fmax < 1e10
