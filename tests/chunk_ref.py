@@ -206,3 +206,51 @@ def kda_chunk_recurrence(q, k, v, alpha, beta, S0=None, C=64, sub=16, rnd=None):
                 o[b, c0:c0 + n, h] = O[:n]
             ST[b, h] = S
     return o, ST, fmax
+
+
+def gdn2_chunk_recurrence(q, k, v, alpha, b_gate, w_gate, S0=None, C=64, sub=16):
+    """Chunkwise form of GDN2: the KDA decay with a key-side erase gate b
+    (erase direction e_t = b_t (.) k_t) and a value-side write gate w
+    (content z_t = w_t (.) v_t); the outer products keep k_t on their right.
+    KDA's algebra with beta_t k_t -> e_t in the rows of A and in W, and
+    beta_t v_t -> z_t:
+
+      A''_ts = sum_j e_tj k_sj e^(G_tj - G_sj)  (s < t),  T = (I + A'')^{-1}
+      U = T Z - T (E (.) e^G) S^T,   O and S as for KDA,
+
+    the exponents referred to each row block's midpoint as in
+    kda_chunk_recurrence.  Float64; returns (o, S_T)."""
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.zeros((B, T, H, V))
+    ST = np.zeros((B, H, V, K))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((V, K)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
+            for c0 in range(0, T, C):
+                n = min(C, T - c0)
+                Kc = np.zeros((C, K)); Qc = np.zeros((C, K)); Ec = np.zeros((C, K))
+                Zc = np.zeros((C, V)); lg = np.zeros((C, K))
+                Kc[:n] = k[b, c0:c0 + n, h]; Qc[:n] = q[b, c0:c0 + n, h]
+                Ec[:n] = b_gate[b, c0:c0 + n, h] * k[b, c0:c0 + n, h]
+                Zc[:n] = w_gate[b, c0:c0 + n, h] * v[b, c0:c0 + n, h]
+                lg[:n] = np.log(alpha[b, c0:c0 + n, h])
+                G = np.cumsum(lg, axis=0)
+                A = np.zeros((C, C)); P = np.zeros((C, C))
+                for i0 in range(0, C, sub):
+                    m = i0 + sub // 2 - 1
+                    last = i0 + sub
+                    lf = np.exp(G[i0:last] - G[m])
+                    ks = Kc[:last] * np.exp(G[m] - G[:last])
+                    A[i0:last, :last] = (Ec[i0:last] * lf) @ ks.T
+                    P[i0:last, :last] = (Qc[i0:last] * lf) @ ks.T
+                tt = np.arange(C)
+                A = A * (tt[None, :] < tt[:, None])
+                P = P * (tt[None, :] <= tt[:, None])
+                Tm = np.linalg.inv(np.eye(C) + A)
+                U = Tm @ Zc - (Tm @ (Ec * np.exp(G))) @ S.T
+                O = (Qc * np.exp(G)) @ S.T + P @ U
+                S = S * np.exp(G[-1])[None, :] + U.T @ (Kc * np.exp(G[-1] - G))
+                o[b, c0:c0 + n, h] = O[:n]
+            ST[b, h] = S
+    return o, ST

@@ -131,3 +131,23 @@ def test_kda_chunk_form_bf16_within_tolerance():
     oc, STc, fmax = kda_chunk_recurrence(q, k, v, alpha, beta, rnd=bf16_round)
     assert rel_err(oc, o) <= TOL["bf16"] / 2 and rel_err(STc, ST) <= TOL["bf16"] / 2
     assert fmax < 1e10
+
+
+@pytest.mark.parametrize("T", [64, 130])
+def test_gdn2_chunk_form_equals_gated_oracle(T):
+    """GDN2's chunk form (erase direction b (.) k in the rows of A'' and in W,
+    write content w (.) v) equals the token-by-token GDN2 oracle."""
+    from chunk_ref import gdn2_chunk_recurrence
+    rng = np.random.default_rng(T + 11)
+    B, H, K, V = 1, 2, 8, 6
+    q = rng.standard_normal((B, T, H, K)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((B, T, H, K)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, V))
+    alpha = rng.uniform(0.3, 1.0, size=(B, T, H, K))
+    bg = rng.uniform(0.0, 1.0, size=(B, T, H, K))
+    wg = rng.uniform(0.0, 1.0, size=(B, T, H, V))
+    S0 = rng.standard_normal((B, H, V, K))
+    o, ST = oracle.recurrence_gated(q, k, v, alpha, b=bg, w=wg, S0=S0, gate="gdn2")
+    oc, STc = gdn2_chunk_recurrence(q, k, v, alpha, bg, wg, S0=S0)
+    np.testing.assert_allclose(oc, o, atol=1e-10, rtol=0)
+    np.testing.assert_allclose(STc, ST, atol=1e-10, rtol=0)
