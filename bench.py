@@ -768,7 +768,31 @@ def oracle_sample(p, seqs):
                           cat([s.beta for s in subs]), None, {})
 
 
-def cpu_baseline(p, seqs=None, reps=1):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(p, seqs=None, reps=1, single_seqs=2):
+    """The float64 oracle on the host cores: the whole workload on every core
+    (one thread per independent sequence), and a few whole sequences on one
+    thread."""
     import oracle
     cores = os.cpu_count() or 1
     B, T, H, K = p.k.shape
@@ -780,7 +804,15 @@ def cpu_baseline(p, seqs=None, reps=1):
         oracle.recurrence(sub.q, sub.k, sub.v, sub.alpha, sub.beta, threads=threads)
     dt = (time.perf_counter() - t0) / reps
     token_heads = seqs * T
+    one = oracle_sample(p, single_seqs)
+    t0 = time.perf_counter()
+    oracle.recurrence(one.q, one.k, one.v, one.alpha, one.beta, threads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": token_heads / H / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "nproc": cores, "cpu_model": cpu_model(),
+            "single_thread": {"value": single_seqs * T / H / dt1, "unit": "tokens/s",
+                              "wall_s": dt1,
+                              "sample": f"{single_seqs} (b, h) sequences x {T} tokens, one thread"},
             "sample": f"{seqs} of {B * H} (b, h) sequences x {T} tokens, float64 C oracle; "
                       f"tokens/s = sequences*T/H / wall time ({dt:.2f} s)"}
 
@@ -823,6 +855,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": headline_config(dict(WORKLOAD, B=Bw), world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": seqs, "kind": "oracle",
+                         "nproc": cores, "cpu_model": cpu_model(),
                          "sample": f"{seqs} (b, h) sequences x first {Tc} tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

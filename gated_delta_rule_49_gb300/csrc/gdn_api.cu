@@ -2,6 +2,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -14,6 +16,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_status_ptr[kMaxDevices];
+uintptr_t g_status_ctx[kMaxDevices];  // the context g_status_ptr was looked up in
 int g_sm_count[kMaxDevices];
 
 int current_device() {
@@ -23,14 +26,35 @@ int current_device() {
 }
 }  // namespace
 
+uintptr_t context_key() {
+    // the driver entry point is fetched through the runtime, so the library
+    // keeps no link-time dependency on libcuda (it loads on machines without
+    // a driver; nothing here runs there)
+    using GetCurrent = CUresult (*)(CUcontext *);
+    static GetCurrent fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<GetCurrent>(p);
+    }();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return 0;
+    return reinterpret_cast<uintptr_t>(ctx);
+}
+
 int *device_status_ptr() {
     const int dev = current_device();
     if (dev < 0) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_status_ptr[dev]) {
+    const uintptr_t ctx = context_key();
+    if (!g_status_ptr[dev] || ctx == 0 || g_status_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
         g_status_ptr[dev] = static_cast<int *>(p);
+        g_status_ctx[dev] = context_key();  // current now that the lookup ran
     }
     return g_status_ptr[dev];
 }

@@ -380,14 +380,14 @@ cudaError_t launch_channel_gram(const void *k, const void *q, int B, int T, int 
     const int splits = gram_splits(B, T, H);
     const int chunks = B * ((T + 63) / 64);
     const int per = (chunks + splits - 1) / splits;
-    static bool attr_set[64] = {};
+    static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (attr_set[dev] != context_key()) {
         const cudaError_t e = cudaFuncSetAttribute(
             gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GramSmem::BYTES);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev] = context_key();
     }
     float *partial = static_cast<float *>(workspace);
     gram_kernel<<<dim3(splits, H), kGramThreads, GramSmem::BYTES, stream>>>(

@@ -317,14 +317,14 @@ cudaError_t launch_pg(const void *q, const void *k, const void *v, const float *
     static_assert(threads >= 32 && threads <= 128 && R % (RPI * RPL) == 0, "tiling");
     static_assert(CPL % 4 == 0 && K % CPL == 0 && 32 % (K / CPL) == 0, "channels per lane");
     auto kern = prefill_gated_kernel<K, R, CPL, RPL, Tin, GATE>;
-    static bool attr_set[64] = {};
+    static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (L::SMEM > 48 * 1024 && !attr_set[dev]) {
+    if (L::SMEM > 48 * 1024 && attr_set[dev] != context_key()) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev] = context_key();
     }
     const long long grid = (long long)B * H * (V / R);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

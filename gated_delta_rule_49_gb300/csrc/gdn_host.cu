@@ -28,14 +28,17 @@ constexpr int kMaxDev = 64;
 struct HostPipe {
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t in_ready[2], in_free[2], out_ready[2], out_free[2], done, s0_ready;
-    bool ok = false;
+    uintptr_t ctx = 0;  // the context the streams and events belong to (0: none yet)
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDev];
 
 cudaError_t pipe_for(int dev, HostPipe **out) {
     HostPipe &p = g_pipe[dev];
-    if (!p.ok) {
+    // made once per device and context (a reset context invalidates the old
+    // handles, which are then simply forgotten)
+    if (p.ctx == 0 || p.ctx != context_key()) {
+        p.ctx = 0;
         cudaError_t e = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking);
         cudaEvent_t *evs[] = {&p.in_ready[0], &p.in_ready[1], &p.in_free[0], &p.in_free[1],
@@ -44,7 +47,7 @@ cudaError_t pipe_for(int dev, HostPipe **out) {
         for (cudaEvent_t *ev : evs)
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
         if (e != cudaSuccess) return e;
-        p.ok = true;
+        p.ctx = context_key();
     }
     *out = &p;
     return cudaSuccess;

@@ -30,6 +30,12 @@ int *device_status_ptr();
 // Streaming multiprocessor count of the current device (cached).
 int sm_count();
 
+// Identifies the CUDA context current on the calling thread (0 if none is
+// current yet).  Per-device caches of symbol addresses, kernel attributes,
+// streams and events remember the context they were made in and are redone
+// when another context is current (e.g. after cudaDeviceReset).
+uintptr_t context_key();
+
 // --- launchers (return the launch error, never synchronise) ---------------
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *alpha,
                           const float *beta, float *S, void *o, int B, int H, int K, int V,

@@ -10,24 +10,31 @@ namespace {
 // Scratch for gdn_prefill_noalloc.  Every GPU that loads the library holds
 // these 32 MiB until the process exits.  In host code `g_noalloc_scratch` is
 // only a host-side stand-in for the symbol, never a device address: the
-// address is looked up per device with cudaGetSymbolAddress below.
+// address is looked up per device with cudaGetSymbolAddress below.  Under
+// CUDA's default lazy module loading the array is only materialised on a
+// device when the first call there looks its address up (a driver allocation
+// that may synchronise); a caller that must not allocate after start-up makes
+// one small call per device at start-up.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDev];
+uintptr_t g_scratch_ctx[kMaxDev];  // the context the address belongs to
 
 // Device address of the scratch array on the current device (looked up once
-// per device, with that device current), or nullptr on failure.
+// per device and context, with that device current), or nullptr on failure.
 void *scratch_address() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    const uintptr_t ctx = gdn::context_key();
+    if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = gdn::context_key();  // current now that the lookup ran
     }
     return g_scratch_ptr[dev];
 }

@@ -549,6 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *sm = smem_raw;
     __shared__ uint64_t kq_full[3], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready[2], nw_free;
     __shared__ uint64_t ua_free[2], pt_free[2];
+    __shared__ uint64_t drain[2];  // abort path: the two MMA-issuing threads' products done
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -577,7 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_v);
         uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full, &bar_p1, &bar_w,
                             &bar_u, &bar_s, &nw_ready[0], &nw_ready[1], &nw_free,
-                            &ua_free[0], &ua_free[1], &pt_free[0], &pt_free[1]};
+                            &ua_free[0], &ua_free[1], &pt_free[0], &pt_free[1],
+                            &drain[0],   &drain[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -976,6 +978,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_v) {
+        // products still in flight read shared memory and write TMEM: each
+        // issuing thread's commit completes once all of its products have
+        if (tid == 0 || tid == kKeyThreads) {
+            uint64_t *d = &drain[tid == 0 ? 0 : 1];
+            mma_commit(d);
+            mbar_wait(d, 0, kSpinLimit / 16);
+        }
         if (tid == 0) {
             if (status) atomicOr(status, kStatusTimeout);
             // let in-flight loads land before the CTA's shared memory is released
@@ -1038,7 +1047,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full, bar_p1;
+    __shared__ uint64_t kq_full, bar_p1, drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -1055,6 +1064,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         tma_prefetch_desc(&tm_k);
         mbar_init(&kq_full, 1);
         mbar_init(&bar_p1, 1);
+        mbar_init(&drain, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -1155,6 +1165,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     if (*abort_v) {
         if (tid == 0) {
             if (status) atomicOr(status, kStatusTimeout);
+            // a product still in flight reads shared memory and writes TMEM
+            mma_commit(&drain);
+            mbar_wait(&drain, 0, kSpinLimit / 16);
             // let an in-flight load land before the CTA's shared memory is released
             mbar_wait(&kq_full, 0, kSpinLimit / 16);
             mbar_wait(&kq_full, 1, kSpinLimit / 16);
@@ -1257,7 +1270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     uint8_t *sm = smem_raw;
     __shared__ uint64_t kq_full[3], v_full[3], tt_full[2], p_full[2], bar_w, bar_u, bar_s, bar_o2,
-        nw_ready[2], ua_free[2];
+        nw_ready[2], ua_free[2], drain[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -1287,7 +1300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint64_t *bars[] = {&kq_full[0], &kq_full[1],  &kq_full[2], &v_full[0],  &v_full[1],
                             &v_full[2],  &tt_full[0],  &tt_full[1], &p_full[0],  &p_full[1],
                             &bar_w,      &bar_u,       &bar_s,      &bar_o2,     &nw_ready[0],
-                            &nw_ready[1], &ua_free[0], &ua_free[1]};
+                            &nw_ready[1], &ua_free[0], &ua_free[1], &drain[0],   &drain[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -1693,6 +1706,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_v) {
+        // products still in flight read shared memory and write TMEM: each
+        // issuing thread's commit completes once all of its products have
+        if (tid == 0 || tid == kKeyThreads) {
+            uint64_t *d = &drain[tid == 0 ? 0 : 1];
+            mma_commit(d);
+            mbar_wait(d, 0, kSpinLimit / 16);
+        }
         if (tid == 0) {
             if (status) atomicOr(status, kStatusTimeout);
             // let in-flight loads land before the CTA's shared memory is released
@@ -1802,17 +1822,17 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
                         const float *beta, uint8_t *prep, long long BH, int T, int Ts, int H,
                         cudaStream_t stream) {
     auto kern = prefill_prep_kernel<K>;
-    static bool attr_set[64] = {};
+    static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (attr_set[dev] != context_key()) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)PrepLayout<K>::SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev] = context_key();
     }
     // persistent CTAs, kPrepCtasPerSm per SM (the loop is correct for any residency)
     const long long total = BH * ((T + 63) / 64);
@@ -1830,19 +1850,19 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
                    const CUtensorMap &mo, const float *alpha, const float *beta, const float *S0,
                    void *o, float *ST, long long BH, int T, int Ts, int H, const SegShape &sh,
                    float *ws, const uint8_t *prep, cudaStream_t stream) {
-    static bool attr_set[2][64] = {};
+    static uintptr_t attr_set[2][64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const int two = prep != nullptr;
     const size_t smem = two ? StLayout<K>::SMEM : TcLayout<K>::SMEM;
-    if (!attr_set[two][dev]) {
+    if (attr_set[two][dev] != context_key()) {
         const cudaError_t e =
             two ? cudaFuncSetAttribute(prefill_state_kernel<K>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                 : cudaFuncSetAttribute(prefill_tc_kernel<K>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set[two][dev] = true;
+        attr_set[two][dev] = context_key();
     }
     __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(o);
     int *status = device_status_ptr();

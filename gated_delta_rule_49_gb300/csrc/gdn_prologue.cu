@@ -205,15 +205,15 @@ cudaError_t launch_gn_t(const void *x, const int *idx, void *y, long long rows, 
         if (blocks > sms * 3) blocks = sms * 3;  // 64 KB of slots: three CTAs per SM
         if (blocks < 1) blocks = 1;
         auto kern = gather_normalize_staged<T, KOUT>;
-        static bool attr_set[64] = {};
+        static uintptr_t attr_set[64] = {};  // context the attributes were set in
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
             return cudaErrorInvalidDevice;
-        if (!attr_set[dev]) {
+        if (attr_set[dev] != context_key()) {
             const cudaError_t e = cudaFuncSetAttribute(
                 kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStagedSmem);
             if (e != cudaSuccess) return e;
-            attr_set[dev] = true;
+            attr_set[dev] = context_key();
         }
         kern<<<(unsigned)blocks, kStagedWarps * 32, kStagedSmem, stream>>>(
             static_cast<const T *>(x), idx, static_cast<T *>(y), rows, H, Kin, rpt, eps,

@@ -202,14 +202,14 @@ cudaError_t launch_trunc_t(float *S, int BH, int r, float *sigma, int max_sweeps
                            cudaStream_t stream) {
     using L = TruncSmem<V, K>;
     auto kern = truncate_kernel<V, K>;
-    static bool attr_set[64] = {};
+    static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (attr_set[dev] != context_key()) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev] = context_key();
     }
     kern<<<BH, K / 2 * kLanesPerPair, L::BYTES, stream>>>(S, r, sigma, max_sweeps,
                                                           device_status_ptr());

@@ -126,7 +126,13 @@ GDN_API size_t gdn_prefill_two_pass_workspace_size(int B, int T, int H, int K, i
  *
  *  - The first call on a device that needs scratch looks up the array's
  *    device address (cudaGetSymbolAddress) with that device current; make
- *    that first call before any stream capture.
+ *    that first call before any stream capture.  Under CUDA's default lazy
+ *    module loading that lookup is also when the driver materialises the
+ *    array on the device (an allocation that may synchronise): a caller
+ *    that must not allocate after start-up makes one small call per device
+ *    at start-up.
+ *  - The address is cached per device and per CUDA context (looked up again
+ *    when another context is current, e.g. after cudaDeviceReset).
  *  - All calls on a device share the one array, and it keeps the contents of
  *    the last call.  Nothing needs clearing (each call writes every scratch
  *    value it reads), but calls that may overlap on the GPU -- on different

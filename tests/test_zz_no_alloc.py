@@ -79,13 +79,31 @@ def test_noalloc_matches_workspace_prefill_twice():
         assert _rel(S, S_ref) <= TOL_BF16, call
 
 
+def rejected_shape():
+    """A problem whose segment-parallel scratch exceeds the array on this
+    device: few long sequences, more heads until the scratch no longer fits
+    (the segment count depends on the SM count, so the shape is searched)."""
+    cap = binding.gdn_prefill_noalloc_max_workspace()
+    for T in (65536, 262144):
+        for H in range(1, 129):
+            need = binding.gdn_prefill_workspace_size(1, T, H, 128, 128, binding.GDN_BF16)
+            if need > cap:
+                return 1, T, H, need
+    return None
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
+    import torch
+    assert torch.cuda.is_available()
     lib = binding.load()
-    B, T, H, K, V = 1, 65536, 24, 128, 128  # 24 long heads: ~58 MiB of scratch
-    need = binding.gdn_prefill_workspace_size(B, T, H, K, V, binding.GDN_BF16)
-    if need <= binding.gdn_prefill_noalloc_max_workspace():
-        pytest.skip("this device needs no more scratch than the array holds for the shape")
+    found = rejected_shape()
+    assert found is not None, "no shape needs more scratch than the array holds"
+    B, T, H, need = found
+    K, V = 128, 128
+    assert need > binding.gdn_prefill_noalloc_max_workspace()
     fake = 0x10000  # never dereferenced: the size check returns before any launch
     rc = lib.gdn_prefill_noalloc(fake, fake, fake, fake, fake, None, fake, fake, B, T, H, K, V,
                                  binding.GDN_BF16, None)
     assert rc == binding.GDN_ERR_WORKSPACE
+    # nothing was launched: the device status word is clean
+    assert binding.gdn_get_last_device_status() == binding.GDN_OK
