@@ -68,44 +68,11 @@ constexpr int kBarKey = 1, kBarState = 2;       // named barrier ids
 constexpr long long kSpinLimit = 2000000000LL;  // ~1 s of SM clocks per wait
 constexpr int kLD = 68;                         // row stride of the fp32 64 x 64 matrix
 
-// Bytes of one chunk's key-side operands in the two-pass form: T', T'' and P,
-// each a 64 x 64 bf16 tile stored as its 128-byte-swizzled shared-memory image.
-constexpr uint32_t kPrepChunkBytes = 3 * 8192;
-
-template <int K>
-struct TcLayout {
-    // q/k stages (three): 64 x 64 bf16 boxes, 8 KB each; K and Q of one
-    // 64-channel block are adjacent so [K;Q] is one 128-row operand
-    static constexpr int NSTAGE = 3;
-    static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
-    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
-    static constexpr uint32_t VB = NSTAGE * STAGE;      // V: two 64-channel boxes
-    static constexpr uint32_t TP = VB + 16384, TPP = TP + 8192;
-    static constexpr uint32_t NW = TP;                  // -W^T (K rows) reuses T', T''
-    static constexpr uint32_t PT = TPP + 8192;          // two buffers of 8 KB
-    static constexpr uint32_t SB = PT + 16384;          // K/64 blocks of 128 rows
-    // U^T (128 rows, split in two 64-row halves): at K = 128 it reuses the
-    // gamma-scaled Q tiles of the chunk's own stage, which are spent by then
-    static constexpr uint32_t UTS = SB + (K / 64) * 16384;
-    static constexpr uint32_t UD = UTS + (K == 128 ? 0u : 16384u);
-    static constexpr uint32_t AF = UD + 16384;          // float [64][68]
-    static constexpr uint32_t XS = AF + 64 * kLD * 4;   // float [3][16][16] block scratch
-    static constexpr uint32_t KGATE = XS + 3 * 256 * 4; // key group: G2, gamma, beta
-    static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;  // state: 3 x (decay[64], gamma_C)
-    static constexpr uint32_t END = SGATE + 3 * 68 * 4;
-    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
-    static constexpr uint32_t V_BYTES = 2u * 8192u;
-    static constexpr size_t SMEM = END;
-    // 227 KB per CTA, of which the kernel's static variables take 1 KB (the
-    // 1024-byte alignment of the dynamic region pads them)
-    static_assert(SMEM + 1024 <= 232448, "shared memory budget");
-    static __device__ __forceinline__ uint32_t ut_half(int st, int hh) {
-        if (K == 128) return st * STAGE + (hh ? QC1 : QC0);
-        return UTS + hh * 8192;
-    }
-    // TMEM columns
-    static constexpr uint32_t D1 = 0, WT = 64, UA = 128, O = 256, DS = 384;
-};
+// Bytes of one chunk's key-side operands in the two-pass form: -W^T (16 KB:
+// 128 key-channel rows of 64 tokens), T''^T and P (8 KB each), every tile
+// stored as its 128-byte-swizzled shared-memory image.
+constexpr uint32_t kPrepNW = 0, kPrepTPP = 16384, kPrepP = 24576;
+constexpr uint32_t kPrepChunkBytes = 32768;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
@@ -151,96 +118,162 @@ __device__ __forceinline__ void chunk_log2_prefix(float a0, float a1, int lane, 
 }
 
 // Blocks of the fp32 64 x 64 matrix in AF (16 x 16 blocks, row stride kLD):
-//   A_ij (i > j) at block position (i, j); after the inverse, T_ii at (i, i)
-//   and T_ij (i > j) at the mirrored position (j, i).
+// A_ij at block position (i, j); the inverse writes D_i = (I + A_ii)^{-1} over
+// the diagonal blocks.
 __device__ __forceinline__ float *blk(float *AF, int i, int j) {
     return AF + 16 * i * kLD + 16 * j;
 }
 
-// Y = sum_k L_k R_k for 16 x 16 blocks (row stride kLD, or ldr for R_0), 4
-// outputs per thread: row `row`, columns [c0, c0 + 4) (two warps per block).
-__device__ __forceinline__ float4 blk_mac(const float *L0, const float *R0, int ldr,
-                                          const float *L1, const float *R1,
-                                          const float *L2, const float *R2, int nterm, int row,
-                                          int c0) {
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *Ls[3] = {L0, L1, L2};
-    const float *Rs[3] = {R0, R1, R2};
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        if (k >= nterm) break;
-        const int ldrk = (k == 0) ? ldr : kLD;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float a = Ls[k][row * kLD + m];
-            const float4 r = *reinterpret_cast<const float4 *>(Rs[k] + m * ldrk + c0);
-            y.x = fmaf(a, r.x, y.x);
-            y.y = fmaf(a, r.y, y.y);
-            y.z = fmaf(a, r.z, y.z);
-            y.w = fmaf(a, r.w, y.w);
-        }
-    }
-    return y;
+// ---- the unit lower triangular inverse T = (I + A)^{-1} of one chunk ----
+//
+// Blocked by 16 x 16: the diagonal blocks D_i = (I + A_ii)^{-1} by forward
+// substitution in float32 on the CUDA cores (one column per thread), then the
+// off-diagonal blocks from the block form of (I + A) T = I,
+//
+//     T_ij = -D_i sum_{m=j}^{i-1} A_im T_mj      (i > j),
+//
+// computed transposed, U = T^T: warp j owns block row j of U (block column j
+// of T), U_ji = -(sum_m U_jm A_im^T) D_i^T, so each product's result is the
+// left operand of the next one and never leaves the warp's registers.  These
+// 16 x 16 x 16 products run on the register-level tensor-core MMA (mma.sync
+// m16n8k16; tcgen05 starts at 64 rows and works from shared memory / TMEM,
+// which would put a round trip on each of the chain's six dependent steps).
+// Operands are float32 values split into bf16 pairs x = hi + lo and each
+// product takes hi*hi + hi*lo + lo*hi with float32 accumulation: about 16
+// significant bits, where T' and T'' are rounded to bf16 (8 bits) afterwards.
+
+struct FragA {  // 16 x 16 left operand, hi and lo halves (m16n8k16 A layout)
+    uint32_t h[4], l[4];
+};
+struct FragB {  // 16 x 16 right operand as two 16 x 8 column tiles
+    uint32_t h[2][2], l[2][2];
+};
+
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// The same products for two rows (r0, r0 + 8) and four columns [c0, c0 + 4)
-// per thread: one warp per block.  Operands are read as float4 (four L columns of a row, four R rows at
-// a time); each output accumulates term by term, m ascending.
-__device__ __forceinline__ void blk_mac2(const float *L0, const float *R0, int ldr,
-                                         const float *L1, const float *R1, const float *L2,
-                                         const float *R2, int nterm, int r0, int c0, float4 &y0,
-                                         float4 &y1) {
-    y0 = make_float4(0.f, 0.f, 0.f, 0.f);
-    y1 = y0;
-    const float *Ls[3] = {L0, L1, L2};
-    const float *Rs[3] = {R0, R1, R2};
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The three terms of A B with split operands (lo*hi, hi*lo, hi*hi) go to
+// three accumulators (16 x 16 as two 16 x 8 tiles each), so consecutive
+// products into the same result do not wait on one another.
+__device__ __forceinline__ void mma_split(float (&d)[3][2][4], const FragA &a, const FragB &b) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        if (k >= nterm) break;
-        const int ldrk = (k == 0) ? ldr : kLD;
+    for (int nt = 0; nt < 2; ++nt) {
+        mma_16816(d[0][nt], a.l, b.h[nt][0], b.h[nt][1]);
+        mma_16816(d[1][nt], a.h, b.l[nt][0], b.l[nt][1]);
+        mma_16816(d[2][nt], a.h, b.h[nt][0], b.h[nt][1]);
+    }
+}
+__device__ __forceinline__ void sum_split(const float (&d)[3][2][4], float (&r)[2][4]) {
 #pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(Ls[k] + r0 * kLD + m);
-            const float4 a1 = *reinterpret_cast<const float4 *>(Ls[k] + (r0 + 8) * kLD + m);
-            const float la0[4] = {a0.x, a0.y, a0.z, a0.w}, la1[4] = {a1.x, a1.y, a1.z, a1.w};
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 r = *reinterpret_cast<const float4 *>(Rs[k] + (m + e) * ldrk + c0);
-                y0.x = fmaf(la0[e], r.x, y0.x);
-                y0.y = fmaf(la0[e], r.y, y0.y);
-                y0.z = fmaf(la0[e], r.z, y0.z);
-                y0.w = fmaf(la0[e], r.w, y0.w);
-                y1.x = fmaf(la1[e], r.x, y1.x);
-                y1.y = fmaf(la1[e], r.y, y1.y);
-                y1.z = fmaf(la1[e], r.z, y1.z);
-                y1.w = fmaf(la1[e], r.w, y1.w);
+        for (int e = 0; e < 4; ++e) r[nt][e] = (d[0][nt][e] + d[1][nt][e]) + d[2][nt][e];
+}
+
+// The accumulator layout of a 16 x 16 result (two 16 x 8 tiles) is the A
+// layout of m16n8k16: row g = lane / 4 (+ 8), columns 2 (lane % 4) (+ 1, + 8).
+__device__ __forceinline__ FragA frag_a(const float (&d)[2][4], float scale) {
+    FragA a;
+    split_bf16(scale * d[0][0], scale * d[0][1], a.h[0], a.l[0]);
+    split_bf16(scale * d[0][2], scale * d[0][3], a.h[1], a.l[1]);
+    split_bf16(scale * d[1][0], scale * d[1][1], a.h[2], a.l[2]);
+    split_bf16(scale * d[1][2], scale * d[1][3], a.h[3], a.l[3]);
+    return a;
+}
+
+// Right operand M^T for a 16 x 16 float32 block M (row stride kLD): element
+// (k, n) of the operand is M[n][k], so each register pair is two adjacent
+// elements of one row of M.
+__device__ __forceinline__ FragB frag_bt(const float *M, int g, int t4) {
+    FragB b;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const float *row = M + (8 * nt + g) * kLD + 2 * t4;
+        const float2 p0 = *reinterpret_cast<const float2 *>(row);
+        const float2 p1 = *reinterpret_cast<const float2 *>(row + 8);
+        split_bf16(p0.x, p0.y, b.h[nt][0], b.l[nt][0]);
+        split_bf16(p1.x, p1.y, b.h[nt][1], b.l[nt][1]);
+    }
+    return b;
+}
+
+// Block row J of U = T^T (warp J of the inverse): U_JJ = D_J^T, then
+// U_Ji = -(sum_{m=J}^{i-1} U_Jm A_im^T) D_i^T for i > J; U_Ji = 0 for i < J.
+// u[i] receives U_Ji in the accumulator layout.  One code path for all four
+// warps (J is warp-uniform, the block indices compile-time), so the four
+// block rows share their instructions.
+__device__ __forceinline__ void inverse_block_row(float *AF, int J, int g, int t4,
+                                                  float (&u)[4][2][4]) {
+    FragA ua[3];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i < J) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[i][nt][e] = 0.f;
+        } else if (i == J) {
+            // U_JJ[r][c] = D_J[c][r]: rows g, g + 8, columns 8 nt + 2 t4 (+ 1)
+            const float *D = blk(AF, i, i);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int c = 8 * nt + 2 * t4;
+                u[i][nt][0] = D[c * kLD + g];
+                u[i][nt][1] = D[(c + 1) * kLD + g];
+                u[i][nt][2] = D[c * kLD + g + 8];
+                u[i][nt][3] = D[(c + 1) * kLD + g + 8];
             }
+            if (i < 3) ua[i] = frag_a(u[i], 1.f);
+        } else {
+            float acc[3][2][4] = {};
+#pragma unroll
+            for (int m = 0; m < i; ++m)
+                if (m >= J) mma_split(acc, ua[m], frag_bt(blk(AF, i, m), g, t4));
+            float x[2][4];
+            sum_split(acc, x);
+            const FragA xa = frag_a(x, -1.f);
+            float acc2[3][2][4] = {};
+            mma_split(acc2, xa, frag_bt(blk(AF, i, i), g, t4));
+            sum_split(acc2, u[i]);
+            if (i < 3) ua[i] = frag_a(u[i], 1.f);
         }
     }
 }
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A in AF (zeros on and above
-// the diagonal), by NT threads (the fused kernel's 256 key-group threads, or
-// the key-side pass's 128, which take the narrow mapping): the four 16 x 16 diagonal
-// blocks by forward substitution (one column per thread), then the
-// off-diagonal blocks level by level, T_ij = -T_ii (sum_{j<=m<i} A_im T_mj),
-// each level a pair of 16 x 16 block products (one warp per block).  XS:
-// scratch for 3 blocks.
-// kNarrow selects the level mapping: two warps per block with one row of four
-// outputs per thread (shorter latency: the one-pass kernel, whose chunk loop
-// waits for it), or one warp per block with two rows of four (a third of the
-// shared-memory traffic: the key-side pass, bound by it).  Every output sums
-// the same terms in the same order either way, so the results are identical.
-template <bool kNarrow, int NT = kKeyThreads>
-__device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid) {
-    static_assert(kNarrow ? (NT >= 128 && NT % 32 == 0) : NT == 256, "inverse thread mapping");
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A in AF (fp32, zeros on
+// and above the diagonal), and from it the bf16 operand tiles
+//   T'^T  = diag(beta gamma) T^T,   T''^T = diag(beta) T^T
+// each 64 rows (token s) of 64 tokens t, 128 bytes per row with the 128-byte
+// swizzle: the MN-major image of the right operand of W^T = K^T T'^T and
+// U~^T = V^T T''^T.  The tiles may be shared or global memory.  Run by NT
+// threads (named barrier kBarKey): the first 64 solve the diagonal blocks,
+// warps 0-3 the off-diagonal ones.  AF's diagonal blocks are overwritten.
+template <int NT>
+__device__ __forceinline__ void chunk_inverse_tprime(float *AF, const float *bet, const float *gam,
+                                                     uint8_t *TPtile, uint8_t *TPPtile, int tid) {
+    static_assert(NT >= 128 && NT % 32 == 0, "inverse thread mapping");
     {
+        // D_i = (I + A_ii)^{-1}, column c of block i per thread
         float x[16];
-        const int bb = tid >> 4, s = tid & 15;
+        const int bb = tid >> 4, c = tid & 15;
         if (tid < 64) {
             const float *Ab = blk(AF, bb, bb);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) x[t] = (t == s) ? 1.f : 0.f;
+            for (int t = 0; t < 16; ++t) x[t] = (t == c) ? 1.f : 0.f;
 #pragma unroll
             for (int t = 1; t < 16; ++t) {
                 float a0 = 0.f, a1 = 0.f;
@@ -257,85 +290,32 @@ __device__ __forceinline__ void unit_lower_inverse(float *AF, float *XS, int tid
         }
         named_sync(kBarKey, NT);  // every read of the diagonal A blocks done
         if (tid < 64) {
-            float *Tb = blk(AF, bb, bb);
+            float *Db = blk(AF, bb, bb);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) Tb[t * kLD + s] = x[t];
+            for (int t = 0; t < 16; ++t) Db[t * kLD + c] = x[t];
         }
         named_sync(kBarKey, NT);
     }
-    if constexpr (!kNarrow) {
-        const int job = tid >> 6;  // which block of this level
-        const int e = tid & 63;
-        const int row = e >> 2, c0 = (e & 3) * 4;
-        // level d: blocks (j + d, j), j = 0 .. 3 - d
+    const int warp = tid >> 5;
+    if (warp < 4) {
+        const int lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+        float u[4][2][4];
+        inverse_block_row(AF, warp, g, t4, u);
+        // rows s0 = 16 warp + g and s0 + 8 of T'^T and T''^T
 #pragma unroll
-        for (int d = 1; d <= 3; ++d) {
-            const int j = job, i = job + d;
-            const bool active = job <= 3 - d;
-            if (active) {
-                // X = sum_{m=j}^{i-1} A_im T_mj  (T_jj on the diagonal, T_mj, m > j, mirrored)
-                float4 y;
-                if (d == 1)
-                    y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, nullptr, nullptr, nullptr,
-                                nullptr, 1, row, c0);
-                else if (d == 2)
-                    y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
-                                blk(AF, j, j + 1), nullptr, nullptr, 2, row, c0);
-                else
-                    y = blk_mac(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1),
-                                blk(AF, j, j + 1), blk(AF, i, j + 2), blk(AF, j, j + 2), 3, row,
-                                c0);
-                *reinterpret_cast<float4 *>(XS + job * 256 + row * 16 + c0) = y;
-            }
-            named_sync(kBarKey, NT);
-            if (active) {
-                // T_ij = -T_ii X, stored mirrored at block (j, i)
-                const float4 y = blk_mac(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr,
-                                         nullptr, nullptr, 1, row, c0);
-                *reinterpret_cast<float4 *>(blk(AF, j, i) + row * kLD + c0) =
-                    make_float4(-y.x, -y.y, -y.z, -y.w);
-            }
-            named_sync(kBarKey, NT);
-        }
-        return;
-    }
-    // one warp per block of a level; lane: rows r0 and r0 + 8 (eight distinct
-    // rows per load: conflict-free with the row stride of 68 floats), columns
-    // [c0, c0 + 4)
-    const int job = tid >> 5;
-    const int r0 = (tid & 31) >> 2, c0 = (tid & 3) * 4;
-    // level d: blocks (j + d, j), j = 0 .. 3 - d
+        for (int hr = 0; hr < 2; ++hr) {
+            const int srow = 16 * warp + g + 8 * hr;
+            const float b = bet[srow], bg = b * gam[srow];
 #pragma unroll
-    for (int d = 1; d <= 3; ++d) {
-        const int j = job, i = job + d;
-        const bool active = job <= 3 - d;
-        if (active) {
-            // X = sum_{m=j}^{i-1} A_im T_mj   (T_jj on the diagonal, T_mj, m > j, mirrored)
-            float4 y0, y1;
-            if (d == 1)
-                blk_mac2(blk(AF, i, j), blk(AF, j, j), kLD, nullptr, nullptr, nullptr, nullptr, 1,
-                         r0, c0, y0, y1);
-            else if (d == 2)
-                blk_mac2(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1), blk(AF, j, j + 1),
-                         nullptr, nullptr, 2, r0, c0, y0, y1);
-            else
-                blk_mac2(blk(AF, i, j), blk(AF, j, j), kLD, blk(AF, i, j + 1), blk(AF, j, j + 1),
-                         blk(AF, i, j + 2), blk(AF, j, j + 2), 3, r0, c0, y0, y1);
-            *reinterpret_cast<float4 *>(XS + job * 256 + r0 * 16 + c0) = y0;
-            *reinterpret_cast<float4 *>(XS + job * 256 + (r0 + 8) * 16 + c0) = y1;
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float v0 = u[i][nt][2 * hr], v1 = u[i][nt][2 * hr + 1];
+                    const uint32_t off = swz128(srow, 2 * i + nt) + 4 * t4;
+                    *reinterpret_cast<uint32_t *>(TPtile + off) = pack_bf16(v0 * bg, v1 * bg);
+                    *reinterpret_cast<uint32_t *>(TPPtile + off) = pack_bf16(v0 * b, v1 * b);
+                }
         }
-        named_sync(kBarKey, NT);
-        if (active) {
-            // T_ij = -T_ii X, stored mirrored at block (j, i)
-            float4 y0, y1;
-            blk_mac2(blk(AF, i, i), XS + job * 256, 16, nullptr, nullptr, nullptr, nullptr, 1, r0,
-                     c0, y0, y1);
-            *reinterpret_cast<float4 *>(blk(AF, j, i) + r0 * kLD + c0) =
-                make_float4(-y0.x, -y0.y, -y0.z, -y0.w);
-            *reinterpret_cast<float4 *>(blk(AF, j, i) + (r0 + 8) * kLD + c0) =
-                make_float4(-y1.x, -y1.y, -y1.z, -y1.w);
-        }
-        named_sync(kBarKey, NT);
     }
 }
 
@@ -384,7 +364,8 @@ __device__ __forceinline__ float decay_exp2(float x) {
 // TMEM; the thread holds TMEM lane quad_row, columns [32 colhalf, +32):
 //   A_ts = beta_t 2^(G_t - G_s) (k_t . k_s) for s < t, else 0
 //   P_ts = 2^(G_t - G_s) (q_t . k_s)       for s <= t, else 0
-// Ptile may be shared or global memory (the tile's swizzled image).
+// Ptile may be shared or global memory (the tile's swizzled image), or null
+// when no outputs are wanted.
 __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colhalf,
                                          const float *G2, const float *bet, float *AF,
                                          uint8_t *Ptile) {
@@ -408,7 +389,7 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
             }
             *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) = make_float4(a[0], a[1], a[2], a[3]);
         }
-    } else {
+    } else if (Ptile != nullptr) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
             const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
@@ -419,44 +400,6 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
         }
         store_row<4>(Ptile, t, 4 * colhalf, v);
     }
-}
-
-// T' = T diag(beta gamma) and T'' = T diag(beta) as bf16 operand tiles from
-// the inverse in AF (T_ii in place, T_ij mirrored at block (j, i)); index tid
-// in [0, 256) writes row tid % 64, columns [16 (tid / 64), +16), so a warp reads
-// 32 consecutive rows of AF (conflict-free with the row stride of 68 floats)
-// and one broadcast slice of beta and gamma.  The tiles may be shared or
-// global memory.
-__device__ __forceinline__ void chunk_tprime(float *AF, const float *bet, const float *gam,
-                                             uint8_t *TPtile, uint8_t *TPPtile, int tid) {
-    const int t = tid & 63, cb = tid >> 6;
-    const int bt = t >> 4;
-    float x[16];
-    if (cb > bt) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) x[c] = 0.f;
-    } else {
-        const float *src = (cb == bt) ? AF + t * kLD + 16 * cb : blk(AF, cb, bt) + (t & 15) * kLD;
-#pragma unroll
-        for (int c = 0; c < 16; c += 4) {
-            const float4 y = *reinterpret_cast<const float4 *>(src + c);
-            x[c] = y.x; x[c + 1] = y.y; x[c + 2] = y.z; x[c + 3] = y.w;
-        }
-    }
-    float tp[16], tpp[16];
-#pragma unroll
-    for (int c = 0; c < 16; c += 4) {
-        const float4 b4 = *reinterpret_cast<const float4 *>(bet + 16 * cb + c);
-        const float4 g4 = *reinterpret_cast<const float4 *>(gam + 16 * cb + c);
-        const float bs[4] = {b4.x, b4.y, b4.z, b4.w}, gs[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            tpp[c + e] = x[c + e] * bs[e];
-            tp[c + e] = tpp[c + e] * gs[e];
-        }
-    }
-    store_row<2>(TPtile, t, 2 * cb, tp);
-    store_row<2>(TPPtile, t, 2 * cb, tpp);
 }
 
 // Which token range, initial state and final-state slot a CTA works on.
@@ -528,501 +471,27 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
     return tk;
 }
 
-template <int K>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ alpha,
-                      const float *__restrict__ beta, const float *__restrict__ S0,
-                      __nv_bfloat16 *__restrict__ o, float *__restrict__ ST, int T, int Ts, int H,
-                      int BH, SegPlan plan, int *status) {
-    using L = TcLayout<K>;
-    constexpr int V = 128;
-    constexpr int KH = K / 2;  // state columns per state-group thread
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // the swizzle atoms and operand descriptors need a 1024-byte aligned
-    // base; the declaration provides it and the kernel checks it
-    if (smem_u32(smem_raw) & 1023u) {
-        if (threadIdx.x == 0 && status) atomicOr(status, kStatusBounds);
-        return;
-    }
-    uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full[3], v_full, bar_p1, bar_w, bar_u, bar_s, nw_ready[2], nw_free;
-    __shared__ uint64_t ua_free[2], pt_free[2];
-    __shared__ uint64_t drain[2];  // abort path: the two MMA-issuing threads' products done
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int abort_flag;
-    volatile int *abort_v = &abort_flag;
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    // ---- this CTA's task ----
-    const SegTask tk = segment_task(plan, K, T, S0, ST, BH);
-    const size_t seq = tk.seq;
-    const int t0 = tk.t0, t1 = tk.t1;
-    const float *s0p = tk.s0p;
-    const bool s0_identity = tk.s0_identity, zero_v = tk.zero_v;
-    float *stp = tk.stp;
-    if (!tk.outputs) o = nullptr;
-    const int b = (int)(seq / H), h = (int)(seq % H);
-    const int nchunks = (t1 - t0 + 63) / 64;
-    const uint32_t base = smem_u32(sm);
-
-    if (warp == 0) {
-        tmem_alloc(&tmem_base_sh, 512);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full, &bar_p1, &bar_w,
-                            &bar_u, &bar_s, &nw_ready[0], &nw_ready[1], &nw_free,
-                            &ua_free[0], &ua_free[1], &pt_free[0], &pt_free[1],
-                            &drain[0],   &drain[1]};
-        for (uint64_t *bb : bars) mbar_init(bb, 1);
-        fence_mbar_init();
-        abort_flag = 0;
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tb = tmem_base_sh;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int quad_row = (warp & 3) * 32 + lane;  // TMEM lane of this thread
-    const int colhalf = (warp >> 2) & 1;          // which 32-column half this warp reads
-
-    auto load_kq = [&](int n) {
-        const int st = n % L::NSTAGE;
-        uint8_t *stg = sm + st * L::STAGE;
-        mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
-        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
-        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
-        if (K == 128) {
-            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
-            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
-        }
-    };
-    auto load_v = [&](int n) {
-        mbar_arrive_expect_tx(&v_full, L::V_BYTES);
-        tma_load_4d(sm + L::VB, &tm_v, &v_full, 0, h, t0 + n * 64, b);
-        tma_load_4d(sm + L::VB + 8192, &tm_v, &v_full, 64, h, t0 + n * 64, b);
-    };
-    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-        const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
-        if (!ok) *abort_v = 1;
-        return ok;
-    };
-
-    constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);  // K-major x K-major
-    constexpr uint32_t I_AMN = idesc_bf16(128, 64, true, false);  // MN-major A
-    constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);  // MN-major B, N = 64
-    constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);    // MN-major B, N = K
-    constexpr uint32_t I_MM128 = idesc_bf16(128, 128, false, false);  // K-major, N = 128
-
-    bool failed = false;
-
-    if (tid < kKeyThreads) {
-        // ================================================================ key group
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
-        float *AF = reinterpret_cast<float *>(sm + L::AF);
-        float *XS = reinterpret_cast<float *>(sm + L::XS);
-        float *G2 = reinterpret_cast<float *>(sm + L::KGATE);
-        float *gam = G2 + 64;
-        float *bet = G2 + 128;
-        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
-        auto prefetch_gates = [&](int n) {
-            if (warp == 1 && n < nchunks) {
-                const int nv = min(64, t1 - t0 - n * 64);
-                const size_t i0 = ((size_t)b * Ts + t0 + n * 64 + lane) * H + h;
-                const size_t i1 = i0 + (size_t)32 * H;
-                pa0 = lane < nv ? alpha[i0] : 1.f;
-                pb0 = lane < nv ? beta[i0] : 0.f;
-                pa1 = lane + 32 < nv ? alpha[i1] : 1.f;
-                pb1 = lane + 32 < nv ? beta[i1] : 0.f;
-            }
-        };
-        prefetch_gates(0);
-        if (tid == 0) {
-            for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
-            if (!zero_v) load_v(0);
-        }
-        for (int n = 0; n < nchunks; ++n) {
-            const int st = n % L::NSTAGE;  // q/k stage
-            const int p2 = n & 1;          // P and U~ buffers
-            const uint32_t stg = base + st * L::STAGE;
-            const int nvalid = min(64, t1 - t0 - n * 64);
-            bool ok = true;
-            // ---- [K;Q] K^T ----
-            if (tid == 0) {
-                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
-                if (ok) {
-                    tc_fence_after();
-                    issue_kq_kt<K>(tb + L::D1, stg, L::KC0, L::KC1);
-                    mma_commit(&bar_p1);
-                }
-                if (ok && n >= 2) ok = wait(&pt_free[p2], ((n - 2) >> 1) & 1);
-                // T' / T'' share their buffer with the previous chunk's -W^T
-                if (ok && n >= 1) ok = wait(&nw_free, (n - 1) & 1);
-                if (ok) ok = wait(&bar_p1, n & 1);
-            }
-            // ---- gates of chunk n (warp 1), then prefetch chunk n + 1 ----
-            if (warp == 1) {
-                chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
-                prefetch_gates(n + 1);
-            }
-            // one thread waited for [K;Q] K^T (and for the P buffer); the barrier
-            // hands both, and the gates, to the whole group
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-
-            // ---- A (fp32, solve input) and P (bf16 operand) ----
-            tc_fence_after();
-            chunk_ap(tb + lane_off + L::D1 + 32 * colhalf, quad_row, colhalf, G2, bet, AF,
-                     sm + L::PT + p2 * 8192);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-            // ---- T = (I + A)^{-1}; T' = T diag(beta gamma), T'' = T diag(beta) ----
-            unit_lower_inverse<false>(AF, XS, tid);
-            chunk_tprime(AF, bet, gam, sm + L::TP, sm + L::TPP, tid);
-            fence_proxy_async_smem();
-            named_sync(kBarKey, kKeyThreads);
-
-            // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
-            if (tid == 0) {
-                ok = true;
-                if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
-                if (!zero_v) ok = ok && wait(&v_full, n & 1);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t lbo_k = K == 128 ? 16384u : (uint32_t)(L::VB - st * L::STAGE);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, lbo_k, 1024),
-                                 sdesc(base + L::TP + ks * 32, 16, 1024), I_AMN, ks > 0);
-                        if (!zero_v)
-                            mma_bf16(tb + L::UA + 64 * p2,
-                                     sdesc(base + L::VB + ks * 2048, 8192, 1024),
-                                     sdesc(base + L::TPP + ks * 32, 16, 1024), I_AMN, ks > 0);
-                    }
-                    mma_commit(&bar_w);
-                }
-            }
-            {
-                // Q <- diag(gamma) Q in place while the W / U~ products run (they
-                // read the K tile and T', T''; this chunk's [K;Q] K^T has finished;
-                // the q tile is read again only by S Q^T)
-                uint8_t *stq = sm + st * L::STAGE;
-#pragma unroll
-                for (int e = tid; e < (K / 64) * 512; e += kKeyThreads) {
-                    const int blk_i = e >> 9, ee = e & 511;
-                    uint4 *p = reinterpret_cast<uint4 *>(stq + (blk_i ? L::QC1 : L::QC0) + ee * 16);
-                    const float g = gam[ee >> 3];
-                    uint4 w = *p;
-                    uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float2 f = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162 *>(&wv[c]));
-                        wv[c] = pack_bf16(f.x * g, f.y * g);
-                    }
-                    *p = w;
-                }
-            }
-            if (tid == 0) {
-                if (ok) ok = wait(&bar_w, n & 1);
-                if (ok && !zero_v && n + 1 < nchunks) load_v(n + 1);  // V consumed
-            }
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-            {
-                // -W^T over T', T'' (consumed by the products above)
-                tc_fence_after();
-                if (quad_row < K) {
-                    float v[32];
-                    tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
-                    tmem_ld_wait();
-                    store_row<4>(sm + L::NW, quad_row, 4 * colhalf, v, -1.f);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-            // one barrier per chunk parity: in the two-pass form the key group
-            // may finish chunk n + 1 before the state group has waited for
-            // chunk n (nothing else holds it back), and two completed phases of
-            // one barrier would be indistinguishable from none; chunk n + 2
-            // needs operands loaded only after the state group passed chunk n
-            if (tid == 0) mbar_arrive(&nw_ready[n & 1]);
-        }
-    } else {
-        // ================================================================ state group
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
-        const int sid = tid - kKeyThreads;  // 0..255
-        const int sw = sid >> 5;            // state warp 0..7
-        const int c = quad_row;             // state row = TMEM lane
-        const int hf = sw >> 2;             // column half
-        float *sg = reinterpret_cast<float *>(sm + L::SGATE);  // 3 slots of 68 floats
-        // state-group gates (warp 8 only): decay[64] and gamma_C of chunk m into
-        // slot m % 3, from alpha values loaded one call earlier
-        float sa0 = 1.f, sa1 = 1.f;
-        auto sg_load = [&](int m) {
-            if (m < nchunks) {
-                const int nv = min(64, t1 - t0 - m * 64);
-                const size_t i0 = ((size_t)b * Ts + t0 + m * 64 + lane) * H + h;
-                sa0 = lane < nv ? alpha[i0] : 1.f;
-                sa1 = lane + 32 < nv ? alpha[i0 + (size_t)32 * H] : 1.f;
-            }
-        };
-        auto sg_compute = [&](int m) {
-            if (m >= nchunks) return;
-            const int nv = min(64, t1 - t0 - m * 64);
-            float g0, g1;
-            chunk_log2_prefix(sa0, sa1, lane, nv, g0, g1);
-            const float gC = __shfl_sync(0xffffffffu, g1, 31);
-            float *slot = sg + (m % 3) * 68;
-            slot[lane] = exp2f(gC - g0);
-            slot[lane + 32] = exp2f(gC - g1);
-            if (lane == 0) slot[64] = exp2f(gC);
-        };
-        if (sw == 0) {
-            for (int m = 0; m < 3; ++m) {
-                sg_load(m);
-                sg_compute(m);
-            }
-            sg_load(3);
-        }
-        // initial state: fp32 registers + bf16 operand copy
-        float S[KH];
-        {
-            const int j0 = hf * KH;
-#pragma unroll
-            for (int j = 0; j < KH; j += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (s0p) x = *reinterpret_cast<const float4 *>(s0p + (size_t)c * K + j0 + j);
-                if (s0_identity) {
-                    x.x = (c == j0 + j) ? 1.f : 0.f;
-                    x.y = (c == j0 + j + 1) ? 1.f : 0.f;
-                    x.z = (c == j0 + j + 2) ? 1.f : 0.f;
-                    x.w = (c == j0 + j + 3) ? 1.f : 0.f;
-                }
-                S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-            }
-#pragma unroll
-            for (int p = 0; p < KH / 32; ++p) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
-                const int j = j0 + 32 * p;
-                store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_sync(kBarState, kStateThreads);
-
-        // U^T += S (-W^T) for chunk m (after the key group handed over -W^T)
-        auto issue_u = [&](int m) -> bool {
-            if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                // with v = 0 there is no U~ product: this one starts the accumulator
-                mma_bf16(tb + L::UA + 64 * (m & 1),
-                         sdesc(base + L::SB + kb * 16384 + ko, 16, 1024),
-                         sdesc(base + L::NW + ks * 2048, 8192, 1024), I_BMN,
-                         zero_v ? (uint32_t)(ks > 0) : 1u);
-            }
-            mma_commit(&nw_free);
-            return true;
-        };
-        // O = [K; gamma Q] S^T for chunk m (token-major; TMEM lanes 64..127 hold
-        // gamma Q S^T), then bar_u tracks both products of the chunk
-        auto issue_o = [&](int m) {
-            tc_fence_after();
-            const uint32_t stg = base + (m % L::NSTAGE) * L::STAGE;
-#pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks) {
-                const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
-                mma_bf16(tb + L::O, sdesc(stg + (kb ? L::KC1 : L::KC0) + ko, 16, 1024),
-                         sdesc(base + L::SB + kb * 16384 + ko, 16, 1024), I_MM128, ks > 0);
-            }
-            mma_commit(&bar_u);
-        };
-        if (sw == 0) {
-            bool ok0 = true;
-            if (lane == 0) {
-                ok0 = issue_u(0);
-                if (ok0) issue_o(0);
-            }
-            ok0 = __shfl_sync(0xffffffffu, ok0, 0);
-            failed = !ok0;
-        }
-
-        for (int n = 0; n < nchunks; ++n) {
-            const int st = n % L::NSTAGE;
-            const int p2 = n & 1;
-            const uint32_t stg = base + st * L::STAGE;
-            const int nvalid = min(64, t1 - t0 - n * 64);
-            const float *slot = sg + (n % 3) * 68;
-            // ---- U epilogue: U^T -> UT halves, U^T diag(decay) -> UD ----
-            bool ok = !failed;
-            if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
-            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
-            {
-                tc_fence_after();
-                float v[32];
-                tmem_ld32(tb + lane_off + L::UA + 64 * p2 + 32 * hf, v);
-                tmem_ld_wait();
-                store_row<4>(sm + L::ut_half(st, c >> 6), c & 63, 4 * hf, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= slot[32 * hf + i];
-                store_row<4>(sm + L::UD, c, 4 * hf, v);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(kBarState, kStateThreads);
-            // ---- O += [any; P] U (token-major) and dS = U^T diag(decay) K ----
-            if (sid == 0) {
-                mbar_arrive(&ua_free[p2]);
-                tc_fence_after();
-                const uint32_t pa = base + L::PT + p2 * 8192 - 8192;  // rows 64..127 = P
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tb + L::O + 64 * hh, sdesc(pa + ks * 32, 16, 1024),
-                                 sdesc(base + L::ut_half(st, hh) + ks * 32, 16, 1024), I_MM, 1);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + L::DS, sdesc(base + L::UD + ks * 32, 16, 1024),
-                             sdesc(stg + L::KC0 + ks * 2048, 16384, 1024), I_DS, ks > 0);
-                mma_commit(&bar_s);
-                mma_commit(&pt_free[p2]);
-                ok = wait(&bar_s, n & 1);
-                if (ok && n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);  // stage consumed
-            }
-            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
-            // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
-            {
-                tc_fence_after();
-                const float gC = slot[64];
-                const int j0 = hf * KH;
-#pragma unroll
-                for (int p = 0; p < KH / 32; ++p) {
-                    float v[32];
-                    tmem_ld32(tb + lane_off + L::DS + j0 + 32 * p, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        S[32 * p + i] = fmaf(gC, S[32 * p + i], v[i]);
-                        v[i] = S[32 * p + i];
-                    }
-                    const int j = j0 + 32 * p;
-                    store_row<4>(sm + L::SB + (j / 64) * 16384, c, (j % 64) / 8, v);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(kBarState, kStateThreads);
-            // ---- next chunk's U product (warp 8) while this chunk's output is stored ----
-            if (sw == 0) {
-                bool ok1 = true;
-                if (lane == 0 && n + 1 < nchunks) ok1 = issue_u(n + 1);
-                ok1 = __shfl_sync(0xffffffffu, ok1, 0);
-                if (!ok1) failed = true;
-                // slot (n + 3) % 3 == n % 3: every reader of this chunk's gates has
-                // passed the barrier above
-                sg_compute(n + 3);
-                sg_load(n + 4);
-            }
-            if ((warp & 3) >= 2) {
-                // token t = TMEM lane - 64; channels [64 hf, 64 hf + 64): two 128 B rows
-                const int t = c - 64;
-                float v0[32], v1[32];
-                tmem_ld32(tb + lane_off + L::O + 64 * hf, v0);
-                tmem_ld32(tb + lane_off + L::O + 64 * hf + 32, v1);
-                tmem_ld_wait();
-                if (o != nullptr && t < nvalid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        o + (((size_t)b * Ts + t0 + n * 64 + t) * H + h) * V + 64 * hf);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(pack_bf16(v0[8 * k], v0[8 * k + 1]),
-                                            pack_bf16(v0[8 * k + 2], v0[8 * k + 3]),
-                                            pack_bf16(v0[8 * k + 4], v0[8 * k + 5]),
-                                            pack_bf16(v0[8 * k + 6], v0[8 * k + 7]));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[4 + k] = make_uint4(pack_bf16(v1[8 * k], v1[8 * k + 1]),
-                                                pack_bf16(v1[8 * k + 2], v1[8 * k + 3]),
-                                                pack_bf16(v1[8 * k + 4], v1[8 * k + 5]),
-                                                pack_bf16(v1[8 * k + 6], v1[8 * k + 7]));
-                }
-            }
-            tc_fence_before();
-            if (named_sync_or(kBarState, kStateThreads, failed)) { failed = true; break; }
-            // O is free again: the next chunk's S Q^T
-            if (sid == 0 && n + 1 < nchunks) issue_o(n + 1);
-        }
-        if (!failed && stp != nullptr) {
-            const int j0 = hf * KH;
-#pragma unroll
-            for (int j = 0; j < KH; j += 4)
-                *reinterpret_cast<float4 *>(stp + (size_t)c * K + j0 + j) =
-                    make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        }
-    }
-
-    if (failed) *abort_v = 1;
-    tc_fence_before();
-    __syncthreads();
-    if (*abort_v) {
-        // products still in flight read shared memory and write TMEM: each
-        // issuing thread's commit completes once all of its products have
-        if (tid == 0 || tid == kKeyThreads) {
-            uint64_t *d = &drain[tid == 0 ? 0 : 1];
-            mma_commit(d);
-            mbar_wait(d, 0, kSpinLimit / 16);
-        }
-        if (tid == 0) {
-            if (status) atomicOr(status, kStatusTimeout);
-            // let in-flight loads land before the CTA's shared memory is released
-            for (int s = 0; s < 3; ++s) {
-                mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
-            }
-            mbar_wait(&v_full, 0, kSpinLimit / 16);
-            mbar_wait(&v_full, 1, kSpinLimit / 16);
-        }
-        __syncthreads();
-    }
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tb, 512);
-    }
-}
-
 // ---------------------------------------------------------------- key-side pass
 // The two-pass form's first kernel.  Everything of a chunk that depends only
-// on its keys, queries and gates -- A, P, the inverse T and T', T'' -- has no
+// on its keys, queries and gates -- A, P, the inverse T, T'' and W -- has no
 // dependence on the state, so it runs for all B * H * ceil(T/64) chunks at
 // once instead of in each sequence's serial chunk loop.  Persistent CTAs of
-// 128 threads (four per SM: the inverse keeps only some warps of a CTA busy
-// between its barriers, so more, smaller CTAs fill the SM better) stride over
-// the chunks; each chunk's [K;Q] K^T
-// is one tcgen05 product into 64 TMEM columns, the next chunk's q/k boxes load
-// (TMA) while the current one is solved, and T', T'', P go to global memory as
-// their swizzled shared-memory images, which the state-side kernel copies in
-// with one bulk copy per chunk.  Same arithmetic as the fused kernel's key
-// group (the shared helpers above), so both forms give identical results.
+// 128 threads (four per SM, so that one CTA's loads and waits hide under the
+// others' work) stride over the chunks; per chunk: [K;Q] K^T on the tensor
+// cores, A and P, the inverse with T'^T into the spent Q box, W^T = K^T T'^T
+// on the tensor cores (into the same 64 TMEM columns), then -W^T, T''^T and P
+// go to global memory as their swizzled shared-memory images, which the
+// state-side kernel copies in with bulk copies.  The next chunk's q/k boxes
+// load once both products have read the stage.  Same arithmetic as the fused
+// kernel's key group (the shared helpers above, the same product
+// instructions), so both forms give identical results.
 template <int K>
 struct PrepLayout {
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;  // one q/k stage
+    static constexpr uint32_t KLBO = K == 128 ? 16384 : 8192;    // next 64-channel block of K
     static constexpr uint32_t AF = STAGE;                        // float [64][68]
-    static constexpr uint32_t XS = AF + 64 * kLD * 4;            // float [3][16][16]
-    static constexpr uint32_t GATE = XS + 3 * 256 * 4;           // G2, gamma, beta
+    static constexpr uint32_t GATE = AF + 64 * kLD * 4;          // G2, gamma, beta
     static constexpr uint32_t END = GATE + 3 * 64 * 4;
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr size_t SMEM = END;
@@ -1047,7 +516,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full, bar_p1, drain;
+    __shared__ uint64_t kq_full, bar_p1, bar_w, drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -1064,6 +533,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         tma_prefetch_desc(&tm_k);
         mbar_init(&kq_full, 1);
         mbar_init(&bar_p1, 1);
+        mbar_init(&bar_w, 1);
         mbar_init(&drain, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -1075,7 +545,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int quad_row = (warp & 3) * 32 + lane;
     float *AF = reinterpret_cast<float *>(sm + L::AF);
-    float *XS = reinterpret_cast<float *>(sm + L::XS);
     float *G2 = reinterpret_cast<float *>(sm + L::GATE);
     float *gam = G2 + 64;
     float *bet = G2 + 128;
@@ -1122,6 +591,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         return true;
     };
 
+    constexpr uint32_t I_ABMN = idesc_bf16(128, 64, true, true);  // MN-major A and B
     const long long G = gridDim.x;
     long long j = blockIdx.x;
     if (tid == 0 && j < nchunk_all) load_kq(j);
@@ -1138,8 +608,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
                 issue_kq_kt<K>(tb, smem_u32(sm), L::KC0, L::KC1);
                 mma_commit(&bar_p1);
                 ok = wait(&bar_p1, it & 1);
-                // the product has read the stage: the next chunk's boxes may land
-                if (ok && j + G < nchunk_all) load_kq(j + G);
             }
         }
         if (warp == 1) {
@@ -1147,16 +615,45 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
             prefetch_gates(j + G);
         }
         if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
-        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T' | T'' | P]
+        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [-W^T | T''^T | P]
         tc_fence_after();
         for (int ch = 0; ch < 2; ++ch)  // both 32-column halves per thread
-            chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, out + 16384);
+            chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, out + kPrepP);
         tc_fence_before();
         named_sync(kBarKey, kPrepThreads);
-        unit_lower_inverse<true, kPrepThreads>(AF, XS, tid);
-        chunk_tprime(AF, bet, gam, out, out + 8192, tid);  // column blocks 0, 1
-        chunk_tprime(AF, bet, gam, out, out + 8192, tid + kPrepThreads);  // 2, 3
-        named_sync(kBarKey, kPrepThreads);  // AF and the gates are rewritten next
+        // T'^T into the spent Q box of channel block 0 (the W^T product's
+        // operand), T''^T straight to global memory
+        chunk_inverse_tprime<kPrepThreads>(AF, bet, gam, sm + L::QC0, out + kPrepTPP, tid);
+        fence_proxy_async_smem();
+        named_sync(kBarKey, kPrepThreads);
+        // ---- W^T = K^T T'^T (the same instruction as in the one-pass kernel) ----
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tb, sdesc(smem_u32(sm) + L::KC0 + ks * 2048, L::KLBO, 1024),
+                         sdesc(smem_u32(sm) + L::QC0 + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+            mma_commit(&bar_w);
+            ok = wait(&bar_w, it & 1);
+            // both products have read the stage: the next chunk's boxes may land
+            if (ok && j + G < nchunk_all) load_kq(j + G);
+        }
+        if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
+        {
+            // -W^T as the right operand image of U^T += S (-W^T)
+            tc_fence_after();
+            if (quad_row < K) {
+#pragma unroll 1
+                for (int ch = 0; ch < 2; ++ch) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + 32 * ch, v);
+                    tmem_ld_wait();
+                    store_row<4>(out + kPrepNW, quad_row, 4 * ch, v, -1.f);
+                }
+            }
+        }
+        tc_fence_before();
+        named_sync(kBarKey, kPrepThreads);  // TMEM, AF and the gates are rewritten next
     }
 
     if (failed) *abort_v = 1;
@@ -1182,47 +679,46 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 
 // ---------------------------------------------------------------- state-side pass
 // The two-pass form's second kernel: one CTA per (b, h) sequence (or segment)
-// walks its chunks like the fused kernel, but loads T', T'', P instead of
-// solving for them.  Its key group forms W^T and U~^T, writes -W^T, scales Q
-// by gamma and hands the state group the chunk's decay factors; it depends on
-// no state and runs ahead.  The state group keeps only the state dependency
-// chain serial:
-//
-//   U^T(n) = U~^T(n) + S(n-1) (-W^T(n))      \  warp 8, issued back to back
-//   O^T(n) = S(n-1) (gamma Q(n))^T           /  at the end of chunk n - 1
-//   epilogue: U^T -> bf16, U^T diag(decay) -> bf16
-//   dS(n)  = U^T diag(decay) K(n)            \  warp 8, issued back to back
-//   O^T(n) += U^T P(n)^T                     /
-//   S(n)   = gamma_C S(n-1) + dS(n)
-//
-// The chain's A operands live in TMEM: the bf16 copy of the state, and the
-// bf16 U^T and U^T diag(decay) written into the spent halves of the U
-// accumulator, so the chain's products read only their B operands from
-// shared memory and the epilogues write no shared memory.  One thread issues
-// every state-side product in chain order; the tensor pipe runs them in issue
-// order and each commit covers all earlier products of the thread, which is
-// what frees the operands (O^T's first product has read S(n-1) once dS(n) is
-// complete, and the U slot is free once O^T(n) is).  O is computed transposed
-// (value channels on the TMEM lanes, 64 token columns), so two O accumulators
-// fit in TMEM and a chunk's output never holds up the next chunk's products.
-// Warps 12-15 stage each chunk's output in a dedicated tile and warp 11 stores
-// it with TMA (a ragged tail is clipped by the tensor map).  Rings: q/k (three
-// stages, chunk n + 3 loaded once dS(n) is complete), V (three), T', T'' and P
-// (two each: T', T'' of chunk n + 2 as soon as U(n) has read -W^T, P of chunk
-// n + 2 once O^T(n) is complete).  Every state quantity is the fused kernel's
-// arithmetic on the same operands, so S_T is bit-identical to it (o agrees to
-// the accumulation order of the transposed product).
+// walks its chunks like the fused kernel, but loads -W^T, T''^T and P
+// instead of solving for them.  Three roles:
+//   key group (warps 0-6): per chunk the gates, the state group's decay
+//       factors and gamma folded into the Q box (no products, no loads).
+//   issuer (warp 7, one thread): every TMA load, and the products that are
+//       not on the state chain -- O^T(n) = S(n-1) (gamma Q(n))^T and
+//       U~^T(n+1) = V^T T''^T -- issued in chunk n's epilogue window, while
+//       the tensor pipe would otherwise idle (one SM issues tcgen05 products
+//       one at a time, ~44 cycles each, so products issued beside the chain's
+//       would delay them).
+//   state group (warps 8-15): the state chain
+//       U^T(n)  = U~^T(n) + S(n-1) (-W^T(n))       (issued at the end of n - 1)
+//       epilogue: U^T -> bf16, U^T diag(decay) -> bf16, in the U slot
+//       dS(n)   = U^T diag(decay) K(n),  O^T(n) += U^T P(n)^T
+//       S(n)    = gamma_C S(n-1) + dS(n)
+//     and the transposed output, staged by warps 12-15 for TMA stores by
+//     warp 11 (a ragged tail is clipped by the tensor map).
+// The chain's A operands live in TMEM (the bf16 state, and bf16 U^T and
+// U^T diag(decay) written back into the spent U accumulator), so its products
+// read only their B operands from shared memory.  Ordering: a commit covers
+// every earlier product of its thread, so bar_u(n) (the state thread's
+// commit after U(n)) also says that dS(n-1) and O^T(n-1) += U^T P^T are
+// complete: the issuer reloads and reuses slots only after it.  The state
+// update waits for the issuer's O^T(n) S-term (bar_os), which reads S(n-1).
+// Rings: q/k (three stages), V, [-W^T | T''^T], P and U (two each), O (two);
+// the loads of chunk n + 2 (P: n + 1) go out in chunk n's window.  Every state
+// quantity is the fused kernel's arithmetic on the same operands, so S_T is
+// bit-identical to it (o agrees to the accumulation order of the transposed
+// product).
 
 template <int K>
 struct StLayout {
     static constexpr int NSTAGE = 3;                             // q/k ring
-    static constexpr int NV = 3;                                 // V ring
+    static constexpr int NV = 2;                                 // V ring
     static constexpr uint32_t KC0 = 0, KC1 = 8192;               // K blocks (KC1: K = 128)
     static constexpr uint32_t QC0 = K == 128 ? 16384 : 8192, QC1 = QC0 + 8192;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
     static constexpr uint32_t VB = NSTAGE * STAGE;               // V ring, 16 KB per chunk
-    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [T' | T'']
-    static constexpr uint32_t PP = PR + 2 * 16384;               // ring of P
+    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [-W^T | T''^T]
+    static constexpr uint32_t PP = PR + 2 * 24576;               // ring of P
     static constexpr uint32_t OST = PP + 2 * 8192;               // output staging, 2 x 64 x 64
     static constexpr uint32_t KGATE = OST + 16384;               // G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;        // 3 x (decay[64], gamma_C)
@@ -1231,14 +727,13 @@ struct StLayout {
     static constexpr uint32_t V_BYTES = 2u * 8192u;
     static constexpr size_t SMEM = END;
     static_assert(SMEM + 1024 <= 232448, "shared memory budget");
-    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * 16384; }
-    static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
-    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // -W^T over T', T''
+    static __device__ __forceinline__ uint32_t nw(int n) { return PR + (n & 1) * 24576; }
+    static __device__ __forceinline__ uint32_t tpp(int n) { return nw(n) + 16384; }
     static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
     static __device__ __forceinline__ uint32_t vbuf(int n) { return VB + (n % NV) * 16384; }
-    // TMEM columns: O^T of even / odd chunks, W^T, U~^T / U^T of even / odd
+    // TMEM columns: O^T of even / odd chunks, U~^T / U^T of even / odd
     // chunks, the bf16 state (two K elements per column), dS
-    static constexpr uint32_t O0 = 0, WT = 64, UA = 128, O1 = 256, SBT = 320, DS = 384;
+    static constexpr uint32_t O0 = 0, O1 = 64, UA = 128, SBT = 256, DS = 384;
     static __device__ __forceinline__ uint32_t ocol(int n) { return (n & 1) ? O1 : O0; }
     static __device__ __forceinline__ uint32_t ua(int n) { return UA + 64 * (n & 1); }
     // After chunk n's epilogue, token half h of its U slot (32 columns) holds
@@ -1251,6 +746,8 @@ struct StLayout {
 };
 
 constexpr int kBarOut = 3, kBarOut2 = 4;  // the output warps (11-15)
+constexpr int kStKeyThreads = 224;        // warps 0-6
+constexpr int kStIssuer = 224;            // warp 7, lane 0
 
 template <int K>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -1269,8 +766,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full[3], v_full[3], tt_full[2], p_full[2], bar_w, bar_u, bar_s, bar_o2,
-        nw_ready[2], ua_free[2], drain[2];
+    __shared__ uint64_t kq_full[3], v_full[2], tt_full[2], p_full[2], key_ready[2], bar_w, bar_u,
+        bar_s, bar_os, bar_o2, drain[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -1285,7 +782,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int b = (int)(seq / H), h = (int)(seq % H);
     const int nchunks = (t1 - t0 + 63) / 64;
     const uint32_t base = smem_u32(sm);
-    // T', T'', P of chunk n of this CTA's token range
+    // -W^T, T''^T, P of chunk n of this CTA's token range
     const uint8_t *prep_seq = prep + (seq * (size_t)((T + 63) / 64) + t0 / 64) * kPrepChunkBytes;
 
     if (warp == 0) {
@@ -1293,14 +790,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        if (outs) tma_prefetch_desc(&tm_o);
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1],  &kq_full[2], &v_full[0],  &v_full[1],
-                            &v_full[2],  &tt_full[0],  &tt_full[1], &p_full[0],  &p_full[1],
-                            &bar_w,      &bar_u,       &bar_s,      &bar_o2,     &nw_ready[0],
-                            &nw_ready[1], &ua_free[0], &ua_free[1], &drain[0],   &drain[1]};
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0],    &v_full[1],
+                            &tt_full[0], &tt_full[1], &p_full[0],  &p_full[1],    &key_ready[0],
+                            &key_ready[1], &bar_w,    &bar_u,      &bar_s,        &bar_os,
+                            &bar_o2,     &drain[0],   &drain[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -1311,39 +804,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tb = tmem_base_sh;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int quad_row = (warp & 3) * 32 + lane;  // TMEM lane of this thread
-    const int colhalf = (warp >> 2) & 1;          // which 32-column half this warp reads
     // decay[64] and gamma_C of chunk n in slot n % 3 (written by the key group)
     float *sg = reinterpret_cast<float *>(sm + L::SGATE);
 
-    auto load_kq = [&](int n) {
-        const int st = n % L::NSTAGE;
-        uint8_t *stg = sm + st * L::STAGE;
-        mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
-        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
-        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
-        if (K == 128) {
-            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
-            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
-        }
-    };
-    auto load_v = [&](int n) {
-        uint64_t *bar = &v_full[n % L::NV];
-        uint8_t *dst = sm + L::vbuf(n);
-        mbar_arrive_expect_tx(bar, L::V_BYTES);
-        tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
-        tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
-    };
-    // T', T'' of chunk n into ring stage n % 2 (key group), P into its own ring
-    // (state group's O^T); one chunk's block in global memory is [T' | T'' | P]
-    auto load_tt = [&](int n) {
-        mbar_arrive_expect_tx(&tt_full[n & 1], 16384);
-        bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes, 16384, &tt_full[n & 1]);
-    };
-    auto load_p = [&](int n) {
-        mbar_arrive_expect_tx(&p_full[n & 1], 8192);
-        bulk_load(sm + L::ptile(n), prep_seq + (size_t)n * kPrepChunkBytes + 16384, 8192,
-                  &p_full[n & 1]);
-    };
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
         if (!ok) *abort_v = 1;
@@ -1351,97 +814,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
 
     constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);  // K-major x K-major, N = 64
-    constexpr uint32_t I_AMN = idesc_bf16(128, 64, true, false);  // MN-major A
+    constexpr uint32_t I_ABMN = idesc_bf16(128, 64, true, true);  // MN-major A and B
     constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);  // MN-major B, N = 64
     constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);    // MN-major B, N = K
 
     bool failed = false;
 
-    if (tid < kKeyThreads) {
+    if (tid < kStKeyThreads) {
         // ================================================================ key group
         asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
         float *G2 = reinterpret_cast<float *>(sm + L::KGATE);
         float *gam = G2 + 64;
         float *bet = G2 + 128;
-        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
-        auto prefetch_gates = [&](int n) {
+        // gate inputs of chunks n and n + 1 in warp 1's registers: each
+        // chunk's alpha / beta are loaded two iterations before they are
+        // used, so the load latency stays off the key group's loop
+        float pa[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, pb[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        auto prefetch_gates = [&](int n, int slot) {
             if (warp == 1 && n < nchunks) {
                 const int nv = min(64, t1 - t0 - n * 64);
                 const size_t i0 = ((size_t)b * Ts + t0 + n * 64 + lane) * H + h;
                 const size_t i1 = i0 + (size_t)32 * H;
-                pa0 = lane < nv ? alpha[i0] : 1.f;
-                pb0 = lane < nv ? beta[i0] : 0.f;
-                pa1 = lane + 32 < nv ? alpha[i1] : 1.f;
-                pb1 = lane + 32 < nv ? beta[i1] : 0.f;
+                pa[slot][0] = lane < nv ? alpha[i0] : 1.f;
+                pb[slot][0] = lane < nv ? beta[i0] : 0.f;
+                pa[slot][1] = lane + 32 < nv ? alpha[i1] : 1.f;
+                pb[slot][1] = lane + 32 < nv ? beta[i1] : 0.f;
             }
         };
-        prefetch_gates(0);
-        if (tid == 0) {
-            for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
-            if (!zero_v)
-                for (int m = 0; m < L::NV && m < nchunks; ++m) load_v(m);
-            for (int m = 0; m < 2 && m < nchunks; ++m) {
-                load_tt(m);
-                if (outs) load_p(m);
-            }
-        }
+        prefetch_gates(0, 0);
+        prefetch_gates(1, 1);
         for (int n = 0; n < nchunks; ++n) {
             const int st = n % L::NSTAGE;  // q/k stage
-            const int p2 = n & 1;          // operand ring stage, U~ accumulator
-            const uint32_t stg = base + st * L::STAGE;
+            const int p2 = n & 1;
             const int nvalid = min(64, t1 - t0 - n * 64);
             bool ok = true;
-            if (tid == 0) {
-                // warm L2 for the key-side block of chunk n + 2 and the V boxes
-                // of chunk n + 4 (copied in only when a ring slot frees)
-                if (n + 2 < nchunks)
-                    bulk_prefetch_l2(prep_seq + (size_t)(n + 2) * kPrepChunkBytes,
-                                     kPrepChunkBytes);
-                if (!zero_v && n + L::NV + 1 < nchunks) {
-                    tma_prefetch_l2_4d(&tm_v, 0, h, t0 + (n + L::NV + 1) * 64, b);
-                    tma_prefetch_l2_4d(&tm_v, 64, h, t0 + (n + L::NV + 1) * 64, b);
-                }
-                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
-                if (ok) ok = wait(&tt_full[p2], (n >> 1) & 1);
-            }
+            if (tid == 0) ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+            if (named_sync_or(kBarKey, kStKeyThreads, !ok)) { failed = true; break; }
             if (warp == 1) {
-                chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
+                if (p2 == 0)
+                    chunk_gates(pa[0][0], pa[0][1], pb[0][0], pb[0][1], lane, nvalid, G2, gam, bet);
+                else
+                    chunk_gates(pa[1][0], pa[1][1], pb[1][0], pb[1][1], lane, nvalid, G2, gam, bet);
                 __syncwarp();
                 // the state group's decay to the chunk end and gamma_C; slot
-                // n % 3 was last read in the state group's epilogue of chunk
-                // n - 3, before the barrier after which this chunk's q/k boxes
-                // are loaded
+                // n % 3 was last read in the state epilogue of chunk n - 3,
+                // which precedes the load of this chunk's q/k boxes
                 float *slot = sg + (n % 3) * 68;
                 const float gC = G2[63];
                 slot[lane] = exp2f(gC - G2[lane]);
                 slot[lane + 32] = exp2f(gC - G2[lane + 32]);
                 if (lane == 0) slot[64] = exp2f(gC);
             }
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-
-            // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
-            if (tid == 0) {
-                if (n >= 2) ok = wait(&ua_free[p2], ((n - 2) >> 1) & 1);
-                if (!zero_v) ok = ok && wait(&v_full[n % L::NV], (n / L::NV) & 1);
-                if (ok) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, 8192, 1024),
-                                 sdesc(base + L::tp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
-                        if (!zero_v)
-                            mma_bf16(tb + L::UA + 64 * p2,
-                                     sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
-                                     sdesc(base + L::tpp(n) + ks * 32, 16, 1024), I_AMN, ks > 0);
-                    }
-                    mma_commit(&bar_w);
-                }
-            }
+            named_sync(kBarKey, kStKeyThreads);
+            // Q <- diag(gamma) Q in place (next read by the O^T S-term)
             uint8_t *stq = sm + st * L::STAGE;
-            // Q <- diag(gamma) Q in place while the products run (they read the
-            // K blocks, V and T', T''; Q is next read by O^T)
-#pragma unroll
-            for (int e = tid; e < (K / 64) * 512; e += kKeyThreads) {
+            for (int e = tid; e < (K / 64) * 512; e += kStKeyThreads) {
                 const int blk_i = e >> 9, ee = e & 511;
                 uint4 *p = reinterpret_cast<uint4 *>(stq + (blk_i ? L::QC1 : L::QC0) + ee * 16);
                 const float g = gam[ee >> 3];
@@ -1455,30 +882,106 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 *p = w;
             }
-            if (tid == 0 && ok) ok = wait(&bar_w, n & 1);
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-            {
-                // -W^T over T', T'' (consumed by the products above)
-                tc_fence_after();
-                if (quad_row < K) {
-                    float v[32];
-                    tmem_ld32(tb + lane_off + L::WT + 32 * colhalf, v);
-                    tmem_ld_wait();
-                    store_row<4>(sm + L::nw(n), quad_row, 4 * colhalf, v, -1.f);
-                }
-            }
             fence_proxy_async_smem();
-            tc_fence_before();
-            if (named_sync_or(kBarKey, kKeyThreads, !ok)) { failed = true; break; }
-            // one barrier per chunk parity: the key group may finish chunk n + 1
-            // before the state group has waited for chunk n; chunk n + 2 needs
-            // operands that are loaded only after the state group passed chunk n
-            if (tid == 0) {
-                mbar_arrive(&nw_ready[p2]);
-                // U~^T has read this V slot (bar_w above)
-                if (!zero_v && n + L::NV < nchunks) load_v(n + L::NV);
+            named_sync(kBarKey, kStKeyThreads);
+            if (tid == 0) mbar_arrive(&key_ready[p2]);
+            // this chunk's register slot takes chunk n + 2's gate inputs
+            if (p2 == 0)
+                prefetch_gates(n + 2, 0);
+            else
+                prefetch_gates(n + 2, 1);
+        }
+    } else if (tid < kKeyThreads) {
+        // ================================================================ issuer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+        if (tid == kStIssuer) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            if (outs) tma_prefetch_desc(&tm_o);
+            auto load_kq = [&](int n) {
+                const int st = n % L::NSTAGE;
+                uint8_t *stg = sm + st * L::STAGE;
+                mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
+                tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
+                tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
+                if (K == 128) {
+                    tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
+                    tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
+                }
+            };
+            auto load_v = [&](int n) {
+                uint64_t *bar = &v_full[n % L::NV];
+                uint8_t *dst = sm + L::vbuf(n);
+                mbar_arrive_expect_tx(bar, L::V_BYTES);
+                tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
+                tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
+            };
+            // chunk n's [-W^T | T''^T] into ring stage n % 2, P into its own ring
+            auto load_tt = [&](int n) {
+                mbar_arrive_expect_tx(&tt_full[n & 1], 24576);
+                bulk_load(sm + L::nw(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepNW, 24576,
+                          &tt_full[n & 1]);
+            };
+            auto load_p = [&](int n) {
+                mbar_arrive_expect_tx(&p_full[n & 1], 8192);
+                bulk_load(sm + L::ptile(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepP, 8192,
+                          &p_full[n & 1]);
+            };
+            // U~^T(n) = V^T T''^T into U slot n % 2
+            auto issue_ut = [&](int n) -> bool {
+                if (!wait(&tt_full[n & 1], (n >> 1) & 1)) return false;
+                if (!wait(&v_full[n % L::NV], (n / L::NV) & 1)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
+                             sdesc(base + L::tpp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+                mma_commit(&bar_w);
+                return true;
+            };
+            for (int m = 0; m < 2 && m < nchunks; ++m) {
+                load_kq(m);
+                load_tt(m);
+                if (!zero_v) load_v(m);
             }
-            prefetch_gates(n + 1);
+            if (outs) load_p(0);
+            bool ok = zero_v || issue_ut(0);
+            for (int n = 0; ok && n < nchunks; ++n) {
+                // ---- chunk n's epilogue window: U(n) is complete ----
+                ok = wait(&bar_u, n & 1);
+                // the previous S-term has read its gamma Q box (waited before
+                // this chunk's commit, while it is the barrier's latest phase)
+                if (ok && outs && n >= 1) ok = wait(&bar_os, (n - 1) & 1);
+                if (ok && outs) {
+                    // O^T(n) = S(n-1) (gamma Q(n))^T
+                    ok = wait(&key_ready[n & 1], (n >> 1) & 1);
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t stg = base + (n % L::NSTAGE) * L::STAGE;
+#pragma unroll
+                        for (int ks = 0; ks < K / 16; ++ks) {
+                            const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                            mma_bf16_ta(tb + L::ocol(n), tb + L::SBT + 8 * ks,
+                                        sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM,
+                                        ks > 0);
+                        }
+                        mma_commit(&bar_os);
+                    }
+                }
+                if (ok && !zero_v && n + 1 < nchunks) ok = issue_ut(n + 1);
+                if (!ok) break;
+                // bar_u(n) also covers dS(n - 1) and O^T(n - 1) += U^T P^T (the
+                // state thread's earlier products), and the previous S-term was
+                // waited for above: stage (n - 1) % 3 is free
+                if (n + 2 < nchunks) {
+                    load_kq(n + 2);
+                    load_tt(n + 2);  // U(n) read -W^T, U~(n) read T''^T
+                    if (!zero_v) load_v(n + 2);
+                }
+                if (outs && n + 1 < nchunks) load_p(n + 1);
+            }
+            if (!ok) failed = true;
         }
     } else {
         // ================================================================ state group
@@ -1517,8 +1020,522 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         named_sync(kBarState, kStateThreads);
 
-        // U^T += S (-W^T) of chunk m, then O^T = S (gamma Q)^T (warp 8, once
-        // the key group handed over -W^T and gamma Q)
+        // U^T = U~^T + S (-W^T) of chunk m (state thread), once its operands
+        // and the key group's decays and gamma Q are in place
+        auto issue_u = [&](int m) -> bool {
+            if (!wait(&key_ready[m & 1], (m >> 1) & 1)) return false;
+            if (!zero_v && !wait(&bar_w, m & 1)) return false;
+            if (!wait(&tt_full[m & 1], (m >> 1) & 1)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < K / 16; ++ks)
+                // with v = 0 there is no U~ product: this one starts the accumulator
+                mma_bf16_ta(tb + L::ua(m), tb + L::SBT + 8 * ks,
+                            sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
+                            zero_v ? (uint32_t)(ks > 0) : 1u);
+            mma_commit(&bar_u);
+            return true;
+        };
+        // chunk m's O^T -> the staging tile, by warps 12-15 (TMEM lane quarter
+        // w % 4, all 64 columns), then a TMA store by warp 11.  Called by warps
+        // 11-15; one thread waits for the products, warp 11 for the previous
+        // store to have read the tile, and all 160 take the same branch on a
+        // timeout (false).
+        auto store_out = [&](int m) -> bool {
+            bool okw = true;
+            if (sid == 128) okw = wait(&bar_o2, m & 1);
+            if (sw == 3 && lane == 0) bulk_wait_read_all();
+            if (named_sync_or(kBarOut, 160, !okw)) return false;
+            if (sw >= 4) {
+                tc_fence_after();
+                const bool odd = lane & 1;
+                uint8_t *tile = sm + L::OST + (c >> 6) * 8192;
+                const uint32_t cb = (uint32_t)(c & 63) >> 3, cw = (uint32_t)(c & 6) * 2;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::ocol(m) + 32 * half, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        // pairs of lanes swap one value: each writes two channels of one token
+                        const float got = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[i + 1], 1);
+                        const uint32_t t = 32 * half + i + (odd ? 1 : 0);
+                        const float lo = odd ? got : v[i], hi = odd ? v[i + 1] : got;
+                        *reinterpret_cast<uint32_t *>(tile + swz128(t, cb) + cw) =
+                            pack_bf16(lo, hi);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+            }
+            named_sync(kBarOut2, 160);  // the tile is written
+            if (sw == 3 && lane == 0) {
+                tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
+                tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
+                bulk_commit_group();
+            }
+            return true;
+        };
+        if (sw == 0) {
+            bool ok0 = true;
+            if (lane == 0) ok0 = issue_u(0);
+            ok0 = __shfl_sync(0xffffffffu, ok0, 0);
+            failed = !ok0;
+        }
+
+        for (int n = 0; n < nchunks; ++n) {
+            const int st = n % L::NSTAGE;
+            const uint32_t stg = base + st * L::STAGE;
+            // ---- U epilogue: bf16 U^T and U^T diag(decay) into the U slot ----
+            const float *slot = sg + (n % 3) * 68;
+            float gC;  // read with the decays: the slot is rewritten for chunk n + 3
+            bool ok = !failed;
+            if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            {
+                tc_fence_after();
+                // each thread rewrites only the 32 columns it has read
+                gC = slot[64];
+                float v[32];
+                tmem_ld32(tb + lane_off + L::ua(n) + 32 * hf, v);
+                tmem_ld_wait();
+                uint32_t w[16];
+                if (outs) {
+                    pack_row(v, w);
+                    tmem_st16(tb + lane_off + L::ua(n) + 32 * hf, w);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= slot[32 * hf + i];
+                pack_row(v, w);
+                tmem_st16(tb + lane_off + L::ua(n) + 32 * hf + 16, w);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            named_sync(kBarState, kStateThreads);
+            // ---- dS = U^T diag(decay) K, then O^T += U^T P^T (warp 8) ----
+            if (sid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ta(tb + L::DS, tb + L::ud_col(n, ks),
+                                sdesc(stg + L::KC0 + ks * 2048, 8192, 1024), I_DS, ks > 0);
+                mma_commit(&bar_s);
+                if (outs) {
+                    // the issuer's S-term of O^T(n) first (it also reads S(n-1),
+                    // which the update below overwrites), and P(n)
+                    ok = wait(&bar_os, n & 1) && wait(&p_full[n & 1], (n >> 1) & 1);
+                    if (ok) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ta(tb + L::ocol(n), tb + L::ut_col(n, ks),
+                                        sdesc(base + L::ptile(n) + ks * 32, 16, 1024), I_MM, 1);
+                        mma_commit(&bar_o2);
+                    }
+                }
+                ok = ok && wait(&bar_s, n & 1);
+            }
+            if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
+            // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
+            {
+                tc_fence_after();
+                const int j0 = hf * KH;
+#pragma unroll
+                for (int p = 0; p < KH / 32; ++p) {
+                    float v[32];
+                    tmem_ld32(tb + lane_off + L::DS + j0 + 32 * p, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        S[32 * p + i] = fmaf(gC, S[32 * p + i], v[i]);
+                        v[i] = S[32 * p + i];
+                    }
+                    uint32_t w[16];
+                    pack_row(v, w);
+                    tmem_st16(tb + lane_off + L::SBT + (j0 + 32 * p) / 2, w);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            named_sync(kBarState, kStateThreads);
+            // ---- next chunk's U (warp 8); this chunk's output (warps 11-15) ----
+            bool ok1 = true;
+            if (sw == 0) {
+                if (lane == 0 && n + 1 < nchunks) ok1 = issue_u(n + 1);
+                ok1 = __shfl_sync(0xffffffffu, ok1, 0);
+            } else if (sw >= 3 && outs) {
+                ok1 = store_out(n);
+            }
+            if (!ok1) failed = true;
+        }
+        if (sw == 3 && lane == 0 && outs) bulk_wait_all();  // outputs written before the CTA ends
+        if (!failed && tk.stp != nullptr) {
+            const int j0 = hf * KH;
+#pragma unroll
+            for (int j = 0; j < KH; j += 4)
+                *reinterpret_cast<float4 *>(tk.stp + (size_t)c * K + j0 + j) =
+                    make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+    }
+
+    if (failed) *abort_v = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_v) {
+        // products still in flight read shared memory and write TMEM: each
+        // issuing thread's commit completes once all of its products have
+        if (tid == kStIssuer || tid == kKeyThreads) {
+            uint64_t *d = &drain[tid == kStIssuer ? 0 : 1];
+            mma_commit(d);
+            mbar_wait(d, 0, kSpinLimit / 16);
+        }
+        if (tid == kStIssuer) {
+            if (status) atomicOr(status, kStatusTimeout);
+            // let in-flight loads land before the CTA's shared memory is released
+            for (int s = 0; s < 3; ++s) {
+                mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
+            }
+            for (int s = 0; s < 2; ++s) {
+                mbar_wait(&v_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&v_full[s], 1, kSpinLimit / 16);
+                mbar_wait(&tt_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&tt_full[s], 1, kSpinLimit / 16);
+                mbar_wait(&p_full[s], 0, kSpinLimit / 16);
+                mbar_wait(&p_full[s], 1, kSpinLimit / 16);
+            }
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
+// ---------------------------------------------------------------- one-pass (fused) kernel
+// The one-pass form: one CTA per (b, h) sequence (or segment) computes the
+// key-side operands of every chunk on chip and runs the state chain beside
+// them, so no operand goes through global memory.  12 warps:
+//   key group   (warps 0-3): gates, [K;Q] K^T on the tensor cores, A and P,
+//               the inverse and T'^T, T''^T (above), then W^T and U~^T, the
+//               -W^T operand over the spent T'^T / T''^T slot, and gamma
+//               folded into the Q tile.  Thread 0 issues its products and
+//               the q/k / V loads.  It depends on no state and runs up to two
+//               chunks ahead of the state group: the T'/T'' (then -W^T), P,
+//               U~ and V slots are per chunk parity, the q/k stages three.
+//   state group (warps 4-11): the state chain of the two-pass state kernel
+//               above, unchanged -- U, epilogue, dS, fp32 update, and the
+//               transposed output staged for TMA stores by warps 7-11.
+// The key group's [K;Q] K^T and W^T share 64 TMEM columns (one is read out
+// before the other is written), which leaves room for two output
+// accumulators.  Handoffs: nw_ready (key -> state: -W^T, U~^T, P, gamma Q
+// and the chunk's decays are in place), tt_free (U has read -W^T: the slot
+// takes chunk n + 2's T'^T, T''^T), uap_free (the U slot and P are spent).
+template <int K>
+struct FuLayout {
+    static constexpr int NSTAGE = 3;
+    // q/k stage: the K and Q boxes of one 64-channel block adjacent, so that
+    // [K;Q] is one 128-row operand; the K blocks KLBO bytes apart
+    static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
+    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
+    static constexpr uint32_t KLBO = K == 128 ? 16384 : 8192;
+    static constexpr uint32_t VB = NSTAGE * STAGE;            // V ring, two 16 KB slots
+    static constexpr uint32_t TT = VB + 2 * 16384;            // [T'^T | T''^T] / -W^T, two slots
+    static constexpr uint32_t PP = TT + 2 * 16384;            // P, two 8 KB slots
+    static constexpr uint32_t OST = PP + 2 * 8192;            // output staging, 2 x 64 x 64
+    static constexpr uint32_t AF = OST + 16384;               // float [64][68]
+    static constexpr uint32_t KGATE = AF + 64 * kLD * 4;      // G2, gamma, beta
+    static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;     // 3 x (decay[64], gamma_C)
+    static constexpr uint32_t END = SGATE + 3 * 68 * 4;
+    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
+    static constexpr uint32_t V_BYTES = 2u * 8192u;
+    static constexpr size_t SMEM = END;
+    static_assert(SMEM + 1024 <= 232448, "shared memory budget");
+    static __device__ __forceinline__ uint32_t tp(int n) { return TT + (n & 1) * 16384; }
+    static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
+    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }
+    static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
+    static __device__ __forceinline__ uint32_t vbuf(int n) { return VB + (n & 1) * 16384; }
+    // TMEM columns: [K;Q] K^T / W^T, U~^T / U^T of even / odd chunks, O^T of
+    // even / odd chunks, the bf16 state, dS
+    static constexpr uint32_t KW = 0, UA = 64, O0 = 192, O1 = 256, SBT = 320, DS = 384;
+    static __device__ __forceinline__ uint32_t ocol(int n) { return (n & 1) ? O1 : O0; }
+    static __device__ __forceinline__ uint32_t ua(int n) { return UA + 64 * (n & 1); }
+    static __device__ __forceinline__ uint32_t ut_col(int n, int ks) {
+        return ua(n) + 32 * (ks >> 1) + 8 * (ks & 1);
+    }
+    static __device__ __forceinline__ uint32_t ud_col(int n, int ks) { return ut_col(n, ks) + 16; }
+};
+
+constexpr int kFuKeyThreads = 128;
+constexpr int kFuThreads = kFuKeyThreads + kStateThreads;
+
+template <int K>
+__global__ void __launch_bounds__(kFuThreads, 1)
+    prefill_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ alpha,
+                         const float *__restrict__ beta, const float *__restrict__ S0,
+                         bool want_o, float *__restrict__ ST, int T, int Ts, int H, int BH,
+                         SegPlan plan, int *status) {
+    using L = FuLayout<K>;
+    constexpr int KH = K / 2;  // state columns per state-group thread
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0 && status) atomicOr(status, kStatusBounds);
+        return;
+    }
+    uint8_t *sm = smem_raw;
+    __shared__ uint64_t kq_full[3], v_full[2], bar_kq, bar_w, bar_u, bar_s, bar_o2, nw_ready[2],
+        tt_free[2], uap_free[2], drain[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+    volatile int *abort_v = &abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const SegTask tk = segment_task(plan, K, T, S0, ST, BH);
+    const size_t seq = tk.seq;
+    const int t0 = tk.t0, t1 = tk.t1;
+    const bool zero_v = tk.zero_v;
+    const bool outs = want_o && tk.outputs;
+    const int b = (int)(seq / H), h = (int)(seq % H);
+    const int nchunks = (t1 - t0 + 63) / 64;
+    const uint32_t base = smem_u32(sm);
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        if (outs) tma_prefetch_desc(&tm_o);
+        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0],   &v_full[1],
+                            &bar_kq,     &bar_w,      &bar_u,      &bar_s,       &bar_o2,
+                            &nw_ready[0], &nw_ready[1], &tt_free[0], &tt_free[1], &uap_free[0],
+                            &uap_free[1], &drain[0],  &drain[1]};
+        for (uint64_t *bb : bars) mbar_init(bb, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base_sh;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int quad_row = (warp & 3) * 32 + lane;  // TMEM lane of this thread
+    // decay[64] and gamma_C of chunk n in slot n % 3 (written by the key group)
+    float *sg = reinterpret_cast<float *>(sm + L::SGATE);
+
+    auto load_kq = [&](int n) {
+        const int st = n % L::NSTAGE;
+        uint8_t *stg = sm + st * L::STAGE;
+        mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
+        tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
+        tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
+        if (K == 128) {
+            tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
+            tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
+        }
+    };
+    auto load_v = [&](int n) {
+        uint64_t *bar = &v_full[n & 1];
+        uint8_t *dst = sm + L::vbuf(n);
+        mbar_arrive_expect_tx(bar, L::V_BYTES);
+        tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
+        tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_or_abort(bar, parity, kSpinLimit, abort_v);
+        if (!ok) *abort_v = 1;
+        return ok;
+    };
+
+    constexpr uint32_t I_MM = idesc_bf16(128, 64, false, false);  // K-major x K-major, N = 64
+    constexpr uint32_t I_ABMN = idesc_bf16(128, 64, true, true);  // MN-major A and B
+    constexpr uint32_t I_BMN = idesc_bf16(128, 64, false, true);  // MN-major B, N = 64
+    constexpr uint32_t I_DS = idesc_bf16(128, K, false, true);    // MN-major B, N = K
+
+    bool failed = false;
+
+    if (tid < kFuKeyThreads) {
+        // ================================================================ key group
+        float *AF = reinterpret_cast<float *>(sm + L::AF);
+        float *G2 = reinterpret_cast<float *>(sm + L::KGATE);
+        float *gam = G2 + 64;
+        float *bet = G2 + 128;
+        float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
+        auto prefetch_gates = [&](int n) {
+            if (warp == 1 && n < nchunks) {
+                const int nv = min(64, t1 - t0 - n * 64);
+                const size_t i0 = ((size_t)b * Ts + t0 + n * 64 + lane) * H + h;
+                const size_t i1 = i0 + (size_t)32 * H;
+                pa0 = lane < nv ? alpha[i0] : 1.f;
+                pb0 = lane < nv ? beta[i0] : 0.f;
+                pa1 = lane + 32 < nv ? alpha[i1] : 1.f;
+                pb1 = lane + 32 < nv ? beta[i1] : 0.f;
+            }
+        };
+        prefetch_gates(0);
+        if (tid == 0) {
+            for (int m = 0; m < L::NSTAGE && m < nchunks; ++m) load_kq(m);
+            if (!zero_v)
+                for (int m = 0; m < 2 && m < nchunks; ++m) load_v(m);
+        }
+        for (int n = 0; n < nchunks; ++n) {
+            const int st = n % L::NSTAGE;  // q/k stage
+            const int p2 = n & 1;          // ring slots of this chunk
+            const uint32_t stg = base + st * L::STAGE;
+            const int nvalid = min(64, t1 - t0 - n * 64);
+            bool ok = true;
+            if (tid == 0) {
+                ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    issue_kq_kt<K>(tb + L::KW, stg, L::KC0, L::KC1);
+                    mma_commit(&bar_kq);
+                }
+                // chunk n - 2 is done with this parity's slots: U has read its
+                // -W^T (T'/T'' slot), and dS and O^T += U^T P^T have read its U
+                // slot and P
+                if (ok && n >= 2) ok = wait(&tt_free[p2], ((n - 2) >> 1) & 1);
+                if (ok && n >= 2) ok = wait(&uap_free[p2], ((n - 2) >> 1) & 1);
+                if (ok) ok = wait(&bar_kq, n & 1);
+            }
+            if (warp == 1) {
+                chunk_gates(pa0, pa1, pb0, pb1, lane, nvalid, G2, gam, bet);
+                __syncwarp();
+                // the state group's decay to the chunk end and gamma_C; slot
+                // n % 3 was last read in the state epilogue of chunk n - 3,
+                // which precedes the uap_free of chunk n - 3 waited for above
+                // (in the previous iteration)
+                float *slot = sg + (n % 3) * 68;
+                const float gC = G2[63];
+                slot[lane] = exp2f(gC - G2[lane]);
+                slot[lane + 32] = exp2f(gC - G2[lane + 32]);
+                if (lane == 0) slot[64] = exp2f(gC);
+            }
+            if (named_sync_or(kBarKey, kFuKeyThreads, !ok)) { failed = true; break; }
+
+            // ---- A (fp32, solve input) and P (bf16 operand) ----
+            tc_fence_after();
+#pragma unroll 1
+            for (int ch = 0; ch < 2; ++ch)
+                chunk_ap(tb + lane_off + L::KW + 32 * ch, quad_row, ch, G2, bet, AF,
+                         outs ? sm + L::ptile(n) : nullptr);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarKey, kFuKeyThreads);
+            // ---- T = (I + A)^{-1}; T'^T, T''^T ----
+            chunk_inverse_tprime<kFuKeyThreads>(AF, bet, gam, sm + L::tp(n), sm + L::tpp(n), tid);
+            fence_proxy_async_smem();
+            named_sync(kBarKey, kFuKeyThreads);
+
+            // ---- W^T = K^T T'^T and U~^T = V^T T''^T ----
+            if (tid == 0) {
+                if (!zero_v) ok = wait(&v_full[p2], (n >> 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16(tb + L::KW, sdesc(stg + L::KC0 + ks * 2048, L::KLBO, 1024),
+                                 sdesc(base + L::tp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+                        if (!zero_v)
+                            mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
+                                     sdesc(base + L::tpp(n) + ks * 2048, 8192, 1024), I_ABMN,
+                                     ks > 0);
+                    }
+                    mma_commit(&bar_w);
+                }
+            }
+            {
+                // Q <- diag(gamma) Q in place while the products run (they read
+                // the K blocks, V and T'^T, T''^T; Q is next read by O^T)
+                uint8_t *stq = sm + st * L::STAGE;
+#pragma unroll
+                for (int e = tid; e < (K / 64) * 512; e += kFuKeyThreads) {
+                    const int blk_i = e >> 9, ee = e & 511;
+                    uint4 *p = reinterpret_cast<uint4 *>(stq + (blk_i ? L::QC1 : L::QC0) + ee * 16);
+                    const float gq = gam[ee >> 3];
+                    uint4 w = *p;
+                    uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 f =
+                            __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[c]));
+                        wv[c] = pack_bf16(f.x * gq, f.y * gq);
+                    }
+                    *p = w;
+                }
+            }
+            if (tid == 0 && ok) {
+                ok = wait(&bar_w, n & 1);
+                // U~^T has read this V slot
+                if (ok && !zero_v && n + 2 < nchunks) load_v(n + 2);
+            }
+            if (named_sync_or(kBarKey, kFuKeyThreads, !ok)) { failed = true; break; }
+            {
+                // -W^T over T'^T, T''^T (consumed by the products above)
+                tc_fence_after();
+                if (quad_row < K) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) {
+                        float v[32];
+                        tmem_ld32(tb + lane_off + L::KW + 32 * ch, v);
+                        tmem_ld_wait();
+                        store_row<4>(sm + L::nw(n), quad_row, 4 * ch, v, -1.f);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_sync_or(kBarKey, kFuKeyThreads, !ok)) { failed = true; break; }
+            if (tid == 0) mbar_arrive(&nw_ready[p2]);
+            prefetch_gates(n + 1);
+        }
+    } else {
+        // ================================================================ state group
+        const int sid = tid - kFuKeyThreads;  // 0..255
+        const int sw = sid >> 5;              // state warp 0..7
+        const int c = quad_row;               // state row = TMEM lane = value channel
+        const int hf = sw >> 2;               // column half
+        // initial state: fp32 registers + bf16 operand copy in TMEM
+        float S[KH];
+        {
+            const int j0 = hf * KH;
+#pragma unroll
+            for (int j = 0; j < KH; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tk.s0p) x = *reinterpret_cast<const float4 *>(tk.s0p + (size_t)c * K + j0 + j);
+                if (tk.s0_identity) {
+                    x.x = (c == j0 + j) ? 1.f : 0.f;
+                    x.y = (c == j0 + j + 1) ? 1.f : 0.f;
+                    x.z = (c == j0 + j + 2) ? 1.f : 0.f;
+                    x.w = (c == j0 + j + 3) ? 1.f : 0.f;
+                }
+                S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+            }
+#pragma unroll
+            for (int p = 0; p < KH / 32; ++p) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = S[32 * p + i];
+                uint32_t w[16];
+                pack_row(v, w);
+                tmem_st16(tb + lane_off + L::SBT + (j0 + 32 * p) / 2, w);
+            }
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        named_sync(kBarState, kStateThreads);
+
+        // U^T += S (-W^T) of chunk m, then O^T = S (gamma Q)^T (warp 4, once
+        // the key group handed chunk m over)
         auto issue_u = [&](int m) -> bool {
             if (!wait(&nw_ready[m & 1], (m >> 1) & 1)) return false;
             tc_fence_after();
@@ -1540,9 +1557,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return true;
         };
-        // chunk m's O^T -> the staging tile, by warps 12-15 (TMEM lane quarter
-        // w % 4, all 64 columns), then a TMA store by warp 11.  Called by warps
-        // 11-15; one thread waits for the products, warp 11 for the previous
+        // chunk m's O^T -> the staging tile, by warps 8-11 (TMEM lane quarter
+        // w % 4, all 64 columns), then a TMA store by warp 7.  Called by warps
+        // 7-11; one thread waits for the products, warp 7 for the previous
         // store to have read the tile, and all 160 take the same branch on a
         // timeout (false).
         auto store_out = [&](int m) -> bool {
@@ -1596,11 +1613,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float *slot = sg + (n % 3) * 68;
             float gC;  // read with the decays: the slot is rewritten for chunk n + 3
             bool ok = !failed;
-            if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
-            if (sid == 32 && ok && n + 2 < nchunks) {
-                // U^T has read -W^T: ring stage n % 2 takes chunk n + 2's T', T''
+            if (sid == 0 && ok) {
                 ok = wait(&bar_u, n & 1);
-                if (ok) load_tt(n + 2);
+                // U^T has read -W^T: the slot takes chunk n + 2's T'^T, T''^T
+                if (ok) mbar_arrive(&tt_free[p2]);
             }
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             {
@@ -1623,31 +1639,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             named_sync(kBarState, kStateThreads);
-            // ---- dS = U^T diag(decay) K, then O^T += U^T P^T (warp 8) ----
+            // ---- dS = U^T diag(decay) K, then O^T += U^T P^T (warp 4) ----
             if (sid == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ta(tb + L::DS, tb + L::ud_col(n, ks),
-                                sdesc(stg + L::KC0 + ks * 2048, 8192, 1024), I_DS, ks > 0);
+                                sdesc(stg + L::KC0 + ks * 2048, L::KLBO, 1024), I_DS, ks > 0);
                 mma_commit(&bar_s);
                 if (outs) {
-                    ok = wait(&p_full[p2], (n >> 1) & 1);
-                    if (ok) {
-                        tc_fence_after();
+                    // P of chunk n was written before its nw_ready
+                    tc_fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_bf16_ta(tb + L::ocol(n), tb + L::ut_col(n, ks),
-                                        sdesc(base + L::ptile(n) + ks * 32, 16, 1024), I_MM, 1);
-                        mma_commit(&bar_o2);
-                    }
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ta(tb + L::ocol(n), tb + L::ut_col(n, ks),
+                                    sdesc(base + L::ptile(n) + ks * 32, 16, 1024), I_MM, 1);
+                    mma_commit(&bar_o2);
                 }
-                ok = ok && wait(&bar_s, n & 1);
+                ok = wait(&bar_s, n & 1);
                 if (ok) {
                     // dS(n) and, before it, O^T's first product have read q/k
                     // stage n % 3 (the key group is done with it): chunk n + 3
                     if (n + L::NSTAGE < nchunks) load_kq(n + L::NSTAGE);
-                    if (!outs) mbar_arrive(&ua_free[p2]);  // dS has read the U slot
+                    if (!outs) mbar_arrive(&uap_free[p2]);  // dS has read the U slot
                 }
             }
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
@@ -1673,18 +1687,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             named_sync(kBarState, kStateThreads);
-            // ---- next chunk's products (warp 8), loads (warp 10), this
-            // ---- chunk's output (warps 11-15) ----
+            // ---- next chunk's products (warp 4), releases (warp 6), this
+            // ---- chunk's output (warps 7-11) ----
             bool ok1 = true;
             if (sw == 0) {
                 if (lane == 0 && n + 1 < nchunks) ok1 = issue_u(n + 1);
             } else if (sw == 2) {
                 // O^T += U^T P^T has completed (after dS, issued before it):
-                // the U slot and P ring stage n % 2 are free
+                // the U slot and P slot of this parity are free
                 if (lane == 0 && outs) {
                     ok1 = wait(&bar_o2, n & 1);
-                    if (ok1) mbar_arrive(&ua_free[p2]);
-                    if (ok1 && n + 2 < nchunks) load_p(n + 2);
+                    if (ok1) mbar_arrive(&uap_free[p2]);
                 }
             } else if (sw >= 3 && outs) {
                 ok1 = store_out(n);
@@ -1708,7 +1721,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (*abort_v) {
         // products still in flight read shared memory and write TMEM: each
         // issuing thread's commit completes once all of its products have
-        if (tid == 0 || tid == kKeyThreads) {
+        if (tid == 0 || tid == kFuKeyThreads) {
             uint64_t *d = &drain[tid == 0 ? 0 : 1];
             mma_commit(d);
             mbar_wait(d, 0, kSpinLimit / 16);
@@ -1720,15 +1733,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
             }
-            for (int s = 0; s < L::NV; ++s) {
+            for (int s = 0; s < 2; ++s) {
                 mbar_wait(&v_full[s], 0, kSpinLimit / 16);
                 mbar_wait(&v_full[s], 1, kSpinLimit / 16);
-            }
-            for (int s = 0; s < 2; ++s) {
-                mbar_wait(&tt_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&tt_full[s], 1, kSpinLimit / 16);
-                mbar_wait(&p_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&p_full[s], 1, kSpinLimit / 16);
             }
         }
         __syncthreads();
@@ -1854,17 +1861,16 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const int two = prep != nullptr;
-    const size_t smem = two ? StLayout<K>::SMEM : TcLayout<K>::SMEM;
+    const size_t smem = two ? StLayout<K>::SMEM : FuLayout<K>::SMEM;
     if (attr_set[two][dev] != context_key()) {
         const cudaError_t e =
             two ? cudaFuncSetAttribute(prefill_state_kernel<K>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                : cudaFuncSetAttribute(prefill_tc_kernel<K>,
+                : cudaFuncSetAttribute(prefill_fused_kernel<K>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set[two][dev] = context_key();
     }
-    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(o);
     int *status = device_status_ptr();
     auto launch = [&](long long grid, SegPlan plan) {
         if (two)
@@ -1872,8 +1878,9 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
                 mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan, prep,
                 status);
         else
-            prefill_tc_kernel<K><<<(unsigned)grid, kTcThreads, smem, stream>>>(
-                mq, mk, mv, alpha, beta, S0, ob, ST, T, Ts, H, (int)BH, plan, status);
+            prefill_fused_kernel<K><<<(unsigned)grid, kFuThreads, smem, stream>>>(
+                mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan,
+                status);
         return cudaGetLastError();
     };
     if (sh.nseg == 1) return launch(BH, SegPlan{kWhole, 1, T, nullptr});
@@ -1895,7 +1902,7 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
     if (!make_token_map(&mq, q, B, T, Ts, H, K) || !make_token_map(&mk, k, B, T, Ts, H, K) ||
         !make_token_map(&mv, v, B, T, Ts, H, 128))
         return cudaErrorInvalidValue;
-    // outputs of the two-pass form go out by TMA store (unused without outputs)
+    // outputs go out by TMA store (the map is unused without outputs)
     if (o) {
         if (!make_token_map(&mo, o, B, T, Ts, H, 128)) return cudaErrorInvalidValue;
     } else {
