@@ -68,11 +68,11 @@ constexpr int kBarKey = 1, kBarState = 2;       // named barrier ids
 constexpr long long kSpinLimit = 2000000000LL;  // ~1 s of SM clocks per wait
 constexpr int kLD = 68;                         // row stride of the fp32 64 x 64 matrix
 
-// Bytes of one chunk's key-side operands in the two-pass form: -W^T (16 KB:
-// 128 key-channel rows of 64 tokens), T''^T and P (8 KB each), every tile
-// stored as its 128-byte-swizzled shared-memory image.
-constexpr uint32_t kPrepNW = 0, kPrepTPP = 16384, kPrepP = 24576;
-constexpr uint32_t kPrepChunkBytes = 32768;
+// Bytes of one chunk's key-side operands in the two-pass form: T'^T, T''^T
+// and P, each a 64 x 64 bf16 tile stored as its 128-byte-swizzled
+// shared-memory image.
+constexpr uint32_t kPrepTP = 0, kPrepTPP = 8192, kPrepP = 16384;
+constexpr uint32_t kPrepChunkBytes = 24576;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
@@ -473,23 +473,20 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
 
 // ---------------------------------------------------------------- key-side pass
 // The two-pass form's first kernel.  Everything of a chunk that depends only
-// on its keys, queries and gates -- A, P, the inverse T, T'' and W -- has no
+// on its keys, queries and gates -- A, P, the inverse T and T', T'' -- has no
 // dependence on the state, so it runs for all B * H * ceil(T/64) chunks at
 // once instead of in each sequence's serial chunk loop.  Persistent CTAs of
 // 128 threads (four per SM, so that one CTA's loads and waits hide under the
-// others' work) stride over the chunks; per chunk: [K;Q] K^T on the tensor
-// cores, A and P, the inverse with T'^T into the spent Q box, W^T = K^T T'^T
-// on the tensor cores (into the same 64 TMEM columns), then -W^T, T''^T and P
-// go to global memory as their swizzled shared-memory images, which the
-// state-side kernel copies in with bulk copies.  The next chunk's q/k boxes
-// load once both products have read the stage.  Same arithmetic as the fused
-// kernel's key group (the shared helpers above, the same product
-// instructions), so both forms give identical results.
+// others' work) stride over the chunks; each chunk's [K;Q] K^T is one tcgen05
+// product into 64 TMEM columns, the next chunk's q/k boxes load (TMA) while
+// the current one is solved, and T'^T, T''^T and P go to global memory as
+// their swizzled shared-memory images, which the state-side kernel copies in
+// with bulk copies.  Same arithmetic as the fused kernel's key group (the
+// shared helpers above), so both forms give identical results.
 template <int K>
 struct PrepLayout {
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;  // one q/k stage
-    static constexpr uint32_t KLBO = K == 128 ? 16384 : 8192;    // next 64-channel block of K
     static constexpr uint32_t AF = STAGE;                        // float [64][68]
     static constexpr uint32_t GATE = AF + 64 * kLD * 4;          // G2, gamma, beta
     static constexpr uint32_t END = GATE + 3 * 64 * 4;
@@ -516,7 +513,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full, bar_p1, bar_w, drain;
+    __shared__ uint64_t kq_full, bar_p1, drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -533,7 +530,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         tma_prefetch_desc(&tm_k);
         mbar_init(&kq_full, 1);
         mbar_init(&bar_p1, 1);
-        mbar_init(&bar_w, 1);
         mbar_init(&drain, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -591,7 +587,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         return true;
     };
 
-    constexpr uint32_t I_ABMN = idesc_bf16(128, 64, true, true);  // MN-major A and B
     const long long G = gridDim.x;
     long long j = blockIdx.x;
     if (tid == 0 && j < nchunk_all) load_kq(j);
@@ -608,6 +603,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
                 issue_kq_kt<K>(tb, smem_u32(sm), L::KC0, L::KC1);
                 mma_commit(&bar_p1);
                 ok = wait(&bar_p1, it & 1);
+                // the product has read the stage: the next chunk's boxes may land
+                if (ok && j + G < nchunk_all) load_kq(j + G);
             }
         }
         if (warp == 1) {
@@ -615,45 +612,14 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
             prefetch_gates(j + G);
         }
         if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
-        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [-W^T | T''^T | P]
+        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T'^T | T''^T | P]
         tc_fence_after();
         for (int ch = 0; ch < 2; ++ch)  // both 32-column halves per thread
             chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, out + kPrepP);
         tc_fence_before();
         named_sync(kBarKey, kPrepThreads);
-        // T'^T into the spent Q box of channel block 0 (the W^T product's
-        // operand), T''^T straight to global memory
-        chunk_inverse_tprime<kPrepThreads>(AF, bet, gam, sm + L::QC0, out + kPrepTPP, tid);
-        fence_proxy_async_smem();
-        named_sync(kBarKey, kPrepThreads);
-        // ---- W^T = K^T T'^T (the same instruction as in the one-pass kernel) ----
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tb, sdesc(smem_u32(sm) + L::KC0 + ks * 2048, L::KLBO, 1024),
-                         sdesc(smem_u32(sm) + L::QC0 + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
-            mma_commit(&bar_w);
-            ok = wait(&bar_w, it & 1);
-            // both products have read the stage: the next chunk's boxes may land
-            if (ok && j + G < nchunk_all) load_kq(j + G);
-        }
-        if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
-        {
-            // -W^T as the right operand image of U^T += S (-W^T)
-            tc_fence_after();
-            if (quad_row < K) {
-#pragma unroll 1
-                for (int ch = 0; ch < 2; ++ch) {
-                    float v[32];
-                    tmem_ld32(tb + lane_off + 32 * ch, v);
-                    tmem_ld_wait();
-                    store_row<4>(out + kPrepNW, quad_row, 4 * ch, v, -1.f);
-                }
-            }
-        }
-        tc_fence_before();
-        named_sync(kBarKey, kPrepThreads);  // TMEM, AF and the gates are rewritten next
+        chunk_inverse_tprime<kPrepThreads>(AF, bet, gam, out + kPrepTP, out + kPrepTPP, tid);
+        named_sync(kBarKey, kPrepThreads);  // AF and the gates are rewritten next
     }
 
     if (failed) *abort_v = 1;
@@ -679,16 +645,17 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 
 // ---------------------------------------------------------------- state-side pass
 // The two-pass form's second kernel: one CTA per (b, h) sequence (or segment)
-// walks its chunks like the fused kernel, but loads -W^T, T''^T and P
+// walks its chunks like the fused kernel, but loads T'^T, T''^T and P
 // instead of solving for them.  Three roles:
 //   key group (warps 0-6): per chunk the gates, the state group's decay
-//       factors and gamma folded into the Q box (no products, no loads).
+//       factors, gamma folded into the Q box, and -W^T from TMEM into the
+//       spent T'/T'' slot (no products, no loads).
 //   issuer (warp 7, one thread): every TMA load, and the products that are
-//       not on the state chain -- O^T(n) = S(n-1) (gamma Q(n))^T and
-//       U~^T(n+1) = V^T T''^T -- issued in chunk n's epilogue window, while
-//       the tensor pipe would otherwise idle (one SM issues tcgen05 products
-//       one at a time, ~44 cycles each, so products issued beside the chain's
-//       would delay them).
+//       not on the state chain -- O^T(n) = S(n-1) (gamma Q(n))^T, and
+//       W^T(n+1) = K^T T'^T, U~^T(n+1) = V^T T''^T -- issued in chunk n's
+//       epilogue window, while the tensor pipe would otherwise idle (an SM
+//       issues tcgen05 products one at a time, ~44 cycles each, so products
+//       issued beside the chain's would delay them).
 //   state group (warps 8-15): the state chain
 //       U^T(n)  = U~^T(n) + S(n-1) (-W^T(n))       (issued at the end of n - 1)
 //       epilogue: U^T -> bf16, U^T diag(decay) -> bf16, in the U slot
@@ -702,12 +669,14 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 // every earlier product of its thread, so bar_u(n) (the state thread's
 // commit after U(n)) also says that dS(n-1) and O^T(n-1) += U^T P^T are
 // complete: the issuer reloads and reuses slots only after it.  The state
-// update waits for the issuer's O^T(n) S-term (bar_os), which reads S(n-1).
-// Rings: q/k (three stages), V, [-W^T | T''^T], P and U (two each), O (two);
-// the loads of chunk n + 2 (P: n + 1) go out in chunk n's window.  Every state
-// quantity is the fused kernel's arithmetic on the same operands, so S_T is
-// bit-identical to it (o agrees to the accumulation order of the transposed
-// product).
+// update waits for the issuer's O^T(n) S-term (bar_os), which reads S(n-1);
+// the issuer writes W^T(n+1) only after the key group has read W^T(n).
+// Every mbarrier wait is for the barrier's latest phase: the next phase needs
+// a step that the waiting thread takes after the wait.  Rings: q/k (three
+// stages), V, [T'^T | T''^T] (then -W^T), P, U and O (two each); the loads of
+// chunk n + 2 (P: n + 1) go out in chunk n's window.  Every state quantity is
+// the fused kernel's arithmetic on the same operands, so S_T is bit-identical
+// to it (o agrees to the accumulation order of the transposed product).
 
 template <int K>
 struct StLayout {
@@ -717,8 +686,8 @@ struct StLayout {
     static constexpr uint32_t QC0 = K == 128 ? 16384 : 8192, QC1 = QC0 + 8192;
     static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
     static constexpr uint32_t VB = NSTAGE * STAGE;               // V ring, 16 KB per chunk
-    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [-W^T | T''^T]
-    static constexpr uint32_t PP = PR + 2 * 24576;               // ring of P
+    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [T'^T | T''^T] / -W^T
+    static constexpr uint32_t PP = PR + 2 * 16384;               // ring of P
     static constexpr uint32_t OST = PP + 2 * 8192;               // output staging, 2 x 64 x 64
     static constexpr uint32_t KGATE = OST + 16384;               // G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;        // 3 x (decay[64], gamma_C)
@@ -727,13 +696,14 @@ struct StLayout {
     static constexpr uint32_t V_BYTES = 2u * 8192u;
     static constexpr size_t SMEM = END;
     static_assert(SMEM + 1024 <= 232448, "shared memory budget");
-    static __device__ __forceinline__ uint32_t nw(int n) { return PR + (n & 1) * 24576; }
-    static __device__ __forceinline__ uint32_t tpp(int n) { return nw(n) + 16384; }
+    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * 16384; }
+    static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
+    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // over T', T''
     static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
     static __device__ __forceinline__ uint32_t vbuf(int n) { return VB + (n % NV) * 16384; }
     // TMEM columns: O^T of even / odd chunks, U~^T / U^T of even / odd
-    // chunks, the bf16 state (two K elements per column), dS
-    static constexpr uint32_t O0 = 0, O1 = 64, UA = 128, SBT = 256, DS = 384;
+    // chunks, the bf16 state (two K elements per column), W^T, dS
+    static constexpr uint32_t O0 = 0, O1 = 64, UA = 128, SBT = 256, WT = 320, DS = 384;
     static __device__ __forceinline__ uint32_t ocol(int n) { return (n & 1) ? O1 : O0; }
     static __device__ __forceinline__ uint32_t ua(int n) { return UA + 64 * (n & 1); }
     // After chunk n's epilogue, token half h of its U slot (32 columns) holds
@@ -882,6 +852,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 *p = w;
             }
+            if (tid == 0) ok = wait(&bar_w, n & 1);  // W^T(n) and U~^T(n) complete
+            if (named_sync_or(kBarKey, kStKeyThreads, !ok)) { failed = true; break; }
+            if (warp < 4) {
+                // -W^T over T'^T, T''^T (both read by the products above)
+                tc_fence_after();
+                if (quad_row < K) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) {
+                        float v[32];
+                        tmem_ld32(tb + lane_off + L::WT + 32 * ch, v);
+                        tmem_ld_wait();
+                        store_row<4>(sm + L::nw(n), quad_row, 4 * ch, v, -1.f);
+                    }
+                }
+                tc_fence_before();
+            }
             fence_proxy_async_smem();
             named_sync(kBarKey, kStKeyThreads);
             if (tid == 0) mbar_arrive(&key_ready[p2]);
@@ -917,10 +903,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
                 tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
             };
-            // chunk n's [-W^T | T''^T] into ring stage n % 2, P into its own ring
+            // chunk n's [T'^T | T''^T] into ring stage n % 2, P into its own ring
             auto load_tt = [&](int n) {
-                mbar_arrive_expect_tx(&tt_full[n & 1], 24576);
-                bulk_load(sm + L::nw(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepNW, 24576,
+                mbar_arrive_expect_tx(&tt_full[n & 1], 16384);
+                bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepTP, 16384,
                           &tt_full[n & 1]);
             };
             auto load_p = [&](int n) {
@@ -928,15 +914,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bulk_load(sm + L::ptile(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepP, 8192,
                           &p_full[n & 1]);
             };
-            // U~^T(n) = V^T T''^T into U slot n % 2
-            auto issue_ut = [&](int n) -> bool {
+            // W^T(n) = K^T T'^T and U~^T(n) = V^T T''^T (U slot n % 2)
+            auto issue_wu = [&](int n) -> bool {
+                if (!wait(&kq_full[n % L::NSTAGE], (n / L::NSTAGE) & 1)) return false;
                 if (!wait(&tt_full[n & 1], (n >> 1) & 1)) return false;
-                if (!wait(&v_full[n % L::NV], (n / L::NV) & 1)) return false;
+                if (!zero_v && !wait(&v_full[n % L::NV], (n / L::NV) & 1)) return false;
                 tc_fence_after();
+                const uint32_t stg = base + (n % L::NSTAGE) * L::STAGE;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
-                             sdesc(base + L::tpp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+                for (int ks = 0; ks < 4; ++ks) {
+                    mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, 8192, 1024),
+                             sdesc(base + L::tp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+                    if (!zero_v)
+                        mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
+                                 sdesc(base + L::tpp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+                }
                 mma_commit(&bar_w);
                 return true;
             };
@@ -946,17 +938,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!zero_v) load_v(m);
             }
             if (outs) load_p(0);
-            bool ok = zero_v || issue_ut(0);
+            bool ok = issue_wu(0);
             for (int n = 0; ok && n < nchunks; ++n) {
                 // ---- chunk n's epilogue window: U(n) is complete ----
                 ok = wait(&bar_u, n & 1);
                 // the previous S-term has read its gamma Q box (waited before
                 // this chunk's commit, while it is the barrier's latest phase)
                 if (ok && outs && n >= 1) ok = wait(&bar_os, (n - 1) & 1);
+                // the key group is done with chunk n: gamma Q(n) is in place and
+                // W^T(n) has been read out (its columns take W^T(n+1) below)
+                ok = ok && wait(&key_ready[n & 1], (n >> 1) & 1);
                 if (ok && outs) {
                     // O^T(n) = S(n-1) (gamma Q(n))^T
-                    ok = wait(&key_ready[n & 1], (n >> 1) & 1);
-                    if (ok) {
+                    {
                         tc_fence_after();
                         const uint32_t stg = base + (n % L::NSTAGE) * L::STAGE;
 #pragma unroll
@@ -969,14 +963,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mma_commit(&bar_os);
                     }
                 }
-                if (ok && !zero_v && n + 1 < nchunks) ok = issue_ut(n + 1);
+                if (ok && n + 1 < nchunks) ok = issue_wu(n + 1);
                 if (!ok) break;
                 // bar_u(n) also covers dS(n - 1) and O^T(n - 1) += U^T P^T (the
                 // state thread's earlier products), and the previous S-term was
                 // waited for above: stage (n - 1) % 3 is free
                 if (n + 2 < nchunks) {
                     load_kq(n + 2);
-                    load_tt(n + 2);  // U(n) read -W^T, U~(n) read T''^T
+                    load_tt(n + 2);  // U(n) read -W^T (written over T'^T, T''^T)
                     if (!zero_v) load_v(n + 2);
                 }
                 if (outs && n + 1 < nchunks) load_p(n + 1);
@@ -1020,12 +1014,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         named_sync(kBarState, kStateThreads);
 
-        // U^T = U~^T + S (-W^T) of chunk m (state thread), once its operands
-        // and the key group's decays and gamma Q are in place
+        // U^T = U~^T + S (-W^T) of chunk m (state thread), once the key group
+        // has written -W^T (after U~^T completed) and the decays and gamma Q
         auto issue_u = [&](int m) -> bool {
             if (!wait(&key_ready[m & 1], (m >> 1) & 1)) return false;
-            if (!zero_v && !wait(&bar_w, m & 1)) return false;
-            if (!wait(&tt_full[m & 1], (m >> 1) & 1)) return false;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks)

@@ -117,13 +117,13 @@ def test_workspace_query(lib):
 
 def test_two_pass_workspace_query(lib):
     two = binding.gdn_prefill_two_pass_workspace_size
-    # 128 sequences run one CTA each (no segment scratch): 32 KiB per 64-token chunk
-    assert two(8, 4096, 16, 128, 128, binding.GDN_BF16) == 8 * 16 * 64 * 32768
-    assert two(8, 4096, 16, 64, 128, binding.GDN_BF16) == 8 * 16 * 64 * 32768
-    assert two(2, 65, 3, 128, 128, binding.GDN_BF16) == 2 * 3 * 2 * 32768  # ragged: 2 chunks
+    # 128 sequences run one CTA each (no segment scratch): 24 KiB per 64-token chunk
+    assert two(8, 4096, 16, 128, 128, binding.GDN_BF16) == 8 * 16 * 64 * 24576
+    assert two(8, 4096, 16, 64, 128, binding.GDN_BF16) == 8 * 16 * 64 * 24576
+    assert two(2, 65, 3, 128, 128, binding.GDN_BF16) == 2 * 3 * 2 * 24576  # ragged: 2 chunks
     for K, V in ((128, 128), (64, 128)):
         need = binding.gdn_prefill_workspace_size(1, 65536, 16, K, V, binding.GDN_BF16)
-        assert two(1, 65536, 16, K, V, binding.GDN_BF16) >= need + 16 * 1024 * 32768
+        assert two(1, 65536, 16, K, V, binding.GDN_BF16) >= need + 16 * 1024 * 24576
     # no two-pass form: float32, the (32, 32) variant, empty or invalid problems
     assert two(8, 4096, 16, 128, 128, binding.GDN_FP32) == 0
     assert two(1, 256, 1, 32, 32, binding.GDN_BF16) == 0

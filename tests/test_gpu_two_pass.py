@@ -28,7 +28,7 @@ def run_both(p, S0=True):
     two = binding.gdn_prefill_two_pass_workspace_size(B, T, H, K, V, binding.GDN_BF16)
     assert two > need
     chunks = (T + 63) // 64
-    assert two - (need + 255) // 256 * 256 == B * H * chunks * 32768
+    assert two - (need + 255) // 256 * 256 == B * H * chunks * 24576
     outs = []
     for ws_bytes in (need, two):
         o = torch.full((B, T, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -80,7 +80,7 @@ def test_two_pass_sizes():
     assert binding.gdn_prefill_two_pass_workspace_size(2, 300, 3, 128, 128, binding.GDN_FP32) == 0
     assert binding.gdn_prefill_two_pass_workspace_size(2, 300, 3, 32, 32, binding.GDN_BF16) == 0
     assert binding.gdn_prefill_two_pass_workspace_size(8, 4096, 16, 128, 128,
-                                                       binding.GDN_BF16) == 8 * 16 * 64 * 32768
+                                                       binding.GDN_BF16) == 8 * 16 * 64 * 24576
 
 
 def test_two_pass_repeated_calls_stay_identical():
