@@ -523,10 +523,20 @@ def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over
         binding.gdn_prefill(qg, kg, dp["v"], dp["alpha"], dp["beta"], None, o, ST, B, T, H,
                             Kout, V, binding.GDN_BF16, ws, wsb)
 
+    # the prologue inside the prefill's key-side pass (no separate pass)
+    wsg = binding.gdn_prefill_gathered_workspace_size(B, T, H, Kin, Kout, V, binding.GDN_BF16)
+    wg = torch.empty(wsg, dtype=torch.uint8, device="cuda")
+
+    def gathered():
+        binding.gdn_prefill_gathered(d["q"], d["k"], idx, Kin, dp["v"], dp["alpha"], dp["beta"],
+                                     None, o, ST, B, T, H, Kout, V, binding.GDN_BF16, wg, wsg)
+
     tp, _ = time_calls(pro, args.steps, args.warmup, torch, barrier)
     tp = max_over_ranks(tp)
     tl, _ = time_calls(pipeline, args.steps, args.warmup, torch, barrier)
     tl = max_over_ranks(tl)
+    tg, _ = time_calls(gathered, args.steps, args.warmup, torch, barrier)
+    tg = max_over_ranks(tg)
     byts = 2 * rows * (2 * Kin + 2 * Kout)
     gbs = byts / (tp / args.steps / 1e3) / 1e9
     return {"workload": f"B={B} T={T} H={H} bf16 q and k, d_k {Kin} -> {Kout}",
@@ -534,7 +544,11 @@ def bench_prologue(args, torch, binding, d, idx, dp, o, peaks, barrier, max_over
             "prologue_hbm_frac": gbs / peaks["hbm_gbs"],
             "pipeline_ms_per_step": tl / args.steps,
             "pipeline_tokens_per_s": B * T * world * args.steps / (tl / 1e3),
-            "launches": args.steps * 6}
+            "gathered_ms_per_step": tg / args.steps,
+            "gathered_tokens_per_s": B * T * world * args.steps / (tg / 1e3),
+            "gathered_speedup_vs_pipeline": tl / tg,
+            "gathered_api": "gdn_prefill_gathered (prologue inside the key-side pass)",
+            "launches": args.steps * (6 + 2)}
 
 
 def bench_truncation(args, torch, binding, d, ST, barrier, max_over_ranks, world):

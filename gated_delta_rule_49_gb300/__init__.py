@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     gdn_get_last_device_status,
     gdn_prefill,
     gdn_prefill_gated,
+    gdn_prefill_gathered,
+    prefill_gathered,
     gdn_decode_step_gated,
     prefill_gated,
     prefill_truncated,

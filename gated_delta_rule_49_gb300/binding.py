@@ -58,6 +58,8 @@ EXPORTS = (
     "gdn_drrqr_select",
     "gdn_prefill_host_workspace_size",
     "gdn_prefill_host",
+    "gdn_prefill_gathered",
+    "gdn_prefill_gathered_workspace_size",
 )
 
 _lock = threading.Lock()
@@ -126,6 +128,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_prefill_host.restype = i
         lib.gdn_prefill_noalloc_max_workspace.argtypes = []
         lib.gdn_prefill_noalloc_max_workspace.restype = sz
+        lib.gdn_prefill_gathered.argtypes = [vp, vp, vp, i] + [vp] * 6 + [i] * 6 + [vp, sz, vp]
+        lib.gdn_prefill_gathered.restype = i
+        lib.gdn_prefill_gathered_workspace_size.argtypes = [i] * 7
+        lib.gdn_prefill_gathered_workspace_size.restype = sz
         _lib = lib
         return lib
 
@@ -353,6 +359,36 @@ def gdn_prefill_host(q, k, v, alpha, beta, S0, o, S_T, B, T, H, K, V, dtype, win
                                  _ptr(o), _ptr(S_T), B, T, H, K, V, dtype, window,
                                  _ptr(workspace), workspace_bytes, _stream(stream))
     return _check(st, "gdn_prefill_host")
+
+
+def gdn_prefill_gathered_workspace_size(B, T, H, K_in, K, V, dtype) -> int:
+    return int(load().gdn_prefill_gathered_workspace_size(B, T, H, K_in, K, V, dtype))
+
+
+def gdn_prefill_gathered(q_full, k_full, idx, K_in, v, alpha, beta, S0, o, S_T, B, T, H, K, V,
+                         dtype, workspace, workspace_bytes, stream=None) -> int:
+    st = load().gdn_prefill_gathered(_ptr(q_full), _ptr(k_full), _ptr(idx), K_in, _ptr(v),
+                                     _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_T), B, T,
+                                     H, K, V, dtype, _ptr(workspace), workspace_bytes,
+                                     _stream(stream))
+    return _check(st, "gdn_prefill_gathered")
+
+
+def prefill_gathered(q_full, k_full, idx, v, alpha, beta, S0=None, want_o=True, want_state=True,
+                     stream=None):
+    """The pruned prefill from full-width q / k ([B, T, H, 128] bf16) and the kept
+    channels idx ([H, 64] int32): returns (o, S_T) with S_T [B, H, 128, 64]."""
+    import torch
+    B, T, H, K_in = k_full.shape
+    K, V = idx.shape[1], v.shape[-1]
+    dt = _dtype_code(k_full)
+    o = torch.empty((B, T, H, V), dtype=v.dtype, device=v.device) if want_o else None
+    ST = torch.empty((B, H, V, K), dtype=torch.float32, device=v.device) if want_state else None
+    need = gdn_prefill_gathered_workspace_size(B, T, H, K_in, K, V, dt)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=v.device)
+    gdn_prefill_gathered(q_full, k_full, idx, K_in, v, alpha, beta, S0, o, ST, B, T, H, K, V, dt,
+                         ws, need, stream)
+    return o, ST
 
 
 def gather_normalize(x, idx, stream=None):

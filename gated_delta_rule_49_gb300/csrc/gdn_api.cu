@@ -173,6 +173,36 @@ int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
                                                B, T, T, H, K, V, GDN_GATE_SCALAR, dtype, st));
 }
 
+size_t gdn_prefill_gathered_workspace_size(int B, int T, int H, int K_in, int K, int V,
+                                           gdn_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || K_in != 128 || K != 64 || V != 128 || dtype != GDN_BF16)
+        return 0;
+    if ((long long)B * H > 0x7fffffffLL) return 0;
+    return gdn::gathered_layout(B, T, H).total;
+}
+
+int gdn_prefill_gathered(const void *q_full, const void *k_full, const int *idx, int K_in,
+                         const void *v, const float *alpha, const float *beta, const float *S0,
+                         void *o, float *S_T, int B, int T, int H, int K, int V, gdn_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || T < 0 || H < 0 || K <= 0 || V <= 0 || K_in <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 || K_in != 128 || K != 64 || V != 128) return GDN_ERR_UNSUPPORTED;
+    if (!o && !S_T) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q_full || !k_full || !idx || !v || !alpha || !beta)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q_full, k_full, idx, v, alpha, beta, S0, o, S_T, workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    if ((long long)B * H == 0) return GDN_OK;
+    if ((long long)B * H > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
+    const size_t need = gdn_prefill_gathered_workspace_size(B, T, H, K_in, K, V, dtype);
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    return from_cuda(gdn::launch_prefill_gathered(q_full, k_full, idx, v, alpha, beta, S0, o, S_T,
+                                                  B, T, H, workspace, workspace_bytes, st));
+}
+
 int gdn_decode_step(const void *q, const void *k, const void *v, const float *alpha,
                     const float *beta, float *S, void *o, int B, int H, int K, int V,
                     gdn_dtype dtype, void *stream) {

@@ -73,6 +73,18 @@ SegShape segment_shape(int BH, int T, int K, int nsm);
 size_t prefill_prep_offset(const SegShape &sh);
 size_t prefill_prep_bytes(long long BH, int T);
 
+// The two-pass prefill from full-width q/k (K_in = 128) on a state pruned to
+// 64 channels: the pruning prologue runs inside the key-side pass.  Workspace
+// byte offsets of its parts (segment slots first, at 0).
+struct GatheredLayout {
+    size_t prep, qg, kg, total;
+};
+GatheredLayout gathered_layout(int B, int T, int H);
+cudaError_t launch_prefill_gathered(const void *q_full, const void *k_full, const int *idx,
+                                    const void *v, const float *alpha, const float *beta,
+                                    const float *S0, void *o, float *ST, int B, int T, int H,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 // Pruning prologue: gather K_out of K_in channels per head and L2-normalise.
 cudaError_t launch_gather_normalize(const void *x, const int *idx, void *y, long long rows,
                                     int H, int Kin, int Kout, gdn_dtype dt, float eps,

@@ -498,13 +498,24 @@ constexpr int kPrepCtasPerSm = 4;
 // four CTAs of dynamic + 1 KB static + 1 KB reserved shared memory per SM
 static_assert(kPrepCtasPerSm * (PrepLayout<128>::SMEM + 2048) <= 233472, "prep residency");
 
-template <int K>
+// The pruning prologue inside the key-side pass (GATHER): the q/k boxes are
+// the full 128-channel rows, the kernel keeps channels idx[h, :] of each row
+// and renormalises them over the kept channels, feeds the gathered [K';Q'] to
+// its own products and writes q', k' ([B, T, H, 64] bf16) for the state pass.
+struct PrepGather {
+    const int *idx;      // [H, 64] kept channels of each head
+    __nv_bfloat16 *qg;   // [B, T, H, 64] gathered, renormalised q
+    __nv_bfloat16 *kg;   // [B, T, H, 64] gathered, renormalised k
+};
+
+template <int K, bool GATHER>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     prefill_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ alpha,
                         const float *__restrict__ beta, uint8_t *__restrict__ prep, int T, int Ts,
-                        int H, long long nchunk_all, int *status) {
-    using L = PrepLayout<K>;
+                        int H, long long nchunk_all, PrepGather gth, int *status) {
+    static_assert(!GATHER || K == 64, "the gathering form keeps 64 of 128 channels");
+    using L = PrepLayout<GATHER ? 128 : K>;  // the q/k stage holds the boxes as loaded
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the swizzle atoms and operand descriptors need a 1024-byte aligned
     // base; the declaration provides it and the kernel checks it
@@ -552,7 +563,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         mbar_arrive_expect_tx(&kq_full, L::KQ_BYTES);
         tma_load_4d(sm + L::KC0, &tm_k, &kq_full, 0, h, n * 64, b);
         tma_load_4d(sm + L::QC0, &tm_q, &kq_full, 0, h, n * 64, b);
-        if (K == 128) {
+        if (K == 128 || GATHER) {  // the gathering form loads the full 128 channels
             tma_load_4d(sm + L::KC1, &tm_k, &kq_full, 64, h, n * 64, b);
             tma_load_4d(sm + L::QC1, &tm_q, &kq_full, 64, h, n * 64, b);
         }
@@ -596,15 +607,79 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         const int n = (int)(j % nch);
         const int nvalid = min(64, T - n * 64);
         bool ok = true;
-        if (tid == 0) {
-            ok = wait(&kq_full, it & 1);
-            if (ok) {
+        if constexpr (GATHER) {
+            if (tid == 0) ok = wait(&kq_full, it & 1);
+            if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
+            // eight lanes per row, eight kept channels per lane (channels
+            // 8 cl .. 8 cl + 7 of idx[h]), four rows per warp pass: warp w owns
+            // rows 32 w .. 32 w + 31 of [K'; Q'] (K tokens, then Q tokens).  The
+            // sum of squares runs in the standalone prologue's order (eight
+            // channels per lane, then the lanes 4, 2, 1 apart), so the rows are
+            // bit-identical to gdn_gather_normalize
+            const long long seq = j / nch;
+            const int h = (int)(seq % H), b = (int)(seq / H);
+            const int sub = lane >> 3, cl = lane & 7;
+            const int4 *ip = reinterpret_cast<const int4 *>(gth.idx + (size_t)h * 64) + 2 * cl;
+            const int4 i0 = __ldg(ip), i1 = __ldg(ip + 1);
+            const int cs[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+            bool bad = false;
+            uint8_t *tile = sm + L::AF;  // [K';Q'] in the A scratch, read before A is written
+#pragma unroll 1
+            for (int pass = 0; pass < 8; ++pass) {
+                const int r = 32 * warp + 4 * pass + sub;  // row of [K'; Q']
+                const int t = r & 63;
+                const uint8_t *src = sm + (r < 64 ? L::KC0 : L::QC0);  // channels 64..127: +16 KB
+                float gv[8], ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = cs[e];
+                    float x = 0.f;
+                    if ((unsigned)c < 128u) {
+                        const int cc = c & 63;
+                        x = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                            src + (c >> 6) * 16384 + swz128(t, cc >> 3) + (cc & 7) * 2));
+                    } else {
+                        bad = true;
+                    }
+                    gv[e] = x;
+                    ss = fmaf(x, x, ss);
+                }
+#pragma unroll
+                for (int off = 4; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+                uint4 w;
+                w.x = pack_bf16(gv[0] * inv, gv[1] * inv);
+                w.y = pack_bf16(gv[2] * inv, gv[3] * inv);
+                w.z = pack_bf16(gv[4] * inv, gv[5] * inv);
+                w.w = pack_bf16(gv[6] * inv, gv[7] * inv);
+                *reinterpret_cast<uint4 *>(tile + swz128(r, cl)) = w;
+                if (t < nvalid)
+                    reinterpret_cast<uint4 *>((r < 64 ? gth.kg : gth.qg) +
+                                              (((size_t)b * T + (size_t)n * 64 + t) * H + h) * 64)[cl] =
+                        w;
+            }
+            if (bad && status) atomicOr(status, kStatusBounds);
+            // the tile feeds the product; the stage's reads precede its reload
+            fence_proxy_async_smem();
+            named_sync(kBarKey, kPrepThreads);
+            if (tid == 0) {
+                if (j + G < nchunk_all) load_kq(j + G);
                 tc_fence_after();
-                issue_kq_kt<K>(tb, smem_u32(sm), L::KC0, L::KC1);
+                issue_kq_kt<K>(tb, smem_u32(sm) + L::AF, 0, 0);
                 mma_commit(&bar_p1);
                 ok = wait(&bar_p1, it & 1);
-                // the product has read the stage: the next chunk's boxes may land
-                if (ok && j + G < nchunk_all) load_kq(j + G);
+            }
+        } else {
+            if (tid == 0) {
+                ok = wait(&kq_full, it & 1);
+                if (ok) {
+                    tc_fence_after();
+                    issue_kq_kt<K>(tb, smem_u32(sm), L::KC0, L::KC1);
+                    mma_commit(&bar_p1);
+                    ok = wait(&bar_p1, it & 1);
+                    // the product has read the stage: the next chunk's boxes may land
+                    if (ok && j + G < nchunk_all) load_kq(j + G);
+                }
             }
         }
         if (warp == 1) {
@@ -1816,17 +1891,18 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
     }
 }
 
-template <int K>
+template <int K, bool GATHER = false>
 cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const float *alpha,
                         const float *beta, uint8_t *prep, long long BH, int T, int Ts, int H,
-                        cudaStream_t stream) {
-    auto kern = prefill_prep_kernel<K>;
+                        cudaStream_t stream, PrepGather gth = PrepGather{nullptr, nullptr, nullptr}) {
+    auto kern = prefill_prep_kernel<K, GATHER>;
+    using L = PrepLayout<GATHER ? 128 : K>;
     static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (attr_set[dev] != context_key()) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)PrepLayout<K>::SMEM);
+                                             (int)L::SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
@@ -1836,8 +1912,8 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
     // persistent CTAs, kPrepCtasPerSm per SM (the loop is correct for any residency)
     const long long total = BH * ((T + 63) / 64);
     const long long grid = std::min<long long>(total, (long long)kPrepCtasPerSm * sm_count());
-    kern<<<(unsigned)grid, kPrepThreads, PrepLayout<K>::SMEM, stream>>>(
-        mq, mk, alpha, beta, prep, T, Ts, H, total, device_status_ptr());
+    kern<<<(unsigned)grid, kPrepThreads, L::SMEM, stream>>>(mq, mk, alpha, beta, prep, T, Ts, H,
+                                                           total, gth, device_status_ptr());
     return cudaGetLastError();
 }
 
@@ -1957,6 +2033,50 @@ size_t prefill_prep_offset(const SegShape &sh) {
 }
 size_t prefill_prep_bytes(long long BH, int T) {
     return (size_t)BH * (size_t)((T + 63) / 64) * kPrepChunkBytes;
+}
+
+// Workspace of the gathering prefill: segment slots, every chunk's key-side
+// operands, then the gathered q' and k' ([B, T, H, 64] bf16 each).
+GatheredLayout gathered_layout(int B, int T, int H) {
+    GatheredLayout g{};
+    const SegShape sh = segment_shape(B * H, T, 64, sm_count());
+    g.prep = prefill_prep_offset(sh);
+    const size_t tok = (size_t)B * T * H * 64 * sizeof(__nv_bfloat16);
+    g.qg = (g.prep + prefill_prep_bytes((long long)B * H, T) + 255) & ~size_t(255);
+    g.kg = (g.qg + tok + 255) & ~size_t(255);
+    g.total = g.kg + tok;
+    return g;
+}
+
+cudaError_t launch_prefill_gathered(const void *q_full, const void *k_full, const int *idx,
+                                    const void *v, const float *alpha, const float *beta,
+                                    const float *S0, void *o, float *ST, int B, int T, int H,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const GatheredLayout g = gathered_layout(B, T, H);
+    if (!workspace || workspace_bytes < g.total) return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto *qg = reinterpret_cast<__nv_bfloat16 *>(ws + g.qg);
+    auto *kg = reinterpret_cast<__nv_bfloat16 *>(ws + g.kg);
+    CUtensorMap mqf, mkf, mq, mk, mv, mo;
+    if (!make_token_map(&mqf, q_full, B, T, T, H, 128) ||
+        !make_token_map(&mkf, k_full, B, T, T, H, 128) || !make_token_map(&mq, qg, B, T, T, H, 64) ||
+        !make_token_map(&mk, kg, B, T, T, H, 64) || !make_token_map(&mv, v, B, T, T, H, 128))
+        return cudaErrorInvalidValue;
+    if (o) {
+        if (!make_token_map(&mo, o, B, T, T, H, 128)) return cudaErrorInvalidValue;
+    } else {
+        mo = mv;
+    }
+    const long long BH = (long long)B * H;
+    const SegShape sh = segment_shape(B * H, T, 64, sm_count());
+    if (BH * (2 * sh.nseg - 1) > 0x7fffffffLL || (sh.nseg > 1 && BH > 65535))
+        return cudaErrorInvalidConfiguration;
+    uint8_t *prep = ws + g.prep;
+    cudaError_t e = launch_prep<64, true>(mqf, mkf, alpha, beta, prep, BH, T, T, H, stream,
+                                          PrepGather{idx, qg, kg});
+    if (e != cudaSuccess) return e;
+    return run_tc<64>(mq, mk, mv, mo, alpha, beta, S0, o, ST, BH, T, T, H, sh,
+                      reinterpret_cast<float *>(ws), prep, stream);
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,

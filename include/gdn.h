@@ -147,6 +147,38 @@ GDN_API int gdn_prefill_noalloc(const void *q, const void *k, const void *v, con
 GDN_API size_t gdn_prefill_noalloc_max_workspace(void);
 
 /*
+ * gdn_prefill_gathered -- gdn_prefill on a channel-pruned state, from the
+ * full-width q and k: the pruning prologue (the formula of
+ * gdn_gather_normalize, below) runs inside the key-side pass of the two-pass
+ * prefill, which loads the full-width q/k rows, keeps and renormalises
+ * channels idx[h, :] on chip for its own products, and leaves the gathered
+ * q', k' in the workspace for the state pass; there is no separate pass over
+ * q and k ("On State Reduction" notes, Sec. 2.6 and Alg. 1: pruning is
+ * deployed as a gather on the projection path).
+ *
+ *   q_full, k_full [B, T, H, K_in] bf16, K_in = 128
+ *   idx            [H, K] int32 kept channels in [0, K_in), K = 64
+ *   v, alpha, beta, S0, o, S_T: as for gdn_prefill with K = 64, V = 128
+ *   workspace      >= gdn_prefill_gathered_workspace_size(B, T, H, K_in, K, V,
+ *                  dtype) bytes, 16-byte aligned, caller-owned device memory
+ *
+ * Results are bit-identical to gdn_gather_normalize on q and k followed by
+ * gdn_prefill with its two-pass workspace.  Other (K_in, K, V) or float32
+ * return GDN_ERR_UNSUPPORTED; a missing or short workspace GDN_ERR_WORKSPACE.
+ * An index outside [0, K_in) is not read: it contributes 0 and sets the
+ * GDN_ERR_DEVICE_BOUNDS device status.
+ */
+GDN_API int gdn_prefill_gathered(const void *q_full, const void *k_full, const int *idx, int K_in,
+                                 const void *v, const float *alpha, const float *beta,
+                                 const float *S0, void *o, float *S_T, int B, int T, int H, int K,
+                                 int V, gdn_dtype dtype, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/* Workspace bytes of gdn_prefill_gathered (0 for an unsupported shape). */
+GDN_API size_t gdn_prefill_gathered_workspace_size(int B, int T, int H, int K_in, int K, int V,
+                                                   gdn_dtype dtype);
+
+/*
  * gdn_decode_step -- one token of the recurrence for every (b, h), with the
  * state updated in place:
  *

@@ -132,6 +132,37 @@ def test_two_pass_workspace_query(lib):
     assert two(8, 4096, 16, 96, 128, binding.GDN_BF16) == 0
 
 
+def test_gathered_prefill_workspace_and_validation(lib):
+    size = binding.gdn_prefill_gathered_workspace_size
+    bf = binding.GDN_BF16
+    # key-side operands (24 KiB per chunk), then q' and k' (bf16, 64 channels)
+    tok = 8 * 4096 * 16 * 64 * 2
+    assert size(8, 4096, 16, 128, 64, 128, bf) == 8 * 16 * 64 * 24576 + 2 * tok
+    # only full width 128 -> 64 kept channels at V = 128, bf16
+    for args in ((8, 4096, 16, 96, 64, 128, bf), (8, 4096, 16, 128, 32, 128, bf),
+                 (8, 4096, 16, 128, 64, 64, bf), (8, 4096, 16, 128, 64, 128, binding.GDN_FP32),
+                 (0, 4096, 16, 128, 64, 128, bf)):
+        assert size(*args) == 0
+    f = lib.gdn_prefill_gathered
+    dummy = 0x10000  # never dereferenced: every check below returns before a launch
+    common = (dummy, dummy, dummy, 128, dummy, dummy, dummy, None, dummy, dummy)
+    # unsupported widths / dtype
+    assert f(dummy, dummy, dummy, 96, dummy, dummy, dummy, None, dummy, dummy, 2, 64, 3, 64, 128,
+             bf, None, 0, None) == binding.GDN_ERR_UNSUPPORTED
+    assert f(*common, 2, 64, 3, 64, 128, binding.GDN_FP32, None, 0, None) == \
+        binding.GDN_ERR_UNSUPPORTED
+    # neither output
+    assert f(dummy, dummy, dummy, 128, dummy, dummy, dummy, None, None, None, 2, 64, 3, 64, 128,
+             bf, None, 0, None) == binding.GDN_ERR_INVALID_ARG
+    # misaligned index pointer
+    assert f(dummy, dummy, dummy + 4, 128, dummy, dummy, dummy, None, dummy, dummy, 2, 64, 3, 64,
+             128, bf, None, 0, None) == binding.GDN_ERR_ALIGNMENT
+    # missing or short workspace
+    assert f(*common, 2, 64, 3, 64, 128, bf, None, 0, None) == binding.GDN_ERR_WORKSPACE
+    need = size(2, 64, 3, 128, 64, 128, bf)
+    assert f(*common, 2, 64, 3, 64, 128, bf, dummy, need - 16, None) == binding.GDN_ERR_WORKSPACE
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.gdn_selftest_wait_timeout(0, None) == binding.GDN_ERR_INVALID_ARG
     assert lib.gdn_selftest_wait_timeout(1 << 40, None) == binding.GDN_ERR_INVALID_ARG
