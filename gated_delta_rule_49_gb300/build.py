@@ -20,6 +20,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
+# the debug variant: device-side index and coordinate checks in the prefill
+# kernels (-DGDN_BOUNDS_CHECK), same C ABI
+BUILD_BOUNDS = os.path.join(PKG, "_build_bounds")
+LIB_BOUNDS = os.path.join(PKG, "libgdn_bounds.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,18 +44,24 @@ def _newest_header() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          bounds_check: bool = False) -> str:
+    """Build libgdn.so (or, with bounds_check, libgdn_bounds.so: the same
+    library with the device-side index checks of the debug build)."""
+    bdir, lib = (BUILD_BOUNDS, LIB_BOUNDS) if bounds_check else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr = _newest_header()
     jobs = []
     objs = []
     for s in srcs:
-        obj = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(s)[:-3] + ".o")
         objs.append(obj)
         if force or ptxas_info or not os.path.exists(obj) or \
                 os.path.getmtime(obj) < max(os.path.getmtime(s), hdr):
             extra = ["-Xptxas", "-v"] if ptxas_info else []
+            if bounds_check:
+                extra.append("-DGDN_BOUNDS_CHECK")
             jobs.append([nvcc(), *_flags(extra), "-c", s, "-o", obj])
 
     def run(cmd):
@@ -67,13 +77,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    if jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(map(os.path.getmtime, objs)):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if jobs or not os.path.exists(lib) or os.path.getmtime(lib) < max(map(os.path.getmtime, objs)):
+        tmp = lib + f".tmp{os.getpid()}"
         subprocess.check_call([nvcc(), "-shared", *ARCH, "-o", tmp, *objs, "-lcuda"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                bounds_check="--bounds-check" in sys.argv))

@@ -23,6 +23,23 @@ enum : int {
 // Chunk length of the chunkwise prefill.
 constexpr int kChunk = 64;
 
+// Debug builds (-DGDN_BOUNDS_CHECK) check the indices and coordinates the
+// prefill kernels derive (segment ranges, TMA box coordinates, key-side block
+// offsets, gate and gathered-row offsets) before using them: a failed check
+// sets the bounds bit of the device status and the access is skipped (a
+// skipped load then leaves its bounded wait to run out, so the call ends with
+// the timeout bit as well).  Release builds compile every check away.
+__device__ __forceinline__ bool bounds_ok(bool cond, int *status) {
+#ifdef GDN_BOUNDS_CHECK
+    if (!cond && status) atomicOr(status, kStatusBounds);
+    return cond;
+#else
+    (void)cond;
+    (void)status;
+    return true;
+#endif
+}
+
 // Address of the current device's status word (nullptr if the symbol lookup
 // failed).  Kernels OR their bits into it.
 int *device_status_ptr();

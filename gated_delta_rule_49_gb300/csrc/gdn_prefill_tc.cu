@@ -557,6 +557,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     float *bet = G2 + 128;
 
     auto load_kq = [&](long long j) {
+        if (!bounds_ok(j >= 0 && j < nchunk_all, status)) return;
         const long long seq = j / nch;
         const int n = (int)(j - seq * nch);
         const int b = (int)(seq / H), h = (int)(seq % H);
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     };
     float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
     auto prefetch_gates = [&](long long j) {
-        if (warp == 1 && j < nchunk_all) {
+        if (warp == 1 && j < nchunk_all && bounds_ok(T <= Ts, status)) {
             const long long seq = j / nch;
             const int n = (int)(j - seq * nch);
             const int b = (int)(seq / H), h = (int)(seq % H);
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
                 w.z = pack_bf16(gv[4] * inv, gv[5] * inv);
                 w.w = pack_bf16(gv[6] * inv, gv[7] * inv);
                 *reinterpret_cast<uint4 *>(tile + swz128(r, cl)) = w;
-                if (t < nvalid)
+                if (t < nvalid && bounds_ok(seq < nchunk_all / nch && n * 64 + t < T, status))
                     reinterpret_cast<uint4 *>((r < 64 ? gth.kg : gth.qg) +
                                               (((size_t)b * T + (size_t)n * 64 + t) * H + h) * 64)[cl] =
                         w;
@@ -820,6 +821,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const SegTask tk = segment_task(plan, K, T, S0, ST, BH);
+    // (every thread takes the same branch, before any barrier or allocation)
+    if (!bounds_ok(tk.seq < (size_t)BH && tk.t0 >= 0 && tk.t0 < tk.t1 && tk.t1 <= T &&
+                       tk.t0 % 64 == 0 && T <= Ts,
+                   status))
+        return;
     const size_t seq = tk.seq;
     const int t0 = tk.t0, t1 = tk.t1;
     const bool zero_v = tk.zero_v;
@@ -961,6 +967,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_desc(&tm_v);
             if (outs) tma_prefetch_desc(&tm_o);
             auto load_kq = [&](int n) {
+                if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
                 const int st = n % L::NSTAGE;
                 uint8_t *stg = sm + st * L::STAGE;
                 mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
@@ -972,6 +979,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             };
             auto load_v = [&](int n) {
+                if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
                 uint64_t *bar = &v_full[n % L::NV];
                 uint8_t *dst = sm + L::vbuf(n);
                 mbar_arrive_expect_tx(bar, L::V_BYTES);
@@ -980,11 +988,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             // chunk n's [T'^T | T''^T] into ring stage n % 2, P into its own ring
             auto load_tt = [&](int n) {
+                if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
                 mbar_arrive_expect_tx(&tt_full[n & 1], 16384);
                 bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepTP, 16384,
                           &tt_full[n & 1]);
             };
             auto load_p = [&](int n) {
+                if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
                 mbar_arrive_expect_tx(&p_full[n & 1], 8192);
                 bulk_load(sm + L::ptile(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepP, 8192,
                           &p_full[n & 1]);
@@ -1138,8 +1148,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             named_sync(kBarOut2, 160);  // the tile is written
             if (sw == 3 && lane == 0) {
-                tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
-                tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
+                if (bounds_ok(m >= 0 && m < nchunks, status)) {
+                    tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
+                    tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
+                }
                 bulk_commit_group();
             }
             return true;
@@ -1365,6 +1377,11 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const SegTask tk = segment_task(plan, K, T, S0, ST, BH);
+    // (every thread takes the same branch, before any barrier or allocation)
+    if (!bounds_ok(tk.seq < (size_t)BH && tk.t0 >= 0 && tk.t0 < tk.t1 && tk.t1 <= T &&
+                       tk.t0 % 64 == 0 && T <= Ts,
+                   status))
+        return;
     const size_t seq = tk.seq;
     const int t0 = tk.t0, t1 = tk.t1;
     const bool zero_v = tk.zero_v;
@@ -1400,6 +1417,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     float *sg = reinterpret_cast<float *>(sm + L::SGATE);
 
     auto load_kq = [&](int n) {
+        if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
         const int st = n % L::NSTAGE;
         uint8_t *stg = sm + st * L::STAGE;
         mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
@@ -1411,6 +1429,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         }
     };
     auto load_v = [&](int n) {
+        if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
         uint64_t *bar = &v_full[n & 1];
         uint8_t *dst = sm + L::vbuf(n);
         mbar_arrive_expect_tx(bar, L::V_BYTES);
@@ -1659,8 +1678,10 @@ __global__ void __launch_bounds__(kFuThreads, 1)
             }
             named_sync(kBarOut2, 160);  // the tile is written
             if (sw == 3 && lane == 0) {
-                tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
-                tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
+                if (bounds_ok(m >= 0 && m < nchunks, status)) {
+                    tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
+                    tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
+                }
                 bulk_commit_group();
             }
             return true;

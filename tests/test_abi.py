@@ -307,3 +307,14 @@ def test_host_prefill_rejects_bad_arguments(lib):
     assert call(wsb=need - 1) == binding.GDN_ERR_WORKSPACE
     assert call(ws=F + 8) == binding.GDN_ERR_ALIGNMENT
     assert call(B=0) == binding.GDN_OK
+
+
+def test_bounds_check_variant_builds_and_exports():
+    """The debug variant (-DGDN_BOUNDS_CHECK) compiles from the same sources and
+    exports the same C ABI."""
+    import ctypes
+    from gated_delta_rule_49_gb300 import build
+    path = build.build(bounds_check=True)
+    dbg = ctypes.CDLL(path)
+    for name in binding.EXPORTS:
+        assert hasattr(dbg, name), name
