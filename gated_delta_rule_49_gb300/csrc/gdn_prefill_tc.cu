@@ -728,8 +728,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 //       spent T'/T'' slot (no products, no loads).
 //   issuer (warp 7, one thread): every TMA load, and the products that are
 //       not on the state chain -- O^T(n) = S(n-1) (gamma Q(n))^T, and
-//       W^T(n+1) = K^T T'^T, U~^T(n+1) = V^T T''^T -- issued in chunk n's
-//       epilogue window, while the tensor pipe would otherwise idle (an SM
+//       W^T(n+1) = K^T T'^T, U~^T(n+1) = V^T T''^T (first: the chain waits
+//       for them) -- issued in chunk n's epilogue window, while the tensor
+//       pipe would otherwise idle (an SM
 //       issues tcgen05 products one at a time, ~44 cycles each, so products
 //       issued beside the chain's would delay them).
 //   state group (warps 8-15): the state chain
@@ -1033,6 +1034,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // the key group is done with chunk n: gamma Q(n) is in place and
                 // W^T(n) has been read out (its columns take W^T(n+1) below)
                 ok = ok && wait(&key_ready[n & 1], (n >> 1) & 1);
+                // the next chunk's W^T and U~^T first: the state chain waits for
+                // them (through the key group's -W^T) at the end of this chunk,
+                // while the S-term below is needed only after the epilogue
+                if (ok && n + 1 < nchunks) ok = issue_wu(n + 1);
                 if (ok && outs) {
                     // O^T(n) = S(n-1) (gamma Q(n))^T
                     {
@@ -1048,7 +1053,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mma_commit(&bar_os);
                     }
                 }
-                if (ok && n + 1 < nchunks) ok = issue_wu(n + 1);
                 if (!ok) break;
                 // bar_u(n) also covers dS(n - 1) and O^T(n - 1) += U^T P^T (the
                 // state thread's earlier products), and the previous S-term was
