@@ -68,11 +68,12 @@ constexpr int kBarKey = 1, kBarState = 2;       // named barrier ids
 constexpr long long kSpinLimit = 2000000000LL;  // ~1 s of SM clocks per wait
 constexpr int kLD = 68;                         // row stride of the fp32 64 x 64 matrix
 
-// Bytes of one chunk's key-side operands in the two-pass form: T'^T, T''^T
-// and P, each a 64 x 64 bf16 tile stored as its 128-byte-swizzled
-// shared-memory image.
-constexpr uint32_t kPrepTP = 0, kPrepTPP = 8192, kPrepP = 16384;
-constexpr uint32_t kPrepChunkBytes = 24576;
+// Bytes of one chunk's key-side operands in the two-pass form: T'^T and
+// T''^T, each a 64 x 64 bf16 tile stored as its 128-byte-swizzled
+// shared-memory image.  (P, which needs q, is formed in the state pass from
+// the q/k boxes it loads anyway.)
+constexpr uint32_t kPrepTP = 0, kPrepTPP = 8192;
+constexpr uint32_t kPrepChunkBytes = 16384;
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
@@ -164,6 +165,45 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 bf16 matrices from shared memory; lane l gives the address of
+// row l % 8 of matrix l / 8 and receives row l / 4, columns 2 (l % 4), +1 of
+// each, in register order.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// One 16 x 16 block of P = (Q K^T) for rows t in [16 i, +16) and columns s in
+// [16 j, +16) of a chunk, from its q and k boxes (64 tokens x 64 channels,
+// 128-byte swizzled; q1 / k1 hold channels 64..127 when K = 128), as two
+// 16 x 8 accumulator tiles of m16n8k16: d[nt] holds rows g, g + 8 and columns
+// 8 nt + 2 t4, +1 (g = lane / 4, t4 = lane % 4).
+template <int K>
+__device__ __forceinline__ void qk_block(uint32_t q0, uint32_t q1, uint32_t k0, uint32_t k1,
+                                         int i, int j, int lane, float (&d)[2][4]) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
+    const uint32_t r = lane & 7, mtx = lane >> 3;
+    // A: matrices (rows +0, k +0), (rows +8, k +0), (rows +0, k +8), (rows +8, k +8)
+    const uint32_t arow = 16 * i + r + 8 * (mtx & 1), achunk = mtx >> 1;
+    // B: (s +0, k +0), (s +0, k +8), (s +8, k +0), (s +8, k +8)
+    const uint32_t brow = 16 * j + r + 8 * (mtx >> 1), bchunk = mtx & 1;
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint32_t qb = ks < 4 ? q0 : q1, kb = ks < 4 ? k0 : k1;
+        const uint32_t c = 2 * (ks & 3);
+        uint32_t a[4], bb[4];
+        ldsm_x4(a, qb + swz128(arow, c + achunk));
+        ldsm_x4(bb, kb + swz128(brow, c + bchunk));
+        mma_16816(d[0], a, bb[0], bb[1]);
+        mma_16816(d[1], a, bb[2], bb[3]);
+    }
 }
 
 // The three terms of A B with split operands (lo*hi, hi*lo, hi*hi) go to
@@ -402,6 +442,47 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
     }
 }
 
+// Block (i, j) of P from its product d (qk_block's layout) as bf16 pairs,
+//   P_ts = 2^(G_t - G_s) (q_t . k_s) for s <= t, else 0
+// (chunk_ap's P entries): w[nt][hr] holds t = 16 i + g + 8 hr and
+// s = 16 j + 8 nt + 2 t4, +1 (g = lane / 4, t4 = lane % 4).
+__device__ __forceinline__ void p_block_pack(const float (&d)[2][4], int i, int j, int lane,
+                                             const float *G2, uint32_t (&w)[2][2]) {
+    const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int t = 16 * i + g + 8 * hr;
+        const float gt = G2[t];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int s = 16 * j + 8 * nt + 2 * t4;
+            const float2 gs = *reinterpret_cast<const float2 *>(G2 + s);
+            const float x0 = s <= t ? decay_exp2(gt - gs.x) * d[nt][2 * hr] : 0.f;
+            const float x1 = s + 1 <= t ? decay_exp2(gt - gs.y) * d[nt][2 * hr + 1] : 0.f;
+            w[nt][hr] = pack_bf16(x0, x1);
+        }
+    }
+}
+// ... into the 128-byte-swizzled P tile (row t, s along the row)
+__device__ __forceinline__ void p_block_store(uint8_t *tile, const uint32_t (&w)[2][2], int i,
+                                              int j, int lane) {
+    const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+            *reinterpret_cast<uint32_t *>(tile + swz128(16 * i + g + 8 * hr, 2 * j + nt) +
+                                          4 * t4) = w[nt][hr];
+}
+// The ten blocks of P on or below the diagonal, one per key-group warp (0-6)
+// and a second for warps 0, 2 and 3 (warp 1 also forms the gates): block u
+// is (i, j) = (3,0) (3,1) (3,2) (3,3) (2,0) (2,1) (2,2) (1,0) (1,1) (0,0).
+__device__ __forceinline__ int p_unit_i(int u) { return u < 4 ? 3 : u < 7 ? 2 : u < 9 ? 1 : 0; }
+__device__ __forceinline__ int p_unit_j(int u) { return u < 4 ? u : u < 7 ? u - 4 : u < 9 ? u - 7 : 0; }
+__device__ __forceinline__ int p_extra_unit(int warp) {
+    return warp == 0 ? 7 : warp == 2 ? 8 : warp == 3 ? 9 : -1;
+}
+
 // Which token range, initial state and final-state slot a CTA works on.
 //   kWhole:  CTA = one (b, h) sequence, tokens [0, T), S0 / S_T as given.
 //   kFirst:  long sequences cut into `nseg` segments of `seg_len` tokens; per
@@ -473,16 +554,19 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
 
 // ---------------------------------------------------------------- key-side pass
 // The two-pass form's first kernel.  Everything of a chunk that depends only
-// on its keys, queries and gates -- A, P, the inverse T and T', T'' -- has no
-// dependence on the state, so it runs for all B * H * ceil(T/64) chunks at
-// once instead of in each sequence's serial chunk loop.  Persistent CTAs of
-// 128 threads (four per SM, so that one CTA's loads and waits hide under the
-// others' work) stride over the chunks; each chunk's [K;Q] K^T is one tcgen05
-// product into 64 TMEM columns, the next chunk's q/k boxes load (TMA) while
-// the current one is solved, and T'^T, T''^T and P go to global memory as
-// their swizzled shared-memory images, which the state-side kernel copies in
-// with bulk copies.  Same arithmetic as the fused kernel's key group (the
-// shared helpers above), so both forms give identical results.
+// on its keys and gates -- A, the inverse T and T', T'' -- has no dependence
+// on the state, so it runs for all B * H * ceil(T/64) chunks at once instead
+// of in each sequence's serial chunk loop.  Persistent CTAs of 128 threads
+// (four per SM, so that one CTA's loads and waits hide under the others'
+// work) stride over the chunks; each chunk's K K^T is one tcgen05 product
+// into 64 TMEM columns (the [K;Q] operand of the fused kernel with a zero Q
+// half: q is not read here), the next chunk's k boxes load (TMA) while the
+// current one is solved, and T'^T and T''^T go to global memory as their
+// swizzled shared-memory images, which the state-side kernel copies in with
+// bulk copies.  Same arithmetic as the fused kernel's key group (the shared
+// helpers above), so both forms give identical states.  The gathering form
+// loads the full-width q and k boxes, and writes the gathered q' and k' for
+// the state pass.
 template <int K>
 struct PrepLayout {
     static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
@@ -491,6 +575,7 @@ struct PrepLayout {
     static constexpr uint32_t GATE = AF + 64 * kLD * 4;          // G2, gamma, beta
     static constexpr uint32_t END = GATE + 3 * 64 * 4;
     static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
+    static constexpr uint32_t K_BYTES = (K == 128 ? 2u : 1u) * 8192u;
     static constexpr size_t SMEM = END;
 };
 constexpr int kPrepThreads = 128;
@@ -545,6 +630,13 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         fence_mbar_init();
         abort_flag = 0;
     }
+    if constexpr (!GATHER) {
+        // the product's Q half (rows 64..127 of [K;Q]) stays zero
+        for (int e = tid; e < (K / 64) * 512; e += kPrepThreads)
+            reinterpret_cast<uint4 *>(sm + ((e >> 9) ? L::QC1 : L::QC0))[e & 511] =
+                make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -561,12 +653,13 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         const long long seq = j / nch;
         const int n = (int)(j - seq * nch);
         const int b = (int)(seq / H), h = (int)(seq % H);
-        mbar_arrive_expect_tx(&kq_full, L::KQ_BYTES);
+        // the gathering form loads q and k, both with all 128 channels
+        mbar_arrive_expect_tx(&kq_full, GATHER ? L::KQ_BYTES : L::K_BYTES);
         tma_load_4d(sm + L::KC0, &tm_k, &kq_full, 0, h, n * 64, b);
-        tma_load_4d(sm + L::QC0, &tm_q, &kq_full, 0, h, n * 64, b);
-        if (K == 128 || GATHER) {  // the gathering form loads the full 128 channels
+        if (GATHER) tma_load_4d(sm + L::QC0, &tm_q, &kq_full, 0, h, n * 64, b);
+        if (K == 128 || GATHER) {
             tma_load_4d(sm + L::KC1, &tm_k, &kq_full, 64, h, n * 64, b);
-            tma_load_4d(sm + L::QC1, &tm_q, &kq_full, 64, h, n * 64, b);
+            if (GATHER) tma_load_4d(sm + L::QC1, &tm_q, &kq_full, 64, h, n * 64, b);
         }
     };
     float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
@@ -688,10 +781,10 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
             prefetch_gates(j + G);
         }
         if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
-        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T'^T | T''^T | P]
+        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T'^T | T''^T]
         tc_fence_after();
         for (int ch = 0; ch < 2; ++ch)  // both 32-column halves per thread
-            chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, out + kPrepP);
+            chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, nullptr);
         tc_fence_before();
         named_sync(kBarKey, kPrepThreads);
         chunk_inverse_tprime<kPrepThreads>(AF, bet, gam, out + kPrepTP, out + kPrepTPP, tid);
@@ -721,18 +814,21 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 
 // ---------------------------------------------------------------- state-side pass
 // The two-pass form's second kernel: one CTA per (b, h) sequence (or segment)
-// walks its chunks like the fused kernel, but loads T'^T, T''^T and P
-// instead of solving for them.  Three roles:
-//   key group (warps 0-6): per chunk the gates, the state group's decay
-//       factors, gamma folded into the Q box, and -W^T from TMEM into the
-//       spent T'/T'' slot (no products, no loads).
-//   issuer (warp 7, one thread): every TMA load, and the products that are
-//       not on the state chain -- O^T(n) = S(n-1) (gamma Q(n))^T, and
-//       W^T(n+1) = K^T T'^T, U~^T(n+1) = V^T T''^T (first: the chain waits
-//       for them) -- issued in chunk n's epilogue window, while the tensor
-//       pipe would otherwise idle (an SM
-//       issues tcgen05 products one at a time, ~44 cycles each, so products
-//       issued beside the chain's would delay them).
+// walks its chunks like the fused kernel, but loads T'^T and T''^T instead
+// of solving for them.  Three roles:
+//   key group (warps 0-6): per chunk P = (Q K^T masked, times the decays)
+//       with warp-level MMAs from the raw q/k boxes (the group is otherwise
+//       idle for most of a chunk, and forming P here saves the key-side pass
+//       its q read and P's trip through memory), the gates, the state
+//       group's decay factors, gamma folded into the Q box, and -W^T from
+//       TMEM into the spent T'/T'' slot (no tensor-memory products, no loads).
+//   issuer (warp 7, one thread): every TMA load, and the products off the
+//       state chain -- O^T(n) = S(n-1) (gamma Q(n))^T once the state thread
+//       has issued U(n), then W^T(n+1) = K^T T'^T and U~^T(n+1) = V^T T''^T
+//       once U(n) is complete -- while the chain's epilogue leaves the
+//       tensor pipe idle.  An SM issues tcgen05 products one at a time, ~47
+//       cycles each, so the chain's own products are never issued beside
+//       these.
 //   state group (warps 8-15): the state chain
 //       U^T(n)  = U~^T(n) + S(n-1) (-W^T(n))       (issued at the end of n - 1)
 //       epilogue: U^T -> bf16, U^T diag(decay) -> bf16, in the U slot
@@ -746,34 +842,41 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 // every earlier product of its thread, so bar_u(n) (the state thread's
 // commit after U(n)) also says that dS(n-1) and O^T(n-1) += U^T P^T are
 // complete: the issuer reloads and reuses slots only after it.  The state
-// update waits for the issuer's O^T(n) S-term (bar_os), which reads S(n-1);
-// the issuer writes W^T(n+1) only after the key group has read W^T(n).
+// thread waits for the S-term (bar_os), which reads S(n-1), before its
+// O^T(n) += U^T P^T and the update; the issuer writes W^T(n+1) only after
+// the key group has read W^T(n).
+// The key group writes P(n) before it signals key_ready(n), once W^T(n) is
+// complete (so U(n - 1), and O^T(n - 2) += U^T P^T before it, which read the
+// slot).
 // Every mbarrier wait is for the barrier's latest phase: the next phase needs
 // a step that the waiting thread takes after the wait.  Rings: q/k (three
 // stages), V, [T'^T | T''^T] (then -W^T), P, U and O (two each); the loads of
-// chunk n + 2 (P: n + 1) go out in chunk n's window.  Every state quantity is
-// the fused kernel's arithmetic on the same operands, so S_T is bit-identical
-// to it (o agrees to the accumulation order of the transposed product).
+// chunk n + 2 go out in chunk n's window.  Every state quantity is the fused
+// kernel's arithmetic on the same operands, so S_T is bit-identical to it (o
+// agrees to the accumulation orders of P and of the transposed product).
 
+// Rings: K and Q (three slots each), V, [T'^T | T''^T] / -W^T and P (two
+// each).  Each K / Q slot holds the 64-channel boxes of one chunk side by
+// side (channels 64..127 at +8 KB when K = 128).
 template <int K>
 struct StLayout {
-    static constexpr int NSTAGE = 3;                             // q/k ring
-    static constexpr int NV = 2;                                 // V ring
-    static constexpr uint32_t KC0 = 0, KC1 = 8192;               // K blocks (KC1: K = 128)
-    static constexpr uint32_t QC0 = K == 128 ? 16384 : 8192, QC1 = QC0 + 8192;
-    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;
-    static constexpr uint32_t VB = NSTAGE * STAGE;               // V ring, 16 KB per chunk
+    static constexpr int NK = 3, NQ = 3, NV = 2, NT = 2;
+    static constexpr uint32_t BOX = K == 128 ? 16384 : 8192;     // one chunk of k or q
+    static constexpr uint32_t KR = 0;                            // K ring
+    static constexpr uint32_t QR = KR + NK * BOX;                // Q ring
+    static constexpr uint32_t VB = QR + NQ * BOX;                // V ring, 16 KB per chunk
     static constexpr uint32_t PR = VB + NV * 16384;              // ring of [T'^T | T''^T] / -W^T
-    static constexpr uint32_t PP = PR + 2 * 16384;               // ring of P
+    static constexpr uint32_t PP = PR + NT * 16384;              // ring of P
     static constexpr uint32_t OST = PP + 2 * 8192;               // output staging, 2 x 64 x 64
     static constexpr uint32_t KGATE = OST + 16384;               // G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;        // 3 x (decay[64], gamma_C)
     static constexpr uint32_t END = SGATE + 3 * 68 * 4;
-    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr uint32_t V_BYTES = 2u * 8192u;
     static constexpr size_t SMEM = END;
     static_assert(SMEM + 1024 <= 232448, "shared memory budget");
-    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n & 1) * 16384; }
+    static __device__ __forceinline__ uint32_t kbuf(int n) { return KR + (n % NK) * BOX; }
+    static __device__ __forceinline__ uint32_t qbuf(int n) { return QR + (n % NQ) * BOX; }
+    static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n % NT) * 16384; }
     static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
     static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // over T', T''
     static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
@@ -813,8 +916,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t kq_full[3], v_full[2], tt_full[2], p_full[2], key_ready[2], bar_w, bar_u,
-        bar_s, bar_os, bar_o2, drain[2];
+    __shared__ uint64_t k_full[3], q_full[3], v_full[2], tt_full[2], key_ready[2], bar_w, bar_u,
+        bar_s, bar_os, bar_o2, u_sig, drain[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -842,9 +945,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        uint64_t *bars[] = {&kq_full[0], &kq_full[1], &kq_full[2], &v_full[0],    &v_full[1],
-                            &tt_full[0], &tt_full[1], &p_full[0],  &p_full[1],    &key_ready[0],
-                            &key_ready[1], &bar_w,    &bar_u,      &bar_s,        &bar_os,
+        uint64_t *bars[] = {&k_full[0],  &k_full[1],  &k_full[2],  &q_full[0],  &q_full[1],
+                            &q_full[2],  &v_full[0],  &v_full[1],  &tt_full[0], &tt_full[1],
+                            &key_ready[0],
+                            &key_ready[1], &bar_w,    &bar_u,      &bar_s,  &bar_os, &u_sig,
                             &bar_o2,     &drain[0],   &drain[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
@@ -895,13 +999,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         prefetch_gates(0, 0);
         prefetch_gates(1, 1);
+        // P's blocks above the diagonal stay zero in both ring slots
+        if (outs)
+            for (int e = tid; e < 2 * 8192 / 16; e += kStKeyThreads)
+                reinterpret_cast<uint4 *>(sm + L::PP)[e] = make_uint4(0u, 0u, 0u, 0u);
+        const int pu2 = p_extra_unit(warp);
         for (int n = 0; n < nchunks; ++n) {
-            const int st = n % L::NSTAGE;  // q/k stage
             const int p2 = n & 1;
             const int nvalid = min(64, t1 - t0 - n * 64);
             bool ok = true;
-            if (tid == 0) ok = wait(&kq_full[st], (n / L::NSTAGE) & 1);
+            if (tid == 0)
+                ok = wait(&q_full[n % L::NQ], (n / L::NQ) & 1) &&
+                     wait(&k_full[n % L::NK], (n / L::NK) & 1);
             if (named_sync_or(kBarKey, kStKeyThreads, !ok)) { failed = true; break; }
+            // P(n) = (Q K^T) from the raw boxes, before Q is scaled in place
+            float pd[2][2][4];
+            if (outs) {
+                const uint32_t qb = base + L::qbuf(n), kb = base + L::kbuf(n);
+                qk_block<K>(qb, qb + 8192, kb, kb + 8192, p_unit_i(warp), p_unit_j(warp), lane,
+                            pd[0]);
+                if (pu2 >= 0)
+                    qk_block<K>(qb, qb + 8192, kb, kb + 8192, p_unit_i(pu2), p_unit_j(pu2), lane,
+                                pd[1]);
+            }
             if (warp == 1) {
                 if (p2 == 0)
                     chunk_gates(pa[0][0], pa[0][1], pb[0][0], pb[0][1], lane, nvalid, G2, gam, bet);
@@ -910,19 +1030,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 // the state group's decay to the chunk end and gamma_C; slot
                 // n % 3 was last read in the state epilogue of chunk n - 3,
-                // which precedes the load of this chunk's q/k boxes
+                // which precedes U(n - 2) and so the load of this chunk's q box
                 float *slot = sg + (n % 3) * 68;
                 const float gC = G2[63];
                 slot[lane] = exp2f(gC - G2[lane]);
                 slot[lane + 32] = exp2f(gC - G2[lane + 32]);
                 if (lane == 0) slot[64] = exp2f(gC);
             }
-            named_sync(kBarKey, kStKeyThreads);
+            named_sync(kBarKey, kStKeyThreads);  // gates in place; raw Q read
+            uint32_t pw[2][2][2];
+            if (outs) {
+                p_block_pack(pd[0], p_unit_i(warp), p_unit_j(warp), lane, G2, pw[0]);
+                if (pu2 >= 0) p_block_pack(pd[1], p_unit_i(pu2), p_unit_j(pu2), lane, G2, pw[1]);
+            }
             // Q <- diag(gamma) Q in place (next read by the O^T S-term)
-            uint8_t *stq = sm + st * L::STAGE;
             for (int e = tid; e < (K / 64) * 512; e += kStKeyThreads) {
                 const int blk_i = e >> 9, ee = e & 511;
-                uint4 *p = reinterpret_cast<uint4 *>(stq + (blk_i ? L::QC1 : L::QC0) + ee * 16);
+                uint4 *p = reinterpret_cast<uint4 *>(sm + L::qbuf(n) + blk_i * 8192 + ee * 16);
                 const float g = gam[ee >> 3];
                 uint4 w = *p;
                 uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
@@ -936,6 +1060,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (tid == 0) ok = wait(&bar_w, n & 1);  // W^T(n) and U~^T(n) complete
             if (named_sync_or(kBarKey, kStKeyThreads, !ok)) { failed = true; break; }
+            if (outs) {
+                // P slot n % 2 was last read by O^T(n - 2) += U^T P^T, which
+                // the state thread issued before U(n - 1); the issuer waited
+                // for U(n - 1) before W^T(n), whose completion was just seen
+                p_block_store(sm + L::ptile(n), pw[0], p_unit_i(warp), p_unit_j(warp), lane);
+                if (pu2 >= 0) p_block_store(sm + L::ptile(n), pw[1], p_unit_i(pu2), p_unit_j(pu2), lane);
+            }
             if (warp < 4) {
                 // -W^T over T'^T, T''^T (both read by the products above)
                 tc_fence_after();
@@ -967,17 +1098,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             if (outs) tma_prefetch_desc(&tm_o);
-            auto load_kq = [&](int n) {
+            // chunk n's k (q) boxes into K (Q) ring slot n % 3
+            auto load_k = [&](int n) {
                 if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
-                const int st = n % L::NSTAGE;
-                uint8_t *stg = sm + st * L::STAGE;
-                mbar_arrive_expect_tx(&kq_full[st], L::KQ_BYTES);
-                tma_load_4d(stg + L::KC0, &tm_k, &kq_full[st], 0, h, t0 + n * 64, b);
-                tma_load_4d(stg + L::QC0, &tm_q, &kq_full[st], 0, h, t0 + n * 64, b);
-                if (K == 128) {
-                    tma_load_4d(stg + L::KC1, &tm_k, &kq_full[st], 64, h, t0 + n * 64, b);
-                    tma_load_4d(stg + L::QC1, &tm_q, &kq_full[st], 64, h, t0 + n * 64, b);
-                }
+                uint64_t *bar = &k_full[n % L::NK];
+                mbar_arrive_expect_tx(bar, L::BOX);
+                tma_load_4d(sm + L::kbuf(n), &tm_k, bar, 0, h, t0 + n * 64, b);
+                if (K == 128) tma_load_4d(sm + L::kbuf(n) + 8192, &tm_k, bar, 64, h, t0 + n * 64, b);
+            };
+            auto load_q = [&](int n) {
+                if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
+                uint64_t *bar = &q_full[n % L::NQ];
+                mbar_arrive_expect_tx(bar, L::BOX);
+                tma_load_4d(sm + L::qbuf(n), &tm_q, bar, 0, h, t0 + n * 64, b);
+                if (K == 128) tma_load_4d(sm + L::qbuf(n) + 8192, &tm_q, bar, 64, h, t0 + n * 64, b);
             };
             auto load_v = [&](int n) {
                 if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
@@ -987,29 +1121,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tma_load_4d(dst, &tm_v, bar, 0, h, t0 + n * 64, b);
                 tma_load_4d(dst + 8192, &tm_v, bar, 64, h, t0 + n * 64, b);
             };
-            // chunk n's [T'^T | T''^T] into ring stage n % 2, P into its own ring
+            // chunk n's [T'^T | T''^T] into ring slot n % 2
             auto load_tt = [&](int n) {
                 if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
-                mbar_arrive_expect_tx(&tt_full[n & 1], 16384);
+                mbar_arrive_expect_tx(&tt_full[n % L::NT], 16384);
                 bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepTP, 16384,
-                          &tt_full[n & 1]);
-            };
-            auto load_p = [&](int n) {
-                if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
-                mbar_arrive_expect_tx(&p_full[n & 1], 8192);
-                bulk_load(sm + L::ptile(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepP, 8192,
-                          &p_full[n & 1]);
+                          &tt_full[n % L::NT]);
             };
             // W^T(n) = K^T T'^T and U~^T(n) = V^T T''^T (U slot n % 2)
             auto issue_wu = [&](int n) -> bool {
-                if (!wait(&kq_full[n % L::NSTAGE], (n / L::NSTAGE) & 1)) return false;
-                if (!wait(&tt_full[n & 1], (n >> 1) & 1)) return false;
+                if (!wait(&k_full[n % L::NK], (n / L::NK) & 1)) return false;
+                if (!wait(&tt_full[n % L::NT], (n / L::NT) & 1)) return false;
                 if (!zero_v && !wait(&v_full[n % L::NV], (n / L::NV) & 1)) return false;
                 tc_fence_after();
-                const uint32_t stg = base + (n % L::NSTAGE) * L::STAGE;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    mma_bf16(tb + L::WT, sdesc(stg + L::KC0 + ks * 2048, 8192, 1024),
+                    mma_bf16(tb + L::WT, sdesc(base + L::kbuf(n) + ks * 2048, 8192, 1024),
                              sdesc(base + L::tp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
                     if (!zero_v)
                         mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
@@ -1019,50 +1146,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 return true;
             };
             for (int m = 0; m < 2 && m < nchunks; ++m) {
-                load_kq(m);
+                load_k(m);
+                load_q(m);
                 load_tt(m);
                 if (!zero_v) load_v(m);
             }
-            if (outs) load_p(0);
             bool ok = issue_wu(0);
             for (int n = 0; ok && n < nchunks; ++n) {
-                // ---- chunk n's epilogue window: U(n) is complete ----
-                ok = wait(&bar_u, n & 1);
-                // the previous S-term has read its gamma Q box (waited before
-                // this chunk's commit, while it is the barrier's latest phase)
-                if (ok && outs && n >= 1) ok = wait(&bar_os, (n - 1) & 1);
-                // the key group is done with chunk n: gamma Q(n) is in place and
-                // W^T(n) has been read out (its columns take W^T(n+1) below)
-                ok = ok && wait(&key_ready[n & 1], (n >> 1) & 1);
-                // the next chunk's W^T and U~^T first: the state chain waits for
-                // them (through the key group's -W^T) at the end of this chunk,
-                // while the S-term below is needed only after the epilogue
-                if (ok && n + 1 < nchunks) ok = issue_wu(n + 1);
+                // ---- chunk n's window ----
+                // the key group is done with chunk n: gamma Q(n) is in place
+                // and W^T(n) has been read out (its columns take W^T(n+1) below)
+                ok = wait(&key_ready[n & 1], (n >> 1) & 1);
                 if (ok && outs) {
-                    // O^T(n) = S(n-1) (gamma Q(n))^T
-                    {
+                    // O^T(n) = S(n-1) (gamma Q(n))^T as soon as the state thread
+                    // has issued U(n) (u_sig): the products run while U(n) does,
+                    // after it.  O^T(n-2) has been read out: its store warps
+                    // joined the state group's barrier at the top of chunk n - 1
+                    ok = wait(&u_sig, n & 1);
+                    if (ok) {
                         tc_fence_after();
-                        const uint32_t stg = base + (n % L::NSTAGE) * L::STAGE;
 #pragma unroll
                         for (int ks = 0; ks < K / 16; ++ks) {
-                            const uint32_t kb = ks / 4, ko = (ks % 4) * 32;
+                            const uint32_t ko = (ks / 4) * 8192 + (ks % 4) * 32;
                             mma_bf16_ta(tb + L::ocol(n), tb + L::SBT + 8 * ks,
-                                        sdesc(stg + (kb ? L::QC1 : L::QC0) + ko, 16, 1024), I_MM,
-                                        ks > 0);
+                                        sdesc(base + L::qbuf(n) + ko, 16, 1024), I_MM, ks > 0);
                         }
                         mma_commit(&bar_os);
                     }
                 }
+                // U(n) is complete, and with it dS(n - 1) and O^T(n - 1) += U^T P^T
+                ok = ok && wait(&bar_u, n & 1);
                 if (!ok) break;
-                // bar_u(n) also covers dS(n - 1) and O^T(n - 1) += U^T P^T (the
-                // state thread's earlier products), and the previous S-term was
-                // waited for above: stage (n - 1) % 3 is free
+                // chunk n + 2's loads first (they have the longest way to
+                // go).  K and Q slot (n + 2) % 3 held chunk n - 1, read by
+                // W^T(n - 1) and dS(n - 1) (bar_u(n) covers the state
+                // thread's earlier products), the key group (done: key_ready)
+                // and this thread's S-term of O^T(n - 1) (done: its bar_w(n)
+                // commit came after it); U(n) has read -W^T(n) (written over
+                // T'^T, T''^T) and U~^T(n) has read V(n)
                 if (n + 2 < nchunks) {
-                    load_kq(n + 2);
-                    load_tt(n + 2);  // U(n) read -W^T (written over T'^T, T''^T)
+                    load_k(n + 2);
+                    load_q(n + 2);
+                    load_tt(n + 2);
                     if (!zero_v) load_v(n + 2);
                 }
-                if (outs && n + 1 < nchunks) load_p(n + 1);
+                // the next chunk's W^T and U~^T: the state chain waits for them
+                // (through the key group's -W^T) at the end of this chunk
+                if (n + 1 < nchunks) ok = issue_wu(n + 1);
             }
             if (!ok) failed = true;
         }
@@ -1104,7 +1234,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_sync(kBarState, kStateThreads);
 
         // U^T = U~^T + S (-W^T) of chunk m (state thread), once the key group
-        // has written -W^T (after U~^T completed) and the decays and gamma Q
+        // has written -W^T (after U~^T completed), P, the decays and gamma Q;
+        // then u_sig tells the issuer that S(m-1) is in place for the S-term.
         auto issue_u = [&](int m) -> bool {
             if (!wait(&key_ready[m & 1], (m >> 1) & 1)) return false;
             tc_fence_after();
@@ -1115,6 +1246,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
                             zero_v ? (uint32_t)(ks > 0) : 1u);
             mma_commit(&bar_u);
+            // the issuer's S-term of O^T(m) may read the bf16 S(m-1) now
+            tc_fence_before();
+            if (outs) mbar_arrive(&u_sig);
             return true;
         };
         // chunk m's O^T -> the staging tile, by warps 12-15 (TMEM lane quarter
@@ -1168,8 +1302,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
 
         for (int n = 0; n < nchunks; ++n) {
-            const int st = n % L::NSTAGE;
-            const uint32_t stg = base + st * L::STAGE;
             // ---- U epilogue: bf16 U^T and U^T diag(decay) into the U slot ----
             const float *slot = sg + (n % 3) * 68;
             float gC;  // read with the decays: the slot is rewritten for chunk n + 3
@@ -1202,12 +1334,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ta(tb + L::DS, tb + L::ud_col(n, ks),
-                                sdesc(stg + L::KC0 + ks * 2048, 8192, 1024), I_DS, ks > 0);
+                                sdesc(base + L::kbuf(n) + ks * 2048, 8192, 1024), I_DS, ks > 0);
                 mma_commit(&bar_s);
                 if (outs) {
-                    // the issuer's S-term of O^T(n) first (it also reads S(n-1),
-                    // which the update below overwrites), and P(n)
-                    ok = wait(&bar_os, n & 1) && wait(&p_full[n & 1], (n >> 1) & 1);
+                    // after the issuer's S-term of O^T(n), which also reads
+                    // S(n-1) (overwritten by the update below); P(n) is in
+                    // place since key_ready(n), waited before U(n)
+                    ok = wait(&bar_os, n & 1);
                     if (ok) {
                         tc_fence_after();
 #pragma unroll
@@ -1276,17 +1409,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tid == kStIssuer) {
             if (status) atomicOr(status, kStatusTimeout);
             // let in-flight loads land before the CTA's shared memory is released
-            for (int s = 0; s < 3; ++s) {
-                mbar_wait(&kq_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&kq_full[s], 1, kSpinLimit / 16);
-            }
-            for (int s = 0; s < 2; ++s) {
-                mbar_wait(&v_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&v_full[s], 1, kSpinLimit / 16);
-                mbar_wait(&tt_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&tt_full[s], 1, kSpinLimit / 16);
-                mbar_wait(&p_full[s], 0, kSpinLimit / 16);
-                mbar_wait(&p_full[s], 1, kSpinLimit / 16);
+            uint64_t *loads[] = {&k_full[0], &k_full[1], &k_full[2], &q_full[0], &q_full[1],
+                                 &q_full[2], &v_full[0], &v_full[1], &tt_full[0], &tt_full[1]};
+            for (uint64_t *lb : loads) {
+                mbar_wait(lb, 0, kSpinLimit / 16);
+                mbar_wait(lb, 1, kSpinLimit / 16);
             }
         }
         __syncthreads();

@@ -101,7 +101,7 @@ GDN_API size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn
 
 /* Bytes of device workspace with which gdn_prefill takes the two-pass form:
  * the segment scratch of gdn_prefill_workspace_size (rounded up to 256 bytes)
- * plus 24 KiB per 64-token chunk per (b, h) for the key-side operands.
+ * plus 16 KiB per 64-token chunk per (b, h) for the key-side operands.
  * 0 when the problem has no two-pass form (float32, or V != 128, or
  * K not in {64, 128}). */
 GDN_API size_t gdn_prefill_two_pass_workspace_size(int B, int T, int H, int K, int V,

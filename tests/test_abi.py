@@ -117,13 +117,13 @@ def test_workspace_query(lib):
 
 def test_two_pass_workspace_query(lib):
     two = binding.gdn_prefill_two_pass_workspace_size
-    # 128 sequences run one CTA each (no segment scratch): 24 KiB per 64-token chunk
-    assert two(8, 4096, 16, 128, 128, binding.GDN_BF16) == 8 * 16 * 64 * 24576
-    assert two(8, 4096, 16, 64, 128, binding.GDN_BF16) == 8 * 16 * 64 * 24576
-    assert two(2, 65, 3, 128, 128, binding.GDN_BF16) == 2 * 3 * 2 * 24576  # ragged: 2 chunks
+    # 128 sequences run one CTA each (no segment scratch): 16 KiB per 64-token chunk
+    assert two(8, 4096, 16, 128, 128, binding.GDN_BF16) == 8 * 16 * 64 * 16384
+    assert two(8, 4096, 16, 64, 128, binding.GDN_BF16) == 8 * 16 * 64 * 16384
+    assert two(2, 65, 3, 128, 128, binding.GDN_BF16) == 2 * 3 * 2 * 16384  # ragged: 2 chunks
     for K, V in ((128, 128), (64, 128)):
         need = binding.gdn_prefill_workspace_size(1, 65536, 16, K, V, binding.GDN_BF16)
-        assert two(1, 65536, 16, K, V, binding.GDN_BF16) >= need + 16 * 1024 * 24576
+        assert two(1, 65536, 16, K, V, binding.GDN_BF16) >= need + 16 * 1024 * 16384
     # no two-pass form: float32, the (32, 32) variant, empty or invalid problems
     assert two(8, 4096, 16, 128, 128, binding.GDN_FP32) == 0
     assert two(1, 256, 1, 32, 32, binding.GDN_BF16) == 0
@@ -135,9 +135,9 @@ def test_two_pass_workspace_query(lib):
 def test_gathered_prefill_workspace_and_validation(lib):
     size = binding.gdn_prefill_gathered_workspace_size
     bf = binding.GDN_BF16
-    # key-side operands (24 KiB per chunk), then q' and k' (bf16, 64 channels)
+    # key-side operands (16 KiB per chunk), then q' and k' (bf16, 64 channels)
     tok = 8 * 4096 * 16 * 64 * 2
-    assert size(8, 4096, 16, 128, 64, 128, bf) == 8 * 16 * 64 * 24576 + 2 * tok
+    assert size(8, 4096, 16, 128, 64, 128, bf) == 8 * 16 * 64 * 16384 + 2 * tok
     # only full width 128 -> 64 kept channels at V = 128, bf16
     for args in ((8, 4096, 16, 96, 64, 128, bf), (8, 4096, 16, 128, 32, 128, bf),
                  (8, 4096, 16, 128, 64, 64, bf), (8, 4096, 16, 128, 64, 128, binding.GDN_FP32),

@@ -28,7 +28,7 @@ def run_both(p, S0=True):
     two = binding.gdn_prefill_two_pass_workspace_size(B, T, H, K, V, binding.GDN_BF16)
     assert two > need
     chunks = (T + 63) // 64
-    assert two - (need + 255) // 256 * 256 == B * H * chunks * 24576
+    assert two - (need + 255) // 256 * 256 == B * H * chunks * 16384
     outs = []
     for ws_bytes in (need, two):
         o = torch.full((B, T, H, V), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -44,11 +44,17 @@ def run_both(p, S0=True):
 
 def assert_same(one, two):
     (o1, s1), (o2, s2) = one, two
+    # the states take the same operands through the same products
     assert np.array_equal(s1.view(np.int32), s2.view(np.int32))
     assert not np.isnan(o2).any()
-    # one bf16 ulp of the larger magnitude (8 significant bits)
+    # o: the two forms sum q_t . k_s in different orders (a tensor-memory
+    # product in one, warp-level MMAs in the other) before P is rounded to
+    # bf16, so an entry of P may land one bf16 step (2^-8 relative) apart,
+    # and the transposed product accumulates in another order; both stay
+    # far inside one part in 10^3 of o (the parity bar is 10^-2)
+    assert rel_err(o2, o1) <= 1e-3, rel_err(o2, o1)
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.maximum(np.abs(o1), np.abs(o2)), 1e-30))) - 7)
-    assert np.all(np.abs(o1 - o2) <= ulp), float(np.max(np.abs(o1 - o2) / ulp))
+    assert np.mean(np.abs(o1 - o2) > ulp) <= 1e-2
 
 
 @pytest.mark.parametrize("K", [128, 64])
@@ -80,7 +86,7 @@ def test_two_pass_sizes():
     assert binding.gdn_prefill_two_pass_workspace_size(2, 300, 3, 128, 128, binding.GDN_FP32) == 0
     assert binding.gdn_prefill_two_pass_workspace_size(2, 300, 3, 32, 32, binding.GDN_BF16) == 0
     assert binding.gdn_prefill_two_pass_workspace_size(8, 4096, 16, 128, 128,
-                                                       binding.GDN_BF16) == 8 * 16 * 64 * 24576
+                                                       binding.GDN_BF16) == 8 * 16 * 64 * 16384
 
 
 def test_two_pass_repeated_calls_stay_identical():
