@@ -2,173 +2,411 @@
 // blog, Sec. 3): S <- U_r U_r^T S, U_r the left singular vectors of the r
 // largest singular values, plus the singular values themselves.
 //
-// One CTA per state, everything in shared memory.  One-sided (Hestenes)
-// Jacobi on the K columns of S: each round of the round-robin ordering
-// rotates K/2 disjoint column pairs at once (8 lanes per pair, the column's
-// V entries spread as float4 pieces at offsets 32 i + 4 l, so the 8 lanes of
-// a pair read 128 contiguous bytes per access), with the rotation that makes
-// the pair orthogonal:
+// One CTA per state.  One-sided (Hestenes) Jacobi on the K columns of S, with
+// the columns held in registers in blocks of four: a group of 16 lanes (half
+// a warp) holds a pair of blocks, V / 16 entries of each of its 8 columns per
+// lane (runs of four: lane l holds entries 64 i + 4 l .. + 3), so a state
+// takes K / 8 groups (8 warps for K = 128, two per scheduler).  A sweep
+// visits every column pair once:
+//   - block rounds: each group rotates the 16 cross pairs of its two blocks,
+//     in four mini-rounds of four disjoint pairs (top column i with bottom
+//     column (i + m) % 4); then the blocks move to the next arrangement of
+//     the round-robin (circle method: block 0 stays, the others step around a
+//     cycle) through shared memory, as 16-byte runs.  K/4 - 1 block rounds
+//     meet every pair of blocks once and return them to their places.
+//   - in the first block round also the 6 pairs inside each block: three
+//     rounds of the fixed pairs (0,3) (1,2) of each block, its columns 1..3
+//     stepping around between rounds (the circle method again).
+// Each mini-round sums its four dot products with a reduce-scatter over the
+// 16 lanes, so lane quad k (lanes 4k .. 4k + 3) ends with pair k's sum and
+// computes that pair's rotation once; the quads then broadcast (c, s).  The
+// quad also carries its pair's two squared norms.  (Measured on the 128
+// final states of the 8 x 4096 x 16 prefill: blocks of four in 8 warps per
+// state beat blocks of eight in 4 warps, whose one warp per scheduler leaves
+// the rotations' latencies exposed, and blocks of two in 16 warps, whose
+// shorter blocks spend more instructions per pair.)
+// The rotation makes the pair orthogonal:
 //
 //   a = |c_p|^2, b = |c_q|^2, g = c_p . c_q,  zeta = (b - a) / (2 g),
 //   t = sign(zeta) / (|zeta| + sqrt(1 + zeta^2)),  c = 1/sqrt(1 + t^2), s = c t,
-//   c_p <- c c_p - s c_q,   c_q <- s c_p + c c_q,
+//   c_p <- c c_p - s c_q,   c_q <- s c_p + c c_q,   a <- a - t g,  b <- b + t g
 //
-// skipped when |g| <= sqrt(V) eps sqrt(a b) (columns orthogonal to float32
-// precision) or |g| <= 1e-12 |S|_F^2 (a coupling far below anything that can
-// move the singular values or subspaces at float32 precision; without this
-// floor the noise-level columns of a low-rank state keep the sweeps going).
-// The rotation itself uses fast reciprocal / square-root forms: an angle that
-// is off in the last bits leaves a residual the next sweep removes.  Sweeps repeat until one rotates nothing
-// (or max_sweeps; then the not-converged status bit is set).  The converged
-// columns are sigma_i u_i; with u_i their directions, W = U^T S (against a
-// copy of the original S) has row norms sigma_i, the r largest select U_r,
-// and S <- U_r W_r.
+// (a and b are recomputed from the columns at every block round; within one
+// the updates above carry them).  It is skipped when |g| <= sqrt(V) eps
+// sqrt(a b) (columns orthogonal to float32 precision) or |g| <= 1e-12 |S|_F^2
+// (a coupling far below anything that can move the singular values or
+// subspaces at float32 precision; without this floor the noise-level columns
+// of a low-rank state keep the sweeps going).  The rotation uses fast
+// reciprocal / square-root forms: an angle that is off in the last bits
+// leaves a residual the next sweep removes.  Sweeps repeat until one rotates
+// nothing (or max_sweeps; then the not-converged status bit is set).  The
+// converged columns are sigma_i u_i; with u_i their directions, W = U^T S
+// (against a copy of the original S) has row norms sigma_i, the r largest
+// select U_r, and S <- U_r W_r.
 #include "gdn_internal.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kLanesPerPair = 8;
+constexpr int kLanes = 16;  // lanes of one column (half a warp)
+constexpr int kBlk = 4;     // columns per block
 // Orthogonality threshold |g| <= sqrt(V) eps sqrt(a b), eps = 2^-24 (float32).
 template <int V>
 __host__ __device__ constexpr float jacobi_tol() { return V == 128 ? 6.75e-7f : 3.38e-7f; }
 
 template <int V, int K>
-struct TruncSmem {
-    static constexpr int A = 0;                       // [K][V] rotated columns
-    static constexpr int S = A + K * V * 4;           // [V][K] original state
-    static constexpr int W = S + V * K * 4;           // [K][K] U^T S
-    static constexpr int NRM = W + K * K * 4;         // [K] 1 / column norms
-    static constexpr int SEL = NRM + K * 4;           // [K] column of rank i
-    static constexpr int BYTES = SEL + K * 4;
+struct TruncLayout {
+    static constexpr int E = V / kLanes;    // entries of a column per lane
+    static constexpr int NB = K / kBlk;     // blocks
+    static constexpr int NS = NB / 2;       // block pairs = lane groups (8 columns each)
+    static constexpr int NT = NS * kLanes;  // threads
+    static constexpr int LDT = K + 4;       // row stride of U^T [V][LDT]
+    // output columns of a thread's 8-row tile (at least one float4)
+    static constexpr int TK = K * K / (NT * 8) > 4 ? K * K / (NT * 8) : 4;
+    // shared memory, in floats
+    static constexpr int SZ0 = V * LDT > K * V ? V * LDT : K * V;
+    static constexpr int SZ1 = K * V > K * K ? K * V : K * K;
+    static constexpr int BOARD0 = 0;                // [K][V] columns; U^T at the end
+    static constexpr int BOARD1 = BOARD0 + SZ0;     // [K][V] columns; W [K][K] at the end
+    static constexpr int SC = BOARD1 + SZ1;         // [V][K] the original S
+    static constexpr int NRM = SC + V * K;          // [K] 1 / column norms
+    static constexpr int SIG = NRM + K;             // [K] sigma^2
+    static constexpr int SEL = SIG + K;             // [K] column of rank i (int)
+    static constexpr size_t BYTES = (size_t)(SEL + K) * 4;
+    static_assert(V % kLanes == 0 && K % (2 * kBlk) == 0 && K <= V, "shape");
+    static_assert(TK % 4 == 0 && K % TK == 0, "tiles");
 };
 
-__device__ __forceinline__ void pair_of(int round, int m, int n, int &p, int &q) {
-    if (m == 0) {
-        p = n - 1;
-        q = round;
-    } else {
-        p = (round + m) % (n - 1);
-        q = (round + n - 1 - m) % (n - 1);
+// Sum four per-lane values over the 16 lanes of the group, scattering: lane
+// quad k (lanes 4k .. 4k + 3, k = lane bits 3 and 2) gets the sum of x[k].
+// The quad's four lanes hold the same sum (the last two levels add the same
+// pairs, in either order).
+__device__ __forceinline__ float reduce_scatter4(const float (&x)[4], int l) {
+    const bool b3 = l & 8, b2 = l & 4;
+    float h[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? x[i] : x[i + 2], keep = b3 ? x[i + 2] : x[i];
+        h[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? h[0] : h[1], keep = b2 ? h[1] : h[0];
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    return r;
+}
+
+// The rotation of one pair from a = |c_p|^2, b = |c_q|^2, g = c_p . c_q:
+// (c, s, t), or (1, 0, 0) when the pair is already orthogonal.  With
+// d = b - a, h = 2 g, r = sqrt(d^2 + h^2) and u = |d| + r, the angle above
+// (zeta = d / h) is t = sign(d) h / u, and 1 + t^2 = 2 r / u, so
+//   c = u / sqrt(2 r u),  s = sign(d) h / sqrt(2 r u),  t = sign(d) h 2 r / (2 r u):
+// two reciprocal square roots in sequence (each ~40 cycles) where the
+// zeta form takes four.  The columns are scaled so that |S|_F ~ 1, which
+// keeps d^2 + h^2 in range.
+__device__ __forceinline__ bool jacobi_angle(float a, float b, float g, float floor_g, float tol2,
+                                             float &c, float &s, float &t) {
+    const bool rot = fabsf(g) > floor_g && g * g > tol2 * a * b;
+    const float d = b - a, h = 2.f * g;
+    const float x = fmaf(d, d, h * h);
+    const float r = x * rsqrtf(x);
+    const float u = fabsf(d) + r;
+    const float rq = rsqrtf(2.f * r * u);
+    const float sh = d >= 0.f ? h : -h;  // sign(d) h, sign(0) = +1
+    c = rot ? u * rq : 1.f;
+    s = rot ? sh * rq : 0.f;
+    t = rot ? sh * (2.f * r) * (rq * rq) : 0.f;
+    return rot;
+}
+
+// Rotate the four disjoint column pairs (P[k], Q[k]) of the group's registers,
+// the quad of pair k computing its rotation: in cross mini-round M top k with
+// bottom 4 + (k + M) % 4, or with INNER the pairs (0,3) (1,2) (4,7) (5,6)
+// inside the blocks.  The quads of a warp may decide differently, so the
+// rotation is predicated (c = 1, s = 0), and skipped as a whole when no pair
+// of the warp rotates.  For the cross pairs the quad's squared norms (ap, aq)
+// are given and updated (a <- a - t g, b <- b + t g); for the inner ones they
+// are summed from the columns.
+template <int E, bool INNER, int M = 0>
+__device__ __forceinline__ void rotate4(float (&X)[8][E], int l, int gbase, float &ap, float &aq,
+                                        float floor_g, float tol2, bool &any) {
+    constexpr int P[4] = {0, 1, INNER ? 4 : 2, INNER ? 5 : 3};
+    constexpr int Q[4] = {INNER ? 3 : 4 + M % 4, INNER ? 2 : 4 + (1 + M) % 4,
+                          INNER ? 7 : 4 + (2 + M) % 4, INNER ? 6 : 4 + (3 + M) % 4};
+    float gx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc = fmaf(X[P[k]][e], X[Q[k]][e], acc);
+        gx[k] = acc;
+    }
+    const float g = reduce_scatter4(gx, l);
+    if (INNER) {
+        float ax[4], bx[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float a0 = 0.f, b0 = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                a0 = fmaf(X[P[k]][e], X[P[k]][e], a0);
+                b0 = fmaf(X[Q[k]][e], X[Q[k]][e], b0);
+            }
+            ax[k] = a0;
+            bx[k] = b0;
+        }
+        ap = reduce_scatter4(ax, l);
+        aq = reduce_scatter4(bx, l);
+    }
+    float c, s, t;
+    const bool rot = jacobi_angle(ap, aq, g, floor_g, tol2, c, s, t);
+    ap = fmaf(-t, g, ap);
+    aq = fmaf(t, g, aq);
+    if (__any_sync(0xffffffffu, rot)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float ck = __shfl_sync(0xffffffffu, c, gbase + 4 * k);
+            const float sk = __shfl_sync(0xffffffffu, s, gbase + 4 * k);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float x = X[P[k]][e], y = X[Q[k]][e];
+                X[P[k]][e] = fmaf(-sk, y, ck * x);
+                X[Q[k]][e] = fmaf(sk, x, ck * y);
+            }
+        }
+        any = true;
     }
 }
 
+// Between the cross mini-rounds quad k's next bottom column is the one quad
+// k + 1 has just rotated: its norm comes from there.
+__device__ __forceinline__ float next_bottom_norm(float aq, int l, int gbase) {
+    return __shfl_sync(0xffffffffu, aq, gbase + ((l + 4) & 15));
+}
+
+// Columns 1..3 of each block step around (column j takes column j - 1,
+// column 1 takes column 3; 3 steps cycle back).
+template <int E>
+__device__ __forceinline__ void step_inner(float (&X)[8][E]) {
+#pragma unroll
+    for (int b0 = 0; b0 < 8; b0 += 4)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float x = X[b0 + 3][e];
+            X[b0 + 3][e] = X[b0 + 2][e];
+            X[b0 + 2][e] = X[b0 + 1][e];
+            X[b0 + 1][e] = x;
+        }
+}
+
+// Squared norms of the quad's pair of columns (top k, bottom k).
+template <int E>
+__device__ __forceinline__ void quad_norms(const float (&X)[8][E], int l, float &ap, float &aq) {
+    float ax[4], bx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float a0 = 0.f, b0 = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            a0 = fmaf(X[k][e], X[k][e], a0);
+            b0 = fmaf(X[4 + k][e], X[4 + k][e], b0);
+        }
+        ax[k] = a0;
+        bx[k] = b0;
+    }
+    ap = reduce_scatter4(ax, l);
+    aq = reduce_scatter4(bx, l);
+}
+
+// Entry e of a column in lane l: runs of CH (4, or E when E < 4) entries,
+// so a group's 16 lanes move a column as 16-byte (8-byte) pieces of one
+// contiguous run.
+template <int E>
+__device__ __forceinline__ int entry_v(int e, int l) {
+    constexpr int CH = E < 4 ? E : 4;
+    return (e / CH) * (kLanes * CH) + l * CH + (e % CH);
+}
+template <int E, int V>
+__device__ __forceinline__ void store_col(float *col, const float (&x)[E], int l) {
+    if constexpr (E >= 4) {
+#pragma unroll
+        for (int i = 0; i < E / 4; ++i)
+            *reinterpret_cast<float4 *>(col + entry_v<E>(4 * i, l)) =
+                make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e += 2)
+            *reinterpret_cast<float2 *>(col + entry_v<E>(e, l)) = make_float2(x[e], x[e + 1]);
+    }
+}
+template <int E, int V>
+__device__ __forceinline__ void load_col(const float *col, float (&x)[E], int l) {
+    if constexpr (E >= 4) {
+#pragma unroll
+        for (int i = 0; i < E / 4; ++i) {
+            const float4 v = *reinterpret_cast<const float4 *>(col + entry_v<E>(4 * i, l));
+            x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            const float2 v = *reinterpret_cast<const float2 *>(col + entry_v<E>(e, l));
+            x[e] = v.x; x[e + 1] = v.y;
+        }
+    }
+}
 template <int V, int K>
-__global__ void __launch_bounds__(K / 2 * kLanesPerPair)
+__global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
     truncate_kernel(float *__restrict__ Sg, int r, float *__restrict__ sigma, int max_sweeps,
                     int *status) {
-    using L = TruncSmem<V, K>;
-    constexpr int NCH = V / 32;  // float4 pieces per lane per column
-    constexpr int NT = K / 2 * kLanesPerPair;
-    extern __shared__ __align__(16) unsigned char smem[];
-    float *A = reinterpret_cast<float *>(smem + L::A);
-    float *Sc = reinterpret_cast<float *>(smem + L::S);
-    float *W = reinterpret_cast<float *>(smem + L::W);
-    float *nrm = reinterpret_cast<float *>(smem + L::NRM);
-    int *sel = reinterpret_cast<int *>(smem + L::SEL);
-    __shared__ int rotated;
-
+    using L = TruncLayout<V, K>;
+    constexpr int E = L::E, NS = L::NS, NT = L::NT, LDT = L::LDT, TK = L::TK;
+    extern __shared__ __align__(16) float smf[];
+    float *Sc = smf + L::SC;
+    float *nrm = smf + L::NRM;
+    float *sig2 = smf + L::SIG;
+    int *sel = reinterpret_cast<int *>(smf + L::SEL);
     __shared__ float fro2;
+
     const int tid = threadIdx.x;
+    const int grp = tid / kLanes, l = tid % kLanes;
     if (tid == 0) fro2 = 0.f;
     __syncthreads();
     float *Sh = Sg + (size_t)blockIdx.x * V * K;
-    float part = 0.f;
-    for (int e = tid * 4; e < V * K; e += NT * 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(Sh + e);
-        part += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-        *reinterpret_cast<float4 *>(Sc + e) = x;
-        const int v = e / K, c = e % K;
-        A[(c + 0) * V + v] = x.x;
-        A[(c + 1) * V + v] = x.y;
-        A[(c + 2) * V + v] = x.z;
-        A[(c + 3) * V + v] = x.w;
-    }
+    {
+        // the original S, and its columns into board 0 ([K][V])
+        float part = 0.f;
+        for (int e4 = tid * 4; e4 < V * K; e4 += NT * 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(Sh + e4);
+            part += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+            *reinterpret_cast<float4 *>(Sc + e4) = x;
+            const int v = e4 / K, c = e4 % K;
+            smf[L::BOARD0 + (c + 0) * V + v] = x.x;
+            smf[L::BOARD0 + (c + 1) * V + v] = x.y;
+            smf[L::BOARD0 + (c + 2) * V + v] = x.z;
+            smf[L::BOARD0 + (c + 3) * V + v] = x.w;
+        }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if ((tid & 31) == 0) atomicAdd(&fro2, part);
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if ((tid & 31) == 0) atomicAdd(&fro2, part);
+    }
     __syncthreads();
-    const float floor_g = 1e-12f * fro2;
+    // the sweeps run on the columns times 2^-e, |S|_F 2^-e in [0.5, 1): an
+    // exact scaling (rotations do not depend on it) that keeps the angle's
+    // squares in range; W below is formed against the original S
+    const int fe = fro2 > 0.f ? ilogbf(sqrtf(fro2)) + 1 : 0;
+    const float scale = ldexpf(1.f, -fe);
+    const float floor_g = 1e-12f * fro2 * scale * scale;
     const float tol2 = jacobi_tol<V>() * jacobi_tol<V>();
 
-    const int m = tid / kLanesPerPair, l = tid % kLanesPerPair;
+    // group grp holds columns 8 grp .. 8 grp + 7: its top block, then its bottom
+    const int gbase = tid & 16;  // the group's first lane in its warp
+    float X[8][E];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        load_col<E, V>(smf + L::BOARD0 + (8 * grp + j) * V, X[j], l);
+#pragma unroll
+        for (int e = 0; e < E; ++e) X[j][e] *= scale;
+    }
+    // where this group's blocks go at each move (board column of their first
+    // column): the top steps to the next group's top (group 0's stays; the
+    // last group's goes to its own bottom), the bottom to the previous
+    // group's bottom (group 0's to group 1's top)
+    const int top_to = grp == 0 ? 0 : grp == NS - 1 ? 8 * grp + 4 : 8 * (grp + 1);
+    const int bot_to = grp == 0 ? 8 : 8 * (grp - 1) + 4;
+
     bool converged = false;
     for (int sweep = 0; sweep < max_sweeps && !converged; ++sweep) {
-        if (tid == 0) rotated = 0;
-        __syncthreads();
-        int p, q;
-        pair_of(0, m, K, p, q);
-        for (int round = 0; round < K - 1; ++round) {
-            float4 cp[NCH], cq[NCH];
-            float a = 0.f, b = 0.f, g = 0.f;
-#pragma unroll
-            for (int i = 0; i < NCH; ++i) {
-                cp[i] = *reinterpret_cast<const float4 *>(A + p * V + 32 * i + 4 * l);
-                cq[i] = *reinterpret_cast<const float4 *>(A + q * V + 32 * i + 4 * l);
-                a += cp[i].x * cp[i].x + cp[i].y * cp[i].y + cp[i].z * cp[i].z + cp[i].w * cp[i].w;
-                b += cq[i].x * cq[i].x + cq[i].y * cq[i].y + cq[i].z * cq[i].z + cq[i].w * cq[i].w;
-                g += cp[i].x * cq[i].x + cp[i].y * cq[i].y + cp[i].z * cq[i].z + cp[i].w * cq[i].w;
-            }
-#pragma unroll
-            for (int off = kLanesPerPair / 2; off > 0; off >>= 1) {
-                a += __shfl_xor_sync(0xffffffffu, a, off);
-                b += __shfl_xor_sync(0xffffffffu, b, off);
-                g += __shfl_xor_sync(0xffffffffu, g, off);
-            }
-            if (fabsf(g) > floor_g && g * g > tol2 * a * b) {
-                const float zeta = __fdividef(b - a, 2.f * g);
-                const float az = fabsf(zeta);
-                float t;
-                if (az > 1e18f) {
-                    t = __fdividef(0.5f, zeta);
-                } else {
-                    const float e1 = fmaf(zeta, zeta, 1.f);
-                    t = __fdividef(copysignf(1.f, zeta), az + e1 * rsqrtf(e1));
+        bool any = false;
+        for (int br = 0; br < L::NB - 1; ++br) {
+            float ap, aq;  // squared norms of the quad's pair
+            if (br == 0) {
+#pragma unroll 1
+                for (int rr = 0; rr < 3; ++rr) {
+                    rotate4<E, true>(X, l, gbase, ap, aq, floor_g, tol2, any);
+                    step_inner<E>(X);
                 }
-                const float c = rsqrtf(fmaf(t, t, 1.f));
-                const float s = c * t;
+            }
+            quad_norms<E>(X, l, ap, aq);
+            rotate4<E, false, 0>(X, l, gbase, ap, aq, floor_g, tol2, any);
+            aq = next_bottom_norm(aq, l, gbase);
+            rotate4<E, false, 1>(X, l, gbase, ap, aq, floor_g, tol2, any);
+            aq = next_bottom_norm(aq, l, gbase);
+            rotate4<E, false, 2>(X, l, gbase, ap, aq, floor_g, tol2, any);
+            aq = next_bottom_norm(aq, l, gbase);
+            rotate4<E, false, 3>(X, l, gbase, ap, aq, floor_g, tol2, any);
+            // move the blocks (boards alternate, so one barrier per round:
+            // a board is rewritten only after the round that read it)
+            float *bd = smf + ((br & 1) ? L::BOARD0 : L::BOARD1);
 #pragma unroll
-                for (int i = 0; i < NCH; ++i) {
-                    const float4 x = cp[i], y = cq[i];
-                    *reinterpret_cast<float4 *>(A + p * V + 32 * i + 4 * l) =
-                        make_float4(c * x.x - s * y.x, c * x.y - s * y.y, c * x.z - s * y.z,
-                                    c * x.w - s * y.w);
-                    *reinterpret_cast<float4 *>(A + q * V + 32 * i + 4 * l) =
-                        make_float4(s * x.x + c * y.x, s * x.y + c * y.y, s * x.z + c * y.z,
-                                    s * x.w + c * y.w);
-                }
-                if (l == 0) rotated = 1;
+            for (int j = 0; j < 4; ++j) {
+                store_col<E, V>(bd + (top_to + j) * V, X[j], l);
+                store_col<E, V>(bd + (bot_to + j) * V, X[4 + j], l);
             }
             __syncthreads();
-            // next round of the round-robin ordering: every index but K - 1 steps by one mod K - 1
-            if (m != 0) p = p == K - 2 ? 0 : p + 1;
-            q = q == K - 2 ? 0 : q + 1;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) load_col<E, V>(bd + (8 * grp + j) * V, X[j], l);
         }
-        converged = rotated == 0;
-        __syncthreads();  // everyone has read `rotated` before it is reset
+        converged = __syncthreads_or(any) == 0;
     }
     if (!converged && tid == 0 && status) atomicOr(status, kStatusNotConverged);
 
-    // Directions u_c = c_c / |c_c| of the converged columns.  Their lengths
-    // are not used as singular values: rotations that are orthogonal only to
-    // rounding let the lengths drift over a few thousand rotations while the
-    // directions stay accurate.  So W = U^T S is formed against the original
-    // S for every column and sigma_c = |W[c]|.
-    for (int c = tid; c < K; c += NT) {
-        float n2 = 0.f;
-        for (int v = 0; v < V; ++v) n2 = fmaf(A[c * V + v], A[c * V + v], n2);
-        nrm[c] = n2 > 0.f ? rsqrtf(n2) : 0.f;  // 1 / |c_c| (0 for a zero column)
+    // U^T (the converged columns, unnormalised) into board 0 as [V][LDT], and
+    // 1 / |c| per column.  Their lengths are not used as singular values:
+    // rotations that are orthogonal only to rounding let the lengths drift
+    // over a few thousand rotations while the directions stay accurate.  So
+    // W = U^T S is formed against the original S for every column and
+    // sigma_c = |W[c]|.
+    float *Ut = smf + L::BOARD0;
+    float *W = smf + L::BOARD1;
+    __syncthreads();  // every thread has read its last blocks from the boards
+    {
+        float ap, aq;
+        quad_norms<E>(X, l, ap, aq);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int e = 0; e < E; ++e) Ut[entry_v<E>(e, l) * LDT + 8 * grp + j] = X[j][e];
+        if ((l & 3) == 0) {
+            nrm[8 * grp + l / 4] = ap > 0.f ? rsqrtf(ap) : 0.f;
+            nrm[8 * grp + 4 + l / 4] = aq > 0.f ? rsqrtf(aq) : 0.f;
+        }
     }
     __syncthreads();
-    constexpr int JS = NT / K;  // thread (j0, kk): rows j0, j0 + JS, ... of column kk
-    const int kk = tid % K, j0 = tid / K;
-    for (int j = j0; j < K; j += JS) {
-        float acc = 0.f;
-        for (int v = 0; v < V; ++v) acc = fmaf(A[j * V + v], Sc[v * K + kk], acc);
-        W[j * K + kk] = acc * nrm[j];
+    // W[c][k] = (1/|c|) sum_v U^T[v][c] S[v][k]: 8 x TK tiles, one per thread
+    for (int tile = tid; tile < (K / 8) * (K / TK); tile += NT) {
+        const int c0 = (tile / (K / TK)) * 8, k0 = (tile % (K / TK)) * TK;
+        float acc[8][TK];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < TK; ++j) acc[i][j] = 0.f;
+        for (int v = 0; v < V; ++v) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(Ut + v * LDT + c0);
+            const float4 a1 = *reinterpret_cast<const float4 *>(Ut + v * LDT + c0 + 4);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float s[TK];
+#pragma unroll
+            for (int j = 0; j < TK; j += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(Sc + v * K + k0 + j);
+                s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < TK; ++j) acc[i][j] = fmaf(a[i], s[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float ni = nrm[c0 + i];
+#pragma unroll
+            for (int j = 0; j < TK; j += 4)
+                *reinterpret_cast<float4 *>(W + (c0 + i) * K + k0 + j) =
+                    make_float4(acc[i][j] * ni, acc[i][j + 1] * ni, acc[i][j + 2] * ni,
+                                acc[i][j + 3] * ni);
+        }
     }
     __syncthreads();
-    float *sig2 = Sc;  // the copy of S is no longer needed: reuse it for sigma^2
     for (int c = tid; c < K; c += NT) {
         float s2 = 0.f;
         for (int k = 0; k < K; ++k) s2 = fmaf(W[c * K + k], W[c * K + k], s2);
@@ -186,21 +424,43 @@ __global__ void __launch_bounds__(K / 2 * kLanesPerPair)
         for (int i = tid; i < K; i += NT) sigma[(size_t)blockIdx.x * K + i] = sqrtf(sig2[sel[i]]);
     if (r >= K) return;  // nothing to cut (K <= V for every supported variant)
 
-    // S <- U_r W_r
-    for (int v = j0; v < V; v += JS) {
-        float acc = 0.f;
-        for (int j = 0; j < r; ++j) {
-            const int c = sel[j];
-            acc = fmaf(A[c * V + v] * nrm[c], W[c * K + kk], acc);
+    // S <- U_r W_r: 8 x TK tiles of [V][K]
+    for (int tile = tid; tile < (V / 8) * (K / TK); tile += NT) {
+        const int v0 = (tile / (K / TK)) * 8, k0 = (tile % (K / TK)) * TK;
+        float acc[8][TK];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < TK; ++j) acc[i][j] = 0.f;
+        for (int jr = 0; jr < r; ++jr) {
+            const int c = sel[jr];
+            const float nc = nrm[c];
+            float w[TK];
+#pragma unroll
+            for (int j = 0; j < TK; j += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(W + c * K + k0 + j);
+                w[j] = x.x; w[j + 1] = x.y; w[j + 2] = x.z; w[j + 3] = x.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float u = Ut[(v0 + i) * LDT + c] * nc;
+#pragma unroll
+                for (int j = 0; j < TK; ++j) acc[i][j] = fmaf(u, w[j], acc[i][j]);
+            }
         }
-        Sh[(size_t)v * K + kk] = acc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < TK; j += 4)
+                *reinterpret_cast<float4 *>(Sh + (size_t)(v0 + i) * K + k0 + j) =
+                    make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
     }
 }
 
 template <int V, int K>
 cudaError_t launch_trunc_t(float *S, int BH, int r, float *sigma, int max_sweeps,
                            cudaStream_t stream) {
-    using L = TruncSmem<V, K>;
+    using L = TruncLayout<V, K>;
     auto kern = truncate_kernel<V, K>;
     static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
@@ -211,8 +471,7 @@ cudaError_t launch_trunc_t(float *S, int BH, int r, float *sigma, int max_sweeps
         if (e != cudaSuccess) return e;
         attr_set[dev] = context_key();
     }
-    kern<<<BH, K / 2 * kLanesPerPair, L::BYTES, stream>>>(S, r, sigma, max_sweeps,
-                                                          device_status_ptr());
+    kern<<<BH, L::NT, L::BYTES, stream>>>(S, r, sigma, max_sweeps, device_status_ptr());
     return cudaGetLastError();
 }
 
