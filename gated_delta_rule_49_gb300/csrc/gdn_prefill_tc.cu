@@ -617,6 +617,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     const int warp = tid >> 5, lane = tid & 31;
     const int nch = (T + 63) / 64;  // chunks per sequence
 
+    // the state pass may be scheduled now (it waits for this grid before
+    // reading the operands; every CTA of this persistent grid is resident)
+    if (tid == 0) pdl_trigger();
     if (warp == 0) {
         tmem_alloc(&tmem_base_sh, 64);
         tmem_relinquish();
@@ -1145,6 +1148,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mma_commit(&bar_w);
                 return true;
             };
+            // launched as a programmatic dependent, this kernel may have started
+            // before the key-side pass ended: its operands (and, in the
+            // gathering form, q' and k') are read only after it
+            pdl_wait();
             for (int m = 0; m < 2 && m < nchunks; ++m) {
                 load_k(m);
                 load_q(m);
@@ -2093,6 +2100,16 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     }
     int *status = device_status_ptr();
     auto launch = [&](long long grid, SegPlan plan) {
+        if (two && plan.mode != kSecond && K == 64)
+            // right after the key-side pass: its tail overlaps this grid's
+            // prologue (the issuer waits for it before the first load).
+            // Measured on the 8 x 4096 x 16 prefill: d_k' = 64 gains 6 us
+            // (0.220 -> 0.214 ms); at d_k = 128 the state CTAs, placed on
+            // whichever SMs the key-side pass frees first, ran 10 us slower,
+            // so that width keeps the plain launch
+            return launch_pdl(prefill_state_kernel<K>, (unsigned)grid, kTcThreads, smem, stream,
+                              mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H,
+                              (int)BH, plan, prep, status);
         if (two)
             prefill_state_kernel<K><<<(unsigned)grid, kTcThreads, smem, stream>>>(
                 mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan, prep,
