@@ -18,6 +18,9 @@ from .binding import (  # noqa: F401
     gdn_get_last_device_status,
     gdn_prefill,
     gdn_prefill_gated,
+    gdn_prefill_gated_chunked,
+    gdn_prefill_gated_chunked_workspace_size,
+    prefill_gated_chunked,
     gdn_prefill_gathered,
     prefill_gathered,
     gdn_decode_step_gated,

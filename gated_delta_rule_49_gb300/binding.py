@@ -60,6 +60,8 @@ EXPORTS = (
     "gdn_prefill_host",
     "gdn_prefill_gathered",
     "gdn_prefill_gathered_workspace_size",
+    "gdn_prefill_gated_chunked",
+    "gdn_prefill_gated_chunked_workspace_size",
 )
 
 _lock = threading.Lock()
@@ -110,6 +112,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_decode_step_gathered.restype = i
         lib.gdn_prefill_gated.argtypes = [vp] * 10 + [i] * 7 + [vp]
         lib.gdn_prefill_gated.restype = i
+        lib.gdn_prefill_gated_chunked.argtypes = [vp] * 10 + [i] * 7 + [vp, sz, vp]
+        lib.gdn_prefill_gated_chunked.restype = i
+        lib.gdn_prefill_gated_chunked_workspace_size.argtypes = [i] * 7
+        lib.gdn_prefill_gated_chunked_workspace_size.restype = sz
         lib.gdn_decode_step_gated.argtypes = [vp] * 9 + [i] * 6 + [vp]
         lib.gdn_decode_step_gated.restype = i
         lib.gdn_state_truncate.argtypes = [vp, i, i, i, i, vp, i, vp]
@@ -237,6 +243,37 @@ def gdn_prefill_gated(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, H, K, V, gat
                                   _ptr(w), _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, K, V, gate,
                                   dtype, _stream(stream))
     return _check(st, "gdn_prefill_gated")
+
+
+def gdn_prefill_gated_chunked(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, H, K, V, gate,
+                              dtype, workspace, workspace_bytes, stream=None) -> int:
+    st = load().gdn_prefill_gated_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                          _ptr(b), _ptr(w), _ptr(S0), _ptr(o), _ptr(S_T), B, T,
+                                          H, K, V, gate, dtype, _ptr(workspace), workspace_bytes,
+                                          _stream(stream))
+    return _check(st, "gdn_prefill_gated_chunked")
+
+
+def gdn_prefill_gated_chunked_workspace_size(B, T, H, K, V, gate, dtype) -> int:
+    return load().gdn_prefill_gated_chunked_workspace_size(B, T, H, K, V, gate, dtype)
+
+
+def prefill_gated_chunked(q, k, v, alpha, beta=None, b=None, w=None, S0=None, gate="kda",
+                          want_o=True, want_state=True, workspace=None, stream=None):
+    """gdn_prefill_gated_chunked on torch CUDA tensors (gate "kda" or "gdn2",
+    K = V = 128, bf16); allocates the workspace unless one is given.
+    Returns (o, S_T)."""
+    import torch
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = torch.empty((B, T, H, V), dtype=v.dtype, device=v.device) if want_o else None
+    ST = torch.empty((B, H, V, K), dtype=torch.float32, device=v.device) if want_state else None
+    need = gdn_prefill_gated_chunked_workspace_size(B, T, H, K, V, GATES[gate], _dtype_code(v))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=v.device)
+    gdn_prefill_gated_chunked(q, k, v, alpha, beta, b, w, S0, o, ST, B, T, H, K, V, GATES[gate],
+                              _dtype_code(v), workspace, workspace.numel(), stream)
+    return o, ST
 
 
 def gdn_decode_step_gated(q, k, v, alpha, beta, b, w, S, o, B, H, K, V, gate, dtype,

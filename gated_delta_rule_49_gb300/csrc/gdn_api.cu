@@ -271,6 +271,40 @@ int gdn_prefill_gated(const void *q, const void *k, const void *v, const float *
                                                H, K, V, gate, dtype, st));
 }
 
+size_t gdn_prefill_gated_chunked_workspace_size(int B, int T, int H, int K, int V,
+                                                gdn_gate gate, gdn_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || K != 128 || V != 128 || dtype != GDN_BF16) return 0;
+    if (gate != GDN_GATE_KDA && gate != GDN_GATE_GDN2) return 0;
+    if ((long long)B * H > 0x7fffffffLL) return 0;
+    return gdn::prefill_gated_tc_workspace(B, T, H, gate);
+}
+
+int gdn_prefill_gated_chunked(const void *q, const void *k, const void *v, const float *alpha,
+                              const float *beta, const float *b, const float *w, const float *S0,
+                              void *o, float *S_T, int B, int T, int H, int K, int V,
+                              gdn_gate gate, gdn_dtype dtype, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    if (B < 0 || T < 0 || H < 0 || K <= 0 || V <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_FP32) return GDN_ERR_INVALID_ARG;
+    if (!valid_gate(gate)) return GDN_ERR_INVALID_ARG;
+    if (gate == GDN_GATE_SCALAR || dtype != GDN_BF16 || K != 128 || V != 128)
+        return GDN_ERR_UNSUPPORTED;
+    if (!o && !S_T) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !gates_match(gate, beta, b, w)))
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, alpha, beta, b, w, S0, o, S_T, workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    if ((long long)B * H == 0) return GDN_OK;
+    if ((long long)B * H > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) return empty_prefill(S0, S_T, B, H, K, V, st);
+    const size_t need = gdn_prefill_gated_chunked_workspace_size(B, T, H, K, V, gate, dtype);
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    return from_cuda(gdn::launch_prefill_gated_tc(q, k, v, alpha, beta, b, w, S0, o, S_T, B, T, H,
+                                                  gate, workspace, st));
+}
+
 int gdn_decode_step_gated(const void *q, const void *k, const void *v, const float *alpha,
                           const float *beta, const float *b, const float *w, float *S, void *o,
                           int B, int H, int K, int V, gdn_gate gate, gdn_dtype dtype,

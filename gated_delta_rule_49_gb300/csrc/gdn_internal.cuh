@@ -117,6 +117,14 @@ cudaError_t launch_decode_gathered(const void *q, const void *k, const int *idx,
 // Channel-gated rules (GDN / KDA / GDN2), token by token on the CUDA cores;
 // also the prefill for float32 inputs and the (32, 32) variant (scalar gate).
 // Tokens [0, T) of [B, Ts, H, *] tensors, as for the chunked prefill.
+// The chunkwise tensor-core prefill of KDA / GDN2 (K = V = 128, bf16;
+// gdn_gated_tc.cu): workspace bytes, and the two launches.
+size_t prefill_gated_tc_workspace(int B, int T, int H, int gate);
+cudaError_t launch_prefill_gated_tc(const void *q, const void *k, const void *v,
+                                    const float *alpha, const float *beta, const float *bgate,
+                                    const float *wgate, const float *S0, void *o, float *ST,
+                                    int B, int T, int H, int gate, void *workspace,
+                                    cudaStream_t stream);
 cudaError_t launch_prefill_gated(const void *q, const void *k, const void *v,
                                  const float *alpha, const float *beta, const float *bg,
                                  const float *wg, const float *S0, void *o, float *ST, int B,

@@ -294,6 +294,40 @@ GDN_API int gdn_prefill_gated(const void *q, const void *k, const void *v, const
                               int V, gdn_gate gate, gdn_dtype dtype, void *stream);
 
 /*
+ * gdn_prefill_gated_chunked -- gdn_prefill_gated for KDA and GDN2 in the
+ * chunkwise form on the tensor cores: 64-token chunks, a key-side pass over
+ * every chunk of every sequence at once (the per-channel gate prefix; the
+ * intra-chunk products A and P with each 16-token row block's exponents
+ * referred to its midpoint, so every factor stays below e^(8 max |log alpha|);
+ * the triangular inverse; W), then one CTA per sequence carrying the float32
+ * state ("Linear Attention Architectures" notes, Secs. 2.5-2.6; the
+ * pseudo-value form of "On State Reduction" notes, Sec. 2.3).  Arguments as
+ * for gdn_prefill_gated, plus
+ *
+ *   workspace  >= gdn_prefill_gated_chunked_workspace_size(...) bytes,
+ *              16-byte aligned, caller-owned device memory (about 64.5 KiB
+ *              per 64-token chunk per (b, h) for KDA, 80.5 KiB for GDN2)
+ *
+ * Supported: gate KDA or GDN2, K = V = 128, bf16; anything else returns
+ * GDN_ERR_UNSUPPORTED (gdn_prefill_gated covers it token by token).  The
+ * operands of the tensor-core products are bf16 (float32 accumulation, the
+ * inverse and the state in float32), so results agree with gdn_prefill_gated
+ * to the bf16 operand rounding, not bit for bit.  o or S_T may be NULL (not
+ * both); S_T may alias S0.  A missing or short workspace returns
+ * GDN_ERR_WORKSPACE.
+ */
+GDN_API int gdn_prefill_gated_chunked(const void *q, const void *k, const void *v,
+                                      const float *alpha, const float *beta, const float *b,
+                                      const float *w, const float *S0, void *o, float *S_T,
+                                      int B, int T, int H, int K, int V, gdn_gate gate,
+                                      gdn_dtype dtype, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
+/* Workspace bytes of gdn_prefill_gated_chunked (0 where it has no form). */
+GDN_API size_t gdn_prefill_gated_chunked_workspace_size(int B, int T, int H, int K, int V,
+                                                        gdn_gate gate, gdn_dtype dtype);
+
+/*
  * gdn_decode_step_gated -- one token of gdn_prefill_gated on a state updated
  * in place:  q, k [B, H, K]; v, o [B, H, V]; alpha [B, H] or [B, H, K];
  * beta [B, H]; b [B, H, K]; w [B, H, V]; S [B, H, V, K].  Which gates must be
