@@ -183,13 +183,17 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
         const size_t th0 = ((size_t)b * T + (size_t)n * 64) * H + h;
         uint8_t *out = ws + (size_t)j * gw_chunk_bytes(GATE);
 
-        // ---- gates: G[t][c] = sum_{s <= t} log2 alpha[s][c] (thread = channel) ----
+        // ---- gates: G[t][c] = sum_{s <= t} log2 alpha[s][c] (thread = channel);
+        // ---- the 64 loads go out together, then the prefix ----
         {
+            float a[64];
+#pragma unroll
+            for (int t = 0; t < 64; ++t)
+                a[t] = t < nvalid ? __ldg(alpha + (th0 + (size_t)t * H) * 128 + tid) : 1.f;
             float g = 0.f;
-#pragma unroll 4
+#pragma unroll
             for (int t = 0; t < 64; ++t) {
-                const float a = t < nvalid ? alpha[(th0 + (size_t)t * H) * 128 + tid] : 1.f;
-                g += log2f(a);
+                g += log2f(a[t]);
                 Gt[t * kGLD + tid] = g;
             }
             reinterpret_cast<float *>(out + kGwF)[tid] = exp2f(g);  // e^(G_C) of the state update
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
 
         // ---- scaled tiles, 16-byte pieces: K~ (.) e^G (W's operand), the
         // ---- erase rows E (GDN2, A's left operand), Q (.) e^G, K (.) e^(G_C - G), Z ----
+#pragma unroll
         for (int p = tid; p < 1024; p += kGpThreads) {
             const int t = p >> 4, c16 = p & 15, c0 = c16 * 8;
             const uint32_t off = piece_off(t, c16);
