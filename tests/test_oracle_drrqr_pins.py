@@ -34,6 +34,57 @@ def test_gram_is_the_sum_over_tokens():
         assert np.allclose(G[h], want, atol=1e-12)
 
 
+def test_gram_hand_computed_case():
+    """Two tokens, one head, K = 2, integer entries, worked by hand:
+    k rows (1, 2), (3, -1); q rows (0, 1), (1, 1) give
+    [[1+9+0+1, 2-3+0+1], [2-3+0+1, 4+1+1+1]] = [[11, 0], [0, 7]]."""
+    k = np.array([[[1.0, 2.0]], [[3.0, -1.0]]])
+    q = np.array([[[0.0, 1.0]], [[1.0, 1.0]]])
+    assert np.array_equal(oracle.channel_gram(k, q)[0], np.array([[11.0, 0.0], [0.0, 7.0]]))
+
+
+def test_gram_spectrum_is_the_squared_singular_values_of_the_stacked_rows():
+    """G_h = M_h^T M_h for M_h the keys and queries of head h stacked as rows:
+    its eigenvalues are the squared singular values of M_h (an SVD, not a sum
+    of outer products), its trace is the summed squared row norms (2N for
+    unit rows), and it is symmetric positive semi-definite."""
+    rng = np.random.default_rng(5)
+    N, H, K = 37, 3, 6
+    k = rng.standard_normal((N, H, K))
+    q = rng.standard_normal((N, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    G = oracle.channel_gram(k, q)
+    for h in range(H):
+        M = np.concatenate([k[:, h], q[:, h]], axis=0)
+        sv = np.linalg.svd(M, compute_uv=False)
+        ev = np.linalg.eigvalsh(G[h])
+        assert np.allclose(np.sort(ev), np.sort(sv ** 2), atol=1e-10)
+        assert abs(np.trace(G[h]) - 2 * N) < 1e-10
+        assert np.allclose(G[h], G[h].T, atol=1e-14)
+        assert ev.min() > -1e-10
+
+
+def test_gram_is_additive_over_token_batches_and_rotates_with_the_channels():
+    """Statistics collected over two batches add up; rotating every key and
+    query by an orthogonal R conjugates the Gram: G(kR, qR) = R^T G R."""
+    rng = np.random.default_rng(6)
+    k = rng.standard_normal((3, 11, 2, 5))
+    q = rng.standard_normal((3, 11, 2, 5))
+    whole = oracle.channel_gram(k, q)
+    parts = oracle.channel_gram(k[:, :4], q[:, :4]) + oracle.channel_gram(k[:, 4:], q[:, 4:])
+    assert np.allclose(whole, parts, atol=1e-12)
+    R, _ = np.linalg.qr(rng.standard_normal((5, 5)))
+    rot = oracle.channel_gram(k @ R, q @ R)
+    for h in range(2):
+        assert np.allclose(rot[h], R.T @ whole[h] @ R, atol=1e-11)
+    # a key channel that is zero everywhere gives a zero row and column
+    k[..., 3] = 0.0
+    q[..., 3] = 0.0
+    Z = oracle.channel_gram(k, q)
+    assert not Z[:, 3, :].any() and not Z[:, :, 3].any()
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_rho_is_the_volume_ratio_of_each_swap(seed):
     """Strong RRQR's test quantity: swapping kept column i with candidate j
