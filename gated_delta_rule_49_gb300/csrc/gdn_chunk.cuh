@@ -197,31 +197,33 @@ __device__ __forceinline__ FragB frag_bt(const float *M, int g, int t4) {
 
 // Block row J of U = T^T (warp J of the inverse): U_JJ = D_J^T, then
 // U_Ji = -(sum_{m=J}^{i-1} U_Jm A_im^T) D_i^T for i > J; U_Ji = 0 for i < J.
-// u[i] receives U_Ji in the accumulator layout.  One code path for all four
-// warps (J is warp-uniform, the block indices compile-time), so the four
-// block rows share their instructions.
-__device__ __forceinline__ void inverse_block_row(float *AF, int J, int g, int t4,
-                                                  float (&u)[4][2][4]) {
+// Each block goes to emit(i, u) in the accumulator layout as soon as it is
+// formed, so only the left operands of the later products stay in registers.
+// One code path for all four warps (J is warp-uniform, the block indices
+// compile-time), so the four block rows share their instructions.
+template <class Emit>
+__device__ __forceinline__ void inverse_block_row(float *AF, int J, int g, int t4, Emit &&emit) {
     FragA ua[3];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+        float u[2][4];
         if (i < J) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) u[i][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) u[nt][e] = 0.f;
         } else if (i == J) {
             // U_JJ[r][c] = D_J[c][r]: rows g, g + 8, columns 8 nt + 2 t4 (+ 1)
             const float *D = blk(AF, i, i);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int c = 8 * nt + 2 * t4;
-                u[i][nt][0] = D[c * kLD + g];
-                u[i][nt][1] = D[(c + 1) * kLD + g];
-                u[i][nt][2] = D[c * kLD + g + 8];
-                u[i][nt][3] = D[(c + 1) * kLD + g + 8];
+                u[nt][0] = D[c * kLD + g];
+                u[nt][1] = D[(c + 1) * kLD + g];
+                u[nt][2] = D[c * kLD + g + 8];
+                u[nt][3] = D[(c + 1) * kLD + g + 8];
             }
-            if (i < 3) ua[i] = frag_a(u[i], 1.f);
+            if (i < 3) ua[i] = frag_a(u, 1.f);
         } else {
             float acc[3][2][4] = {};
 #pragma unroll
@@ -232,9 +234,10 @@ __device__ __forceinline__ void inverse_block_row(float *AF, int J, int g, int t
             const FragA xa = frag_a(x, -1.f);
             float acc2[3][2][4] = {};
             mma_split(acc2, xa, frag_bt(blk(AF, i, i), g, t4));
-            sum_split(acc2, u[i]);
-            if (i < 3) ua[i] = frag_a(u[i], 1.f);
+            sum_split(acc2, u);
+            if (i < 3) ua[i] = frag_a(u, 1.f);
         }
+        emit(i, u);
     }
 }
 
@@ -283,23 +286,24 @@ __device__ __forceinline__ void chunk_inverse_tprime(float *AF, const float *bet
     const int warp = tid >> 5;
     if (warp < 4) {
         const int lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-        float u[4][2][4];
-        inverse_block_row(AF, warp, g, t4, u);
         // rows s0 = 16 warp + g and s0 + 8 of T'^T and T''^T
+        const int s0 = 16 * warp + g;
+        const float b0 = bet[s0], b1 = bet[s0 + 8];
+        const float bg0 = b0 * gam[s0], bg1 = b1 * gam[s0 + 8];
+        inverse_block_row(AF, warp, g, t4, [&](int i, const float (&u)[2][4]) {
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int srow = 16 * warp + g + 8 * hr;
-            const float b = bet[srow], bg = b * gam[srow];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int hr = 0; hr < 2; ++hr) {
+                const int srow = s0 + 8 * hr;
+                const float b = hr ? b1 : b0, bg = hr ? bg1 : bg0;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    const float v0 = u[i][nt][2 * hr], v1 = u[i][nt][2 * hr + 1];
+                    const float v0 = u[nt][2 * hr], v1 = u[nt][2 * hr + 1];
                     const uint32_t off = swz128(srow, 2 * i + nt) + 4 * t4;
                     *reinterpret_cast<uint32_t *>(TPtile + off) = pack_bf16(v0 * bg, v1 * bg);
                     *reinterpret_cast<uint32_t *>(TPPtile + off) = pack_bf16(v0 * b, v1 * b);
                 }
-        }
+            }
+        });
     }
 }
 

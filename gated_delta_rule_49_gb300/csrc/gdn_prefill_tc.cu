@@ -273,21 +273,36 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
 // helpers above), so both forms give identical states.  The gathering form
 // loads the full-width q and k boxes, and writes the gathered q' and k' for
 // the state pass.
-template <int K>
+// The product reads 128 rows of its A operand, [K;Q] in the fused kernel's
+// layout; here only the K rows (TMEM lanes 0..63) are used, so lanes 64..127
+// may hold anything, and rows 64..127 of A are whatever lies 8 KB past each
+// box: the next k box, or the start of the A scratch (written only between
+// the products, after the previous one has completed).  The stage then holds
+// just the k boxes.  The gathering form loads the full-width q and k boxes.
+template <int K, bool GATHER>
 struct PrepLayout {
-    static constexpr uint32_t KC0 = 0, QC0 = 8192, KC1 = 16384, QC1 = 24576;
-    static constexpr uint32_t STAGE = K == 128 ? 32768 : 16384;  // one q/k stage
-    static constexpr uint32_t AF = STAGE;                        // float [64][68]
-    static constexpr uint32_t GATE = AF + 64 * kLD * 4;          // G2, gamma, beta
+    static constexpr uint32_t KC0 = 0, QC0 = 8192;
+    static constexpr uint32_t KC1 = GATHER ? 16384 : 8192, QC1 = 24576;  // QC*: gathering only
+    static constexpr uint32_t STAGE = GATHER ? 32768 : (K == 128 ? 16384 : 8192);
+    static constexpr uint32_t AF = STAGE;                  // float [64][68]
+    static constexpr uint32_t GATE = AF + 64 * kLD * 4;    // G2, gamma, beta
     static constexpr uint32_t END = GATE + 3 * 64 * 4;
-    static constexpr uint32_t KQ_BYTES = (K == 128 ? 4u : 2u) * 8192u;
+    static constexpr uint32_t KQ_BYTES = 4u * 8192u;
     static constexpr uint32_t K_BYTES = (K == 128 ? 2u : 1u) * 8192u;
     static constexpr size_t SMEM = END;
+    static_assert(GATHER || AF >= (K == 128 ? KC1 : KC0) + 8192,
+                  "rows 64..127 of the last box's A read");
+    static_assert(GATHER || 64 * kLD * 4 >= 8192, "the A scratch covers those rows");
 };
 constexpr int kPrepThreads = 128;
-constexpr int kPrepCtasPerSm = 4;
-// four CTAs of dynamic + 1 KB static + 1 KB reserved shared memory per SM
-static_assert(kPrepCtasPerSm * (PrepLayout<128>::SMEM + 2048) <= 233472, "prep residency");
+// resident CTAs per SM (five or six with the k-only stage ran slower: the
+// register budget they leave spills the inverse)
+constexpr int prep_ctas_per_sm(bool) { return 4; }
+// the CTAs' dynamic + 1 KB static + 1 KB reserved shared memory per SM
+static_assert(prep_ctas_per_sm(false) * (PrepLayout<128, false>::SMEM + 2048) <= 233472,
+              "prep residency");
+static_assert(prep_ctas_per_sm(true) * (PrepLayout<64, true>::SMEM + 2048) <= 233472,
+              "prep residency");
 
 // The pruning prologue inside the key-side pass (GATHER): the q/k boxes are
 // the full 128-channel rows, the kernel keeps channels idx[h, :] of each row
@@ -300,13 +315,13 @@ struct PrepGather {
 };
 
 template <int K, bool GATHER>
-__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
+__global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
     prefill_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const float *__restrict__ alpha,
                         const float *__restrict__ beta, uint8_t *__restrict__ prep, int T, int Ts,
                         int H, long long nchunk_all, PrepGather gth, int *status) {
     static_assert(!GATHER || K == 64, "the gathering form keeps 64 of 128 channels");
-    using L = PrepLayout<GATHER ? 128 : K>;  // the q/k stage holds the boxes as loaded
+    using L = PrepLayout<K, GATHER>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the swizzle atoms and operand descriptors need a 1024-byte aligned
     // base; the declaration provides it and the kernel checks it
@@ -338,13 +353,6 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         mbar_init(&drain, 1);
         fence_mbar_init();
         abort_flag = 0;
-    }
-    if constexpr (!GATHER) {
-        // the product's Q half (rows 64..127 of [K;Q]) stays zero
-        for (int e = tid; e < (K / 64) * 512; e += kPrepThreads)
-            reinterpret_cast<uint4 *>(sm + ((e >> 9) ? L::QC1 : L::QC0))[e & 511] =
-                make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -492,8 +500,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
         uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T'^T | T''^T]
         tc_fence_after();
-        for (int ch = 0; ch < 2; ++ch)  // both 32-column halves per thread
-            chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, nullptr);
+        if (warp < 2)  // TMEM lanes 0..63: the K rows; both 32-column halves per thread
+            for (int ch = 0; ch < 2; ++ch)
+                chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, nullptr);
         tc_fence_before();
         named_sync(kBarKey, kPrepThreads);
         chunk_inverse_tprime<kPrepThreads>(AF, bet, gam, out + kPrepTP, out + kPrepTPP, tid);
@@ -526,22 +535,23 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 // walks its chunks like the fused kernel, but loads T'^T and T''^T instead
 // of solving for them.  Three roles:
 //   key group (warps 0-6): per chunk P = (Q K^T masked, times the decays)
-//       with warp-level MMAs from the raw q/k boxes (the group is otherwise
-//       idle for most of a chunk, and forming P here saves the key-side pass
-//       its q read and P's trip through memory), the gates, the state
-//       group's decay factors, gamma folded into the Q box, and -W^T from
-//       TMEM into the spent T'/T'' slot (no tensor-memory products, no loads).
+//       with warp-level MMAs from the raw q/k boxes (forming P here saves the
+//       key-side pass its q read and P's trip through memory), the gates,
+//       the state group's decay factors and gamma folded into the Q box (no
+//       tensor-memory products, no loads).  It runs up to a chunk ahead of
+//       the state group.
 //   issuer (warp 7, one thread): every TMA load, and the products off the
 //       state chain -- O^T(n) = S(n-1) (gamma Q(n))^T once the state thread
-//       has issued U(n), then W^T(n+1) = K^T T'^T and U~^T(n+1) = V^T T''^T
-//       once U(n) is complete -- while the chain's epilogue leaves the
-//       tensor pipe idle.  An SM issues tcgen05 products one at a time, ~47
-//       cycles each, so the chain's own products are never issued beside
-//       these.
+//       has issued U(n) (it runs behind it), then, once U(n) is complete,
+//       W^T(n+1) = K^T T'^T and U~^T(n+1) = V^T T''^T (its U slot was
+//       U(n-1)'s) -- while the chain's epilogue leaves the tensor pipe idle.
+//       An SM issues tcgen05 products one at a time, so the chain's own
+//       products are never issued beside these.
 //   state group (warps 8-15): the state chain
 //       U^T(n)  = U~^T(n) + S(n-1) (-W^T(n))       (issued at the end of n - 1)
 //       epilogue: U^T -> bf16, U^T diag(decay) -> bf16, in the U slot
 //       dS(n)   = U^T diag(decay) K(n),  O^T(n) += U^T P(n)^T
+//       -W^T(n+1) from TMEM into its operand tile, while dS(n) runs
 //       S(n)    = gamma_C S(n-1) + dS(n)
 //     and the transposed output, staged by warps 12-15 for TMA stores by
 //     warp 11 (a ragged tail is clipped by the tensor map).
@@ -552,21 +562,23 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 // commit after U(n)) also says that dS(n-1) and O^T(n-1) += U^T P^T are
 // complete: the issuer reloads and reuses slots only after it.  The state
 // thread waits for the S-term (bar_os), which reads S(n-1), before its
-// O^T(n) += U^T P^T and the update; the issuer writes W^T(n+1) only after
-// the key group has read W^T(n).
-// The key group writes P(n) before it signals key_ready(n), once W^T(n) is
-// complete (so U(n - 1), and O^T(n - 2) += U^T P^T before it, which read the
-// slot).
+// O^T(n) += U^T P^T and the update, for U~^T(n) (bar_ut) before U(n), and
+// for the key group's chunk n (key_ready(n): decays, P(n), gamma Q(n)) before
+// the epilogue of chunk n; the issuer writes W^T(n+1) only after the state
+// group has read W^T(n) (u_sig(n) follows it).  The key group stores P(n)
+// once O^T(n-1) += U^T P^T is complete (bar_o2), and with it O^T(n-2)'s,
+// the last reader of the slot.
 // Every mbarrier wait is for the barrier's latest phase: the next phase needs
-// a step that the waiting thread takes after the wait.  Rings: q/k (three
-// stages), V, [T'^T | T''^T] (then -W^T), P, U and O (two each); the loads of
-// chunk n + 2 go out in chunk n's window.  Every state quantity is the fused
-// kernel's arithmetic on the same operands, so S_T is bit-identical to it (o
-// agrees to the accumulation orders of P and of the transposed product).
+// a step that the waiting thread takes after the wait (key_ready is a ring of
+// four because the key group may run ahead).  Rings: q/k (three stages), V,
+// [T'^T | T''^T], P, U and O (two each); the loads of chunk n + 2 go out in
+// chunk n's window.  Every state quantity is the fused kernel's arithmetic on
+// the same operands, so S_T is bit-identical to it (o agrees to the
+// accumulation orders of P and of the transposed product).
 
-// Rings: K and Q (three slots each), V, [T'^T | T''^T] / -W^T and P (two
-// each).  Each K / Q slot holds the 64-channel boxes of one chunk side by
-// side (channels 64..127 at +8 KB when K = 128).
+// Rings: K and Q (three slots each), V, [T'^T | T''^T] and P (two each);
+// one -W^T tile.  Each K / Q slot holds the 64-channel boxes of one chunk
+// side by side (channels 64..127 at +8 KB when K = 128).
 template <int K>
 struct StLayout {
     static constexpr int NK = 3, NQ = 3, NV = 2, NT = 2;
@@ -574,10 +586,11 @@ struct StLayout {
     static constexpr uint32_t KR = 0;                            // K ring
     static constexpr uint32_t QR = KR + NK * BOX;                // Q ring
     static constexpr uint32_t VB = QR + NQ * BOX;                // V ring, 16 KB per chunk
-    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [T'^T | T''^T] / -W^T
+    static constexpr uint32_t PR = VB + NV * 16384;              // ring of [T'^T | T''^T]
     static constexpr uint32_t PP = PR + NT * 16384;              // ring of P
     static constexpr uint32_t OST = PP + 2 * 8192;               // output staging, 2 x 64 x 64
-    static constexpr uint32_t KGATE = OST + 16384;               // G2, gamma, beta
+    static constexpr uint32_t NWB = OST + 16384;                 // -W^T, K x 64
+    static constexpr uint32_t KGATE = NWB + 16384;               // G2, gamma, beta
     static constexpr uint32_t SGATE = KGATE + 3 * 64 * 4;        // 3 x (decay[64], gamma_C)
     static constexpr uint32_t END = SGATE + 3 * 68 * 4;
     static constexpr uint32_t V_BYTES = 2u * 8192u;
@@ -587,7 +600,6 @@ struct StLayout {
     static __device__ __forceinline__ uint32_t qbuf(int n) { return QR + (n % NQ) * BOX; }
     static __device__ __forceinline__ uint32_t tp(int n) { return PR + (n % NT) * 16384; }
     static __device__ __forceinline__ uint32_t tpp(int n) { return tp(n) + 8192; }
-    static __device__ __forceinline__ uint32_t nw(int n) { return tp(n); }  // over T', T''
     static __device__ __forceinline__ uint32_t ptile(int n) { return PP + (n & 1) * 8192; }
     static __device__ __forceinline__ uint32_t vbuf(int n) { return VB + (n % NV) * 16384; }
     // TMEM columns: O^T of even / odd chunks, U~^T / U^T of even / odd
@@ -625,8 +637,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sm = smem_raw;
-    __shared__ uint64_t k_full[3], q_full[3], v_full[2], tt_full[2], key_ready[2], bar_w, bar_u,
-        bar_s, bar_os, bar_o2, u_sig, drain[2];
+    __shared__ uint64_t k_full[3], q_full[3], v_full[2], tt_full[2], key_ready[4], bar_w, bar_ut,
+        bar_u, bar_s, bar_os, bar_o2, u_sig, drain[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int *abort_v = &abort_flag;
@@ -656,9 +668,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         uint64_t *bars[] = {&k_full[0],  &k_full[1],  &k_full[2],  &q_full[0],  &q_full[1],
                             &q_full[2],  &v_full[0],  &v_full[1],  &tt_full[0], &tt_full[1],
-                            &key_ready[0],
-                            &key_ready[1], &bar_w,    &bar_u,      &bar_s,  &bar_os, &u_sig,
-                            &bar_o2,     &drain[0],   &drain[1]};
+                            &key_ready[0], &key_ready[1], &key_ready[2], &key_ready[3],
+                            &bar_w,    &bar_ut,     &bar_u,  &bar_s,  &bar_os,
+                            &u_sig,      &bar_o2,     &drain[0],   &drain[1]};
         for (uint64_t *bb : bars) mbar_init(bb, 1);
         fence_mbar_init();
         abort_flag = 0;
@@ -767,32 +779,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 *p = w;
             }
-            if (tid == 0) ok = wait(&bar_w, n & 1);  // W^T(n) and U~^T(n) complete
-            if (named_sync_or(kBarKey, kStKeyThreads, !ok)) { failed = true; break; }
             if (outs) {
-                // P slot n % 2 was last read by O^T(n - 2) += U^T P^T, which
-                // the state thread issued before U(n - 1); the issuer waited
-                // for U(n - 1) before W^T(n), whose completion was just seen
+                // P slot n % 2 was last read by O^T(n - 2) += U^T P^T: complete
+                // with O^T(n - 1) += U^T P^T (bar_o2), which the state thread
+                // issues only after key_ready(n - 1), so no later phase of
+                // bar_o2 can have completed yet
+                if (tid == 0 && n >= 1) ok = wait(&bar_o2, (n - 1) & 1);
+                if (named_sync_or(kBarKey, kStKeyThreads, !ok)) { failed = true; break; }
                 p_block_store(sm + L::ptile(n), pw[0], p_unit_i(warp), p_unit_j(warp), lane);
                 if (pu2 >= 0) p_block_store(sm + L::ptile(n), pw[1], p_unit_i(pu2), p_unit_j(pu2), lane);
             }
-            if (warp < 4) {
-                // -W^T over T'^T, T''^T (both read by the products above)
-                tc_fence_after();
-                if (quad_row < K) {
-#pragma unroll 1
-                    for (int ch = 0; ch < 2; ++ch) {
-                        float v[32];
-                        tmem_ld32(tb + lane_off + L::WT + 32 * ch, v);
-                        tmem_ld_wait();
-                        store_row<4>(sm + L::nw(n), quad_row, 4 * ch, v, -1.f);
-                    }
-                }
-                tc_fence_before();
-            }
             fence_proxy_async_smem();
             named_sync(kBarKey, kStKeyThreads);
-            if (tid == 0) mbar_arrive(&key_ready[p2]);
+            if (tid == 0) mbar_arrive(&key_ready[n & 3]);
             // this chunk's register slot takes chunk n + 2's gate inputs
             if (p2 == 0)
                 prefetch_gates(n + 2, 0);
@@ -837,21 +836,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bulk_load(sm + L::tp(n), prep_seq + (size_t)n * kPrepChunkBytes + kPrepTP, 16384,
                           &tt_full[n % L::NT]);
             };
-            // W^T(n) = K^T T'^T and U~^T(n) = V^T T''^T (U slot n % 2)
-            auto issue_wu = [&](int n) -> bool {
+            // W^T(n) = K^T T'^T into the W^T columns
+            auto issue_w = [&](int n) -> bool {
                 if (!wait(&k_full[n % L::NK], (n / L::NK) & 1)) return false;
                 if (!wait(&tt_full[n % L::NT], (n / L::NT) & 1)) return false;
-                if (!zero_v && !wait(&v_full[n % L::NV], (n / L::NV) & 1)) return false;
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+                for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tb + L::WT, sdesc(base + L::kbuf(n) + ks * 2048, 8192, 1024),
                              sdesc(base + L::tp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
-                    if (!zero_v)
-                        mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
-                                 sdesc(base + L::tpp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
-                }
                 mma_commit(&bar_w);
+                return true;
+            };
+            // U~^T(n) = V^T T''^T into U slot n % 2 (none with v = 0)
+            auto issue_ut = [&](int n) -> bool {
+                if (zero_v) return true;
+                if (!wait(&v_full[n % L::NV], (n / L::NV) & 1)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + L::ua(n), sdesc(base + L::vbuf(n) + ks * 2048, 8192, 1024),
+                             sdesc(base + L::tpp(n) + ks * 2048, 8192, 1024), I_ABMN, ks > 0);
+                mma_commit(&bar_ut);
                 return true;
             };
             // launched as a programmatic dependent, this kernel may have started
@@ -864,28 +870,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 load_tt(m);
                 if (!zero_v) load_v(m);
             }
-            bool ok = issue_wu(0);
+            bool ok = issue_w(0) && issue_ut(0);
             for (int n = 0; ok && n < nchunks; ++n) {
                 // ---- chunk n's window ----
-                // the key group is done with chunk n: gamma Q(n) is in place
-                // and W^T(n) has been read out (its columns take W^T(n+1) below)
-                ok = wait(&key_ready[n & 1], (n >> 1) & 1);
+                // the key group is done with chunk n (gamma Q(n) is in place),
+                // and the state thread has issued U(n) (u_sig), after the state
+                // group read W^T(n) out (its columns take W^T(n+1) below)
+                ok = wait(&key_ready[n & 3], (n >> 2) & 1) && wait(&u_sig, n & 1);
                 if (ok && outs) {
-                    // O^T(n) = S(n-1) (gamma Q(n))^T as soon as the state thread
-                    // has issued U(n) (u_sig): the products run while U(n) does,
-                    // after it.  O^T(n-2) has been read out: its store warps
-                    // joined the state group's barrier at the top of chunk n - 1
-                    ok = wait(&u_sig, n & 1);
-                    if (ok) {
-                        tc_fence_after();
+                    // O^T(n) = S(n-1) (gamma Q(n))^T.  O^T(n-2) has been read
+                    // out: its store warps joined the state group's barrier at
+                    // the top of chunk n - 1
+                    tc_fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < K / 16; ++ks) {
-                            const uint32_t ko = (ks / 4) * 8192 + (ks % 4) * 32;
-                            mma_bf16_ta(tb + L::ocol(n), tb + L::SBT + 8 * ks,
-                                        sdesc(base + L::qbuf(n) + ko, 16, 1024), I_MM, ks > 0);
-                        }
-                        mma_commit(&bar_os);
+                    for (int ks = 0; ks < K / 16; ++ks) {
+                        const uint32_t ko = (ks / 4) * 8192 + (ks % 4) * 32;
+                        mma_bf16_ta(tb + L::ocol(n), tb + L::SBT + 8 * ks,
+                                    sdesc(base + L::qbuf(n) + ko, 16, 1024), I_MM, ks > 0);
                     }
+                    mma_commit(&bar_os);
                 }
                 // U(n) is complete, and with it dS(n - 1) and O^T(n - 1) += U^T P^T
                 ok = ok && wait(&bar_u, n & 1);
@@ -894,18 +897,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // go).  K and Q slot (n + 2) % 3 held chunk n - 1, read by
                 // W^T(n - 1) and dS(n - 1) (bar_u(n) covers the state
                 // thread's earlier products), the key group (done: key_ready)
-                // and this thread's S-term of O^T(n - 1) (done: its bar_w(n)
-                // commit came after it); U(n) has read -W^T(n) (written over
-                // T'^T, T''^T) and U~^T(n) has read V(n)
+                // and this thread's S-term of O^T(n - 1) (done: the state
+                // thread waited for it before O^T(n - 1) += U^T P^T); the
+                // [T'^T | T''^T] slot held chunk n, read by W^T(n) (seen by the
+                // state group) and U~^T(n) (before U(n)); V(n) was read by U~^T(n)
                 if (n + 2 < nchunks) {
                     load_k(n + 2);
                     load_q(n + 2);
                     load_tt(n + 2);
                     if (!zero_v) load_v(n + 2);
                 }
-                // the next chunk's W^T and U~^T: the state chain waits for them
-                // (through the key group's -W^T) at the end of this chunk
-                if (n + 1 < nchunks) ok = issue_wu(n + 1);
+                // the next chunk's W^T (the state group reads it out into the
+                // -W^T tile while dS(n) runs) and U~^T, into U(n - 1)'s slot
+                if (n + 1 < nchunks) ok = issue_w(n + 1) && issue_ut(n + 1);
             }
             if (!ok) failed = true;
         }
@@ -946,22 +950,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         named_sync(kBarState, kStateThreads);
 
-        // U^T = U~^T + S (-W^T) of chunk m (state thread), once the key group
-        // has written -W^T (after U~^T completed), P, the decays and gamma Q;
-        // then u_sig tells the issuer that S(m-1) is in place for the S-term.
+        // U^T = U~^T + S (-W^T) of chunk m (state thread), once the state
+        // group has written -W^T and U~^T is complete; then u_sig tells the
+        // issuer that U(m) is issued and S(m-1) in place for the S-term.
         auto issue_u = [&](int m) -> bool {
-            if (!wait(&key_ready[m & 1], (m >> 1) & 1)) return false;
+            if (!zero_v && !wait(&bar_ut, m & 1)) return false;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < K / 16; ++ks)
                 // with v = 0 there is no U~ product: this one starts the accumulator
                 mma_bf16_ta(tb + L::ua(m), tb + L::SBT + 8 * ks,
-                            sdesc(base + L::nw(m) + ks * 2048, 8192, 1024), I_BMN,
+                            sdesc(base + L::NWB + ks * 2048, 8192, 1024), I_BMN,
                             zero_v ? (uint32_t)(ks > 0) : 1u);
             mma_commit(&bar_u);
             // the issuer's S-term of O^T(m) may read the bf16 S(m-1) now
             tc_fence_before();
-            if (outs) mbar_arrive(&u_sig);
+            mbar_arrive(&u_sig);
             return true;
         };
         // chunk m's O^T -> the staging tile, by warps 12-15 (TMEM lane quarter
@@ -1007,7 +1011,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return true;
         };
-        if (sw == 0) {
+        // -W^T(m) from TMEM into its operand tile: state warp sw reads TMEM
+        // lane quarter sw % 4, column half sw / 4, once W^T(m) is complete
+        // (U(m - 1), the reader of the previous -W^T, is complete too).  All
+        // state threads take the same branch on a timeout (false).
+        auto read_w = [&](int m) -> bool {
+            bool okw = true;
+            if (sid == 0) okw = wait(&bar_w, m & 1);
+            if (named_sync_or(kBarState, kStateThreads, !okw)) return false;
+            if (quad_row < K) {
+                tc_fence_after();
+                float v[32];
+                tmem_ld32(tb + lane_off + L::WT + 32 * hf, v);
+                tmem_ld_wait();
+                store_row<4>(sm + L::NWB, quad_row, 4 * hf, v, -1.f);
+            }
+            // the tile feeds U(m); W^T's columns take W^T(m + 1) after u_sig(m)
+            fence_proxy_async_smem();
+            tc_fence_before();
+            return true;
+        };
+        if (!read_w(0)) failed = true;
+        named_sync(kBarState, kStateThreads);
+        if (sw == 0 && !failed) {
             bool ok0 = true;
             if (lane == 0) ok0 = issue_u(0);
             ok0 = __shfl_sync(0xffffffffu, ok0, 0);
@@ -1019,7 +1045,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float *slot = sg + (n % 3) * 68;
             float gC;  // read with the decays: the slot is rewritten for chunk n + 3
             bool ok = !failed;
-            if (sid == 0 && ok) ok = wait(&bar_u, n & 1);
+            // U(n) complete; the key group's decays, P(n) and gamma Q(n) in place
+            if (sid == 0 && ok) ok = wait(&bar_u, n & 1) && wait(&key_ready[n & 3], (n >> 2) & 1);
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             {
                 tc_fence_after();
@@ -1052,7 +1079,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (outs) {
                     // after the issuer's S-term of O^T(n), which also reads
                     // S(n-1) (overwritten by the update below); P(n) is in
-                    // place since key_ready(n), waited before U(n)
+                    // place since key_ready(n), waited before the epilogue
                     ok = wait(&bar_os, n & 1);
                     if (ok) {
                         tc_fence_after();
@@ -1063,8 +1090,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mma_commit(&bar_o2);
                     }
                 }
-                ok = ok && wait(&bar_s, n & 1);
             }
+            // ---- -W^T(n+1) while dS(n) runs ----
+            if (n + 1 < nchunks && !read_w(n + 1)) ok = false;
+            if (sid == 0) ok = ok && wait(&bar_s, n & 1);
             if (named_sync_or(kBarState, kStateThreads, !ok)) { failed = true; break; }
             // ---- state update: S <- gamma_C S + dS, and its bf16 copy ----
             {
@@ -1761,7 +1790,7 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
                         const float *beta, uint8_t *prep, long long BH, int T, int Ts, int H,
                         cudaStream_t stream, PrepGather gth = PrepGather{nullptr, nullptr, nullptr}) {
     auto kern = prefill_prep_kernel<K, GATHER>;
-    using L = PrepLayout<GATHER ? 128 : K>;
+    using L = PrepLayout<K, GATHER>;
     static uintptr_t attr_set[64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -1774,9 +1803,10 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
         if (e != cudaSuccess) return e;
         attr_set[dev] = context_key();
     }
-    // persistent CTAs, kPrepCtasPerSm per SM (the loop is correct for any residency)
+    // persistent CTAs, prep_ctas_per_sm per SM (the loop is correct for any residency)
     const long long total = BH * ((T + 63) / 64);
-    const long long grid = std::min<long long>(total, (long long)kPrepCtasPerSm * sm_count());
+    const long long grid =
+        std::min<long long>(total, (long long)prep_ctas_per_sm(GATHER) * sm_count());
     kern<<<(unsigned)grid, kPrepThreads, L::SMEM, stream>>>(mq, mk, alpha, beta, prep, T, Ts, H,
                                                            total, gth, device_status_ptr());
     return cudaGetLastError();
