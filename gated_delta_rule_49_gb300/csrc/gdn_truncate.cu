@@ -2,12 +2,21 @@
 // blog, Sec. 3): S <- U_r U_r^T S, U_r the left singular vectors of the r
 // largest singular values, plus the singular values themselves.
 //
-// One CTA per state.  One-sided (Hestenes) Jacobi on the K columns of S, with
-// the columns held in registers in blocks of four: a group of 16 lanes (half
-// a warp) holds a pair of blocks, V / 16 entries of each of its 8 columns per
-// lane (runs of four: lane l holds entries 64 i + 4 l .. + 3), so a state
-// takes K / 8 groups (8 warps for K = 128, two per scheduler).  A sweep
-// visits every column pair once:
+// One CTA per state.  First a Householder QR, S = Q R (Q is not formed; the
+// columns in registers, 16 per warp, one barrier per reflector): the Jacobi
+// sweeps then run on the K columns of R^T, which are much closer to
+// orthogonal than those of S (the preconditioned one-sided Jacobi SVD; on
+// the prefill's final states the slowest state needs 9 to 10 sweeps instead
+// of 19 to 20).  With
+// R^T J = U_x Sigma the columns of U_x are the right singular vectors of S,
+// so Y = S U_x = (Q J) Sigma has column norms sigma_c (formed against the
+// original S), and S_r = Y_r U_x,r^T.
+// One-sided (Hestenes) Jacobi on the K columns of R^T, with the columns held
+// in registers in blocks of four: a group of 16 lanes (half a warp) holds a
+// pair of blocks, K / 16 entries of each of its 8 columns per lane (runs of
+// four: lane l holds entries 64 i + 4 l .. + 3), so a state takes K / 8
+// groups (8 warps for K = 128, two per scheduler).  A sweep visits every
+// column pair once:
 //   - block rounds: each group rotates the 16 cross pairs of its two blocks,
 //     in four mini-rounds of four disjoint pairs (top column i with bottom
 //     column (i + m) % 4); then the blocks move to the next arrangement of
@@ -39,10 +48,7 @@
 // of a low-rank state keep the sweeps going).  The rotation uses fast
 // reciprocal / square-root forms: an angle that is off in the last bits
 // leaves a residual the next sweep removes.  Sweeps repeat until one rotates
-// nothing (or max_sweeps; then the not-converged status bit is set).  The
-// converged columns are sigma_i u_i; with u_i their directions, W = U^T S
-// (against a copy of the original S) has row norms sigma_i, the r largest
-// select U_r, and S <- U_r W_r.
+// nothing (or max_sweeps; then the not-converged status bit is set).
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -50,31 +56,35 @@ namespace {
 
 constexpr int kLanes = 16;  // lanes of one column (half a warp)
 constexpr int kBlk = 4;     // columns per block
-// Orthogonality threshold |g| <= sqrt(V) eps sqrt(a b), eps = 2^-24 (float32).
-template <int V>
-__host__ __device__ constexpr float jacobi_tol() { return V == 128 ? 6.75e-7f : 3.38e-7f; }
+// Orthogonality threshold |g| <= sqrt(n) eps sqrt(a b) for columns of length
+// n, eps = 2^-24 (float32).
+template <int N>
+__host__ __device__ constexpr float jacobi_tol() {
+    return N == 128 ? 6.75e-7f : N == 64 ? 4.77e-7f : 3.38e-7f;
+}
 
 template <int V, int K>
 struct TruncLayout {
-    static constexpr int E = V / kLanes;    // entries of a column per lane
+    static constexpr int E = K / kLanes;    // entries of a column of R^T per lane
     static constexpr int NB = K / kBlk;     // blocks
     static constexpr int NS = NB / 2;       // block pairs = lane groups (8 columns each)
-    static constexpr int NT = NS * kLanes;  // threads
-    static constexpr int LDT = K + 4;       // row stride of U^T [V][LDT]
-    // output columns of a thread's 8-row tile (at least one float4)
+    static constexpr int NT = NS * kLanes;  // threads (16 columns per warp in the QR)
+    static constexpr int LDT = K + 4;       // row stride of U_x [K][LDT]
+    // columns of a thread's 8-row output tile (at least one float4): TK of
+    // S_r [V][K], TV of Y^T [K][V]
     static constexpr int TK = K * K / (NT * 8) > 4 ? K * K / (NT * 8) : 4;
+    static constexpr int TV = K * V / (NT * 8) > 4 ? K * V / (NT * 8) : 4;
     // shared memory, in floats
-    static constexpr int SZ0 = V * LDT > K * V ? V * LDT : K * V;
-    static constexpr int SZ1 = K * V > K * K ? K * V : K * K;
-    static constexpr int BOARD0 = 0;                // [K][V] columns; U^T at the end
-    static constexpr int BOARD1 = BOARD0 + SZ0;     // [K][V] columns; W [K][K] at the end
-    static constexpr int SC = BOARD1 + SZ1;         // [V][K] the original S
-    static constexpr int NRM = SC + V * K;          // [K] 1 / column norms
+    static constexpr int BOARD0 = 0;                // QR reflectors; board [K][K]; U_x [K][LDT]
+    static constexpr int BOARD1 = BOARD0 + K * LDT; // board [K][K]; U_x^T [K][K] at the end
+    static constexpr int SC = BOARD1 + K * K;       // [V][K] the original S; Y^T [K][V]
+    static constexpr int NRM = SC + V * K;          // [K] diag(R), then 1 / column norms
     static constexpr int SIG = NRM + K;             // [K] sigma^2
     static constexpr int SEL = SIG + K;             // [K] column of rank i (int)
     static constexpr size_t BYTES = (size_t)(SEL + K) * 4;
-    static_assert(V % kLanes == 0 && K % (2 * kBlk) == 0 && K <= V, "shape");
-    static_assert(TK % 4 == 0 && K % TK == 0, "tiles");
+    static_assert(V % kLanes == 0 && K % (2 * kBlk) == 0 && K <= V && NT == 2 * K, "shape");
+    static_assert(TK % 4 == 0 && K % TK == 0 && TV % 4 == 0 && V % TV == 0, "tiles");
+    static_assert((K / 8) * (V / TV) <= NT, "one Y^T tile per thread at most");
 };
 
 // Sum four per-lane values over the 16 lanes of the group, scattering: lane
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
     truncate_kernel(float *__restrict__ Sg, int r, float *__restrict__ sigma, int max_sweeps,
                     int *status) {
     using L = TruncLayout<V, K>;
-    constexpr int E = L::E, NS = L::NS, NT = L::NT, LDT = L::LDT, TK = L::TK;
+    constexpr int E = L::E, NS = L::NS, NT = L::NT, LDT = L::LDT, TK = L::TK, TV = L::TV;
     extern __shared__ __align__(16) float smf[];
     float *Sc = smf + L::SC;
     float *nrm = smf + L::NRM;
@@ -274,37 +284,139 @@ __global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
     __syncthreads();
     float *Sh = Sg + (size_t)blockIdx.x * V * K;
     {
-        // the original S, and its columns into board 0 ([K][V])
+        // the original S
         float part = 0.f;
         for (int e4 = tid * 4; e4 < V * K; e4 += NT * 4) {
             const float4 x = *reinterpret_cast<const float4 *>(Sh + e4);
             part += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
             *reinterpret_cast<float4 *>(Sc + e4) = x;
-            const int v = e4 / K, c = e4 % K;
-            smf[L::BOARD0 + (c + 0) * V + v] = x.x;
-            smf[L::BOARD0 + (c + 1) * V + v] = x.y;
-            smf[L::BOARD0 + (c + 2) * V + v] = x.z;
-            smf[L::BOARD0 + (c + 3) * V + v] = x.w;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
         if ((tid & 31) == 0) atomicAdd(&fro2, part);
     }
+
+    // ---- Householder QR, S = Q R (Q is not formed) ----
+    // Warp w owns columns w + NW cc (cc < 16, NW = K / 16 warps); its lane
+    // group g (lanes 8 g .. 8 g + 7) holds cc = 4 g .. 4 g + 3, and lane slice
+    // s = lane % 8 rows RP s .. RP s + RP - 1 of each (RP = V / 8), in
+    // registers.  Step j reflects the columns right of j with
+    // H_j = I - beta v v^T, v = A[j.., j] - alpha e_j, alpha = -sign(A[j][j]) |A[j.., j]|,
+    // v_i = 0 above row j: v is published in shared memory (two buffers) by
+    // the lane group owning column j, once its step j - 1 update of that
+    // column is done; v^T a_c is a lane-local sum and a reduction over the
+    // group's 8 lanes (the four columns of a group together).  Columns c <= j
+    // take a zero step.  One barrier per step.  R[j][j] = alpha goes to nrm[j];
+    // R[i][c], i < c, is row i of column c's registers when all is done.
+    constexpr int NW = NT / 32, RP = V / 8;
+    float *vbuf = smf + L::BOARD0;         // [2][V] reflectors (board 0 is free)
+    float *bbuf = smf + L::BOARD0 + 2 * V; // [2] beta
+    const int warp = tid >> 5, lane = tid & 31, qg = lane >> 3, qs = lane & 7;
+    const unsigned gmask = 0xffu << (8 * qg);  // the lane group
+    float a[4][RP];
+    __syncthreads();  // the original S is in place
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int k = 0; k < RP; ++k) a[q][k] = Sc[(RP * qs + k) * K + warp + NW * (4 * qg + q)];
+    // the reflector of column c (this group's column q) from its rows >= c
+    // after the earlier steps, into buffer c & 1 (called by the 8 lanes)
+    auto publish = [&](const float (&x)[RP], int c) {
+        float ss = 0.f, x0 = 0.f;
+#pragma unroll
+        for (int k = 0; k < RP; ++k) {
+            const int row = RP * qs + k;
+            if (row >= c) ss = fmaf(x[k], x[k], ss);
+            if (row == c) x0 = x[k];
+        }
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) {
+            ss += __shfl_xor_sync(gmask, ss, off);
+            x0 += __shfl_xor_sync(gmask, x0, off);  // one lane holds it, the rest 0
+        }
+        const float alpha = ss > 0.f ? -copysignf(sqrtf(ss), x0) : 0.f;
+        const float den = ss - x0 * alpha;  // v^T v / 2 (>= ss)
+        float *vb = vbuf + (c & 1) * V + RP * qs;
+#pragma unroll
+        for (int k = 0; k < RP; k += 4) {
+            float o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int row = RP * qs + k + u;
+                o[u] = row > c ? x[k + u] : row == c ? x0 - alpha : 0.f;
+            }
+            *reinterpret_cast<float4 *>(vb + k) = make_float4(o[0], o[1], o[2], o[3]);
+        }
+        if (qs == 0) {
+            bbuf[c & 1] = den > 0.f ? 1.f / den : 0.f;
+            nrm[c] = alpha;
+        }
+    };
+    if (warp == 0 && qg == 0) publish(a[0], 0);
+    for (int j = 0; j < K; ++j) {
+        __syncthreads();  // reflector j published
+        const float *vb = vbuf + (j & 1) * V + RP * qs;
+        const float beta = bbuf[j & 1];
+        float vv[RP];
+#pragma unroll
+        for (int k = 0; k < RP; k += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(vb + k);
+            vv[k] = x.x; vv[k + 1] = x.y; vv[k + 2] = x.z; vv[k + 3] = x.w;
+        }
+        float d[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < RP; k += 2) {
+                e0 = fmaf(vv[k], a[q][k], e0);
+                e1 = fmaf(vv[k + 1], a[q][k + 1], e1);
+            }
+            d[q] = e0 + e1;
+        }
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[q] += __shfl_xor_sync(0xffffffffu, d[q], off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float t = warp + NW * (4 * qg + q) > j ? beta * d[q] : 0.f;
+#pragma unroll
+            for (int k = 0; k < RP; ++k) a[q][k] = fmaf(-t, vv[k], a[q][k]);
+        }
+        // the group owning column j + 1 publishes its reflector
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (warp + NW * (4 * qg + q) == j + 1) publish(a[q], j + 1);
+    }
+    // the columns of R^T (rows of R) into board 0, [K][K]: entry i of column
+    // c is R[c][i], from row c of column i's registers
+    __syncthreads();  // every read of the reflector buffers is done
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int i = warp + NW * (4 * qg + q);
+#pragma unroll
+        for (int k = 0; k < RP; ++k) {
+            const int c = RP * qs + k;
+            if (c < K) smf[L::BOARD0 + c * K + i] = c < i ? a[q][k] : c == i ? nrm[i] : 0.f;
+        }
+    }
     __syncthreads();
+
     // the sweeps run on the columns times 2^-e, |S|_F 2^-e in [0.5, 1): an
     // exact scaling (rotations do not depend on it) that keeps the angle's
-    // squares in range; W below is formed against the original S
+    // squares in range (|R|_F = |S|_F); Y below is formed against the original S
     const int fe = fro2 > 0.f ? ilogbf(sqrtf(fro2)) + 1 : 0;
     const float scale = ldexpf(1.f, -fe);
     const float floor_g = 1e-12f * fro2 * scale * scale;
-    const float tol2 = jacobi_tol<V>() * jacobi_tol<V>();
+    const float tol2 = jacobi_tol<K>() * jacobi_tol<K>();
 
     // group grp holds columns 8 grp .. 8 grp + 7: its top block, then its bottom
     const int gbase = tid & 16;  // the group's first lane in its warp
     float X[8][E];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        load_col<E, V>(smf + L::BOARD0 + (8 * grp + j) * V, X[j], l);
+        load_col<E, K>(smf + L::BOARD0 + (8 * grp + j) * K, X[j], l);
 #pragma unroll
         for (int e = 0; e < E; ++e) X[j][e] *= scale;
     }
@@ -340,68 +452,80 @@ __global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
             float *bd = smf + ((br & 1) ? L::BOARD0 : L::BOARD1);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                store_col<E, V>(bd + (top_to + j) * V, X[j], l);
-                store_col<E, V>(bd + (bot_to + j) * V, X[4 + j], l);
+                store_col<E, K>(bd + (top_to + j) * K, X[j], l);
+                store_col<E, K>(bd + (bot_to + j) * K, X[4 + j], l);
             }
             __syncthreads();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) load_col<E, V>(bd + (8 * grp + j) * V, X[j], l);
+            for (int j = 0; j < 8; ++j) load_col<E, K>(bd + (8 * grp + j) * K, X[j], l);
         }
         converged = __syncthreads_or(any) == 0;
     }
     if (!converged && tid == 0 && status) atomicOr(status, kStatusNotConverged);
 
-    // U^T (the converged columns, unnormalised) into board 0 as [V][LDT], and
+    // U_x (the converged columns, unnormalised) into board 0 as [K][LDT], and
     // 1 / |c| per column.  Their lengths are not used as singular values:
     // rotations that are orthogonal only to rounding let the lengths drift
     // over a few thousand rotations while the directions stay accurate.  So
-    // W = U^T S is formed against the original S for every column and
-    // sigma_c = |W[c]|.
-    float *Ut = smf + L::BOARD0;
-    float *W = smf + L::BOARD1;
+    // Y = S U_x is formed against the original S and sigma_c = |Y[:, c]|.
+    float *Ux = smf + L::BOARD0;   // [K][LDT]: entry k of column c at [k][c]
+    float *UxT = smf + L::BOARD1;  // [K][K]: column c contiguous
+    float *Yt = Sc;                // [K][V], over the original S once it is read
     __syncthreads();  // every thread has read its last blocks from the boards
     {
         float ap, aq;
         quad_norms<E>(X, l, ap, aq);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 8; ++j) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) Ut[entry_v<E>(e, l) * LDT + 8 * grp + j] = X[j][e];
+            for (int e = 0; e < E; ++e) Ux[entry_v<E>(e, l) * LDT + 8 * grp + j] = X[j][e];
+            store_col<E, K>(UxT + (8 * grp + j) * K, X[j], l);
+        }
         if ((l & 3) == 0) {
             nrm[8 * grp + l / 4] = ap > 0.f ? rsqrtf(ap) : 0.f;
             nrm[8 * grp + 4 + l / 4] = aq > 0.f ? rsqrtf(aq) : 0.f;
         }
     }
     __syncthreads();
-    // W[c][k] = (1/|c|) sum_v U^T[v][c] S[v][k]: 8 x TK tiles, one per thread
-    for (int tile = tid; tile < (K / 8) * (K / TK); tile += NT) {
-        const int c0 = (tile / (K / TK)) * 8, k0 = (tile % (K / TK)) * TK;
-        float acc[8][TK];
+    // Y^T[c][v] = (1/|c|) sum_k U_x[k][c] S[v][k] against the original S:
+    // one 8 x TV tile per thread, the lanes of a warp on consecutive column
+    // tiles (so the rows of S they read are shared), k four at a time; the
+    // tiles are written over S after every thread has read it
+    const bool has_tile = tid < (K / 8) * (V / TV);
+    const int c0 = (tid % (K / 8)) * 8, v0 = (tid / (K / 8)) * TV;
+    float acc[8][TV];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < TK; ++j) acc[i][j] = 0.f;
-        for (int v = 0; v < V; ++v) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(Ut + v * LDT + c0);
-            const float4 a1 = *reinterpret_cast<const float4 *>(Ut + v * LDT + c0 + 4);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float s[TK];
+        for (int j = 0; j < TV; ++j) acc[i][j] = 0.f;
+    if (has_tile) {
+        for (int k = 0; k < K; k += 4) {
+            float sv[TV][4];
 #pragma unroll
-            for (int j = 0; j < TK; j += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(Sc + v * K + k0 + j);
-                s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+            for (int j = 0; j < TV; ++j) {
+                const float4 x = *reinterpret_cast<const float4 *>(Sc + (v0 + j) * K + k);
+                sv[j][0] = x.x; sv[j][1] = x.y; sv[j][2] = x.z; sv[j][3] = x.w;
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int u = 0; u < 4; ++u) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(Ux + (k + u) * LDT + c0);
+                const float4 a1 = *reinterpret_cast<const float4 *>(Ux + (k + u) * LDT + c0 + 4);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-                for (int j = 0; j < TK; ++j) acc[i][j] = fmaf(a[i], s[j], acc[i][j]);
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < TV; ++j) acc[i][j] = fmaf(a[i], sv[j][u], acc[i][j]);
+            }
         }
+    }
+    __syncthreads();
+    if (has_tile) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float ni = nrm[c0 + i];
 #pragma unroll
-            for (int j = 0; j < TK; j += 4)
-                *reinterpret_cast<float4 *>(W + (c0 + i) * K + k0 + j) =
+            for (int j = 0; j < TV; j += 4)
+                *reinterpret_cast<float4 *>(Yt + (c0 + i) * V + v0 + j) =
                     make_float4(acc[i][j] * ni, acc[i][j + 1] * ni, acc[i][j + 2] * ni,
                                 acc[i][j + 3] * ni);
         }
@@ -409,7 +533,7 @@ __global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
     __syncthreads();
     for (int c = tid; c < K; c += NT) {
         float s2 = 0.f;
-        for (int k = 0; k < K; ++k) s2 = fmaf(W[c * K + k], W[c * K + k], s2);
+        for (int v = 0; v < V; ++v) s2 = fmaf(Yt[c * V + v], Yt[c * V + v], s2);
         sig2[c] = s2;
     }
     __syncthreads();
@@ -424,7 +548,7 @@ __global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
         for (int i = tid; i < K; i += NT) sigma[(size_t)blockIdx.x * K + i] = sqrtf(sig2[sel[i]]);
     if (r >= K) return;  // nothing to cut (K <= V for every supported variant)
 
-    // S <- U_r W_r: 8 x TK tiles of [V][K]
+    // S <- Y_r U_x,r^T: 8 x TK tiles of [V][K]
     for (int tile = tid; tile < (V / 8) * (K / TK); tile += NT) {
         const int v0 = (tile / (K / TK)) * 8, k0 = (tile % (K / TK)) * TK;
         float acc[8][TK];
@@ -435,18 +559,19 @@ __global__ void __launch_bounds__(TruncLayout<V, K>::NT, 1)
         for (int jr = 0; jr < r; ++jr) {
             const int c = sel[jr];
             const float nc = nrm[c];
-            float w[TK];
+            const float4 y0 = *reinterpret_cast<const float4 *>(Yt + c * V + v0);
+            const float4 y1 = *reinterpret_cast<const float4 *>(Yt + c * V + v0 + 4);
+            const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+            float u[TK];
 #pragma unroll
             for (int j = 0; j < TK; j += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(W + c * K + k0 + j);
-                w[j] = x.x; w[j + 1] = x.y; w[j + 2] = x.z; w[j + 3] = x.w;
+                const float4 x = *reinterpret_cast<const float4 *>(UxT + c * K + k0 + j);
+                u[j] = x.x * nc; u[j + 1] = x.y * nc; u[j + 2] = x.z * nc; u[j + 3] = x.w * nc;
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float u = Ut[(v0 + i) * LDT + c] * nc;
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < TK; ++j) acc[i][j] = fmaf(u, w[j], acc[i][j]);
-            }
+                for (int j = 0; j < TK; ++j) acc[i][j] = fmaf(y[i], u[j], acc[i][j]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i)

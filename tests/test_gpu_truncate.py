@@ -50,6 +50,29 @@ def test_truncate_constructed_spectrum(K, V, r):
 
 
 @pytest.mark.parametrize("K,V", VARIANTS)
+@pytest.mark.parametrize("r", [1, 4, 12, 24])
+def test_truncate_without_sigma_clustered_tail(K, V, r):
+    """r well-separated leading values over a tail of many nearly equal tiny
+    ones (the near-degenerate cluster a low-rank state ends in): without
+    sigma the result is the best rank-r approximation, and the sweeps
+    converge."""
+    import torch
+    rng = np.random.default_rng(r * 11 + K)
+    n = min(V, K)
+    S, want = [], []
+    for _ in range(6):
+        a, b = _orthonormal(rng, V, n), _orthonormal(rng, K, n)
+        sig = np.concatenate([3.0 * 0.8 ** np.arange(r),
+                              1e-3 * (1.0 + 1e-4 * rng.standard_normal(n - r))])
+        S.append((a * sig) @ b.T)
+        want.append((a[:, :r] * sig[:r]) @ b[:, :r].T)
+    dS = torch.from_numpy(np.stack(S).astype(np.float32)).cuda()
+    binding.state_truncate(dS, r)
+    assert rel_err(to_np(dS), np.stack(want)) <= 1e-4
+    assert binding.gdn_get_last_device_status() == binding.GDN_OK
+
+
+@pytest.mark.parametrize("K,V", VARIANTS)
 def test_truncate_prefill_states_against_oracle(K, V):
     """Final states of a short run (decaying, gapless-looking spectra): where
     the gap at r is clear the truncation matches the oracle's; everywhere the
