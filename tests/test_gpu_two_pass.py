@@ -112,6 +112,28 @@ def test_two_pass_repeated_calls_stay_identical():
             assert torch.equal(cur[0], first[0]) and torch.equal(cur[1], first[1])
 
 
+def test_one_pass_repeated_calls_stay_identical():
+    # the one-pass form (no workspace): the key group runs up to two chunks
+    # ahead of the state group in every CTA; repeated calls over many CTAs
+    # give identical bytes
+    import torch
+    B, T, H, K, V = 8, 1024, 16, 128, 128
+    p = inputs.make_prefill(B=B, T=T, H=H, K=K, seed=6)
+    d = problem_to_dev(p)
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device="cuda")
+    ST = torch.empty((B, H, V, K), device="cuda")
+    first = None
+    for _ in range(10):
+        binding.gdn_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], None, o, ST, B, T, H,
+                            K, V, binding.GDN_BF16, None, 0)
+        assert binding.gdn_get_last_device_status() == binding.GDN_OK
+        cur = (o.view(torch.int16).clone(), ST.view(torch.int32).clone())
+        if first is None:
+            first = cur
+        else:
+            assert torch.equal(cur[0], first[0]) and torch.equal(cur[1], first[1])
+
+
 @pytest.mark.parametrize("want_o,want_S", [(True, False), (False, True)])
 def test_two_pass_outputs_or_state_alone(want_o, want_S):
     import torch
