@@ -29,8 +29,12 @@
 //     block products of A and P on warp-level MMAs (one row block per warp),
 //     the inverse (the scalar prefill's split-bf16 blocked inverse), W^T on
 //     tcgen05, and the state pass's operands -- T_b^T, P, -W^T, Q (.) e^G,
-//     K (.) e^(G_C - G), e^(G_C) and (GDN2) Z -- written to the workspace as
+//     K (.) e^(G_C - G) and e^(G_C) -- written to the workspace as
 //     their swizzled shared-memory images.
+//   gated_z_kernel (GDN2): Z = w (.) V into the same workspace, element by
+//     element, ahead of the key-side pass: HBM-bound work that costs the
+//     instruction-bound key-side pass more when interleaved with its own
+//     (0.648 against 0.615 ms per call on the gated workload).
 //   prefill_gated_state_kernel: one CTA per sequence; the scalar state pass's
 //     chain without its key group: U~ by an issuer thread, U, dS and O by the
 //     state thread, the float32 state in registers with a bf16 copy in TMEM.
@@ -102,8 +106,7 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
     prefill_gated_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                               const __grid_constant__ CUtensorMap tm_k,
                               const float *__restrict__ alpha, const float *__restrict__ beta,
-                              const float *__restrict__ bgate, const float *__restrict__ wgate,
-                              const __nv_bfloat16 *__restrict__ v, uint8_t *__restrict__ ws,
+                              const float *__restrict__ bgate, uint8_t *__restrict__ ws,
                               int T, int H, long long nchunk_all, int *status) {
     using L = GpLayout;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
         if (named_sync_or(kBarKey, kGpThreads, !ok)) { failed = true; break; }
 
         // ---- scaled tiles, 16-byte pieces: K~ (.) e^G (W's operand), the
-        // ---- erase rows E (GDN2, A's left operand), Q (.) e^G, K (.) e^(G_C - G), Z ----
+        // ---- erase rows E (GDN2, A's left operand), Q (.) e^G, K (.) e^(G_C - G) ----
 #pragma unroll
         for (int p = tid; p < 1024; p += kGpThreads) {
             const int t = p >> 4, c16 = p & 15, c0 = c16 * 8;
@@ -244,25 +247,6 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
                 *reinterpret_cast<uint4 *>(sm + L::AF + off) = make_uint4(ev[0], ev[1], ev[2], ev[3]);
             *reinterpret_cast<uint4 *>(out + kGwQ + off) = make_uint4(qt[0], qt[1], qt[2], qt[3]);
             *reinterpret_cast<uint4 *>(out + kGwK + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-            if (GATE == kGdn2) {
-                uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                if (t < nvalid) {
-                    const size_t th = th0 + (size_t)t * H;
-                    const uint4 vr = *reinterpret_cast<const uint4 *>(v + th * 128 + c0);
-                    const float4 *wp = reinterpret_cast<const float4 *>(wgate + th * 128 + c0);
-                    const float4 w0 = wp[0], w1 = wp[1];
-                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                    const uint32_t vw[4] = {vr.x, vr.y, vr.z, vr.w};
-                    uint32_t zw[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 vf = bf16x2_to_f2(vw[e]);
-                        zw[e] = pack_bf16(wv[2 * e] * vf.x, wv[2 * e + 1] * vf.y);
-                    }
-                    z = make_uint4(zw[0], zw[1], zw[2], zw[3]);
-                }
-                *reinterpret_cast<uint4 *>(out + kGwZ + off) = z;
-            }
         }
         named_sync(kBarKey, kGpThreads);
 
@@ -391,6 +375,63 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tb, 64);
+    }
+}
+
+// ---------------------------------------------------------------- GDN2 write content
+// Z = w (.) V of every chunk into the workspace as its two 128-byte-swizzled
+// [64][64] bf16 boxes (rows past T zero), one 16-byte piece (8 channels of a
+// token) per thread and step, four steps' loads issued together, eight CTAs
+// per SM.  (Run beside the key-side pass instead, on a second stream with one
+// CTA per SM in the registers that pass leaves, it had too few loads in
+// flight: 0.63 ms per call.)
+constexpr int kZThreads = 256, kZUnroll = 4, kZCtasPerSm = 8;
+__global__ void __launch_bounds__(kZThreads)
+    gated_z_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ wgate,
+                   uint8_t *__restrict__ ws, int T, int H, long long npieces) {
+    const int nch = (T + 63) / 64;
+    const long long stride = (long long)gridDim.x * kZThreads;
+    for (long long p0 = (long long)blockIdx.x * kZThreads + threadIdx.x; p0 < npieces;
+         p0 += stride * kZUnroll) {
+        uint4 vr[kZUnroll];
+        float4 w0[kZUnroll], w1[kZUnroll];
+        bool live[kZUnroll];
+#pragma unroll
+        for (int u = 0; u < kZUnroll; ++u) {
+            const long long p = p0 + u * stride;
+            const long long j = p >> 10;  // chunk
+            const int t = (int)(p & 1023) >> 4, c0 = ((int)p & 15) * 8;
+            const long long seq = j / nch;
+            const int n = (int)(j - seq * nch);
+            live[u] = p < npieces && n * 64 + t < T;
+            vr[u] = make_uint4(0u, 0u, 0u, 0u);
+            w0[u] = w1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (live[u]) {
+                const size_t th = ((size_t)(seq / H) * T + (size_t)n * 64 + t) * H + seq % H;
+                vr[u] = __ldg(reinterpret_cast<const uint4 *>(v + th * 128 + c0));
+                const float4 *wp = reinterpret_cast<const float4 *>(wgate + th * 128 + c0);
+                w0[u] = __ldg(wp);
+                w1[u] = __ldg(wp + 1);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kZUnroll; ++u) {
+            const long long p = p0 + u * stride;
+            if (p >= npieces) break;
+            const long long j = p >> 10;
+            const int t = (int)(p & 1023) >> 4, c16 = (int)p & 15;
+            const float wv[8] = {w0[u].x, w0[u].y, w0[u].z, w0[u].w,
+                                 w1[u].x, w1[u].y, w1[u].z, w1[u].w};
+            const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+            uint32_t zw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 vf = bf16x2_to_f2(vw[e]);
+                zw[e] = live[u] ? pack_bf16(wv[2 * e] * vf.x, wv[2 * e + 1] * vf.y) : 0u;
+            }
+            *reinterpret_cast<uint4 *>(ws + (size_t)j * gw_chunk_bytes(kGdn2) + kGwZ +
+                                       piece_off(t, c16)) = make_uint4(zw[0], zw[1], zw[2], zw[3]);
+        }
     }
 }
 
@@ -813,9 +854,22 @@ cudaError_t launch_gated_tc_t(const void *q, const void *k, const void *v, const
     const long long total = BH * ((T + 63) / 64);
     const long long grid = std::min<long long>(total, (long long)kGpCtasPerSm * sm_count());
     int *status = device_status_ptr();
-    prep<<<(unsigned)grid, kGpThreads, GpLayout::SMEM, stream>>>(
-        mq, mk, alpha, beta, bgate, wgate, static_cast<const __nv_bfloat16 *>(v), ws, T, H, total,
-        status);
+    if (GATE != kGdn2) {
+        prep<<<(unsigned)grid, kGpThreads, GpLayout::SMEM, stream>>>(mq, mk, alpha, beta, bgate,
+                                                                     ws, T, H, total, status);
+    } else {
+        // Z first, then the key-side pass (both write their own parts of the
+        // workspace chunks)
+        const long long zgrid =
+            std::min<long long>((total * 1024 + kZThreads - 1) / kZThreads,
+                                (long long)kZCtasPerSm * sm_count());
+        gated_z_kernel<<<(unsigned)zgrid, kZThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(v), wgate, ws, T, H, total * 1024);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        prep<<<(unsigned)grid, kGpThreads, GpLayout::SMEM, stream>>>(mq, mk, alpha, beta, bgate,
+                                                                     ws, T, H, total, status);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     state<<<(unsigned)BH, kGsThreads, GsLayout::SMEM, stream>>>(mv, mo, S0, o != nullptr, ST, T,
