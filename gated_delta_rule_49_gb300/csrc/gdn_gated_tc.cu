@@ -32,9 +32,11 @@
 //     K (.) e^(G_C - G) and e^(G_C) -- written to the workspace as
 //     their swizzled shared-memory images.
 //   gated_z_kernel (GDN2): Z = w (.) V into the same workspace, element by
-//     element, ahead of the key-side pass: HBM-bound work that costs the
-//     instruction-bound key-side pass more when interleaved with its own
-//     (0.648 against 0.615 ms per call on the gated workload).
+//     element, on a second stream beside the key-side pass: HBM-bound work
+//     that cost the instruction-bound key-side pass ~128 us interleaved with
+//     its own, and runs in that pass's shadow here (0.578 ms per call on the
+//     gated workload; 0.606 ms with the two kernels one after the other, and
+//     0.647 ms with Z inside the key-side pass).
 //   prefill_gated_state_kernel: one CTA per sequence; the scalar state pass's
 //     chain without its key group: U~ by an issuer thread, U, dS and O by the
 //     state thread, the float32 state in registers with a bf16 copy in TMEM.
@@ -43,6 +45,7 @@
 #include "gdn_chunk.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace gdn {
 namespace {
@@ -380,46 +383,48 @@ __global__ void __launch_bounds__(kGpThreads, kGpCtasPerSm)
 
 // ---------------------------------------------------------------- GDN2 write content
 // Z = w (.) V of every chunk into the workspace as its two 128-byte-swizzled
-// [64][64] bf16 boxes (rows past T zero), one 16-byte piece (8 channels of a
-// token) per thread and step, four steps' loads issued together, eight CTAs
-// per SM.  (Run beside the key-side pass instead, on a second stream with one
-// CTA per SM in the registers that pass leaves, it had too few loads in
-// flight: 0.63 ms per call.)
-constexpr int kZThreads = 256, kZUnroll = 4, kZCtasPerSm = 8;
-__global__ void __launch_bounds__(kZThreads)
-    gated_z_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ wgate,
-                   uint8_t *__restrict__ ws, int T, int H, long long npieces) {
+// [64][64] bf16 boxes.  One 16-byte piece (8 channels of a token and head) per
+// thread and step, taken in the memory order of v and w (piece p covers
+// elements 8 p .. 8 p + 7 of both: contiguous streams), four steps' loads
+// issued together; then the rows of each sequence's last chunk past T are
+// zeroed.  One 128-thread CTA per SM, beside the key-side pass's two: no
+// shared memory and at most 80 registers a thread (what those two CTAs leave
+// on an SM), which the minimum of six resident CTAs in the launch bounds asks
+// of the compiler.
+constexpr int kZThreads = 128, kZUnroll = 4;
+__device__ __forceinline__ uint8_t *z_piece(uint8_t *ws, int T, int H, long long tok, int h,
+                                            int c16) {
     const int nch = (T + 63) / 64;
+    const long long b = tok / T;
+    const int t = (int)(tok - b * T);
+    const long long j = (b * H + h) * nch + (t >> 6);
+    return ws + (size_t)j * gw_chunk_bytes(kGdn2) + kGwZ + piece_off(t & 63, c16);
+}
+__global__ void __launch_bounds__(kZThreads, 6)
+    gated_z_kernel(const __nv_bfloat16 *__restrict__ v, const float *__restrict__ wgate,
+                   uint8_t *__restrict__ ws, int B, int T, int H) {
+    const long long npieces = (long long)B * T * H * 16;
     const long long stride = (long long)gridDim.x * kZThreads;
     for (long long p0 = (long long)blockIdx.x * kZThreads + threadIdx.x; p0 < npieces;
          p0 += stride * kZUnroll) {
         uint4 vr[kZUnroll];
         float4 w0[kZUnroll], w1[kZUnroll];
-        bool live[kZUnroll];
 #pragma unroll
         for (int u = 0; u < kZUnroll; ++u) {
             const long long p = p0 + u * stride;
-            const long long j = p >> 10;  // chunk
-            const int t = (int)(p & 1023) >> 4, c0 = ((int)p & 15) * 8;
-            const long long seq = j / nch;
-            const int n = (int)(j - seq * nch);
-            live[u] = p < npieces && n * 64 + t < T;
             vr[u] = make_uint4(0u, 0u, 0u, 0u);
             w0[u] = w1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (live[u]) {
-                const size_t th = ((size_t)(seq / H) * T + (size_t)n * 64 + t) * H + seq % H;
-                vr[u] = __ldg(reinterpret_cast<const uint4 *>(v + th * 128 + c0));
-                const float4 *wp = reinterpret_cast<const float4 *>(wgate + th * 128 + c0);
-                w0[u] = __ldg(wp);
-                w1[u] = __ldg(wp + 1);
+            if (p < npieces) {
+                vr[u] = __ldcs(reinterpret_cast<const uint4 *>(v) + p);
+                w0[u] = __ldcs(reinterpret_cast<const float4 *>(wgate) + 2 * p);
+                w1[u] = __ldcs(reinterpret_cast<const float4 *>(wgate) + 2 * p + 1);
             }
         }
 #pragma unroll
         for (int u = 0; u < kZUnroll; ++u) {
             const long long p = p0 + u * stride;
             if (p >= npieces) break;
-            const long long j = p >> 10;
-            const int t = (int)(p & 1023) >> 4, c16 = (int)p & 15;
+            const long long row = p >> 4;  // token-head
             const float wv[8] = {w0[u].x, w0[u].y, w0[u].z, w0[u].w,
                                  w1[u].x, w1[u].y, w1[u].z, w1[u].w};
             const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
@@ -427,12 +432,51 @@ __global__ void __launch_bounds__(kZThreads)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 vf = bf16x2_to_f2(vw[e]);
-                zw[e] = live[u] ? pack_bf16(wv[2 * e] * vf.x, wv[2 * e + 1] * vf.y) : 0u;
+                zw[e] = pack_bf16(wv[2 * e] * vf.x, wv[2 * e + 1] * vf.y);
             }
-            *reinterpret_cast<uint4 *>(ws + (size_t)j * gw_chunk_bytes(kGdn2) + kGwZ +
-                                       piece_off(t, c16)) = make_uint4(zw[0], zw[1], zw[2], zw[3]);
+            *reinterpret_cast<uint4 *>(z_piece(ws, T, H, row / H, (int)(row % H), (int)p & 15)) =
+                make_uint4(zw[0], zw[1], zw[2], zw[3]);
         }
     }
+    // rows of the last chunk past T: zero
+    const int pad = (64 - T % 64) % 64;
+    const long long npad = (long long)B * H * pad * 16;
+    for (long long p = (long long)blockIdx.x * kZThreads + threadIdx.x; p < npad; p += stride) {
+        const int c16 = (int)(p & 15);
+        const long long r = p >> 4;  // (b, h, padded row)
+        const int pr = (int)(r % pad);
+        const long long bh = r / pad;
+        const int nch = (T + 63) / 64;
+        const long long j = bh * nch + nch - 1;
+        *reinterpret_cast<uint4 *>(ws + (size_t)j * gw_chunk_bytes(kGdn2) + kGwZ +
+                                   piece_off(T % 64 + pr, c16)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// The side stream for gated_z_kernel on the current device and context, with
+// the fork / join events; created once, nullptr when that fails (the kernel
+// then runs on the caller's stream).
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    uintptr_t ctx = 0;
+};
+std::mutex g_side_mu;  // also held while a call enqueues its fork and join
+SideStream g_side[64];
+SideStream *side_stream(int dev) {
+    SideStream &ss = g_side[dev];
+    if (ss.ctx != context_key() || !ss.s) {
+        ss = SideStream{};
+        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            ss = SideStream{};
+            return nullptr;
+        }
+        ss.ctx = context_key();
+    }
+    return &ss;
 }
 
 // ---------------------------------------------------------------- state pass
@@ -847,6 +891,12 @@ cudaError_t launch_gated_tc_t(const void *q, const void *k, const void *v, const
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)GsLayout::SMEM);
+        // the Z kernel (no shared memory) shares SMs with the key-side pass:
+        // the same carveout, so that an SM it reaches first still takes that
+        // pass's two CTAs
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gated_z_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         attr_set[dev] = context_key();
     }
@@ -858,17 +908,35 @@ cudaError_t launch_gated_tc_t(const void *q, const void *k, const void *v, const
         prep<<<(unsigned)grid, kGpThreads, GpLayout::SMEM, stream>>>(mq, mk, alpha, beta, bgate,
                                                                      ws, T, H, total, status);
     } else {
-        // Z first, then the key-side pass (both write their own parts of the
-        // workspace chunks)
-        const long long zgrid =
-            std::min<long long>((total * 1024 + kZThreads - 1) / kZThreads,
-                                (long long)kZCtasPerSm * sm_count());
-        gated_z_kernel<<<(unsigned)zgrid, kZThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(v), wgate, ws, T, H, total * 1024);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        // Z on the side stream, forked from the caller's stream (after its
+        // writes of v and w) and joined back before the state pass
+        std::lock_guard<std::mutex> lock(g_side_mu);
+        SideStream *ss = side_stream(dev);
+        cudaStream_t zs = ss ? ss->s : stream;
+        cudaError_t e = cudaSuccess;
+        // (the key-side pass is launched first, so that its CTAs are placed
+        // first; the fork event marks the caller's earlier work only)
+        if (ss) {
+            e = cudaEventRecord(ss->fork, stream);
+            if (e != cudaSuccess) return e;
+        }
         prep<<<(unsigned)grid, kGpThreads, GpLayout::SMEM, stream>>>(mq, mk, alpha, beta, bgate,
                                                                      ws, T, H, total, status);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (ss) {
+            e = cudaStreamWaitEvent(zs, ss->fork, 0);
+            if (e != cudaSuccess) return e;
+        }
+        gated_z_kernel<<<(unsigned)sm_count(), kZThreads, 0, zs>>>(
+            static_cast<const __nv_bfloat16 *>(v), wgate, ws, B, T, H);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (ss) {
+            e = cudaEventRecord(ss->join, zs);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ss->join, 0);
+            if (e != cudaSuccess) return e;
+        }
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

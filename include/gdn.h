@@ -307,6 +307,12 @@ GDN_API int gdn_prefill_gated(const void *q, const void *k, const void *v, const
  *   workspace  >= gdn_prefill_gated_chunked_workspace_size(...) bytes,
  *              16-byte aligned, caller-owned device memory (about 64.5 KiB
  *              per 64-token chunk per (b, h) for KDA, 80.5 KiB for GDN2)
+ *   b, w       (GDN2) 16-byte aligned, like q, k and v
+ *
+ * For GDN2 the call forks one elementwise kernel (w (.) v into the
+ * workspace) onto a stream of the library's own, one per device, and joins
+ * it back into `stream` before the state pass: work on `stream` stays
+ * ordered as usual, and stream capture records the fork and the join.
  *
  * Supported: gate KDA or GDN2, K = V = 128, bf16; anything else returns
  * GDN_ERR_UNSUPPORTED (gdn_prefill_gated covers it token by token).  The
