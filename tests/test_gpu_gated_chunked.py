@@ -113,6 +113,56 @@ def test_gated_chunked_in_place_and_repeatable():
     assert rel_err(to_np(firsts[1].view(torch.float32)), S_ref) <= TOL["bf16"]
 
 
+def test_gdn2_chunked_graph_capture_and_single_calls():
+    """GDN2 forks its write-content kernel onto a second stream and joins it
+    back: eager calls, a single call after an idle GPU, and a CUDA graph
+    replay of the call give identical bytes."""
+    import torch
+    p = inputs.make_channel_gated(seed=9, B=2, T=333, H=3, K=128, V=128, gate="gdn2",
+                                  with_S0=True)
+    B, T, H, K = p.k.shape
+    gate = binding.GATES["gdn2"]
+    need = binding.gdn_prefill_gated_chunked_workspace_size(B, T, H, K, 128, gate, binding.GDN_BF16)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    q, k, v = to_dev(p.q, "bf16"), to_dev(p.k, "bf16"), to_dev(p.v, "bf16")
+    al, bg, wg, S0 = _f32(p.alpha), _f32(p.b), _f32(p.w), _f32(p.S0)
+    o = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device="cuda")
+    ST = torch.empty((B, H, 128, K), device="cuda")
+
+    def call():
+        binding.gdn_prefill_gated_chunked(q, k, v, al, None, bg, wg, S0, o, ST, B, T, H, K, 128,
+                                          gate, binding.GDN_BF16, ws, need)
+
+    call()
+    torch.cuda.synchronize()
+    ref = (o.view(torch.int16).clone(), ST.view(torch.int32).clone())
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(to_np(o), o_ref) <= TOL["bf16"] and rel_err(to_np(ST), S_ref) <= TOL["bf16"]
+    for _ in range(3):  # single calls, the GPU idle in between
+        o.zero_()
+        ST.zero_()
+        torch.cuda.synchronize()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), ref[0]) and torch.equal(ST.view(torch.int32), ref[1])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()  # warm-up on the capturing stream
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    o.zero_()
+    ST.zero_()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert binding.gdn_get_last_device_status() == binding.GDN_OK
+    assert torch.equal(o.view(torch.int16), ref[0]) and torch.equal(ST.view(torch.int32), ref[1])
+
+
 def test_gated_chunked_rejects():
     """Unsupported shapes and gates, a short workspace: errors, no launch."""
     import torch
