@@ -694,7 +694,9 @@ def bench_gated(args, torch, binding, inputs, peaks, barrier, max_over_ranks, wo
         gbs = byts / (mc / 1e3) / 1e9
         out[gate] = {"ms_per_step": mc, "tokens_per_s": B * T * world / (mc / 1e3),
                      "achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
-                     "algorithmic_bytes": byts, "launches": 2 * steps,
+                     "algorithmic_bytes": byts,
+                     # key-side and state passes; GDN2 adds its write-content kernel
+                     "launches": (3 if gate == "gdn2" else 2) * steps,
                      "workspace_bytes": need, "device_status": status,
                      "token_kernel": {"ms_per_step": mt,
                                       "tokens_per_s": B * T * world / (mt / 1e3),
