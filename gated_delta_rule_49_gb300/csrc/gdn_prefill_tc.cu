@@ -106,6 +106,24 @@ __device__ __forceinline__ void issue_kq_kt(uint32_t d1, uint32_t stg, uint32_t 
     }
 }
 
+// A_ts for s in [s0, s0 + 32) of row t (float32, into AF) from k_t . k_s in v
+__device__ __forceinline__ void chunk_a_row(const float (&v)[32], int t, int s0,
+                                            const float *G2, const float *bet, float *AF) {
+    const float gt = G2[t], bt = bet[t];
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
+        const float gs[4] = {g.x, g.y, g.z, g.w};
+        float a[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+            const int s = s0 + i + e2;
+            a[e2] = s < t ? bt * decay_exp2(gt - gs[e2]) * v[i + e2] : 0.f;
+        }
+        *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) = make_float4(a[0], a[1], a[2], a[3]);
+    }
+}
+
 // A (float32, rows 0..63 of AF) and P (bf16 operand tile) from [K;Q] K^T in
 // TMEM; the thread holds TMEM lane quad_row, columns [32 colhalf, +32):
 //   A_ts = beta_t 2^(G_t - G_s) (k_t . k_s) for s < t, else 0
@@ -122,19 +140,7 @@ __device__ __forceinline__ void chunk_ap(uint32_t taddr, int quad_row, int colha
     const float gt = G2[t];
     const int s0 = 32 * colhalf;
     if (quad_row < 64) {
-        const float bt = bet[t];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 g = *reinterpret_cast<const float4 *>(G2 + s0 + i);
-            const float gs[4] = {g.x, g.y, g.z, g.w};
-            float a[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                const int s = s0 + i + e2;
-                a[e2] = s < t ? bt * decay_exp2(gt - gs[e2]) * v[i + e2] : 0.f;
-            }
-            *reinterpret_cast<float4 *>(AF + t * kLD + s0 + i) = make_float4(a[0], a[1], a[2], a[3]);
-        }
+        chunk_a_row(v, t, s0, G2, bet, AF);
     } else if (Ptile != nullptr) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -281,18 +287,20 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
 // just the k boxes.  The gathering form loads the full-width q and k boxes.
 template <int K, bool GATHER>
 struct PrepLayout {
-    static constexpr uint32_t KC0 = 0, QC0 = 8192;
-    static constexpr uint32_t KC1 = GATHER ? 16384 : 8192, QC1 = 24576;  // QC*: gathering only
-    static constexpr uint32_t STAGE = GATHER ? 32768 : (K == 128 ? 16384 : 8192);
+    // gathering: the q and k boxes of all 128 channels.  Otherwise each k box
+    // is loaded twice, 8 KB apart, so that the product's A operand (128 rows)
+    // is [K; K] and TMEM lanes 64..127 hold K K^T again
+    static constexpr uint32_t KC0 = 0, QC0 = 8192, KDUP = 8192;
+    static constexpr uint32_t KC1 = 16384, QC1 = 24576;  // KC1: K = 128 or gathering
+    static constexpr uint32_t STAGE = (GATHER || K == 128) ? 32768 : 16384;
     static constexpr uint32_t AF = STAGE;                  // float [64][68]
     static constexpr uint32_t GATE = AF + 64 * kLD * 4;    // G2, gamma, beta
     static constexpr uint32_t END = GATE + 3 * 64 * 4;
     static constexpr uint32_t KQ_BYTES = 4u * 8192u;
-    static constexpr uint32_t K_BYTES = (K == 128 ? 2u : 1u) * 8192u;
+    static constexpr uint32_t K_BYTES = (K == 128 ? 4u : 2u) * 8192u;
     static constexpr size_t SMEM = END;
-    static_assert(GATHER || AF >= (K == 128 ? KC1 : KC0) + 8192,
-                  "rows 64..127 of the last box's A read");
-    static_assert(GATHER || 64 * kLD * 4 >= 8192, "the A scratch covers those rows");
+    static_assert(GATHER || STAGE >= (K == 128 ? KC1 : KC0) + 16384, "[K; K] of the last box");
+    static_assert(!GATHER || 64 * kLD * 4 >= 16384, "the A scratch holds the gathered [K'; K']");
 };
 constexpr int kPrepThreads = 128;
 // resident CTAs per SM (five or six with the k-only stage ran slower: the
@@ -374,9 +382,11 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
         mbar_arrive_expect_tx(&kq_full, GATHER ? L::KQ_BYTES : L::K_BYTES);
         tma_load_4d(sm + L::KC0, &tm_k, &kq_full, 0, h, n * 64, b);
         if (GATHER) tma_load_4d(sm + L::QC0, &tm_q, &kq_full, 0, h, n * 64, b);
+        else tma_load_4d(sm + L::KC0 + L::KDUP, &tm_k, &kq_full, 0, h, n * 64, b);
         if (K == 128 || GATHER) {
             tma_load_4d(sm + L::KC1, &tm_k, &kq_full, 64, h, n * 64, b);
             if (GATHER) tma_load_4d(sm + L::QC1, &tm_q, &kq_full, 64, h, n * 64, b);
+            else tma_load_4d(sm + L::KC1 + L::KDUP, &tm_k, &kq_full, 64, h, n * 64, b);
         }
     };
     float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
@@ -434,7 +444,7 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
             const int4 i0 = __ldg(ip), i1 = __ldg(ip + 1);
             const int cs[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
             bool bad = false;
-            uint8_t *tile = sm + L::AF;  // [K';Q'] in the A scratch, read before A is written
+            uint8_t *tile = sm + L::AF;  // [K';K'] in the A scratch, read before A is written
 #pragma unroll 1
             for (int pass = 0; pass < 8; ++pass) {
                 const int r = 32 * warp + 4 * pass + sub;  // row of [K'; Q']
@@ -463,7 +473,11 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
                 w.y = pack_bf16(gv[2] * inv, gv[3] * inv);
                 w.z = pack_bf16(gv[4] * inv, gv[5] * inv);
                 w.w = pack_bf16(gv[6] * inv, gv[7] * inv);
-                *reinterpret_cast<uint4 *>(tile + swz128(r, cl)) = w;
+                // the tile is [K'; K'] (A's 128 rows), the q' rows go out only
+                if (r < 64) {
+                    *reinterpret_cast<uint4 *>(tile + swz128(r, cl)) = w;
+                    *reinterpret_cast<uint4 *>(tile + swz128(r + 64, cl)) = w;
+                }
                 if (t < nvalid && bounds_ok(seq < nchunk_all / nch && n * 64 + t < T, status))
                     reinterpret_cast<uint4 *>((r < 64 ? gth.kg : gth.qg) +
                                               (((size_t)b * T + (size_t)n * 64 + t) * H + h) * 64)[cl] =
@@ -500,9 +514,14 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
         if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
         uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T'^T | T''^T]
         tc_fence_after();
-        if (warp < 2)  // TMEM lanes 0..63: the K rows; both 32-column halves per thread
-            for (int ch = 0; ch < 2; ++ch)
-                chunk_ap(tb + lane_off + 32 * ch, quad_row, ch, G2, bet, AF, nullptr);
+        {   // lanes 64..127 repeat K K^T: warps 0-1 form columns 0..31 of A's
+            // rows, warps 2-3 columns 32..63
+            const int ch = warp >> 1, t = quad_row & 63;
+            float v[32];
+            tmem_ld32(tb + lane_off + 32 * ch, v);
+            tmem_ld_wait();
+            chunk_a_row(v, t, 32 * ch, G2, bet, AF);
+        }
         tc_fence_before();
         named_sync(kBarKey, kPrepThreads);
         chunk_inverse_tprime<kPrepThreads>(AF, bet, gam, out + kPrepTP, out + kPrepTPP, tid);
