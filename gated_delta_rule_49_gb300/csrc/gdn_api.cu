@@ -123,7 +123,8 @@ size_t gdn_prefill_two_pass_workspace_size(int B, int T, int H, int K, int V, gd
         return 0;
     if ((long long)B * H > 0x7fffffffLL) return 0;
     const gdn::SegShape sh = gdn::segment_shape(B * H, T, K, gdn::sm_count());
-    return gdn::prefill_prep_offset(sh) + gdn::prefill_prep_bytes((long long)B * H, T);
+    return gdn::prefill_prep_offset(sh) + gdn::prefill_prep_bytes((long long)B * H, T) +
+           gdn::prefill_x_bytes(sh, (long long)B * H, T);
 }
 
 namespace {

@@ -89,12 +89,16 @@ SegShape segment_shape(int BH, int T, int K, int nsm);
 // whenever workspace_bytes >= offset + bytes.
 size_t prefill_prep_offset(const SegShape &sh);
 size_t prefill_prep_bytes(long long BH, int T);
+// Segment-parallel problems: the X buffer ([B, T, H, 128] bf16) right after
+// the key-side operands, with which the two-pass form needs no second pass
+// over the segments (0 for whole sequences).
+size_t prefill_x_bytes(const SegShape &sh, long long BH, int T);
 
 // The two-pass prefill from full-width q/k (K_in = 128) on a state pruned to
 // 64 channels: the pruning prologue runs inside the key-side pass.  Workspace
 // byte offsets of its parts (segment slots first, at 0).
 struct GatheredLayout {
-    size_t prep, qg, kg, total;
+    size_t prep, qg, kg, x, total;  // x: the segments' X buffer (empty for whole sequences)
 };
 GatheredLayout gathered_layout(int B, int T, int H);
 cudaError_t launch_prefill_gathered(const void *q_full, const void *k_full, const int *idx,

@@ -204,9 +204,14 @@ __device__ __forceinline__ int p_extra_unit(int warp) {
 //            same recurrence run on the rows of the identity with v = 0).
 //   kSecond: segments p >= 1 again from their start states (slot S, filled by
 //            the combine kernel) with outputs; the last one writes S_T.
+//   kFirstX: kFirst with every run writing outputs: the zero-start runs o0 of
+//            their segment into o, the identity-start runs (v = 0) X into the
+//            X buffer; o = o0 + S_start X^T then replaces the second pass.
 // The end state of a segment is affine in its start state (the update is
-// S -> alpha S (I - beta k k^T) + beta v k^T), so S_end = S_start M + H.
-enum SegMode : int { kWhole = 0, kFirst = 1, kSecond = 2 };
+// S -> alpha S (I - beta k k^T) + beta v k^T), so S_end = S_start M + H; so
+// is every output of the segment: o_t = o0_t + S_start x_t, where x_t is the
+// output of the same recurrence run on the rows of the identity with v = 0.
+enum SegMode : int { kWhole = 0, kFirst = 1, kSecond = 2, kFirstX = 3 };
 struct SegPlan {
     int mode;
     int nseg;
@@ -222,12 +227,13 @@ struct SegTask {
     float *stp;        // end-state destination (nullptr: none)
     bool zero_v;       // v = 0 (transition-matrix run)
     bool outputs;      // this run writes o
+    bool out_x;        // ... into the X buffer instead
 };
 __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int T,
                                                 const float *S0, float *ST, int BH) {
     constexpr int V = 128;
     const size_t VK = (size_t)V * K;
-    SegTask tk{blockIdx.x, 0, T, nullptr, false, nullptr, false, true};
+    SegTask tk{blockIdx.x, 0, T, nullptr, false, nullptr, false, true, false};
     if (plan.mode == kWhole) {
         if (S0) tk.s0p = S0 + tk.seq * VK;
         if (ST) tk.stp = ST + tk.seq * VK;
@@ -237,7 +243,8 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
         return plan.ws + ((kind * (size_t)BH + sq) * plan.nseg + p) * VK;
     };
     int p;
-    if (plan.mode == kFirst) {
+    if (plan.mode == kFirst || plan.mode == kFirstX) {
+        const bool x = plan.mode == kFirstX;
         tk.seq = blockIdx.x / (2 * plan.nseg - 1);
         const int i = blockIdx.x % (2 * plan.nseg - 1);
         p = (i + 1) / 2;
@@ -245,13 +252,14 @@ __device__ __forceinline__ SegTask segment_task(const SegPlan &plan, int K, int 
             if (S0) tk.s0p = S0 + tk.seq * VK;
             tk.stp = slot(0, tk.seq, 0);  // end of segment 0 (E)
         } else if (i & 1) {
-            tk.stp = slot(0, tk.seq, p);  // zero start: H
-            tk.outputs = false;
+            tk.stp = slot(0, tk.seq, p);  // zero start: H (and o0)
+            tk.outputs = x;
         } else {
-            tk.s0_identity = true;        // identity start, v = 0: M
+            tk.s0_identity = true;        // identity start, v = 0: M (and X)
             tk.zero_v = true;
             tk.stp = slot(1, tk.seq, p);
-            tk.outputs = false;
+            tk.outputs = x;
+            tk.out_x = x;
         }
     } else {
         tk.seq = blockIdx.x / (plan.nseg - 1);
@@ -644,7 +652,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ alpha,
+                         const __grid_constant__ CUtensorMap tm_o,
+                         const __grid_constant__ CUtensorMap tm_x, const float *__restrict__ alpha,
                          const float *__restrict__ beta, const float *__restrict__ S0,
                          bool want_o, float *__restrict__ ST, int T, int Ts, int H, int BH,
                          SegPlan plan, const uint8_t *__restrict__ prep, int *status) {
@@ -674,6 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int t0 = tk.t0, t1 = tk.t1;
     const bool zero_v = tk.zero_v;
     const bool outs = want_o && tk.outputs;
+    const CUtensorMap *tm_out = tk.out_x ? &tm_x : &tm_o;  // where the outputs go
     const int b = (int)(seq / H), h = (int)(seq % H);
     const int nchunks = (t1 - t0 + 63) / 64;
     const uint32_t base = smem_u32(sm);
@@ -824,7 +834,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            if (outs) tma_prefetch_desc(&tm_o);
+            if (outs) tma_prefetch_desc(tm_out);
             // chunk n's k (q) boxes into K (Q) ring slot n % 3
             auto load_k = [&](int n) {
                 if (!bounds_ok(n >= 0 && n < nchunks, status)) return;
@@ -1023,8 +1033,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             named_sync(kBarOut2, 160);  // the tile is written
             if (sw == 3 && lane == 0) {
                 if (bounds_ok(m >= 0 && m < nchunks, status)) {
-                    tma_store_4d(&tm_o, sm + L::OST, 0, h, t0 + m * 64, b);
-                    tma_store_4d(&tm_o, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
+                    tma_store_4d(tm_out, sm + L::OST, 0, h, t0 + m * 64, b);
+                    tma_store_4d(tm_out, sm + L::OST + 8192, 64, h, t0 + m * 64, b);
                 }
                 bulk_commit_group();
             }
@@ -1762,19 +1772,45 @@ bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int Ts, int H
 namespace {
 
 // Start states of the later segments: S_1 = E (end of segment 0) and
-// S_{p+1} = S_p M_p + H_p, in float32.  Rows of the state are independent, so
-// a CTA owns 16 rows of one sequence: thread (i, j) = (tid / 16, tid % 16)
-// holds row i, columns j, j + 16, ...
+// S_{p+1} = S_p M_p + H_p, in float32 (with ST: one step more, the end
+// state).  Rows of the state are independent, so a CTA owns 16 rows of one
+// sequence: thread (i, j) = (tid / 16, tid % 16) holds row i, columns j,
+// j + 16, ...  Each step's M_p is staged in shared memory by coalesced
+// 16-byte loads (the next step's while this one computes) before the
+// 16 x K x K product reads it.
 template <int K>
-__global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH, int nseg) {
+struct CombineLayout {
+    static constexpr size_t SROW = 0;                            // [16][K + 4] float
+    static constexpr size_t MS = 16 * (K + 4) * 4;               // two [K][K] float buffers
+    static constexpr size_t SMEM = MS + 2 * (size_t)K * K * 4;
+};
+template <int K>
+__global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH, int nseg,
+                                                              float *ST) {
+    using L = CombineLayout<K>;
     constexpr int V = 128;
     constexpr int NJ = K / 16;
-    __shared__ float srow[16][K + 4];
+    extern __shared__ __align__(16) uint8_t smem_cb[];
+    float(*srow)[K + 4] = reinterpret_cast<float(*)[K + 4]>(smem_cb + L::SROW);
+    float *ms = reinterpret_cast<float *>(smem_cb + L::MS);
     const size_t VK = (size_t)V * K;
     const size_t seq = blockIdx.x;
     const int r0 = blockIdx.y * 16;
-    const int i = threadIdx.x >> 4, jl = threadIdx.x & 15;
+    const int tid = threadIdx.x;
+    const int i = tid >> 4, jl = tid & 15;
     auto slot = [&](int kind, int p) { return ws + ((kind * (size_t)BH + seq) * nseg + p) * VK; };
+    // M_p into buffer p % 2: K * K / 4 pieces of 16 bytes, cp.async (L2 only)
+    auto stage = [&](int p) {
+        const float *M = slot(1, p);
+        float *dst = ms + (size_t)(p & 1) * K * K;
+        for (int e = tid; e < K * K / 4; e += 256)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 4 * e)),
+                         "l"(M + 4 * e)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    const int last = ST != nullptr ? nseg : nseg - 1;  // steps p = 1 .. last - 1
+    if (1 < last) stage(1);
     const size_t rowoff = (size_t)(r0 + i) * K + jl;
     float sv[NJ];
     const float *E = slot(0, 0);
@@ -1784,24 +1820,177 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
         float *Sp = slot(2, p);
 #pragma unroll
         for (int q = 0; q < NJ; ++q) Sp[rowoff + 16 * q] = sv[q];
-        if (p == nseg - 1) break;
-        __syncthreads();  // every read of the previous rows done
+        if (p >= last) break;
+        __syncthreads();  // every read of the previous rows and of buffer (p + 1) % 2 done
 #pragma unroll
         for (int q = 0; q < NJ; ++q) srow[i][jl + 16 * q] = sv[q];
-        __syncthreads();
-        const float *M = slot(1, p);
+        if (p + 1 < last) {
+            stage(p + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();  // M_p and the rows in place
+        const float *Ms = ms + (size_t)(p & 1) * K * K;
         const float *Hp = slot(0, p);
         float acc[NJ];
 #pragma unroll
         for (int q = 0; q < NJ; ++q) acc[q] = Hp[rowoff + 16 * q];
+#pragma unroll 4
         for (int m = 0; m < K; ++m) {
             const float x = srow[i][m];
 #pragma unroll
-            for (int q = 0; q < NJ; ++q) acc[q] = fmaf(x, M[(size_t)m * K + jl + 16 * q], acc[q]);
+            for (int q = 0; q < NJ; ++q) acc[q] = fmaf(x, Ms[(size_t)m * K + jl + 16 * q], acc[q]);
         }
 #pragma unroll
         for (int q = 0; q < NJ; ++q) sv[q] = acc[q];
     }
+    if (ST != nullptr) {
+#pragma unroll
+        for (int q = 0; q < NJ; ++q) ST[seq * VK + rowoff + 16 * q] = sv[q];
+    }
+}
+
+// The outputs of segments p >= 1 from their start states (kFirstX):
+// o_t <- o0_t + S_p x_t, for the tokens of segment p, with o0 (bf16, written
+// by the zero-start run) in o and x (bf16, the first K of 128 channels,
+// written by the identity-start run) in X.  S_p enters the products as bf16,
+// as the state does in the state pass's own output products.  One CTA per
+// (sequence, segment, split) walks 64-token tiles: S_p stays in shared
+// memory, x tiles feed warp-level MMAs (m16n8k16, fp32 accumulation), each
+// result is added to o0 in a shared-memory tile that is then written back
+// in whole 16-byte pieces of o's rows.  The next tile's x and this tile's o0
+// load (cp.async) while the products run; two CTAs share an SM.
+constexpr int kCorrThreads = 256;
+template <int K>
+struct CorrLayout {
+    static constexpr int LDB = K + 8;                        // bf16 row stride of S, x tiles
+    static constexpr int LDO = 128 + 8;                      // bf16 row stride of the o tile
+    static constexpr size_t SB = 0;                          // S_p [128][LDB]
+    static constexpr size_t XT = SB + 128 * LDB * 2;         // two x tiles [64][LDB]
+    static constexpr size_t OT = XT + 2 * 64 * LDB * 2;      // o0 -> o tile [64][LDO]
+    static constexpr size_t SMEM = OT + 64 * LDO * 2;
+};
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+template <int K>
+__global__ void __launch_bounds__(kCorrThreads, 2)
+    segment_correct_kernel(const float *__restrict__ ws, const __nv_bfloat16 *__restrict__ X,
+                           __nv_bfloat16 *o, int T, int Ts, int H, int BH, int nseg, int seg_len,
+                           int *status) {
+    using L = CorrLayout<K>;
+    constexpr int V = 128;
+    extern __shared__ __align__(16) uint8_t smem_c[];
+    __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(smem_c + L::SB);
+    __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(smem_c + L::OT);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long seq = blockIdx.x;
+    const int p = (int)blockIdx.y + 1;
+    if (!bounds_ok(seq < BH && p < nseg && T <= Ts, status)) return;
+    const int b = (int)(seq / H), h = (int)(seq % H);
+    const size_t VK = (size_t)V * K;
+    const int tb0 = p * seg_len, tb1 = min(T, tb0 + seg_len);
+    const int ntile = (tb1 - tb0 + 63) / 64;
+    // x buffer of the CTA's it-th tile
+    auto xtile = [&](int it) {
+        return reinterpret_cast<__nv_bfloat16 *>(smem_c + L::XT) + (it & 1) * 64 * L::LDB;
+    };
+    // x rows of a tile (zeros past the segment's end) into buffer it % 2
+    auto load_x = [&](int tile, int it) {
+        const int t0 = tb0 + 64 * tile, nt = min(64, tb1 - t0);
+        __nv_bfloat16 *xt = xtile(it);
+        for (int e = tid; e < 64 * (K / 8); e += kCorrThreads) {
+            const int r = e / (K / 8), c8 = e % (K / 8);
+            const int rr = r < nt ? r : 0;
+            cp_async16(xt + r * L::LDB + 8 * c8,
+                       X + (((size_t)b * T + t0 + rr) * H + h) * V + 8 * c8, r < nt);
+        }
+        cp_async_commit();
+    };
+    auto load_o = [&](int tile) {
+        const int t0 = tb0 + 64 * tile, nt = min(64, tb1 - t0);
+        for (int e = tid; e < 64 * (V / 8); e += kCorrThreads) {
+            const int r = e / (V / 8), c8 = e % (V / 8);
+            const int rr = r < nt ? r : 0;
+            cp_async16(ot + r * L::LDO + 8 * c8,
+                       o + (((size_t)b * Ts + t0 + rr) * H + h) * V + 8 * c8, r < nt);
+        }
+        cp_async_commit();
+    };
+    const int tile0 = (int)blockIdx.z;
+    if (tile0 < ntile) load_x(tile0, 0);
+    const float *Sp = ws + ((2 * (size_t)BH + seq) * nseg + p) * VK;  // slot S of (seq, p)
+    for (int e = tid; e < V * K / 4; e += kCorrThreads) {
+        const float4 f = reinterpret_cast<const float4 *>(Sp)[e];
+        const int r = (4 * e) / K, c = (4 * e) % K;
+        uint2 w;
+        w.x = pack_bf16(f.x, f.y);
+        w.y = pack_bf16(f.z, f.w);
+        *reinterpret_cast<uint2 *>(sb + r * L::LDB + c) = w;
+    }
+    const int mb = warp & 3, nh = warp >> 2;  // tokens 16 mb.., values 64 nh..
+    const int g = lane >> 2, t4 = lane & 3;
+    for (int tile = tile0, it = 0; tile < ntile; tile += (int)gridDim.z, ++it) {
+        const int t0 = tb0 + 64 * tile, nt = min(64, tb1 - t0);
+        // the previous tile's write-back is done with ot (and its x buffer)
+        __syncthreads();
+        load_o(tile);
+        const bool more = tile + (int)gridDim.z < ntile;
+        if (more) load_x(tile + (int)gridDim.z, it + 1);
+        // this tile's x: every group but the newest one or two
+        if (more) cp_async_wait<2>(); else cp_async_wait<1>();
+        __syncthreads();
+        const __nv_bfloat16 *xt = xtile(it);
+        float d[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < K / 16; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, smem_u32(xt + (16 * mb + (lane & 7) + 8 * ((lane >> 3) & 1)) * L::LDB +
+                                16 * ks + 8 * (lane >> 4)));
+#pragma unroll
+            for (int jp = 0; jp < 4; ++jp) {  // n-tiles 2 jp, 2 jp + 1
+                const int mi = lane >> 3;
+                const int row = 64 * nh + 8 * (2 * jp + (mi >> 1)) + (lane & 7);
+                uint32_t bb[4];
+                ldsm_x4(bb, smem_u32(sb + row * L::LDB + 16 * ks + 8 * (mi & 1)));
+                mma_16816(d[2 * jp], a, bb[0], bb[1]);
+                mma_16816(d[2 * jp + 1], a, bb[2], bb[3]);
+            }
+        }
+        // this tile's o0 (the next tile's x may still be in flight)
+        if (more) cp_async_wait<1>(); else cp_async_wait<0>();
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int col = 64 * nh + 8 * j + 2 * t4;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                uint32_t *pr = reinterpret_cast<uint32_t *>(ot + (16 * mb + g + 8 * hr) * L::LDO + col);
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pr));
+                *pr = pack_bf16(f.x + d[j][2 * hr], f.y + d[j][2 * hr + 1]);
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < 64 * (V / 8); e += kCorrThreads) {
+            const int r = e / (V / 8), c8 = e % (V / 8);
+            if (r < nt)
+                reinterpret_cast<uint4 *>(o + (((size_t)b * Ts + t0 + r) * H + h) * V)[c8] =
+                    *reinterpret_cast<const uint4 *>(ot + r * L::LDO + 8 * c8);
+        }
+    }
+    cp_async_wait<0>();
 }
 
 template <int K, bool GATHER = false>
@@ -1833,12 +2022,16 @@ cudaError_t launch_prep(const CUtensorMap &mq, const CUtensorMap &mk, const floa
 
 // Whole-sequence launch, or the segment-parallel sequence (first pass,
 // combine, second pass) of the one-pass kernel (prep == nullptr) or of the
-// state-side kernel of the two-pass form.
+// state-side kernel of the two-pass form.  The two-pass form with an X
+// buffer (xbuf, tensor map mx) replaces the second pass: the first pass
+// writes every segment's o0 and X, the combine the end state, and
+// segment_correct_kernel adds S_p x_t; without outputs it needs neither.
 template <int K>
 cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                    const CUtensorMap &mo, const float *alpha, const float *beta, const float *S0,
                    void *o, float *ST, long long BH, int T, int Ts, int H, const SegShape &sh,
-                   float *ws, const uint8_t *prep, cudaStream_t stream) {
+                   float *ws, const uint8_t *prep, cudaStream_t stream,
+                   const CUtensorMap *mx = nullptr, const __nv_bfloat16 *xbuf = nullptr) {
     static uintptr_t attr_set[2][64] = {};  // context the attributes were set in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -1854,6 +2047,7 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
         attr_set[two][dev] = context_key();
     }
     int *status = device_status_ptr();
+    const CUtensorMap &mxo = mx ? *mx : mo;  // the X map (unused unless kFirstX)
     auto launch = [&](long long grid, SegPlan plan) {
         if (two && plan.mode != kSecond && K == 64)
             // right after the key-side pass: its tail overlaps this grid's
@@ -1863,12 +2057,12 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
             // whichever SMs the key-side pass frees first, ran 10 us slower,
             // so that width keeps the plain launch
             return launch_pdl(prefill_state_kernel<K>, (unsigned)grid, kTcThreads, smem, stream,
-                              mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H,
+                              mq, mk, mv, mo, mxo, alpha, beta, S0, o != nullptr, ST, T, Ts, H,
                               (int)BH, plan, prep, status);
         if (two)
             prefill_state_kernel<K><<<(unsigned)grid, kTcThreads, smem, stream>>>(
-                mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan, prep,
-                status);
+                mq, mk, mv, mo, mxo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan,
+                prep, status);
         else
             prefill_fused_kernel<K><<<(unsigned)grid, kFuThreads, smem, stream>>>(
                 mq, mk, mv, mo, alpha, beta, S0, o != nullptr, ST, T, Ts, H, (int)BH, plan,
@@ -1876,13 +2070,43 @@ cudaError_t run_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
         return cudaGetLastError();
     };
     if (sh.nseg == 1) return launch(BH, SegPlan{kWhole, 1, T, nullptr});
-    cudaError_t e = launch(BH * (2 * sh.nseg - 1), SegPlan{kFirst, sh.nseg, sh.seg_len, ws});
+    // no second pass: the two-pass form when it has the X buffer or no outputs
+    const bool corr = two && (o == nullptr || (mx != nullptr && xbuf != nullptr));
+    cudaError_t e = launch(BH * (2 * sh.nseg - 1),
+                           SegPlan{corr && o ? kFirstX : kFirst, sh.nseg, sh.seg_len, ws});
     if (e != cudaSuccess) return e;
-    segment_combine_kernel<K><<<dim3((unsigned)BH, 128 / 16), 256, 0, stream>>>(ws, (int)BH,
-                                                                                sh.nseg);
+    static uintptr_t comb_set[64] = {};
+    if (comb_set[dev] != context_key()) {
+        e = cudaFuncSetAttribute(segment_combine_kernel<K>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)CombineLayout<K>::SMEM);
+        if (e != cudaSuccess) return e;
+        comb_set[dev] = context_key();
+    }
+    segment_combine_kernel<K><<<dim3((unsigned)BH, 128 / 16), 256, CombineLayout<K>::SMEM,
+                                stream>>>(ws, (int)BH, sh.nseg, corr ? ST : nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch(BH * (sh.nseg - 1), SegPlan{kSecond, sh.nseg, sh.seg_len, ws});
+    if (!corr) return launch(BH * (sh.nseg - 1), SegPlan{kSecond, sh.nseg, sh.seg_len, ws});
+    if (o == nullptr) return cudaSuccess;
+    using CL = CorrLayout<K>;
+    static uintptr_t corr_set[64] = {};
+    if (corr_set[dev] != context_key()) {
+        e = cudaFuncSetAttribute(segment_correct_kernel<K>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CL::SMEM);
+        if (e != cudaSuccess) return e;
+        corr_set[dev] = context_key();
+    }
+    // splits of each segment's tiles: the grid within one wave of two CTAs per SM
+    const long long cells = BH * (sh.nseg - 1);
+    const int tiles = (sh.seg_len + 63) / 64;
+    const int split = (int)std::max<long long>(
+        1, std::min<long long>(tiles, 2LL * sm_count() / cells));
+    if (BH > 0x7fffffffLL || sh.nseg - 1 > 65535) return cudaErrorInvalidConfiguration;
+    segment_correct_kernel<K><<<dim3((unsigned)BH, (unsigned)(sh.nseg - 1), (unsigned)split),
+                                kCorrThreads, CL::SMEM, stream>>>(
+        ws, xbuf, static_cast<__nv_bfloat16 *>(o), T, Ts, H, (int)BH, sh.nseg, sh.seg_len, status);
+    return cudaGetLastError();
 }
 
 template <int K>
@@ -1914,10 +2138,18 @@ cudaError_t launch_tc_t(const void *q, const void *k, const void *v, const float
     const size_t need = prep_off + prefill_prep_bytes(BH, T);
     if (workspace && workspace_bytes >= need) {
         uint8_t *prep = static_cast<uint8_t *>(workspace) + prep_off;
+        // segments' X buffer after the operands, when the workspace holds it
+        const size_t xbytes = prefill_x_bytes(sh, BH, T);
+        CUtensorMap mx;
+        __nv_bfloat16 *xbuf = nullptr;
+        if (xbytes > 0 && workspace_bytes >= need + xbytes) {
+            xbuf = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(workspace) + need);
+            if (!make_token_map(&mx, xbuf, B, T, T, H, 128)) return cudaErrorInvalidValue;
+        }
         const cudaError_t e = launch_prep<K>(mq, mk, alpha, beta, prep, BH, T, Ts, H, stream);
         if (e != cudaSuccess) return e;
         return run_tc<K>(mq, mk, mv, mo, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, prep,
-                         stream);
+                         stream, xbuf ? &mx : nullptr, xbuf);
     }
     return run_tc<K>(mq, mk, mv, mo, alpha, beta, S0, o, ST, BH, T, Ts, H, sh, ws, nullptr,
                      stream);
@@ -1955,6 +2187,10 @@ SegShape segment_shape(int BH, int T, int K, int nsm) {
 size_t prefill_prep_offset(const SegShape &sh) {
     return sh.nseg > 1 ? (sh.workspace_bytes + 255) & ~size_t(255) : 0;
 }
+size_t prefill_x_bytes(const SegShape &sh, long long BH, int T) {
+    return sh.nseg > 1 ? ((size_t)BH * (size_t)T * 128 * sizeof(__nv_bfloat16) + 255) & ~size_t(255)
+                       : 0;
+}
 size_t prefill_prep_bytes(long long BH, int T) {
     return (size_t)BH * (size_t)((T + 63) / 64) * kPrepChunkBytes;
 }
@@ -1968,7 +2204,8 @@ GatheredLayout gathered_layout(int B, int T, int H) {
     const size_t tok = (size_t)B * T * H * 64 * sizeof(__nv_bfloat16);
     g.qg = (g.prep + prefill_prep_bytes((long long)B * H, T) + 255) & ~size_t(255);
     g.kg = (g.qg + tok + 255) & ~size_t(255);
-    g.total = g.kg + tok;
+    g.x = (g.kg + tok + 255) & ~size_t(255);
+    g.total = g.x + prefill_x_bytes(sh, (long long)B * H, T);
     return g;
 }
 
@@ -1996,11 +2233,18 @@ cudaError_t launch_prefill_gathered(const void *q_full, const void *k_full, cons
     if (BH * (2 * sh.nseg - 1) > 0x7fffffffLL || (sh.nseg > 1 && BH > 65535))
         return cudaErrorInvalidConfiguration;
     uint8_t *prep = ws + g.prep;
+    // segments: the X buffer, as in the plain two-pass form
+    CUtensorMap mx;
+    __nv_bfloat16 *xbuf = nullptr;
+    if (g.total > g.x) {
+        xbuf = reinterpret_cast<__nv_bfloat16 *>(ws + g.x);
+        if (!make_token_map(&mx, xbuf, B, T, T, H, 128)) return cudaErrorInvalidValue;
+    }
     cudaError_t e = launch_prep<64, true>(mqf, mkf, alpha, beta, prep, BH, T, T, H, stream,
                                           PrepGather{idx, qg, kg});
     if (e != cudaSuccess) return e;
     return run_tc<64>(mq, mk, mv, mo, alpha, beta, S0, o, ST, BH, T, T, H, sh,
-                      reinterpret_cast<float *>(ws), prep, stream);
+                      reinterpret_cast<float *>(ws), prep, stream, xbuf ? &mx : nullptr, xbuf);
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *alpha,

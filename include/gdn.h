@@ -86,10 +86,16 @@ typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
  * workspace: device scratch of at least gdn_prefill_workspace_size() bytes
  * (may be NULL when that size is 0); 256-byte aligned.  With at least
  * gdn_prefill_two_pass_workspace_size() bytes the bf16 tensor-core path runs
- * in two passes: first the state-independent part of every chunk (A, P, the
+ * in two passes: first the state-independent part of every chunk (A, the
  * triangular inverse) for all chunks of all sequences at once, then the
- * state recurrence, which only loads those operands.  The results are
- * bit-identical to the one-pass form; only the speed differs.
+ * state recurrence, which only loads those operands.  For whole sequences
+ * the results are bit-identical to the one-pass form; only the speed
+ * differs.  Segment-parallel problems (few, long sequences) take another
+ * route there: every segment's outputs from a zero start and the map x of
+ * its start state, then o += S_start x and the end state from the chain of
+ * segment maps, instead of a second pass over the segments; those results
+ * agree with the one-pass form to rounding (a bf16 step of o, the float32
+ * chain of S_T).
  */
 GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const float *alpha,
                 const float *beta, const float *S0, void *o, float *S_T, int B, int T, int H,
@@ -101,7 +107,11 @@ GDN_API size_t gdn_prefill_workspace_size(int B, int T, int H, int K, int V, gdn
 
 /* Bytes of device workspace with which gdn_prefill takes the two-pass form:
  * the segment scratch of gdn_prefill_workspace_size (rounded up to 256 bytes)
- * plus 16 KiB per 64-token chunk per (b, h) for the key-side operands.
+ * plus 16 KiB per 64-token chunk per (b, h) for the key-side operands, plus,
+ * for segment-parallel problems, B*T*H*128 bf16 (rounded up to 256 bytes)
+ * for the segments' maps x.  With the operands only (no x buffer) a
+ * segment-parallel call that wants o runs the second pass like the one-pass
+ * form.
  * 0 when the problem has no two-pass form (float32, or V != 128, or
  * K not in {64, 128}). */
 GDN_API size_t gdn_prefill_two_pass_workspace_size(int B, int T, int H, int K, int V,
