@@ -381,10 +381,20 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
     float *gam = G2 + 64;
     float *bet = G2 + 128;
 
+    // item j of the persistent loop: chunk n of sequence seq, taken in
+    // reverse chunk-major order (chunk nch - 1 of every sequence first), so
+    // that the operands the state pass reads first are the ones written last,
+    // still in L2 when it starts
+    const long long BHs = nchunk_all / nch;
+    auto item = [&](long long j, long long &seq, int &n) {
+        seq = j % BHs;
+        n = nch - 1 - (int)(j / BHs);
+    };
     auto load_kq = [&](long long j) {
         if (!bounds_ok(j >= 0 && j < nchunk_all, status)) return;
-        const long long seq = j / nch;
-        const int n = (int)(j - seq * nch);
+        long long seq;
+        int n;
+        item(j, seq, n);
         const int b = (int)(seq / H), h = (int)(seq % H);
         // the gathering form loads q and k, both with all 128 channels
         mbar_arrive_expect_tx(&kq_full, GATHER ? L::KQ_BYTES : L::K_BYTES);
@@ -400,8 +410,9 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
     float pa0 = 1.f, pa1 = 1.f, pb0 = 0.f, pb1 = 0.f;  // prefetched gate inputs (warp 1)
     auto prefetch_gates = [&](long long j) {
         if (warp == 1 && j < nchunk_all && bounds_ok(T <= Ts, status)) {
-            const long long seq = j / nch;
-            const int n = (int)(j - seq * nch);
+            long long seq;
+            int n;
+            item(j, seq, n);
             const int b = (int)(seq / H), h = (int)(seq % H);
             const int nv = min(64, T - n * 64);
             const size_t i0 = ((size_t)b * Ts + n * 64 + lane) * H + h;
@@ -433,7 +444,9 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
     prefetch_gates(j);
     bool failed = false;
     for (int it = 0; j < nchunk_all; j += G, ++it) {
-        const int n = (int)(j % nch);
+        long long seq;
+        int n;
+        item(j, seq, n);
         const int nvalid = min(64, T - n * 64);
         bool ok = true;
         if constexpr (GATHER) {
@@ -445,7 +458,6 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
             // sum of squares runs in the standalone prologue's order (eight
             // channels per lane, then the lanes 4, 2, 1 apart), so the rows are
             // bit-identical to gdn_gather_normalize
-            const long long seq = j / nch;
             const int h = (int)(seq % H), b = (int)(seq / H);
             const int sub = lane >> 3, cl = lane & 7;
             const int4 *ip = reinterpret_cast<const int4 *>(gth.idx + (size_t)h * 64) + 2 * cl;
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(kPrepThreads, prep_ctas_per_sm(GATHER))
             prefetch_gates(j + G);
         }
         if (named_sync_or(kBarKey, kPrepThreads, !ok)) { failed = true; break; }
-        uint8_t *out = prep + (size_t)j * kPrepChunkBytes;  // [T'^T | T''^T]
+        uint8_t *out = prep + ((size_t)seq * nch + n) * kPrepChunkBytes;  // [T'^T | T''^T]
         tc_fence_after();
         {   // lanes 64..127 repeat K K^T: warps 0-1 form columns 0..31 of A's
             // rows, warps 2-3 columns 32..63
