@@ -151,3 +151,26 @@ def test_gdn2_chunk_form_equals_gated_oracle(T):
     oc, STc = gdn2_chunk_recurrence(q, k, v, alpha, bg, wg, S0=S0)
     np.testing.assert_allclose(oc, o, atol=1e-10, rtol=0)
     np.testing.assert_allclose(STc, ST, atol=1e-10, rtol=0)
+
+
+@pytest.mark.parametrize("K,V,T", [(4, 6, 37), (8, 8, 100), (8, 12, 1)])
+def test_segment_outputs_and_end_state_affine_in_start_state(K, V, T):
+    """The segment-parallel prefill's two routes rest on this: a segment's
+    end state is S_end = S_start M + H and each output is o_t = o0_t +
+    S_start x_t, where (o0, H) come from a zero start and (x, M) are the
+    first K rows of the output and end state of the run from the rows of the
+    identity with v = 0 (the update S -> alpha S (I - beta k k^T) + beta v
+    k^T and the read-out o = S q are affine in S)."""
+    rng = np.random.default_rng(K * 100 + V + T)
+    B, H = 2, 3
+    q, k, v, alpha, beta, S = _gdn_problem(rng, B, T, H, K, V)
+    o, ST = oracle.recurrence(q, k, v, alpha, beta, S0=S)
+    o0, Hs = oracle.recurrence(q, k, v, alpha, beta)
+    ident = np.zeros((B, H, V, K))
+    ident[:, :, np.arange(K), np.arange(K)] = 1.0
+    oM, SM = oracle.recurrence(q, k, np.zeros_like(v), alpha, beta, S0=ident)
+    x, M = oM[..., :K], SM[:, :, :K, :]
+    if V > K:  # the rows past the identity stay zero
+        assert np.abs(oM[..., K:]).max() == 0.0 and np.abs(SM[:, :, K:, :]).max() == 0.0
+    np.testing.assert_allclose(ST, np.einsum("bhvk,bhkj->bhvj", S, M) + Hs, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(o, o0 + np.einsum("bhvk,bthk->bthv", S, x), atol=1e-12, rtol=0)
