@@ -1871,8 +1871,8 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
 // (sequence, segment, split) walks 64-token tiles: S_p stays in shared
 // memory, x tiles feed warp-level MMAs (m16n8k16, fp32 accumulation), each
 // result is added to o0 in a shared-memory tile that is then written back
-// in whole 16-byte pieces of o's rows.  The next tile's x and this tile's o0
-// load (cp.async) while the products run; two CTAs share an SM.
+// in whole 16-byte pieces of o's rows.  The next tile's x and o0 load
+// (cp.async) while this tile's products run; two CTAs share an SM.
 constexpr int kCorrThreads = 256;
 template <int K>
 struct CorrLayout {
@@ -1880,8 +1880,8 @@ struct CorrLayout {
     static constexpr int LDO = 128 + 8;                      // bf16 row stride of the o tile
     static constexpr size_t SB = 0;                          // S_p [128][LDB]
     static constexpr size_t XT = SB + 128 * LDB * 2;         // two x tiles [64][LDB]
-    static constexpr size_t OT = XT + 2 * 64 * LDB * 2;      // o0 -> o tile [64][LDO]
-    static constexpr size_t SMEM = OT + 64 * LDO * 2;
+    static constexpr size_t OT = XT + 2 * 64 * LDB * 2;      // two o0 -> o tiles [64][LDO]
+    static constexpr size_t SMEM = OT + 2 * 64 * LDO * 2;
 };
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
@@ -1904,7 +1904,6 @@ __global__ void __launch_bounds__(kCorrThreads, 2)
     constexpr int V = 128;
     extern __shared__ __align__(16) uint8_t smem_c[];
     __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(smem_c + L::SB);
-    __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(smem_c + L::OT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long seq = blockIdx.x;
     const int p = (int)blockIdx.y + 1;
@@ -1929,8 +1928,13 @@ __global__ void __launch_bounds__(kCorrThreads, 2)
         }
         cp_async_commit();
     };
-    auto load_o = [&](int tile) {
+    // o buffer of the CTA's it-th tile
+    auto otile = [&](int it) {
+        return reinterpret_cast<__nv_bfloat16 *>(smem_c + L::OT) + (it & 1) * 64 * L::LDO;
+    };
+    auto load_o = [&](int tile, int it) {
         const int t0 = tb0 + 64 * tile, nt = min(64, tb1 - t0);
+        __nv_bfloat16 *ot = otile(it);
         for (int e = tid; e < 64 * (V / 8); e += kCorrThreads) {
             const int r = e / (V / 8), c8 = e % (V / 8);
             const int rr = r < nt ? r : 0;
@@ -1940,7 +1944,10 @@ __global__ void __launch_bounds__(kCorrThreads, 2)
         cp_async_commit();
     };
     const int tile0 = (int)blockIdx.z;
-    if (tile0 < ntile) load_x(tile0, 0);
+    if (tile0 < ntile) {
+        load_x(tile0, 0);
+        load_o(tile0, 0);
+    }
     const float *Sp = ws + ((2 * (size_t)BH + seq) * nseg + p) * VK;  // slot S of (seq, p)
     for (int e = tid; e < V * K / 4; e += kCorrThreads) {
         const float4 f = reinterpret_cast<const float4 *>(Sp)[e];
@@ -1954,15 +1961,19 @@ __global__ void __launch_bounds__(kCorrThreads, 2)
     const int g = lane >> 2, t4 = lane & 3;
     for (int tile = tile0, it = 0; tile < ntile; tile += (int)gridDim.z, ++it) {
         const int t0 = tb0 + 64 * tile, nt = min(64, tb1 - t0);
-        // the previous tile's write-back is done with ot (and its x buffer)
+        // the previous tile's products and write-back are done with buffers
+        // (it + 1) % 2
         __syncthreads();
-        load_o(tile);
         const bool more = tile + (int)gridDim.z < ntile;
-        if (more) load_x(tile + (int)gridDim.z, it + 1);
-        // this tile's x: every group but the newest one or two
-        if (more) cp_async_wait<2>(); else cp_async_wait<1>();
+        if (more) {
+            load_x(tile + (int)gridDim.z, it + 1);
+            load_o(tile + (int)gridDim.z, it + 1);
+        }
+        // this tile's x and o0: every group but the next tile's two
+        if (more) cp_async_wait<2>(); else cp_async_wait<0>();
         __syncthreads();
         const __nv_bfloat16 *xt = xtile(it);
+        __nv_bfloat16 *ot = otile(it);
         float d[8][4];
 #pragma unroll
         for (int j = 0; j < 8; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
@@ -1981,9 +1992,6 @@ __global__ void __launch_bounds__(kCorrThreads, 2)
                 mma_16816(d[2 * jp + 1], a, bb[2], bb[3]);
             }
         }
-        // this tile's o0 (the next tile's x may still be in flight)
-        if (more) cp_async_wait<1>(); else cp_async_wait<0>();
-        __syncthreads();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int col = 64 * nh + 8 * j + 2 * t4;
