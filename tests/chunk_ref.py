@@ -63,6 +63,35 @@ def bf16_round(x):
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def f32_round(x):
+    """Round float64 values to float32 (returned as float64)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def bf16_split(x, parts):
+    """x as the sum of `parts` bfloat16 numbers: hi = bf16(x), then each
+    next part the bf16 of what the float32 value still lacks."""
+    out, rest = [], f32_round(x)
+    for _ in range(parts):
+        p = bf16_round(rest)
+        out.append(p)
+        rest = f32_round(rest - p)
+    return out
+
+
+def mm_bf16_split(a, b, parts):
+    """a @ b on bf16 tensor cores with float32 operands split into `parts`
+    bf16 parts: the products of part i of a and part j of b with i + j <
+    parts (2 parts: hi hi + hi lo + lo hi), accumulated in float32."""
+    A, Bp = bf16_split(a, parts), bf16_split(b, parts)
+    acc = np.zeros((np.shape(a)[0], np.shape(b)[1]), np.float32)
+    for i, ai in enumerate(A):
+        for j, bj in enumerate(Bp):
+            if i + j < parts:
+                acc += ai.astype(np.float32) @ bj.astype(np.float32)
+    return acc.astype(np.float64)
+
+
 def _chunk_operands(k, q, v, alpha, beta, b, h, c0, C):
     """Zero-padded chunk tiles and its scalar-gate quantities."""
     T = k.shape[1]
@@ -82,7 +111,8 @@ def _chunk_operands(k, q, v, alpha, beta, b, h, c0, C):
                 Tp=Tm * (be * gam)[None, :], Tpp=Tm * be[None, :])
 
 
-def chunk_state_chain(q, k, v, alpha, beta, S0=None, C=64, lookahead=False, rnd=None):
+def chunk_state_chain(q, k, v, alpha, beta, S0=None, C=64, lookahead=False, rnd=None,
+                      prod=None):
     """The state pass of the two-pass prefill, one sequence per (b, h), on the
     key-side operands T' = T diag(beta gamma), T'' = T diag(beta) and P.
 
@@ -103,7 +133,9 @@ def chunk_state_chain(q, k, v, alpha, beta, S0=None, C=64, lookahead=False, rnd=
     rnd (e.g. bf16_round) is applied where the kernel rounds an MMA operand:
     T', T'', P, NW (and gamma_n NW, M), the state copy, U^T, U^T diag(dec)
     and gamma Q; products then accumulate in float32 and the state stays
-    float32, as on the GPU.  Returns (o, S_T) like chunk_recurrence.
+    float32, as on the GPU.  prod, if given, forms every product instead
+    (e.g. mm_bf16_split with rnd=f32_round: float32 operands on bf16 tensor
+    cores).  Returns (o, S_T) like chunk_recurrence.
     """
     r = rnd if rnd is not None else (lambda x: x)
     acc = np.float32 if rnd is not None else np.float64
@@ -111,7 +143,8 @@ def chunk_state_chain(q, k, v, alpha, beta, S0=None, C=64, lookahead=False, rnd=
     V = v.shape[-1]
     o = np.zeros((B, T, H, V))
     ST = np.zeros((B, H, V, K))
-    mm = lambda a, b_: (np.asarray(a, acc) @ np.asarray(b_, acc)).astype(np.float64)
+    mm = prod if prod is not None else (
+        lambda a, b_: (np.asarray(a, acc) @ np.asarray(b_, acc)).astype(np.float64))
     for b in range(B):
         for h in range(H):
             S = np.zeros((V, K)) if S0 is None else np.array(S0[b, h], dtype=np.float64)

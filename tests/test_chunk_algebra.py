@@ -174,3 +174,35 @@ def test_segment_outputs_and_end_state_affine_in_start_state(K, V, T):
         assert np.abs(oM[..., K:]).max() == 0.0 and np.abs(SM[:, :, K:, :]).max() == 0.0
     np.testing.assert_allclose(ST, np.einsum("bhvk,bhkj->bhvj", S, M) + Hs, atol=1e-12, rtol=0)
     np.testing.assert_allclose(o, o0 + np.einsum("bhvk,bthk->bthv", S, x), atol=1e-12, rtol=0)
+
+
+def test_split_bf16_products_meet_the_fp32_bound():
+    """A float32 mode on the bf16 tensor cores: with every operand of the
+    state chain split into hi + lo bf16 parts (three products per product:
+    hi hi, hi lo, lo hi; float32 accumulation and state), the chain stays
+    inside the all-float32 bound of 1e-4 on long-horizon gates and keys in a
+    narrow cone (the case with the thinnest margin): ~1.5e-5 of o and
+    ~2e-5 of S_T, where one bf16 part gives ~6e-3 / ~9e-3."""
+    from chunk_ref import chunk_state_chain, f32_round, mm_bf16_split
+    rng = np.random.default_rng(3)
+    B, T, H, K, V = 1, 1024, 2, 128, 128
+    mu = rng.standard_normal((H, K))
+    mu *= 8.18 / np.linalg.norm(mu, axis=-1, keepdims=True)
+    k = mu[None, None] + 0.35 * rng.standard_normal((B, T, H, K))
+    k = f32_round(k / np.linalg.norm(k, axis=-1, keepdims=True))
+    q = rng.standard_normal((B, T, H, K))
+    q = f32_round(q / np.linalg.norm(q, axis=-1, keepdims=True))
+    v = f32_round(rng.standard_normal((B, T, H, V)))
+    alpha = f32_round(rng.uniform(0.9995, 0.9999, size=(B, T, H)))
+    beta = f32_round(1 / (1 + np.exp(-rng.standard_normal((B, T, H)))))
+    o_ref, S_ref = oracle.recurrence(q, k, v, alpha, beta)
+
+    def err(parts):
+        o, S = chunk_state_chain(q, k, v, alpha, beta, rnd=f32_round,
+                                 prod=lambda a, b: mm_bf16_split(a, b, parts))
+        return (np.abs(o - o_ref).max() / np.abs(o_ref).max(),
+                np.abs(S - S_ref).max() / np.abs(S_ref).max())
+
+    one, two = err(1), err(2)
+    assert max(two) <= 3e-5, two      # 1e-4 with a margin of 3
+    assert min(one) >= 1e-3, one      # one bf16 part is not enough for float32
