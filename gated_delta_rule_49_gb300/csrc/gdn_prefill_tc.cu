@@ -1786,14 +1786,15 @@ namespace {
 // Start states of the later segments: S_1 = E (end of segment 0) and
 // S_{p+1} = S_p M_p + H_p, in float32 (with ST: one step more, the end
 // state).  Rows of the state are independent, so a CTA owns 16 rows of one
-// sequence: thread (i, j) = (tid / 16, tid % 16) holds row i, columns j,
-// j + 16, ...  Each step's M_p is staged in shared memory by coalesced
-// 16-byte loads (the next step's while this one computes) before the
-// 16 x K x K product reads it.
+// sequence; thread (j, g) = (tid % K, tid / K) holds column j of rows
+// g RP .. g RP + RP - 1 (RP = K / 16).  Each step's M_p is staged in shared
+// memory by coalesced 16-byte copies (the next step's while this one
+// computes); the product reads one M element per row group and the 16 rows'
+// entries of column m as broadcast float4 reads of a transposed copy.
 template <int K>
 struct CombineLayout {
-    static constexpr size_t SROW = 0;                            // [16][K + 4] float
-    static constexpr size_t MS = 16 * (K + 4) * 4;               // two [K][K] float buffers
+    static constexpr size_t ST = 0;                              // rows^T [K][16] float
+    static constexpr size_t MS = (size_t)K * 16 * 4;             // two [K][K] float buffers
     static constexpr size_t SMEM = MS + 2 * (size_t)K * K * 4;
 };
 template <int K>
@@ -1801,15 +1802,16 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
                                                               float *ST) {
     using L = CombineLayout<K>;
     constexpr int V = 128;
-    constexpr int NJ = K / 16;
+    constexpr int RP = K / 16;  // rows per thread
+    static_assert(256 / K * RP == 16 && RP % 4 == 0, "combine thread mapping");
     extern __shared__ __align__(16) uint8_t smem_cb[];
-    float(*srow)[K + 4] = reinterpret_cast<float(*)[K + 4]>(smem_cb + L::SROW);
+    float *rowt = reinterpret_cast<float *>(smem_cb + L::ST);  // [m][row of the CTA]
     float *ms = reinterpret_cast<float *>(smem_cb + L::MS);
     const size_t VK = (size_t)V * K;
     const size_t seq = blockIdx.x;
     const int r0 = blockIdx.y * 16;
     const int tid = threadIdx.x;
-    const int i = tid >> 4, jl = tid & 15;
+    const int j = tid % K, g = tid / K;
     auto slot = [&](int kind, int p) { return ws + ((kind * (size_t)BH + seq) * nseg + p) * VK; };
     // M_p into buffer p % 2: K * K / 4 pieces of 16 bytes, cp.async (L2 only)
     auto stage = [&](int p) {
@@ -1823,19 +1825,22 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
     };
     const int last = ST != nullptr ? nseg : nseg - 1;  // steps p = 1 .. last - 1
     if (1 < last) stage(1);
-    const size_t rowoff = (size_t)(r0 + i) * K + jl;
-    float sv[NJ];
+    // element (row r0 + g RP + i, column j) of a V x K slot
+    auto at = [&](int i) { return (size_t)(r0 + g * RP + i) * K + j; };
+    float sv[RP];
     const float *E = slot(0, 0);
 #pragma unroll
-    for (int q = 0; q < NJ; ++q) sv[q] = E[rowoff + 16 * q];
+    for (int i = 0; i < RP; ++i) sv[i] = E[at(i)];
     for (int p = 1; p < nseg; ++p) {
         float *Sp = slot(2, p);
 #pragma unroll
-        for (int q = 0; q < NJ; ++q) Sp[rowoff + 16 * q] = sv[q];
+        for (int i = 0; i < RP; ++i) Sp[at(i)] = sv[i];
         if (p >= last) break;
         __syncthreads();  // every read of the previous rows and of buffer (p + 1) % 2 done
 #pragma unroll
-        for (int q = 0; q < NJ; ++q) srow[i][jl + 16 * q] = sv[q];
+        for (int i = 0; i < RP; i += 4)
+            *reinterpret_cast<float4 *>(rowt + j * 16 + g * RP + i) =
+                make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
         if (p + 1 < last) {
             stage(p + 1);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -1845,21 +1850,27 @@ __global__ void __launch_bounds__(256) segment_combine_kernel(float *ws, int BH,
         __syncthreads();  // M_p and the rows in place
         const float *Ms = ms + (size_t)(p & 1) * K * K;
         const float *Hp = slot(0, p);
-        float acc[NJ];
+        float acc[RP];
 #pragma unroll
-        for (int q = 0; q < NJ; ++q) acc[q] = Hp[rowoff + 16 * q];
+        for (int i = 0; i < RP; ++i) acc[i] = Hp[at(i)];
 #pragma unroll 4
         for (int m = 0; m < K; ++m) {
-            const float x = srow[i][m];
+            const float mv = Ms[(size_t)m * K + j];
 #pragma unroll
-            for (int q = 0; q < NJ; ++q) acc[q] = fmaf(x, Ms[(size_t)m * K + jl + 16 * q], acc[q]);
+            for (int i = 0; i < RP; i += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(rowt + m * 16 + g * RP + i);
+                acc[i] = fmaf(x.x, mv, acc[i]);
+                acc[i + 1] = fmaf(x.y, mv, acc[i + 1]);
+                acc[i + 2] = fmaf(x.z, mv, acc[i + 2]);
+                acc[i + 3] = fmaf(x.w, mv, acc[i + 3]);
+            }
         }
 #pragma unroll
-        for (int q = 0; q < NJ; ++q) sv[q] = acc[q];
+        for (int i = 0; i < RP; ++i) sv[i] = acc[i];
     }
     if (ST != nullptr) {
 #pragma unroll
-        for (int q = 0; q < NJ; ++q) ST[seq * VK + rowoff + 16 * q] = sv[q];
+        for (int i = 0; i < RP; ++i) ST[seq * VK + at(i)] = sv[i];
     }
 }
 
